@@ -1,0 +1,55 @@
+"""torch.autograd wrappers over the C ABI (the pages' ``diffusion_attn_func``).
+
+``diffusion_attn_func(q, k, v, block_size)`` mirrors the API of "Fast
+Diffusion Attention" (section "Try it"): q, k, v are (batch, 2n, heads,
+headdim) bf16 tensors ordered [noisy | clean]; the forward saves out and the
+log-sum-exp, and the backward recomputes from them (section 4.5 of
+"FlashAttention: Exact Attention Without Materialization").
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import binding
+
+
+class DiffusionAttnFunc(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, block_size):
+        q, k, v = (t.contiguous() for t in (q, k, v))
+        out, lse = binding.dfa_forward(q, k, v, block_size)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.block_size = block_size
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        dq, dk, dv = binding.dfa_backward(q, k, v, out, dout.contiguous(), lse, ctx.block_size)
+        return dq, dk, dv, None
+
+
+class CausalAttnFunc(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v):
+        q, k, v = (t.contiguous() for t in (q, k, v))
+        out, lse = binding.dfa_causal_forward(q, k, v)
+        ctx.save_for_backward(q, k, v, out, lse)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        dq, dk, dv = binding.dfa_causal_backward(q, k, v, out, dout.contiguous(), lse)
+        return dq, dk, dv
+
+
+def diffusion_attn_func(q, k, v, block_size):
+    """Attention under the block-diffusion mask; differentiable."""
+    return DiffusionAttnFunc.apply(q, k, v, block_size)
+
+
+def causal_attn_func(q, k, v):
+    """Causal attention on (Bc, L, H, d), Bc even; the yardstick kernels."""
+    return CausalAttnFunc.apply(q, k, v)

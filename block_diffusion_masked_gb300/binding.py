@@ -1,0 +1,196 @@
+"""ctypes binding of libdfa.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (see
+``include/dfa.h``) and does nothing but check tensor shapes, dtypes and
+devices, allocate outputs with PyTorch, and pass raw pointers, sizes and the
+current CUDA stream to the library.  Every step of the computation runs in
+the library's CUDA kernels; there is no other implementation to fall back to,
+so a missing or unloadable library raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdfa.so")
+
+DFA_OK = 0
+DFA_EINVAL = -1
+DFA_EUNSUPPORTED = -2
+DFA_ECUDA = -3
+DFA_ETIMEOUT = -4
+DFA_EDEVICE = -5
+MODE_DIFFUSION = 0
+MODE_CAUSAL = 1
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGNATURES = {
+    "dfa_version": (_I, []),
+    "dfa_error_string": (ctypes.c_char_p, [_I]),
+    "dfa_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "dfa_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _I, _P]),
+    "dfa_causal_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "dfa_causal_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _P]),
+    "dfa_status": (_I, [_P]),
+    "dfa_fwd_segments": (_I, [_I] * 7 + [ctypes.POINTER(_I)]),
+    "dfa_bwd_segments": (_I, [_I] * 7 + [ctypes.POINTER(_I)]),
+    "dfa_tile_full": (_I, [_I] * 7),
+    "dfa_tile_visits": (ctypes.c_longlong, [_I] * 6),
+    "dfa_tile_shape": (_I, [_I] + [ctypes.POINTER(_I)] * 4),
+}
+
+
+class DfaError(RuntimeError):
+    def __init__(self, fn, code):
+        msg = lib().dfa_error_string(code).decode()
+        super().__init__(f"{fn} failed: {msg} ({code})")
+        self.code = code
+
+
+def lib():
+    """Load libdfa.so (built in-tree by ``build()``) once and return it."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libdfa.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(fn, rc):
+    if rc != DFA_OK:
+        raise DfaError(fn, rc)
+
+
+def _stream_ptr(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check_qkv(*ts):
+    q = ts[0]
+    if q.dim() != 4:
+        raise ValueError("expected (batch, seqlen, heads, headdim) tensors")
+    for t in ts:
+        if t.shape != q.shape:
+            raise ValueError("all tensors must have the shape of q")
+        if t.dtype != torch.bfloat16:
+            raise TypeError("tensors must be bfloat16")
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError("tensors must live on the same CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def dfa_forward(q, k, v, block_size, out=None, lse=None):
+    """Block-diffusion attention forward.  q, k, v: (B, 2n, H, d) bf16 CUDA.
+
+    Returns (out, lse) with out (B, 2n, H, d) bf16 and lse (B, H, 2n) fp32.
+    """
+    _check_qkv(q, k, v)
+    B, L, H, d = q.shape
+    if L % 2:
+        raise ValueError("the sequence must be [noisy | clean] with an even length 2n")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L // 2, H, d,
+                               int(block_size), _stream_ptr(q))
+    _check("dfa_forward", rc)
+    return out, lse
+
+
+def dfa_backward(q, k, v, out, dout, lse, block_size, dq=None, dk=None, dv=None):
+    """Block-diffusion attention backward; returns (dq, dk, dv) bf16."""
+    _check_qkv(q, k, v, out, dout)
+    B, L, H, d = q.shape
+    if lse.shape != (B, H, L) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 (B, H, 2n)")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                _ptr(dq), _ptr(dk), _ptr(dv), B, L // 2, H, d, int(block_size),
+                                _stream_ptr(q))
+    _check("dfa_backward", rc)
+    return dq, dk, dv
+
+
+def dfa_causal_forward(q, k, v, out=None, lse=None):
+    """Causal attention on (Bc, L, H, d) (Bc even): the yardstick."""
+    _check_qkv(q, k, v)
+    B, L, H, d = q.shape
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_causal_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, H, d,
+                                      _stream_ptr(q))
+    _check("dfa_causal_forward", rc)
+    return out, lse
+
+
+def dfa_causal_backward(q, k, v, out, dout, lse, dq=None, dk=None, dv=None):
+    _check_qkv(q, k, v, out, dout)
+    B, L, H, d = q.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_causal_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
+                                       _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, L, H, d,
+                                       _stream_ptr(q))
+    _check("dfa_causal_backward", rc)
+    return dq, dk, dv
+
+
+def dfa_status(device=None):
+    """Synchronise the current stream and return (and clear) the device status code."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        return lib().dfa_status(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+
+
+# ------------------------------------------------------------- geometry
+
+def dfa_fwd_segments(mode, n, block_size, block_m, block_n, q_half, q_tile):
+    buf = (_I * 8)()
+    cnt = lib().dfa_fwd_segments(mode, n, block_size, block_m, block_n, q_half, q_tile, buf)
+    _check("dfa_fwd_segments", 0 if cnt >= 0 else cnt)
+    return [tuple(buf[4 * i:4 * i + 4]) for i in range(cnt)]
+
+
+def dfa_bwd_segments(mode, n, block_size, block_m, block_n, k_half, k_tile):
+    buf = (_I * 8)()
+    cnt = lib().dfa_bwd_segments(mode, n, block_size, block_m, block_n, k_half, k_tile, buf)
+    _check("dfa_bwd_segments", 0 if cnt >= 0 else cnt)
+    return [tuple(buf[4 * i:4 * i + 4]) for i in range(cnt)]
+
+
+def dfa_tile_full(rule, n, block_size, q_start, block_m, k_start, block_n):
+    return lib().dfa_tile_full(rule, n, block_size, q_start, block_m, k_start, block_n)
+
+
+def dfa_tile_visits(mode, n, block_size, block_m, block_n, pass_):
+    return lib().dfa_tile_visits(mode, n, block_size, block_m, block_n, pass_)
+
+
+def dfa_tile_shape(headdim):
+    vals = [_I() for _ in range(4)]
+    _check("dfa_tile_shape", lib().dfa_tile_shape(headdim, *[ctypes.byref(x) for x in vals]))
+    return tuple(x.value for x in vals)

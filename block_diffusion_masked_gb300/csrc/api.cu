@@ -1,0 +1,329 @@
+// C ABI of libdfa: argument checks, tensor maps, scratch, launches.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "dfa.h"
+#include "geometry.cuh"
+#include "params.cuh"
+
+// Device status word: kernels OR error bits into it, dfa_status() reads and
+// clears it.  Host code reaches it through cudaGetSymbolAddress.
+static __device__ unsigned g_dfa_status;
+
+namespace dfa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  unsigned* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device set-up on first use: check the architecture (the library holds
+// sm_103a code only) and find the device address of the status word.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DFA_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DFA_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return DFA_ECUDA;
+    s.supported = (major == 10 && minor == 3);
+    if (s.supported) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_dfa_status) != cudaSuccess) return DFA_ECUDA;
+      s.status = static_cast<unsigned*>(addr);
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return DFA_ECUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    s.ready = true;
+  }
+  if (!s.supported) return DFA_EUNSUPPORTED;
+  *out = &s;
+  return DFA_OK;
+}
+
+// View a (B, 2n, H, d) bf16 tensor as 5-D (d, H, n, half, B) -- strides
+// increasing -- and load boxes of (64, 1, rows, 1, 1) with 128-byte swizzle:
+// `rows` consecutive positions of one half of one head, 64 head dims each.
+// Rows past the end of a half read zero.
+int make_map(CUtensorMap* map, const void* base, int B, int n, int H, int d, int rows) {
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(n), 2, static_cast<cuuint64_t>(B)};
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(H) * d * 2;
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * 2, row_bytes, row_bytes * n,
+                                 row_bytes * 2 * n};
+  const cuuint32_t box[5] = {64, 1, static_cast<cuuint32_t>(rows), 1, 1};
+  const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFA_OK : DFA_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int n, int H, int d, int bs) {
+  if (B < 0 || n < 1 || H < 1 || bs < 1) return DFA_EINVAL;
+  if (d != 64 && d != 128 && d != 256) return DFA_EUNSUPPORTED;
+  // Index arithmetic inside the kernels uses 64-bit offsets; tile counts and
+  // the grid use 32-bit integers.
+  if (static_cast<long long>(n) * 2 > (1LL << 30)) return DFA_EINVAL;
+  return DFA_OK;
+}
+
+int forward_impl(int mode, const void* q, const void* k, const void* v, void* out, float* lse,
+                 int B, int n, int H, int d, int bs, cudaStream_t stream) {
+  int rc = check_common(B, n, H, d, bs);
+  if (rc) return rc;
+  if (B == 0) return DFA_OK;
+  if (!q || !k || !v || !out || !lse) return DFA_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return DFA_EINVAL;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds))) return rc;
+  TileShape ts;
+  tile_shape_for(d, &ts);
+  FwdParams p;
+  if ((rc = make_map(&p.tm_q, q, B, n, H, d, ts.fwd_bm))) return rc;
+  if ((rc = make_map(&p.tm_k, k, B, n, H, d, ts.fwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_v, v, B, n, H, d, ts.fwd_bn))) return rc;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = ds->status;
+  p.B = B;
+  p.n = n;
+  p.H = H;
+  p.bs = bs < n ? bs : n;
+  p.mode = mode;
+  p.q_tiles = cdiv(n, ts.fwd_bm);
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  return launch_forward(p, d, stream) == cudaSuccess ? DFA_OK : DFA_ECUDA;
+}
+
+int backward_impl(int mode, const void* q, const void* k, const void* v, const void* out,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int n,
+                  int H, int d, int bs, cudaStream_t stream) {
+  int rc = check_common(B, n, H, d, bs);
+  if (rc) return rc;
+  if (d == 256) return DFA_EUNSUPPORTED;
+  if (B == 0) return DFA_OK;
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return DFA_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return DFA_EINVAL;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds))) return rc;
+  TileShape ts;
+  tile_shape_for(d, &ts);
+  const size_t L = 2 * static_cast<size_t>(n);
+  const size_t elems = static_cast<size_t>(B) * L * H * d;
+  const size_t rows = static_cast<size_t>(B) * H * L;
+  float* dq_acc = nullptr;
+  float* delta = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&dq_acc), elems * sizeof(float), stream) !=
+      cudaSuccess)
+    return DFA_ECUDA;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&delta), rows * sizeof(float), stream) !=
+      cudaSuccess) {
+    cudaFreeAsync(dq_acc, stream);
+    return DFA_ECUDA;
+  }
+  BwdParams p;
+  rc = make_map(&p.tm_q, q, B, n, H, d, ts.bwd_bm);
+  if (!rc) rc = make_map(&p.tm_do, dout, B, n, H, d, ts.bwd_bm);
+  if (!rc) rc = make_map(&p.tm_k, k, B, n, H, d, ts.bwd_bn);
+  if (!rc) rc = make_map(&p.tm_v, v, B, n, H, d, ts.bwd_bn);
+  if (!rc) {
+    p.lse = lse;
+    p.delta = delta;
+    p.dq_acc = dq_acc;
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.status = ds->status;
+    p.B = B;
+    p.n = n;
+    p.H = H;
+    p.bs = bs < n ? bs : n;
+    p.mode = mode;
+    p.k_tiles = cdiv(n, ts.bwd_bn);
+    p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    cudaError_t e = launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(out),
+                                          static_cast<const __nv_bfloat16*>(dout), delta, dq_acc,
+                                          B, static_cast<int>(L), H, d, stream);
+    if (e == cudaSuccess) e = launch_backward(p, d, stream);
+    if (e == cudaSuccess)
+      e = launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq),
+                            static_cast<long long>(elems), stream);
+    if (e != cudaSuccess) rc = DFA_ECUDA;
+  }
+  cudaFreeAsync(delta, stream);
+  cudaFreeAsync(dq_acc, stream);
+  return rc;
+}
+
+}  // namespace
+}  // namespace dfa
+
+using namespace dfa;
+
+extern "C" {
+
+int dfa_version(void) { return 100; }
+
+const char* dfa_error_string(int code) {
+  switch (code) {
+    case DFA_OK: return "ok";
+    case DFA_EINVAL: return "invalid argument";
+    case DFA_EUNSUPPORTED: return "unsupported head dimension or device";
+    case DFA_ECUDA: return "CUDA call failed";
+    case DFA_ETIMEOUT: return "a kernel wait timed out";
+    case DFA_EDEVICE: return "a kernel index check failed";
+    default: return "unknown error";
+  }
+}
+
+int dfa_forward(const void* q, const void* k, const void* v, void* out, float* lse, int batch,
+                int n, int heads, int headdim, int block_size, dfa_stream_t stream) {
+  return forward_impl(MODE_DIFFUSION, q, k, v, out, lse, batch, n, heads, headdim, block_size,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int dfa_backward(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int batch, int n, int heads,
+                 int headdim, int block_size, dfa_stream_t stream) {
+  return backward_impl(MODE_DIFFUSION, q, k, v, out, dout, lse, dq, dk, dv, batch, n, heads,
+                       headdim, block_size, static_cast<cudaStream_t>(stream));
+}
+
+// Causal attention on (batch, seqlen, heads, headdim).  A contiguous tensor of
+// that shape is, byte for byte, a (batch/2, 2*seqlen, heads, headdim) tensor
+// whose halves are consecutive sequences, so the diffusion kernels run it in
+// their causal mode (each half attends causally to itself).  batch must be
+// even, as it is for the yardstick on the 2B halves of B samples.
+int dfa_causal_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+                       int batch, int seqlen, int heads, int headdim, dfa_stream_t stream) {
+  if (batch < 0 || seqlen < 1) return DFA_EINVAL;
+  if (batch % 2) return DFA_EINVAL;
+  return forward_impl(MODE_CAUSAL, q, k, v, out, lse, batch / 2, seqlen, heads, headdim, 1,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int dfa_causal_backward(const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        int batch, int seqlen, int heads, int headdim, dfa_stream_t stream) {
+  if (batch < 0 || seqlen < 1) return DFA_EINVAL;
+  if (batch % 2) return DFA_EINVAL;
+  return backward_impl(MODE_CAUSAL, q, k, v, out, dout, lse, dq, dk, dv, batch / 2, seqlen, heads,
+                       headdim, 1, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_status(dfa_stream_t stream) {
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DFA_ECUDA;
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_dfa_status, sizeof(word)) != cudaSuccess) return DFA_ECUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_dfa_status, &zero, sizeof(zero)) != cudaSuccess) return DFA_ECUDA;
+  if (word & kStatusTimeout) return DFA_ETIMEOUT;
+  if (word & kStatusIndex) return DFA_EDEVICE;
+  return DFA_OK;
+}
+
+static int encode_segments(const Segment* seg, int cnt, int* out) {
+  for (int i = 0; i < cnt; ++i) {
+    out[4 * i + 0] = seg[i].half;
+    out[4 * i + 1] = seg[i].rule;
+    out[4 * i + 2] = seg[i].t_begin;
+    out[4 * i + 3] = seg[i].t_end;
+  }
+  return cnt;
+}
+
+static bool geom_args_ok(int mode, int n, int bs, int bm, int bn, int half) {
+  return (mode == MODE_DIFFUSION || mode == MODE_CAUSAL) && n >= 1 && bs >= 1 && bm >= 1 &&
+         bn >= 1 && (half == 0 || half == 1);
+}
+
+int dfa_fwd_segments(int mode, int n, int block_size, int block_m, int block_n, int q_half,
+                     int q_tile, int* seg) {
+  if (!seg || !geom_args_ok(mode, n, block_size, block_m, block_n, q_half) || q_tile < 0)
+    return DFA_EINVAL;
+  Segment s[2];
+  const int cnt = fwd_segments(mode, n, block_size < n ? block_size : n, block_m, block_n, q_half,
+                               q_tile, s);
+  return encode_segments(s, cnt, seg);
+}
+
+int dfa_bwd_segments(int mode, int n, int block_size, int block_m, int block_n, int k_half,
+                     int k_tile, int* seg) {
+  if (!seg || !geom_args_ok(mode, n, block_size, block_m, block_n, k_half) || k_tile < 0)
+    return DFA_EINVAL;
+  Segment s[2];
+  const int cnt = bwd_segments(mode, n, block_size < n ? block_size : n, block_m, block_n, k_half,
+                               k_tile, s);
+  return encode_segments(s, cnt, seg);
+}
+
+int dfa_tile_full(int rule, int n, int block_size, int q_start, int block_m, int k_start,
+                  int block_n) {
+  if (n < 1 || block_size < 1 || block_m < 1 || block_n < 1) return DFA_EINVAL;
+  return tile_full(rule, n, block_size < n ? block_size : n, q_start, block_m, k_start, block_n)
+             ? 1
+             : 0;
+}
+
+long long dfa_tile_visits(int mode, int n, int block_size, int block_m, int block_n, int pass) {
+  if (!geom_args_ok(mode, n, block_size, block_m, block_n, 0) || (pass != 0 && pass != 1))
+    return DFA_EINVAL;
+  const int bs = block_size < n ? block_size : n;
+  long long total = 0;
+  const int tiles = cdiv(n, pass == 0 ? block_m : block_n);
+  for (int half = 0; half < 2; ++half)
+    for (int t = 0; t < tiles; ++t) {
+      Segment s[2];
+      const int cnt = pass == 0 ? fwd_segments(mode, n, bs, block_m, block_n, half, t, s)
+                                : bwd_segments(mode, n, bs, block_m, block_n, half, t, s);
+      for (int i = 0; i < cnt; ++i) total += s[i].t_end - s[i].t_begin;
+    }
+  return total;
+}
+
+int dfa_tile_shape(int headdim, int* fwd_block_m, int* fwd_block_n, int* bwd_block_n,
+                   int* bwd_block_m) {
+  TileShape t;
+  if (!tile_shape_for(headdim, &t)) return DFA_EUNSUPPORTED;
+  if (fwd_block_m) *fwd_block_m = t.fwd_bm;
+  if (fwd_block_n) *fwd_block_n = t.fwd_bn;
+  if (bwd_block_n) *bwd_block_n = t.bwd_bn;
+  if (bwd_block_m) *bwd_block_m = t.bwd_bm;
+  return DFA_OK;
+}
+
+}  // extern "C"

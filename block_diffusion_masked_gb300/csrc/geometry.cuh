@@ -1,0 +1,181 @@
+// Tile geometry of block-diffusion attention, shared by the host scheduler
+// and the kernels.
+//
+// Source: "Fast Diffusion Attention", sections "Block diffusion in one
+// picture" (the mask) and "Visit only the visible tiles" (the two halves are
+// tiled separately; a query tile visits exactly the key tiles that intersect
+// the mask, and in the backward pass a key tile visits exactly the query
+// tiles that see it; only tiles cut by a block boundary are masked element by
+// element).
+//
+// Every rule below makes the visible set of one query row a single interval
+// of key positions inside one half, and the set of query rows that see one
+// key a single interval of query positions; both interval ends are
+// non-decreasing in the row (resp. key) index.  Unions over a tile and the
+// "fully visible" test therefore only look at the first and last row.
+#pragma once
+
+#if defined(__CUDACC__)
+#define DFA_HD __host__ __device__ __forceinline__
+#else
+#define DFA_HD inline
+#endif
+
+namespace dfa {
+
+enum Half : int { HALF_NOISY = 0, HALF_CLEAN = 1 };
+enum Mode : int { MODE_DIFFUSION = 0, MODE_CAUSAL = 1 };
+// Which (query half, key half) pair a tile belongs to.
+enum Rule : int { RULE_NONE = -1, RULE_NN = 0, RULE_NC = 1, RULE_CC = 2, RULE_CAUSAL = 3 };
+
+struct Interval {
+  int lo, hi;  // [lo, hi), empty when lo >= hi
+};
+
+struct Segment {
+  int half;     // the other side's half (key half forward, query half backward)
+  int rule;
+  int t_begin;  // first tile index inside that half
+  int t_end;    // one past the last tile
+};
+
+DFA_HD int imin(int a, int b) { return a < b ? a : b; }
+DFA_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+DFA_HD int rule_for(int mode, int q_half, int k_half) {
+  if (mode == MODE_CAUSAL) return q_half == k_half ? RULE_CAUSAL : RULE_NONE;
+  if (q_half == HALF_NOISY) return k_half == HALF_NOISY ? RULE_NN : RULE_NC;
+  return k_half == HALF_CLEAN ? RULE_CC : RULE_NONE;
+}
+
+// Keys (positions inside their half) visible to query row r of its half.
+// block_size must already be clamped to [1, n].
+DFA_HD Interval key_interval(int rule, int r, int n, int bs) {
+  if (r < 0 || r >= n) return {0, 0};
+  const int b0 = (r / bs) * bs;
+  const int b1 = imin(n, b0 + bs);
+  switch (rule) {
+    case RULE_NN: return {b0, b1};        // own noisy block, both directions
+    case RULE_NC: return {0, b0};         // clean blocks strictly before
+    case RULE_CC: return {0, b1};         // clean blocks up to its own
+    case RULE_CAUSAL: return {0, r + 1};
+    default: return {0, 0};
+  }
+}
+
+// Query rows (inside their half) that see key j of its half.
+DFA_HD Interval query_interval(int rule, int j, int n, int bs) {
+  if (j < 0 || j >= n) return {0, 0};
+  const int b0 = (j / bs) * bs;
+  const int b1 = imin(n, b0 + bs);
+  switch (rule) {
+    case RULE_NN: return {b0, b1};
+    case RULE_NC: return {b1, n};         // noisy rows of strictly later blocks
+    case RULE_CC: return {b0, n};
+    case RULE_CAUSAL: return {j, n};
+    default: return {0, 0};
+  }
+}
+
+// Every pair of the tile [qs, qs+bm) x [ks, ks+bn) is visible (no padding rows
+// or keys, no block boundary cutting it).
+DFA_HD bool tile_full(int rule, int n, int bs, int qs, int bm, int ks, int bn) {
+  if (rule == RULE_NONE || qs + bm > n || ks + bn > n || qs < 0 || ks < 0) return false;
+  const Interval first = key_interval(rule, qs, n, bs);
+  const Interval last = key_interval(rule, qs + bm - 1, n, bs);
+  return last.lo <= ks && ks + bn <= first.hi;
+}
+
+// Forward: key-tile segments of query tile qt of half q_half.  Clean keys
+// first, then the noisy diagonal.  Returns the number of segments (0..2).
+DFA_HD int fwd_segments(int mode, int n, int bs, int bm, int bn, int q_half, int qt,
+                        Segment* seg) {
+  const int qs = qt * bm;
+  const int qe = imin(n, qs + bm);
+  int cnt = 0;
+  if (qs >= qe) return 0;
+  for (int kh = HALF_CLEAN; kh >= HALF_NOISY; --kh) {
+    const int rule = rule_for(mode, q_half, kh);
+    if (rule == RULE_NONE) continue;
+    const int lo = key_interval(rule, qs, n, bs).lo;
+    const int hi = key_interval(rule, qe - 1, n, bs).hi;
+    if (lo >= hi) continue;
+    seg[cnt].half = kh;
+    seg[cnt].rule = rule;
+    seg[cnt].t_begin = lo / bn;
+    seg[cnt].t_end = cdiv(hi, bn);
+    ++cnt;
+  }
+  return cnt;
+}
+
+// Backward: query-tile segments that see key tile kt of half k_half.  Clean
+// queries first, then noisy queries.
+DFA_HD int bwd_segments(int mode, int n, int bs, int bm, int bn, int k_half, int kt,
+                        Segment* seg) {
+  const int ks = kt * bn;
+  const int ke = imin(n, ks + bn);
+  int cnt = 0;
+  if (ks >= ke) return 0;
+  for (int qh = HALF_CLEAN; qh >= HALF_NOISY; --qh) {
+    const int rule = rule_for(mode, qh, k_half);
+    if (rule == RULE_NONE) continue;
+    const int lo = query_interval(rule, ks, n, bs).lo;
+    const int hi = query_interval(rule, ke - 1, n, bs).hi;
+    if (lo >= hi) continue;
+    seg[cnt].half = qh;
+    seg[cnt].rule = rule;
+    seg[cnt].t_begin = lo / bm;
+    seg[cnt].t_end = cdiv(hi, bm);
+    ++cnt;
+  }
+  return cnt;
+}
+
+// Work decoding.  Forward: one work item per (batch, head, half, query tile),
+// longest first: query tiles in decreasing index, both halves of every
+// (batch, head) side by side.  Backward: key tiles; in the diffusion mode the
+// clean key tiles (seen by clean and noisy queries) come first in increasing
+// index, then the noisy key tiles (seen only by their own noisy blocks).
+struct WorkItem {
+  int b, h, half, tile;
+};
+
+DFA_HD WorkItem fwd_work(int w, int mode, int B, int H, int tiles) {
+  (void)mode;
+  const int per = 2 * B * H;
+  WorkItem it;
+  it.tile = tiles - 1 - w / per;
+  const int rem = w % per;
+  it.half = rem & 1;
+  const int bh = rem >> 1;
+  it.b = bh / H;
+  it.h = bh % H;
+  return it;
+}
+
+DFA_HD WorkItem bwd_work(int w, int mode, int B, int H, int tiles) {
+  const int bhn = B * H;
+  WorkItem it;
+  int bh;
+  if (mode == MODE_CAUSAL) {
+    it.tile = w / (2 * bhn);
+    const int rem = w % (2 * bhn);
+    it.half = rem & 1;
+    bh = rem >> 1;
+  } else if (w < bhn * tiles) {
+    it.half = HALF_CLEAN;
+    it.tile = w / bhn;
+    bh = w % bhn;
+  } else {
+    const int w2 = w - bhn * tiles;
+    it.half = HALF_NOISY;
+    it.tile = w2 / bhn;
+    bh = w2 % bhn;
+  }
+  it.b = bh / H;
+  it.h = bh % H;
+  return it;
+}
+
+}  // namespace dfa

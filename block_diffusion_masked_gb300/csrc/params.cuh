@@ -1,0 +1,69 @@
+// Parameter blocks handed from the C ABI layer to the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace dfa {
+
+// Device status bits, OR-ed into the status word a kernel receives.
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusIndex = 2u;
+
+// Forward kernel parameters.  Tensor maps view q/k/v as 5-D arrays
+// (headdim, heads, n, half, batch) so that a tile never crosses the
+// noisy/clean boundary and rows past the end of a half read as zeros.
+struct FwdParams {
+  CUtensorMap tm_q;  // box (64, 1, block_m, 1, 1)
+  CUtensorMap tm_k;  // box (64, 1, block_n, 1, 1)
+  CUtensorMap tm_v;  // box (64, 1, block_n, 1, 1)
+  __nv_bfloat16* out;
+  float* lse;
+  unsigned* status;
+  int B, n, H, bs, mode;
+  int q_tiles;       // tiles per half along the queries
+  float scale_log2;  // softmax scale * log2(e)
+};
+
+struct BwdParams {
+  CUtensorMap tm_q;   // box (64, 1, block_m, 1, 1)
+  CUtensorMap tm_do;  // box (64, 1, block_m, 1, 1)
+  CUtensorMap tm_k;   // box (64, 1, block_n, 1, 1)
+  CUtensorMap tm_v;   // box (64, 1, block_n, 1, 1)
+  const float* lse;   // (B, H, 2n)
+  const float* delta; // (B, H, 2n): rowsum(dout * out)
+  float* dq_acc;      // (B, 2n, H, d) fp32, zeroed before the kernel
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  unsigned* status;
+  int B, n, H, bs, mode;
+  int k_tiles;        // tiles per half along the keys
+  float scale;        // softmax scale
+  float scale_log2;   // scale * log2(e)
+};
+
+// Launchers (one per translation unit).  Return a cudaError_t.
+cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream);
+cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const __nv_bfloat16* out, const __nv_bfloat16* dout,
+                                  float* delta, float* dq_acc, int B, int L, int H, int d,
+                                  cudaStream_t stream);
+cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, long long count,
+                              cudaStream_t stream);
+
+// Tile shapes per head dimension.
+struct TileShape {
+  int fwd_bm, fwd_bn, bwd_bn, bwd_bm;
+};
+inline bool tile_shape_for(int d, TileShape* t) {
+  switch (d) {
+    case 64: *t = {128, 128, 128, 128}; return true;
+    case 128: *t = {128, 128, 128, 64}; return true;
+    case 256: *t = {128, 64, 128, 64}; return true;
+    default: return false;
+  }
+}
+
+}  // namespace dfa

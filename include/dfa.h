@@ -1,0 +1,148 @@
+/*
+ * dfa.h - C ABI of libdfa: exact softmax attention under the block-diffusion
+ * mask, forward and backward, on NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  A sample is the concatenation [noisy | clean] of two halves
+ * of n tokens ("Fast Diffusion Attention", section "Block diffusion in one
+ * picture").  Positions inside a half are cut into blocks of block_size
+ * tokens, starting at the first position of the half (the last block is
+ * short when block_size does not divide n; block_size > n gives one block
+ * per half).  With blk(p) the block of position p inside its half:
+ *   noisy query i, noisy key j : visible iff blk(j) == blk(i)
+ *   noisy query i, clean key j : visible iff blk(j) <  blk(i)
+ *   clean query i, clean key j : visible iff blk(j) <= blk(i)
+ *   clean query i, noisy key j : never visible.
+ * out = softmax(scale * q k^T restricted to visible pairs) v, scale =
+ * 1/sqrt(headdim); lse is the natural-log log-sum-exp of the scaled visible
+ * scores of each row, kept for the recompute-based backward ("FlashAttention:
+ * Exact Attention Without Materialization", section 4.5).  No score or
+ * probability matrix is ever written to device memory.
+ *
+ * Layout.  Every q/k/v/out/dout/dq/dk/dv tensor is a contiguous row-major
+ * bfloat16 array of shape (batch, 2n, heads, headdim): positions [0, n) are
+ * the noisy half, [n, 2n) the clean half.  lse is a contiguous float32 array
+ * of shape (batch, heads, 2n).  Every base pointer must be 16-byte aligned.
+ * headdim must be 64, 128 or 256.
+ *
+ * Pointers.  All tensor pointers are DEVICE pointers on the current CUDA
+ * device, owned by the caller; the library never frees or retains them.
+ * `stream` is a cudaStream_t passed as an opaque pointer (NULL = the legacy
+ * default stream).  All calls are asynchronous on that stream: a return of
+ * DFA_OK means the work was enqueued.
+ *
+ * Errors.  Functions return 0 (DFA_OK) or a negative code below; nothing
+ * else crosses the ABI.  Argument errors are detected on the host before any
+ * launch.  Kernels never trap: every wait inside a kernel is bounded, and a
+ * kernel that gives up records DFA_ETIMEOUT in a device status word that
+ * dfa_status() reads.
+ */
+#ifndef DFA_H_
+#define DFA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFA_OK 0
+#define DFA_EINVAL (-1)        /* bad shape, null or misaligned pointer      */
+#define DFA_EUNSUPPORTED (-2)  /* headdim not supported, or device not sm_103 */
+#define DFA_ECUDA (-3)         /* a CUDA runtime/driver call failed           */
+#define DFA_ETIMEOUT (-4)      /* a kernel's bounded wait gave up             */
+#define DFA_EDEVICE (-5)       /* a kernel's own index check failed           */
+
+#define DFA_MODE_DIFFUSION 0   /* block-diffusion mask over [noisy | clean]   */
+#define DFA_MODE_CAUSAL 1      /* causal mask inside each half (yardstick)    */
+
+typedef void *dfa_stream_t;
+
+/* Library version as 10000*major + 100*minor + patch. */
+int dfa_version(void);
+
+/* Human-readable name of a return code (static storage, never NULL). */
+const char *dfa_error_string(int code);
+
+/*
+ * Forward pass ("Fast Diffusion Attention", "Visit only the visible tiles";
+ * "FlashAttention: Exact Attention Without Materialization", sections 4.1-4.2
+ * and 5.1).  Reads q, k, v; writes out (batch, 2n, heads, headdim) bf16 and
+ * lse (batch, heads, 2n) fp32.  n >= 1, block_size >= 1.  Allocates nothing.
+ */
+int dfa_forward(const void *q, const void *k, const void *v, void *out, float *lse,
+                int batch, int n, int heads, int headdim, int block_size,
+                dfa_stream_t stream);
+
+/*
+ * Backward pass ("FlashAttention: Exact Attention Without Materialization",
+ * section 4.5; the key-tile enumeration of "Visit only the visible tiles").
+ * Given q, k, v, the forward's out and lse, and dout, writes dq, dk, dv
+ * (batch, 2n, heads, headdim) bf16: the gradients of sum(dout * out).
+ * Scratch: a float32 dq accumulator of the shape of q and a float32 row
+ * vector D = rowsum(dout * out) of the shape of lse are allocated and freed
+ * stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync).
+ */
+int dfa_backward(const void *q, const void *k, const void *v, const void *out,
+                 const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                 int batch, int n, int heads, int headdim, int block_size,
+                 dfa_stream_t stream);
+
+/*
+ * The yardstick of "Fast Diffusion Attention", section "The right yardstick":
+ * causal attention on `batch` independent sequences of length `seqlen`, same
+ * layout (batch, seqlen, heads, headdim), lse (batch, heads, seqlen), run by
+ * the same kernels with causal tile enumeration.  Viewing a (B, 2n, H, d)
+ * tensor as (2B, n, H, d) gives causal attention on the 2B halves.  batch
+ * must be even (DFA_EINVAL otherwise): the kernels pair consecutive sequences
+ * as the two halves of one sample.  Scratch of dfa_causal_backward as for
+ * dfa_backward.
+ */
+int dfa_causal_forward(const void *q, const void *k, const void *v, void *out, float *lse,
+                       int batch, int seqlen, int heads, int headdim, dfa_stream_t stream);
+int dfa_causal_backward(const void *q, const void *k, const void *v, const void *out,
+                        const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                        int batch, int seqlen, int heads, int headdim, dfa_stream_t stream);
+
+/*
+ * Synchronise `stream`, then return and clear the device status word of the
+ * current device: DFA_OK, DFA_ETIMEOUT or DFA_EDEVICE (or DFA_ECUDA if the
+ * synchronisation itself failed).
+ */
+int dfa_status(dfa_stream_t stream);
+
+/*
+ * Tile geometry, host side, for tests and schedulers.  mode is one of
+ * DFA_MODE_*; halves are 0 (noisy) and 1 (clean); tiles are block_m query
+ * rows by block_n keys, counted inside a half.
+ *
+ * dfa_fwd_segments: key tiles visited by query tile q_tile of half q_half.
+ * Writes up to 2 segments as 4 ints each (key_half, rule, first_tile,
+ * end_tile) into seg[8] and returns their number (or a negative code).
+ *
+ * dfa_bwd_segments: query tiles that see key tile k_tile of half k_half,
+ * same encoding with the query half in place of the key half.
+ *
+ * dfa_tile_full: 1 if every (query, key) pair of the tile is visible under
+ * `rule` (so the kernels skip per-element masking), else 0.
+ *
+ * dfa_tile_visits: total tile visits per (batch, head) of the forward
+ * (pass 0) or backward (pass 1) enumeration.
+ */
+int dfa_fwd_segments(int mode, int n, int block_size, int block_m, int block_n,
+                     int q_half, int q_tile, int *seg);
+int dfa_bwd_segments(int mode, int n, int block_size, int block_m, int block_n,
+                     int k_half, int k_tile, int *seg);
+int dfa_tile_full(int rule, int n, int block_size, int q_start, int block_m,
+                  int k_start, int block_n);
+long long dfa_tile_visits(int mode, int n, int block_size, int block_m, int block_n, int pass);
+
+/*
+ * Tile shapes the kernels use for a head dimension: forward query rows and
+ * keys per tile, backward keys and query rows per tile.  Returns DFA_OK or
+ * DFA_EUNSUPPORTED.
+ */
+int dfa_tile_shape(int headdim, int *fwd_block_m, int *fwd_block_n,
+                   int *bwd_block_n, int *bwd_block_m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFA_H_ */

@@ -1,0 +1,175 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Same seeded bf16 inputs on both sides.  Error measure (normwise, per tensor):
+max |gpu - oracle| / max |oracle|.  Bars: 1e-2 for out, 2e-2 for dq, dk and
+dv (bf16 inputs, fp32 accumulation); |lse - oracle| <= 1e-3 absolute.
+Small shapes are compared in full; the full-size workloads are run at full
+size and compared on sampled (batch, head) pairs, computed by the oracle one
+head at a time.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_diffusion_masked_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 1e-2
+TOL_GRAD = 2e-2
+TOL_LSE = 1e-3
+
+
+@pytest.fixture(scope="module")
+def b():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_diffusion_masked_gb300 import binding, build
+
+    build.build()
+    binding.lib()
+    return binding
+
+
+def _np(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def normwise(got, ref):
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def _run_gpu(b, q, k, v, do, bs, backward=True):
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    out, lse = b.dfa_forward(qd, kd, vd, bs)
+    grads = b.dfa_backward(qd, kd, vd, out, dod, lse, bs) if backward else None
+    torch.cuda.synchronize()
+    assert b.dfa_status() == 0
+    res = {"out": _np(out), "lse": lse.cpu().double().numpy()}
+    if backward:
+        res.update(dq=_np(grads[0]), dk=_np(grads[1]), dv=_np(grads[2]))
+    return res
+
+
+def _check(res, q, k, v, do, bs, heads=None, backward=True):
+    qn, kn, vn, don = (_np(t) for t in (q, k, v, do))
+    if heads is None:
+        B, _, H, _ = q.shape
+        heads = [(bb, hh) for bb in range(B) for hh in range(H)]
+    out, lse = oracle.diffusion_forward(qn, kn, vn, bs, heads=heads)
+    sel = tuple(np.array(x) for x in zip(*heads))
+
+    def pick(a, layout):  # layout "bshd" or "bhs"
+        return a[sel[0], :, sel[1]] if layout == "bshd" else a[sel[0], sel[1]]
+
+    errs = {"out": normwise(pick(res["out"], "bshd"), pick(out, "bshd")),
+            "lse": float(np.abs(pick(res["lse"], "bhs") - pick(lse, "bhs")).max())}
+    if backward:
+        dq, dk, dv = oracle.diffusion_backward(qn, kn, vn, don, bs, heads=heads)
+        for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
+            errs[name] = normwise(pick(res[name], "bshd"), pick(ref, "bshd"))
+    assert np.isfinite(list(errs.values())).all(), errs
+    assert errs["out"] <= TOL_OUT, errs
+    assert errs["lse"] <= TOL_LSE, errs
+    for name in ("dq", "dk", "dv"):
+        if name in errs:
+            assert errs[name] <= TOL_GRAD, errs
+    return errs
+
+
+def test_tiny_workload(b):
+    w = inputs.WORKLOADS["tiny"]
+    q, k, v, do = inputs.make_workload_inputs(w)
+    res = _run_gpu(b, q, k, v, do, w.block_size)
+    _check(res, q, k, v, do, w.block_size)
+
+
+EDGE = [
+    # (B, n, H, d, bs): ragged halves, block sizes that cut tiles, bs > n
+    (1, 1, 1, 64, 1),
+    (1, 67, 2, 64, 1),
+    (1, 67, 2, 128, 3),
+    (2, 129, 1, 128, 5),
+    (1, 129, 2, 64, 64),
+    (1, 200, 1, 128, 300),
+    (1, 256, 2, 128, 16),
+    (2, 300, 1, 64, 7),
+    (1, 384, 1, 128, 128),
+    (1, 130, 1, 128, 1),
+]
+
+
+@pytest.mark.parametrize("B,n,H,d,bs", EDGE)
+def test_edge_cases(b, B, n, H, d, bs):
+    q, k, v, do = inputs.make_inputs(B, n, H, d, seed=100 + n + bs)
+    res = _run_gpu(b, q, k, v, do, bs)
+    _check(res, q, k, v, do, bs)
+
+
+@pytest.mark.parametrize("n,bs", [(67, 3), (256, 64), (300, 1)])
+def test_headdim_256_forward(b, n, bs):
+    q, k, v, do = inputs.make_inputs(1, n, 2, 256, seed=7 + n)
+    res = _run_gpu(b, q, k, v, do, bs, backward=False)
+    _check(res, q, k, v, do, bs, backward=False)
+
+
+def test_causal_yardstick(b):
+    # causal attention on the (2B, n, H, d) view of a (B, 2n, H, d) batch
+    B, n, H, d = 2, 200, 2, 128
+    q, k, v, do = inputs.make_inputs(B, n, H, d, seed=11)
+    dev = torch.device("cuda", 0)
+    qc, kc, vc, doc = (t.view(2 * B, n, H, d).to(dev) for t in (q, k, v, do))
+    out, lse = b.dfa_causal_forward(qc, kc, vc)
+    dq, dk, dv = b.dfa_causal_backward(qc, kc, vc, out, doc, lse)
+    torch.cuda.synchronize()
+    assert b.dfa_status() == 0
+    qn, kn, vn, don = (_np(t.view(2 * B, n, H, d)) for t in (q, k, v, do))
+    ro, rl = oracle.causal_forward(qn, kn, vn)
+    rq, rk, rv = oracle.causal_backward(qn, kn, vn, don)
+    assert normwise(_np(out), ro) <= TOL_OUT
+    assert np.abs(lse.cpu().double().numpy() - rl).max() <= TOL_LSE
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert normwise(_np(got), ref) <= TOL_GRAD
+
+
+def test_autograd_function(b):
+    from block_diffusion_masked_gb300 import diffusion_attn_func
+
+    q, k, v, do = inputs.make_inputs(1, 96, 2, 64, seed=5)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd = (t.to(dev).requires_grad_(True) for t in (q, k, v))
+    out = diffusion_attn_func(qd, kd, vd, 8)
+    out.backward(do.to(dev))
+    res = {"out": _np(out), "lse": np.zeros((1, 2, 192)), "dq": _np(qd.grad), "dk": _np(kd.grad),
+           "dv": _np(vd.grad)}
+    qn, kn, vn, don = (_np(t) for t in (q, k, v, do))
+    ro, _ = oracle.diffusion_forward(qn, kn, vn, 8)
+    rq, rk, rv = oracle.diffusion_backward(qn, kn, vn, don, 8)
+    assert normwise(res["out"], ro) <= TOL_OUT
+    for name, ref in (("dq", rq), ("dk", rk), ("dv", rv)):
+        assert normwise(res[name], ref) <= TOL_GRAD
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,heads", [
+    ("small", [(0, 0), (7, 15)]),
+    ("mid", [(3, 31)]),
+    ("long", [(0, 9)]),
+])
+def test_full_size_workloads_sampled(b, name, heads):
+    w = inputs.WORKLOADS[name]
+    q, k, v, do = inputs.make_workload_inputs(w)
+    res = _run_gpu(b, q, k, v, do, w.block_size)
+    _check(res, q, k, v, do, w.block_size, heads=heads)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["hd256_bs1", "hd256_bs64", "hd256_bs128"])
+def test_full_size_headdim_256_forward_sampled(b, name):
+    w = inputs.WORKLOADS[name]
+    q, k, v, do = inputs.make_workload_inputs(w)
+    res = _run_gpu(b, q, k, v, do, w.block_size, backward=False)
+    _check(res, q, k, v, do, w.block_size, heads=[(1, 7)], backward=False)

@@ -39,6 +39,9 @@ _SIGNATURES = {
     "dfa_causal_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "dfa_causal_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _P]),
     "dfa_status": (_I, [_P]),
+    "dfa_bwd_preprocess": (_I, [_P] * 4 + [_I] * 4 + [_P]),
+    "dfa_bwd_main": (_I, [_P] * 9 + [_I] * 6 + [_P]),
+    "dfa_bwd_dq_convert": (_I, [_P] * 2 + [_I] * 4 + [_P]),
     "dfa_fwd_segments": (_I, [_I] * 7 + [ctypes.POINTER(_I)]),
     "dfa_bwd_segments": (_I, [_I] * 7 + [ctypes.POINTER(_I)]),
     "dfa_tile_full": (_I, [_I] * 7),
@@ -157,6 +160,35 @@ def dfa_causal_backward(q, k, v, out, dout, lse, dq=None, dk=None, dv=None):
                                        _stream_ptr(q))
     _check("dfa_causal_backward", rc)
     return dq, dk, dv
+
+
+def dfa_bwd_preprocess(out, dout, delta, dq_acc):
+    """Step 1 of the backward: delta = rowsum(dout * out); dq_acc = 0."""
+    _check_qkv(out, dout)
+    B, L, H, d = out.shape
+    with torch.cuda.device(out.device):
+        rc = lib().dfa_bwd_preprocess(_ptr(out), _ptr(dout), _ptr(delta), _ptr(dq_acc), B, L // 2,
+                                      H, d, _stream_ptr(out))
+    _check("dfa_bwd_preprocess", rc)
+
+
+def dfa_bwd_main(q, k, v, dout, lse, delta, dq_acc, dk, dv, block_size, mode=MODE_DIFFUSION):
+    """Step 2 of the backward: the tensor-core kernel (dk, dv, dq_acc += dq)."""
+    _check_qkv(q, k, v, dout, dk, dv)
+    B, L, H, d = q.shape
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(delta),
+                                _ptr(dq_acc), _ptr(dk), _ptr(dv), B, L // 2, H, d,
+                                int(block_size), int(mode), _stream_ptr(q))
+    _check("dfa_bwd_main", rc)
+
+
+def dfa_bwd_dq_convert(dq_acc, dq):
+    """Step 3 of the backward: dq = bf16(dq_acc)."""
+    B, L, H, d = dq.shape
+    with torch.cuda.device(dq.device):
+        rc = lib().dfa_bwd_dq_convert(_ptr(dq_acc), _ptr(dq), B, L // 2, H, d, _stream_ptr(dq))
+    _check("dfa_bwd_dq_convert", rc)
 
 
 def dfa_status(device=None):

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <initializer_list>
 #include <mutex>
 
 #include "dfa.h"
@@ -123,6 +124,79 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   return launch_forward(p, d, stream) == cudaSuccess ? DFA_OK : DFA_ECUDA;
 }
 
+bool aligned_all(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return false;
+  return true;
+}
+
+// The tensor-core backward step alone: caller-owned delta and dq_acc.
+int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const void* dout,
+                  const float* lse, const float* delta, float* dq_acc, void* dk, void* dv, int B,
+                  int n, int H, int d, int bs, cudaStream_t stream) {
+  int rc = check_common(B, n, H, d, bs);
+  if (rc) return rc;
+  if (d == 256) return DFA_EUNSUPPORTED;
+  if (B == 0) return DFA_OK;
+  if (!aligned_all({q, k, v, dout, dq_acc, dk, dv}) || !lse || !delta ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(delta) & 3u))
+    return DFA_EINVAL;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds))) return rc;
+  TileShape ts;
+  tile_shape_for(d, &ts);
+  BwdParams p;
+  if ((rc = make_map(&p.tm_q, q, B, n, H, d, ts.bwd_bm))) return rc;
+  if ((rc = make_map(&p.tm_do, dout, B, n, H, d, ts.bwd_bm))) return rc;
+  if ((rc = make_map(&p.tm_k, k, B, n, H, d, ts.bwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_v, v, B, n, H, d, ts.bwd_bn))) return rc;
+  p.lse = lse;
+  p.delta = delta;
+  p.dq_acc = dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.status = ds->status;
+  p.B = B;
+  p.n = n;
+  p.H = H;
+  p.bs = bs < n ? bs : n;
+  p.mode = mode;
+  p.k_tiles = cdiv(n, ts.bwd_bn);
+  p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  return launch_backward(p, d, stream) == cudaSuccess ? DFA_OK : DFA_ECUDA;
+}
+
+int preprocess_impl(const void* out, const void* dout, float* delta, float* dq_acc, int B, int n,
+                    int H, int d, cudaStream_t stream) {
+  int rc = check_common(B, n, H, d, 1);
+  if (rc) return rc;
+  if (B == 0) return DFA_OK;
+  if (!aligned_all({out, dout, dq_acc}) || !delta || (reinterpret_cast<uintptr_t>(delta) & 3u))
+    return DFA_EINVAL;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds))) return rc;
+  return launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(out),
+                               static_cast<const __nv_bfloat16*>(dout), delta, dq_acc, B, 2 * n, H,
+                               d, stream) == cudaSuccess
+             ? DFA_OK
+             : DFA_ECUDA;
+}
+
+int convert_impl(const float* dq_acc, void* dq, int B, int n, int H, int d, cudaStream_t stream) {
+  int rc = check_common(B, n, H, d, 1);
+  if (rc) return rc;
+  if (B == 0) return DFA_OK;
+  if (!aligned_all({dq_acc, dq})) return DFA_EINVAL;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds))) return rc;
+  const long long elems = static_cast<long long>(B) * 2 * n * H * d;
+  return launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), elems, stream) == cudaSuccess
+             ? DFA_OK
+             : DFA_ECUDA;
+}
+
+// Full backward: stream-ordered scratch, then the three steps.
 int backward_impl(int mode, const void* q, const void* k, const void* v, const void* out,
                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int n,
                   int H, int d, int bs, cudaStream_t stream) {
@@ -130,15 +204,11 @@ int backward_impl(int mode, const void* q, const void* k, const void* v, const v
   if (rc) return rc;
   if (d == 256) return DFA_EUNSUPPORTED;
   if (B == 0) return DFA_OK;
-  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return DFA_EINVAL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+  if (!aligned_all({q, k, v, out, dout, dq, dk, dv}) || !lse ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return DFA_EINVAL;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds))) return rc;
-  TileShape ts;
-  tile_shape_for(d, &ts);
   const size_t L = 2 * static_cast<size_t>(n);
   const size_t elems = static_cast<size_t>(B) * L * H * d;
   const size_t rows = static_cast<size_t>(B) * H * L;
@@ -152,35 +222,9 @@ int backward_impl(int mode, const void* q, const void* k, const void* v, const v
     cudaFreeAsync(dq_acc, stream);
     return DFA_ECUDA;
   }
-  BwdParams p;
-  rc = make_map(&p.tm_q, q, B, n, H, d, ts.bwd_bm);
-  if (!rc) rc = make_map(&p.tm_do, dout, B, n, H, d, ts.bwd_bm);
-  if (!rc) rc = make_map(&p.tm_k, k, B, n, H, d, ts.bwd_bn);
-  if (!rc) rc = make_map(&p.tm_v, v, B, n, H, d, ts.bwd_bn);
-  if (!rc) {
-    p.lse = lse;
-    p.delta = delta;
-    p.dq_acc = dq_acc;
-    p.dk = static_cast<__nv_bfloat16*>(dk);
-    p.dv = static_cast<__nv_bfloat16*>(dv);
-    p.status = ds->status;
-    p.B = B;
-    p.n = n;
-    p.H = H;
-    p.bs = bs < n ? bs : n;
-    p.mode = mode;
-    p.k_tiles = cdiv(n, ts.bwd_bn);
-    p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
-    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
-    cudaError_t e = launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(out),
-                                          static_cast<const __nv_bfloat16*>(dout), delta, dq_acc,
-                                          B, static_cast<int>(L), H, d, stream);
-    if (e == cudaSuccess) e = launch_backward(p, d, stream);
-    if (e == cudaSuccess)
-      e = launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq),
-                            static_cast<long long>(elems), stream);
-    if (e != cudaSuccess) rc = DFA_ECUDA;
-  }
+  rc = preprocess_impl(out, dout, delta, dq_acc, B, n, H, d, stream);
+  if (!rc) rc = bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, d, bs, stream);
+  if (!rc) rc = convert_impl(dq_acc, dq, B, n, H, d, stream);
   cudaFreeAsync(delta, stream);
   cudaFreeAsync(dq_acc, stream);
   return rc;
@@ -240,6 +284,25 @@ int dfa_causal_backward(const void* q, const void* k, const void* v, const void*
   if (batch % 2) return DFA_EINVAL;
   return backward_impl(MODE_CAUSAL, q, k, v, out, dout, lse, dq, dk, dv, batch / 2, seqlen, heads,
                        headdim, 1, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_bwd_preprocess(const void* out, const void* dout, float* delta, float* dq_acc, int batch,
+                       int n, int heads, int headdim, dfa_stream_t stream) {
+  return preprocess_impl(out, dout, delta, dq_acc, batch, n, heads, headdim,
+                         static_cast<cudaStream_t>(stream));
+}
+
+int dfa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse,
+                 const float* delta, float* dq_acc, void* dk, void* dv, int batch, int n,
+                 int heads, int headdim, int block_size, int mode, dfa_stream_t stream) {
+  if (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) return DFA_EINVAL;
+  return bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, batch, n, heads, headdim,
+                       mode == MODE_CAUSAL ? 1 : block_size, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_bwd_dq_convert(const float* dq_acc, void* dq, int batch, int n, int heads, int headdim,
+                       dfa_stream_t stream) {
+  return convert_impl(dq_acc, dq, batch, n, heads, headdim, static_cast<cudaStream_t>(stream));
 }
 
 int dfa_status(dfa_stream_t stream) {

@@ -139,7 +139,6 @@ __global__ void __launch_bounds__(192, 1) dfa_bwd_kernel(const __grid_constant__
       }
     }
     __syncwarp();
-    const float* lse_bh = p.lse + (static_cast<size_t>(wi.b) * p.H + wi.h) * L;
     const float* del_bh = p.delta + (static_cast<size_t>(wi.b) * p.H + wi.h) * L;
     bool ok = true;
     int i = 0;
@@ -160,7 +159,9 @@ __global__ void __launch_bounds__(192, 1) dfa_bwd_kernel(const __grid_constant__
         const int q = qt * BMQ + c;
         const bool valid = q < p.n;
         const size_t pos = static_cast<size_t>(seg[s].half) * p.n + q;
-        lse_s[c] = valid ? lse_bh[pos] * 1.4426950408889634f : INFINITY;
+        lse_s[c] = valid ? p.lse[lse_offset(p.mode, wi.b, wi.h, seg[s].half, q, p.H, p.n)] *
+                               1.4426950408889634f
+                         : INFINITY;
         del_s[c] = valid ? del_bh[pos] : 0.f;
       }
       __syncwarp();

@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(192, 1) dfa_fwd_kernel(const __grid_constant__
       if (valid) {
         const float lse = l_run > 0.f ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f
                                       : -INFINITY;
-        p.lse[(static_cast<size_t>(wi.b) * p.H + wi.h) * L + pos] = lse;
+        p.lse[lse_offset(p.mode, wi.b, wi.h, wi.half, r, p.H, p.n)] = lse;
       }
     }
   }

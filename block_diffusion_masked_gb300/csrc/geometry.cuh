@@ -132,6 +132,15 @@ DFA_HD int bwd_segments(int mode, int n, int bs, int bm, int bn, int k_half, int
   return cnt;
 }
 
+// Offset of the log-sum-exp of row r of half `half` of sample b, head h.
+// Diffusion mode: lse is (B, H, 2n).  Causal mode: the sample is a pair of
+// consecutive sequences (2b, 2b+1) of length n and lse is (2B, H, n).
+DFA_HD long long lse_offset(int mode, int b, int h, int half, int r, int H, int n) {
+  if (mode == MODE_CAUSAL)
+    return ((2LL * b + half) * H + h) * static_cast<long long>(n) + r;
+  return (static_cast<long long>(b) * H + h) * (2LL * n) + static_cast<long long>(half) * n + r;
+}
+
 // Work decoding.  Forward: one work item per (batch, head, half, query tile),
 // longest first: query tiles in decreasing index, both halves of every
 // (batch, head) side by side.  Backward: key tiles; in the diffusion mode the

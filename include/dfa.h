@@ -102,6 +102,29 @@ int dfa_causal_backward(const void *q, const void *k, const void *v, const void 
                         int batch, int seqlen, int heads, int headdim, dfa_stream_t stream);
 
 /*
+ * The three steps dfa_backward runs, for callers that own the scratch or
+ * time the steps one by one.  `mode` is DFA_MODE_DIFFUSION or
+ * DFA_MODE_CAUSAL; in the causal mode (batch, n) describe the paired view
+ * (batch samples of two consecutive sequences of length n), block_size is
+ * ignored and lse is laid out (2*batch, heads, n) as dfa_causal_forward
+ * writes it.  delta is always (batch, heads, 2n).
+ *   dfa_bwd_preprocess: delta = rowsum(dout * out), float32 (batch, heads, 2n);
+ *     dq_acc (float32, shape of q) set to zero.
+ *   dfa_bwd_main: the tensor-core backward: writes dk, dv (bf16) and adds
+ *     dq (already scaled) into dq_acc with float32 atomics.
+ *   dfa_bwd_dq_convert: dq = bf16(dq_acc), round to nearest even.
+ * dq_acc and delta are device buffers the caller allocated (16-byte aligned).
+ */
+int dfa_bwd_preprocess(const void *out, const void *dout, float *delta, float *dq_acc,
+                       int batch, int n, int heads, int headdim, dfa_stream_t stream);
+int dfa_bwd_main(const void *q, const void *k, const void *v, const void *dout,
+                 const float *lse, const float *delta, float *dq_acc, void *dk, void *dv,
+                 int batch, int n, int heads, int headdim, int block_size, int mode,
+                 dfa_stream_t stream);
+int dfa_bwd_dq_convert(const float *dq_acc, void *dq, int batch, int n, int heads,
+                       int headdim, dfa_stream_t stream);
+
+/*
  * Synchronise `stream`, then return and clear the device status word of the
  * current device: DFA_OK, DFA_ETIMEOUT or DFA_EDEVICE (or DFA_ECUDA if the
  * synchronisation itself failed).

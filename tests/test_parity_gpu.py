@@ -69,8 +69,13 @@ def _check(res, q, k, v, do, bs, heads=None, backward=True):
             "lse": float(np.abs(pick(res["lse"], "bhs") - pick(lse, "bhs")).max())}
     if backward:
         dq, dk, dv = oracle.diffusion_backward(qn, kn, vn, don, bs, heads=heads)
-        for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
-            errs[name] = normwise(pick(res[name], "bshd"), pick(ref, "bshd"))
+        refs = {"dq": pick(dq, "bshd"), "dk": pick(dk, "bshd"), "dv": pick(dv, "bshd")}
+        # A gradient can be exactly zero (every row seeing a single key makes
+        # dS = 0): then measure it against 1e-3 of the largest gradient.
+        floor = 1e-3 * max(np.abs(r).max() for r in refs.values())
+        for name, ref in refs.items():
+            got = pick(res[name], "bshd")
+            errs[name] = float(np.abs(got - ref).max() / max(np.abs(ref).max(), floor))
     assert np.isfinite(list(errs.values())).all(), errs
     assert errs["out"] <= TOL_OUT, errs
     assert errs["lse"] <= TOL_LSE, errs

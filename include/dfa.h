@@ -125,6 +125,29 @@ int dfa_bwd_dq_convert(const float *dq_acc, void *dq, int batch, int n, int head
                        int headdim, dfa_stream_t stream);
 
 /*
+ * dfa_backward without any allocation.  No passage of the pages has a
+ * counterpart: this entry point exists for callers that cannot let a library
+ * allocate device memory -- a framework whose own caching allocator must
+ * account for every byte, or a latency-critical step where an allocation
+ * could block or fail part-way.  Same arguments, results and errors as
+ * dfa_backward, but the float32 scratch (dq accumulator and D) lives in one
+ * fixed 32 MiB array inside the library that every GPU loading the library
+ * holds until the process exits.  The problem must fit it:
+ *   batch * heads * 2n * (headdim + 1) * 4 bytes <= 32 MiB,
+ * otherwise DFA_EINVAL is returned before any work is enqueued.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the one array and it keeps the last call's contents (the dq
+ * accumulator is zeroed at the start of every call): calls whose work
+ * overlaps on the GPU -- on different streams, or from different threads --
+ * race on it and must be serialised by the caller.
+ */
+int dfa_backward_noalloc(const void *q, const void *k, const void *v, const void *out,
+                         const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                         int batch, int n, int heads, int headdim, int block_size,
+                         dfa_stream_t stream);
+
+/*
  * Synchronise `stream`, then return and clear the device status word of the
  * current device: DFA_OK, DFA_ETIMEOUT or DFA_EDEVICE (or DFA_ECUDA if the
  * synchronisation itself failed).

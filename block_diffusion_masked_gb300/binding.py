@@ -34,6 +34,7 @@ _I = ctypes.c_int
 _SIGNATURES = {
     "dfa_version": (_I, []),
     "dfa_error_string": (ctypes.c_char_p, [_I]),
+    "dfa_last_cuda_error": (ctypes.c_char_p, []),
     "dfa_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "dfa_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _I, _P]),
     "dfa_causal_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
@@ -53,6 +54,8 @@ _SIGNATURES = {
 class DfaError(RuntimeError):
     def __init__(self, fn, code):
         msg = lib().dfa_error_string(code).decode()
+        if code == DFA_ECUDA:
+            msg += ": " + lib().dfa_last_cuda_error().decode()
         super().__init__(f"{fn} failed: {msg} ({code})")
         self.code = code
 

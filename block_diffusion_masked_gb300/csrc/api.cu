@@ -23,10 +23,18 @@ struct DeviceState {
   bool ready = false;
   bool supported = false;
   unsigned* status = nullptr;
+  long long l2_bytes = 0;
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+thread_local cudaError_t t_last_error = cudaSuccess;
+
+// Remember a failing CUDA call's code for dfa_last_cuda_error().
+int cuda_fail(cudaError_t e) {
+  t_last_error = e;
+  return DFA_ECUDA;
+}
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // Per-device set-up on first use: check the architecture (the library holds
@@ -43,6 +51,9 @@ int device_state(DeviceState** out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return DFA_ECUDA;
     s.supported = (major == 10 && minor == 3);
+    int l2 = 0;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return DFA_ECUDA;
+    s.l2_bytes = l2;
     if (s.supported) {
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_dfa_status) != cudaSuccess) return DFA_ECUDA;
@@ -120,8 +131,11 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   p.bs = bs < n ? bs : n;
   p.mode = mode;
   p.q_tiles = cdiv(n, ts.fwd_bm);
+  // q, k, v and out of one (batch, head)
+  p.group = l2_group(8LL * 2 * n * d, ds->l2_bytes, B * H);
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
-  return launch_forward(p, d, stream) == cudaSuccess ? DFA_OK : DFA_ECUDA;
+  const cudaError_t e = launch_forward(p, d, stream);
+  return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
 
 bool aligned_all(std::initializer_list<const void*> ps) {
@@ -162,9 +176,12 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   p.bs = bs < n ? bs : n;
   p.mode = mode;
   p.k_tiles = cdiv(n, ts.bwd_bn);
+  // q, k, v, dout (bf16) and the float32 dq accumulator of one (batch, head)
+  p.group = l2_group(12LL * 2 * n * d, ds->l2_bytes, B * H);
   p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
-  return launch_backward(p, d, stream) == cudaSuccess ? DFA_OK : DFA_ECUDA;
+  const cudaError_t e = launch_backward(p, d, stream);
+  return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
 
 int preprocess_impl(const void* out, const void* dout, float* delta, float* dq_acc, int B, int n,
@@ -176,11 +193,11 @@ int preprocess_impl(const void* out, const void* dout, float* delta, float* dq_a
     return DFA_EINVAL;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds))) return rc;
-  return launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(out),
-                               static_cast<const __nv_bfloat16*>(dout), delta, dq_acc, B, 2 * n, H,
-                               d, stream) == cudaSuccess
-             ? DFA_OK
-             : DFA_ECUDA;
+  const cudaError_t e =
+      launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(out),
+                            static_cast<const __nv_bfloat16*>(dout), delta, dq_acc, B, 2 * n, H, d,
+                            stream);
+  return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
 
 int convert_impl(const float* dq_acc, void* dq, int B, int n, int H, int d, cudaStream_t stream) {
@@ -191,9 +208,8 @@ int convert_impl(const float* dq_acc, void* dq, int B, int n, int H, int d, cuda
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds))) return rc;
   const long long elems = static_cast<long long>(B) * 2 * n * H * d;
-  return launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), elems, stream) == cudaSuccess
-             ? DFA_OK
-             : DFA_ECUDA;
+  const cudaError_t e = launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), elems, stream);
+  return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
 
 // Full backward: stream-ordered scratch, then the three steps.
@@ -304,6 +320,8 @@ int dfa_bwd_dq_convert(const float* dq_acc, void* dq, int batch, int n, int head
                        dfa_stream_t stream) {
   return convert_impl(dq_acc, dq, batch, n, heads, headdim, static_cast<cudaStream_t>(stream));
 }
+
+const char* dfa_last_cuda_error(void) { return cudaGetErrorString(t_last_error); }
 
 int dfa_status(dfa_stream_t stream) {
   DeviceState* ds = nullptr;

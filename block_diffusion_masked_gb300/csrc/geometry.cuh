@@ -141,50 +141,70 @@ DFA_HD long long lse_offset(int mode, int b, int h, int half, int r, int H, int 
   return (static_cast<long long>(b) * H + h) * (2LL * n) + static_cast<long long>(half) * n + r;
 }
 
-// Work decoding.  Forward: one work item per (batch, head, half, query tile),
-// longest first: query tiles in decreasing index, both halves of every
-// (batch, head) side by side.  Backward: key tiles; in the diffusion mode the
-// clean key tiles (seen by clean and noisy queries) come first in increasing
-// index, then the noisy key tiles (seen only by their own noisy blocks).
+// Work decoding.  The (batch, head) pairs are cut into groups of `group`
+// heads; a group's work items are handed out together, so the group's
+// tensors stay in L2 while its tiles run ("Fast Diffusion Attention",
+// "Ampere and Ada": L2-aware block order).  Inside a group, the items go
+// longest first ("Hopper": the scheduler hands out tiles longest first).
+// Forward: one item per (batch, head, half, query tile): query tiles in
+// decreasing index, both halves side by side.  Backward: key tiles; in the
+// diffusion mode the clean key tiles (seen by clean and noisy queries) in
+// increasing index, then the noisy key tiles (seen only by their own noisy
+// blocks); in the causal mode key tiles in increasing index, halves side by
+// side.
 struct WorkItem {
   int b, h, half, tile;
 };
 
-DFA_HD WorkItem fwd_work(int w, int mode, int B, int H, int tiles) {
+// Split w into (rank inside its (batch, head), batch-head index) for groups
+// of `group` heads with `per_bh` items each.
+DFA_HD void group_split(int w, int BH, int group, int per_bh, int* rank, int* bh) {
+  const int g = w / (group * per_bh);
+  const int first = g * group;
+  const int gsize = imin(group, BH - first);
+  const int idx = w - first * per_bh;
+  *rank = idx / gsize;
+  *bh = first + idx % gsize;
+}
+
+DFA_HD WorkItem fwd_work(int w, int mode, int B, int H, int tiles, int group) {
   (void)mode;
-  const int per = 2 * B * H;
+  int rank, bh;
+  group_split(w, B * H, group, 2 * tiles, &rank, &bh);
   WorkItem it;
-  it.tile = tiles - 1 - w / per;
-  const int rem = w % per;
-  it.half = rem & 1;
-  const int bh = rem >> 1;
+  it.tile = tiles - 1 - (rank >> 1);
+  it.half = rank & 1;
   it.b = bh / H;
   it.h = bh % H;
   return it;
 }
 
-DFA_HD WorkItem bwd_work(int w, int mode, int B, int H, int tiles) {
-  const int bhn = B * H;
+DFA_HD WorkItem bwd_work(int w, int mode, int B, int H, int tiles, int group) {
+  int rank, bh;
+  group_split(w, B * H, group, 2 * tiles, &rank, &bh);
   WorkItem it;
-  int bh;
   if (mode == MODE_CAUSAL) {
-    it.tile = w / (2 * bhn);
-    const int rem = w % (2 * bhn);
-    it.half = rem & 1;
-    bh = rem >> 1;
-  } else if (w < bhn * tiles) {
+    it.tile = rank >> 1;
+    it.half = rank & 1;
+  } else if (rank < tiles) {
     it.half = HALF_CLEAN;
-    it.tile = w / bhn;
-    bh = w % bhn;
+    it.tile = rank;
   } else {
-    const int w2 = w - bhn * tiles;
     it.half = HALF_NOISY;
-    it.tile = w2 / bhn;
-    bh = w2 % bhn;
+    it.tile = rank - tiles;
   }
   it.b = bh / H;
   it.h = bh % H;
   return it;
+}
+
+// Heads per group: the group's working set (bytes_per_bh each) kept within
+// about half of L2.
+inline int l2_group(long long bytes_per_bh, long long l2_bytes, int BH) {
+  long long g = (l2_bytes / 2) / (bytes_per_bh > 0 ? bytes_per_bh : 1);
+  if (g < 1) g = 1;
+  if (g > BH) g = BH;
+  return static_cast<int>(g);
 }
 
 }  // namespace dfa

@@ -24,6 +24,7 @@ struct FwdParams {
   unsigned* status;
   int B, n, H, bs, mode;
   int q_tiles;       // tiles per half along the queries
+  int group;         // (batch, head) pairs per scheduling group
   float scale_log2;  // softmax scale * log2(e)
 };
 
@@ -40,6 +41,7 @@ struct BwdParams {
   unsigned* status;
   int B, n, H, bs, mode;
   int k_tiles;        // tiles per half along the keys
+  int group;          // (batch, head) pairs per scheduling group
   float scale;        // softmax scale
   float scale_log2;   // scale * log2(e)
 };

@@ -61,6 +61,10 @@ int dfa_version(void);
 /* Human-readable name of a return code (static storage, never NULL). */
 const char *dfa_error_string(int code);
 
+/* Description of the CUDA error behind the calling thread's last DFA_ECUDA
+ * from a kernel launch (static storage, never NULL). */
+const char *dfa_last_cuda_error(void);
+
 /*
  * Forward pass ("Fast Diffusion Attention", "Visit only the visible tiles";
  * "FlashAttention: Exact Attention Without Materialization", sections 4.1-4.2

@@ -336,372 +336,6 @@ __global__ void __launch_bounds__(192, 1) dfa_fwd_kernel(const __grid_constant__
   }
 }
 
-// ---------------------------------------------------------------------------
-// Two softmax warpgroups on one query tile (headdim 64 and 128).
-//
-// Warpgroup w (warps 4w..4w+3) takes the key tiles j with j % 2 == w and
-// keeps its own running maximum, running sum and output accumulator O[w] in
-// TMEM, so the two warpgroups never wait for each other inside the loop.  At
-// the end the two partial states are merged with the rescaling rule of the
-// online softmax ("FlashAttention: Exact Attention Without Materialization",
-// section 4.2), which is exact.  Scores S[w] = Q K^T land in TMEM; the
-// probabilities are written back as bf16 into the same TMEM columns and feed
-// O[w] += P V as the MMA's A operand, so they never touch shared memory.
-// The reference maximum of a row is only moved (and O, sum rescaled) when the
-// tile maximum exceeds it by more than 2^8 -- exact in real arithmetic, and
-// probabilities stay below 256.
-// Warps 0-7 softmax, warp 8 TMA producer, warp 9 MMA issuer.
-template <int D, int STAGES>
-struct Fwd2Cfg {
-  static constexpr int BM = 128;
-  static constexpr int BN = 128;
-  static constexpr int kChunks = D / 64;
-  static constexpr int kQBytes = BM * D * 2;
-  static constexpr int kKVBytes = BN * D * 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + STAGES * kKVBytes;
-  static constexpr int kOffML = kOffV + STAGES * kKVBytes;  // [2][128] x (m, l)
-  static constexpr int kOffBar = kOffML + 2 * BM * 8;
-  enum {
-    BAR_Q = 0,
-    BAR_KFULL = 1,
-    BAR_KEMPTY = BAR_KFULL + STAGES,
-    BAR_VFULL = BAR_KEMPTY + STAGES,
-    BAR_VEMPTY = BAR_VFULL + STAGES,
-    BAR_SFULL = BAR_VEMPTY + STAGES,  // [2]
-    BAR_PFULL = BAR_SFULL + 2,        // [2]
-    BAR_ALL = BAR_PFULL + 2,
-    BAR_XCHG = BAR_ALL + 1,
-    NUM_BARS = BAR_XCHG + 1
-  };
-  static constexpr int kOffTmemSlot = kOffBar + NUM_BARS * 8;
-  static constexpr int kOffAbort = kOffTmemSlot + 4;
-  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
-  static constexpr int kTmemS = 0;       // S[w] at w * BN; P[w] in its first BN / 2 columns
-  static constexpr int kTmemO = 2 * BN;  // O[w] at kTmemO + w * D
-  static constexpr int kTmemCols = 512;
-  static constexpr int kThreads = 320;
-  static constexpr float kRescaleThreshold = 8.0f;  // log2 units
-  static_assert(2 * BN + 2 * D <= kTmemCols, "TMEM budget");
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
-};
-
-template <int D, int STAGES>
-__global__ void __launch_bounds__(320, 1) dfa_fwd2_kernel(const __grid_constant__ FwdParams p) {
-  using C = Fwd2Cfg<D, STAGES>;
-  constexpr int BM = C::BM;
-  constexpr int BN = C::BN;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
-  const AbortFlag ab{abort_flag, p.status};
-#define BAR(i) (sbase + C::kOffBar + 8 * (i))
-
-  const WorkItem wi = fwd_work(blockIdx.x, p.mode, p.B, p.H, p.q_tiles, p.group);
-  Segment seg[2];
-  const int nseg = fwd_segments(p.mode, p.n, p.bs, BM, BN, wi.half, wi.tile, seg);
-  const int n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
-  const int ntiles = n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
-  const int qs = wi.tile * BM;
-
-  if (threadIdx.x == 0) {
-    mbar_init(BAR(C::BAR_Q), 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(BAR(C::BAR_KFULL + s), 1);
-      mbar_init(BAR(C::BAR_KEMPTY + s), 1);
-      mbar_init(BAR(C::BAR_VFULL + s), 1);
-      mbar_init(BAR(C::BAR_VEMPTY + s), 1);
-    }
-    for (int w = 0; w < 2; ++w) {
-      mbar_init(BAR(C::BAR_SFULL + w), 1);
-      mbar_init(BAR(C::BAR_PFULL + w), 128);
-    }
-    mbar_init(BAR(C::BAR_ALL), 1);
-    mbar_init(BAR(C::BAR_XCHG), 256);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 9) {
-    tmem_alloc(sbase + C::kOffTmemSlot, C::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kOffTmemSlot);
-
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(BAR(C::BAR_Q), C::kQBytes);
-#pragma unroll
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_5d(sbase + C::kOffQ + c * BM * 128, &p.tm_q, BAR(C::BAR_Q), 64 * c, wi.h, qs,
-                    wi.half, wi.b);
-      bool ok = true;
-      int j = 0;
-      for (; j < ntiles && ok; ++j) {
-        const int s = j < n0 ? 0 : 1;
-        const int kt = seg[s].t_begin + (s ? j - n0 : j);
-        const int st = j % STAGES;
-        const int round = j / STAGES;
-        if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_KEMPTY + st), (round - 1) & 1, ab))) break;
-        mbar_arrive_expect_tx(BAR(C::BAR_KFULL + st), C::kKVBytes);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
-                      BAR(C::BAR_KFULL + st), 64 * c, wi.h, kt * BN, seg[s].half, wi.b);
-        if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_VEMPTY + st), (round - 1) & 1, ab))) {
-          ++j;  // K of this tile is in flight
-          break;
-        }
-        mbar_arrive_expect_tx(BAR(C::BAR_VFULL + st), C::kKVBytes);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
-                      BAR(C::BAR_VFULL + st), 64 * c, wi.h, kt * BN, seg[s].half, wi.b);
-      }
-      if (!ok) {
-        mbar_wait_limited(BAR(C::BAR_Q), 0, 100000000ull);
-        for (int t = (j > STAGES ? j - STAGES : 0); t < j; ++t) {
-          mbar_wait_limited(BAR(C::BAR_KFULL + t % STAGES), (t / STAGES) & 1, 100000000ull);
-          mbar_wait_limited(BAR(C::BAR_VFULL + t % STAGES), (t / STAGES) & 1, 100000000ull);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(BM, BN, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16(BM, D, false, true);
-      const uint64_t dQ = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
-      const uint64_t dK = sdesc_sw128(sbase + C::kOffK, 16, 1024);
-      const uint64_t dV = sdesc_sw128(sbase + C::kOffV, BN * 128, 1024);
-      auto adv = [](uint64_t d, uint32_t bytes) { return d + static_cast<uint64_t>(bytes >> 4); };
-      bool ok = mbar_wait(BAR(C::BAR_Q), 0, ab);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % STAGES;
-        if (!mbar_wait(BAR(C::BAR_KFULL + st), (j / STAGES) & 1, ab)) return false;
-        tc_fence_after();
-        const int w = j & 1;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kTmemS + w * BN, adv(dQ, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
-                 adv(dK, st * C::kKVBytes + (kk >> 2) * (BN * 128) + (kk & 3) * 32), kIdS,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(BAR(C::BAR_SFULL + w));
-        mma_commit(BAR(C::BAR_KEMPTY + st));
-        return true;
-      };
-      if (ok && ntiles > 0) ok = issue_s(0);
-      if (ok && ntiles > 1) ok = issue_s(1);
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int w = j & 1;
-        const int st = j % STAGES;
-        if (!(ok = mbar_wait(BAR(C::BAR_PFULL + w), (j >> 1) & 1, ab))) break;
-        if (!(ok = mbar_wait(BAR(C::BAR_VFULL + st), (j / STAGES) & 1, ab))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + C::kTmemO + w * D, tmem + C::kTmemS + w * BN + 8 * kk,
-                 adv(dV, st * C::kKVBytes + kk * 16 * 128), kIdPV, (j >= 2 || kk > 0) ? 1u : 0u);
-        mma_commit(BAR(C::BAR_VEMPTY + st));
-        // S of tile j+2 reuses the TMEM columns P of tile j was read from.
-        if (j + 2 < ntiles) ok = issue_s(j + 2);
-      }
-      mma_commit(BAR(C::BAR_ALL));
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ softmax
-    const int w = warp >> 2;
-    const int row = (warp & 3) * 32 + lane;
-    const int r = qs + row;  // row inside the half
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t s_col = t_lane + C::kTmemS + w * BN;
-    const uint32_t o_col = t_lane + C::kTmemO + w * D;
-    const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY;  // reference maximum, scaled log2 units
-    float l_run = 0.f;        // running sum of 2^(s * sl2 - m_ref)
-    bool ok = true;
-    for (int j = w; j < ntiles && ok; j += 2) {
-      const int s = j < n0 ? 0 : 1;
-      const int kt = seg[s].t_begin + (s ? j - n0 : j);
-      if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + w), (j >> 1) & 1, ab))) break;
-      tc_fence_after();
-      const int ks = kt * BN;
-      const bool full = tile_full(seg[s].rule, p.n, p.bs, qs, BM, ks, BN);
-      // Visible keys of this row inside the tile: columns [clo, chi).
-      int clo = 0, chi = BN;
-      if (!full) {
-        const Interval iv = key_interval(seg[s].rule, r, p.n, p.bs);
-        clo = iv.lo - ks;
-        chi = iv.hi - ks;
-      }
-      // Pass 1: row maximum, 64 columns at a time.
-      float mx = -INFINITY;
-#pragma unroll
-      for (int h = 0; h < BN / 64; ++h) {
-        uint32_t sr[64];
-        tmem_ld32(s_col + 64 * h, sr);
-        tmem_ld32(s_col + 64 * h + 32, sr + 32);
-        tmem_wait_ld();
-        tmem_pin<64>(sr);
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int cc = 64 * h + c;
-            if (cc >= clo && cc < chi) mx = fmaxf(mx, __uint_as_float(sr[c]));
-          }
-        }
-      }
-      const float m_tile = mx * sl2;
-      const bool move = m_tile > m_ref + C::kRescaleThreshold;
-      float corr = 1.f;
-      if (move) {
-        corr = ex2_approx(m_ref - m_tile);  // 0 while m_ref = -inf
-        l_run *= corr;
-        m_ref = m_tile;
-      }
-      // O[w] holds the products of this warpgroup's earlier tiles (all
-      // complete: S of this tile was issued after them).
-      if (j >= 2 && __any_sync(0xffffffffu, move)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(o_col + 32 * c, o);
-          tmem_wait_ld();
-          tmem_pin<32>(o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          tmem_st32(o_col + 32 * c, o);
-        }
-      }
-      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-      // Pass 2: probabilities, 32 columns at a time, written back as bf16
-      // pairs into columns [16c, 16c + 16) -- already read by then.
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(s_col + 32 * c, sr);
-        tmem_wait_ld();
-        tmem_pin<32>(sr);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * e]), sl2, -m_use));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -m_use));
-          if (!full) {
-            const int c0 = 32 * c + 2 * e;
-            if (c0 < clo || c0 >= chi) p0 = 0.f;
-            if (c0 + 1 < clo || c0 + 1 >= chi) p1 = 0.f;
-          }
-          rs += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(s_col + 16 * c, pk);
-      }
-      l_run += rs;
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(BAR(C::BAR_PFULL + w));
-    }
-
-    // ------------------------------------------------------------ merge
-    float2* ml = reinterpret_cast<float2*>(smem + C::kOffML);
-    ml[w * BM + row] = make_float2(m_ref, l_run);
-    mbar_arrive(BAR(C::BAR_XCHG));
-    if (ok) ok = mbar_wait_warp(BAR(C::BAR_ALL), 0, ab);
-    if (ok) ok = mbar_wait_warp(BAR(C::BAR_XCHG), 0, ab);
-    tc_fence_after();
-    if (ok) {
-      const float2 a = ml[row];       // warpgroup 0
-      const float2 b = ml[BM + row];  // warpgroup 1
-      const float m = fmaxf(a.x, b.x);
-      const float fa = a.y > 0.f ? ex2_approx(a.x - m) : 0.f;
-      const float fb = b.y > 0.f ? ex2_approx(b.y > 0.f ? b.x - m : 0.f) : 0.f;
-      const float lsum = a.y * fa + b.y * fb;
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      const size_t L = 2 * static_cast<size_t>(p.n);
-      const size_t pos = static_cast<size_t>(wi.half) * p.n + r;
-      const bool valid = r < p.n;
-      __nv_bfloat16* orow = p.out + ((wi.b * L + pos) * p.H + wi.h) * D;
-      // warpgroup w writes head dims [w * D / 2, (w + 1) * D / 2)
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = w * (D / 2) + 32 * c;
-        uint32_t oa[32], ob[32];
-        tmem_ld32(t_lane + C::kTmemO + col, oa);
-        tmem_ld32(t_lane + C::kTmemO + D + col, ob);
-        tmem_wait_ld();
-        tmem_pin<32>(oa);
-        tmem_pin<32>(ob);
-        if (valid) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t wv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float v2[2];
-#pragma unroll
-              for (int h2 = 0; h2 < 2; ++h2) {
-                const int k = g * 8 + 2 * e + h2;
-                const float x = (fa > 0.f ? __uint_as_float(oa[k]) * fa : 0.f) +
-                                (fb > 0.f ? __uint_as_float(ob[k]) * fb : 0.f);
-                v2[h2] = x * inv;
-              }
-              wv[e] = pack_bf16x2(v2[0], v2[1]);
-            }
-            st_global_v4(orow + col + 8 * g, wv[0], wv[1], wv[2], wv[3]);
-          }
-        }
-      }
-      if (valid && w == 0) {
-        const float lse = lsum > 0.f ? (m + lg2_approx(lsum)) * 0.69314718055994531f : -INFINITY;
-        p.lse[lse_offset(p.mode, wi.b, wi.h, wi.half, r, p.H, p.n)] = lse;
-      }
-    }
-  }
-#undef BAR
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 9) {
-    if (lane == 0)
-      mbar_wait_limited(sbase + C::kOffBar + 8 * C::BAR_ALL, 0, 1000000000ull);
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
-  }
-}
-
-template <int D, int STAGES>
-static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
-  using C = Fwd2Cfg<D, STAGES>;
-  auto kern = dfa_fwd2_kernel<D, STAGES>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  const long long blocks = 2LL * p.B * p.H * p.q_tiles;
-  if (blocks <= 0) return cudaSuccess;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
-}
-
 template <int D, int BN, int STAGES>
 static cudaError_t launch_fwd_impl(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D, BN, STAGES>;
@@ -718,8 +352,8 @@ static cudaError_t launch_fwd_impl(const FwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream) {
   switch (headdim) {
-    case 64: return launch_fwd2_impl<64, 3>(p, stream);
-    case 128: return launch_fwd2_impl<128, 2>(p, stream);
+    case 64:
+    case 128: return launch_forward_two_warpgroups(p, headdim, stream);
     case 256: return launch_fwd_impl<256, 64, 2>(p, stream);
     default: return cudaErrorInvalidValue;
   }

@@ -1,0 +1,445 @@
+// Persistent forward kernel of block-diffusion attention (headdim 64, 128).
+//
+// One CTA per SM walks a strided list of work items, one item being one
+// 128-row query tile of one half of one (batch, head) (items ordered longest
+// first inside groups of heads that share L2).  For its item it visits
+// exactly the key tiles the mask reaches ("Fast Diffusion Attention", "Visit
+// only the visible tiles") and runs the loop of "FlashAttention: Exact
+// Attention Without Materialization", section 5.1, with the online softmax of
+// section 4.2.
+//
+// Two softmax warpgroups share the query tile: warpgroup w takes the key tiles
+// j with j % 2 == w and keeps its own running maximum, running sum and output
+// accumulator O[w] in TMEM, so the warpgroups never wait for each other
+// inside the loop; at the end of the item the two partial states are merged
+// with the online-softmax rescaling rule (exact).  Scores S[w] = Q K^T land in
+// TMEM; probabilities are written back as bf16 into the same TMEM columns and
+// feed O[w] += P V as the MMA's A operand.  A row's reference maximum is only
+// moved (O and the sum rescaled) when a tile maximum exceeds it by more than
+// 2^8: exact in real arithmetic, and probabilities stay below 256.
+//
+// The K/V ring, the query double buffer and all barrier phases run on across
+// items, so the loads and S products of the next item overlap the merge and
+// stores of the current one.
+// Warps 0-7 softmax, warp 8 TMA producer, warp 9 MMA issuer, warps 10-11
+// idle.  The producer/MMA warpgroup hands registers to the softmax
+// warpgroups (setmaxnreg): launched with 168 per thread, it drops to 56 and
+// the softmax warpgroups rise to 224, which keeps a row's 128 scores in
+// registers.  256 * (224 - 168) == 128 * (168 - 56): the pool balances.
+#include <cuda_bf16.h>
+
+#include "geometry.cuh"
+#include "params.cuh"
+#include "sm100.cuh"
+
+namespace dfa {
+
+template <int D, int STAGES>
+struct Fwd2Cfg {
+  static constexpr int BM = 128;
+  static constexpr int BN = 128;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int kOffQ = 0;  // 2 buffers
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;
+  static constexpr int kOffV = kOffK + STAGES * kKVBytes;
+  static constexpr int kOffML = kOffV + STAGES * kKVBytes;  // [item % 2][warpgroup][row] (m, l)
+  static constexpr int kOffBar = kOffML + 2 * 2 * BM * 8;
+  enum {
+    BAR_QFULL = 0,                    // [2]
+    BAR_QEMPTY = BAR_QFULL + 2,       // [2]
+    BAR_KFULL = BAR_QEMPTY + 2,       // [STAGES]
+    BAR_KEMPTY = BAR_KFULL + STAGES,  // [STAGES]
+    BAR_VFULL = BAR_KEMPTY + STAGES,  // [STAGES]
+    BAR_VEMPTY = BAR_VFULL + STAGES,  // [STAGES]
+    BAR_SFULL = BAR_VEMPTY + STAGES,  // [2] per warpgroup
+    BAR_PFULL = BAR_SFULL + 2,        // [2] per warpgroup
+    BAR_ITEMDONE = BAR_PFULL + 2,     // every product of an item complete
+    BAR_OFREE = BAR_ITEMDONE + 1,     // both O accumulators read out
+    BAR_XCHG = BAR_OFREE + 1,         // both warpgroups' (m, l) in shared memory
+    BAR_ALL = BAR_XCHG + 1,           // every MMA of the CTA complete
+    NUM_BARS = BAR_ALL + 1
+  };
+  static constexpr int kOffTmemSlot = kOffBar + NUM_BARS * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
+  static constexpr int kTmemS = 0;       // S[w] at w * BN; P[w] in its first BN / 2 columns
+  static constexpr int kTmemO = 2 * BN;  // O[w] at kTmemO + w * D
+  static constexpr int kTmemCols = 512;
+  static constexpr int kThreads = 384;
+  static constexpr float kRescaleThreshold = 8.0f;  // log2 units
+  static_assert(2 * BN + 2 * D <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct ItemGeom {
+  WorkItem wi;
+  Segment seg[2];
+  int n0, ntiles, qs;
+};
+
+__device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, int bn,
+                                          ItemGeom* g) {
+  g->wi = fwd_work(item, p.mode, p.B, p.H, p.q_tiles, p.group);
+  const int nseg = fwd_segments(p.mode, p.n, p.bs, bm, bn, g->wi.half, g->wi.tile, g->seg);
+  g->n0 = nseg > 0 ? g->seg[0].t_end - g->seg[0].t_begin : 0;
+  g->ntiles = g->n0 + (nseg > 1 ? g->seg[1].t_end - g->seg[1].t_begin : 0);
+  g->qs = g->wi.tile * bm;
+}
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant__ FwdParams p) {
+  using C = Fwd2Cfg<D, STAGES>;
+  constexpr int BM = C::BM;
+  constexpr int BN = C::BN;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  const AbortFlag ab{abort_flag, p.status};
+  const int num_items = 2 * p.B * p.H * p.q_tiles;
+#define BAR(i) (sbase + C::kOffBar + 8 * (i))
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(BAR(C::BAR_QFULL + b), 1);
+      mbar_init(BAR(C::BAR_QEMPTY + b), 1);
+      mbar_init(BAR(C::BAR_SFULL + b), 1);
+      mbar_init(BAR(C::BAR_PFULL + b), 128);
+    }
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(BAR(C::BAR_KFULL + s), 1);
+      mbar_init(BAR(C::BAR_KEMPTY + s), 1);
+      mbar_init(BAR(C::BAR_VFULL + s), 1);
+      mbar_init(BAR(C::BAR_VEMPTY + s), 1);
+    }
+    mbar_init(BAR(C::BAR_ITEMDONE), 1);
+    mbar_init(BAR(C::BAR_OFREE), 256);
+    mbar_init(BAR(C::BAR_XCHG), 256);
+    mbar_init(BAR(C::BAR_ALL), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(sbase + C::kOffTmemSlot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kOffTmemSlot);
+
+  if (warp >= 8) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+   if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      bool ok = true;
+      int g = 0;  // K/V ring position across items
+      int k = 0;
+      for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x, ++k) {
+        ItemGeom ig;
+        item_geom(p, item, BM, BN, &ig);
+        const int qb = k & 1;
+        if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_QEMPTY + qb), ((k >> 1) - 1) & 1, ab))) break;
+        mbar_arrive_expect_tx(BAR(C::BAR_QFULL + qb), C::kQBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, &p.tm_q,
+                      BAR(C::BAR_QFULL + qb), 64 * c, ig.wi.h, ig.qs, ig.wi.half, ig.wi.b);
+        for (int j = 0; j < ig.ntiles; ++j, ++g) {
+          const int s = j < ig.n0 ? 0 : 1;
+          const int kt = ig.seg[s].t_begin + (s ? j - ig.n0 : j);
+          const int st = g % STAGES;
+          const int round = g / STAGES;
+          if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_KEMPTY + st), (round - 1) & 1, ab))) break;
+          mbar_arrive_expect_tx(BAR(C::BAR_KFULL + st), C::kKVBytes);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
+                        BAR(C::BAR_KFULL + st), 64 * c, ig.wi.h, kt * BN, ig.seg[s].half, ig.wi.b);
+          if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_VEMPTY + st), (round - 1) & 1, ab))) break;
+          mbar_arrive_expect_tx(BAR(C::BAR_VFULL + st), C::kKVBytes);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
+                        BAR(C::BAR_VFULL + st), 64 * c, ig.wi.h, kt * BN, ig.seg[s].half, ig.wi.b);
+        }
+      }
+      if (!ok) {
+        // Unwinding: give the copies already issued time to land.
+        const unsigned long long t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 20000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+   } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(BM, BN, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(BM, D, false, true);
+      const uint64_t dQ = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
+      const uint64_t dK = sdesc_sw128(sbase + C::kOffK, 16, 1024);
+      const uint64_t dV = sdesc_sw128(sbase + C::kOffV, BN * 128, 1024);
+      auto adv = [](uint64_t d, uint32_t bytes) { return d + static_cast<uint64_t>(bytes >> 4); };
+      bool ok = true;
+      int g = 0;                // K/V ring position
+      int cnt[2] = {0, 0};      // tiles handed to each warpgroup so far
+      int k = 0;
+      for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x, ++k) {
+        ItemGeom ig;
+        item_geom(p, item, BM, BN, &ig);
+        const int qb = k & 1;
+        if (!(ok = mbar_wait(BAR(C::BAR_QFULL + qb), (k >> 1) & 1, ab))) break;
+        tc_fence_after();
+        const int g0 = g;
+        auto issue_s = [&](int j) -> bool {
+          const int gg = g0 + j;
+          const int st = gg % STAGES;
+          if (!mbar_wait(BAR(C::BAR_KFULL + st), (gg / STAGES) & 1, ab)) return false;
+          tc_fence_after();
+          const int w = j & 1;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::kTmemS + w * BN,
+                   adv(dQ, qb * C::kQBytes + (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                   adv(dK, st * C::kKVBytes + (kk >> 2) * (BN * 128) + (kk & 3) * 32), kIdS,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(BAR(C::BAR_SFULL + w));
+          mma_commit(BAR(C::BAR_KEMPTY + st));
+          return true;
+        };
+        if (ig.ntiles > 0 && !(ok = issue_s(0))) break;
+        if (ig.ntiles > 1 && !(ok = issue_s(1))) break;
+        // The O accumulators still hold the previous item until it is read out.
+        if (k >= 1 && !(ok = mbar_wait(BAR(C::BAR_OFREE), (k - 1) & 1, ab))) break;
+        tc_fence_after();
+        for (int j = 0; j < ig.ntiles && ok; ++j) {
+          const int w = j & 1;
+          const int c = cnt[w] + (j >> 1);
+          const int gg = g0 + j;
+          const int st = gg % STAGES;
+          if (!(ok = mbar_wait(BAR(C::BAR_PFULL + w), c & 1, ab))) break;
+          if (!(ok = mbar_wait(BAR(C::BAR_VFULL + st), (gg / STAGES) & 1, ab))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + C::kTmemO + w * D, tmem + C::kTmemS + w * BN + 8 * kk,
+                   adv(dV, st * C::kKVBytes + kk * 16 * 128), kIdPV, (j >= 2 || kk > 0) ? 1u : 0u);
+          mma_commit(BAR(C::BAR_VEMPTY + st));
+          // S of tile j+2 reuses the TMEM columns P of tile j was read from.
+          if (j + 2 < ig.ntiles) ok = issue_s(j + 2);
+        }
+        if (!ok) break;
+        mma_commit(BAR(C::BAR_QEMPTY + qb));
+        mma_commit(BAR(C::BAR_ITEMDONE));
+        g += ig.ntiles;
+        cnt[0] += (ig.ntiles + 1) >> 1;
+        cnt[1] += ig.ntiles >> 1;
+      }
+      mma_commit(BAR(C::BAR_ALL));
+    }
+    __syncwarp();
+   }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    // ------------------------------------------------------------ softmax
+    const int w = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_col = t_lane + C::kTmemS + w * BN;
+    const uint32_t o_col = t_lane + C::kTmemO + w * D;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    int cnt = 0;  // tiles this warpgroup has processed so far
+    int k = 0;
+    for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x, ++k) {
+      ItemGeom ig;
+      item_geom(p, item, BM, BN, &ig);
+      const int qs = ig.qs;
+      const int r = qs + row;  // row inside the half
+      float m_ref = -INFINITY;  // reference maximum, scaled log2 units
+      float l_run = 0.f;        // running sum of 2^(s * sl2 - m_ref)
+      for (int j = w; j < ig.ntiles; j += 2, ++cnt) {
+        const int s = j < ig.n0 ? 0 : 1;
+        const int kt = ig.seg[s].t_begin + (s ? j - ig.n0 : j);
+        if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + w), cnt & 1, ab))) break;
+        tc_fence_after();
+        const int ks = kt * BN;
+        const bool full = tile_full(ig.seg[s].rule, p.n, p.bs, qs, BM, ks, BN);
+        // The tile's score row in registers; hidden keys -> -inf, so they
+        // drop out of the maximum and get probability 0.
+        uint32_t sr[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_col + 32 * c, sr + 32 * c);
+        tmem_wait_ld();
+        tmem_pin<BN>(sr);
+        if (!full) {
+          const Interval iv = key_interval(ig.seg[s].rule, r, p.n, p.bs);
+          const int clo = iv.lo - ks, chi = iv.hi - ks;
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c < clo || c >= chi) sr[c] = __float_as_uint(-INFINITY);
+        }
+        const float m_tile = max_tree<BN>(sr) * sl2;
+        const bool move = m_tile > m_ref + C::kRescaleThreshold;
+        float corr = 1.f;
+        if (move) {
+          corr = ex2_approx(m_ref - m_tile);  // 0 while m_ref = -inf
+          l_run *= corr;
+          m_ref = m_tile;
+        }
+        // O[w] holds this warpgroup's earlier products of the item (complete:
+        // S of this tile was issued after them).
+        if (j >= 2 && __any_sync(0xffffffffu, move)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_col + 32 * c, o);
+            tmem_wait_ld();
+            tmem_pin<32>(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st32(o_col + 32 * c, o);
+          }
+        }
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        // Probabilities 2^(s * sl2 - m_use), two lanes per instruction for
+        // the scaling and the sums (four independent pair accumulators),
+        // written back as bf16 pairs into columns [16c, 16c + 16) -- the
+        // scores there are already in registers.
+        const uint64_t scale2 = f2_pack(sl2, sl2);
+        const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[32 * c + 2 * e]),
+                                              __uint_as_float(sr[32 * c + 2 * e + 1])),
+                                      scale2, neg_m2);
+            float x0, x1;
+            f2_unpack(x, x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(s_col + 16 * c, pk);
+        }
+        float a0, a1, b0, b1, c0, c1, d0, d1;
+        f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+        f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+        (void)c0; (void)c1; (void)d0; (void)d1;
+        l_run += (a0 + a1) + (b0 + b1);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(BAR(C::BAR_PFULL + w));
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- merge
+      float2* ml = reinterpret_cast<float2*>(smem + C::kOffML) + (k & 1) * 2 * BM;
+      ml[w * BM + row] = make_float2(m_ref, l_run);
+      mbar_arrive(BAR(C::BAR_XCHG));
+      if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMDONE), k & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(BAR(C::BAR_XCHG), k & 1, ab))) break;
+      tc_fence_after();
+      const float2 a = ml[row];       // warpgroup 0
+      const float2 b = ml[BM + row];  // warpgroup 1
+      const float m = fmaxf(a.x, b.x);
+      const float fa = a.y > 0.f ? ex2_approx(a.x - m) : 0.f;
+      const float fb = b.y > 0.f ? ex2_approx(b.x - m) : 0.f;
+      const float lsum = a.y * fa + b.y * fb;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const size_t L = 2 * static_cast<size_t>(p.n);
+      const size_t pos = static_cast<size_t>(ig.wi.half) * p.n + r;
+      const bool valid = r < p.n;
+      __nv_bfloat16* orow = p.out + ((ig.wi.b * L + pos) * p.H + ig.wi.h) * D;
+      // warpgroup w writes head dims [w * D / 2, (w + 1) * D / 2)
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = w * (D / 2) + 32 * c;
+        uint32_t oa[32], ob[32];
+        tmem_ld32(t_lane + C::kTmemO + col, oa);
+        tmem_ld32(t_lane + C::kTmemO + D + col, ob);
+        tmem_wait_ld();
+        tmem_pin<32>(oa);
+        tmem_pin<32>(ob);
+        if (valid) {
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float v2[2];
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const int kk = gq * 8 + 2 * e + h2;
+                const float x = (fa > 0.f ? __uint_as_float(oa[kk]) * fa : 0.f) +
+                                (fb > 0.f ? __uint_as_float(ob[kk]) * fb : 0.f);
+                v2[h2] = x * inv;
+              }
+              wv[e] = pack_bf16x2(v2[0], v2[1]);
+            }
+            st_global_v4(orow + col + 8 * gq, wv[0], wv[1], wv[2], wv[3]);
+          }
+        }
+      }
+      if (valid && w == 0) {
+        const float lse = lsum > 0.f ? (m + lg2_approx(lsum)) * 0.69314718055994531f : -INFINITY;
+        p.lse[lse_offset(p.mode, ig.wi.b, ig.wi.h, ig.wi.half, r, p.H, p.n)] = lse;
+      }
+      tc_fence_before();
+      mbar_arrive(BAR(C::BAR_OFREE));
+    }
+  }
+#undef BAR
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    if (lane == 0) mbar_wait_limited(sbase + C::kOffBar + 8 * C::BAR_ALL, 0, 1000000000ull);
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int STAGES>
+static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
+  using C = Fwd2Cfg<D, STAGES>;
+  auto kern = dfa_fwd2_kernel<D, STAGES>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long items = 2LL * p.B * p.H * p.q_tiles;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const long long grid = items < sms ? items : sms;
+  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_forward_two_warpgroups(const FwdParams& p, int headdim, cudaStream_t stream) {
+  switch (headdim) {
+    case 64: return launch_fwd2_impl<64, 4>(p, stream);
+    case 128: return launch_fwd2_impl<128, 2>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dfa

@@ -48,6 +48,7 @@ struct BwdParams {
 
 // Launchers (one per translation unit).  Return a cudaError_t.
 cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream);
+cudaError_t launch_forward_two_warpgroups(const FwdParams& p, int headdim, cudaStream_t stream);
 cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* out, const __nv_bfloat16* dout,
                                   float* delta, float* dq_acc, int B, int L, int H, int d,

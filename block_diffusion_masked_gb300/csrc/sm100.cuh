@@ -290,6 +290,55 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pair arithmetic: two fp32 lanes per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Maximum of n values with a tree of three-input maxima.
+template <int N>
+__device__ __forceinline__ float max_tree(const uint32_t* v) {
+  float m[(N + 2) / 3];
+  constexpr int M = (N + 2) / 3;
+#pragma unroll
+  for (int i = 0; i < M; ++i) {
+    const float a = __uint_as_float(v[3 * i]);
+    const float b = 3 * i + 1 < N ? __uint_as_float(v[3 * i + 1]) : a;
+    const float c = 3 * i + 2 < N ? __uint_as_float(v[3 * i + 2]) : a;
+    m[i] = fmax3(a, b, c);
+  }
+  if constexpr (M == 1) {
+    return m[0];
+  } else {
+    uint32_t u[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) u[i] = __float_as_uint(m[i]);
+    return max_tree<M>(u);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

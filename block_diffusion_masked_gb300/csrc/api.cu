@@ -150,7 +150,6 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
                   int n, int H, int d, int bs, cudaStream_t stream) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
-  if (d == 256) return DFA_EUNSUPPORTED;
   if (B == 0) return DFA_OK;
   if (!aligned_all({q, k, v, dout, dq_acc, dk, dv}) || !lse || !delta ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(delta) & 3u))
@@ -218,7 +217,6 @@ int backward_impl(int mode, const void* q, const void* k, const void* v, const v
                   int H, int d, int bs, cudaStream_t stream) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
-  if (d == 256) return DFA_EUNSUPPORTED;
   if (B == 0) return DFA_OK;
   if (!aligned_all({q, k, v, out, dout, dq, dk, dv}) || !lse ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))

@@ -19,11 +19,14 @@
 //   dV  += P^T dO,  dK += dS^T Q    (A operand read from TMEM)
 //   dQ   = dS K                     -> TMEM S[b] (S is consumed by then),
 //        then added to a float32 accumulator in device memory.
-// Warp roles (320 threads): two compute warpgroups, warpgroup b handling the
+// Warp roles (384 threads): two compute warpgroups, warpgroup b handling the
 // query tiles i with i % 2 == b (thread t of a warpgroup owns key row t of
 // the tile, TMEM lane t), so that the MMAs of one tile overlap the
 // softmax-gradient work of the other; warp 8 loads (TMA for Q/dO, plain loads
-// for LSE/D); warp 9 issues the MMAs.
+// for LSE/D); warp 9 issues the MMAs; warps 10-11 idle.  The load/MMA
+// warpgroup drops to 72 registers and the compute warpgroups rise to 216
+// (setmaxnreg; launched with 168: 256 * 48 == 128 * 96), so a 64-query
+// slice of S^T and dP^T is read from TMEM in one batch.
 #include <cuda_bf16.h>
 
 #include "geometry.cuh"
@@ -76,7 +79,7 @@ struct BwdCfg {
   static constexpr int kTmemDV = kTmemDK + D;
   static constexpr int kDqCols = kDqTransposed ? BMQ : D;
   static constexpr int kTmemCols = 512;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 384;
   static constexpr int kProducerWarp = 8;
   static constexpr int kMmaWarp = 9;
   static_assert(kTmemDV + D <= kTmemCols, "TMEM budget");
@@ -87,7 +90,7 @@ struct BwdCfg {
 };
 
 template <int D, int BMQ>
-__global__ void __launch_bounds__(320, 1) dfa_bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D, BMQ>;
   constexpr int BN = C::BN;
   constexpr int STAGES = C::STAGES;
@@ -136,7 +139,9 @@ __global__ void __launch_bounds__(320, 1) dfa_bwd_kernel(const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kOffTmemSlot);
 
-  if (warp == C::kProducerWarp) {
+  if (warp >= 8) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
+   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ loads
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
@@ -166,10 +171,12 @@ __global__ void __launch_bounds__(320, 1) dfa_bwd_kernel(const __grid_constant__
         const int q = qt * BMQ + lane + 32 * e;
         const bool valid = q < p.n;
         const size_t pos = static_cast<size_t>(seg[s].half) * p.n + q;
+        // Stored negated: -LSE * log2(e) and -D, the addends of the packed
+        // arithmetic below.  Rows past the half: probability 0.
         lse_r[e] = valid ? p.lse[lse_offset(p.mode, wi.b, wi.h, seg[s].half, q, p.H, p.n)] *
-                               1.4426950408889634f
-                         : INFINITY;
-        del_r[e] = valid ? del_bh[pos] : 0.f;
+                               -1.4426950408889634f
+                         : -INFINITY;
+        del_r[e] = valid ? -del_bh[pos] : 0.f;
       }
     };
     if (ntiles > 0) load_rows(0);
@@ -213,7 +220,7 @@ __global__ void __launch_bounds__(320, 1) dfa_bwd_kernel(const __grid_constant__
         mbar_wait_limited(BAR(C::BAR_QFULL + t % STAGES), (t / STAGES) & 1, 100000000ull);
     }
     __syncwarp();
-  } else if (warp == C::kMmaWarp) {
+   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(BN, BMQ, false, false);      // K Q^T, V dO^T
@@ -308,7 +315,9 @@ __global__ void __launch_bounds__(320, 1) dfa_bwd_kernel(const __grid_constant__
       mma_commit(BAR(C::BAR_ALL));
     }
     __syncwarp();
+   }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
     // ------------------------------------------------------------ compute
     const int wg = warp >> 2;            // this warpgroup handles tiles i % 2 == wg
     const int row = (warp & 3) * 32 + lane;  // key row of the tile / TMEM lane
@@ -377,51 +386,61 @@ __global__ void __launch_bounds__(320, 1) dfa_bwd_kernel(const __grid_constant__
       return true;
     };
 
-    // P^T and dS^T of one 32-query chunk: S^T / dP^T in, bf16 P^T / dS^T back
-    // into the same 32 dP columns (P^T in the first 16, dS^T in the last 16)
-    // and dS^T into the swizzled shared tile.
-    auto chunk = [&](auto masked, int cc, uint32_t s_col, uint32_t dp_col, uint32_t ds_s,
-                     const float* lse_s, const float* del_s, int qs, Interval iv) {
-      uint32_t sr[32], dpr[32];
-      tmem_ld32(s_col + 32 * cc, sr);
-      tmem_ld32(dp_col + 32 * cc, dpr);
-      float lv[32], dl[32];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float4 a = reinterpret_cast<const float4*>(lse_s + 32 * cc)[e];
-        const float4 d = reinterpret_cast<const float4*>(del_s + 32 * cc)[e];
-        lv[4 * e] = a.x; lv[4 * e + 1] = a.y; lv[4 * e + 2] = a.z; lv[4 * e + 3] = a.w;
-        dl[4 * e] = d.x; dl[4 * e + 1] = d.y; dl[4 * e + 2] = d.z; dl[4 * e + 3] = d.w;
-      }
+    // P^T and dS^T of one 64-query slice h: S^T and dP^T in (one batch of
+    // TMEM loads), bf16 P^T / dS^T back into the dP columns of each 32-query
+    // chunk (P^T in its first 16 columns, dS^T in its last 16), dS^T also into
+    // the swizzled shared tile.  Pairs of columns go through packed f32x2
+    // arithmetic: x = s * sl2 - lse2, p = 2^x, ds = p * (dp - D).
+    auto slice = [&](auto masked, int h, uint32_t s_col, uint32_t dp_col, uint32_t ds_s,
+                     const float* nlse_s, const float* ndel_s, int qs, Interval iv) {
+      uint32_t sr[64], dpr[64];
+      tmem_ld32(s_col + 64 * h, sr);
+      tmem_ld32(s_col + 64 * h + 32, sr + 32);
+      tmem_ld32(dp_col + 64 * h, dpr);
+      tmem_ld32(dp_col + 64 * h + 32, dpr + 32);
       tmem_wait_ld();
-      tmem_pin<32>(sr);
-      tmem_pin<32>(dpr);
-      uint32_t wp[16], wd[16];
+      tmem_pin<64>(sr);
+      tmem_pin<64>(dpr);
+      const uint64_t scale2 = f2_pack(sl2, sl2);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        float pv[2], dv[2];
+      for (int cc = 0; cc < 2; ++cc) {
+        const int cbase = 64 * h + 32 * cc;  // first query column of the chunk
+        uint32_t wp[16], wd[16];
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int cl = 2 * e + h2;
-          float pr = ex2_approx(fmaf(__uint_as_float(sr[cl]), sl2, -lv[cl]));
+        for (int e = 0; e < 16; ++e) {
+          const int cl = 32 * cc + 2 * e;  // column inside the slice
+          const float2 nl = *reinterpret_cast<const float2*>(nlse_s + cbase + 2 * e);
+          const float2 nd = *reinterpret_cast<const float2*>(ndel_s + cbase + 2 * e);
+          const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[cl]), __uint_as_float(sr[cl + 1])),
+                                    scale2, f2_pack(nl.x, nl.y));
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          float p0 = ex2_approx(x0);
+          float p1 = ex2_approx(x1);
           if (decltype(masked)::value) {
-            const int q = qs + 32 * cc + cl;
-            if (q < iv.lo || q >= iv.hi) pr = 0.f;
+            const int q = qs + cbase + 2 * e;
+            if (q < iv.lo || q >= iv.hi) p0 = 0.f;
+            if (q + 1 < iv.lo || q + 1 >= iv.hi) p1 = 0.f;
           }
-          pv[h2] = pr;
-          dv[h2] = pr * (__uint_as_float(dpr[cl]) - dl[cl]);
+          const uint64_t pp = f2_pack(p0, p1);
+          const uint64_t dd =
+              f2_add(f2_pack(__uint_as_float(dpr[cl]), __uint_as_float(dpr[cl + 1])),
+                     f2_pack(nd.x, nd.y));
+          float d0, d1;
+          f2_unpack(f2_mul(pp, dd), d0, d1);
+          wp[e] = pack_bf16x2(p0, p1);
+          wd[e] = pack_bf16x2(d0, d1);
         }
-        wp[e] = pack_bf16x2(pv[0], pv[1]);
-        wd[e] = pack_bf16x2(dv[0], dv[1]);
-      }
-      tmem_st16(dp_col + 32 * cc, wp);
-      tmem_st16(dp_col + 32 * cc + 16, wd);
-      const int a = cc >> 1;  // 64-column swizzle atom
+        const int chunk = 2 * h + cc;
+        tmem_st16(dp_col + 32 * chunk, wp);
+        tmem_st16(dp_col + 32 * chunk + 16, wd);
+        const int a = chunk >> 1;  // 64-column swizzle atom
 #pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4) {
-        const int u = (cc & 1) * 4 + u4;  // 16-byte unit inside the row
-        const uint32_t off = a * (BN * 128) + row * 128 + ((u ^ (row & 7)) << 4);
-        st_shared_v4(ds_s + off, wd[4 * u4], wd[4 * u4 + 1], wd[4 * u4 + 2], wd[4 * u4 + 3]);
+        for (int u4 = 0; u4 < 4; ++u4) {
+          const int u = (chunk & 1) * 4 + u4;  // 16-byte unit inside the row
+          const uint32_t off = a * (BN * 128) + row * 128 + ((u ^ (row & 7)) << 4);
+          st_shared_v4(ds_s + off, wd[4 * u4], wd[4 * u4 + 1], wd[4 * u4 + 2], wd[4 * u4 + 3]);
+        }
       }
     };
 
@@ -445,12 +464,12 @@ __global__ void __launch_bounds__(320, 1) dfa_bwd_kernel(const __grid_constant__
       const uint32_t ds_s = sbase + C::kOffDS + b * C::kDSBytes;
       if (full) {
 #pragma unroll 1
-        for (int cc = 0; cc < BMQ / 32; ++cc)
-          chunk(std::false_type{}, cc, s_col, dp_col, ds_s, lse_s, del_s, qs, iv);
+        for (int h = 0; h < BMQ / 64; ++h)
+          slice(std::false_type{}, h, s_col, dp_col, ds_s, lse_s, del_s, qs, iv);
       } else {
 #pragma unroll 1
-        for (int cc = 0; cc < BMQ / 32; ++cc)
-          chunk(std::true_type{}, cc, s_col, dp_col, ds_s, lse_s, del_s, qs, iv);
+        for (int h = 0; h < BMQ / 64; ++h)
+          slice(std::true_type{}, h, s_col, dp_col, ds_s, lse_s, del_s, qs, iv);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -526,7 +545,8 @@ static cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
 cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream) {
   switch (headdim) {
     case 64: return launch_bwd_impl<64, 128>(p, stream);
-    case 128: return launch_bwd_impl<128, 64>(p, stream);
+    case 128: return launch_backward_d128(p, stream);
+    case 256: return launch_backward_d256(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

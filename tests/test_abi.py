@@ -66,6 +66,7 @@ def test_host_side_argument_checks(lib):
     assert lib.dfa_forward(ctypes.c_void_p(0x1008), p, p, p, p, 1, 64, 2, 64, 4, s) == b.DFA_EINVAL
     assert lib.dfa_backward(p, p, p, p, p, p, p, p, null, 1, 64, 2, 64, 4, s) == b.DFA_EINVAL
     assert lib.dfa_backward(p, p, p, p, p, p, p, p, p, 1, 64, 2, 80, 4, s) == b.DFA_EUNSUPPORTED
+    assert lib.dfa_backward(p, p, p, p, p, p, p, p, p, 1, 64, 2, 96, 4, s) == b.DFA_EUNSUPPORTED
     assert lib.dfa_causal_forward(p, p, p, p, p, 3, 64, 2, 64, s) == b.DFA_EINVAL  # odd batch
     # an empty batch is a no-op
     assert lib.dfa_forward(p, p, p, p, p, 0, 64, 2, 64, 4, s) == b.DFA_OK

@@ -115,10 +115,10 @@ def test_edge_cases(b, B, n, H, d, bs):
 
 
 @pytest.mark.parametrize("n,bs", [(67, 3), (256, 64), (300, 1)])
-def test_headdim_256_forward(b, n, bs):
+def test_headdim_256(b, n, bs):
     q, k, v, do = inputs.make_inputs(1, n, 2, 256, seed=7 + n)
-    res = _run_gpu(b, q, k, v, do, bs, backward=False)
-    _check(res, q, k, v, do, bs, backward=False)
+    res = _run_gpu(b, q, k, v, do, bs)
+    _check(res, q, k, v, do, bs)
 
 
 def test_causal_yardstick(b):
@@ -173,8 +173,8 @@ def test_full_size_workloads_sampled(b, name, heads):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["hd256_bs1", "hd256_bs64", "hd256_bs128"])
-def test_full_size_headdim_256_forward_sampled(b, name):
+def test_full_size_headdim_256_sampled(b, name):
     w = inputs.WORKLOADS[name]
     q, k, v, do = inputs.make_workload_inputs(w)
-    res = _run_gpu(b, q, k, v, do, w.block_size, backward=False)
-    _check(res, q, k, v, do, w.block_size, heads=[(1, 7)], backward=False)
+    res = _run_gpu(b, q, k, v, do, w.block_size)
+    _check(res, q, k, v, do, w.block_size, heads=[(1, 7)])

@@ -58,6 +58,22 @@ def causal_flops(w: inputs.Workload):
     return fwd, 2.5 * fwd
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of per-rank timings (a no-op on one rank)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tflops(flop_per_rank_step, ms_per_step, world):
+    """Whole-job throughput: every rank processes its own workload (weak scaling)."""
+    return world * flop_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -248,18 +264,13 @@ def run_gpu(args, w, rank, world):
     if binding.dfa_status() != 0:
         raise RuntimeError("device status set during the timed region")
 
-    if world > 1:
-        import torch.distributed as dist
-
-        tt = torch.tensor([t_ms, tc_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms, tc_ms = tt.tolist()
+    t_ms, tc_ms = max_over_ranks([t_ms, tc_ms], dev)
 
     f_fwd, f_bwd = flops(w)
     c_fwd, c_bwd = causal_flops(w)
     ms_step = t_ms / args.steps
-    value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
-    causal_value = world * (c_fwd + c_bwd) / (tc_ms / args.steps * 1e-3) / 1e12
+    value = job_tflops(f_fwd + f_bwd, ms_step, world)
+    causal_value = job_tflops(c_fwd + c_bwd, tc_ms / args.steps, world)
     fwd_ms, pre_ms, main_ms, conv_ms = parts.tolist()
     peaks = measured_peaks()
 
@@ -288,15 +299,9 @@ def run_gpu(args, w, rank, world):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = tt.item()
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1)], dev)[0]
     tensor_bytes = q.numel() * 2
-    e2e = {"value": world * (f_fwd + f_bwd) / (e2e_ms / args.steps * 1e-3) / 1e12,
+    e2e = {"value": job_tflops(f_fwd + f_bwd, e2e_ms / args.steps, world),
            "unit": "TFLOPS", "h2d_bytes_per_step": 4 * tensor_bytes,
            "d2h_bytes_per_step": 4 * tensor_bytes + host_lse.numel() * 4}
 

@@ -40,6 +40,7 @@ _SIGNATURES = {
     "dfa_causal_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "dfa_causal_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _P]),
     "dfa_status": (_I, [_P]),
+    "dfa_selftest_wait_timeout": (_I, [_I, _P]),
     "dfa_bwd_preprocess": (_I, [_P] * 4 + [_I] * 4 + [_P]),
     "dfa_bwd_main": (_I, [_P] * 9 + [_I] * 6 + [_P]),
     "dfa_bwd_dq_convert": (_I, [_P] * 2 + [_I] * 4 + [_P]),
@@ -192,6 +193,15 @@ def dfa_bwd_dq_convert(dq_acc, dq):
     with torch.cuda.device(dq.device):
         rc = lib().dfa_bwd_dq_convert(_ptr(dq_acc), _ptr(dq), B, L // 2, H, d, _stream_ptr(dq))
     _check("dfa_bwd_dq_convert", rc)
+
+
+def dfa_selftest_wait_timeout(limit_us=20000):
+    """Run the bounded-wait self-test on the current stream (see dfa.h)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        rc = lib().dfa_selftest_wait_timeout(int(limit_us),
+                                             ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    _check("dfa_selftest_wait_timeout", rc)
 
 
 def dfa_status(device=None):

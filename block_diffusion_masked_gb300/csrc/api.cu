@@ -319,6 +319,16 @@ int dfa_bwd_dq_convert(const float* dq_acc, void* dq, int batch, int n, int head
   return convert_impl(dq_acc, dq, batch, n, heads, headdim, static_cast<cudaStream_t>(stream));
 }
 
+int dfa_selftest_wait_timeout(int limit_us, dfa_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return DFA_EINVAL;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc) return rc;
+  const cudaError_t e = launch_selftest_wait(ds->status, 1000ull * limit_us,
+                                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DFA_OK : cuda_fail(e);
+}
+
 const char* dfa_last_cuda_error(void) { return cudaGetErrorString(t_last_error); }
 
 int dfa_status(dfa_stream_t stream) {

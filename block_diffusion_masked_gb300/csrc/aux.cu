@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 
 #include "params.cuh"
+#include "sm100.cuh"
 
 namespace dfa {
 
@@ -69,6 +70,30 @@ __global__ void __launch_bounds__(256) dfa_dq_convert_kernel(const float4* __res
     w.w = *reinterpret_cast<uint32_t*>(&t);
     dst[g] = w;
   }
+}
+
+// Failure-detection self-test: one warp waits, through the same bounded
+// wait the attention kernels use, on an mbarrier that nothing arrives on.
+// The wait gives up after `limit_ns`, records the timeout in the status word
+// and the kernel returns normally.
+__global__ void dfa_selftest_wait_kernel(unsigned* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const AbortFlag ab{&abort_flag, status};
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, ab, limit_ns);
+  __syncwarp();
+}
+
+cudaError_t launch_selftest_wait(unsigned* status, unsigned long long limit_ns,
+                                 cudaStream_t stream) {
+  dfa_selftest_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
 }
 
 static int grid_for(long long work, int per_block) {

@@ -55,6 +55,8 @@ cudaError_t launch_backward_d256(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* out, const __nv_bfloat16* dout,
                                   float* delta, float* dq_acc, int B, int L, int H, int d,
                                   cudaStream_t stream);
+cudaError_t launch_selftest_wait(unsigned* status, unsigned long long limit_ns,
+                                 cudaStream_t stream);
 cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, long long count,
                               cudaStream_t stream);
 

@@ -69,14 +69,15 @@ struct AbortFlag {
 
 // Wait for phase `parity` of barrier `bar` to complete.  Returns false when
 // the CTA is aborting (this wait timed out, or another warp's did).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const AbortFlag& ab) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const AbortFlag& ab,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*ab.flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *ab.flag = 1;
         atomicOr(ab.status, kStatusTimeout);
         return false;

@@ -159,6 +159,17 @@ int dfa_backward_noalloc(const void *q, const void *k, const void *v, const void
 int dfa_status(dfa_stream_t stream);
 
 /*
+ * Failure-detection self-test.  Launches one warp that waits, through the
+ * same bounded wait the attention kernels use, on an mbarrier that nothing
+ * ever arrives on.  After limit_us microseconds (1 .. 1,000,000) the wait
+ * gives up, DFA_ETIMEOUT is recorded in the device status word and the
+ * kernel returns; the next dfa_status() reports it and the context stays
+ * usable.  No passage of the pages has a counterpart: it checks the guard
+ * that turns a kernel-side hang into an error code.
+ */
+int dfa_selftest_wait_timeout(int limit_us, dfa_stream_t stream);
+
+/*
  * Tile geometry, host side, for tests and schedulers.  mode is one of
  * DFA_MODE_*; halves are 0 (noisy) and 1 (clean); tiles are block_m query
  * rows by block_n keys, counted inside a half.

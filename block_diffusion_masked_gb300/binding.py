@@ -49,6 +49,7 @@ _SIGNATURES = {
     "dfa_tile_full": (_I, [_I] * 7),
     "dfa_tile_visits": (ctypes.c_longlong, [_I] * 6),
     "dfa_tile_shape": (_I, [_I] + [ctypes.POINTER(_I)] * 4),
+    "dfa_work_item": (_I, [_I] * 7 + [ctypes.POINTER(_I)]),
 }
 
 
@@ -233,6 +234,13 @@ def dfa_tile_full(rule, n, block_size, q_start, block_m, k_start, block_n):
 
 def dfa_tile_visits(mode, n, block_size, block_m, block_n, pass_):
     return lib().dfa_tile_visits(mode, n, block_size, block_m, block_n, pass_)
+
+
+def dfa_work_item(pass_, mode, w, batch, heads, tiles, group):
+    """(batch, head, half, tile) of the w-th work item of a pass (0 forward, 1 backward)."""
+    buf = (_I * 4)()
+    _check("dfa_work_item", lib().dfa_work_item(pass_, mode, w, batch, heads, tiles, group, buf))
+    return tuple(buf)
 
 
 def dfa_tile_shape(headdim):

@@ -14,6 +14,12 @@
 // clears it.  Host code reaches it through cudaGetSymbolAddress.
 static __device__ unsigned g_dfa_status;
 
+// Work counters of the persistent kernels: one pair of words per slot, a
+// slot per stream (see sched_for_stream).  Zero at load; every launch leaves
+// its slot zero again when its last CTA finishes.
+constexpr int kSchedSlots = 256;
+static __device__ unsigned g_dfa_sched[kSchedSlots * 8];
+
 namespace dfa {
 namespace {
 
@@ -23,7 +29,11 @@ struct DeviceState {
   bool ready = false;
   bool supported = false;
   unsigned* status = nullptr;
+  unsigned* sched = nullptr;  // kSchedSlots slots of 8 words
   long long l2_bytes = 0;
+  const void* slot_key[kSchedSlots] = {};
+  int slots_used = 0;
+  int slot_next = 0;
 };
 
 std::mutex g_mu;
@@ -58,6 +68,8 @@ int device_state(DeviceState** out) {
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_dfa_status) != cudaSuccess) return DFA_ECUDA;
       s.status = static_cast<unsigned*>(addr);
+      if (cudaGetSymbolAddress(&addr, g_dfa_sched) != cudaSuccess) return DFA_ECUDA;
+      s.sched = static_cast<unsigned*>(addr);
     }
     if (!g_encode) {
       void* fn = nullptr;
@@ -73,6 +85,30 @@ int device_state(DeviceState** out) {
   if (!s.supported) return DFA_EUNSUPPORTED;
   *out = &s;
   return DFA_OK;
+}
+
+// Work counter for a launch on `stream`.  Launches on one stream run one
+// after another, so they can share a counter (each leaves it zero); launches
+// on different streams may run at the same time and get different slots.
+// The per-thread default stream has one handle for many streams, so it is
+// keyed by the calling thread.  Past kSchedSlots streams the oldest slot is
+// reused.
+thread_local char t_stream_key;
+unsigned* sched_for_stream(DeviceState* s, cudaStream_t stream) {
+  const void* key = stream == cudaStreamPerThread ? static_cast<const void*>(&t_stream_key)
+                                                  : static_cast<const void*>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < s->slots_used; ++i)
+    if (s->slot_key[i] == key) return s->sched + 8 * i;
+  int i;
+  if (s->slots_used < kSchedSlots) {
+    i = s->slots_used++;
+  } else {
+    i = s->slot_next;
+    s->slot_next = (s->slot_next + 1) % kSchedSlots;
+  }
+  s->slot_key[i] = key;
+  return s->sched + 8 * i;
 }
 
 // View a (B, 2n, H, d) bf16 tensor as 5-D (d, H, n, half, B) -- strides
@@ -133,6 +169,7 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   p.q_tiles = cdiv(n, ts.fwd_bm);
   // q, k, v and out of one (batch, head)
   p.group = l2_group(8LL * 2 * n * d, ds->l2_bytes, B * H);
+  p.sched = sched_for_stream(ds, stream);
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   const cudaError_t e = launch_forward(p, d, stream);
   return e == cudaSuccess ? DFA_OK : cuda_fail(e);
@@ -177,6 +214,8 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   p.k_tiles = cdiv(n, ts.bwd_bn);
   // q, k, v, dout (bf16) and the float32 dq accumulator of one (batch, head)
   p.group = l2_group(12LL * 2 * n * d, ds->l2_bytes, B * H);
+  p.sched = sched_for_stream(ds, stream);
+  p.items = 0;  // set by the launcher
   p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   const cudaError_t e = launch_backward(p, d, stream);
@@ -402,6 +441,22 @@ long long dfa_tile_visits(int mode, int n, int block_size, int block_m, int bloc
       for (int i = 0; i < cnt; ++i) total += s[i].t_end - s[i].t_begin;
     }
   return total;
+}
+
+int dfa_work_item(int pass, int mode, int w, int batch, int heads, int tiles, int group,
+                  int* item) {
+  if ((pass != 0 && pass != 1) || (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) || batch < 1 ||
+      heads < 1 || tiles < 1 || group < 1 || !item)
+    return DFA_EINVAL;
+  const long long items = 2LL * batch * heads * tiles;
+  if (items > 0x7fffffffLL || w < 0 || w >= items) return DFA_EINVAL;
+  const WorkItem it = pass == 0 ? fwd_work(w, mode, batch, heads, tiles, group)
+                                : bwd_work(w, mode, batch, heads, tiles, group);
+  item[0] = it.b;
+  item[1] = it.h;
+  item[2] = it.half;
+  item[3] = it.tile;
+  return DFA_OK;
 }
 
 int dfa_tile_shape(int headdim, int* fwd_block_m, int* fwd_block_n, int* bwd_block_n,

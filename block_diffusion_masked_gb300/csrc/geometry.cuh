@@ -141,17 +141,22 @@ DFA_HD long long lse_offset(int mode, int b, int h, int half, int r, int H, int 
   return (static_cast<long long>(b) * H + h) * (2LL * n) + static_cast<long long>(half) * n + r;
 }
 
-// Work decoding.  The (batch, head) pairs are cut into groups of `group`
-// heads; a group's work items are handed out together, so the group's
-// tensors stay in L2 while its tiles run ("Fast Diffusion Attention",
-// "Ampere and Ada": L2-aware block order).  Inside a group, the items go
-// longest first ("Hopper": the scheduler hands out tiles longest first).
+// Work decoding.  An item's "rank" orders the items of one (batch, head)
+// longest first ("Fast Diffusion Attention", "Hopper": the scheduler hands
+// out tiles longest first).  The (batch, head) pairs are cut into groups of
+// `group` heads whose items are handed out together, so the group's tensors
+// stay in L2 while its tiles run ("Ampere and Ada": L2-aware block order).
+// The shortest ranks of every (batch, head) are held back and handed out
+// last, rank by rank over all pairs: they reuse little from L2, and ending on
+// short items lets the persistent kernels, which take items from a shared
+// counter, finish together.
 // Forward: one item per (batch, head, half, query tile): query tiles in
-// decreasing index, both halves side by side.  Backward: key tiles; in the
-// diffusion mode the clean key tiles (seen by clean and noisy queries) in
-// increasing index, then the noisy key tiles (seen only by their own noisy
-// blocks); in the causal mode key tiles in increasing index, halves side by
-// side.
+// decreasing index, both halves side by side; the last two tiles of each
+// half form the tail.  Backward: key tiles; in the diffusion mode the clean
+// key tiles (seen by clean and noisy queries) in increasing index, then the
+// noisy key tiles (seen only by their own noisy blocks), which form the
+// tail; in the causal mode key tiles in increasing index, halves side by
+// side, the last two tiles of each half forming the tail.
 struct WorkItem {
   int b, h, half, tile;
 };
@@ -167,10 +172,32 @@ DFA_HD void group_split(int w, int BH, int group, int per_bh, int* rank, int* bh
   *bh = first + idx % gsize;
 }
 
-DFA_HD WorkItem fwd_work(int w, int mode, int B, int H, int tiles, int group) {
+// Ranks [0, ranks - tail) group by group, then the last `tail` ranks of all
+// (batch, head) pairs.
+DFA_HD void work_split(int w, int BH, int group, int ranks, int tail, int* rank, int* bh) {
+  const int head = ranks - tail;
+  const long long grouped = static_cast<long long>(BH) * head;
+  if (w < grouped) {
+    group_split(w, BH, group, head, rank, bh);
+    return;
+  }
+  const long long t = w - grouped;
+  *rank = head + static_cast<int>(t / BH);
+  *bh = static_cast<int>(t % BH);
+}
+
+DFA_HD int fwd_tail_ranks(int mode, int tiles) {
   (void)mode;
+  return imin(2 * tiles, 4);
+}
+
+DFA_HD int bwd_tail_ranks(int mode, int tiles) {
+  return mode == MODE_CAUSAL ? imin(2 * tiles, 4) : tiles;
+}
+
+DFA_HD WorkItem fwd_work(int w, int mode, int B, int H, int tiles, int group) {
   int rank, bh;
-  group_split(w, B * H, group, 2 * tiles, &rank, &bh);
+  work_split(w, B * H, group, 2 * tiles, fwd_tail_ranks(mode, tiles), &rank, &bh);
   WorkItem it;
   it.tile = tiles - 1 - (rank >> 1);
   it.half = rank & 1;
@@ -181,7 +208,7 @@ DFA_HD WorkItem fwd_work(int w, int mode, int B, int H, int tiles, int group) {
 
 DFA_HD WorkItem bwd_work(int w, int mode, int B, int H, int tiles, int group) {
   int rank, bh;
-  group_split(w, B * H, group, 2 * tiles, &rank, &bh);
+  work_split(w, B * H, group, 2 * tiles, bwd_tail_ranks(mode, tiles), &rank, &bh);
   WorkItem it;
   if (mode == MODE_CAUSAL) {
     it.tile = rank >> 1;

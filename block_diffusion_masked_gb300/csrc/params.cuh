@@ -26,6 +26,7 @@ struct FwdParams {
   int q_tiles;       // tiles per half along the queries
   int group;         // (batch, head) pairs per scheduling group
   float scale_log2;  // softmax scale * log2(e)
+  unsigned* sched;   // work counter of a persistent launch (see sched_next)
 };
 
 struct BwdParams {
@@ -44,7 +45,28 @@ struct BwdParams {
   int group;          // (batch, head) pairs per scheduling group
   float scale;        // softmax scale
   float scale_log2;   // scale * log2(e)
+  unsigned* sched;    // work counter of a persistent launch (see sched_next)
+  int items;          // work items of the launch
 };
+
+#if defined(__CUDACC__)
+// Work counter of a persistent launch, two words zero before the launch:
+// sched[0] hands out item indices in order, sched[1] counts CTAs that have
+// finished.  The last CTA to finish sets both back to zero, so the next
+// launch on the same stream finds them zero again.
+__device__ __forceinline__ int sched_next(unsigned* sched, int items) {
+  const unsigned w = atomicAdd(sched, 1u);
+  return w < static_cast<unsigned>(items) ? static_cast<int>(w) : -1;
+}
+// One thread per CTA, after the CTA's last sched_next.
+__device__ __forceinline__ void sched_finish(unsigned* sched) {
+  __threadfence();
+  if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+    atomicExch(sched, 0u);
+    atomicExch(sched + 1, 0u);
+  }
+}
+#endif
 
 // Launchers (one per translation unit).  Return a cudaError_t.
 cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream);

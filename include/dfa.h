@@ -30,6 +30,15 @@
  * default stream).  All calls are asynchronous on that stream: a return of
  * DFA_OK means the work was enqueued.
  *
+ * Concurrency.  The persistent kernels draw work items from a counter the
+ * library keeps in device memory, one per stream (up to 256 streams per
+ * device; past that the least recently added stream's counter is shared).
+ * Each launch leaves its counter zero when it finishes, so launches on one
+ * stream never interfere, and launches on different streams use different
+ * counters.  A CUDA graph captured from a stream keeps that stream's counter:
+ * do not replay it while other work of the same stream, or another replay
+ * of it, is running.
+ *
  * Errors.  Functions return 0 (DFA_OK) or a negative code below; nothing
  * else crosses the ABI.  Argument errors are detected on the host before any
  * launch.  Kernels never trap: every wait inside a kernel is bounded, and a
@@ -194,6 +203,20 @@ int dfa_bwd_segments(int mode, int n, int block_size, int block_m, int block_n,
 int dfa_tile_full(int rule, int n, int block_size, int q_start, int block_m,
                   int k_start, int block_n);
 long long dfa_tile_visits(int mode, int n, int block_size, int block_m, int block_n, int pass);
+
+/*
+ * Work order of the kernels, host side, for tests and schedulers: the w-th
+ * work item (0 <= w < 2 * batch * heads * tiles) of the forward (pass 0,
+ * one item per query tile) or backward (pass 1, one item per key tile)
+ * enumeration, for `tiles` tiles per half and scheduling groups of `group`
+ * (batch, head) pairs.  Writes (batch, head, half, tile) into item[4].
+ * Inside a group the items of a (batch, head) go longest first; the
+ * shortest ones of all pairs come last ("Fast Diffusion Attention",
+ * "Hopper" and "Ampere and Ada": longest-first, L2-aware order).  The
+ * persistent kernels hand the items out in this order from a work counter.
+ */
+int dfa_work_item(int pass, int mode, int w, int batch, int heads, int tiles, int group,
+                  int *item);
 
 /*
  * Tile shapes the kernels use for a head dimension: forward query rows and

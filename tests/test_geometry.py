@@ -121,3 +121,45 @@ def test_noisy_diagonal_overhead_matches_page():
         diff = bb.dfa_tile_visits(0, n, 16, 128, 128, 0)
         causal = bb.dfa_tile_visits(1, n, 1, 128, 128, 0)
         assert lo < diff / causal - 1 < hi, (n, diff, causal)
+
+
+def _visits(b, pass_, mode, n, bs, half, tile, bm, bn):
+    fn = b.dfa_fwd_segments if pass_ == 0 else b.dfa_bwd_segments
+    return sum(e - s for (_, _, s, e) in fn(mode, n, bs, bm, bn, half, tile))
+
+
+@pytest.mark.parametrize("pass_", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("batch,heads,n,bs,group", [
+    (1, 1, 300, 16, 1), (2, 3, 700, 1, 2), (3, 5, 1024, 64, 4), (2, 4, 512, 512, 3),
+    (1, 7, 129, 7, 7), (4, 2, 2048, 16, 3),
+])
+def test_work_order_is_longest_first_with_short_tail(b, pass_, mode, batch, heads, n, bs, group):
+    """The persistent kernels take items in this order from a counter: it must
+    cover every (batch, head, half, tile) once, go longest first for each
+    (batch, head) inside the grouped part, and end on the shortest items."""
+    bm, bn = (128, 128) if pass_ == 0 else (64, 128)
+    tiles = -(-n // (bm if pass_ == 0 else bn))
+    BH = batch * heads
+    total = 2 * BH * tiles
+    order = [b.dfa_work_item(pass_, mode, w, batch, heads, tiles, group) for w in range(total)]
+    assert sorted(order) == sorted((x, y, h, t) for x in range(batch) for y in range(heads)
+                                   for h in range(2) for t in range(tiles))
+    bs_eff = min(bs, n)
+    vis = [_visits(b, pass_, mode, n, bs_eff, h, t, bm, bn) for (_, _, h, t) in order]
+    tail = min(2 * tiles, 4) if (pass_ == 0 or mode == 1) else tiles
+    head = total - BH * tail
+    if head > 0:
+        if n % 128 == 0:  # a ragged last tile can be shorter than a tail item
+            assert max(vis[head:]) <= min(vis[:head])
+        seen = {}
+        for (x, y, _, _), c in zip(order[:head], vis[:head]):
+            assert c <= seen.get((x, y), c)
+            seen[(x, y)] = c
+    # tail: rank by rank over all pairs, each rank covering every pair once
+    for r in range(tail):
+        chunk = order[head + r * BH: head + (r + 1) * BH]
+        assert sorted((x, y) for (x, y, _, _) in chunk) == [(x, y) for x in range(batch)
+                                                            for y in range(heads)]
+    with pytest.raises(b.DfaError):
+        b.dfa_work_item(pass_, mode, total, batch, heads, tiles, group)

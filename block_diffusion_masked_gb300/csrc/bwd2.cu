@@ -37,6 +37,8 @@
 // to 184 (setmaxnreg; launched with 168: 256 * 16 == 128 * 32).
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "geometry.cuh"
 #include "params.cuh"
 #include "sm100.cuh"
@@ -417,33 +419,42 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         const float* nlse_s = reinterpret_cast<const float*>(smem + C::kOffLSE) + st * BMQ;
         const float* ndel_s = reinterpret_cast<const float*>(smem + C::kOffDEL) + st * BMQ;
         const bool full = tile_full(rule, p.n, p.bs, qs, BMQ, ks, BN);
-        const Interval iv = query_interval(rule, j, p.n, p.bs);
         // P^T and dS^T in packed pairs: x = s * sl2 - lse2, p = 2^x,
         // ds = p * (dp - D); bf16 pairs packed two chunks of 16 words each.
+        // A tile cut by the mask keeps the query columns [clo, chi) that see
+        // key j; the masked and unmasked loops are separate straight-line
+        // code, so no branch splits the unrolled loop.
         uint32_t wp[BMQ / 2], wd[BMQ / 2];
+        auto grad = [&](auto masked, int clo, int chi) {
 #pragma unroll
-        for (int e = 0; e < BMQ / 2; ++e) {
-          const float2 nl = *reinterpret_cast<const float2*>(nlse_s + 2 * e);
-          const float2 nd = *reinterpret_cast<const float2*>(ndel_s + 2 * e);
-          const uint64_t x = f2_fma(
-              f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), scale2,
-              f2_pack(nl.x, nl.y));
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          float p0 = ex2_approx(x0);
-          float p1 = ex2_approx(x1);
-          if (!full) {
-            const int q = qs + 2 * e;
-            if (q < iv.lo || q >= iv.hi) p0 = 0.f;
-            if (q + 1 < iv.lo || q + 1 >= iv.hi) p1 = 0.f;
+          for (int e = 0; e < BMQ / 2; ++e) {
+            const float2 nl = *reinterpret_cast<const float2*>(nlse_s + 2 * e);
+            const float2 nd = *reinterpret_cast<const float2*>(ndel_s + 2 * e);
+            const uint64_t x = f2_fma(
+                f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), scale2,
+                f2_pack(nl.x, nl.y));
+            float x0, x1;
+            f2_unpack(x, x0, x1);
+            float p0 = ex2_approx(x0);
+            float p1 = ex2_approx(x1);
+            if constexpr (decltype(masked)::value) {
+              p0 = (2 * e >= clo && 2 * e < chi) ? p0 : 0.f;
+              p1 = (2 * e + 1 >= clo && 2 * e + 1 < chi) ? p1 : 0.f;
+            }
+            const uint64_t dd = f2_add(
+                f2_pack(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1])),
+                f2_pack(nd.x, nd.y));
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
+            wp[e] = pack_bf16x2(p0, p1);
+            wd[e] = pack_bf16x2(d0, d1);
           }
-          const uint64_t dd = f2_add(
-              f2_pack(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1])),
-              f2_pack(nd.x, nd.y));
-          float d0, d1;
-          f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
-          wp[e] = pack_bf16x2(p0, p1);
-          wd[e] = pack_bf16x2(d0, d1);
+        };
+        if (full) {
+          grad(std::false_type{}, 0, BMQ);
+        } else {
+          const Interval iv = query_interval(rule, j, p.n, p.bs);
+          grad(std::true_type{}, iv.lo - qs, iv.hi - qs);
         }
         // PdS (TMEM) and the dS^T shared tile still feed the previous tile's
         // products until they complete.

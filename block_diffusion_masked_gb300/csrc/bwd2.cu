@@ -25,19 +25,18 @@
 // Persistent: one CTA per SM takes items from a work counter until none are
 // left, so the load of the next item's K and V and of its first query tiles
 // overlaps the end of the current item, and short items fill the SMs that
-// finish early.  Two compute warpgroups take alternate query tiles (counted
-// over the CTA's whole run).  A warpgroup releases S and dP as soon as it has
-// read them into registers, so the scores of the next tile are computed
-// while it works; P^T / dS^T and dQ have TMEM columns of their own, so no
-// product waits for a read-out it does not need.  At the end of an item
-// warpgroup 0 writes dV and warpgroup 1 writes dK; the next item's first dV /
-// dK products wait until both have been read out of TMEM.
+// finish early.  Both compute warpgroups work on every query tile, each on
+// half of its query columns; a tile's dQ is read out of TMEM during the next
+// tile's turn, once that tile's P^T / dS^T are handed over, so no warpgroup
+// waits for the products of the tile it has just finished.  S and dP are
+// released as soon as they are in registers, so the scores of the next tile
+// are computed while the warpgroups work.  At the end of an item warpgroup 0
+// writes dV and warpgroup 1 writes dK; the next item's first dV / dK
+// products wait until both have been read out of TMEM.
 // Warps 0-7 compute, warp 8 loads, warp 9 issues MMAs, warps 10-11 idle; the
 // load/MMA warpgroup drops to 136 registers and the compute warpgroups rise
 // to 184 (setmaxnreg; launched with 168: 256 * 16 == 128 * 32).
 #include <cuda_bf16.h>
-
-#include <type_traits>
 
 #include "geometry.cuh"
 #include "params.cuh"
@@ -69,10 +68,8 @@ struct Bwd2Cfg {
     BAR_KVFULL = 0,  // K and V of an item loaded
     BAR_QFULL = 1,
     BAR_QEMPTY = BAR_QFULL + STAGES,
-    // S^T and dP^T of a tile computed; one barrier per warpgroup, so that a
-    // warpgroup never waits for a phase two ahead of the last one it saw.
-    BAR_SDPFULL = BAR_QEMPTY + STAGES,  // [2]
-    BAR_SDPFREE = BAR_SDPFULL + 2,      // S^T / dP^T read into registers
+    BAR_SDPFULL = BAR_QEMPTY + STAGES,  // S^T and dP^T of a tile computed
+    BAR_SDPFREE = BAR_SDPFULL + 1,      // S^T / dP^T read into registers
     BAR_PDSFULL = BAR_SDPFREE + 1,      // P^T / dS^T of a tile in place
     BAR_MMA2 = BAR_PDSFULL + 1,         // dV, dK, dQ of a tile done
     BAR_DQFREE = BAR_MMA2 + 1,          // dQ of a tile read out of TMEM
@@ -155,11 +152,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
       mbar_init(BAR(C::BAR_QEMPTY + s), 1);
     }
     mbar_init(BAR(C::BAR_SDPFULL), 1);
-    mbar_init(BAR(C::BAR_SDPFULL + 1), 1);
-    mbar_init(BAR(C::BAR_SDPFREE), 128);
-    mbar_init(BAR(C::BAR_PDSFULL), 128);
+    mbar_init(BAR(C::BAR_SDPFREE), 256);
+    mbar_init(BAR(C::BAR_PDSFULL), 256);
     mbar_init(BAR(C::BAR_MMA2), 1);
-    mbar_init(BAR(C::BAR_DQFREE), 128);
+    mbar_init(BAR(C::BAR_DQFREE), 256);
     mbar_init(BAR(C::BAR_ITEMDONE), 1);
     mbar_init(BAR(C::BAR_ACCFREE), 256);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
@@ -348,7 +344,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
           // products of tile gg-1 (the stage's last readers) are issued.
           if (STAGES == 1 && i >= 1 && !(ok = issue_second(gg - 1, i == 1))) break;
           if (!(ok = mbar_wait(BAR(C::BAR_QFULL + st), (gg / STAGES) & 1, ab))) break;
-          // S and dP are free once the previous tile's warpgroup has read them.
+          // S and dP are free once both warpgroups have read the previous tile's.
           if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_SDPFREE), (gg - 1) & 1, ab))) break;
           tc_fence_after();
           const uint32_t st_off = st * C::kQBytes;
@@ -366,7 +362,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
             mma_ss(tmem + C::kTmemDP, adv(dV_kmaj, koff), adv(dO_kmaj, st_off + qoff), kIdS,
                    kk > 0 ? 1u : 0u);
           }
-          mma_commit(BAR(C::BAR_SDPFULL + (gg & 1)));
+          mma_commit(BAR(C::BAR_SDPFULL));
           if (STAGES > 1 && i >= 1 && !(ok = issue_second(gg - 1, i == 1))) break;
         }
         if (!ok) break;
@@ -382,11 +378,46 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
     // ------------------------------------------------------------ compute
-    const int wg = warp >> 2;                // this warpgroup takes tiles gg % 2 == wg
+    // Both warpgroups work on every query tile: warpgroup wg takes query
+    // columns [32 wg, 32 wg + 32) of S^T, dP^T, P^T / dS^T and dQ^T.  The dQ
+    // of a tile is read out of TMEM in the next tile's turn, after that
+    // tile's P^T / dS^T are handed over, so no warpgroup waits for the dV,
+    // dK, dQ products of the tile it has just finished.
+    constexpr int HC = BMQ / 2;              // query columns per warpgroup
+    const int wg = warp >> 2;
+    const int c0 = wg * HC;                  // first column of this warpgroup
     const int row = (warp & 3) * 32 + lane;  // key row of the tile / TMEM lane
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const float sl2 = p.scale_log2;
     const uint64_t scale2 = f2_pack(sl2, sl2);
+    const size_t dq_stride = static_cast<size_t>(p.H) * D;
+    // dQ^T of the tile whose products completed last: TMEM lane = head dim
+    // `row`, columns = queries; added into the float32 accumulator.
+    auto drain_dq = [&](const Bwd2Item& it, int qh, int qs) {
+      uint32_t dq[HC];
+      tmem_ld32(t_lane + C::kTmemDQ + c0, dq);
+      tmem_wait_ld();
+      tmem_pin<HC>(dq);
+      tc_fence_before();
+      mbar_arrive(BAR(C::BAR_DQFREE));
+      float* ptr = p.dq_acc +
+                   ((static_cast<size_t>(it.wi.b) * L + static_cast<size_t>(qh) * p.n + qs + c0) *
+                        p.H + it.wi.h) * D + it.dh * DH + row;
+      if (qs + c0 + HC <= p.n) {
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+          red_add_f32(ptr, __uint_as_float(dq[c]) * p.scale);
+          ptr += dq_stride;
+        }
+      } else {
+        const int qmax = p.n - qs - c0;
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+          if (c < qmax) red_add_f32(ptr, __uint_as_float(dq[c]) * p.scale);
+          ptr += dq_stride;
+        }
+      }
+    };
     bool ok = true;
     int g = 0, k = 0;
     while (ok) {
@@ -396,120 +427,91 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
       const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
       const int ks = it.wi.tile * BN;
       const int j = ks + row;  // key inside its half
-      for (int i = ((g & 1) == wg) ? 0 : 1; i < it.ntiles && ok; i += 2) {
+      for (int i = 0; i < it.ntiles && ok; ++i) {
         const int gg = g + i;
         const int qt = it.qtile(i);
-        const int qh = it.qhalf(i);
         const int rule = it.rule(i);
         const int st = gg % STAGES;
         const int qs = qt * BMQ;
-        if (!(ok = mbar_wait_warp(BAR(C::BAR_SDPFULL + (gg & 1)), (gg >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(BAR(C::BAR_SDPFULL), gg & 1, ab))) break;
         tc_fence_after();
-        uint32_t sr[BMQ], dpr[BMQ];
-        tmem_ld32(t_lane + C::kTmemS, sr);
-        tmem_ld32(t_lane + C::kTmemS + 32, sr + 32);
-        tmem_ld32(t_lane + C::kTmemDP, dpr);
-        tmem_ld32(t_lane + C::kTmemDP + 32, dpr + 32);
+        uint32_t sr[HC], dpr[HC];
+        tmem_ld32(t_lane + C::kTmemS + c0, sr);
+        tmem_ld32(t_lane + C::kTmemDP + c0, dpr);
         tmem_wait_ld();
-        tmem_pin<BMQ>(sr);
-        tmem_pin<BMQ>(dpr);
+        tmem_pin<HC>(sr);
+        tmem_pin<HC>(dpr);
         tc_fence_before();
         mbar_arrive(BAR(C::BAR_SDPFREE));
 
-        const float* nlse_s = reinterpret_cast<const float*>(smem + C::kOffLSE) + st * BMQ;
-        const float* ndel_s = reinterpret_cast<const float*>(smem + C::kOffDEL) + st * BMQ;
-        const bool full = tile_full(rule, p.n, p.bs, qs, BMQ, ks, BN);
-        // P^T and dS^T in packed pairs: x = s * sl2 - lse2, p = 2^x,
-        // ds = p * (dp - D); bf16 pairs packed two chunks of 16 words each.
-        // A tile cut by the mask keeps the query columns [clo, chi) that see
-        // key j; the masked and unmasked loops are separate straight-line
-        // code, so no branch splits the unrolled loop.
-        uint32_t wp[BMQ / 2], wd[BMQ / 2];
-        auto grad = [&](auto masked, int clo, int chi) {
-#pragma unroll
-          for (int e = 0; e < BMQ / 2; ++e) {
-            const float2 nl = *reinterpret_cast<const float2*>(nlse_s + 2 * e);
-            const float2 nd = *reinterpret_cast<const float2*>(ndel_s + 2 * e);
-            const uint64_t x = f2_fma(
-                f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), scale2,
-                f2_pack(nl.x, nl.y));
-            float x0, x1;
-            f2_unpack(x, x0, x1);
-            float p0 = ex2_approx(x0);
-            float p1 = ex2_approx(x1);
-            if constexpr (decltype(masked)::value) {
-              p0 = (2 * e >= clo && 2 * e < chi) ? p0 : 0.f;
-              p1 = (2 * e + 1 >= clo && 2 * e + 1 < chi) ? p1 : 0.f;
-            }
-            const uint64_t dd = f2_add(
-                f2_pack(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1])),
-                f2_pack(nd.x, nd.y));
-            float d0, d1;
-            f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
-            wp[e] = pack_bf16x2(p0, p1);
-            wd[e] = pack_bf16x2(d0, d1);
-          }
-        };
-        if (full) {
-          grad(std::false_type{}, 0, BMQ);
-        } else {
+        const float* nlse_s = reinterpret_cast<const float*>(smem + C::kOffLSE) + st * BMQ + c0;
+        const float* ndel_s = reinterpret_cast<const float*>(smem + C::kOffDEL) + st * BMQ + c0;
+        // Columns (queries) that see key j: all of this warpgroup's on a
+        // tile the mask does not cut, else those in [clo, chi), as a mask.
+        uint32_t keep = 0xffffffffu;
+        if (!tile_full(rule, p.n, p.bs, qs, BMQ, ks, BN)) {
           const Interval iv = query_interval(rule, j, p.n, p.bs);
-          grad(std::true_type{}, iv.lo - qs, iv.hi - qs);
+          const int lo = iv.lo - qs - c0, hi = iv.hi - qs - c0;
+          const int clo = lo < 0 ? 0 : (lo > HC ? HC : lo);
+          const int chi = hi < clo ? clo : (hi > HC ? HC : hi);
+          const uint32_t below_hi = chi >= 32 ? 0xffffffffu : ((1u << chi) - 1u);
+          const uint32_t below_lo = clo >= 32 ? 0xffffffffu : ((1u << clo) - 1u);
+          keep = below_hi & ~below_lo;
+        }
+        // P^T and dS^T in packed pairs: x = s * sl2 - lse2, p = 2^x,
+        // ds = p * (dp - D).  A hidden pair's p is cleared by AND with its
+        // column's mask bit spread to a word, so every tile runs the same
+        // straight-line code.
+        uint32_t wp[HC / 2], wd[HC / 2];
+#pragma unroll
+        for (int e = 0; e < HC / 2; ++e) {
+          const float2 nl = *reinterpret_cast<const float2*>(nlse_s + 2 * e);
+          const float2 nd = *reinterpret_cast<const float2*>(ndel_s + 2 * e);
+          const uint64_t x = f2_fma(
+              f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), scale2,
+              f2_pack(nl.x, nl.y));
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          const float p0 =
+              __uint_as_float(__float_as_uint(ex2_approx(x0)) & bit_spread(keep, 2 * e));
+          const float p1 =
+              __uint_as_float(__float_as_uint(ex2_approx(x1)) & bit_spread(keep, 2 * e + 1));
+          const uint64_t dd = f2_add(
+              f2_pack(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1])),
+              f2_pack(nd.x, nd.y));
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
+          wp[e] = pack_bf16x2(p0, p1);
+          wd[e] = pack_bf16x2(d0, d1);
         }
         // PdS (TMEM) and the dS^T shared tile still feed the previous tile's
         // products until they complete.
         if (gg >= 1 && !(ok = mbar_wait_warp(BAR(C::BAR_MMA2), (gg - 1) & 1, ab))) break;
         tc_fence_after();
+        // PdS chunk wg: P^T in its first 16 columns, dS^T in the last 16.
+        tmem_st16(t_lane + C::kTmemPDS + 32 * wg, wp);
+        tmem_st16(t_lane + C::kTmemPDS + 32 * wg + 16, wd);
+        // dS^T row `row` of the shared tile: 16-byte units 4 wg .. 4 wg + 3.
 #pragma unroll
-        for (int c = 0; c < BMQ / 32; ++c) {
-          tmem_st16(t_lane + C::kTmemPDS + 32 * c, wp + 16 * c);
-          tmem_st16(t_lane + C::kTmemPDS + 32 * c + 16, wd + 16 * c);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u4 = 0; u4 < 4; ++u4) {
+          const int u = 4 * wg + u4;
           const uint32_t off = row * 128 + ((u ^ (row & 7)) << 4);
-          st_shared_v4(sbase + C::kOffDS + off, wd[4 * u], wd[4 * u + 1], wd[4 * u + 2],
-                       wd[4 * u + 3]);
+          st_shared_v4(sbase + C::kOffDS + off, wd[4 * u4], wd[4 * u4 + 1], wd[4 * u4 + 2],
+                       wd[4 * u4 + 3]);
         }
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(BAR(C::BAR_PDSFULL));
-
-        // dQ of this tile: TMEM lane = head dim `row`, columns = queries.
-        if (!(ok = mbar_wait_warp(BAR(C::BAR_MMA2), gg & 1, ab))) break;
-        tc_fence_after();
-        uint32_t dq[BMQ];
-        tmem_ld32(t_lane + C::kTmemDQ, dq);
-        tmem_ld32(t_lane + C::kTmemDQ + 32, dq + 32);
-        tmem_wait_ld();
-        tmem_pin<BMQ>(dq);
-        tc_fence_before();
-        mbar_arrive(BAR(C::BAR_DQFREE));
-        const size_t stride = static_cast<size_t>(p.H) * D;
-        float* ptr = p.dq_acc +
-                     ((static_cast<size_t>(it.wi.b) * L + static_cast<size_t>(qh) * p.n + qs) *
-                          p.H + it.wi.h) * D + it.dh * DH + row;
-        if (qs + BMQ <= p.n) {
-#pragma unroll
-          for (int c = 0; c < BMQ; ++c) {
-            red_add_f32(ptr, __uint_as_float(dq[c]) * p.scale);
-            ptr += stride;
-          }
-        } else {
-          const int qmax = p.n - qs;
-#pragma unroll
-          for (int c = 0; c < BMQ; ++c) {
-            if (c < qmax) red_add_f32(ptr, __uint_as_float(dq[c]) * p.scale);
-            ptr += stride;
-          }
-        }
+        // The previous tile's products are complete (waited above): its dQ.
+        if (i >= 1) drain_dq(it, it.qhalf(i - 1), it.qtile(i - 1) * BMQ);
       }
       if (!ok) break;
 
       // -------------------------------------------------------- item epilogue
       // Warpgroup 0 writes dV, warpgroup 1 writes dK, once the item's MMAs are
       // done; TMEM is released as soon as both have read their accumulator.
+      // Then the dQ of the item's last tile.
       if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMDONE), k & 1, ab))) break;
       tc_fence_after();
       const uint32_t col = wg == 0 ? C::kTmemDV : C::kTmemDK;
@@ -541,6 +543,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
           st_global_v4(dst + 8 * g8, w[0], w[1], w[2], w[3]);
         }
       }
+      if (it.ntiles > 0) drain_dq(it, it.qhalf(it.ntiles - 1), it.qtile(it.ntiles - 1) * BMQ);
       g += it.ntiles;
       ++k;
     }

@@ -90,6 +90,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
 // every lane then observes the completed phase itself (acquire).  Keeps the
 // warp converged for the .sync.aligned tcgen05 instructions that follow.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const AbortFlag& ab) {
+  // Fast path: the phase is already complete for every lane.
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   int ok = 0;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, ab) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -343,6 +345,13 @@ __device__ __forceinline__ float max_tree(const uint32_t* v) {
     for (int i = 0; i < M; ++i) u[i] = __float_as_uint(m[i]);
     return max_tree<M>(u);
   }
+}
+
+// Bit BIT of w spread over a whole word: 0xffffffff if set, else 0
+// (shift the bit to the sign position, then shift arithmetically back).
+// `bit` is in [0, 32); inside unrolled loops it folds to a constant.
+__device__ __forceinline__ uint32_t bit_spread(uint32_t w, int bit) {
+  return static_cast<uint32_t>(static_cast<int32_t>(w << (31 - bit)) >> 31);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -444,8 +444,8 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         tc_fence_before();
         mbar_arrive(BAR(C::BAR_SDPFREE));
 
-        const float* nlse_s = reinterpret_cast<const float*>(smem + C::kOffLSE) + st * BMQ + c0;
-        const float* ndel_s = reinterpret_cast<const float*>(smem + C::kOffDEL) + st * BMQ + c0;
+        const uint32_t nlse_s = sbase + C::kOffLSE + 4 * (st * BMQ + c0);
+        const uint32_t ndel_s = sbase + C::kOffDEL + 4 * (st * BMQ + c0);
         // Columns (queries) that see key j: all of this warpgroup's on a
         // tile the mask does not cut, else those in [clo, chi), as a mask.
         uint32_t keep = 0xffffffffu;
@@ -465,8 +465,8 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         uint32_t wp[HC / 2], wd[HC / 2];
 #pragma unroll
         for (int e = 0; e < HC / 2; ++e) {
-          const float2 nl = *reinterpret_cast<const float2*>(nlse_s + 2 * e);
-          const float2 nd = *reinterpret_cast<const float2*>(ndel_s + 2 * e);
+          const float2 nl = ld_shared_v2_f32(nlse_s + 8 * e);
+          const float2 nd = ld_shared_v2_f32(ndel_s + 8 * e);
           const uint64_t x = f2_fma(
               f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), scale2,
               f2_pack(nl.x, nl.y));

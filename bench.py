@@ -314,8 +314,10 @@ def run_gpu(args, w, rank, world):
         except Exception as exc:  # context only
             sdpa = f"unavailable: {exc}"
 
-    dominant = max((("dfa_fwd_kernel", fwd_ms, f_fwd), ("dfa_bwd_kernel", main_ms, f_bwd)),
-                   key=lambda x: x[1])
+    # kernel names as the library launches them for this head dimension
+    fwd_name = "dfa_fwd_kernel<256>" if d == 256 else f"dfa_fwd2_kernel<{d}>"
+    bwd_name = "dfa_bwd_kernel<64>" if d == 64 else f"dfa_bwd2_kernel<{d}>"
+    dominant = max(((fwd_name, fwd_ms, f_fwd), (bwd_name, main_ms, f_bwd)), key=lambda x: x[1])
     achieved = dominant[2] / (dominant[1] * 1e-3) / 1e12
     res = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,

@@ -152,12 +152,12 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
       mbar_init(BAR(C::BAR_QEMPTY + s), 1);
     }
     mbar_init(BAR(C::BAR_SDPFULL), 1);
-    mbar_init(BAR(C::BAR_SDPFREE), 256);
-    mbar_init(BAR(C::BAR_PDSFULL), 256);
+    mbar_init(BAR(C::BAR_SDPFREE), 8);
+    mbar_init(BAR(C::BAR_PDSFULL), 8);
     mbar_init(BAR(C::BAR_MMA2), 1);
-    mbar_init(BAR(C::BAR_DQFREE), 256);
+    mbar_init(BAR(C::BAR_DQFREE), 8);
     mbar_init(BAR(C::BAR_ITEMDONE), 1);
-    mbar_init(BAR(C::BAR_ACCFREE), 256);
+    mbar_init(BAR(C::BAR_ACCFREE), 8);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
     mbar_init(BAR(C::BAR_ALL), 1);
     *abort_flag = 0;
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
       tmem_wait_ld();
       tmem_pin<HC>(dq);
       tc_fence_before();
-      mbar_arrive(BAR(C::BAR_DQFREE));
+      mbar_arrive_warp(BAR(C::BAR_DQFREE));
       float* ptr = p.dq_acc +
                    ((static_cast<size_t>(it.wi.b) * L + static_cast<size_t>(qh) * p.n + qs + c0) *
                         p.H + it.wi.h) * D + it.dh * DH + row;
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         tmem_pin<HC>(sr);
         tmem_pin<HC>(dpr);
         tc_fence_before();
-        mbar_arrive(BAR(C::BAR_SDPFREE));
+        mbar_arrive_warp(BAR(C::BAR_SDPFREE));
 
         const uint32_t nlse_s = sbase + C::kOffLSE + 4 * (st * BMQ + c0);
         const uint32_t ndel_s = sbase + C::kOffDEL + 4 * (st * BMQ + c0);
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(BAR(C::BAR_PDSFULL));
+        mbar_arrive_warp(BAR(C::BAR_PDSFULL));
         // The previous tile's products are complete (waited above): its dQ.
         if (i >= 1) drain_dq(it, it.qhalf(i - 1), it.qtile(i - 1) * BMQ);
       }
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         for (int e = 0; e < DH; ++e) o[e] = 0u;
       }
       tc_fence_before();
-      mbar_arrive(BAR(C::BAR_ACCFREE));
+      mbar_arrive_warp(BAR(C::BAR_ACCFREE));
       if (j < p.n) {
         const size_t pos = static_cast<size_t>(it.wi.half) * p.n + j;
         const size_t off =

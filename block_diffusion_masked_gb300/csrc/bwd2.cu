@@ -104,7 +104,6 @@ struct Bwd2Item {
   int half0, rule0, tb0, half1, rule1, tb1;
   __device__ __forceinline__ int qtile(int t) const { return t < n0 ? tb0 + t : tb1 + (t - n0); }
   __device__ __forceinline__ int qhalf(int t) const { return t < n0 ? half0 : half1; }
-  __device__ __forceinline__ int rule(int t) const { return t < n0 ? rule0 : rule1; }
 };
 
 template <int NDH, int BMQ, int BN>
@@ -427,10 +426,14 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
       const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
       const int ks = it.wi.tile * BN;
       const int j = ks + row;  // key inside its half
+      // Query rows that see key j, per segment of the item: computed once,
+      // so a tile needs no division and no per-tile visibility test (a tile
+      // the mask does not cut gives the full column mask below).
+      const Interval iv0 = query_interval(it.rule0, j, p.n, p.bs);
+      const Interval iv1 = query_interval(it.rule1, j, p.n, p.bs);
       for (int i = 0; i < it.ntiles && ok; ++i) {
         const int gg = g + i;
         const int qt = it.qtile(i);
-        const int rule = it.rule(i);
         const int st = gg % STAGES;
         const int qs = qt * BMQ;
         if (!(ok = mbar_wait_warp(BAR(C::BAR_SDPFULL), gg & 1, ab))) break;
@@ -446,11 +449,11 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
 
         const uint32_t nlse_s = sbase + C::kOffLSE + 4 * (st * BMQ + c0);
         const uint32_t ndel_s = sbase + C::kOffDEL + 4 * (st * BMQ + c0);
-        // Columns (queries) that see key j: all of this warpgroup's on a
-        // tile the mask does not cut, else those in [clo, chi), as a mask.
-        uint32_t keep = 0xffffffffu;
-        if (!tile_full(rule, p.n, p.bs, qs, BMQ, ks, BN)) {
-          const Interval iv = query_interval(rule, j, p.n, p.bs);
+        // Columns (queries) of this warpgroup that see key j, as a mask:
+        // those in [clo, chi) (all of them on a tile the mask does not cut).
+        uint32_t keep;
+        {
+          const Interval iv = i < it.n0 ? iv0 : iv1;
           const int lo = iv.lo - qs - c0, hi = iv.hi - qs - c0;
           const int clo = lo < 0 ? 0 : (lo > HC ? HC : lo);
           const int chi = hi < clo ? clo : (hi > HC ? HC : hi);

@@ -283,11 +283,24 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         tmem_wait_ld();
         tmem_pin<BN>(sr);
         if (!full) {
+          // Keys [clo, chi) of the tile are visible to row r: a 32-bit mask
+          // per 32 columns, hidden scores set to -inf with one AND / OR each,
+          // in straight-line code.
           const Interval iv = key_interval(ig.seg[s].rule, r, p.n, p.bs);
           const int clo = iv.lo - ks, chi = iv.hi - ks;
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (c < clo || c >= chi) sr[c] = __float_as_uint(-INFINITY);
+          for (int c32 = 0; c32 < BN / 32; ++c32) {
+            const int lo = clo - 32 * c32 < 0 ? 0 : (clo - 32 * c32 > 32 ? 32 : clo - 32 * c32);
+            const int hi = chi - 32 * c32 < lo ? lo : (chi - 32 * c32 > 32 ? 32 : chi - 32 * c32);
+            const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+            const uint32_t below_lo = lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u);
+            const uint32_t keep = below_hi & ~below_lo;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const uint32_t m = bit_spread(keep, e);
+              sr[32 * c32 + e] = (sr[32 * c32 + e] & m) | (0xff800000u & ~m);
+            }
+          }
         }
         const float m_tile = max_tree<BN>(sr) * sl2;
         const bool move = m_tile > m_ref + C::kRescaleThreshold;

@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
     mbar_init(BAR(C::BAR_ITEMDONE), 1);
     mbar_init(BAR(C::BAR_ACCFREE), 8);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
-    mbar_init(BAR(C::BAR_ALL), 1);
+    mbar_init(BAR(C::BAR_ALL), 2);  // one commit per issuing warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -280,95 +280,105 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         mbar_wait_limited(BAR(C::BAR_QFULL + t % STAGES), (t / STAGES) & 1, 100000000ull);
     }
     __syncwarp();
-   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+   } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two independent streams of products, each issued by its own warp so
+    // that their issue overlaps: warp 9 issues S^T and dP^T of every tile,
+    // warp 10 the dV, dK and dQ^T products.  Everything one stream needs
+    // from the other is ordered through the compute warpgroups' barriers
+    // (S^T / dP^T complete -> P^T / dS^T written -> second products).
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(BN, BMQ, false, false);  // K Q^T, V dO^T
       constexpr uint32_t kIdKV = idesc_bf16(BN, DH, false, true);   // P^T dO, dS^T Q
       constexpr uint32_t kIdDQ = idesc_bf16(DH, BMQ, true, true);   // K^T dS^T
-      const uint64_t dK_kmaj = sdesc_sw128(sbase + C::kOffK, 16, 1024);
-      const uint64_t dV_kmaj = sdesc_sw128(sbase + C::kOffV, 16, 1024);
-      const uint64_t dQ_kmaj = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
-      const uint64_t dO_kmaj = sdesc_sw128(sbase + C::kOffDO, 16, 1024);
-      const uint64_t dDS_mn = sdesc_sw128(sbase + C::kOffDS, BN * 128, 1024);
       auto adv = [](uint64_t d, uint32_t bytes) { return d + static_cast<uint64_t>(bytes >> 4); };
       bool ok = true;
       int g = 0, k = 0;
-      uint64_t dK_mn = 0, dQ_mn = 0, dO_mn = 0;
-
-      // dV, dK, dQ of global tile gg, once its P^T / dS^T are in place;
-      // `first`: the item's first tile, which starts the dK / dV sums.
-      auto issue_second = [&](int gg, bool first) -> bool {
-        const uint32_t st_off = (gg % STAGES) * C::kQBytes;
-        if (!mbar_wait(BAR(C::BAR_PDSFULL), gg & 1, ab)) return false;
-        // dK / dV of the previous item must be read out before they restart.
-        if (first && k >= 1 && !mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab)) return false;
-        tc_fence_after();
-        const uint32_t pds = tmem + C::kTmemPDS;
+      if (warp == 9) {
+        const uint64_t dK_kmaj = sdesc_sw128(sbase + C::kOffK, 16, 1024);
+        const uint64_t dV_kmaj = sdesc_sw128(sbase + C::kOffV, 16, 1024);
+        const uint64_t dQ_kmaj = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
+        const uint64_t dO_kmaj = sdesc_sw128(sbase + C::kOffDO, 16, 1024);
+        while (ok) {
+          if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
+          const int v = item_ring[k & 3];
+          if (v < 0) break;
+          const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
+          if (!(ok = mbar_wait(BAR(C::BAR_KVFULL), k & 1, ab))) break;
+          for (int i = 0; i < it.ntiles && ok; ++i) {
+            const int gg = g + i;
+            const int st = gg % STAGES;
+            if (!(ok = mbar_wait(BAR(C::BAR_QFULL + st), (gg / STAGES) & 1, ab))) break;
+            // S and dP are free once both warpgroups have read the previous tile's.
+            if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_SDPFREE), (gg - 1) & 1, ab))) break;
+            tc_fence_after();
+            const uint32_t st_off = st * C::kQBytes;
 #pragma unroll
-        for (int kk = 0; kk < BMQ / 16; ++kk) {
-          // queries [16kk, 16kk+16): chunk kk/2, P^T first 16 columns, dS^T last 16
-          const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
-          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + C::kTmemDV, pds + col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV, acc);
-          mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128), kIdKV,
-                 acc);
-        }
-        // The DQ columns still hold dQ of tile gg-1 until it has been read out.
-        if (gg >= 1 && !mbar_wait(BAR(C::BAR_DQFREE), (gg - 1) & 1, ab)) return false;
-        tc_fence_after();
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+              const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
+              mma_ss(tmem + C::kTmemS, adv(dK_kmaj, koff), adv(dQ_kmaj, st_off + qoff), kIdS,
+                     kk > 0 ? 1u : 0u);
+            }
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ss(tmem + C::kTmemDQ, adv(dK_mn, kk * 16 * 128), adv(dDS_mn, kk * 16 * 128), kIdDQ,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(BAR(C::BAR_MMA2));
-        mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
-        return true;
-      };
-
-      while (ok) {
-        if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
-        const int v = item_ring[k & 3];
-        if (v < 0) break;
-        const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
-        // The head-dim half dh starts at 64-wide chunk 2 dh of K, Q and dO.
-        dK_mn = sdesc_sw128(sbase + C::kOffK + it.dh * 2 * (BN * 128), BN * 128, 1024);
-        dQ_mn = sdesc_sw128(sbase + C::kOffQ + it.dh * 2 * (BMQ * 128), BMQ * 128, 1024);
-        dO_mn = sdesc_sw128(sbase + C::kOffDO + it.dh * 2 * (BMQ * 128), BMQ * 128, 1024);
-        if (!(ok = mbar_wait(BAR(C::BAR_KVFULL), k & 1, ab))) break;
-        for (int i = 0; i < it.ntiles && ok; ++i) {
-          const int gg = g + i;
-          const int st = gg % STAGES;
-          // With a single Q / dO stage, tile gg can only be loaded once the
-          // products of tile gg-1 (the stage's last readers) are issued.
-          if (STAGES == 1 && i >= 1 && !(ok = issue_second(gg - 1, i == 1))) break;
-          if (!(ok = mbar_wait(BAR(C::BAR_QFULL + st), (gg / STAGES) & 1, ab))) break;
-          // S and dP are free once both warpgroups have read the previous tile's.
-          if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_SDPFREE), (gg - 1) & 1, ab))) break;
-          tc_fence_after();
-          const uint32_t st_off = st * C::kQBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-            const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
-            mma_ss(tmem + C::kTmemS, adv(dK_kmaj, koff), adv(dQ_kmaj, st_off + qoff), kIdS,
-                   kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+              const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
+              mma_ss(tmem + C::kTmemDP, adv(dV_kmaj, koff), adv(dO_kmaj, st_off + qoff), kIdS,
+                     kk > 0 ? 1u : 0u);
+            }
+            mma_commit(BAR(C::BAR_SDPFULL));
           }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-            const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
-            mma_ss(tmem + C::kTmemDP, adv(dV_kmaj, koff), adv(dO_kmaj, st_off + qoff), kIdS,
-                   kk > 0 ? 1u : 0u);
-          }
-          mma_commit(BAR(C::BAR_SDPFULL));
-          if (STAGES > 1 && i >= 1 && !(ok = issue_second(gg - 1, i == 1))) break;
+          g += it.ntiles;
+          ++k;
         }
-        if (!ok) break;
-        if (it.ntiles > 0 && !(ok = issue_second(g + it.ntiles - 1, it.ntiles == 1))) break;
-        mma_commit(BAR(C::BAR_ITEMDONE));
-        g += it.ntiles;
-        ++k;
+      } else {
+        const uint64_t dDS_mn = sdesc_sw128(sbase + C::kOffDS, BN * 128, 1024);
+        while (ok) {
+          if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
+          const int v = item_ring[k & 3];
+          if (v < 0) break;
+          const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
+          // The head-dim half dh starts at 64-wide chunk 2 dh of K, Q and dO.
+          const uint64_t dK_mn =
+              sdesc_sw128(sbase + C::kOffK + it.dh * 2 * (BN * 128), BN * 128, 1024);
+          const uint64_t dQ_mn =
+              sdesc_sw128(sbase + C::kOffQ + it.dh * 2 * (BMQ * 128), BMQ * 128, 1024);
+          const uint64_t dO_mn =
+              sdesc_sw128(sbase + C::kOffDO + it.dh * 2 * (BMQ * 128), BMQ * 128, 1024);
+          for (int i = 0; i < it.ntiles && ok; ++i) {
+            // dV, dK, dQ of tile gg once its P^T / dS^T are in place.
+            const int gg = g + i;
+            const uint32_t st_off = (gg % STAGES) * C::kQBytes;
+            if (!(ok = mbar_wait(BAR(C::BAR_PDSFULL), gg & 1, ab))) break;
+            // dK / dV of the previous item must be read out before they restart.
+            if (i == 0 && k >= 1 && !(ok = mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab))) break;
+            tc_fence_after();
+            const uint32_t pds = tmem + C::kTmemPDS;
+#pragma unroll
+            for (int kk = 0; kk < BMQ / 16; ++kk) {
+              // queries [16kk, 16kk+16): chunk kk/2, P^T first 16 columns, dS^T last 16
+              const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+              const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+              mma_ts(tmem + C::kTmemDV, pds + col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV, acc);
+              mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128), kIdKV,
+                     acc);
+            }
+            // The DQ columns still hold dQ of tile gg-1 until it has been read out.
+            if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_DQFREE), (gg - 1) & 1, ab))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ss(tmem + C::kTmemDQ, adv(dK_mn, kk * 16 * 128), adv(dDS_mn, kk * 16 * 128),
+                     kIdDQ, kk > 0 ? 1u : 0u);
+            mma_commit(BAR(C::BAR_MMA2));
+            mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
+          }
+          if (!ok) break;
+          mma_commit(BAR(C::BAR_ITEMDONE));
+          g += it.ntiles;
+          ++k;
+        }
       }
       mma_commit(BAR(C::BAR_ALL));
     }

@@ -61,7 +61,13 @@ struct Bwd2Cfg {
   static constexpr int kOffQ = kOffV + kKVBytes;
   static constexpr int kOffDO = kOffQ + STAGES * kQBytes;
   static constexpr int kOffDS = kOffDO + STAGES * kQBytes;
-  static constexpr int kOffLSE = kOffDS + kDSBytes;           // STAGES x BMQ floats
+  // dQ of half a query tile per warpgroup, float32 [BMQ / 2 queries][DH],
+  // the source of a bulk reduce-add into the accumulator (headdim 128; with
+  // 256 the shared memory is full and dQ goes out with per-thread atomics).
+  static constexpr bool kTmaDQ = D == 128;
+  static constexpr int kDQSBytes = (BMQ / 2) * DH * 4;
+  static constexpr int kOffDQS = kOffDS + kDSBytes;
+  static constexpr int kOffLSE = kOffDQS + (kTmaDQ ? 2 * kDQSBytes : 0);  // STAGES x BMQ floats
   static constexpr int kOffDEL = kOffLSE + STAGES * BMQ * 4;  // STAGES x BMQ floats
   static constexpr int kOffBar = kOffDEL + STAGES * BMQ * 4;
   enum {
@@ -76,7 +82,9 @@ struct Bwd2Cfg {
     BAR_ITEMDONE = BAR_DQFREE + 1,      // every MMA of an item done
     BAR_ACCFREE = BAR_ITEMDONE + 1,     // dK / dV of an item read out of TMEM
     BAR_ITEMFULL = BAR_ACCFREE + 1,     // [4] item index published
-    BAR_ALL = BAR_ITEMFULL + 4,         // every MMA of the CTA done
+    BAR_DQSFREE = BAR_ITEMFULL + 4,     // [2] a warpgroup's dQ staging tile free
+    BAR_DQSFULL = BAR_DQSFREE + 2,      // [2] ... and written by its 4 warps
+    BAR_ALL = BAR_DQSFULL + 2,          // every MMA of the CTA done
     NUM_BARS = BAR_ALL + 1
   };
   static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 item indices
@@ -153,12 +161,16 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
     mbar_init(BAR(C::BAR_SDPFULL), 1);
     mbar_init(BAR(C::BAR_SDPFREE), 8);
     mbar_init(BAR(C::BAR_PDSFULL), 8);
-    mbar_init(BAR(C::BAR_MMA2), 1);
+    mbar_init(BAR(C::BAR_MMA2), 2);      // warps 10 and 11
     mbar_init(BAR(C::BAR_DQFREE), 8);
-    mbar_init(BAR(C::BAR_ITEMDONE), 1);
+    mbar_init(BAR(C::BAR_ITEMDONE), 2);  // warps 10 and 11
     mbar_init(BAR(C::BAR_ACCFREE), 8);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
-    mbar_init(BAR(C::BAR_ALL), 2);  // one commit per issuing warp
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(BAR(C::BAR_DQSFREE + s), 1);
+      mbar_init(BAR(C::BAR_DQSFULL + s), 4);
+    }
+    mbar_init(BAR(C::BAR_ALL), 3);  // one commit per issuing warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -280,13 +292,14 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         mbar_wait_limited(BAR(C::BAR_QFULL + t % STAGES), (t / STAGES) & 1, 100000000ull);
     }
     __syncwarp();
-   } else if (warp == 9 || warp == 10) {
+   } else {
     // ------------------------------------------------------------ MMA issuers
-    // Two independent streams of products, each issued by its own warp so
+    // Three independent streams of products, each issued by its own warp so
     // that their issue overlaps: warp 9 issues S^T and dP^T of every tile,
-    // warp 10 the dV, dK and dQ^T products.  Everything one stream needs
-    // from the other is ordered through the compute warpgroups' barriers
-    // (S^T / dP^T complete -> P^T / dS^T written -> second products).
+    // warp 10 dV and dK, warp 11 dQ^T.  Everything one stream needs from
+    // another is ordered through the compute warpgroups' barriers (S^T / dP^T
+    // complete -> P^T / dS^T written -> second products); MMA2 and ITEMDONE
+    // count one commit from each of warps 10 and 11.
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(BN, BMQ, false, false);  // K Q^T, V dO^T
       constexpr uint32_t kIdKV = idesc_bf16(BN, DH, false, true);   // P^T dO, dS^T Q
@@ -333,6 +346,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
           ++k;
         }
       } else {
+        const bool kv = warp == 10;  // this warp issues dV / dK, else dQ^T
         const uint64_t dDS_mn = sdesc_sw128(sbase + C::kOffDS, BN * 128, 1024);
         while (ok) {
           if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
@@ -346,33 +360,41 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
               sdesc_sw128(sbase + C::kOffQ + it.dh * 2 * (BMQ * 128), BMQ * 128, 1024);
           const uint64_t dO_mn =
               sdesc_sw128(sbase + C::kOffDO + it.dh * 2 * (BMQ * 128), BMQ * 128, 1024);
+          // dK / dV of the previous item must be read out before they restart
+          // (waited for every item, so that ITEMDONE(k) always follows
+          // ACCFREE(k - 1)).
+          if (kv && k >= 1 && !(ok = mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab))) break;
           for (int i = 0; i < it.ntiles && ok; ++i) {
             // dV, dK, dQ of tile gg once its P^T / dS^T are in place.
             const int gg = g + i;
             const uint32_t st_off = (gg % STAGES) * C::kQBytes;
             if (!(ok = mbar_wait(BAR(C::BAR_PDSFULL), gg & 1, ab))) break;
-            // dK / dV of the previous item must be read out before they restart.
-            if (i == 0 && k >= 1 && !(ok = mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab))) break;
-            tc_fence_after();
-            const uint32_t pds = tmem + C::kTmemPDS;
+            if (kv) {
+              tc_fence_after();
+              const uint32_t pds = tmem + C::kTmemPDS;
 #pragma unroll
-            for (int kk = 0; kk < BMQ / 16; ++kk) {
-              // queries [16kk, 16kk+16): chunk kk/2, P^T first 16 columns, dS^T last 16
-              const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
-              const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-              mma_ts(tmem + C::kTmemDV, pds + col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV, acc);
-              mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128), kIdKV,
-                     acc);
+              for (int kk = 0; kk < BMQ / 16; ++kk) {
+                // queries [16kk, 16kk+16): chunk kk/2, P^T first 16 columns, dS^T last 16
+                const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                mma_ts(tmem + C::kTmemDV, pds + col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV,
+                       acc);
+                mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128),
+                       kIdKV, acc);
+              }
+              mma_commit(BAR(C::BAR_MMA2));
+              // dQ^T reads no Q / dO: the stage is free once dV / dK are done.
+              mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
+            } else {
+              // The DQ columns still hold dQ of tile gg-1 until it has been read out.
+              if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_DQFREE), (gg - 1) & 1, ab))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk)
+                mma_ss(tmem + C::kTmemDQ, adv(dK_mn, kk * 16 * 128), adv(dDS_mn, kk * 16 * 128),
+                       kIdDQ, kk > 0 ? 1u : 0u);
+              mma_commit(BAR(C::BAR_MMA2));
             }
-            // The DQ columns still hold dQ of tile gg-1 until it has been read out.
-            if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_DQFREE), (gg - 1) & 1, ab))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ss(tmem + C::kTmemDQ, adv(dK_mn, kk * 16 * 128), adv(dDS_mn, kk * 16 * 128),
-                     kIdDQ, kk > 0 ? 1u : 0u);
-            mma_commit(BAR(C::BAR_MMA2));
-            mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
           }
           if (!ok) break;
           mma_commit(BAR(C::BAR_ITEMDONE));
@@ -402,13 +424,43 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
     const size_t dq_stride = static_cast<size_t>(p.H) * D;
     // dQ^T of the tile whose products completed last: TMEM lane = head dim
     // `row`, columns = queries; added into the float32 accumulator.
-    auto drain_dq = [&](const Bwd2Item& it, int qh, int qs) {
+    int n_drain = 0;  // drains done by this warpgroup
+    auto drain_dq = [&](const Bwd2Item& it, int qh, int qs) -> bool {
       uint32_t dq[HC];
       tmem_ld32(t_lane + C::kTmemDQ + c0, dq);
       tmem_wait_ld();
       tmem_pin<HC>(dq);
       tc_fence_before();
       mbar_arrive_warp(BAR(C::BAR_DQFREE));
+      if constexpr (C::kTmaDQ) {
+        // Stage the warpgroup's 32 queries x 128 head dims (scaled) in shared
+        // memory and let the copy engine add them into the accumulator.  The
+        // warpgroup's lead thread frees the staging tile once its previous
+        // reduce has read it, and issues the next reduce once all 4 warps
+        // have written.  Phase t of both barriers belongs to the
+        // warpgroup's t-th drain.
+        const bool leader = (warp & 3) == 0 && lane == 0;
+        const uint32_t stg = sbase + C::kOffDQS + wg * C::kDQSBytes;
+        if (leader) {
+          bulk_wait_read_all();
+          mbar_arrive(BAR(C::BAR_DQSFREE + wg));
+        }
+        if (!mbar_wait_warp(BAR(C::BAR_DQSFREE + wg), n_drain & 1, ab)) return false;
+#pragma unroll
+        for (int c = 0; c < HC; ++c)
+          st_shared_f32(stg + c * (DH * 4) + row * 4, __uint_as_float(dq[c]) * p.scale);
+        fence_proxy_async_smem();
+        mbar_arrive_warp(BAR(C::BAR_DQSFULL + wg));
+        if (leader) {
+          if (!mbar_wait(BAR(C::BAR_DQSFULL + wg), n_drain & 1, ab)) return false;
+          if (qs + c0 < p.n) {
+            tma_reduce_add_5d(&p.tm_dq, stg, it.dh * DH, it.wi.h, qs + c0, qh, it.wi.b);
+            bulk_commit_group();
+          }
+        }
+        ++n_drain;
+        return true;
+      }
       float* ptr = p.dq_acc +
                    ((static_cast<size_t>(it.wi.b) * L + static_cast<size_t>(qh) * p.n + qs + c0) *
                         p.H + it.wi.h) * D + it.dh * DH + row;
@@ -426,6 +478,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
           ptr += dq_stride;
         }
       }
+      return true;
     };
     bool ok = true;
     int g = 0, k = 0;
@@ -517,7 +570,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         tc_fence_before();
         mbar_arrive_warp(BAR(C::BAR_PDSFULL));
         // The previous tile's products are complete (waited above): its dQ.
-        if (i >= 1) drain_dq(it, it.qhalf(i - 1), it.qtile(i - 1) * BMQ);
+        if (i >= 1 && !(ok = drain_dq(it, it.qhalf(i - 1), it.qtile(i - 1) * BMQ))) break;
       }
       if (!ok) break;
 
@@ -556,9 +609,15 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
           st_global_v4(dst + 8 * g8, w[0], w[1], w[2], w[3]);
         }
       }
-      if (it.ntiles > 0) drain_dq(it, it.qhalf(it.ntiles - 1), it.qtile(it.ntiles - 1) * BMQ);
+      if (it.ntiles > 0 &&
+          !(ok = drain_dq(it, it.qhalf(it.ntiles - 1), it.qtile(it.ntiles - 1) * BMQ)))
+        break;
       g += it.ntiles;
       ++k;
+    }
+    // The last bulk reduce-adds must be complete before the CTA exits.
+    if constexpr (C::kTmaDQ) {
+      if ((warp & 3) == 0 && lane == 0) bulk_wait_all();
     }
   }
 #undef BAR

@@ -34,6 +34,7 @@ struct BwdParams {
   CUtensorMap tm_do;  // box (64, 1, block_m, 1, 1)
   CUtensorMap tm_k;   // box (64, 1, block_n, 1, 1)
   CUtensorMap tm_v;   // box (64, 1, block_n, 1, 1)
+  CUtensorMap tm_dq;  // float32 dq_acc, box (128, 1, block_m / 2, 1, 1); headdim >= 128
   const float* lse;   // (B, H, 2n)
   const float* delta; // (B, H, 2n): rowsum(dout * out)
   float* dq_acc;      // (B, 2n, H, d) fp32, zeroed before the kernel

@@ -131,16 +131,16 @@ int make_map(CUtensorMap* map, const void* base, int B, int n, int H, int d, int
 }
 
 // The float32 dQ accumulator (B, 2n, H, d) as 5-D (d, H, n, half, B) with
-// boxes of (128, 1, rows, 1, 1), no swizzle: the target of the backward's
-// bulk reduce-add of a query tile's dQ (rows past the end of a half are
-// skipped by the copy engine).
+// boxes of (32, 1, rows, 1, 1), no swizzle: the target of the backward's
+// bulk reduce-add of one warp's part of a query tile's dQ (rows past the
+// end of a half are skipped by the copy engine).
 int make_map_f32(CUtensorMap* map, const void* base, int B, int n, int H, int d, int rows) {
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(n), 2, static_cast<cuuint64_t>(B)};
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(H) * d * 4;
   const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * 4, row_bytes, row_bytes * n,
                                  row_bytes * 2 * n};
-  const cuuint32_t box[5] = {128, 1, static_cast<cuuint32_t>(rows), 1, 1};
+  const cuuint32_t box[5] = {32, 1, static_cast<cuuint32_t>(rows), 1, 1};
   const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -219,7 +219,9 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   if ((rc = make_map(&p.tm_do, dout, B, n, H, d, ts.bwd_bm))) return rc;
   if ((rc = make_map(&p.tm_k, k, B, n, H, d, ts.bwd_bn))) return rc;
   if ((rc = make_map(&p.tm_v, v, B, n, H, d, ts.bwd_bn))) return rc;
-  if (d >= 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, B, n, H, d, ts.bwd_bm / 2))) return rc;
+  if (d == 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, B, n, H, d,
+                                      ts.bwd_bm / kBwd2WarpgroupsD128)))
+    return rc;
   p.lse = lse;
   p.delta = delta;
   p.dq_acc = dq_acc;

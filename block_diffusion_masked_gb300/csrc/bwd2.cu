@@ -44,13 +44,29 @@
 
 namespace dfa {
 
-template <int D_, int STAGES_>
+template <int D_, int STAGES_, int NWG_>
 struct Bwd2Cfg {
   static constexpr int D = D_;
+  static constexpr int NWG = NWG_;             // compute warpgroups
+  static constexpr int kComputeWarps = 4 * NWG;
+  static constexpr int kWarpLoad = kComputeWarps;      // TMA producer
+  static constexpr int kWarpS = kComputeWarps + 1;     // S^T / dP^T issuer, owns TMEM
+  static constexpr int kWarpKV = kComputeWarps + 2;    // dV / dK issuer
+  static constexpr int kWarpDQ = kComputeWarps + 3;    // dQ^T issuer
+  static constexpr int kThreads = 32 * (kComputeWarps + 4);
+  // setmaxnreg split: the launch gives every thread kRegLaunch registers;
+  // the 4 control warps drop to kRegCtl, the compute warps rise to
+  // kRegCompute, within the launch's pool.
+  static constexpr int kRegLaunch = NWG == 2 ? 168 : 96;
+  static constexpr int kRegCtl = NWG == 2 ? 136 : 64;
+  static constexpr int kRegCompute = NWG == 2 ? 184 : 104;
+  static_assert(kRegCtl * 128 + kRegCompute * 128 * NWG <= kRegLaunch * kThreads,
+                "register split exceeds the launch pool");
   static constexpr int DH = 128;       // head dims accumulated per item
   static constexpr int NDH = D / DH;   // items per key tile
   static constexpr int BN = 128;  // keys per tile (MMA M)
   static constexpr int BMQ = 64;  // queries per tile
+  static constexpr int HC = BMQ / NWG;  // query columns per compute warpgroup
   static constexpr int STAGES = STAGES_;
   static constexpr int kChunks = D / 64;
   static constexpr int kKVBytes = BN * D * 2;
@@ -61,13 +77,14 @@ struct Bwd2Cfg {
   static constexpr int kOffQ = kOffV + kKVBytes;
   static constexpr int kOffDO = kOffQ + STAGES * kQBytes;
   static constexpr int kOffDS = kOffDO + STAGES * kQBytes;
-  // dQ of half a query tile per warpgroup, float32 [BMQ / 2 queries][DH],
-  // the source of a bulk reduce-add into the accumulator (headdim 128; with
-  // 256 the shared memory is full and dQ goes out with per-thread atomics).
+  // dQ staging, one tile per compute warp: float32 [HC queries][32 head
+  // dims], the source of that warp's bulk reduce-add into the accumulator
+  // (headdim 128; with 256 the shared memory is full and dQ goes out with
+  // per-thread atomics).
   static constexpr bool kTmaDQ = D == 128;
-  static constexpr int kDQSBytes = (BMQ / 2) * DH * 4;
+  static constexpr int kDQSBytes = HC * 32 * 4;
   static constexpr int kOffDQS = kOffDS + kDSBytes;
-  static constexpr int kOffLSE = kOffDQS + (kTmaDQ ? 2 * kDQSBytes : 0);  // STAGES x BMQ floats
+  static constexpr int kOffLSE = kOffDQS + (kTmaDQ ? kComputeWarps * kDQSBytes : 0);  // STAGES x BMQ floats
   static constexpr int kOffDEL = kOffLSE + STAGES * BMQ * 4;  // STAGES x BMQ floats
   static constexpr int kOffBar = kOffDEL + STAGES * BMQ * 4;
   enum {
@@ -82,9 +99,7 @@ struct Bwd2Cfg {
     BAR_ITEMDONE = BAR_DQFREE + 1,      // every MMA of an item done
     BAR_ACCFREE = BAR_ITEMDONE + 1,     // dK / dV of an item read out of TMEM
     BAR_ITEMFULL = BAR_ACCFREE + 1,     // [4] item index published
-    BAR_DQSFREE = BAR_ITEMFULL + 4,     // [2] a warpgroup's dQ staging tile free
-    BAR_DQSFULL = BAR_DQSFREE + 2,      // [2] ... and written by its 4 warps
-    BAR_ALL = BAR_DQSFULL + 2,          // every MMA of the CTA done
+    BAR_ALL = BAR_ITEMFULL + 4,         // every MMA of the CTA done
     NUM_BARS = BAR_ALL + 1
   };
   static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 item indices
@@ -98,7 +113,6 @@ struct Bwd2Cfg {
   static constexpr int kTmemDK = 256;
   static constexpr int kTmemDV = 384;
   static constexpr int kTmemCols = 512;
-  static constexpr int kThreads = 384;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -132,9 +146,10 @@ __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   return it;
 }
 
-template <int D_, int STAGES_>
-__global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant__ BwdParams p) {
-  using C = Bwd2Cfg<D_, STAGES_>;
+template <int D_, int STAGES_, int NWG_>
+__global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
+    dfa_bwd2_kernel(const __grid_constant__ BwdParams p) {
+  using C = Bwd2Cfg<D_, STAGES_, NWG_>;
   constexpr int DH = C::DH;
   constexpr int D = C::D;
   constexpr int BN = C::BN;
@@ -159,22 +174,18 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
       mbar_init(BAR(C::BAR_QEMPTY + s), 1);
     }
     mbar_init(BAR(C::BAR_SDPFULL), 1);
-    mbar_init(BAR(C::BAR_SDPFREE), 8);
-    mbar_init(BAR(C::BAR_PDSFULL), 8);
+    mbar_init(BAR(C::BAR_SDPFREE), C::kComputeWarps);
+    mbar_init(BAR(C::BAR_PDSFULL), C::kComputeWarps);
     mbar_init(BAR(C::BAR_MMA2), 2);      // warps 10 and 11
-    mbar_init(BAR(C::BAR_DQFREE), 8);
+    mbar_init(BAR(C::BAR_DQFREE), C::kComputeWarps);
     mbar_init(BAR(C::BAR_ITEMDONE), 2);  // warps 10 and 11
-    mbar_init(BAR(C::BAR_ACCFREE), 8);
+    mbar_init(BAR(C::BAR_ACCFREE), C::kComputeWarps);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(BAR(C::BAR_DQSFREE + s), 1);
-      mbar_init(BAR(C::BAR_DQSFULL + s), 4);
-    }
     mbar_init(BAR(C::BAR_ALL), 3);  // one commit per issuing warp
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == C::kWarpS) {
     tmem_alloc(sbase + C::kOffTmemSlot, C::kTmemCols);
     tmem_relinquish();
   }
@@ -190,9 +201,9 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
   // done, and an item is done only after both compute warpgroups have read
   // the dK / dV of the item before it, so a slot is never overwritten
   // before every reader has taken its index.
-  if (warp >= 8) {
-   asm volatile("setmaxnreg.dec.sync.aligned.u32 136;");
-   if (warp == 8) {
+  if (warp >= C::kComputeWarps) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegCtl));
+   if (warp == C::kWarpLoad) {
     // ------------------------------------------------------------ loads
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
@@ -307,7 +318,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
       auto adv = [](uint64_t d, uint32_t bytes) { return d + static_cast<uint64_t>(bytes >> 4); };
       bool ok = true;
       int g = 0, k = 0;
-      if (warp == 9) {
+      if (warp == C::kWarpS) {
         const uint64_t dK_kmaj = sdesc_sw128(sbase + C::kOffK, 16, 1024);
         const uint64_t dV_kmaj = sdesc_sw128(sbase + C::kOffV, 16, 1024);
         const uint64_t dQ_kmaj = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
@@ -346,7 +357,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
           ++k;
         }
       } else {
-        const bool kv = warp == 10;  // this warp issues dV / dK, else dQ^T
+        const bool kv = warp == C::kWarpKV;  // this warp issues dV / dK, else dQ^T
         const uint64_t dDS_mn = sdesc_sw128(sbase + C::kOffDS, BN * 128, 1024);
         while (ok) {
           if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
@@ -407,14 +418,14 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
     __syncwarp();
    }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegCompute));
     // ------------------------------------------------------------ compute
     // Both warpgroups work on every query tile: warpgroup wg takes query
     // columns [32 wg, 32 wg + 32) of S^T, dP^T, P^T / dS^T and dQ^T.  The dQ
     // of a tile is read out of TMEM in the next tile's turn, after that
     // tile's P^T / dS^T are handed over, so no warpgroup waits for the dV,
     // dK, dQ products of the tile it has just finished.
-    constexpr int HC = BMQ / 2;              // query columns per warpgroup
+    constexpr int HC = C::HC;                // query columns per warpgroup
     const int wg = warp >> 2;
     const int c0 = wg * HC;                  // first column of this warpgroup
     const int row = (warp & 3) * 32 + lane;  // key row of the tile / TMEM lane
@@ -424,41 +435,31 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
     const size_t dq_stride = static_cast<size_t>(p.H) * D;
     // dQ^T of the tile whose products completed last: TMEM lane = head dim
     // `row`, columns = queries; added into the float32 accumulator.
-    int n_drain = 0;  // drains done by this warpgroup
     auto drain_dq = [&](const Bwd2Item& it, int qh, int qs) -> bool {
       uint32_t dq[HC];
-      tmem_ld32(t_lane + C::kTmemDQ + c0, dq);
+      tmem_ld_cols<HC>(t_lane + C::kTmemDQ + c0, dq);
       tmem_wait_ld();
       tmem_pin<HC>(dq);
       tc_fence_before();
       mbar_arrive_warp(BAR(C::BAR_DQFREE));
       if constexpr (C::kTmaDQ) {
-        // Stage the warpgroup's 32 queries x 128 head dims (scaled) in shared
-        // memory and let the copy engine add them into the accumulator.  The
-        // warpgroup's lead thread frees the staging tile once its previous
-        // reduce has read it, and issues the next reduce once all 4 warps
-        // have written.  Phase t of both barriers belongs to the
-        // warpgroup's t-th drain.
-        const bool leader = (warp & 3) == 0 && lane == 0;
-        const uint32_t stg = sbase + C::kOffDQS + wg * C::kDQSBytes;
-        if (leader) {
-          bulk_wait_read_all();
-          mbar_arrive(BAR(C::BAR_DQSFREE + wg));
-        }
-        if (!mbar_wait_warp(BAR(C::BAR_DQSFREE + wg), n_drain & 1, ab)) return false;
+        // Stage the warp's HC queries x 32 head dims (scaled) in its own
+        // shared tile and let the copy engine add them into the accumulator.
+        // Lane 0 issues the reduce; before the warp rewrites the tile it
+        // waits until lane 0's previous reduce has read it.
+        const uint32_t stg = sbase + C::kOffDQS + warp * C::kDQSBytes;
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll
         for (int c = 0; c < HC; ++c)
-          st_shared_f32(stg + c * (DH * 4) + row * 4, __uint_as_float(dq[c]) * p.scale);
+          st_shared_f32(stg + c * 128 + lane * 4, __uint_as_float(dq[c]) * p.scale);
         fence_proxy_async_smem();
-        mbar_arrive_warp(BAR(C::BAR_DQSFULL + wg));
-        if (leader) {
-          if (!mbar_wait(BAR(C::BAR_DQSFULL + wg), n_drain & 1, ab)) return false;
-          if (qs + c0 < p.n) {
-            tma_reduce_add_5d(&p.tm_dq, stg, it.dh * DH, it.wi.h, qs + c0, qh, it.wi.b);
-            bulk_commit_group();
-          }
+        __syncwarp();
+        if (lane == 0 && qs + c0 < p.n) {
+          tma_reduce_add_5d(&p.tm_dq, stg, it.dh * DH + 32 * (warp & 3), it.wi.h, qs + c0, qh,
+                            it.wi.b);
+          bulk_commit_group();
         }
-        ++n_drain;
         return true;
       }
       float* ptr = p.dq_acc +
@@ -502,8 +503,8 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         if (!(ok = mbar_wait_warp(BAR(C::BAR_SDPFULL), gg & 1, ab))) break;
         tc_fence_after();
         uint32_t sr[HC], dpr[HC];
-        tmem_ld32(t_lane + C::kTmemS + c0, sr);
-        tmem_ld32(t_lane + C::kTmemDP + c0, dpr);
+        tmem_ld_cols<HC>(t_lane + C::kTmemS + c0, sr);
+        tmem_ld_cols<HC>(t_lane + C::kTmemDP + c0, dpr);
         tmem_wait_ld();
         tmem_pin<HC>(sr);
         tmem_pin<HC>(dpr);
@@ -554,13 +555,16 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
         // products until they complete.
         if (gg >= 1 && !(ok = mbar_wait_warp(BAR(C::BAR_MMA2), (gg - 1) & 1, ab))) break;
         tc_fence_after();
-        // PdS chunk wg: P^T in its first 16 columns, dS^T in the last 16.
-        tmem_st16(t_lane + C::kTmemPDS + 32 * wg, wp);
-        tmem_st16(t_lane + C::kTmemPDS + 32 * wg + 16, wd);
-        // dS^T row `row` of the shared tile: 16-byte units 4 wg .. 4 wg + 3.
+        // PdS chunk c0 / 32 holds P^T of its 32 queries in its first 16
+        // columns and dS^T in the last 16; this warpgroup's HC / 2 words of
+        // each start at word (c0 % 32) / 2.
+        const uint32_t pds_col = C::kTmemPDS + 32 * (c0 / 32) + (c0 % 32) / 2;
+        tmem_st_cols<HC / 2>(t_lane + pds_col, wp);
+        tmem_st_cols<HC / 2>(t_lane + pds_col + 16, wd);
+        // dS^T row `row` of the shared tile: 16-byte units c0 / 8 onwards.
 #pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
-          const int u = 4 * wg + u4;
+        for (int u4 = 0; u4 < HC / 8; ++u4) {
+          const int u = c0 / 8 + u4;
           const uint32_t off = row * 128 + ((u ^ (row & 7)) << 4);
           st_shared_v4(sbase + C::kOffDS + off, wd[4 * u4], wd[4 * u4 + 1], wd[4 * u4 + 2],
                        wd[4 * u4 + 3]);
@@ -575,32 +579,37 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
       if (!ok) break;
 
       // -------------------------------------------------------- item epilogue
-      // Warpgroup 0 writes dV, warpgroup 1 writes dK, once the item's MMAs are
-      // done; TMEM is released as soon as both have read their accumulator.
-      // Then the dQ of the item's last tile.
+      // The first half of the warpgroups writes dV, the second dK, each
+      // warpgroup DW head dims of it, once the item's MMAs are done; TMEM is
+      // released as soon as all have read their part.  Then the dQ of the
+      // item's last tile.
       if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMDONE), k & 1, ab))) break;
       tc_fence_after();
-      const uint32_t col = wg == 0 ? C::kTmemDV : C::kTmemDK;
-      uint32_t o[DH];
+      constexpr int PER = C::NWG / 2;  // warpgroups per accumulator
+      constexpr int DW = DH / PER;     // head dims per warpgroup
+      const bool is_v = wg < PER;
+      const int d0 = (wg % PER) * DW;
+      const uint32_t col = (is_v ? C::kTmemDV : C::kTmemDK) + d0;
+      uint32_t o[DW];
       if (it.ntiles > 0) {
 #pragma unroll
-        for (int c = 0; c < DH / 32; ++c) tmem_ld32(t_lane + col + 32 * c, o + 32 * c);
+        for (int c = 0; c < DW / 32; ++c) tmem_ld32(t_lane + col + 32 * c, o + 32 * c);
         tmem_wait_ld();
-        tmem_pin<DH>(o);
+        tmem_pin<DW>(o);
       } else {
 #pragma unroll
-        for (int e = 0; e < DH; ++e) o[e] = 0u;
+        for (int e = 0; e < DW; ++e) o[e] = 0u;
       }
       tc_fence_before();
       mbar_arrive_warp(BAR(C::BAR_ACCFREE));
       if (j < p.n) {
         const size_t pos = static_cast<size_t>(it.wi.half) * p.n + j;
         const size_t off =
-            ((static_cast<size_t>(it.wi.b) * L + pos) * p.H + it.wi.h) * D + it.dh * DH;
-        __nv_bfloat16* dst = (wg == 0 ? p.dv : p.dk) + off;
-        const float mul = wg == 0 ? 1.f : p.scale;
+            ((static_cast<size_t>(it.wi.b) * L + pos) * p.H + it.wi.h) * D + it.dh * DH + d0;
+        __nv_bfloat16* dst = (is_v ? p.dv : p.dk) + off;
+        const float mul = is_v ? 1.f : p.scale;
 #pragma unroll
-        for (int g8 = 0; g8 < DH / 8; ++g8) {
+        for (int g8 = 0; g8 < DW / 8; ++g8) {
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
@@ -617,14 +626,14 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
     }
     // The last bulk reduce-adds must be complete before the CTA exits.
     if constexpr (C::kTmaDQ) {
-      if ((warp & 3) == 0 && lane == 0) bulk_wait_all();
+      if (lane == 0) bulk_wait_all();
     }
   }
 #undef BAR
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::kWarpS) {
     if (lane == 0) mbar_wait_limited(sbase + C::kOffBar + 8 * C::BAR_ALL, 0, 1000000000ull);
     __syncwarp();
     tc_fence_after();
@@ -633,13 +642,19 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd2_kernel(const __grid_constant_
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int STAGES>
+template <int D, int STAGES, int NWG>
 static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
-  using C = Bwd2Cfg<D, STAGES>;
-  auto kern = dfa_bwd2_kernel<D, STAGES>;
+  using C = Bwd2Cfg<D, STAGES, NWG>;
+  auto kern = dfa_bwd2_kernel<D, STAGES, NWG>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  // The setmaxnreg split must fit the registers the kernel is launched with,
+  // or the compute warps' increase would never be granted: refuse to launch.
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+  if (fa.numRegs * C::kThreads < C::kRegCtl * 128 + C::kRegCompute * 128 * C::NWG)
+    return cudaErrorInvalidConfiguration;
   const long long items = 2LL * p.B * p.H * p.k_tiles * C::NDH;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -655,11 +670,11 @@ static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_backward_d128(const BwdParams& p, cudaStream_t stream) {
-  return launch_bwd2_impl<128, 3>(p, stream);
+  return launch_bwd2_impl<128, 3, kBwd2WarpgroupsD128>(p, stream);
 }
 
 cudaError_t launch_backward_d256(const BwdParams& p, cudaStream_t stream) {
-  return launch_bwd2_impl<256, 1>(p, stream);
+  return launch_bwd2_impl<256, 1, 2>(p, stream);
 }
 
 }  // namespace dfa

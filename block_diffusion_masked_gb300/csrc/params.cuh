@@ -34,7 +34,7 @@ struct BwdParams {
   CUtensorMap tm_do;  // box (64, 1, block_m, 1, 1)
   CUtensorMap tm_k;   // box (64, 1, block_n, 1, 1)
   CUtensorMap tm_v;   // box (64, 1, block_n, 1, 1)
-  CUtensorMap tm_dq;  // float32 dq_acc, box (128, 1, block_m / 2, 1, 1); headdim >= 128
+  CUtensorMap tm_dq;  // float32 dq_acc, box (32, 1, query columns per warpgroup, 1, 1); headdim 128
   const float* lse;   // (B, H, 2n)
   const float* delta; // (B, H, 2n): rowsum(dout * out)
   float* dq_acc;      // (B, 2n, H, d) fp32, zeroed before the kernel
@@ -82,6 +82,10 @@ cudaError_t launch_selftest_wait(unsigned* status, unsigned long long limit_ns,
                                  cudaStream_t stream);
 cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, long long count,
                               cudaStream_t stream);
+
+// Compute warpgroups of the headdim-128 backward kernel; each takes
+// 64 / this query columns of a tile and stages that many rows of dQ.
+constexpr int kBwd2WarpgroupsD128 = 2;
 
 // Tile shapes per head dimension.
 struct TileShape {

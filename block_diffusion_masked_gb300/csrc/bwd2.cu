@@ -25,17 +25,21 @@
 // Persistent: one CTA per SM takes items from a work counter until none are
 // left, so the load of the next item's K and V and of its first query tiles
 // overlaps the end of the current item, and short items fill the SMs that
-// finish early.  Both compute warpgroups work on every query tile, each on
-// half of its query columns; a tile's dQ is read out of TMEM during the next
+// finish early.  The compute warpgroups all work on every query tile, each
+// on its own query columns; a tile's dQ is read out of TMEM during the next
 // tile's turn, once that tile's P^T / dS^T are handed over, so no warpgroup
 // waits for the products of the tile it has just finished.  S and dP are
 // released as soon as they are in registers, so the scores of the next tile
-// are computed while the warpgroups work.  At the end of an item warpgroup 0
-// writes dV and warpgroup 1 writes dK; the next item's first dV / dK
-// products wait until both have been read out of TMEM.
-// Warps 0-7 compute, warp 8 loads, warp 9 issues MMAs, warps 10-11 idle; the
-// load/MMA warpgroup drops to 136 registers and the compute warpgroups rise
-// to 184 (setmaxnreg; launched with 168: 256 * 16 == 128 * 32).
+// are computed while the warpgroups work.  At the end of an item the first
+// half of the warpgroups writes dV and the second half dK; the next item's
+// first dV / dK products wait until all have been read out of TMEM.
+// With headdim 128 each warp adds its part of dQ into the float32
+// accumulator with a bulk tensor reduce from a shared staging tile; with 256
+// (no shared memory left) each thread adds its own with atomics.
+// Warps: 4 per compute warpgroup, then one TMA producer and three MMA
+// issuers (S^T / dP^T; dV / dK; dQ^T), whose streams are independent and so
+// are issued in parallel.  The control warps drop registers to the compute
+// warpgroups (setmaxnreg) within the pool the launch provides.
 #include <cuda_bf16.h>
 
 #include "geometry.cuh"
@@ -44,9 +48,13 @@
 
 namespace dfa {
 
-template <int D_, int STAGES_, int NWG_>
+template <int D_, int STAGES_, int NWG_, int KVBUF_>
 struct Bwd2Cfg {
   static constexpr int D = D_;
+  // K / V buffers: with two, the next item's K and V load while the current
+  // item runs, and its first products need not wait for the current item's
+  // last ones.
+  static constexpr int KVBUF = KVBUF_;
   static constexpr int NWG = NWG_;             // compute warpgroups
   static constexpr int kComputeWarps = 4 * NWG;
   static constexpr int kWarpLoad = kComputeWarps;      // TMA producer
@@ -72,32 +80,32 @@ struct Bwd2Cfg {
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int kQBytes = BMQ * D * 2;
   static constexpr int kDSBytes = BN * BMQ * 2;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kOffK + kKVBytes;
-  static constexpr int kOffQ = kOffV + kKVBytes;
+  static constexpr int kOffK = 0;                          // [KVBUF]
+  static constexpr int kOffV = kOffK + KVBUF * kKVBytes;   // [KVBUF]
+  static constexpr int kOffQ = kOffV + KVBUF * kKVBytes;
   static constexpr int kOffDO = kOffQ + STAGES * kQBytes;
   static constexpr int kOffDS = kOffDO + STAGES * kQBytes;
   // dQ staging, one tile per compute warp: float32 [HC queries][32 head
   // dims], the source of that warp's bulk reduce-add into the accumulator
   // (headdim 128; with 256 the shared memory is full and dQ goes out with
   // per-thread atomics).
-  static constexpr bool kTmaDQ = D == 128;
+  static constexpr bool kTmaDQ = D == 128 && KVBUF == 1;
   static constexpr int kDQSBytes = HC * 32 * 4;
   static constexpr int kOffDQS = kOffDS + kDSBytes;
   static constexpr int kOffLSE = kOffDQS + (kTmaDQ ? kComputeWarps * kDQSBytes : 0);  // STAGES x BMQ floats
   static constexpr int kOffDEL = kOffLSE + STAGES * BMQ * 4;  // STAGES x BMQ floats
   static constexpr int kOffBar = kOffDEL + STAGES * BMQ * 4;
   enum {
-    BAR_KVFULL = 0,  // K and V of an item loaded
-    BAR_QFULL = 1,
+    BAR_KVFULL = 0,  // [KVBUF] K and V of an item loaded
+    BAR_QFULL = KVBUF,
     BAR_QEMPTY = BAR_QFULL + STAGES,
     BAR_SDPFULL = BAR_QEMPTY + STAGES,  // S^T and dP^T of a tile computed
     BAR_SDPFREE = BAR_SDPFULL + 1,      // S^T / dP^T read into registers
     BAR_PDSFULL = BAR_SDPFREE + 1,      // P^T / dS^T of a tile in place
     BAR_MMA2 = BAR_PDSFULL + 1,         // dV, dK, dQ of a tile done
     BAR_DQFREE = BAR_MMA2 + 1,          // dQ of a tile read out of TMEM
-    BAR_ITEMDONE = BAR_DQFREE + 1,      // every MMA of an item done
-    BAR_ACCFREE = BAR_ITEMDONE + 1,     // dK / dV of an item read out of TMEM
+    BAR_ITEMDONE = BAR_DQFREE + 1,      // [KVBUF] every MMA of an item done
+    BAR_ACCFREE = BAR_ITEMDONE + KVBUF, // dK / dV of an item read out of TMEM
     BAR_ITEMFULL = BAR_ACCFREE + 1,     // [4] item index published
     BAR_ALL = BAR_ITEMFULL + 4,         // every MMA of the CTA done
     NUM_BARS = BAR_ALL + 1
@@ -146,10 +154,10 @@ __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   return it;
 }
 
-template <int D_, int STAGES_, int NWG_>
-__global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
+template <int D_, int STAGES_, int NWG_, int KVBUF_>
+__global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 1)
     dfa_bwd2_kernel(const __grid_constant__ BwdParams p) {
-  using C = Bwd2Cfg<D_, STAGES_, NWG_>;
+  using C = Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>;
   constexpr int DH = C::DH;
   constexpr int D = C::D;
   constexpr int BN = C::BN;
@@ -168,7 +176,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
 
   if (threadIdx.x == 0) {
-    mbar_init(BAR(C::BAR_KVFULL), 1);
+    for (int s = 0; s < C::KVBUF; ++s) {
+      mbar_init(BAR(C::BAR_KVFULL + s), 1);
+      mbar_init(BAR(C::BAR_ITEMDONE + s), 2);  // warps issuing dV / dK and dQ
+    }
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(BAR(C::BAR_QFULL + s), 1);
       mbar_init(BAR(C::BAR_QEMPTY + s), 1);
@@ -178,7 +189,6 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
     mbar_init(BAR(C::BAR_PDSFULL), C::kComputeWarps);
     mbar_init(BAR(C::BAR_MMA2), 2);      // warps 10 and 11
     mbar_init(BAR(C::BAR_DQFREE), C::kComputeWarps);
-    mbar_init(BAR(C::BAR_ITEMDONE), 2);  // warps 10 and 11
     mbar_init(BAR(C::BAR_ACCFREE), C::kComputeWarps);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
     mbar_init(BAR(C::BAR_ALL), 3);  // one commit per issuing warp
@@ -197,10 +207,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
   // Items are numbered k = 0, 1, ... in the order this CTA takes them, query
   // tiles g = 0, 1, ... over all of the CTA's items; every barrier phase
   // below is counted in one of the two.  The item ring holds the index of
-  // item k in slot k % 4: the loader writes slot k only after item k - 2 is
-  // done, and an item is done only after both compute warpgroups have read
-  // the dK / dV of the item before it, so a slot is never overwritten
-  // before every reader has taken its index.
+  // item k in slot k % 4: the loader writes slot k only after item
+  // k - 1 - KVBUF is done, and an item is done only after every compute
+  // warpgroup has read the dK / dV of the item before it, so a slot is never
+  // overwritten before every reader has taken its index.
   if (warp >= C::kComputeWarps) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegCtl));
    if (warp == C::kWarpLoad) {
@@ -268,25 +278,29 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
       v = __shfl_sync(0xffffffffu, v, 0);
       if (v < 0) break;
       const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
-      // The first query tiles only need stages that the current item frees
+      // K / V buffer `kvs` was last used by item k - KVBUF.  With one buffer
+      // the first query tiles only need stages that the current item frees
       // before its last product, so they go ahead of the K / V load, which
-      // waits for the whole item.
-      const int pre = imin(it.ntiles, STAGES - 1);
+      // waits for the whole item; with two the K / V load goes first.
+      const int kvs = k % C::KVBUF;
+      const int pre = C::KVBUF == 1 ? imin(it.ntiles, STAGES - 1) : 0;
       for (int t = 0; t < pre && ok; ++t) ok = load_q(it, t, g + t);
       if (!ok) break;
-      if (k > 0) {
+      if (k >= C::KVBUF) {
         int w = 0;
-        if (lane == 0) w = mbar_wait(BAR(C::BAR_ITEMDONE), (k - 1) & 1, ab) ? 1 : 0;
+        if (lane == 0)
+          w = mbar_wait(BAR(C::BAR_ITEMDONE + kvs), (k / C::KVBUF - 1) & 1, ab) ? 1 : 0;
         if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
       }
       if (lane == 0) {
         const int ks = it.wi.tile * BN;
-        mbar_arrive_expect_tx(BAR(C::BAR_KVFULL), 2 * C::kKVBytes);
+        const uint32_t full = BAR(C::BAR_KVFULL + kvs);
+        mbar_arrive_expect_tx(full, 2 * C::kKVBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_5d(sbase + C::kOffK + c * BN * 128, &p.tm_k, BAR(C::BAR_KVFULL), 64 * c,
+          tma_load_5d(sbase + C::kOffK + kvs * C::kKVBytes + c * BN * 128, &p.tm_k, full, 64 * c,
                       it.wi.h, ks, it.wi.half, it.wi.b);
-          tma_load_5d(sbase + C::kOffV + c * BN * 128, &p.tm_v, BAR(C::BAR_KVFULL), 64 * c,
+          tma_load_5d(sbase + C::kOffV + kvs * C::kKVBytes + c * BN * 128, &p.tm_v, full, 64 * c,
                       it.wi.h, ks, it.wi.half, it.wi.b);
         }
       }
@@ -298,7 +312,9 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
     }
     // Unwinding after a failed wait: let the copies in flight land.
     if (!ok && lane == 0) {
-      if (kv_issued > 0) mbar_wait_limited(BAR(C::BAR_KVFULL), (kv_issued - 1) & 1, 100000000ull);
+      if (kv_issued > 0)
+        mbar_wait_limited(BAR(C::BAR_KVFULL + (kv_issued - 1) % C::KVBUF),
+                          ((kv_issued - 1) / C::KVBUF) & 1, 100000000ull);
       for (int t = (q_issued > STAGES ? q_issued - STAGES : 0); t < q_issued; ++t)
         mbar_wait_limited(BAR(C::BAR_QFULL + t % STAGES), (t / STAGES) & 1, 100000000ull);
     }
@@ -319,8 +335,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
       bool ok = true;
       int g = 0, k = 0;
       if (warp == C::kWarpS) {
-        const uint64_t dK_kmaj = sdesc_sw128(sbase + C::kOffK, 16, 1024);
-        const uint64_t dV_kmaj = sdesc_sw128(sbase + C::kOffV, 16, 1024);
+        const uint64_t dK_kmaj0 = sdesc_sw128(sbase + C::kOffK, 16, 1024);
+        const uint64_t dV_kmaj0 = sdesc_sw128(sbase + C::kOffV, 16, 1024);
         const uint64_t dQ_kmaj = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
         const uint64_t dO_kmaj = sdesc_sw128(sbase + C::kOffDO, 16, 1024);
         while (ok) {
@@ -328,7 +344,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
           const int v = item_ring[k & 3];
           if (v < 0) break;
           const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
-          if (!(ok = mbar_wait(BAR(C::BAR_KVFULL), k & 1, ab))) break;
+          const int kvs = k % C::KVBUF;
+          const uint64_t dK_kmaj = adv(dK_kmaj0, kvs * C::kKVBytes);
+          const uint64_t dV_kmaj = adv(dV_kmaj0, kvs * C::kKVBytes);
+          if (!(ok = mbar_wait(BAR(C::BAR_KVFULL + kvs), (k / C::KVBUF) & 1, ab))) break;
           for (int i = 0; i < it.ntiles && ok; ++i) {
             const int gg = g + i;
             const int st = gg % STAGES;
@@ -366,7 +385,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
           const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
           // The head-dim half dh starts at 64-wide chunk 2 dh of K, Q and dO.
           const uint64_t dK_mn =
-              sdesc_sw128(sbase + C::kOffK + it.dh * 2 * (BN * 128), BN * 128, 1024);
+              sdesc_sw128(sbase + C::kOffK + (k % C::KVBUF) * C::kKVBytes + it.dh * 2 * (BN * 128),
+                          BN * 128, 1024);
           const uint64_t dQ_mn =
               sdesc_sw128(sbase + C::kOffQ + it.dh * 2 * (BMQ * 128), BMQ * 128, 1024);
           const uint64_t dO_mn =
@@ -408,7 +428,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
             }
           }
           if (!ok) break;
-          mma_commit(BAR(C::BAR_ITEMDONE));
+          mma_commit(BAR(C::BAR_ITEMDONE + k % C::KVBUF));
           g += it.ntiles;
           ++k;
         }
@@ -583,7 +603,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
       // warpgroup DW head dims of it, once the item's MMAs are done; TMEM is
       // released as soon as all have read their part.  Then the dQ of the
       // item's last tile.
-      if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMDONE), k & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMDONE + k % C::KVBUF), (k / C::KVBUF) & 1, ab)))
+        break;
       tc_fence_after();
       constexpr int PER = C::NWG / 2;  // warpgroups per accumulator
       constexpr int DW = DH / PER;     // head dims per warpgroup
@@ -642,10 +663,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_>::kThreads, 1)
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int STAGES, int NWG>
+template <int D, int STAGES, int NWG, int KVBUF>
 static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
-  using C = Bwd2Cfg<D, STAGES, NWG>;
-  auto kern = dfa_bwd2_kernel<D, STAGES, NWG>;
+  using C = Bwd2Cfg<D, STAGES, NWG, KVBUF>;
+  auto kern = dfa_bwd2_kernel<D, STAGES, NWG, KVBUF>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -670,11 +691,11 @@ static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_backward_d128(const BwdParams& p, cudaStream_t stream) {
-  return launch_bwd2_impl<128, 3, kBwd2WarpgroupsD128>(p, stream);
+  return launch_bwd2_impl<128, 3, kBwd2WarpgroupsD128, 1>(p, stream);
 }
 
 cudaError_t launch_backward_d256(const BwdParams& p, cudaStream_t stream) {
-  return launch_bwd2_impl<256, 1, 2>(p, stream);
+  return launch_bwd2_impl<256, 1, 2, 1>(p, stream);
 }
 
 }  // namespace dfa

@@ -1,8 +1,9 @@
 // Persistent forward kernel of block-diffusion attention (headdim 64, 128).
 //
-// One CTA per SM walks a strided list of work items, one item being one
-// 128-row query tile of one half of one (batch, head) (items ordered longest
-// first inside groups of heads that share L2).  For its item it visits
+// One CTA per SM takes work items from a work counter until none are left,
+// one item being one 128-row query tile of one half of one (batch, head)
+// (items ordered longest first inside groups of heads that share L2, the
+// shortest of all heads last).  For its item it visits
 // exactly the key tiles the mask reaches ("Fast Diffusion Attention", "Visit
 // only the visible tiles") and runs the loop of "FlashAttention: Exact
 // Attention Without Materialization", section 5.1, with the online softmax of
@@ -58,10 +59,12 @@ struct Fwd2Cfg {
     BAR_ITEMDONE = BAR_PFULL + 2,     // every product of an item complete
     BAR_OFREE = BAR_ITEMDONE + 1,     // both O accumulators read out
     BAR_XCHG = BAR_OFREE + 1,         // both warpgroups' (m, l) in shared memory
-    BAR_ALL = BAR_XCHG + 1,           // every MMA of the CTA complete
+    BAR_ITEMFULL = BAR_XCHG + 1,      // [4] item index published
+    BAR_ALL = BAR_ITEMFULL + 4,       // every MMA of the CTA complete
     NUM_BARS = BAR_ALL + 1
   };
-  static constexpr int kOffTmemSlot = kOffBar + NUM_BARS * 8;
+  static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 item indices
+  static constexpr int kOffTmemSlot = kOffItem + 16;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
   static constexpr int kTmemS = 0;       // S[w] at w * BN; P[w] in its first BN / 2 columns
@@ -100,6 +103,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::kOffItem);
   const AbortFlag ab{abort_flag, p.status};
   const int num_items = 2 * p.B * p.H * p.q_tiles;
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
@@ -120,6 +124,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     mbar_init(BAR(C::BAR_ITEMDONE), 1);
     mbar_init(BAR(C::BAR_OFREE), 256);
     mbar_init(BAR(C::BAR_XCHG), 256);
+    for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
     mbar_init(BAR(C::BAR_ALL), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -144,7 +149,16 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       bool ok = true;
       int g = 0;  // K/V ring position across items
       int k = 0;
-      for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x, ++k) {
+      for (; ok; ++k) {
+        // Items come from the work counter and are published to the other
+        // roles through slot k % 4 of the item ring.  The slot last held item
+        // k - 4, whose readers are all done: this loader has already waited
+        // for item k - 3's products, which the MMA warp issues only after
+        // the softmax warpgroups have finished item k - 4.
+        const int item = sched_next(p.sched, num_items);
+        item_ring[k & 3] = item;
+        mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
+        if (item < 0) break;
         ItemGeom ig;
         item_geom(p, item, BM, BN, &ig);
         const int qb = k & 1;
@@ -194,7 +208,10 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       int g = 0;                // K/V ring position
       int cnt[2] = {0, 0};      // tiles handed to each warpgroup so far
       int k = 0;
-      for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x, ++k) {
+      for (; ok; ++k) {
+        if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
+        const int item = item_ring[k & 3];
+        if (item < 0) break;
         ItemGeom ig;
         item_geom(p, item, BM, BN, &ig);
         const int qb = k & 1;
@@ -261,7 +278,10 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     bool ok = true;
     int cnt = 0;  // tiles this warpgroup has processed so far
     int k = 0;
-    for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x, ++k) {
+    for (; ok; ++k) {
+      if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
+      const int item = item_ring[k & 3];
+      if (item < 0) break;
       ItemGeom ig;
       item_geom(p, item, BM, BN, &ig);
       const int qs = ig.qs;
@@ -426,6 +446,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
 template <int D, int STAGES>

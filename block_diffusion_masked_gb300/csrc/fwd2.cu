@@ -76,18 +76,29 @@ struct Fwd2Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
+// One work item: query tile and the key tiles it visits (at most two
+// segments, kept in scalars so that nothing is indexed dynamically).
 struct ItemGeom {
   WorkItem wi;
-  Segment seg[2];
   int n0, ntiles, qs;
+  int half0, rule0, tb0, half1, rule1, tb1;
+  __device__ __forceinline__ int ktile(int j) const { return j < n0 ? tb0 + j : tb1 + (j - n0); }
+  __device__ __forceinline__ int khalf(int j) const { return j < n0 ? half0 : half1; }
 };
 
 __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, int bn,
                                           ItemGeom* g) {
   g->wi = fwd_work(item, p.mode, p.B, p.H, p.q_tiles, p.group);
-  const int nseg = fwd_segments(p.mode, p.n, p.bs, bm, bn, g->wi.half, g->wi.tile, g->seg);
-  g->n0 = nseg > 0 ? g->seg[0].t_end - g->seg[0].t_begin : 0;
-  g->ntiles = g->n0 + (nseg > 1 ? g->seg[1].t_end - g->seg[1].t_begin : 0);
+  Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
+  const int nseg = fwd_segments(p.mode, p.n, p.bs, bm, bn, g->wi.half, g->wi.tile, seg);
+  g->n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
+  g->ntiles = g->n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
+  g->half0 = seg[0].half;
+  g->rule0 = seg[0].rule;
+  g->tb0 = seg[0].t_begin;
+  g->half1 = seg[1].half;
+  g->rule1 = seg[1].rule;
+  g->tb1 = seg[1].t_begin;
   g->qs = g->wi.tile * bm;
 }
 
@@ -169,8 +180,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
           tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, &p.tm_q,
                       BAR(C::BAR_QFULL + qb), 64 * c, ig.wi.h, ig.qs, ig.wi.half, ig.wi.b);
         for (int j = 0; j < ig.ntiles; ++j, ++g) {
-          const int s = j < ig.n0 ? 0 : 1;
-          const int kt = ig.seg[s].t_begin + (s ? j - ig.n0 : j);
+          const int kt = ig.ktile(j);
+          const int kh = ig.khalf(j);
           const int st = g % STAGES;
           const int round = g / STAGES;
           if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_KEMPTY + st), (round - 1) & 1, ab))) break;
@@ -178,13 +189,13 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
-                        BAR(C::BAR_KFULL + st), 64 * c, ig.wi.h, kt * BN, ig.seg[s].half, ig.wi.b);
+                        BAR(C::BAR_KFULL + st), 64 * c, ig.wi.h, kt * BN, kh, ig.wi.b);
           if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_VEMPTY + st), (round - 1) & 1, ab))) break;
           mbar_arrive_expect_tx(BAR(C::BAR_VFULL + st), C::kKVBytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
-                        BAR(C::BAR_VFULL + st), 64 * c, ig.wi.h, kt * BN, ig.seg[s].half, ig.wi.b);
+                        BAR(C::BAR_VFULL + st), 64 * c, ig.wi.h, kt * BN, kh, ig.wi.b);
         }
       }
       if (!ok) {
@@ -286,15 +297,22 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       item_geom(p, item, BM, BN, &ig);
       const int qs = ig.qs;
       const int r = qs + row;  // row inside the half
+      // Keys visible to row r, per segment of the item: computed once, so a
+      // tile needs no division (rows past the end of the half see nothing).
+      const Interval kv0 = key_interval(ig.rule0, r, p.n, p.bs);
+      const Interval kv1 = key_interval(ig.rule1, r, p.n, p.bs);
       float m_ref = -INFINITY;  // reference maximum, scaled log2 units
       float l_run = 0.f;        // running sum of 2^(s * sl2 - m_ref)
       for (int j = w; j < ig.ntiles; j += 2, ++cnt) {
         const int s = j < ig.n0 ? 0 : 1;
-        const int kt = ig.seg[s].t_begin + (s ? j - ig.n0 : j);
+        const int kt = ig.ktile(j);
         if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + w), cnt & 1, ab))) break;
         tc_fence_after();
         const int ks = kt * BN;
-        const bool full = tile_full(ig.seg[s].rule, p.n, p.bs, qs, BM, ks, BN);
+        const Interval iv = s ? kv1 : kv0;
+        const int clo = iv.lo - ks, chi = iv.hi - ks;
+        // The warp masks element by element only if one of its rows needs it.
+        const bool full = __all_sync(0xffffffffu, clo <= 0 && chi >= BN);
         // The tile's score row in registers; hidden keys -> -inf, so they
         // drop out of the maximum and get probability 0.
         uint32_t sr[BN];
@@ -306,8 +324,6 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
           // Keys [clo, chi) of the tile are visible to row r: a 32-bit mask
           // per 32 columns, hidden scores set to -inf with one AND / OR each,
           // in straight-line code.
-          const Interval iv = key_interval(ig.seg[s].rule, r, p.n, p.bs);
-          const int clo = iv.lo - ks, chi = iv.hi - ks;
 #pragma unroll
           for (int c32 = 0; c32 < BN / 32; ++c32) {
             const int lo = clo - 32 * c32 < 0 ? 0 : (clo - 32 * c32 > 32 ? 32 : clo - 32 * c32);

@@ -177,6 +177,12 @@ def cpu_baseline(w: inputs.Workload, budget_s=12.0, max_heads=None):
 
 # ------------------------------------------------------------------ GPU arm
 
+# DRAM traffic (read + write bytes) per launch of the dominant kernel from
+# one ncu capture (profiles/dfa_bwd2_kernel_small_b8_n1024_h16_d128_bs16.md),
+# keyed by workload and kernel; any other pair reports null.
+NCU_TRAFFIC = {("small", "dfa_bwd2_kernel<128>"): 813.4e6}
+
+
 def run_gpu(args, w, rank, world):
     import torch
 
@@ -344,7 +350,8 @@ def run_gpu(args, w, rank, world):
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"],
                      "peak_source": peaks["source"] + " bf16 burst (cuBLAS 8192^3)",
-                     "traffic": None},
+                     "traffic": NCU_TRAFFIC.get((w.name, dominant[0])),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)"},
         "clocks": clocks,
     }
     if sdpa is not None:

@@ -1,27 +1,34 @@
-// Backward kernel of block-diffusion attention on sm_103a.
+// Backward kernel of block-diffusion attention, headdim 64, on sm_103a.
 //
 // Recompute-based backward of "FlashAttention: Exact Attention Without
 // Materialization", section 4.5: from q, k, v, dout, the forward's
 // log-sum-exp and D = rowsum(dout * out), recompute the probabilities on
-// chip and accumulate the gradients.  Key-tile major: one CTA owns one
-// 128-key tile of one half of one (batch, head), keeps its K and V in shared
-// memory and its dK and dV accumulators in TMEM, and walks exactly the query
-// tiles that see it ("Fast Diffusion Attention", "Visit only the visible
-// tiles"): a clean key tile is seen by the clean queries of its block onward
-// and by the noisy queries of the later blocks; a noisy key tile only by the
-// noisy queries of its own blocks.
+// chip and accumulate the gradients.  Key-tile major: a work item is one
+// 128-key tile of one half of one (batch, head); its CTA keeps K and V in
+// shared memory and the dK and dV accumulators in TMEM, and walks exactly
+// the 128-query tiles that see it ("Fast Diffusion Attention", "Visit only
+// the visible tiles"): a clean key tile is seen by the clean queries of its
+// block onward and by the noisy queries of the later blocks; a noisy key
+// tile only by the noisy queries of its own blocks.
 //
-// Per query tile i (tensor cores, accumulators in TMEM), b = i % 2:
+// Per query tile g (counted over the CTA's whole run), b = g % 2:
 //   S^T  = K Q^T                    -> TMEM S[b]
-//   dP^T = V dO^T                   -> TMEM dP[b] (one buffer for d = 64)
+//   dP^T = V dO^T                   -> TMEM dP (one buffer)
 //   P^T  = exp(scale S^T - LSE)  (0 on hidden pairs), dS^T = P^T (dP^T - D)
 //        written back as bf16 into the columns of dP, dS^T also to shared
 //   dV  += P^T dO,  dK += dS^T Q    (A operand read from TMEM)
 //   dQ   = dS K                     -> TMEM S[b] (S is consumed by then),
-//        then added to a float32 accumulator in device memory.
+//        then added to a float32 accumulator in device memory, one query
+//        row per thread with 16-byte atomics.
+// Persistent: one CTA per SM takes items from a work counter until none are
+// left (the same order and counter as the other kernels); the barrier phases
+// run on across items, the next item's first query tiles load while the
+// current item ends, and K / V reload once the current item's products are
+// done.  At the end of an item warpgroup 0 writes dV and warpgroup 1 dK; the
+// next item's first dV / dK products wait until both have been read out.
 // Warp roles (384 threads): two compute warpgroups, warpgroup b handling the
-// query tiles i with i % 2 == b (thread t of a warpgroup owns key row t of
-// the tile, TMEM lane t), so that the MMAs of one tile overlap the
+// query tiles with g % 2 == b (thread t of a warpgroup owns key row t of the
+// tile, TMEM lane t), so that the MMAs of one tile overlap the
 // softmax-gradient work of the other; warp 8 loads (TMA for Q/dO, plain loads
 // for LSE/D); warp 9 issues the MMAs; warps 10-11 idle.  The load/MMA
 // warpgroup drops to 72 registers and the compute warpgroups rise to 216
@@ -51,9 +58,6 @@ struct BwdCfg {
   static constexpr int kOffLSE = kOffDS + 2 * kDSBytes;       // STAGES x BMQ floats
   static constexpr int kOffDEL = kOffLSE + STAGES * BMQ * 4;  // STAGES x BMQ floats
   static constexpr int kOffBar = kOffDEL + STAGES * BMQ * 4;
-  // dP^T is double-buffered when TMEM has room (headdim 128); with headdim
-  // 64 the 128-query tiles leave room for one buffer only.
-  static constexpr int kDPBufs = (2 * BMQ + 2 * BMQ + 2 * D <= 512) ? 2 : 1;
   enum {
     BAR_KV = 0,
     BAR_QFULL = 1,
@@ -63,38 +67,62 @@ struct BwdCfg {
     BAR_PDS = BAR_DPFULL + 2,         // [2]
     BAR_MMA2 = BAR_PDS + 2,           // [2]
     BAR_DQFREE = BAR_MMA2 + 2,        // [2]
-    BAR_ALL = BAR_DQFREE + 2,         // every MMA done (epilogue, drain)
+    BAR_ITEMDONE = BAR_DQFREE + 2,    // every product of an item done
+    BAR_ACCFREE = BAR_ITEMDONE + 1,   // dK / dV of an item read out of TMEM
+    BAR_ITEMFULL = BAR_ACCFREE + 1,   // [4] item index published
+    BAR_ALL = BAR_ITEMFULL + 4,       // every MMA done (TMEM release)
     NUM_BARS = BAR_ALL + 1
   };
-  static constexpr int kOffTmemSlot = kOffBar + NUM_BARS * 8;
+  static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 item indices
+  static constexpr int kOffTmemSlot = kOffItem + 16;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
-  // dQ is computed transposed (rows = head dims) when headdim = 128, so that
-  // each warp's float atomics cover 32 consecutive head dims of one query;
-  // with headdim 64 it is computed as (queries x head dims).
-  static constexpr bool kDqTransposed = (D == 128);
-  static constexpr int kTmemS = 0;                     // S[b] at b * BMQ
-  static constexpr int kTmemDP = 2 * BMQ;              // dP[b] at kTmemDP + b * BMQ
-  static constexpr int kTmemDK = kTmemDP + kDPBufs * BMQ;
+  static constexpr int kTmemS = 0;          // S[b] at b * BMQ; dQ of the tile after S is read
+  static constexpr int kTmemDP = 2 * BMQ;   // dP, then P^T / dS^T
+  static constexpr int kTmemDK = kTmemDP + BMQ;
   static constexpr int kTmemDV = kTmemDK + D;
-  static constexpr int kDqCols = kDqTransposed ? BMQ : D;
   static constexpr int kTmemCols = 512;
   static constexpr int kThreads = 384;
   static constexpr int kProducerWarp = 8;
   static constexpr int kMmaWarp = 9;
   static_assert(kTmemDV + D <= kTmemCols, "TMEM budget");
-  static_assert(kDqCols <= BMQ, "dQ must fit in an S buffer");
+  static_assert(D <= BMQ, "dQ must fit in an S buffer");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kDqTransposed ? (D == 128) : (BMQ == 128), "dQ MMA needs M = 128");
-  static_assert(BMQ % 32 == 0, "query tile");
+  static_assert(BMQ == 128 && D == 64, "layout of this kernel: 128-query tiles, headdim 64");
 };
+
+// One work item: key tile and the query tiles that see it (at most two
+// segments, kept in scalars so that nothing is indexed dynamically).
+struct BwdItem {
+  WorkItem wi;
+  int n0, ntiles;
+  int half0, rule0, tb0, half1, rule1, tb1;
+  __device__ __forceinline__ int qtile(int t) const { return t < n0 ? tb0 + t : tb1 + (t - n0); }
+  __device__ __forceinline__ int qhalf(int t) const { return t < n0 ? half0 : half1; }
+};
+
+template <int BMQ, int BN>
+__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
+  BwdItem it;
+  it.wi = bwd_work(v, p.mode, p.B, p.H, p.k_tiles, p.group);
+  Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
+  const int nseg = bwd_segments(p.mode, p.n, p.bs, BMQ, BN, it.wi.half, it.wi.tile, seg);
+  it.n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
+  it.ntiles = it.n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
+  it.half0 = seg[0].half;
+  it.rule0 = seg[0].rule;
+  it.tb0 = seg[0].t_begin;
+  it.half1 = seg[1].half;
+  it.rule1 = seg[1].rule;
+  it.tb1 = seg[1].t_begin;
+  return it;
+}
 
 template <int D, int BMQ>
 __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D, BMQ>;
   constexpr int BN = C::BN;
   constexpr int STAGES = C::STAGES;
-  constexpr int DPB = C::kDPBufs;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -102,16 +130,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::kOffItem);
   const AbortFlag ab{abort_flag, p.status};
-#define BAR(i) (sbase + C::kOffBar + 8 * (i))
-
-  const WorkItem wi = bwd_work(blockIdx.x, p.mode, p.B, p.H, p.k_tiles, p.group);
-  Segment seg[2];
-  const int nseg = bwd_segments(p.mode, p.n, p.bs, BMQ, BN, wi.half, wi.tile, seg);
-  const int n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
-  const int ntiles = n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
-  const int ks = wi.tile * BN;
   const size_t L = 2 * static_cast<size_t>(p.n);
+#define BAR(i) (sbase + C::kOffBar + 8 * (i))
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::BAR_KV), 1);
@@ -122,10 +144,13 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(C::BAR_SFULL + b), 1);
       mbar_init(BAR(C::BAR_DPFULL + b), 1);
-      mbar_init(BAR(C::BAR_PDS + b), 128);
+      mbar_init(BAR(C::BAR_PDS + b), 4);    // warps of the tile's warpgroup
       mbar_init(BAR(C::BAR_MMA2 + b), 1);
-      mbar_init(BAR(C::BAR_DQFREE + b), 128);
+      mbar_init(BAR(C::BAR_DQFREE + b), 4);
     }
+    mbar_init(BAR(C::BAR_ITEMDONE), 1);
+    mbar_init(BAR(C::BAR_ACCFREE), 8);
+    for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
     mbar_init(BAR(C::BAR_ALL), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -139,6 +164,12 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kOffTmemSlot);
 
+  // Items are numbered k = 0, 1, ... in the order this CTA takes them, query
+  // tiles g = 0, 1, ... over all of the CTA's items; every barrier phase
+  // below is counted in one of the two.  Slot k % 4 of the item ring holds
+  // item k; the loader writes it only after item k - 2 is done, which needs
+  // both compute warpgroups to have read the dK / dV of item k - 3, so every
+  // reader of the slot's previous item has taken its index.
   if (warp >= 8) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
    if (warp == C::kProducerWarp) {
@@ -148,50 +179,32 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       tma_prefetch_desc(&p.tm_do);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(BAR(C::BAR_KV), 2 * C::kKVBytes);
-#pragma unroll
-      for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_5d(sbase + C::kOffK + c * BN * 128, &p.tm_k, BAR(C::BAR_KV), 64 * c, wi.h, ks,
-                    wi.half, wi.b);
-        tma_load_5d(sbase + C::kOffV + c * BN * 128, &p.tm_v, BAR(C::BAR_KV), 64 * c, wi.h, ks,
-                    wi.half, wi.b);
-      }
     }
-    __syncwarp();
-    const float* del_bh = p.delta + (static_cast<size_t>(wi.b) * p.H + wi.h) * L;
-    // LSE and D of a query tile are read into registers one tile ahead, so
-    // that their latency overlaps the wait for a free stage.
     constexpr int kPerLane = BMQ / 32;
-    float lse_r[kPerLane], del_r[kPerLane];
-    auto load_rows = [&](int it) {
-      const int s = it < n0 ? 0 : 1;
-      const int qt = seg[s].t_begin + (s ? it - n0 : it);
+    bool ok = true;
+    int g = 0, k = 0, q_issued = 0, kv_issued = 0;
+    // Q, dO and the negated -LSE * log2(e), -D of the item's t-th query tile
+    // into the stage of global tile gg.  Rows past the half: probability 0.
+    auto load_q = [&](const BwdItem& it, int t, int gg) -> bool {
+      const int qt = it.qtile(t);
+      const int half = it.qhalf(t);
+      const float* del_bh = p.delta + (static_cast<size_t>(it.wi.b) * p.H + it.wi.h) * L;
+      float lse_r[kPerLane], del_r[kPerLane];
 #pragma unroll
       for (int e = 0; e < kPerLane; ++e) {
         const int q = qt * BMQ + lane + 32 * e;
         const bool valid = q < p.n;
-        const size_t pos = static_cast<size_t>(seg[s].half) * p.n + q;
-        // Stored negated: -LSE * log2(e) and -D, the addends of the packed
-        // arithmetic below.  Rows past the half: probability 0.
-        lse_r[e] = valid ? p.lse[lse_offset(p.mode, wi.b, wi.h, seg[s].half, q, p.H, p.n)] *
+        lse_r[e] = valid ? p.lse[lse_offset(p.mode, it.wi.b, it.wi.h, half, q, p.H, p.n)] *
                                -1.4426950408889634f
                          : -INFINITY;
-        del_r[e] = valid ? -del_bh[pos] : 0.f;
+        del_r[e] = valid ? -del_bh[static_cast<size_t>(half) * p.n + q] : 0.f;
       }
-    };
-    if (ntiles > 0) load_rows(0);
-    bool ok = true;
-    int i = 0;
-    for (; i < ntiles && ok; ++i) {
-      const int s = i < n0 ? 0 : 1;
-      const int qt = seg[s].t_begin + (s ? i - n0 : i);
-      const int st = i % STAGES;
-      const int round = i / STAGES;
+      const int st = gg % STAGES;
+      const int round = gg / STAGES;
       if (round > 0) {
         int w = 0;
         if (lane == 0) w = mbar_wait(BAR(C::BAR_QEMPTY + st), (round - 1) & 1, ab) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-        if (!ok) break;
+        if (__shfl_sync(0xffffffffu, w, 0) == 0) return false;
       }
       float* lse_s = reinterpret_cast<float*>(smem + C::kOffLSE) + st * BMQ;
       float* del_s = reinterpret_cast<float*>(smem + C::kOffDEL) + st * BMQ;
@@ -206,27 +219,66 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           tma_load_5d(sbase + C::kOffQ + st * C::kQBytes + c * BMQ * 128, &p.tm_q,
-                      BAR(C::BAR_QFULL + st), 64 * c, wi.h, qt * BMQ, seg[s].half, wi.b);
+                      BAR(C::BAR_QFULL + st), 64 * c, it.wi.h, qt * BMQ, half, it.wi.b);
           tma_load_5d(sbase + C::kOffDO + st * C::kQBytes + c * BMQ * 128, &p.tm_do,
-                      BAR(C::BAR_QFULL + st), 64 * c, wi.h, qt * BMQ, seg[s].half, wi.b);
+                      BAR(C::BAR_QFULL + st), 64 * c, it.wi.h, qt * BMQ, half, it.wi.b);
         }
       }
       __syncwarp();
-      if (i + 1 < ntiles) load_rows(i + 1);
+      q_issued = gg + 1;
+      return true;
+    };
+    while (ok) {
+      int v = -1;
+      if (lane == 0) {
+        v = sched_next(p.sched, p.items);
+        item_ring[k & 3] = v;
+        mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
+      }
+      v = __shfl_sync(0xffffffffu, v, 0);
+      if (v < 0) break;
+      const BwdItem it = bwd_item<BMQ, BN>(p, v);
+      // The first query tiles only need stages the current item frees before
+      // its last products, so they go ahead of the K / V load, which waits
+      // for the whole item.
+      const int pre = imin(it.ntiles, STAGES - 1);
+      for (int t = 0; t < pre && ok; ++t) ok = load_q(it, t, g + t);
+      if (!ok) break;
+      if (k > 0) {
+        int w = 0;
+        if (lane == 0) w = mbar_wait(BAR(C::BAR_ITEMDONE), (k - 1) & 1, ab) ? 1 : 0;
+        if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
+      }
+      if (lane == 0) {
+        const int ks = it.wi.tile * BN;
+        mbar_arrive_expect_tx(BAR(C::BAR_KV), 2 * C::kKVBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_5d(sbase + C::kOffK + c * BN * 128, &p.tm_k, BAR(C::BAR_KV), 64 * c, it.wi.h,
+                      ks, it.wi.half, it.wi.b);
+          tma_load_5d(sbase + C::kOffV + c * BN * 128, &p.tm_v, BAR(C::BAR_KV), 64 * c, it.wi.h,
+                      ks, it.wi.half, it.wi.b);
+        }
+      }
+      __syncwarp();
+      kv_issued = k + 1;
+      for (int t = pre; t < it.ntiles && ok; ++t) ok = load_q(it, t, g + t);
+      g += it.ntiles;
+      ++k;
     }
+    // Unwinding after a failed wait: let the copies in flight land.
     if (!ok && lane == 0) {
-      mbar_wait_limited(BAR(C::BAR_KV), 0, 100000000ull);
-      for (int t = (i > STAGES ? i - STAGES : 0); t < i; ++t)
+      if (kv_issued > 0) mbar_wait_limited(BAR(C::BAR_KV), (kv_issued - 1) & 1, 100000000ull);
+      for (int t = (q_issued > STAGES ? q_issued - STAGES : 0); t < q_issued; ++t)
         mbar_wait_limited(BAR(C::BAR_QFULL + t % STAGES), (t / STAGES) & 1, 100000000ull);
     }
     __syncwarp();
    } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(BN, BMQ, false, false);      // K Q^T, V dO^T
-      constexpr uint32_t kIdKV = idesc_bf16(BN, D, false, true);        // P^T dO, dS^T Q
-      constexpr uint32_t kIdDQ = C::kDqTransposed ? idesc_bf16(D, BMQ, true, true)   // K^T dS^T
-                                                  : idesc_bf16(BMQ, D, true, true);  // dS K
+      constexpr uint32_t kIdS = idesc_bf16(BN, BMQ, false, false);  // K Q^T, V dO^T
+      constexpr uint32_t kIdKV = idesc_bf16(BN, D, false, true);    // P^T dO, dS^T Q
+      constexpr uint32_t kIdDQ = idesc_bf16(BMQ, D, true, true);    // dS K
       // Descriptors of the stage-0 / buffer-0 tiles; the others are reached by
       // adding byte offsets >> 4 to the start-address field.
       const uint64_t dK_kmaj = sdesc_sw128(sbase + C::kOffK, 16, 1024);
@@ -238,80 +290,90 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       const uint64_t dO_mn = sdesc_sw128(sbase + C::kOffDO, BMQ * 128, 1024);
       const uint64_t dDS_mn = sdesc_sw128(sbase + C::kOffDS, BN * 128, 1024);
       auto adv = [](uint64_t d, uint32_t bytes) { return d + static_cast<uint64_t>(bytes >> 4); };
-      bool ok = mbar_wait(BAR(C::BAR_KV), 0, ab);
+      bool ok = true;
+      int g = 0, k = 0;
 
-      auto issue_dp = [&](int i) {
-        const uint32_t st_off = (i % STAGES) * C::kQBytes;
-        const uint32_t d_dp = tmem + C::kTmemDP + (DPB == 2 ? (i & 1) * BMQ : 0);
+      auto issue_dp = [&](int gg) {
+        const uint32_t st_off = (gg % STAGES) * C::kQBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
-          mma_ss(d_dp, adv(dV_kmaj, koff), adv(dO_kmaj, st_off + qoff), kIdS, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::kTmemDP, adv(dV_kmaj, koff), adv(dO_kmaj, st_off + qoff), kIdS,
+                 kk > 0 ? 1u : 0u);
         }
-        mma_commit(BAR(C::BAR_DPFULL + (i & 1)));
+        mma_commit(BAR(C::BAR_DPFULL + (gg & 1)));
       };
-      // dV, dK and dQ of tile j, once its P^T / dS^T are in place.
-      auto issue_second = [&](int j) -> bool {
-        const int b = j & 1;
-        const uint32_t st_off = (j % STAGES) * C::kQBytes;
-        if (!mbar_wait(BAR(C::BAR_PDS + b), (j >> 1) & 1, ab)) return false;
+      // dV, dK and dQ of global tile gg, once its P^T / dS^T are in place;
+      // `first`: the item's first tile, which starts the dK / dV sums.
+      auto issue_second = [&](int gg, bool first) -> bool {
+        const int b = gg & 1;
+        const uint32_t st_off = (gg % STAGES) * C::kQBytes;
+        if (!mbar_wait(BAR(C::BAR_PDS + b), (gg >> 1) & 1, ab)) return false;
+        // dK / dV of the previous item must be read out before they restart.
+        if (first && k >= 1 && !mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t pds = tmem + C::kTmemDP + (DPB == 2 ? b * BMQ : 0);
+        const uint32_t pds = tmem + C::kTmemDP;
 #pragma unroll
         for (int kk = 0; kk < BMQ / 16; ++kk) {
           // P^T / dS^T of queries [16kk, 16kk+16): columns of 32-query chunk
           // kk/2, P^T in its first 16 columns, dS^T in its last 16.
           const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
-          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
           mma_ts(tmem + C::kTmemDV, pds + col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV, acc);
           mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128), kIdKV,
                  acc);
         }
         const uint32_t ds_off = b * C::kDSBytes;
-        const uint32_t d_dq = tmem + C::kTmemS + b * BMQ;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t kdesc = adv(dK_mn, kk * 16 * 128);
-          const uint64_t sdesc = adv(dDS_mn, ds_off + kk * 16 * 128);
-          if (C::kDqTransposed)
-            mma_ss(d_dq, kdesc, sdesc, kIdDQ, kk > 0 ? 1u : 0u);
-          else
-            mma_ss(d_dq, sdesc, kdesc, kIdDQ, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ss(tmem + C::kTmemS + b * BMQ, adv(dDS_mn, ds_off + kk * 16 * 128),
+                 adv(dK_mn, kk * 16 * 128), kIdDQ, kk > 0 ? 1u : 0u);
         mma_commit(BAR(C::BAR_MMA2 + b));
-        mma_commit(BAR(C::BAR_QEMPTY + (j % STAGES)));
+        mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
         return true;
       };
 
-      for (int i = 0; i < ntiles && ok; ++i) {
-        const int b = i & 1;
-        const int st = i % STAGES;
-        if (!(ok = mbar_wait(BAR(C::BAR_QFULL + st), (i / STAGES) & 1, ab))) break;
-        // S[b] held dQ of tile i-2: wait until it has been read out.
-        if (i >= 2 && !(ok = mbar_wait(BAR(C::BAR_DQFREE + b), ((i - 2) >> 1) & 1, ab))) break;
-        tc_fence_after();
-        const uint32_t st_off = st * C::kQBytes;
+      while (ok) {
+        if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
+        const int v = item_ring[k & 3];
+        if (v < 0) break;
+        const BwdItem it = bwd_item<BMQ, BN>(p, v);
+        if (!(ok = mbar_wait(BAR(C::BAR_KV), k & 1, ab))) break;
+        for (int i = 0; i < it.ntiles && ok; ++i) {
+          const int gg = g + i;
+          const int b = gg & 1;
+          const int st = gg % STAGES;
+          if (!(ok = mbar_wait(BAR(C::BAR_QFULL + st), (gg / STAGES) & 1, ab))) break;
+          // S[b] held dQ of tile gg-2: wait until it has been read out.
+          if (gg >= 2 && !(ok = mbar_wait(BAR(C::BAR_DQFREE + b), ((gg - 2) >> 1) & 1, ab))) break;
+          tc_fence_after();
+          const uint32_t st_off = st * C::kQBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-          const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
-          mma_ss(tmem + C::kTmemS + b * BMQ, adv(dK_kmaj, koff), adv(dQ_kmaj, st_off + qoff), kIdS,
-                 kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
+            mma_ss(tmem + C::kTmemS + b * BMQ, adv(dK_kmaj, koff), adv(dQ_kmaj, st_off + qoff),
+                   kIdS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(BAR(C::BAR_SFULL + b));
+          // One dP buffer: it still holds P^T / dS^T of tile gg-1 until the
+          // dV / dK products of tile gg-1 have been issued (the previous
+          // item's last tile was issued at that item's end).
+          if (i >= 1 && !(ok = issue_second(gg - 1, i == 1))) break;
+          issue_dp(gg);
         }
-        mma_commit(BAR(C::BAR_SFULL + b));
-        if (DPB == 2) {
-          issue_dp(i);
-          if (i >= 1 && !(ok = issue_second(i - 1))) break;
-        } else {
-          // One dP buffer: it still holds P^T / dS^T of tile i-1 until the
-          // dV / dK products of tile i-1 have been issued.
-          if (i >= 1 && !(ok = issue_second(i - 1))) break;
-          issue_dp(i);
+        if (!ok) break;
+        if (it.ntiles > 0) {
+          if (!(ok = issue_second(g + it.ntiles - 1, it.ntiles == 1))) break;
+        } else if (k >= 1 && !(ok = mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab))) {
+          break;
         }
+        mma_commit(BAR(C::BAR_ITEMDONE));
+        g += it.ntiles;
+        ++k;
       }
-      if (ok && ntiles > 0) issue_second(ntiles - 1);
-      // Every MMA is complete when BAR_ALL fires (epilogue; TMEM release).
+      // Every MMA is complete when BAR_ALL fires (TMEM release).
       mma_commit(BAR(C::BAR_ALL));
     }
     __syncwarp();
@@ -319,69 +381,33 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
     // ------------------------------------------------------------ compute
-    const int wg = warp >> 2;            // this warpgroup handles tiles i % 2 == wg
+    const int wg = warp >> 2;                // this warpgroup handles tiles g % 2 == wg
     const int row = (warp & 3) * 32 + lane;  // key row of the tile / TMEM lane
-    const int j = ks + row;                  // key inside its half
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const float sl2 = p.scale_log2;
-    bool ok = true;
 
-    // Read dQ of tile `it` out of TMEM S[it%2] and add it to dq_acc.
-    auto drain_dq = [&](int it) -> bool {
-      const int b = it & 1;
-      if (!mbar_wait_warp(BAR(C::BAR_MMA2 + b), (it >> 1) & 1, ab)) return false;
+    // dQ of global tile gg (TMEM S[gg % 2], lane = query `row` of the tile,
+    // columns = head dims), added to dq_acc with 16-byte atomics.
+    auto drain_dq = [&](const BwdItem& it, int gg, int t) -> bool {
+      const int b = gg & 1;
+      if (!mbar_wait_warp(BAR(C::BAR_MMA2 + b), (gg >> 1) & 1, ab)) return false;
       tc_fence_after();
-      const int s = it < n0 ? 0 : 1;
-      const int qt = seg[s].t_begin + (s ? it - n0 : it);
-      const int qh = seg[s].half;
-      const int qs = qt * BMQ;
-      const uint32_t src = t_lane + C::kTmemS + b * BMQ;
-      if (C::kDqTransposed) {
-        // TMEM lane = head dim `row`; columns = queries of the tile.
-        uint32_t dq[BMQ];
+      uint32_t dq[D];
 #pragma unroll
-        for (int c = 0; c < BMQ / 32; ++c) tmem_ld32(src + 32 * c, dq + 32 * c);
-        tmem_wait_ld();
-        tmem_pin<BMQ>(dq);
-        tc_fence_before();
-        mbar_arrive(BAR(C::BAR_DQFREE + b));
-        const size_t stride = static_cast<size_t>(p.H) * D;
-        float* ptr = p.dq_acc + ((static_cast<size_t>(wi.b) * L + static_cast<size_t>(qh) * p.n +
-                                  qs) * p.H + wi.h) * D + row;
-        if (qs + BMQ <= p.n) {
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(t_lane + C::kTmemS + b * BMQ + 32 * c, dq + 32 * c);
+      tmem_wait_ld();
+      tmem_pin<D>(dq);
+      tc_fence_before();
+      mbar_arrive_warp(BAR(C::BAR_DQFREE + b));
+      const int q = it.qtile(t) * BMQ + row;
+      if (q < p.n) {
+        float* dst = p.dq_acc + ((static_cast<size_t>(it.wi.b) * L +
+                                  static_cast<size_t>(it.qhalf(t)) * p.n + q) * p.H + it.wi.h) * D;
 #pragma unroll
-          for (int c = 0; c < BMQ; ++c) {
-            red_add_f32(ptr, __uint_as_float(dq[c]) * p.scale);
-            ptr += stride;
-          }
-        } else {
-          const int qmax = p.n - qs;
-#pragma unroll
-          for (int c = 0; c < BMQ; ++c) {
-            if (c < qmax) red_add_f32(ptr, __uint_as_float(dq[c]) * p.scale);
-            ptr += stride;
-          }
-        }
-      } else {
-        // TMEM lane = query `row` of the tile; columns = head dims.
-        uint32_t dq[D];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(src + 32 * c, dq + 32 * c);
-        tmem_wait_ld();
-        tmem_pin<D>(dq);
-        tc_fence_before();
-        mbar_arrive(BAR(C::BAR_DQFREE + b));
-        const int q = qs + row;
-        if (q < p.n) {
-          float* dst = p.dq_acc + ((static_cast<size_t>(wi.b) * L + static_cast<size_t>(qh) * p.n +
-                                    q) * p.H + wi.h) * D;
-#pragma unroll
-          for (int c = 0; c < D; c += 4)
-            red_add_v4_f32(dst + c, __uint_as_float(dq[c]) * p.scale,
-                           __uint_as_float(dq[c + 1]) * p.scale,
-                           __uint_as_float(dq[c + 2]) * p.scale,
-                           __uint_as_float(dq[c + 3]) * p.scale);
-        }
+        for (int c = 0; c < D; c += 4)
+          red_add_v4_f32(dst + c, __uint_as_float(dq[c]) * p.scale,
+                         __uint_as_float(dq[c + 1]) * p.scale, __uint_as_float(dq[c + 2]) * p.scale,
+                         __uint_as_float(dq[c + 3]) * p.scale);
       }
       return true;
     };
@@ -390,14 +416,16 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     // TMEM loads), bf16 P^T / dS^T back into the dP columns of each 32-query
     // chunk (P^T in its first 16 columns, dS^T in its last 16), dS^T also into
     // the swizzled shared tile.  Pairs of columns go through packed f32x2
-    // arithmetic: x = s * sl2 - lse2, p = 2^x, ds = p * (dp - D).
-    auto slice = [&](auto masked, int h, uint32_t s_col, uint32_t dp_col, uint32_t ds_s,
-                     const float* nlse_s, const float* ndel_s, int qs, Interval iv) {
+    // arithmetic: x = s * sl2 - lse2, p = 2^x, ds = p * (dp - D); a hidden
+    // pair's p is cleared by AND with its column's mask bit (keep_lo /
+    // keep_hi: columns 0-31 / 32-63 of the slice).
+    auto slice = [&](int h, uint32_t s_col, uint32_t ds_s, uint32_t nlse_s, uint32_t ndel_s,
+                     uint32_t keep_lo, uint32_t keep_hi) {
       uint32_t sr[64], dpr[64];
       tmem_ld32(s_col + 64 * h, sr);
       tmem_ld32(s_col + 64 * h + 32, sr + 32);
-      tmem_ld32(dp_col + 64 * h, dpr);
-      tmem_ld32(dp_col + 64 * h + 32, dpr + 32);
+      tmem_ld32(t_lane + C::kTmemDP + 64 * h, dpr);
+      tmem_ld32(t_lane + C::kTmemDP + 64 * h + 32, dpr + 32);
       tmem_wait_ld();
       tmem_pin<64>(sr);
       tmem_pin<64>(dpr);
@@ -405,23 +433,21 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int cbase = 64 * h + 32 * cc;  // first query column of the chunk
+        const uint32_t keep = cc ? keep_hi : keep_lo;
         uint32_t wp[16], wd[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int cl = 32 * cc + 2 * e;  // column inside the slice
-          const float2 nl = *reinterpret_cast<const float2*>(nlse_s + cbase + 2 * e);
-          const float2 nd = *reinterpret_cast<const float2*>(ndel_s + cbase + 2 * e);
+          const float2 nl = ld_shared_v2_f32(nlse_s + 4 * (cbase + 2 * e));
+          const float2 nd = ld_shared_v2_f32(ndel_s + 4 * (cbase + 2 * e));
           const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[cl]), __uint_as_float(sr[cl + 1])),
                                     scale2, f2_pack(nl.x, nl.y));
           float x0, x1;
           f2_unpack(x, x0, x1);
-          float p0 = ex2_approx(x0);
-          float p1 = ex2_approx(x1);
-          if (decltype(masked)::value) {
-            const int q = qs + cbase + 2 * e;
-            if (q < iv.lo || q >= iv.hi) p0 = 0.f;
-            if (q + 1 < iv.lo || q + 1 >= iv.hi) p1 = 0.f;
-          }
+          const float p0 =
+              __uint_as_float(__float_as_uint(ex2_approx(x0)) & bit_spread(keep, 2 * e));
+          const float p1 =
+              __uint_as_float(__float_as_uint(ex2_approx(x1)) & bit_spread(keep, 2 * e + 1));
           const uint64_t pp = f2_pack(p0, p1);
           const uint64_t dd =
               f2_add(f2_pack(__uint_as_float(dpr[cl]), __uint_as_float(dpr[cl + 1])),
@@ -432,8 +458,8 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
           wd[e] = pack_bf16x2(d0, d1);
         }
         const int chunk = 2 * h + cc;
-        tmem_st16(dp_col + 32 * chunk, wp);
-        tmem_st16(dp_col + 32 * chunk + 16, wd);
+        tmem_st16(t_lane + C::kTmemDP + 32 * chunk, wp);
+        tmem_st16(t_lane + C::kTmemDP + 32 * chunk + 16, wd);
         const int a = chunk >> 1;  // 64-column swizzle atom
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
@@ -444,75 +470,88 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       }
     };
 
-    for (int i = wg; i < ntiles && ok; i += 2) {
-      const int s = i < n0 ? 0 : 1;
-      const int qt = seg[s].t_begin + (s ? i - n0 : i);
-      const int st = i % STAGES;
-      const int b = i & 1;
-      const int dpb = DPB == 2 ? b : 0;
-      if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + b), (i >> 1) & 1, ab))) break;
-      if (!(ok = mbar_wait_warp(BAR(C::BAR_DPFULL + b), (i >> 1) & 1, ab))) break;
+    bool ok = true;
+    int g = 0, k = 0;
+    while (ok) {
+      if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
+      const int v = item_ring[k & 3];
+      if (v < 0) break;
+      const BwdItem it = bwd_item<BMQ, BN>(p, v);
+      const int ks = it.wi.tile * BN;
+      const int j = ks + row;  // key inside its half
+      // Query rows that see key j, per segment of the item: computed once,
+      // so a tile needs no division and no per-tile visibility test.
+      const Interval iv0 = query_interval(it.rule0, j, p.n, p.bs);
+      const Interval iv1 = query_interval(it.rule1, j, p.n, p.bs);
+      for (int i = ((g & 1) == wg) ? 0 : 1; i < it.ntiles && ok; i += 2) {
+        const int gg = g + i;
+        const int st = gg % STAGES;
+        const int b = gg & 1;
+        if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + b), (gg >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(BAR(C::BAR_DPFULL + b), (gg >> 1) & 1, ab))) break;
+        tc_fence_after();
+        const uint32_t nlse_s = sbase + C::kOffLSE + 4 * st * BMQ;
+        const uint32_t ndel_s = sbase + C::kOffDEL + 4 * st * BMQ;
+        const int qs = it.qtile(i) * BMQ;
+        // Columns (queries) that see key j, as a 128-bit mask in 4 words.
+        const Interval iv = i < it.n0 ? iv0 : iv1;
+        uint32_t keep[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int lo0 = iv.lo - qs - 32 * w, hi0 = iv.hi - qs - 32 * w;
+          const int lo = lo0 < 0 ? 0 : (lo0 > 32 ? 32 : lo0);
+          const int hi = hi0 < lo ? lo : (hi0 > 32 ? 32 : hi0);
+          const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+          const uint32_t below_lo = lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u);
+          keep[w] = below_hi & ~below_lo;
+        }
+        const uint32_t s_col = t_lane + C::kTmemS + b * BMQ;
+        const uint32_t ds_s = sbase + C::kOffDS + b * C::kDSBytes;
+        slice(0, s_col, ds_s, nlse_s, ndel_s, keep[0], keep[1]);
+        slice(1, s_col, ds_s, nlse_s, ndel_s, keep[2], keep[3]);
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive_warp(BAR(C::BAR_PDS + b));
+        if (!(ok = drain_dq(it, gg, i))) break;
+      }
+      if (!ok) break;
+
+      // -------------------------------------------------------- item epilogue
+      // Warpgroup 0 writes dV, warpgroup 1 writes dK, once the item's MMAs
+      // are done; TMEM is released as soon as both have read their part.
+      if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMDONE), k & 1, ab))) break;
       tc_fence_after();
-
-      const float* lse_s = reinterpret_cast<const float*>(smem + C::kOffLSE) + st * BMQ;
-      const float* del_s = reinterpret_cast<const float*>(smem + C::kOffDEL) + st * BMQ;
-      const int qs = qt * BMQ;
-      const bool full = tile_full(seg[s].rule, p.n, p.bs, qs, BMQ, ks, BN);
-      const Interval iv = query_interval(seg[s].rule, j, p.n, p.bs);
-      const uint32_t s_col = t_lane + C::kTmemS + b * BMQ;
-      const uint32_t dp_col = t_lane + C::kTmemDP + dpb * BMQ;
-      const uint32_t ds_s = sbase + C::kOffDS + b * C::kDSBytes;
-      if (full) {
-#pragma unroll 1
-        for (int h = 0; h < BMQ / 64; ++h)
-          slice(std::false_type{}, h, s_col, dp_col, ds_s, lse_s, del_s, qs, iv);
-      } else {
-#pragma unroll 1
-        for (int h = 0; h < BMQ / 64; ++h)
-          slice(std::true_type{}, h, s_col, dp_col, ds_s, lse_s, del_s, qs, iv);
-      }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(BAR(C::BAR_PDS + b));
-
-      if (!(ok = drain_dq(i))) break;
-    }
-
-    // ------------------------------------------------------------ epilogue
-    // Warpgroup 0 writes dV, warpgroup 1 writes dK, once every MMA is done.
-    if (ok) ok = mbar_wait_warp(BAR(C::BAR_ALL), 0, ab);
-    tc_fence_after();
-    if (ok) {
-      const bool valid = j < p.n;
-      const size_t pos = static_cast<size_t>(wi.half) * p.n + j;
-      const size_t off = ((static_cast<size_t>(wi.b) * L + pos) * p.H + wi.h) * D;
-      __nv_bfloat16* dst = (wg == 0 ? p.dv : p.dk) + off;
-      const float mul = wg == 0 ? 1.f : p.scale;
       const uint32_t col = wg == 0 ? C::kTmemDV : C::kTmemDK;
+      uint32_t o[D];
+      if (it.ntiles > 0) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        if (ntiles > 0) {
-          tmem_ld32(t_lane + col + 32 * c, o);
-          tmem_wait_ld();
-          tmem_pin<32>(o);
-        } else {
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(t_lane + col + 32 * c, o + 32 * c);
+        tmem_wait_ld();
+        tmem_pin<D>(o);
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        if (valid) {
+        for (int e = 0; e < D; ++e) o[e] = 0u;
+      }
+      tc_fence_before();
+      mbar_arrive_warp(BAR(C::BAR_ACCFREE));
+      if (j < p.n) {
+        const size_t pos = static_cast<size_t>(it.wi.half) * p.n + j;
+        const size_t off = ((static_cast<size_t>(it.wi.b) * L + pos) * p.H + it.wi.h) * D;
+        __nv_bfloat16* dst = (wg == 0 ? p.dv : p.dk) + off;
+        const float mul = wg == 0 ? 1.f : p.scale;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t w[4];
+        for (int g8 = 0; g8 < D / 8; ++g8) {
+          uint32_t w4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(o[g * 8 + 2 * e]) * mul,
-                                 __uint_as_float(o[g * 8 + 2 * e + 1]) * mul);
-            st_global_v4(dst + 32 * c + 8 * g, w[0], w[1], w[2], w[3]);
-          }
+          for (int e = 0; e < 4; ++e)
+            w4[e] = pack_bf16x2(__uint_as_float(o[g8 * 8 + 2 * e]) * mul,
+                                __uint_as_float(o[g8 * 8 + 2 * e + 1]) * mul);
+          st_global_v4(dst + 8 * g8, w4[0], w4[1], w4[2], w4[3]);
         }
       }
+      g += it.ntiles;
+      ++k;
     }
   }
 #undef BAR
@@ -526,6 +565,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
 template <int D, int BMQ>
@@ -535,10 +575,17 @@ static cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long blocks = 2LL * p.B * p.H * p.k_tiles;
-  if (blocks <= 0) return cudaSuccess;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
+  const long long items = 2LL * p.B * p.H * p.k_tiles;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  BwdParams q = p;
+  q.items = static_cast<int>(items);
+  const long long grid = items < sms ? items : sms;
+  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(q);
   return cudaGetLastError();
 }
 

@@ -22,11 +22,12 @@
 // The K/V ring, the query double buffer and all barrier phases run on across
 // items, so the loads and S products of the next item overlap the merge and
 // stores of the current one.
-// Warps 0-7 softmax, warp 8 TMA producer, warp 9 MMA issuer, warps 10-11
-// idle.  The producer/MMA warpgroup hands registers to the softmax
-// warpgroups (setmaxnreg): launched with 168 per thread, it drops to 56 and
-// the softmax warpgroups rise to 224, which keeps a row's 128 scores in
-// registers.  256 * (224 - 168) == 128 * (168 - 56): the pool balances.
+// Warps 0-7 softmax, warp 8 loads Q and K (and takes the items), warp 10
+// loads V, warp 9 issues the MMAs, warp 11 idle.  The load/MMA warpgroup
+// hands registers to the softmax warpgroups (setmaxnreg): launched with 168
+// per thread, it drops to 56 and the softmax warpgroups rise to 224, which
+// keeps a row's 128 scores in registers.  256 * (224 - 168) == 128 * (168 -
+// 56): the pool balances.
 #include <cuda_bf16.h>
 
 #include "geometry.cuh"
@@ -151,9 +152,13 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
 
   if (warp >= 8) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
-   if (warp == 8) {
-    // ------------------------------------------------------------ producer
+   if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ producers
+    // Warp 8 takes items, publishes them and loads Q and the K ring; warp 10
+    // loads the V ring, so that K tiles (needed first, by S) are not held
+    // up behind the wait for a V slot.
     if (lane == 0) {
+      const bool kload = warp == 8;
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
@@ -161,41 +166,47 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       int g = 0;  // K/V ring position across items
       int k = 0;
       for (; ok; ++k) {
-        // Items come from the work counter and are published to the other
-        // roles through slot k % 4 of the item ring.  The slot last held item
-        // k - 4, whose readers are all done: this loader has already waited
-        // for item k - 3's products, which the MMA warp issues only after
-        // the softmax warpgroups have finished item k - 4.
-        const int item = sched_next(p.sched, num_items);
-        item_ring[k & 3] = item;
-        mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
+        int item;
+        if (kload) {
+          // Items come from the work counter and are published to the other
+          // roles through slot k % 4 of the item ring.  The slot last held
+          // item k - 4, whose readers are all done: this loader has already
+          // waited for item k - 3's products, which the MMA warp issues only
+          // after the softmax warpgroups have finished item k - 4 (and the V
+          // loader read it before loading item k - 4's last V tile, which
+          // those products needed).
+          item = sched_next(p.sched, num_items);
+          item_ring[k & 3] = item;
+          mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
+        } else {
+          if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
+          item = item_ring[k & 3];
+        }
         if (item < 0) break;
         ItemGeom ig;
         item_geom(p, item, BM, BN, &ig);
-        const int qb = k & 1;
-        if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_QEMPTY + qb), ((k >> 1) - 1) & 1, ab))) break;
-        mbar_arrive_expect_tx(BAR(C::BAR_QFULL + qb), C::kQBytes);
+        if (kload) {
+          const int qb = k & 1;
+          if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_QEMPTY + qb), ((k >> 1) - 1) & 1, ab))) break;
+          mbar_arrive_expect_tx(BAR(C::BAR_QFULL + qb), C::kQBytes);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, &p.tm_q,
-                      BAR(C::BAR_QFULL + qb), 64 * c, ig.wi.h, ig.qs, ig.wi.half, ig.wi.b);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, &p.tm_q,
+                        BAR(C::BAR_QFULL + qb), 64 * c, ig.wi.h, ig.qs, ig.wi.half, ig.wi.b);
+        }
         for (int j = 0; j < ig.ntiles; ++j, ++g) {
           const int kt = ig.ktile(j);
           const int kh = ig.khalf(j);
           const int st = g % STAGES;
           const int round = g / STAGES;
-          if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_KEMPTY + st), (round - 1) & 1, ab))) break;
-          mbar_arrive_expect_tx(BAR(C::BAR_KFULL + st), C::kKVBytes);
+          const uint32_t empty = BAR((kload ? C::BAR_KEMPTY : C::BAR_VEMPTY) + st);
+          const uint32_t full = BAR((kload ? C::BAR_KFULL : C::BAR_VFULL) + st);
+          if (round > 0 && !(ok = mbar_wait(empty, (round - 1) & 1, ab))) break;
+          mbar_arrive_expect_tx(full, C::kKVBytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
-                        BAR(C::BAR_KFULL + st), 64 * c, ig.wi.h, kt * BN, kh, ig.wi.b);
-          if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_VEMPTY + st), (round - 1) & 1, ab))) break;
-          mbar_arrive_expect_tx(BAR(C::BAR_VFULL + st), C::kKVBytes);
-#pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
-                        BAR(C::BAR_VFULL + st), 64 * c, ig.wi.h, kt * BN, kh, ig.wi.b);
+            tma_load_5d(sbase + (kload ? C::kOffK : C::kOffV) + st * C::kKVBytes + c * BN * 128,
+                        kload ? &p.tm_k : &p.tm_v, full, 64 * c, ig.wi.h, kt * BN, kh, ig.wi.b);
         }
       }
       if (!ok) {

@@ -226,12 +226,16 @@ DFA_HD WorkItem bwd_work(int w, int mode, int B, int H, int tiles, int group) {
 }
 
 // Heads per group: the group's working set (bytes_per_bh each) kept within
-// about half of L2.
+// about half of L2, and the heads spread evenly over the fewest groups that
+// allows.  Even groups matter: a group's longest items start when the group
+// does, so a small last group would leave its long items running alone at
+// the end of the launch.
 inline int l2_group(long long bytes_per_bh, long long l2_bytes, int BH) {
   long long g = (l2_bytes / 2) / (bytes_per_bh > 0 ? bytes_per_bh : 1);
   if (g < 1) g = 1;
   if (g > BH) g = BH;
-  return static_cast<int>(g);
+  const long long groups = (BH + g - 1) / g;
+  return static_cast<int>((BH + groups - 1) / groups);
 }
 
 }  // namespace dfa

@@ -180,7 +180,7 @@ def cpu_baseline(w: inputs.Workload, budget_s=12.0, max_heads=None):
 # DRAM traffic (read + write bytes) per launch of the dominant kernel from
 # one ncu capture (profiles/dfa_bwd2_kernel_small_b8_n1024_h16_d128_bs16.md),
 # keyed by workload and kernel; any other pair reports null.
-NCU_TRAFFIC = {("small", "dfa_bwd2_kernel<128>"): 813.4e6}
+NCU_TRAFFIC = {("small", "dfa_bwd2_kernel<128>"): 808.4e6}
 
 
 def run_gpu(args, w, rank, world):
@@ -209,10 +209,11 @@ def run_gpu(args, w, rank, world):
     def diff_step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        binding.dfa_forward(q, k, v, w.block_size, out=out, lse=lse)
+        # the forward launch also zeroes the dq accumulator
+        binding.dfa_fwd_main(q, k, v, out, lse, dq_acc, w.block_size)
         if ev is not None:
             ev[1].record(stream)
-        binding.dfa_bwd_preprocess(out, do, delta, dq_acc)
+        binding.dfa_bwd_preprocess(out, do, delta, None)
         if ev is not None:
             ev[2].record(stream)
         binding.dfa_bwd_main(q, k, v, do, lse, delta, dq_acc, dk, dv, w.block_size)
@@ -225,10 +226,11 @@ def run_gpu(args, w, rank, world):
     def causal_step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        binding.dfa_causal_forward(qc, kc, vc, out=outc, lse=lsec)
+        binding.dfa_fwd_main(q, k, v, outc.view(B, L, H, d), lsec, dq_acc, 1,
+                             mode=binding.MODE_CAUSAL)
         if ev is not None:
             ev[1].record(stream)
-        binding.dfa_bwd_preprocess(outc.view(B, L, H, d), do, delta, dq_acc)
+        binding.dfa_bwd_preprocess(outc.view(B, L, H, d), do, delta, None)
         if ev is not None:
             ev[2].record(stream)
         binding.dfa_bwd_main(q, k, v, do, lsec, delta, dq_acc, dkc.view(B, L, H, d),

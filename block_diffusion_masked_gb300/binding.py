@@ -41,6 +41,7 @@ _SIGNATURES = {
     "dfa_causal_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _P]),
     "dfa_status": (_I, [_P]),
     "dfa_selftest_wait_timeout": (_I, [_I, _P]),
+    "dfa_fwd_main": (_I, [_P] * 6 + [_I] * 6 + [_P]),
     "dfa_bwd_preprocess": (_I, [_P] * 4 + [_I] * 4 + [_P]),
     "dfa_bwd_main": (_I, [_P] * 9 + [_I] * 6 + [_P]),
     "dfa_bwd_dq_convert": (_I, [_P] * 2 + [_I] * 4 + [_P]),
@@ -167,13 +168,32 @@ def dfa_causal_backward(q, k, v, out, dout, lse, dq=None, dk=None, dv=None):
     return dq, dk, dv
 
 
+def _ptr_or_null(t):
+    return ctypes.c_void_p(None) if t is None else _ptr(t)
+
+
+def dfa_fwd_main(q, k, v, out, lse, dq_acc, block_size, mode=MODE_DIFFUSION):
+    """The forward step; also zeroes dq_acc (float32, shape of q) unless None.
+
+    q, k, v, out: (B, 2n, H, d) bf16; lse (B, H, 2n) fp32 (in the causal mode
+    the paired view's (2B, H, n) layout, as dfa_causal_forward writes it).
+    """
+    _check_qkv(q, k, v, out)
+    B, L, H, d = q.shape
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_fwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                _ptr_or_null(dq_acc), B, L // 2, H, d, int(block_size), int(mode),
+                                _stream_ptr(q))
+    _check("dfa_fwd_main", rc)
+
+
 def dfa_bwd_preprocess(out, dout, delta, dq_acc):
-    """Step 1 of the backward: delta = rowsum(dout * out); dq_acc = 0."""
+    """Step 1 of the backward: delta = rowsum(dout * out); dq_acc = 0 unless None."""
     _check_qkv(out, dout)
     B, L, H, d = out.shape
     with torch.cuda.device(out.device):
-        rc = lib().dfa_bwd_preprocess(_ptr(out), _ptr(dout), _ptr(delta), _ptr(dq_acc), B, L // 2,
-                                      H, d, _stream_ptr(out))
+        rc = lib().dfa_bwd_preprocess(_ptr(out), _ptr(dout), _ptr(delta), _ptr_or_null(dq_acc),
+                                      B, L // 2, H, d, _stream_ptr(out))
     _check("dfa_bwd_preprocess", rc)
 
 

@@ -161,13 +161,13 @@ int check_common(int B, int n, int H, int d, int bs) {
 }
 
 int forward_impl(int mode, const void* q, const void* k, const void* v, void* out, float* lse,
-                 int B, int n, int H, int d, int bs, cudaStream_t stream) {
+                 float* dq_acc, int B, int n, int H, int d, int bs, cudaStream_t stream) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
   if (B == 0) return DFA_OK;
   if (!q || !k || !v || !out || !lse) return DFA_EINVAL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (dq_acc && !aligned16(dq_acc)))
     return DFA_EINVAL;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds))) return rc;
@@ -190,6 +190,9 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   p.group = l2_group(8LL * 2 * n * d, ds->l2_bytes, B * H);
   p.sched = sched_for_stream(ds, stream);
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  p.zero_dst = reinterpret_cast<float4*>(dq_acc);
+  // B * 2n * H * d floats, d a multiple of 64: whole 16-byte groups
+  p.zero_groups = dq_acc ? static_cast<long long>(B) * 2 * n * H * d / 4 : 0;
   const cudaError_t e = launch_forward(p, d, stream);
   return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
@@ -249,7 +252,8 @@ int preprocess_impl(const void* out, const void* dout, float* delta, float* dq_a
   int rc = check_common(B, n, H, d, 1);
   if (rc) return rc;
   if (B == 0) return DFA_OK;
-  if (!aligned_all({out, dout, dq_acc}) || !delta || (reinterpret_cast<uintptr_t>(delta) & 3u))
+  if (!aligned_all({out, dout}) || (dq_acc && !aligned16(dq_acc)) || !delta ||
+      (reinterpret_cast<uintptr_t>(delta) & 3u))
     return DFA_EINVAL;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds))) return rc;
@@ -328,8 +332,8 @@ const char* dfa_error_string(int code) {
 
 int dfa_forward(const void* q, const void* k, const void* v, void* out, float* lse, int batch,
                 int n, int heads, int headdim, int block_size, dfa_stream_t stream) {
-  return forward_impl(MODE_DIFFUSION, q, k, v, out, lse, batch, n, heads, headdim, block_size,
-                      static_cast<cudaStream_t>(stream));
+  return forward_impl(MODE_DIFFUSION, q, k, v, out, lse, nullptr, batch, n, heads, headdim,
+                      block_size, static_cast<cudaStream_t>(stream));
 }
 
 int dfa_backward(const void* q, const void* k, const void* v, const void* out, const void* dout,
@@ -348,8 +352,8 @@ int dfa_causal_forward(const void* q, const void* k, const void* v, void* out, f
                        int batch, int seqlen, int heads, int headdim, dfa_stream_t stream) {
   if (batch < 0 || seqlen < 1) return DFA_EINVAL;
   if (batch % 2) return DFA_EINVAL;
-  return forward_impl(MODE_CAUSAL, q, k, v, out, lse, batch / 2, seqlen, heads, headdim, 1,
-                      static_cast<cudaStream_t>(stream));
+  return forward_impl(MODE_CAUSAL, q, k, v, out, lse, nullptr, batch / 2, seqlen, heads, headdim,
+                      1, static_cast<cudaStream_t>(stream));
 }
 
 int dfa_causal_backward(const void* q, const void* k, const void* v, const void* out,
@@ -359,6 +363,14 @@ int dfa_causal_backward(const void* q, const void* k, const void* v, const void*
   if (batch % 2) return DFA_EINVAL;
   return backward_impl(MODE_CAUSAL, q, k, v, out, dout, lse, dq, dk, dv, batch / 2, seqlen, heads,
                        headdim, 1, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_fwd_main(const void* q, const void* k, const void* v, void* out, float* lse,
+                 float* dq_acc, int batch, int n, int heads, int headdim, int block_size, int mode,
+                 dfa_stream_t stream) {
+  if (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) return DFA_EINVAL;
+  return forward_impl(mode, q, k, v, out, lse, dq_acc, batch, n, heads, headdim,
+                      mode == MODE_CAUSAL ? 1 : block_size, static_cast<cudaStream_t>(stream));
 }
 
 int dfa_bwd_preprocess(const void* out, const void* dout, float* delta, float* dq_acc, int batch,

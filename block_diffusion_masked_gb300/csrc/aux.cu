@@ -3,8 +3,8 @@
 // preprocess: D_i = sum_d dout_i,d * out_i,d for every row (the term of the
 // softmax gradient that "FlashAttention: Exact Attention Without
 // Materialization", section 4.5, recomputes instead of storing P), and zero
-// the float32 dQ accumulator.  One warp per (batch, position, head) row; the
-// row's out/dout bytes are read once, coalesced.
+// the float32 dQ accumulator unless the forward did.  The rows' out/dout
+// bytes are read once, coalesced, 16 bytes per lane.
 //
 // convert: dq = bf16(dq_acc), round to nearest even, 8 elements per thread.
 #include <cuda_bf16.h>
@@ -14,38 +14,69 @@
 
 namespace dfa {
 
+// Each lane reads 16 bytes of out and of dout (8 elements), D / 8 lanes per
+// row; a warp takes kUnroll row groups of consecutive positions of one
+// (batch, head) and issues all their loads before any reduction, so that
+// enough bytes are in flight to cover the memory latency.  Grid: x = chunks
+// of 8 * kRowsPerPass positions, y = (batch, head) pairs (strided when there
+// are more than the grid's y extent).  dq_acc may be null: then only D is
+// computed (the forward zeroed the accumulator).
 template <int D>
 __global__ void __launch_bounds__(256) dfa_bwd_preprocess_kernel(
     const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
-    float* __restrict__ delta, float* __restrict__ dq_acc, int B, int L, int H) {
-  constexpr int PER_LANE = D / 32;  // 2, 4 or 8 elements
-  const long long rows = static_cast<long long>(B) * L * H;
+    float* __restrict__ delta, float* __restrict__ dq_acc, int L, int H, int BH) {
+  constexpr int kLanesPerRow = D / 8;             // 8, 16 or 32
+  constexpr int kRowsPerGroup = 32 / kLanesPerRow;  // rows one warp load covers
+  constexpr int kUnroll = 4;
+  constexpr int kRowsPerPass = kRowsPerGroup * kUnroll;
   const int lane = threadIdx.x & 31;
-  const long long warps_total = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       r < rows; r += warps_total) {
-    const size_t base = static_cast<size_t>(r) * D + lane * PER_LANE;
-    float acc = 0.f;
+  const int sub = lane / kLanesPerRow;  // row of the group
+  const int col = (lane % kLanesPerRow) * 8;
+  const long long p0 =
+      (static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kRowsPerPass;
+  if (p0 >= L) return;  // warp-uniform
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    const int b = bh / H;
+    const int h = bh - b * H;
+    uint4 o[kUnroll], g[kUnroll];
 #pragma unroll
-    for (int e = 0; e < PER_LANE; e += 2) {
-      const __nv_bfloat162 o = *reinterpret_cast<const __nv_bfloat162*>(out + base + e);
-      const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(dout + base + e);
-      const float2 of = __bfloat1622float2(o);
-      const float2 gf = __bfloat1622float2(g);
-      acc = fmaf(of.x, gf.x, acc);
-      acc = fmaf(of.y, gf.y, acc);
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long pos = p0 + u * kRowsPerGroup + sub;
+      if (pos < L) {
+        const size_t base = ((static_cast<size_t>(b) * L + pos) * H + h) * D + col;
+        o[u] = *reinterpret_cast<const uint4*>(out + base);
+        g[u] = *reinterpret_cast<const uint4*>(dout + base);
+      } else {
+        o[u] = make_uint4(0u, 0u, 0u, 0u);
+        g[u] = o[u];
+      }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long pos = p0 + u * kRowsPerGroup + sub;
+      const uint32_t ow[4] = {o[u].x, o[u].y, o[u].z, o[u].w};
+      const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+      float acc = 0.f;
 #pragma unroll
-    for (int e = 0; e < PER_LANE; ++e) dq_acc[base + e] = 0.f;
-    if (lane == 0) {
-      // r enumerates (b, position, head); delta is laid out (b, head, position).
-      const long long h = r % H;
-      const long long bp = r / H;
-      const long long pos = bp % L;
-      const long long b = bp / L;
-      delta[(b * H + h) * L + pos] = acc;
+      for (int e = 0; e < 4; ++e) {
+        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+        acc = fmaf(of.x, gf.x, acc);
+        acc = fmaf(of.y, gf.y, acc);
+      }
+#pragma unroll
+      for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (pos < L) {
+        if (dq_acc != nullptr) {
+          float4* z = reinterpret_cast<float4*>(
+              dq_acc + ((static_cast<size_t>(b) * L + pos) * H + h) * D + col);
+          z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+          z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // delta is laid out (b, head, position)
+        if (lane % kLanesPerRow == 0) delta[static_cast<size_t>(bh) * L + pos] = acc;
+      }
     }
   }
 }
@@ -109,18 +140,24 @@ static int grid_for(long long work, int per_block) {
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* out, const __nv_bfloat16* dout,
                                   float* delta, float* dq_acc, int B, int L, int H, int d,
                                   cudaStream_t stream) {
-  const long long rows = static_cast<long long>(B) * L * H;
-  if (rows == 0) return cudaSuccess;
-  const int grid = grid_for(rows, 8);
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh == 0 || L == 0) return cudaSuccess;
+  if (bh > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // 8 warps of 1024 / d positions each per block
+  const long long per_block = 8192 / d;
+  const long long chunks = (L + per_block - 1) / per_block;
+  if (chunks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(chunks), static_cast<unsigned>(bh < 65535 ? bh : 65535));
+  const int BH = static_cast<int>(bh);
   switch (d) {
     case 64:
-      dfa_bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(out, dout, delta, dq_acc, B, L, H);
+      dfa_bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(out, dout, delta, dq_acc, L, H, BH);
       break;
     case 128:
-      dfa_bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(out, dout, delta, dq_acc, B, L, H);
+      dfa_bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(out, dout, delta, dq_acc, L, H, BH);
       break;
     case 256:
-      dfa_bwd_preprocess_kernel<256><<<grid, 256, 0, stream>>>(out, dout, delta, dq_acc, B, L, H);
+      dfa_bwd_preprocess_kernel<256><<<grid, 256, 0, stream>>>(out, dout, delta, dq_acc, L, H, BH);
       break;
     default:
       return cudaErrorInvalidValue;

@@ -11,6 +11,8 @@
 //
 // Warp roles (192 threads):
 //   warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t);
+//              on request they first zero their CTA's share of the
+//              backward's float32 dq accumulator;
 //   warp 4     TMA producer: Q once, then K/V tiles through a STAGES-deep ring;
 //   warp 5     MMA issuer: S = Q K^T into one of two TMEM score buffers,
 //              O += P V into a TMEM accumulator, both with tcgen05.mma.
@@ -206,6 +208,10 @@ __global__ void __launch_bounds__(192, 1) dfa_fwd_kernel(const __grid_constant__
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    // The backward's dq accumulator, if the caller asks for it, is zeroed
+    // here while the first scores are computed: this CTA's share of the
+    // stores, issued and left to drain.
+    if (p.zero_dst != nullptr) grid_zero16(p.zero_dst, p.zero_groups, threadIdx.x, 128);
     const int row = warp * 32 + lane;
     const int r = qs + row;  // row inside the half
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);

@@ -23,7 +23,8 @@
 // items, so the loads and S products of the next item overlap the merge and
 // stores of the current one.
 // Warps 0-7 softmax, warp 8 loads Q and K (and takes the items), warp 10
-// loads V, warp 9 issues the MMAs, warp 11 idle.  The load/MMA warpgroup
+// loads V, warp 9 issues the MMAs, warp 11 zeroes the backward's float32 dq
+// accumulator when the caller asks for it (otherwise idle).  The load/MMA warpgroup
 // hands registers to the softmax warpgroups (setmaxnreg): launched with 168
 // per thread, it drops to 56 and the softmax warpgroups rise to 224, which
 // keeps a row's 128 scores in registers.  256 * (224 - 168) == 128 * (168 -
@@ -287,6 +288,11 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       mma_commit(BAR(C::BAR_ALL));
     }
     __syncwarp();
+   } else if (p.zero_dst != nullptr) {
+    // Warp 11 zeroes the backward's dq accumulator, paced by the work counter
+    // so that the stores spread over the launch instead of competing with
+    // the first loads of every CTA.
+    zero_paced(p.zero_dst, p.zero_groups, p.sched, 2 * p.B * p.H * p.q_tiles, lane);
    }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");

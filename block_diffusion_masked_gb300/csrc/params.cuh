@@ -27,6 +27,10 @@ struct FwdParams {
   int group;         // (batch, head) pairs per scheduling group
   float scale_log2;  // softmax scale * log2(e)
   unsigned* sched;   // work counter of a persistent launch (see sched_next)
+  // Optional: the backward's float32 dq accumulator, zeroed by the forward
+  // launch alongside its tensor-core work (zero_groups 16-byte groups).
+  float4* zero_dst;
+  long long zero_groups;
 };
 
 struct BwdParams {

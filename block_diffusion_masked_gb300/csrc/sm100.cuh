@@ -446,6 +446,58 @@ __device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a, uint32_t b, 
                : "memory");
 }
 
+// Store 16 zero bytes with the streaming (evict-first) hint: the lines are not
+// read again by this kernel and should not push its operands out of L2.
+__device__ __forceinline__ void st_global_cs_zero16(void* ptr) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %1, %1, %1};" ::"l"(ptr), "r"(0u) : "memory");
+}
+
+// Zero `groups` 16-byte groups at `dst`, spread over every CTA of the grid:
+// the `nthreads` threads numbered `tid` of each CTA take groups
+// blockIdx.x * nthreads + tid, then every gridDim.x * nthreads further.
+__device__ __forceinline__ void grid_zero16(float4* dst, long long groups, int tid, int nthreads) {
+  const long long stride = static_cast<long long>(gridDim.x) * nthreads;
+  for (long long g = static_cast<long long>(blockIdx.x) * nthreads + tid; g < groups; g += stride)
+    st_global_cs_zero16(dst + g);
+}
+
+// One warp zeroes its CTA's grid-stride share of `groups` 16-byte groups
+// (as grid_zero16 with 32 threads), keeping pace with a persistent launch's
+// work counter: once `taken` of `items` items have been handed out, the
+// share is zeroed up to the fraction (taken + gridDim.x) / items.  Stores
+// only; a pause between batches ends when the counter moves or after 2 s
+// without movement, when the rest of the share is zeroed at once.
+__device__ __forceinline__ void zero_paced(float4* dst, long long groups, const unsigned* counter,
+                                           int items, int lane) {
+  const long long stride = static_cast<long long>(gridDim.x) * 32;
+  const long long base = static_cast<long long>(blockIdx.x) * 32;
+  const long long iters = base < groups ? (groups - base + stride - 1) / stride : 0;
+  long long done = 0;
+  unsigned long long t_moved = global_timer_ns();
+  while (done < iters) {
+    unsigned taken = 0;
+    if (lane == 0) taken = *reinterpret_cast<const volatile unsigned*>(counter);
+    taken = __shfl_sync(0xffffffffu, taken, 0);
+    long long t = static_cast<long long>(taken) + gridDim.x;
+    if (t > items) t = items;
+    long long target = iters * t / items;
+    if (target <= done) {
+      unsigned long long now = global_timer_ns();
+      now = __shfl_sync(0xffffffffu, now, 0);
+      if (now - t_moved < kWaitLimitNs) {
+        __nanosleep(500);
+        continue;
+      }
+      target = iters;
+    }
+    for (; done < target; ++done) {
+      const long long g = base + lane + done * stride;
+      if (g < groups) st_global_cs_zero16(dst + g);
+    }
+    t_moved = __shfl_sync(0xffffffffu, global_timer_ns(), 0);
+  }
+}
+
 __device__ __forceinline__ void red_add_f32(float* ptr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(ptr), "f"(v) : "memory");
 }

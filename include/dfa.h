@@ -115,19 +115,28 @@ int dfa_causal_backward(const void *q, const void *k, const void *v, const void 
                         int batch, int seqlen, int heads, int headdim, dfa_stream_t stream);
 
 /*
- * The three steps dfa_backward runs, for callers that own the scratch or
- * time the steps one by one.  `mode` is DFA_MODE_DIFFUSION or
+ * The forward and the three steps dfa_backward runs, for callers that own
+ * the scratch or time the steps one by one.  `mode` is DFA_MODE_DIFFUSION or
  * DFA_MODE_CAUSAL; in the causal mode (batch, n) describe the paired view
  * (batch samples of two consecutive sequences of length n), block_size is
  * ignored and lse is laid out (2*batch, heads, n) as dfa_causal_forward
  * writes it.  delta is always (batch, heads, 2n).
+ *   dfa_fwd_main: dfa_forward (or, in the causal mode, dfa_causal_forward
+ *     on the paired view); if dq_acc is not NULL the same launch also sets
+ *     dq_acc (float32, shape of q) to zero, with stores that otherwise idle
+ *     warps issue alongside the tensor-core work, so that the backward needs
+ *     no separate pass over it.
  *   dfa_bwd_preprocess: delta = rowsum(dout * out), float32 (batch, heads, 2n);
- *     dq_acc (float32, shape of q) set to zero.
+ *     dq_acc (float32, shape of q) set to zero unless dq_acc is NULL (then
+ *     the caller zeroed it, e.g. through dfa_fwd_main).
  *   dfa_bwd_main: the tensor-core backward: writes dk, dv (bf16) and adds
  *     dq (already scaled) into dq_acc with float32 atomics.
  *   dfa_bwd_dq_convert: dq = bf16(dq_acc), round to nearest even.
  * dq_acc and delta are device buffers the caller allocated (16-byte aligned).
  */
+int dfa_fwd_main(const void *q, const void *k, const void *v, void *out, float *lse,
+                 float *dq_acc, int batch, int n, int heads, int headdim, int block_size,
+                 int mode, dfa_stream_t stream);
 int dfa_bwd_preprocess(const void *out, const void *dout, float *delta, float *dq_acc,
                        int batch, int n, int heads, int headdim, dfa_stream_t stream);
 int dfa_bwd_main(const void *q, const void *k, const void *v, const void *dout,

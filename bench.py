@@ -248,15 +248,29 @@ def run_gpu(args, w, rank, world):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def timed(step, K, per_kernel=True):
+    def timed(step, K):
+        # K steps back to back, events only around the whole region: an event
+        # between two launches would stop the second from being launched
+        # while the first is still running (chained launches).
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        start.record(stream)
+        for _ in range(K):
+            step()
+        end.record(stream)
+        barrier()
+        return start.elapsed_time(end)
+
+    def per_kernel(step, K):
+        # A separate pass with events between the launches: each kernel's
+        # own duration (launch gaps included, overlap excluded).
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
         barrier()
         for i in range(K):
-            step(evs[i] if per_kernel else None)
+            step(evs[i])
         barrier()
-        total = evs[0][0].elapsed_time(evs[-1][4])
         parts = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])
-        return total, parts.mean(axis=0)
+        return parts.mean(axis=0)
 
     for _ in range(args.warmup):
         diff_step()
@@ -266,9 +280,11 @@ def run_gpu(args, w, rank, world):
         raise RuntimeError("device status set during warm-up")
 
     with ClockSampler(dev.index) as clk:
-        t_ms, parts = timed(diff_step, args.steps)
+        t_ms = timed(diff_step, args.steps)
     clocks = clk.summary()
-    tc_ms, parts_c = timed(causal_step, args.steps)
+    tc_ms = timed(causal_step, args.steps)
+    parts = per_kernel(diff_step, args.steps)
+    parts_c = per_kernel(causal_step, args.steps)
     if binding.dfa_status() != 0:
         raise RuntimeError("device status set during the timed region")
 

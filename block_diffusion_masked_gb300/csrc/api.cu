@@ -177,6 +177,7 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   if ((rc = make_map(&p.tm_q, q, B, n, H, d, ts.fwd_bm))) return rc;
   if ((rc = make_map(&p.tm_k, k, B, n, H, d, ts.fwd_bn))) return rc;
   if ((rc = make_map(&p.tm_v, v, B, n, H, d, ts.fwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_o, out, B, n, H, d, ts.fwd_bm))) return rc;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.status = ds->status;

@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(256) dfa_bwd_preprocess_kernel(
   constexpr int kRowsPerGroup = 32 / kLanesPerRow;  // rows one warp load covers
   constexpr int kUnroll = 4;
   constexpr int kRowsPerPass = kRowsPerGroup * kUnroll;
+  grid_dependency_wait();  // out and dout come from the kernels before this one
   const int lane = threadIdx.x & 31;
   const int sub = lane / kLanesPerRow;  // row of the group
   const int col = (lane % kLanesPerRow) * 8;
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(256) dfa_bwd_preprocess_kernel(
 __global__ void __launch_bounds__(256) dfa_dq_convert_kernel(const float4* __restrict__ src,
                                                              uint4* __restrict__ dst,
                                                              long long groups) {
+  grid_dependency_wait();  // dq_acc comes from the kernel before this one
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
        g += stride) {
@@ -151,14 +153,14 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16* out, const __nv_bfloat16*
   const int BH = static_cast<int>(bh);
   switch (d) {
     case 64:
-      dfa_bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(out, dout, delta, dq_acc, L, H, BH);
-      break;
+      return launch_chained(dfa_bwd_preprocess_kernel<64>, grid, dim3(256), 0, stream, out, dout,
+                            delta, dq_acc, L, H, BH);
     case 128:
-      dfa_bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(out, dout, delta, dq_acc, L, H, BH);
-      break;
+      return launch_chained(dfa_bwd_preprocess_kernel<128>, grid, dim3(256), 0, stream, out, dout,
+                            delta, dq_acc, L, H, BH);
     case 256:
-      dfa_bwd_preprocess_kernel<256><<<grid, 256, 0, stream>>>(out, dout, delta, dq_acc, L, H, BH);
-      break;
+      return launch_chained(dfa_bwd_preprocess_kernel<256>, grid, dim3(256), 0, stream, out, dout,
+                            delta, dq_acc, L, H, BH);
     default:
       return cudaErrorInvalidValue;
   }
@@ -169,9 +171,9 @@ cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, long long 
                               cudaStream_t stream) {
   if (count == 0) return cudaSuccess;
   const long long groups = count / 8;  // count is a multiple of 64 (headdim)
-  dfa_dq_convert_kernel<<<grid_for(groups, 256), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint4*>(dq), groups);
-  return cudaGetLastError();
+  return launch_chained(dfa_dq_convert_kernel, dim3(grid_for(groups, 256)), dim3(256), 0, stream,
+                        reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint4*>(dq),
+                        groups);
 }
 
 }  // namespace dfa

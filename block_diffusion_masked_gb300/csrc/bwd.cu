@@ -73,8 +73,8 @@ struct BwdCfg {
     BAR_ALL = BAR_ITEMFULL + 4,       // every MMA done (TMEM release)
     NUM_BARS = BAR_ALL + 1
   };
-  static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 item indices
-  static constexpr int kOffTmemSlot = kOffItem + 16;
+  static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 decoded items (BwdItem)
+  static constexpr int kOffTmemSlot = kOffItem + 4 * 64;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
   static constexpr int kTmemS = 0;          // S[b] at b * BMQ; dQ of the tile after S is read
@@ -92,8 +92,11 @@ struct BwdCfg {
 };
 
 // One work item: key tile and the query tiles that see it (at most two
-// segments, kept in scalars so that nothing is indexed dynamically).
+// segments, kept in scalars so that nothing is indexed dynamically).  The
+// producer decodes each item once and publishes the decoded form to the other
+// roles through a ring in shared memory; v < 0 means no work is left.
 struct BwdItem {
+  int v;
   WorkItem wi;
   int n0, ntiles;
   int half0, rule0, tb0, half1, rule1, tb1;
@@ -101,9 +104,13 @@ struct BwdItem {
   __device__ __forceinline__ int qhalf(int t) const { return t < n0 ? half0 : half1; }
 };
 
+static_assert(sizeof(BwdItem) <= 64, "item ring slot");
+
 template <int BMQ, int BN>
 __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   BwdItem it;
+  it.v = v;
+  if (v < 0) return it;
   it.wi = bwd_work(v, p.mode, p.B, p.H, p.k_tiles, p.group);
   Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
   const int nseg = bwd_segments(p.mode, p.n, p.bs, BMQ, BN, it.wi.half, it.wi.tile, seg);
@@ -130,7 +137,9 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
-  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::kOffItem);
+  // Slot s of the item ring; written by the producer before it arrives on
+  // ITEMFULL[s] (release), read by the other roles after their wait (acquire).
+  auto ring = [&](int s) { return reinterpret_cast<BwdItem*>(smem + C::kOffItem + 64 * s); };
   const AbortFlag ab{abort_flag, p.status};
   const size_t L = 2 * static_cast<size_t>(p.n);
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
@@ -163,6 +172,12 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kOffTmemSlot);
+  // The prologue above touches only shared memory and TMEM.  Global memory
+  // (inputs, outputs, the work counter) waits for the stream's previous
+  // kernel; the next kernel may be launched now (its CTAs take each SM as
+  // this kernel's CTA there exits).
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   // Items are numbered k = 0, 1, ... in the order this CTA takes them, query
   // tiles g = 0, 1, ... over all of the CTA's items; every barrier phase
@@ -230,14 +245,14 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     };
     while (ok) {
       int v = -1;
+      if (lane == 0) v = sched_next(p.sched, p.items);
+      v = __shfl_sync(0xffffffffu, v, 0);
+      const BwdItem it = bwd_item<BMQ, BN>(p, v);
       if (lane == 0) {
-        v = sched_next(p.sched, p.items);
-        item_ring[k & 3] = v;
+        *ring(k & 3) = it;
         mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
       }
-      v = __shfl_sync(0xffffffffu, v, 0);
       if (v < 0) break;
-      const BwdItem it = bwd_item<BMQ, BN>(p, v);
       // The first query tiles only need stages the current item frees before
       // its last products, so they go ahead of the K / V load, which waits
       // for the whole item.
@@ -336,9 +351,8 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
 
       while (ok) {
         if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
-        const int v = item_ring[k & 3];
-        if (v < 0) break;
-        const BwdItem it = bwd_item<BMQ, BN>(p, v);
+        const BwdItem it = *ring(k & 3);
+        if (it.v < 0) break;
         if (!(ok = mbar_wait(BAR(C::BAR_KV), k & 1, ab))) break;
         for (int i = 0; i < it.ntiles && ok; ++i) {
           const int gg = g + i;
@@ -474,9 +488,8 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     int g = 0, k = 0;
     while (ok) {
       if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
-      const int v = item_ring[k & 3];
-      if (v < 0) break;
-      const BwdItem it = bwd_item<BMQ, BN>(p, v);
+      const BwdItem it = *ring(k & 3);
+      if (it.v < 0) break;
       const int ks = it.wi.tile * BN;
       const int j = ks + row;  // key inside its half
       // Query rows that see key j, per segment of the item: computed once,
@@ -585,8 +598,8 @@ static cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   BwdParams q = p;
   q.items = static_cast<int>(items);
   const long long grid = items < sms ? items : sms;
-  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(q);
-  return cudaGetLastError();
+  return launch_chained(kern, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads), C::kSmemBytes,
+                        stream, q);
 }
 
 cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream) {

@@ -110,8 +110,8 @@ struct Bwd2Cfg {
     BAR_ALL = BAR_ITEMFULL + 4,         // every MMA of the CTA done
     NUM_BARS = BAR_ALL + 1
   };
-  static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 item indices
-  static constexpr int kOffTmemSlot = kOffItem + 16;
+  static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 decoded items (Bwd2Item)
+  static constexpr int kOffTmemSlot = kOffItem + 4 * 64;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
   static constexpr int kTmemS = 0;
@@ -126,8 +126,11 @@ struct Bwd2Cfg {
 
 // One work item: key tile, head-dim half and the query tiles that see it
 // (at most two segments, kept in scalars so that nothing is indexed
-// dynamically).
+// dynamically).  The producer decodes each item once and publishes the
+// decoded form to the other roles through a ring in shared memory; v < 0
+// means no work is left.
 struct Bwd2Item {
+  int v;
   WorkItem wi;
   int dh;
   int n0, ntiles;
@@ -136,9 +139,13 @@ struct Bwd2Item {
   __device__ __forceinline__ int qhalf(int t) const { return t < n0 ? half0 : half1; }
 };
 
+static_assert(sizeof(Bwd2Item) <= 64, "item ring slot");
+
 template <int NDH, int BMQ, int BN>
 __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   Bwd2Item it;
+  it.v = v;
+  if (v < 0) return it;
   it.dh = v % NDH;
   it.wi = bwd_work(v / NDH, p.mode, p.B, p.H, p.k_tiles, p.group);
   Segment seg[2] = {};
@@ -170,7 +177,9 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
-  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::kOffItem);
+  // Slot s of the item ring; written by the producer before it arrives on
+  // ITEMFULL[s] (release), read by the other roles after their wait (acquire).
+  auto ring = [&](int s) { return reinterpret_cast<Bwd2Item*>(smem + C::kOffItem + 64 * s); };
   const AbortFlag ab{abort_flag, p.status};
   const size_t L = 2 * static_cast<size_t>(p.n);
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
@@ -203,6 +212,12 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kOffTmemSlot);
+  // The prologue above touches only shared memory and TMEM.  Global memory
+  // (inputs, outputs, the work counter) waits for the stream's previous
+  // kernel; the next kernel may be launched now (its CTAs take each SM as
+  // this kernel's CTA there exits).
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   // Items are numbered k = 0, 1, ... in the order this CTA takes them, query
   // tiles g = 0, 1, ... over all of the CTA's items; every barrier phase
@@ -270,14 +285,14 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
     };
     while (ok) {
       int v = -1;
+      if (lane == 0) v = sched_next(p.sched, p.items);
+      v = __shfl_sync(0xffffffffu, v, 0);
+      const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
       if (lane == 0) {
-        v = sched_next(p.sched, p.items);
-        item_ring[k & 3] = v;
+        *ring(k & 3) = it;
         mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
       }
-      v = __shfl_sync(0xffffffffu, v, 0);
       if (v < 0) break;
-      const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
       // K / V buffer `kvs` was last used by item k - KVBUF.  With one buffer
       // the first query tiles only need stages that the current item frees
       // before its last product, so they go ahead of the K / V load, which
@@ -341,9 +356,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         const uint64_t dO_kmaj = sdesc_sw128(sbase + C::kOffDO, 16, 1024);
         while (ok) {
           if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
-          const int v = item_ring[k & 3];
-          if (v < 0) break;
-          const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
+          const Bwd2Item it = *ring(k & 3);
+          if (it.v < 0) break;
           const int kvs = k % C::KVBUF;
           const uint64_t dK_kmaj = adv(dK_kmaj0, kvs * C::kKVBytes);
           const uint64_t dV_kmaj = adv(dV_kmaj0, kvs * C::kKVBytes);
@@ -380,9 +394,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         const uint64_t dDS_mn = sdesc_sw128(sbase + C::kOffDS, BN * 128, 1024);
         while (ok) {
           if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
-          const int v = item_ring[k & 3];
-          if (v < 0) break;
-          const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
+          const Bwd2Item it = *ring(k & 3);
+          if (it.v < 0) break;
           // The head-dim half dh starts at 64-wide chunk 2 dh of K, Q and dO.
           const uint64_t dK_mn =
               sdesc_sw128(sbase + C::kOffK + (k % C::KVBUF) * C::kKVBytes + it.dh * 2 * (BN * 128),
@@ -505,9 +518,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
     int g = 0, k = 0;
     while (ok) {
       if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
-      const int v = item_ring[k & 3];
-      if (v < 0) break;
-      const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
+      const Bwd2Item it = *ring(k & 3);
+      if (it.v < 0) break;
       const int ks = it.wi.tile * BN;
       const int j = ks + row;  // key inside its half
       // Query rows that see key j, per segment of the item: computed once,
@@ -686,8 +698,8 @@ static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
   BwdParams q = p;
   q.items = static_cast<int>(items);
   const long long grid = items < sms ? items : sms;
-  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(q);
-  return cudaGetLastError();
+  return launch_chained(kern, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads), C::kSmemBytes,
+                        stream, q);
 }
 
 cudaError_t launch_backward_d128(const BwdParams& p, cudaStream_t stream) {

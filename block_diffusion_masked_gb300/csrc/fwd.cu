@@ -110,6 +110,9 @@ __global__ void __launch_bounds__(192, 1) dfa_fwd_kernel(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kOffTmemSlot);
+  // The prologue above touches only shared memory and TMEM; global memory
+  // waits for the stream's previous kernel.
+  grid_dependency_wait();
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -352,8 +355,8 @@ static cudaError_t launch_fwd_impl(const FwdParams& p, cudaStream_t stream) {
   const long long blocks = 2LL * p.B * p.H * p.q_tiles;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(kern, dim3(static_cast<unsigned>(blocks)), dim3(C::kThreads),
+                        C::kSmemBytes, stream, p);
 }
 
 cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream) {

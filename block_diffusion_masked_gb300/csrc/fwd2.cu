@@ -23,8 +23,9 @@
 // items, so the loads and S products of the next item overlap the merge and
 // stores of the current one.
 // Warps 0-7 softmax, warp 8 loads Q and K (and takes the items), warp 10
-// loads V, warp 9 issues the MMAs, warp 11 zeroes the backward's float32 dq
-// accumulator when the caller asks for it (otherwise idle).  The load/MMA warpgroup
+// loads V, warp 9 issues the MMAs, warp 11 stores the out tiles (staged by
+// the softmax warpgroups in the item's query buffer) with TMA and zeroes the
+// backward's float32 dq accumulator when the caller asks for it.  The load/MMA warpgroup
 // hands registers to the softmax warpgroups (setmaxnreg): launched with 168
 // per thread, it drops to 56 and the softmax warpgroups rise to 224, which
 // keeps a row's 128 scores in registers.  256 * (224 - 168) == 128 * (168 -
@@ -61,12 +62,13 @@ struct Fwd2Cfg {
     BAR_ITEMDONE = BAR_PFULL + 2,     // every product of an item complete
     BAR_OFREE = BAR_ITEMDONE + 1,     // both O accumulators read out
     BAR_XCHG = BAR_OFREE + 1,         // both warpgroups' (m, l) in shared memory
-    BAR_ITEMFULL = BAR_XCHG + 1,      // [4] item index published
-    BAR_ALL = BAR_ITEMFULL + 4,       // every MMA of the CTA complete
+    BAR_ITEMFULL = BAR_XCHG + 1,      // [4] item published
+    BAR_OSTAGED = BAR_ITEMFULL + 4,   // [2] per query buffer: the item's out tile staged in it
+    BAR_ALL = BAR_OSTAGED + 2,        // every MMA of the CTA complete
     NUM_BARS = BAR_ALL + 1
   };
-  static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 item indices
-  static constexpr int kOffTmemSlot = kOffItem + 16;
+  static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 decoded items (ItemGeom)
+  static constexpr int kOffTmemSlot = kOffItem + 4 * 64;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
   static constexpr int kTmemS = 0;       // S[w] at w * BN; P[w] in its first BN / 2 columns
@@ -79,8 +81,11 @@ struct Fwd2Cfg {
 };
 
 // One work item: query tile and the key tiles it visits (at most two
-// segments, kept in scalars so that nothing is indexed dynamically).
+// segments, kept in scalars so that nothing is indexed dynamically).  The
+// producer decodes each item once and publishes the decoded form to the other
+// roles through a ring in shared memory; item < 0 means no work is left.
 struct ItemGeom {
+  int item;
   WorkItem wi;
   int n0, ntiles, qs;
   int half0, rule0, tb0, half1, rule1, tb1;
@@ -88,8 +93,12 @@ struct ItemGeom {
   __device__ __forceinline__ int khalf(int j) const { return j < n0 ? half0 : half1; }
 };
 
+static_assert(sizeof(ItemGeom) <= 64, "item ring slot");
+
 __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, int bn,
                                           ItemGeom* g) {
+  g->item = item;
+  if (item < 0) return;
   g->wi = fwd_work(item, p.mode, p.B, p.H, p.q_tiles, p.group);
   Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
   const int nseg = fwd_segments(p.mode, p.n, p.bs, bm, bn, g->wi.half, g->wi.tile, seg);
@@ -116,7 +125,9 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
-  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::kOffItem);
+  // Slot s of the item ring; written by warp 8 before it arrives on
+  // ITEMFULL[s] (release), read by the other roles after their wait (acquire).
+  auto ring = [&](int s) { return reinterpret_cast<ItemGeom*>(smem + C::kOffItem + 64 * s); };
   const AbortFlag ab{abort_flag, p.status};
   const int num_items = 2 * p.B * p.H * p.q_tiles;
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
@@ -138,6 +149,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     mbar_init(BAR(C::BAR_OFREE), 256);
     mbar_init(BAR(C::BAR_XCHG), 256);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
+    mbar_init(BAR(C::BAR_OSTAGED + 0), 256);
+    mbar_init(BAR(C::BAR_OSTAGED + 1), 256);
     mbar_init(BAR(C::BAR_ALL), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -150,6 +163,12 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kOffTmemSlot);
+  // The prologue above touches only shared memory and TMEM.  Global memory
+  // (inputs, outputs, the work counter) waits for the stream's previous
+  // kernel; the next kernel may be launched now (its CTAs take each SM as
+  // this kernel's CTA there exits).
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp >= 8) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
@@ -167,25 +186,23 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       int g = 0;  // K/V ring position across items
       int k = 0;
       for (; ok; ++k) {
-        int item;
+        ItemGeom ig;
         if (kload) {
-          // Items come from the work counter and are published to the other
-          // roles through slot k % 4 of the item ring.  The slot last held
-          // item k - 4, whose readers are all done: this loader has already
-          // waited for item k - 3's products, which the MMA warp issues only
-          // after the softmax warpgroups have finished item k - 4 (and the V
-          // loader read it before loading item k - 4's last V tile, which
-          // those products needed).
-          item = sched_next(p.sched, num_items);
-          item_ring[k & 3] = item;
+          // Items come from the work counter and are published, decoded, to
+          // the other roles through slot k % 4 of the item ring.  The slot
+          // last held item k - 4, whose readers are all done: this loader has
+          // already waited for item k - 3's products, which the MMA warp
+          // issues only after the softmax warpgroups have finished item k - 4
+          // (and the V loader read it before loading item k - 4's last V
+          // tile, which those products needed).
+          item_geom(p, sched_next(p.sched, num_items), BM, BN, &ig);
+          *ring(k & 3) = ig;
           mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
         } else {
           if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
-          item = item_ring[k & 3];
+          ig = *ring(k & 3);
         }
-        if (item < 0) break;
-        ItemGeom ig;
-        item_geom(p, item, BM, BN, &ig);
+        if (ig.item < 0) break;
         if (kload) {
           const int qb = k & 1;
           if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_QEMPTY + qb), ((k >> 1) - 1) & 1, ab))) break;
@@ -233,10 +250,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       int k = 0;
       for (; ok; ++k) {
         if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
-        const int item = item_ring[k & 3];
-        if (item < 0) break;
-        ItemGeom ig;
-        item_geom(p, item, BM, BN, &ig);
+        const ItemGeom ig = *ring(k & 3);
+        if (ig.item < 0) break;
         const int qb = k & 1;
         if (!(ok = mbar_wait(BAR(C::BAR_QFULL + qb), (k >> 1) & 1, ab))) break;
         tc_fence_after();
@@ -279,7 +294,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
           if (j + 2 < ig.ntiles) ok = issue_s(j + 2);
         }
         if (!ok) break;
-        mma_commit(BAR(C::BAR_QEMPTY + qb));
+        // The query buffer is released by warp 11, once the item's out tile,
+        // staged in it, has been stored.
         mma_commit(BAR(C::BAR_ITEMDONE));
         g += ig.ntiles;
         cnt[0] += (ig.ntiles + 1) >> 1;
@@ -288,11 +304,45 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       mma_commit(BAR(C::BAR_ALL));
     }
     __syncwarp();
-   } else if (p.zero_dst != nullptr) {
-    // Warp 11 zeroes the backward's dq accumulator, paced by the work counter
-    // so that the stores spread over the launch instead of competing with
-    // the first loads of every CTA.
-    zero_paced(p.zero_dst, p.zero_groups, p.sched, 2 * p.B * p.H * p.q_tiles, lane);
+   } else {
+    // ------------------------------------------------------------ out stores
+    // Warp 11 stores each item's out tile, which the softmax warpgroups stage
+    // (bf16, 128-byte swizzled) in the item's query buffer, with TMA, and
+    // then hands the buffer back to the producer.  Between items it zeroes
+    // the backward's dq accumulator when asked, paced by the work counter so
+    // that the stores spread over the launch.
+    // Ring slots and staging barriers cannot run two phases ahead of this
+    // warp: the producer publishes item k + 4, and the softmax warpgroups
+    // stage item k + 2, only after this warp has released item k's buffer.
+    ZeroShare zs;
+    if (p.zero_dst != nullptr) zs.init(p.zero_dst, p.zero_groups);
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int qb = k & 1;
+      if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
+      const ItemGeom ig = *ring(k & 3);
+      if (ig.item < 0) break;
+      if (!(ok = mbar_wait_warp(BAR(C::BAR_OSTAGED + qb), (k >> 1) & 1, ab))) break;
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_store_5d(&p.tm_o, sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, 64 * c,
+                       ig.wi.h, ig.qs, ig.wi.half, ig.wi.b);
+        bulk_commit_group();
+        bulk_wait_read_all();
+        mbar_arrive(BAR(C::BAR_QEMPTY + qb));
+      }
+      __syncwarp();
+      if (p.zero_dst != nullptr) {
+        unsigned taken = 0;
+        if (lane == 0) taken = *reinterpret_cast<const volatile unsigned*>(p.sched);
+        taken = __shfl_sync(0xffffffffu, taken, 0);
+        zs.upto(static_cast<long long>(taken) + gridDim.x, num_items, lane);
+      }
+    }
+    if (p.zero_dst != nullptr) zs.upto(1, 1, lane);
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
    }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
@@ -303,15 +353,78 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     const uint32_t s_col = t_lane + C::kTmemS + w * BN;
     const uint32_t o_col = t_lane + C::kTmemO + w * D;
     const float sl2 = p.scale_log2;
+    // ---------------------------------------------------------- merge
+    // Item kk (sample b, head h, half, query tile at qs) ends: the two
+    // warpgroups' partial states are combined with the online-softmax rule.
+    auto merge = [&](int kk, int b, int h, int half, int qs, float m_ref,
+                     float l_run) -> bool {
+      float2* ml = reinterpret_cast<float2*>(smem + C::kOffML) + (kk & 1) * 2 * BM;
+      ml[w * BM + row] = make_float2(m_ref, l_run);
+      mbar_arrive(BAR(C::BAR_XCHG));
+      if (!mbar_wait_warp(BAR(C::BAR_ITEMDONE), kk & 1, ab)) return false;
+      if (!mbar_wait_warp(BAR(C::BAR_XCHG), kk & 1, ab)) return false;
+      tc_fence_after();
+      const float2 ma = ml[row];       // warpgroup 0
+      const float2 mb = ml[BM + row];  // warpgroup 1
+      const float m = fmaxf(ma.x, mb.x);
+      const float fa = ma.y > 0.f ? ex2_approx(ma.x - m) : 0.f;
+      const float fb = mb.y > 0.f ? ex2_approx(mb.x - m) : 0.f;
+      const float lsum = ma.y * fa + mb.y * fb;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const int r = qs + row;
+      // The out tile goes, as bf16, into this item's query buffer (free: the
+      // item's last product has completed) in the 128-byte-swizzled layout of
+      // a TMA box, for warp 11 to store; rows past the end of the half are
+      // dropped by the copy.  Warpgroup w stages head dims
+      // [w * D / 2, (w + 1) * D / 2).
+      const uint32_t stage = sbase + C::kOffQ + (kk & 1) * C::kQBytes;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = w * (D / 2) + 32 * c;
+        uint32_t oa[32], ob[32];
+        tmem_ld32(t_lane + C::kTmemO + col, oa);
+        tmem_ld32(t_lane + C::kTmemO + D + col, ob);
+        tmem_wait_ld();
+        tmem_pin<32>(oa);
+        tmem_pin<32>(ob);
+#pragma unroll
+        for (int gq = 0; gq < 4; ++gq) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float v2[2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int q8 = gq * 8 + 2 * e + h2;
+              const float x = (fa > 0.f ? __uint_as_float(oa[q8]) * fa : 0.f) +
+                              (fb > 0.f ? __uint_as_float(ob[q8]) * fb : 0.f);
+              v2[h2] = x * inv;
+            }
+            wv[e] = pack_bf16x2(v2[0], v2[1]);
+          }
+          const int unit = col / 8 + gq;  // 16-byte unit of the row
+          st_shared_v4(stage + (unit >> 3) * (BM * 128) + row * 128 +
+                           (((unit & 7) ^ (row & 7)) << 4),
+                       wv[0], wv[1], wv[2], wv[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(BAR(C::BAR_OSTAGED + (kk & 1)));
+      if (r < p.n && w == 0) {
+        const float lse = lsum > 0.f ? (m + lg2_approx(lsum)) * 0.69314718055994531f : -INFINITY;
+        p.lse[lse_offset(p.mode, b, h, half, r, p.H, p.n)] = lse;
+      }
+      tc_fence_before();
+      mbar_arrive(BAR(C::BAR_OFREE));
+      return true;
+    };
     bool ok = true;
     int cnt = 0;  // tiles this warpgroup has processed so far
     int k = 0;
     for (; ok; ++k) {
       if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
-      const int item = item_ring[k & 3];
-      if (item < 0) break;
-      ItemGeom ig;
-      item_geom(p, item, BM, BN, &ig);
+      const ItemGeom ig = *ring(k & 3);
+      if (ig.item < 0) break;
       const int qs = ig.qs;
       const int r = qs + row;  // row inside the half
       // Keys visible to row r, per segment of the item: computed once, so a
@@ -412,61 +525,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         mbar_arrive(BAR(C::BAR_PFULL + w));
       }
       if (!ok) break;
-
-      // ---------------------------------------------------------- merge
-      float2* ml = reinterpret_cast<float2*>(smem + C::kOffML) + (k & 1) * 2 * BM;
-      ml[w * BM + row] = make_float2(m_ref, l_run);
-      mbar_arrive(BAR(C::BAR_XCHG));
-      if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMDONE), k & 1, ab))) break;
-      if (!(ok = mbar_wait_warp(BAR(C::BAR_XCHG), k & 1, ab))) break;
-      tc_fence_after();
-      const float2 a = ml[row];       // warpgroup 0
-      const float2 b = ml[BM + row];  // warpgroup 1
-      const float m = fmaxf(a.x, b.x);
-      const float fa = a.y > 0.f ? ex2_approx(a.x - m) : 0.f;
-      const float fb = b.y > 0.f ? ex2_approx(b.x - m) : 0.f;
-      const float lsum = a.y * fa + b.y * fb;
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      const size_t L = 2 * static_cast<size_t>(p.n);
-      const size_t pos = static_cast<size_t>(ig.wi.half) * p.n + r;
-      const bool valid = r < p.n;
-      __nv_bfloat16* orow = p.out + ((ig.wi.b * L + pos) * p.H + ig.wi.h) * D;
-      // warpgroup w writes head dims [w * D / 2, (w + 1) * D / 2)
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = w * (D / 2) + 32 * c;
-        uint32_t oa[32], ob[32];
-        tmem_ld32(t_lane + C::kTmemO + col, oa);
-        tmem_ld32(t_lane + C::kTmemO + D + col, ob);
-        tmem_wait_ld();
-        tmem_pin<32>(oa);
-        tmem_pin<32>(ob);
-        if (valid) {
-#pragma unroll
-          for (int gq = 0; gq < 4; ++gq) {
-            uint32_t wv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float v2[2];
-#pragma unroll
-              for (int h2 = 0; h2 < 2; ++h2) {
-                const int kk = gq * 8 + 2 * e + h2;
-                const float x = (fa > 0.f ? __uint_as_float(oa[kk]) * fa : 0.f) +
-                                (fb > 0.f ? __uint_as_float(ob[kk]) * fb : 0.f);
-                v2[h2] = x * inv;
-              }
-              wv[e] = pack_bf16x2(v2[0], v2[1]);
-            }
-            st_global_v4(orow + col + 8 * gq, wv[0], wv[1], wv[2], wv[3]);
-          }
-        }
-      }
-      if (valid && w == 0) {
-        const float lse = lsum > 0.f ? (m + lg2_approx(lsum)) * 0.69314718055994531f : -INFINITY;
-        p.lse[lse_offset(p.mode, ig.wi.b, ig.wi.h, ig.wi.half, r, p.H, p.n)] = lse;
-      }
-      tc_fence_before();
-      mbar_arrive(BAR(C::BAR_OFREE));
+      ok = merge(k, ig.wi.b, ig.wi.h, ig.wi.half, qs, m_ref, l_run);
     }
   }
 #undef BAR
@@ -497,8 +556,8 @@ static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
   const long long grid = items < sms ? items : sms;
-  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(kern, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads), C::kSmemBytes,
+                        stream, p);
 }
 
 cudaError_t launch_forward_two_warpgroups(const FwdParams& p, int headdim, cudaStream_t stream) {

@@ -19,6 +19,7 @@ struct FwdParams {
   CUtensorMap tm_q;  // box (64, 1, block_m, 1, 1)
   CUtensorMap tm_k;  // box (64, 1, block_n, 1, 1)
   CUtensorMap tm_v;  // box (64, 1, block_n, 1, 1)
+  CUtensorMap tm_o;  // out, box (64, 1, block_m, 1, 1) (persistent forward's stores)
   __nv_bfloat16* out;
   float* lse;
   unsigned* status;
@@ -72,6 +73,26 @@ __device__ __forceinline__ void sched_finish(unsigned* sched) {
   }
 }
 #endif
+
+// Launch with programmatic stream serialization: the kernel may be launched
+// while the kernel before it in the stream is still running, and waits for
+// it (griddepcontrol.wait, grid_dependency_wait) before touching global
+// memory, so that its launch and prologue overlap the predecessor's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // Launchers (one per translation unit).  Return a cudaError_t.
 cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream);

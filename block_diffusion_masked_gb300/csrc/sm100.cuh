@@ -123,6 +123,16 @@ __device__ __forceinline__ bool mbar_wait_limited(uint32_t bar, uint32_t parity,
 
 // ------------------------------------------------------------------ fences
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible; let the next grid in the
+// stream be launched (its CTAs are placed as this grid's CTAs exit).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -155,6 +165,14 @@ __device__ __forceinline__ void tma_reduce_add_5d(const CUtensorMap* map, uint32
                                                   int c1, int c2, int c3, int c4) {
   asm volatile(
       "cp.reduce.async.bulk.tensor.5d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group"
       " [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
       "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
       : "memory");
@@ -461,42 +479,28 @@ __device__ __forceinline__ void grid_zero16(float4* dst, long long groups, int t
     st_global_cs_zero16(dst + g);
 }
 
-// One warp zeroes its CTA's grid-stride share of `groups` 16-byte groups
-// (as grid_zero16 with 32 threads), keeping pace with a persistent launch's
-// work counter: once `taken` of `items` items have been handed out, the
-// share is zeroed up to the fraction (taken + gridDim.x) / items.  Stores
-// only; a pause between batches ends when the counter moves or after 2 s
-// without movement, when the rest of the share is zeroed at once.
-__device__ __forceinline__ void zero_paced(float4* dst, long long groups, const unsigned* counter,
-                                           int items, int lane) {
-  const long long stride = static_cast<long long>(gridDim.x) * 32;
-  const long long base = static_cast<long long>(blockIdx.x) * 32;
-  const long long iters = base < groups ? (groups - base + stride - 1) / stride : 0;
-  long long done = 0;
-  unsigned long long t_moved = global_timer_ns();
-  while (done < iters) {
-    unsigned taken = 0;
-    if (lane == 0) taken = *reinterpret_cast<const volatile unsigned*>(counter);
-    taken = __shfl_sync(0xffffffffu, taken, 0);
-    long long t = static_cast<long long>(taken) + gridDim.x;
-    if (t > items) t = items;
-    long long target = iters * t / items;
-    if (target <= done) {
-      unsigned long long now = global_timer_ns();
-      now = __shfl_sync(0xffffffffu, now, 0);
-      if (now - t_moved < kWaitLimitNs) {
-        __nanosleep(500);
-        continue;
-      }
-      target = iters;
-    }
+// One warp's zeroing of its CTA's grid-stride share of `groups` 16-byte
+// groups (the groups g = blockIdx.x * 32 + lane + i * gridDim.x * 32), done
+// in steps: upto(num, den) zeroes the share up to the fraction num / den.
+struct ZeroShare {
+  float4* dst;
+  long long groups, base, stride, iters, done;
+  __device__ __forceinline__ void init(float4* d, long long g) {
+    dst = d;
+    groups = g;
+    stride = static_cast<long long>(gridDim.x) * 32;
+    base = static_cast<long long>(blockIdx.x) * 32;
+    iters = base < groups ? (groups - base + stride - 1) / stride : 0;
+    done = 0;
+  }
+  __device__ __forceinline__ void upto(long long num, long long den, int lane) {
+    const long long target = num >= den ? iters : iters * num / den;
     for (; done < target; ++done) {
       const long long g = base + lane + done * stride;
       if (g < groups) st_global_cs_zero16(dst + g);
     }
-    t_moved = __shfl_sync(0xffffffffu, global_timer_ns(), 0);
   }
-}
+};
 
 __device__ __forceinline__ void red_add_f32(float* ptr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(ptr), "f"(v) : "memory");

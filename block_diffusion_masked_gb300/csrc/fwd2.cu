@@ -22,10 +22,11 @@
 // The K/V ring, the query double buffer and all barrier phases run on across
 // items, so the loads and S products of the next item overlap the merge and
 // stores of the current one.
-// Warps 0-7 softmax, warp 8 loads Q and K (and takes the items), warp 10
-// loads V, warp 9 issues the MMAs, warp 11 stores the out tiles (staged by
-// the softmax warpgroups in the item's query buffer) with TMA and zeroes the
-// backward's float32 dq accumulator when the caller asks for it.  The load/MMA warpgroup
+// Warps 0-7 softmax; warp 8 takes the items and loads Q, K and V; warp 10
+// issues S = Q K^T and warp 9 O += P V; warp 11 stores the out tiles (staged
+// by the softmax warpgroups in the item's query buffer) with TMA and zeroes
+// the backward's float32 dq accumulator when the caller asks for it.
+// The load/MMA warpgroup
 // hands registers to the softmax warpgroups (setmaxnreg): launched with 168
 // per thread, it drops to 56 and the softmax warpgroups rise to 224, which
 // keeps a row's 128 scores in registers.  256 * (224 - 168) == 128 * (168 -
@@ -59,7 +60,8 @@ struct Fwd2Cfg {
     BAR_VEMPTY = BAR_VFULL + STAGES,  // [STAGES]
     BAR_SFULL = BAR_VEMPTY + STAGES,  // [2] per warpgroup
     BAR_PFULL = BAR_SFULL + 2,        // [2] per warpgroup
-    BAR_ITEMDONE = BAR_PFULL + 2,     // every product of an item complete
+    BAR_PVDONE = BAR_PFULL + 2,       // [2] per warpgroup: its last P V complete
+    BAR_ITEMDONE = BAR_PVDONE + 2,    // every product of an item complete
     BAR_OFREE = BAR_ITEMDONE + 1,     // both O accumulators read out
     BAR_XCHG = BAR_OFREE + 1,         // both warpgroups' (m, l) in shared memory
     BAR_ITEMFULL = BAR_XCHG + 1,      // [4] item published
@@ -135,9 +137,10 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(C::BAR_QFULL + b), 1);
-      mbar_init(BAR(C::BAR_QEMPTY + b), 1);
       mbar_init(BAR(C::BAR_SFULL + b), 1);
       mbar_init(BAR(C::BAR_PFULL + b), 128);
+      mbar_init(BAR(C::BAR_QEMPTY + b), 1);
+      mbar_init(BAR(C::BAR_PVDONE + b), 1);
     }
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(BAR(C::BAR_KFULL + s), 1);
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
     mbar_init(BAR(C::BAR_OSTAGED + 0), 256);
     mbar_init(BAR(C::BAR_OSTAGED + 1), 256);
-    mbar_init(BAR(C::BAR_ALL), 1);
+    mbar_init(BAR(C::BAR_ALL), 2);  // both MMA-issuing warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -172,61 +175,70 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
 
   if (warp >= 8) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
-   if (warp == 8 || warp == 10) {
-    // ------------------------------------------------------------ producers
-    // Warp 8 takes items, publishes them and loads Q and the K ring; warp 10
-    // loads the V ring, so that K tiles (needed first, by S) are not held
-    // up behind the wait for a V slot.
+   if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    // Takes items, publishes them and loads Q and the K and V rings.  The V
+    // load of a tile is issued after the K load of the next one, so that a K
+    // tile (needed first, by S) never waits behind a V slot.
     if (lane == 0) {
-      const bool kload = warp == 8;
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       bool ok = true;
       int g = 0;  // K/V ring position across items
-      int k = 0;
-      for (; ok; ++k) {
-        ItemGeom ig;
-        if (kload) {
-          // Items come from the work counter and are published, decoded, to
-          // the other roles through slot k % 4 of the item ring.  The slot
-          // last held item k - 4, whose readers are all done: this loader has
-          // already waited for item k - 3's products, which the MMA warp
-          // issues only after the softmax warpgroups have finished item k - 4
-          // (and the V loader read it before loading item k - 4's last V
-          // tile, which those products needed).
-          item_geom(p, sched_next(p.sched, num_items), BM, BN, &ig);
-          *ring(k & 3) = ig;
-          mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
-        } else {
-          if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
-          ig = *ring(k & 3);
-        }
-        if (ig.item < 0) break;
-        if (kload) {
-          const int qb = k & 1;
-          if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_QEMPTY + qb), ((k >> 1) - 1) & 1, ab))) break;
-          mbar_arrive_expect_tx(BAR(C::BAR_QFULL + qb), C::kQBytes);
+      // The V tile still to be loaded: ring position vg (< 0: none) and its
+      // coordinates.
+      int vg = -1, vh = 0, vb = 0, vkt = 0, vkh = 0;
+      auto load_v = [&]() -> bool {
+        const int st = vg % STAGES;
+        const int round = vg / STAGES;
+        if (round > 0 && !mbar_wait(BAR(C::BAR_VEMPTY + st), (round - 1) & 1, ab)) return false;
+        mbar_arrive_expect_tx(BAR(C::BAR_VFULL + st), C::kKVBytes);
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, &p.tm_q,
-                        BAR(C::BAR_QFULL + qb), 64 * c, ig.wi.h, ig.qs, ig.wi.half, ig.wi.b);
-        }
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
+                      BAR(C::BAR_VFULL + st), 64 * c, vh, vkt * BN, vkh, vb);
+        vg = -1;
+        return true;
+      };
+      for (int k = 0; ok; ++k) {
+        // Items come from the work counter and are published, decoded, to the
+        // other roles through slot k % 4 of the item ring.  The slot last held
+        // item k - 4, whose readers are all done: for item k - 1's query
+        // buffer this loader has already waited until warp 11 stored item
+        // k - 3's out tile, which exists only after every role has read item
+        // k - 4's slot.
+        ItemGeom ig;
+        item_geom(p, sched_next(p.sched, num_items), BM, BN, &ig);
+        *ring(k & 3) = ig;
+        mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
+        if (ig.item < 0) break;
+        const int qb = k & 1;
+        if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_QEMPTY + qb), ((k >> 1) - 1) & 1, ab))) break;
+        mbar_arrive_expect_tx(BAR(C::BAR_QFULL + qb), C::kQBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, &p.tm_q,
+                      BAR(C::BAR_QFULL + qb), 64 * c, ig.wi.h, ig.qs, ig.wi.half, ig.wi.b);
         for (int j = 0; j < ig.ntiles; ++j, ++g) {
-          const int kt = ig.ktile(j);
-          const int kh = ig.khalf(j);
           const int st = g % STAGES;
           const int round = g / STAGES;
-          const uint32_t empty = BAR((kload ? C::BAR_KEMPTY : C::BAR_VEMPTY) + st);
-          const uint32_t full = BAR((kload ? C::BAR_KFULL : C::BAR_VFULL) + st);
-          if (round > 0 && !(ok = mbar_wait(empty, (round - 1) & 1, ab))) break;
-          mbar_arrive_expect_tx(full, C::kKVBytes);
+          if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_KEMPTY + st), (round - 1) & 1, ab))) break;
+          mbar_arrive_expect_tx(BAR(C::BAR_KFULL + st), C::kKVBytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_5d(sbase + (kload ? C::kOffK : C::kOffV) + st * C::kKVBytes + c * BN * 128,
-                        kload ? &p.tm_k : &p.tm_v, full, 64 * c, ig.wi.h, kt * BN, kh, ig.wi.b);
+            tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
+                        BAR(C::BAR_KFULL + st), 64 * c, ig.wi.h, ig.ktile(j) * BN, ig.khalf(j),
+                        ig.wi.b);
+          if (vg >= 0 && !(ok = load_v())) break;
+          vg = g;
+          vh = ig.wi.h;
+          vb = ig.wi.b;
+          vkt = ig.ktile(j);
+          vkh = ig.khalf(j);
         }
       }
+      if (ok && vg >= 0) ok = load_v();
       if (!ok) {
         // Unwinding: give the copies already issued time to land.
         const unsigned long long t0 = global_timer_ns();
@@ -235,9 +247,16 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       }
     }
     __syncwarp();
-   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+   } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 10 issues S = Q K^T, warp 9 O += P V.  Issued from one warp, the
+    // products slow down while the softmax warps that share its scheduler are
+    // busy; from two warps on two schedulers they keep the tensor pipe fed.
+    // The two streams meet only through barriers: S of a warpgroup's tile
+    // overwrites the TMEM columns its previous P was read from, so it waits
+    // for that P V (PVDONE); P V waits for the warpgroup's P (PFULL).
     if (lane == 0) {
+      const bool s_warp = warp == 10;
       constexpr uint32_t kIdS = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(BM, D, false, true);
       const uint64_t dQ = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
@@ -245,58 +264,55 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       const uint64_t dV = sdesc_sw128(sbase + C::kOffV, BN * 128, 1024);
       auto adv = [](uint64_t d, uint32_t bytes) { return d + static_cast<uint64_t>(bytes >> 4); };
       bool ok = true;
-      int g = 0;                // K/V ring position
-      int cnt[2] = {0, 0};      // tiles handed to each warpgroup so far
-      int k = 0;
-      for (; ok; ++k) {
+      int g = 0;            // K/V ring position
+      int cnt[2] = {0, 0};  // tiles handed to each warpgroup so far
+      for (int k = 0; ok; ++k) {
         if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
         const ItemGeom ig = *ring(k & 3);
         if (ig.item < 0) break;
         const int qb = k & 1;
-        if (!(ok = mbar_wait(BAR(C::BAR_QFULL + qb), (k >> 1) & 1, ab))) break;
-        tc_fence_after();
-        const int g0 = g;
-        auto issue_s = [&](int j) -> bool {
-          const int gg = g0 + j;
-          const int st = gg % STAGES;
-          if (!mbar_wait(BAR(C::BAR_KFULL + st), (gg / STAGES) & 1, ab)) return false;
-          tc_fence_after();
-          const int w = j & 1;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + C::kTmemS + w * BN,
-                   adv(dQ, qb * C::kQBytes + (kk >> 2) * (BM * 128) + (kk & 3) * 32),
-                   adv(dK, st * C::kKVBytes + (kk >> 2) * (BN * 128) + (kk & 3) * 32), kIdS,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(BAR(C::BAR_SFULL + w));
-          mma_commit(BAR(C::BAR_KEMPTY + st));
-          return true;
-        };
-        if (ig.ntiles > 0 && !(ok = issue_s(0))) break;
-        if (ig.ntiles > 1 && !(ok = issue_s(1))) break;
-        // The O accumulators still hold the previous item until it is read out.
-        if (k >= 1 && !(ok = mbar_wait(BAR(C::BAR_OFREE), (k - 1) & 1, ab))) break;
+        if (s_warp) {
+          if (!(ok = mbar_wait(BAR(C::BAR_QFULL + qb), (k >> 1) & 1, ab))) break;
+        } else {
+          // The O accumulators still hold the previous item until it is read out.
+          if (k >= 1 && !(ok = mbar_wait(BAR(C::BAR_OFREE), (k - 1) & 1, ab))) break;
+        }
         tc_fence_after();
         for (int j = 0; j < ig.ntiles && ok; ++j) {
           const int w = j & 1;
-          const int c = cnt[w] + (j >> 1);
-          const int gg = g0 + j;
+          const int c = cnt[w] + (j >> 1);  // this warpgroup's tile count
+          const int gg = g + j;
           const int st = gg % STAGES;
-          if (!(ok = mbar_wait(BAR(C::BAR_PFULL + w), c & 1, ab))) break;
-          if (!(ok = mbar_wait(BAR(C::BAR_VFULL + st), (gg / STAGES) & 1, ab))) break;
-          tc_fence_after();
+          if (s_warp) {
+            if (!(ok = mbar_wait(BAR(C::BAR_KFULL + st), (gg / STAGES) & 1, ab))) break;
+            if (c >= 1 && !(ok = mbar_wait(BAR(C::BAR_PVDONE + w), (c - 1) & 1, ab))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + C::kTmemO + w * D, tmem + C::kTmemS + w * BN + 8 * kk,
-                   adv(dV, st * C::kKVBytes + kk * 16 * 128), kIdPV, (j >= 2 || kk > 0) ? 1u : 0u);
-          mma_commit(BAR(C::BAR_VEMPTY + st));
-          // S of tile j+2 reuses the TMEM columns P of tile j was read from.
-          if (j + 2 < ig.ntiles) ok = issue_s(j + 2);
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + C::kTmemS + w * BN,
+                     adv(dQ, qb * C::kQBytes + (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                     adv(dK, st * C::kKVBytes + (kk >> 2) * (BN * 128) + (kk & 3) * 32), kIdS,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(BAR(C::BAR_SFULL + w));
+            mma_commit(BAR(C::BAR_KEMPTY + st));
+          } else {
+            if (!(ok = mbar_wait(BAR(C::BAR_PFULL + w), c & 1, ab))) break;
+            if (!(ok = mbar_wait(BAR(C::BAR_VFULL + st), (gg / STAGES) & 1, ab))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts(tmem + C::kTmemO + w * D, tmem + C::kTmemS + w * BN + 8 * kk,
+                     adv(dV, st * C::kKVBytes + kk * 16 * 128), kIdPV,
+                     (j >= 2 || kk > 0) ? 1u : 0u);
+            mma_commit(BAR(C::BAR_VEMPTY + st));
+            mma_commit(BAR(C::BAR_PVDONE + w));
+          }
         }
         if (!ok) break;
-        // The query buffer is released by warp 11, once the item's out tile,
-        // staged in it, has been stored.
-        mma_commit(BAR(C::BAR_ITEMDONE));
+        // Every S of the item precedes its P, so the last P V completes the
+        // item.  Its query buffer is released by warp 11, once the item's out
+        // tile, staged in it, has been stored.
+        if (!s_warp) mma_commit(BAR(C::BAR_ITEMDONE));
         g += ig.ntiles;
         cnt[0] += (ig.ntiles + 1) >> 1;
         cnt[1] += ig.ntiles >> 1;
@@ -374,7 +390,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       const int r = qs + row;
       // The out tile goes, as bf16, into this item's query buffer (free: the
       // item's last product has completed) in the 128-byte-swizzled layout of
-      // a TMA box, for warp 11 to store; rows past the end of the half are
+      // a TMA box, for the producer to store; rows past the end of the half are
       // dropped by the copy.  Warpgroup w stages head dims
       // [w * D / 2, (w + 1) * D / 2).
       const uint32_t stage = sbase + C::kOffQ + (kk & 1) * C::kQBytes;

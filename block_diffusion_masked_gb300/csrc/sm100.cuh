@@ -95,6 +95,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
   }
 }
 
+// As mbar_wait, running side() between polls: side() checks some other
+// barrier without blocking and does its work when that one is ready, so that
+// one thread can serve two independent streams of waits.
+template <typename Side>
+__device__ __forceinline__ bool mbar_wait_with(uint32_t bar, uint32_t parity, const AbortFlag& ab,
+                                               Side&& side,
+                                               unsigned long long limit_ns = kWaitLimitNs) {
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    side();
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*ab.flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *ab.flag = 1;
+        atomicOr(ab.status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // Warp-uniform wait: lane 0 polls (bounded), the verdict is broadcast, and
 // every lane then observes the completed phase itself (acquire).  Keeps the
 // warp converged for the .sync.aligned tcgen05 instructions that follow.

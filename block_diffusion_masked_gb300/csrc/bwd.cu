@@ -30,7 +30,9 @@
 // query tiles with g % 2 == b (thread t of a warpgroup owns key row t of the
 // tile, TMEM lane t), so that the MMAs of one tile overlap the
 // softmax-gradient work of the other; warp 8 loads (TMA for Q/dO, plain loads
-// for LSE/D); warp 9 issues the MMAs; warps 10-11 idle.  The load/MMA
+// for LSE/D); warp 9 issues S^T, warp 10 dP^T, dV and dK, warp 11 dQ (on
+// three schedulers, so that the busy compute warps sharing a scheduler with
+// one of them do not starve the tensor pipe).  The load/MMA
 // warpgroup drops to 72 registers and the compute warpgroups rise to 216
 // (setmaxnreg; launched with 168: 256 * 48 == 128 * 96), so a 64-query
 // slice of S^T and dP^T is read from TMEM in one batch.
@@ -84,7 +86,9 @@ struct BwdCfg {
   static constexpr int kTmemCols = 512;
   static constexpr int kThreads = 384;
   static constexpr int kProducerWarp = 8;
-  static constexpr int kMmaWarp = 9;
+  static constexpr int kMmaWarp = 9;    // S^T; owns TMEM
+  static constexpr int kMma2Warp = 10;  // dP^T, dV, dK
+  static constexpr int kMma3Warp = 11;  // dQ
   static_assert(kTmemDV + D <= kTmemCols, "TMEM budget");
   static_assert(D <= BMQ, "dQ must fit in an S buffer");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -157,10 +161,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       mbar_init(BAR(C::BAR_MMA2 + b), 1);
       mbar_init(BAR(C::BAR_DQFREE + b), 4);
     }
-    mbar_init(BAR(C::BAR_ITEMDONE), 1);
+    mbar_init(BAR(C::BAR_ITEMDONE), 2);  // warps 10 and 11
     mbar_init(BAR(C::BAR_ACCFREE), 8);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
-    mbar_init(BAR(C::BAR_ALL), 1);
+    mbar_init(BAR(C::BAR_ALL), 3);  // the three MMA-issuing warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -288,9 +292,15 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         mbar_wait_limited(BAR(C::BAR_QFULL + t % STAGES), (t / STAGES) & 1, 100000000ull);
     }
     __syncwarp();
-   } else if (warp == C::kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+   } else if (warp == C::kMmaWarp || warp == C::kMma2Warp || warp == C::kMma3Warp) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 9: S^T of every tile (it overwrites S[b], which held dQ of tile
+    // g - 2: DQFREE).  Warp 10, in its own order: dV / dK of tile g - 1, then
+    // dP^T of tile g, which overwrites the dP columns those products read
+    // P^T / dS^T from.  Warp 11: dQ of every tile (MMA2: dQ in S[b]).
     if (lane == 0) {
+      const bool s_warp = warp == C::kMmaWarp;
+      const bool dq_warp = warp == C::kMma3Warp;
       constexpr uint32_t kIdS = idesc_bf16(BN, BMQ, false, false);  // K Q^T, V dO^T
       constexpr uint32_t kIdKV = idesc_bf16(BN, D, false, true);    // P^T dO, dS^T Q
       constexpr uint32_t kIdDQ = idesc_bf16(BMQ, D, true, true);    // dS K
@@ -319,7 +329,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         }
         mma_commit(BAR(C::BAR_DPFULL + (gg & 1)));
       };
-      // dV, dK and dQ of global tile gg, once its P^T / dS^T are in place;
+      // dV and dK of global tile gg, once its P^T / dS^T are in place;
       // `first`: the item's first tile, which starts the dK / dV sums.
       auto issue_second = [&](int gg, bool first) -> bool {
         const int b = gg & 1;
@@ -339,13 +349,22 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
           mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128), kIdKV,
                  acc);
         }
+        // dQ^T reads no Q / dO: the stage is free once dV / dK are done.
+        mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
+        return true;
+      };
+      // dQ of global tile gg (warp 11): dS K into S[b], whose S^T the
+      // warpgroup has read once P^T / dS^T are in place.
+      auto issue_dq = [&](int gg) -> bool {
+        const int b = gg & 1;
+        if (!mbar_wait(BAR(C::BAR_PDS + b), (gg >> 1) & 1, ab)) return false;
+        tc_fence_after();
         const uint32_t ds_off = b * C::kDSBytes;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ss(tmem + C::kTmemS + b * BMQ, adv(dDS_mn, ds_off + kk * 16 * 128),
                  adv(dK_mn, kk * 16 * 128), kIdDQ, kk > 0 ? 1u : 0u);
         mma_commit(BAR(C::BAR_MMA2 + b));
-        mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
         return true;
       };
 
@@ -353,37 +372,57 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
         const BwdItem it = *ring(k & 3);
         if (it.v < 0) break;
+        // Every role waits for the item's K / V: ITEMDONE(k) then counts
+        // commits made after ITEMDONE(k - 1) completed.
         if (!(ok = mbar_wait(BAR(C::BAR_KV), k & 1, ab))) break;
+        if (dq_warp) {
+          for (int i = 0; i < it.ntiles && ok; ++i) ok = issue_dq(g + i);
+          if (!ok) break;
+          // ITEMDONE counts one commit from each of warps 10 and 11.
+          mma_commit(BAR(C::BAR_ITEMDONE));
+          g += it.ntiles;
+          ++k;
+          continue;
+        }
         for (int i = 0; i < it.ntiles && ok; ++i) {
           const int gg = g + i;
           const int b = gg & 1;
           const int st = gg % STAGES;
           if (!(ok = mbar_wait(BAR(C::BAR_QFULL + st), (gg / STAGES) & 1, ab))) break;
-          // S[b] held dQ of tile gg-2: wait until it has been read out.
-          if (gg >= 2 && !(ok = mbar_wait(BAR(C::BAR_DQFREE + b), ((gg - 2) >> 1) & 1, ab))) break;
-          tc_fence_after();
-          const uint32_t st_off = st * C::kQBytes;
+          if (s_warp) {
+            // S[b] held dQ of tile gg-2: wait until it has been read out.
+            if (gg >= 2 && !(ok = mbar_wait(BAR(C::BAR_DQFREE + b), ((gg - 2) >> 1) & 1, ab)))
+              break;
+            tc_fence_after();
+            const uint32_t st_off = st * C::kQBytes;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-            const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
-            mma_ss(tmem + C::kTmemS + b * BMQ, adv(dK_kmaj, koff), adv(dQ_kmaj, st_off + qoff),
-                   kIdS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+              const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
+              mma_ss(tmem + C::kTmemS + b * BMQ, adv(dK_kmaj, koff),
+                     adv(dQ_kmaj, st_off + qoff), kIdS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(BAR(C::BAR_SFULL + b));
+          } else {
+            // One dP buffer: it still holds P^T / dS^T of tile gg-1 until the
+            // dV / dK products of tile gg-1 have been issued (the previous
+            // item's last tile was issued at that item's end).
+            if (i >= 1 && !(ok = issue_second(gg - 1, i == 1))) break;
+            tc_fence_after();
+            issue_dp(gg);
           }
-          mma_commit(BAR(C::BAR_SFULL + b));
-          // One dP buffer: it still holds P^T / dS^T of tile gg-1 until the
-          // dV / dK products of tile gg-1 have been issued (the previous
-          // item's last tile was issued at that item's end).
-          if (i >= 1 && !(ok = issue_second(gg - 1, i == 1))) break;
-          issue_dp(gg);
         }
         if (!ok) break;
-        if (it.ntiles > 0) {
-          if (!(ok = issue_second(g + it.ntiles - 1, it.ntiles == 1))) break;
-        } else if (k >= 1 && !(ok = mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab))) {
-          break;
+        if (!s_warp) {
+          if (it.ntiles > 0) {
+            if (!(ok = issue_second(g + it.ntiles - 1, it.ntiles == 1))) break;
+          } else if (k >= 1 && !(ok = mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab))) {
+            break;
+          }
+          // Every S^T of the item precedes its P^T / dS^T, so the last
+          // products of warps 10 and 11 complete the item.
+          mma_commit(BAR(C::BAR_ITEMDONE));
         }
-        mma_commit(BAR(C::BAR_ITEMDONE));
         g += it.ntiles;
         ++k;
       }

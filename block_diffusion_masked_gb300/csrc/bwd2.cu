@@ -37,8 +37,9 @@
 // accumulator with a bulk tensor reduce from a shared staging tile; with 256
 // (no shared memory left) each thread adds its own with atomics.
 // Warps: 4 per compute warpgroup, then one TMA producer and three MMA
-// issuers (S^T / dP^T; dV / dK; dQ^T), whose streams are independent and so
-// are issued in parallel.  The control warps drop registers to the compute
+// issuers (S^T; dV / dK then dQ^T; dP^T), on three schedulers: a single
+// issuing warp is slowed by the busy compute warps sharing its scheduler,
+// and S^T and dP^T, which every tile waits for, are issued in parallel.  The control warps drop registers to the compute
 // warpgroups (setmaxnreg) within the pool the launch provides.
 #include <cuda_bf16.h>
 
@@ -58,9 +59,9 @@ struct Bwd2Cfg {
   static constexpr int NWG = NWG_;             // compute warpgroups
   static constexpr int kComputeWarps = 4 * NWG;
   static constexpr int kWarpLoad = kComputeWarps;      // TMA producer
-  static constexpr int kWarpS = kComputeWarps + 1;     // S^T / dP^T issuer, owns TMEM
-  static constexpr int kWarpKV = kComputeWarps + 2;    // dV / dK issuer
-  static constexpr int kWarpDQ = kComputeWarps + 3;    // dQ^T issuer
+  static constexpr int kWarpS = kComputeWarps + 1;     // S^T issuer, owns TMEM
+  static constexpr int kWarpKV = kComputeWarps + 2;    // dV / dK and dQ^T issuer
+  static constexpr int kWarpDP = kComputeWarps + 3;    // dP^T issuer
   static constexpr int kThreads = 32 * (kComputeWarps + 4);
   // setmaxnreg split: the launch gives every thread kRegLaunch registers;
   // the 4 control warps drop to kRegCtl, the compute warps rise to
@@ -187,16 +188,16 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::KVBUF; ++s) {
       mbar_init(BAR(C::BAR_KVFULL + s), 1);
-      mbar_init(BAR(C::BAR_ITEMDONE + s), 2);  // warps issuing dV / dK and dQ
+      mbar_init(BAR(C::BAR_ITEMDONE + s), 1);  // the warp issuing dV / dK and dQ
     }
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(BAR(C::BAR_QFULL + s), 1);
       mbar_init(BAR(C::BAR_QEMPTY + s), 1);
     }
-    mbar_init(BAR(C::BAR_SDPFULL), 1);
+    mbar_init(BAR(C::BAR_SDPFULL), 2);  // the S^T and the dP^T warps
     mbar_init(BAR(C::BAR_SDPFREE), C::kComputeWarps);
     mbar_init(BAR(C::BAR_PDSFULL), C::kComputeWarps);
-    mbar_init(BAR(C::BAR_MMA2), 2);      // warps 10 and 11
+    mbar_init(BAR(C::BAR_MMA2), 1);
     mbar_init(BAR(C::BAR_DQFREE), C::kComputeWarps);
     mbar_init(BAR(C::BAR_ACCFREE), C::kComputeWarps);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
@@ -337,11 +338,12 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
    } else {
     // ------------------------------------------------------------ MMA issuers
     // Three independent streams of products, each issued by its own warp so
-    // that their issue overlaps: warp 9 issues S^T and dP^T of every tile,
-    // warp 10 dV and dK, warp 11 dQ^T.  Everything one stream needs from
+    // that their issue overlaps: warp 9 issues S^T of every tile, warp 11
+    // dP^T, warp 10 dV, dK and then dQ^T.  Everything one stream needs from
     // another is ordered through the compute warpgroups' barriers (S^T / dP^T
-    // complete -> P^T / dS^T written -> second products); MMA2 and ITEMDONE
-    // count one commit from each of warps 10 and 11.
+    // complete -> P^T / dS^T written -> second products); SDPFULL counts one
+    // commit from each of warps 9 and 11 (each waits for SDPFREE of the
+    // previous tile first, so neither runs a phase ahead).
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(BN, BMQ, false, false);  // K Q^T, V dO^T
       constexpr uint32_t kIdKV = idesc_bf16(BN, DH, false, true);   // P^T dO, dS^T Q
@@ -349,7 +351,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       auto adv = [](uint64_t d, uint32_t bytes) { return d + static_cast<uint64_t>(bytes >> 4); };
       bool ok = true;
       int g = 0, k = 0;
-      if (warp == C::kWarpS) {
+      if (warp == C::kWarpS || warp == C::kWarpDP) {
+        const bool dp = warp == C::kWarpDP;
         const uint64_t dK_kmaj0 = sdesc_sw128(sbase + C::kOffK, 16, 1024);
         const uint64_t dV_kmaj0 = sdesc_sw128(sbase + C::kOffV, 16, 1024);
         const uint64_t dQ_kmaj = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
@@ -370,19 +373,15 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
             if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_SDPFREE), (gg - 1) & 1, ab))) break;
             tc_fence_after();
             const uint32_t st_off = st * C::kQBytes;
+            // S^T = K Q^T (warp 9) or dP^T = V dO^T (warp 11).
+            const uint32_t acc = dp ? C::kTmemDP : C::kTmemS;
+            const uint64_t a0 = dp ? dV_kmaj : dK_kmaj;
+            const uint64_t b0 = dp ? dO_kmaj : dQ_kmaj;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
               const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
-              mma_ss(tmem + C::kTmemS, adv(dK_kmaj, koff), adv(dQ_kmaj, st_off + qoff), kIdS,
-                     kk > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-              const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
-              mma_ss(tmem + C::kTmemDP, adv(dV_kmaj, koff), adv(dO_kmaj, st_off + qoff), kIdS,
-                     kk > 0 ? 1u : 0u);
+              mma_ss(tmem + acc, adv(a0, koff), adv(b0, st_off + qoff), kIdS, kk > 0 ? 1u : 0u);
             }
             mma_commit(BAR(C::BAR_SDPFULL));
           }
@@ -390,7 +389,6 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           ++k;
         }
       } else {
-        const bool kv = warp == C::kWarpKV;  // this warp issues dV / dK, else dQ^T
         const uint64_t dDS_mn = sdesc_sw128(sbase + C::kOffDS, BN * 128, 1024);
         while (ok) {
           if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
@@ -407,38 +405,34 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           // dK / dV of the previous item must be read out before they restart
           // (waited for every item, so that ITEMDONE(k) always follows
           // ACCFREE(k - 1)).
-          if (kv && k >= 1 && !(ok = mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab))) break;
+          if (k >= 1 && !(ok = mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab))) break;
           for (int i = 0; i < it.ntiles && ok; ++i) {
             // dV, dK, dQ of tile gg once its P^T / dS^T are in place.
             const int gg = g + i;
             const uint32_t st_off = (gg % STAGES) * C::kQBytes;
             if (!(ok = mbar_wait(BAR(C::BAR_PDSFULL), gg & 1, ab))) break;
-            if (kv) {
-              tc_fence_after();
-              const uint32_t pds = tmem + C::kTmemPDS;
+            tc_fence_after();
+            const uint32_t pds = tmem + C::kTmemPDS;
 #pragma unroll
-              for (int kk = 0; kk < BMQ / 16; ++kk) {
-                // queries [16kk, 16kk+16): chunk kk/2, P^T first 16 columns, dS^T last 16
-                const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
-                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                mma_ts(tmem + C::kTmemDV, pds + col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV,
-                       acc);
-                mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128),
-                       kIdKV, acc);
-              }
-              mma_commit(BAR(C::BAR_MMA2));
-              // dQ^T reads no Q / dO: the stage is free once dV / dK are done.
-              mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
-            } else {
-              // The DQ columns still hold dQ of tile gg-1 until it has been read out.
-              if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_DQFREE), (gg - 1) & 1, ab))) break;
-              tc_fence_after();
-#pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk)
-                mma_ss(tmem + C::kTmemDQ, adv(dK_mn, kk * 16 * 128), adv(dDS_mn, kk * 16 * 128),
-                       kIdDQ, kk > 0 ? 1u : 0u);
-              mma_commit(BAR(C::BAR_MMA2));
+            for (int kk = 0; kk < BMQ / 16; ++kk) {
+              // queries [16kk, 16kk+16): chunk kk/2, P^T first 16 columns, dS^T last 16
+              const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+              const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+              mma_ts(tmem + C::kTmemDV, pds + col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV,
+                     acc);
+              mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128),
+                     kIdKV, acc);
             }
+            // dQ^T reads no Q / dO: the stage is free once dV / dK are done.
+            mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
+            // The DQ columns still hold dQ of tile gg-1 until it has been read out.
+            if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_DQFREE), (gg - 1) & 1, ab))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ss(tmem + C::kTmemDQ, adv(dK_mn, kk * 16 * 128), adv(dDS_mn, kk * 16 * 128),
+                     kIdDQ, kk > 0 ? 1u : 0u);
+            mma_commit(BAR(C::BAR_MMA2));
           }
           if (!ok) break;
           mma_commit(BAR(C::BAR_ITEMDONE + k % C::KVBUF));

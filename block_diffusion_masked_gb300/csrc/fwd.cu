@@ -9,13 +9,15 @@
 // Materialization", section 5.1: S = Q K^T, running max and sum (section
 // 4.2), O += P V; only O and the log-sum-exp reach device memory.
 //
-// Warp roles (192 threads):
+// Warp roles (224 threads):
 //   warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t);
 //              on request they first zero their CTA's share of the
 //              backward's float32 dq accumulator;
 //   warp 4     TMA producer: Q once, then K/V tiles through a STAGES-deep ring;
-//   warp 5     MMA issuer: S = Q K^T into one of two TMEM score buffers,
-//              O += P V into a TMEM accumulator, both with tcgen05.mma.
+//   warp 5     MMA issuer of S = Q K^T into one of two TMEM score buffers;
+//   warp 6     MMA issuer of O += P V into a TMEM accumulator (two issuing
+//              warps on two schedulers: one alone is slowed by the busy
+//              softmax warp that shares its scheduler).
 // Scores live in TMEM, probabilities in a 128-byte-swizzled shared tile.
 #include <cuda_bf16.h>
 
@@ -57,14 +59,14 @@ struct FwdCfg {
   static constexpr int kTmemS1 = BN;
   static constexpr int kTmemO = 2 * BN;
   static constexpr int kTmemCols = 512;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 224;
   static_assert(2 * BN + D <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(BN % 64 == 0 && D % 64 == 0, "tile shape");
 };
 
 template <int D, int BN, int STAGES>
-__global__ void __launch_bounds__(192, 1) dfa_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D, BN, STAGES>;
   constexpr int BM = C::BM;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(192, 1) dfa_fwd_kernel(const __grid_constant__
     }
     mbar_init(BAR(C::BAR_PFULL), 128);
     mbar_init(BAR(C::BAR_PVDONE), 1);
-    mbar_init(BAR(C::BAR_DRAIN), 1);
+    mbar_init(BAR(C::BAR_DRAIN), 2);  // both MMA-issuing warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -159,51 +161,55 @@ __global__ void __launch_bounds__(192, 1) dfa_fwd_kernel(const __grid_constant__
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 5 || warp == 6) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 5 issues S = Q K^T, warp 6 O += P V; the two streams share no
+    // operand (S double-buffered in TMEM, P in shared memory), so each only
+    // waits for the softmax warps, and they issue from two schedulers.
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(BM, D, false, true);
-      bool ok = mbar_wait(BAR(C::BAR_Q), 0, ab);
-      tc_fence_after();
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i % STAGES;
-        if (!mbar_wait(BAR(C::BAR_PFULL), i & 1, ab)) return false;
-        if (!mbar_wait(BAR(C::BAR_VFULL + st), (i / STAGES) & 1, ab)) return false;
-        tc_fence_after();
+      bool ok = true;
+      if (warp == 6) {
+        for (int i = 0; i < ntiles && ok; ++i) {
+          const int st = i % STAGES;
+          if (!(ok = mbar_wait(BAR(C::BAR_PFULL), i & 1, ab))) break;
+          if (!(ok = mbar_wait(BAR(C::BAR_VFULL + st), (i / STAGES) & 1, ab))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(sbase + C::kOffP + (kk >> 2) * (BM * 128) + (kk & 3) * 32,
-                                         16, 1024);
-          const uint64_t b =
-              sdesc_sw128(sbase + C::kOffV + st * C::kKVBytes + kk * 16 * 128, BN * 128, 1024);
-          mma_ss(tmem + C::kTmemO, a, b, kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(
+                sbase + C::kOffP + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t b =
+                sdesc_sw128(sbase + C::kOffV + st * C::kKVBytes + kk * 16 * 128, BN * 128, 1024);
+            mma_ss(tmem + C::kTmemO, a, b, kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(BAR(C::BAR_PVDONE));
+          mma_commit(BAR(C::BAR_VEMPTY + st));
         }
-        mma_commit(BAR(C::BAR_PVDONE));
-        mma_commit(BAR(C::BAR_VEMPTY + st));
-        return true;
-      };
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int st = j % STAGES;
-        const int buf = j & 1;
-        if (!(ok = mbar_wait(BAR(C::BAR_KFULL + st), (j / STAGES) & 1, ab))) break;
-        if (j >= 2 && !(ok = mbar_wait(BAR(C::BAR_SFREE + buf), ((j - 2) >> 1) & 1, ab))) break;
+      } else {
+        ok = mbar_wait(BAR(C::BAR_Q), 0, ab);
         tc_fence_after();
-        const uint32_t d_s = tmem + (buf ? C::kTmemS1 : C::kTmemS0);
+        for (int j = 0; j < ntiles && ok; ++j) {
+          const int st = j % STAGES;
+          const int buf = j & 1;
+          if (!(ok = mbar_wait(BAR(C::BAR_KFULL + st), (j / STAGES) & 1, ab))) break;
+          if (j >= 2 && !(ok = mbar_wait(BAR(C::BAR_SFREE + buf), ((j - 2) >> 1) & 1, ab))) break;
+          tc_fence_after();
+          const uint32_t d_s = tmem + (buf ? C::kTmemS1 : C::kTmemS0);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(sbase + C::kOffQ + (kk >> 2) * (BM * 128) + (kk & 3) * 32,
-                                         16, 1024);
-          const uint64_t b = sdesc_sw128(
-              sbase + C::kOffK + st * C::kKVBytes + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16,
-              1024);
-          mma_ss(d_s, a, b, kIdS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(
+                sbase + C::kOffQ + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = sdesc_sw128(
+                sbase + C::kOffK + st * C::kKVBytes + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16,
+                1024);
+            mma_ss(d_s, a, b, kIdS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(BAR(C::BAR_SFULL + buf));
+          mma_commit(BAR(C::BAR_KEMPTY + st));
         }
-        mma_commit(BAR(C::BAR_SFULL + buf));
-        mma_commit(BAR(C::BAR_KEMPTY + st));
-        if (j >= 1) ok = issue_pv(j - 1);
       }
-      if (ok && ntiles > 0) issue_pv(ntiles - 1);
       // Every MMA must be complete before the TMEM is released.
       mma_commit(BAR(C::BAR_DRAIN));
       mbar_wait_limited(BAR(C::BAR_DRAIN), 0, 1000000000ull);

@@ -26,8 +26,6 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
-
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -83,28 +81,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*ab.flag) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
-        *ab.flag = 1;
-        atomicOr(ab.status, kStatusTimeout);
-        return false;
-      }
-    }
-  }
-}
-
-// As mbar_wait, running side() between polls: side() checks some other
-// barrier without blocking and does its work when that one is ready, so that
-// one thread can serve two independent streams of waits.
-template <typename Side>
-__device__ __forceinline__ bool mbar_wait_with(uint32_t bar, uint32_t parity, const AbortFlag& ab,
-                                               Side&& side,
-                                               unsigned long long limit_ns = kWaitLimitNs) {
-  const unsigned long long t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    side();
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*ab.flag) return false;
@@ -228,10 +204,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 
 // TMEM address of (lane, column).
-__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
-  return base + (lane << 16) + col;
-}
-
 // Each thread of the warp reads 32 consecutive 32-bit columns of its own TMEM
 // lane (lane = 32 * (warp % 4) + lane_id).  Registers are valid only after
 // tmem_wait_ld(); tmem_pin() ties later uses to that wait.

@@ -123,9 +123,9 @@ int dfa_causal_backward(const void *q, const void *k, const void *v, const void 
  * writes it.  delta is always (batch, heads, 2n).
  *   dfa_fwd_main: dfa_forward (or, in the causal mode, dfa_causal_forward
  *     on the paired view); if dq_acc is not NULL the same launch also sets
- *     dq_acc (float32, shape of q) to zero, with stores that otherwise idle
- *     warps issue alongside the tensor-core work, so that the backward needs
- *     no separate pass over it.
+ *     dq_acc (float32, shape of q) to zero, with stores issued alongside
+ *     the tensor-core work by warps that are not on its critical path, so
+ *     that the backward needs no separate pass over it.
  *   dfa_bwd_preprocess: delta = rowsum(dout * out), float32 (batch, heads, 2n);
  *     dq_acc (float32, shape of q) set to zero unless dq_acc is NULL (then
  *     the caller zeroed it, e.g. through dfa_fwd_main).

@@ -171,6 +171,22 @@ def _check_layout(q):
         raise ValueError("expected (batch, 2n, heads, headdim) with an even 2n")
 
 
+def _kv_head(q, k):
+    """Map query head h to its key/value head.
+
+    Multi-query and grouped-query attention ("Fast Diffusion Attention",
+    "GQA-grouped backward"): k and v carry H_kv heads, H_kv dividing the H
+    query heads; query head h reads key/value head h // (H / H_kv), so each
+    key/value head serves a run of H / H_kv consecutive query heads (the
+    pages do not spell out the grouping; this is the usual one).
+    """
+    H, Hk = q.shape[2], k.shape[2]
+    if Hk < 1 or H % Hk:
+        raise ValueError("key/value heads must divide query heads")
+    g = H // Hk
+    return lambda h: h // g
+
+
 def diffusion_forward(q, k, v, block_size, heads=None):
     """Block-diffusion attention forward for every (batch, head) or a subset.
 
@@ -180,26 +196,43 @@ def diffusion_forward(q, k, v, block_size, heads=None):
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     _check_layout(q)
     B, L, H, d = q.shape
+    kvh = _kv_head(q, k)
     mask = diffusion_mask(L // 2, block_size)
     out = np.full((B, L, H, d), np.nan)
     lse = np.full((B, H, L), np.nan)
     for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]):
-        o, s = masked_attention_forward(q[b, :, h], k[b, :, h], v[b, :, h], mask)
+        o, s = masked_attention_forward(q[b, :, h], k[b, :, kvh(h)], v[b, :, kvh(h)], mask)
         out[b, :, h] = o
         lse[b, h] = s
     return out, lse
 
 
 def diffusion_backward(q, k, v, dout, block_size, heads=None):
-    """Gradients dq, dk, dv (B, 2n, H, d) float64 of block-diffusion attention."""
+    """Gradients dq (B, 2n, H, d) and dk, dv (B, 2n, H_kv, d), float64.
+
+    With fewer key/value heads than query heads, the gradient of a key/value
+    head is the sum over the query heads that read it.  ``heads`` lists
+    (b, h) pairs of query heads to compute; dk, dv are then summed over the
+    listed heads only (a full key/value head needs all of its query heads).
+    """
     q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
     _check_layout(q)
     B, L, H, d = q.shape
+    kvh = _kv_head(q, k)
     mask = diffusion_mask(L // 2, block_size)
-    dq, dk, dv = (np.full((B, L, H, d), np.nan) for _ in range(3))
+    dq = np.full((B, L, H, d), np.nan)
+    dk, dv = (np.full(k.shape, np.nan) for _ in range(2))
+    touched = set()
     for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]):
-        g = masked_attention_backward(q[b, :, h], k[b, :, h], v[b, :, h], dout[b, :, h], mask)
-        dq[b, :, h], dk[b, :, h], dv[b, :, h] = g
+        hk = kvh(h)
+        g = masked_attention_backward(q[b, :, h], k[b, :, hk], v[b, :, hk], dout[b, :, h], mask)
+        dq[b, :, h] = g[0]
+        if (b, hk) not in touched:  # first query head of this key/value head
+            touched.add((b, hk))
+            dk[b, :, hk] = 0.0
+            dv[b, :, hk] = 0.0
+        dk[b, :, hk] += g[1]
+        dv[b, :, hk] += g[2]
     return dq, dk, dv
 
 
@@ -207,11 +240,12 @@ def causal_forward(q, k, v, heads=None):
     """Causal attention on (Bc, L, H, d): the yardstick of "The right yardstick"."""
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     B, L, H, d = q.shape
+    kvh = _kv_head(q, k)
     mask = causal_mask(L)
     out = np.full((B, L, H, d), np.nan)
     lse = np.full((B, H, L), np.nan)
     for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]):
-        o, s = masked_attention_forward(q[b, :, h], k[b, :, h], v[b, :, h], mask)
+        o, s = masked_attention_forward(q[b, :, h], k[b, :, kvh(h)], v[b, :, kvh(h)], mask)
         out[b, :, h] = o
         lse[b, h] = s
     return out, lse
@@ -221,11 +255,21 @@ def causal_backward(q, k, v, dout, heads=None):
     """Gradients of causal attention on (Bc, L, H, d), float64."""
     q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
     B, L, H, d = q.shape
+    kvh = _kv_head(q, k)
     mask = causal_mask(L)
-    dq, dk, dv = (np.full((B, L, H, d), np.nan) for _ in range(3))
+    dq = np.full((B, L, H, d), np.nan)
+    dk, dv = (np.full(k.shape, np.nan) for _ in range(2))
+    touched = set()
     for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]):
-        g = masked_attention_backward(q[b, :, h], k[b, :, h], v[b, :, h], dout[b, :, h], mask)
-        dq[b, :, h], dk[b, :, h], dv[b, :, h] = g
+        hk = kvh(h)
+        g = masked_attention_backward(q[b, :, h], k[b, :, hk], v[b, :, hk], dout[b, :, h], mask)
+        dq[b, :, h] = g[0]
+        if (b, hk) not in touched:  # first query head of this key/value head
+            touched.add((b, hk))
+            dk[b, :, hk] = 0.0
+            dv[b, :, hk] = 0.0
+        dk[b, :, hk] += g[1]
+        dv[b, :, hk] += g[2]
     return dq, dk, dv
 
 

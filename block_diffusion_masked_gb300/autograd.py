@@ -2,7 +2,9 @@
 
 ``diffusion_attn_func(q, k, v, block_size)`` mirrors the API of "Fast
 Diffusion Attention" (section "Try it"): q, k, v are (batch, 2n, heads,
-headdim) bf16 tensors ordered [noisy | clean]; the forward saves out and the
+headdim) bf16 tensors ordered [noisy | clean] (k and v may carry fewer
+heads, a divisor of q's: grouped-query / multi-query attention, query head h
+reading key/value head h // (heads // kv_heads)); the forward saves out and the
 log-sum-exp, and the backward recomputes from them (section 4.5 of
 "FlashAttention: Exact Attention Without Materialization").
 """
@@ -18,7 +20,10 @@ class DiffusionAttnFunc(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, block_size):
         q, k, v = (t.contiguous() for t in (q, k, v))
-        out, lse = binding.dfa_forward(q, k, v, block_size)
+        if k.shape[2] == q.shape[2]:
+            out, lse = binding.dfa_forward(q, k, v, block_size)
+        else:
+            out, lse = binding.dfa_forward_gqa(q, k, v, block_size)
         ctx.save_for_backward(q, k, v, out, lse)
         ctx.block_size = block_size
         return out
@@ -26,7 +31,8 @@ class DiffusionAttnFunc(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dout):
         q, k, v, out, lse = ctx.saved_tensors
-        dq, dk, dv = binding.dfa_backward(q, k, v, out, dout.contiguous(), lse, ctx.block_size)
+        bwd = binding.dfa_backward if k.shape[2] == q.shape[2] else binding.dfa_backward_gqa
+        dq, dk, dv = bwd(q, k, v, out, dout.contiguous(), lse, ctx.block_size)
         return dq, dk, dv, None
 
 

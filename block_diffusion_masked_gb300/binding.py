@@ -37,6 +37,8 @@ _SIGNATURES = {
     "dfa_last_cuda_error": (ctypes.c_char_p, []),
     "dfa_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "dfa_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _I, _P]),
+    "dfa_forward_gqa": (_I, [_P] * 5 + [_I] * 6 + [_P]),
+    "dfa_backward_gqa": (_I, [_P] * 9 + [_I] * 6 + [_P]),
     "dfa_causal_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "dfa_causal_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _P]),
     "dfa_status": (_I, [_P]),
@@ -138,6 +140,62 @@ def dfa_backward(q, k, v, out, dout, lse, block_size, dq=None, dk=None, dv=None)
                                 _ptr(dq), _ptr(dk), _ptr(dv), B, L // 2, H, d, int(block_size),
                                 _stream_ptr(q))
     _check("dfa_backward", rc)
+    return dq, dk, dv
+
+
+def _check_grouped(q, k, v, *more):
+    """q (and ``more``) share one shape, k and v another with fewer heads."""
+    _check_qkv(q, *more)
+    _check_qkv(k, v)
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("expected (batch, seqlen, heads, headdim) tensors")
+    if k.device != q.device:
+        raise ValueError("tensors must live on the same CUDA device")
+    B, L, H, d = q.shape
+    Hk = k.shape[2]
+    if k.shape[0] != B or k.shape[1] != L or k.shape[3] != d:
+        raise ValueError("k and v must be (batch, seqlen, kv_heads, headdim) like q")
+    if Hk < 1 or H % Hk:
+        raise ValueError("kv_heads must divide the query heads")
+    return Hk
+
+
+def dfa_forward_gqa(q, k, v, block_size, out=None, lse=None):
+    """Forward with grouped key/value heads: q (B, 2n, H, d), k, v (B, 2n, Hk, d).
+
+    Query head h reads key/value head h // (H // Hk).  Returns (out, lse)
+    like :func:`dfa_forward`.
+    """
+    Hk = _check_grouped(q, k, v)
+    B, L, H, d = q.shape
+    if L % 2:
+        raise ValueError("the sequence must be [noisy | clean] with an even length 2n")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_forward_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L // 2, H,
+                                   Hk, d, int(block_size), _stream_ptr(q))
+    _check("dfa_forward_gqa", rc)
+    return out, lse
+
+
+def dfa_backward_gqa(q, k, v, out, dout, lse, block_size, dq=None, dk=None, dv=None):
+    """Backward with grouped key/value heads; dk, dv have the shape of k.
+
+    The gradient of a key/value head sums over its query heads.
+    """
+    Hk = _check_grouped(q, k, v, out, dout)
+    B, L, H, d = q.shape
+    if lse.shape != (B, H, L) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 (B, H, 2n)")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_backward_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), B, L // 2, H, Hk, d,
+                                    int(block_size), _stream_ptr(q))
+    _check("dfa_backward_gqa", rc)
     return dq, dk, dv
 
 

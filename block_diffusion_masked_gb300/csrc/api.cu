@@ -160,10 +160,15 @@ int check_common(int B, int n, int H, int d, int bs) {
   return DFA_OK;
 }
 
+// Query heads per key/value head, or 0 when Hk does not divide H.
+int kv_group_of(int H, int Hk) { return Hk >= 1 && Hk <= H && H % Hk == 0 ? H / Hk : 0; }
+
 int forward_impl(int mode, const void* q, const void* k, const void* v, void* out, float* lse,
-                 float* dq_acc, int B, int n, int H, int d, int bs, cudaStream_t stream) {
+                 float* dq_acc, int B, int n, int H, int Hk, int d, int bs, cudaStream_t stream) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
+  const int G = kv_group_of(H, Hk);
+  if (G == 0) return DFA_EINVAL;
   if (B == 0) return DFA_OK;
   if (!q || !k || !v || !out || !lse) return DFA_EINVAL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
@@ -175,8 +180,8 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   tile_shape_for(d, &ts);
   FwdParams p;
   if ((rc = make_map(&p.tm_q, q, B, n, H, d, ts.fwd_bm))) return rc;
-  if ((rc = make_map(&p.tm_k, k, B, n, H, d, ts.fwd_bn))) return rc;
-  if ((rc = make_map(&p.tm_v, v, B, n, H, d, ts.fwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_k, k, B, n, Hk, d, ts.fwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_v, v, B, n, Hk, d, ts.fwd_bn))) return rc;
   if ((rc = make_map(&p.tm_o, out, B, n, H, d, ts.fwd_bm))) return rc;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
@@ -184,6 +189,7 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   p.B = B;
   p.n = n;
   p.H = H;
+  p.kv_group = G;
   p.bs = bs < n ? bs : n;
   p.mode = mode;
   p.q_tiles = cdiv(n, ts.fwd_bm);
@@ -207,9 +213,11 @@ bool aligned_all(std::initializer_list<const void*> ps) {
 // The tensor-core backward step alone: caller-owned delta and dq_acc.
 int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const void* dout,
                   const float* lse, const float* delta, float* dq_acc, void* dk, void* dv, int B,
-                  int n, int H, int d, int bs, cudaStream_t stream) {
+                  int n, int H, int Hk, int d, int bs, cudaStream_t stream) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
+  const int G = kv_group_of(H, Hk);
+  if (G == 0) return DFA_EINVAL;
   if (B == 0) return DFA_OK;
   if (!aligned_all({q, k, v, dout, dq_acc, dk, dv}) || !lse || !delta ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(delta) & 3u))
@@ -221,8 +229,8 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   BwdParams p;
   if ((rc = make_map(&p.tm_q, q, B, n, H, d, ts.bwd_bm))) return rc;
   if ((rc = make_map(&p.tm_do, dout, B, n, H, d, ts.bwd_bm))) return rc;
-  if ((rc = make_map(&p.tm_k, k, B, n, H, d, ts.bwd_bn))) return rc;
-  if ((rc = make_map(&p.tm_v, v, B, n, H, d, ts.bwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_k, k, B, n, Hk, d, ts.bwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_v, v, B, n, Hk, d, ts.bwd_bn))) return rc;
   if (d == 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, B, n, H, d,
                                       ts.bwd_bm / kBwd2WarpgroupsD128)))
     return rc;
@@ -235,11 +243,14 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   p.B = B;
   p.n = n;
   p.H = H;
+  p.Hk = Hk;
+  p.kv_group = G;
   p.bs = bs < n ? bs : n;
   p.mode = mode;
   p.k_tiles = cdiv(n, ts.bwd_bn);
-  // q, k, v, dout (bf16) and the float32 dq accumulator of one (batch, head)
-  p.group = l2_group(12LL * 2 * n * d, ds->l2_bytes, B * H);
+  // per (batch, key/value head): k, v (bf16) and, for each of its G query
+  // heads, q, dout (bf16) and the float32 dq accumulator
+  p.group = l2_group((4LL + 8LL * G) * 2 * n * d, ds->l2_bytes, B * Hk);
   p.sched = sched_for_stream(ds, stream);
   p.items = 0;  // set by the launcher
   p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
@@ -280,9 +291,10 @@ int convert_impl(const float* dq_acc, void* dq, int B, int n, int H, int d, cuda
 // Full backward: stream-ordered scratch, then the three steps.
 int backward_impl(int mode, const void* q, const void* k, const void* v, const void* out,
                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int n,
-                  int H, int d, int bs, cudaStream_t stream) {
+                  int H, int Hk, int d, int bs, cudaStream_t stream) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
+  if (kv_group_of(H, Hk) == 0) return DFA_EINVAL;
   if (B == 0) return DFA_OK;
   if (!aligned_all({q, k, v, out, dout, dq, dk, dv}) || !lse ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
@@ -303,7 +315,8 @@ int backward_impl(int mode, const void* q, const void* k, const void* v, const v
     return DFA_ECUDA;
   }
   rc = preprocess_impl(out, dout, delta, dq_acc, B, n, H, d, stream);
-  if (!rc) rc = bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, d, bs, stream);
+  if (!rc)
+    rc = bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, Hk, d, bs, stream);
   if (!rc) rc = convert_impl(dq_acc, dq, B, n, H, d, stream);
   cudaFreeAsync(delta, stream);
   cudaFreeAsync(dq_acc, stream);
@@ -333,15 +346,30 @@ const char* dfa_error_string(int code) {
 
 int dfa_forward(const void* q, const void* k, const void* v, void* out, float* lse, int batch,
                 int n, int heads, int headdim, int block_size, dfa_stream_t stream) {
-  return forward_impl(MODE_DIFFUSION, q, k, v, out, lse, nullptr, batch, n, heads, headdim,
+  return forward_impl(MODE_DIFFUSION, q, k, v, out, lse, nullptr, batch, n, heads, heads, headdim,
                       block_size, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_forward_gqa(const void* q, const void* k, const void* v, void* out, float* lse, int batch,
+                    int n, int heads, int kv_heads, int headdim, int block_size,
+                    dfa_stream_t stream) {
+  return forward_impl(MODE_DIFFUSION, q, k, v, out, lse, nullptr, batch, n, heads, kv_heads,
+                      headdim, block_size, static_cast<cudaStream_t>(stream));
 }
 
 int dfa_backward(const void* q, const void* k, const void* v, const void* out, const void* dout,
                  const float* lse, void* dq, void* dk, void* dv, int batch, int n, int heads,
                  int headdim, int block_size, dfa_stream_t stream) {
   return backward_impl(MODE_DIFFUSION, q, k, v, out, dout, lse, dq, dk, dv, batch, n, heads,
-                       headdim, block_size, static_cast<cudaStream_t>(stream));
+                       heads, headdim, block_size, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_backward_gqa(const void* q, const void* k, const void* v, const void* out,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv, int batch,
+                     int n, int heads, int kv_heads, int headdim, int block_size,
+                     dfa_stream_t stream) {
+  return backward_impl(MODE_DIFFUSION, q, k, v, out, dout, lse, dq, dk, dv, batch, n, heads,
+                       kv_heads, headdim, block_size, static_cast<cudaStream_t>(stream));
 }
 
 // Causal attention on (batch, seqlen, heads, headdim).  A contiguous tensor of
@@ -353,8 +381,8 @@ int dfa_causal_forward(const void* q, const void* k, const void* v, void* out, f
                        int batch, int seqlen, int heads, int headdim, dfa_stream_t stream) {
   if (batch < 0 || seqlen < 1) return DFA_EINVAL;
   if (batch % 2) return DFA_EINVAL;
-  return forward_impl(MODE_CAUSAL, q, k, v, out, lse, nullptr, batch / 2, seqlen, heads, headdim,
-                      1, static_cast<cudaStream_t>(stream));
+  return forward_impl(MODE_CAUSAL, q, k, v, out, lse, nullptr, batch / 2, seqlen, heads, heads,
+                      headdim, 1, static_cast<cudaStream_t>(stream));
 }
 
 int dfa_causal_backward(const void* q, const void* k, const void* v, const void* out,
@@ -363,14 +391,14 @@ int dfa_causal_backward(const void* q, const void* k, const void* v, const void*
   if (batch < 0 || seqlen < 1) return DFA_EINVAL;
   if (batch % 2) return DFA_EINVAL;
   return backward_impl(MODE_CAUSAL, q, k, v, out, dout, lse, dq, dk, dv, batch / 2, seqlen, heads,
-                       headdim, 1, static_cast<cudaStream_t>(stream));
+                       heads, headdim, 1, static_cast<cudaStream_t>(stream));
 }
 
 int dfa_fwd_main(const void* q, const void* k, const void* v, void* out, float* lse,
                  float* dq_acc, int batch, int n, int heads, int headdim, int block_size, int mode,
                  dfa_stream_t stream) {
   if (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) return DFA_EINVAL;
-  return forward_impl(mode, q, k, v, out, lse, dq_acc, batch, n, heads, headdim,
+  return forward_impl(mode, q, k, v, out, lse, dq_acc, batch, n, heads, heads, headdim,
                       mode == MODE_CAUSAL ? 1 : block_size, static_cast<cudaStream_t>(stream));
 }
 
@@ -384,8 +412,9 @@ int dfa_bwd_main(const void* q, const void* k, const void* v, const void* dout, 
                  const float* delta, float* dq_acc, void* dk, void* dv, int batch, int n,
                  int heads, int headdim, int block_size, int mode, dfa_stream_t stream) {
   if (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) return DFA_EINVAL;
-  return bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, batch, n, heads, headdim,
-                       mode == MODE_CAUSAL ? 1 : block_size, static_cast<cudaStream_t>(stream));
+  return bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, batch, n, heads, heads,
+                       headdim, mode == MODE_CAUSAL ? 1 : block_size,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int dfa_bwd_dq_convert(const float* dq_acc, void* dq, int batch, int n, int heads, int headdim,

@@ -95,17 +95,31 @@ struct BwdCfg {
   static_assert(BMQ == 128 && D == 64, "layout of this kernel: 128-query tiles, headdim 64");
 };
 
-// One work item: key tile and the query tiles that see it (at most two
-// segments, kept in scalars so that nothing is indexed dynamically).  The
-// producer decodes each item once and publishes the decoded form to the other
-// roles through a ring in shared memory; v < 0 means no work is left.
+// One work item: key tile of one key/value head and the query tiles that
+// see it (at most two segments per query head, kept in scalars so that
+// nothing is indexed dynamically).  With grouped key/value heads
+// ("Fast Diffusion Attention": GQA-grouped backward) the item walks the same
+// query tiles of each of the kv_group query heads h0, h0 + 1, ... that read
+// its key/value head, so that dK and dV sum over the group in TMEM.  The
+// producer decodes each item once and publishes the decoded form to the
+// other roles through a ring in shared memory; v < 0 means no work is left.
 struct BwdItem {
   int v;
-  WorkItem wi;
-  int n0, ntiles;
+  WorkItem wi;  // wi.h: the key/value head
+  int n0, nth, ntiles;  // tiles of segment 0, per query head, in all
+  int h0;               // first query head of the group
   int half0, rule0, tb0, half1, rule1, tb1;
-  __device__ __forceinline__ int qtile(int t) const { return t < n0 ? tb0 + t : tb1 + (t - n0); }
-  __device__ __forceinline__ int qhalf(int t) const { return t < n0 ? half0 : half1; }
+  // Tile t is local tile l of query head h0 + hh.
+  __device__ __forceinline__ void split(int t, int& hh, int& l) const {
+    hh = 0;
+    l = t;
+    if (l >= nth) {
+      hh = l / nth;
+      l -= hh * nth;
+    }
+  }
+  __device__ __forceinline__ int ltile(int l) const { return l < n0 ? tb0 + l : tb1 + (l - n0); }
+  __device__ __forceinline__ int lhalf(int l) const { return l < n0 ? half0 : half1; }
 };
 
 static_assert(sizeof(BwdItem) <= 64, "item ring slot");
@@ -115,11 +129,13 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   BwdItem it;
   it.v = v;
   if (v < 0) return it;
-  it.wi = bwd_work(v, p.mode, p.B, p.H, p.k_tiles, p.group);
+  it.wi = bwd_work(v, p.mode, p.B, p.Hk, p.k_tiles, p.group);
+  it.h0 = it.wi.h * p.kv_group;
   Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
   const int nseg = bwd_segments(p.mode, p.n, p.bs, BMQ, BN, it.wi.half, it.wi.tile, seg);
   it.n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
-  it.ntiles = it.n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
+  it.nth = it.n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
+  it.ntiles = it.nth * p.kv_group;
   it.half0 = seg[0].half;
   it.rule0 = seg[0].rule;
   it.tb0 = seg[0].t_begin;
@@ -205,15 +221,18 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     // Q, dO and the negated -LSE * log2(e), -D of the item's t-th query tile
     // into the stage of global tile gg.  Rows past the half: probability 0.
     auto load_q = [&](const BwdItem& it, int t, int gg) -> bool {
-      const int qt = it.qtile(t);
-      const int half = it.qhalf(t);
-      const float* del_bh = p.delta + (static_cast<size_t>(it.wi.b) * p.H + it.wi.h) * L;
+      int hh, l;
+      it.split(t, hh, l);
+      const int qt = it.ltile(l);
+      const int half = it.lhalf(l);
+      const int h = it.h0 + hh;  // query head
+      const float* del_bh = p.delta + (static_cast<size_t>(it.wi.b) * p.H + h) * L;
       float lse_r[kPerLane], del_r[kPerLane];
 #pragma unroll
       for (int e = 0; e < kPerLane; ++e) {
         const int q = qt * BMQ + lane + 32 * e;
         const bool valid = q < p.n;
-        lse_r[e] = valid ? p.lse[lse_offset(p.mode, it.wi.b, it.wi.h, half, q, p.H, p.n)] *
+        lse_r[e] = valid ? p.lse[lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n)] *
                                -1.4426950408889634f
                          : -INFINITY;
         del_r[e] = valid ? -del_bh[static_cast<size_t>(half) * p.n + q] : 0.f;
@@ -238,9 +257,9 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           tma_load_5d(sbase + C::kOffQ + st * C::kQBytes + c * BMQ * 128, &p.tm_q,
-                      BAR(C::BAR_QFULL + st), 64 * c, it.wi.h, qt * BMQ, half, it.wi.b);
+                      BAR(C::BAR_QFULL + st), 64 * c, h, qt * BMQ, half, it.wi.b);
           tma_load_5d(sbase + C::kOffDO + st * C::kQBytes + c * BMQ * 128, &p.tm_do,
-                      BAR(C::BAR_QFULL + st), 64 * c, it.wi.h, qt * BMQ, half, it.wi.b);
+                      BAR(C::BAR_QFULL + st), 64 * c, h, qt * BMQ, half, it.wi.b);
         }
       }
       __syncwarp();
@@ -452,10 +471,12 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       tmem_pin<D>(dq);
       tc_fence_before();
       mbar_arrive_warp(BAR(C::BAR_DQFREE + b));
-      const int q = it.qtile(t) * BMQ + row;
+      int hh, l;
+      it.split(t, hh, l);
+      const int q = it.ltile(l) * BMQ + row;
       if (q < p.n) {
-        float* dst = p.dq_acc + ((static_cast<size_t>(it.wi.b) * L +
-                                  static_cast<size_t>(it.qhalf(t)) * p.n + q) * p.H + it.wi.h) * D;
+        const size_t pos = static_cast<size_t>(it.lhalf(l)) * p.n + q;
+        float* dst = p.dq_acc + ((static_cast<size_t>(it.wi.b) * L + pos) * p.H + it.h0 + hh) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 4)
           red_add_v4_f32(dst + c, __uint_as_float(dq[c]) * p.scale,
@@ -544,9 +565,11 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         tc_fence_after();
         const uint32_t nlse_s = sbase + C::kOffLSE + 4 * st * BMQ;
         const uint32_t ndel_s = sbase + C::kOffDEL + 4 * st * BMQ;
-        const int qs = it.qtile(i) * BMQ;
+        int hh, l;
+        it.split(i, hh, l);
+        const int qs = it.ltile(l) * BMQ;
         // Columns (queries) that see key j, as a 128-bit mask in 4 words.
-        const Interval iv = i < it.n0 ? iv0 : iv1;
+        const Interval iv = l < it.n0 ? iv0 : iv1;
         uint32_t keep[4];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
@@ -589,7 +612,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       mbar_arrive_warp(BAR(C::BAR_ACCFREE));
       if (j < p.n) {
         const size_t pos = static_cast<size_t>(it.wi.half) * p.n + j;
-        const size_t off = ((static_cast<size_t>(it.wi.b) * L + pos) * p.H + it.wi.h) * D;
+        const size_t off = ((static_cast<size_t>(it.wi.b) * L + pos) * p.Hk + it.wi.h) * D;
         __nv_bfloat16* dst = (wg == 0 ? p.dv : p.dk) + off;
         const float mul = wg == 0 ? 1.f : p.scale;
 #pragma unroll
@@ -627,7 +650,7 @@ static cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long items = 2LL * p.B * p.H * p.k_tiles;
+  const long long items = 2LL * p.B * p.Hk * p.k_tiles;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;

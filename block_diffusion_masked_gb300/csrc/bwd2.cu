@@ -125,19 +125,33 @@ struct Bwd2Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// One work item: key tile, head-dim half and the query tiles that see it
-// (at most two segments, kept in scalars so that nothing is indexed
-// dynamically).  The producer decodes each item once and publishes the
-// decoded form to the other roles through a ring in shared memory; v < 0
-// means no work is left.
+// One work item: key tile of one key/value head, head-dim half and the
+// query tiles that see it (at most two segments per query head, kept in
+// scalars so that nothing is indexed dynamically).  With grouped key/value
+// heads ("Fast Diffusion Attention": GQA-grouped backward) the item walks
+// the same query tiles of each of the kv_group query heads that read its
+// key/value head, h0, h0 + 1, ..., so that dK and dV sum over the group in
+// TMEM.  The producer decodes each item once and publishes the decoded form
+// to the other roles through a ring in shared memory; v < 0 means no work is
+// left.
 struct Bwd2Item {
   int v;
-  WorkItem wi;
+  WorkItem wi;  // wi.h: the key/value head
   int dh;
-  int n0, ntiles;
+  int n0, nth, ntiles;  // tiles of segment 0, per query head, in all
+  int h0;               // first query head of the group
   int half0, rule0, tb0, half1, rule1, tb1;
-  __device__ __forceinline__ int qtile(int t) const { return t < n0 ? tb0 + t : tb1 + (t - n0); }
-  __device__ __forceinline__ int qhalf(int t) const { return t < n0 ? half0 : half1; }
+  // Tile t is local tile l of query head h0 + hh.
+  __device__ __forceinline__ void split(int t, int& hh, int& l) const {
+    hh = 0;
+    l = t;
+    if (l >= nth) {
+      hh = l / nth;
+      l -= hh * nth;
+    }
+  }
+  __device__ __forceinline__ int ltile(int l) const { return l < n0 ? tb0 + l : tb1 + (l - n0); }
+  __device__ __forceinline__ int lhalf(int l) const { return l < n0 ? half0 : half1; }
 };
 
 static_assert(sizeof(Bwd2Item) <= 64, "item ring slot");
@@ -148,11 +162,13 @@ __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   it.v = v;
   if (v < 0) return it;
   it.dh = v % NDH;
-  it.wi = bwd_work(v / NDH, p.mode, p.B, p.H, p.k_tiles, p.group);
+  it.wi = bwd_work(v / NDH, p.mode, p.B, p.Hk, p.k_tiles, p.group);
+  it.h0 = it.wi.h * p.kv_group;
   Segment seg[2] = {};
   const int nseg = bwd_segments(p.mode, p.n, p.bs, BMQ, BN, it.wi.half, it.wi.tile, seg);
   it.n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
-  it.ntiles = it.n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
+  it.nth = it.n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
+  it.ntiles = it.nth * p.kv_group;
   it.half0 = seg[0].half;
   it.rule0 = seg[0].rule;
   it.tb0 = seg[0].t_begin;
@@ -242,15 +258,18 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
     // Q, dO, -LSE * log2(e) and -D of the item's t-th query tile into the
     // stage of global tile gg.
     auto load_q = [&](const Bwd2Item& it, int t, int gg) -> bool {
-      const int qt = it.qtile(t);
-      const int half = it.qhalf(t);
-      const float* del_bh = p.delta + (static_cast<size_t>(it.wi.b) * p.H + it.wi.h) * L;
+      int hh, l;
+      it.split(t, hh, l);
+      const int qt = it.ltile(l);
+      const int half = it.lhalf(l);
+      const int h = it.h0 + hh;  // query head
+      const float* del_bh = p.delta + (static_cast<size_t>(it.wi.b) * p.H + h) * L;
       float lse_r[2], del_r[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int q = qt * BMQ + lane + 32 * e;
         const bool valid = q < p.n;
-        lse_r[e] = valid ? p.lse[lse_offset(p.mode, it.wi.b, it.wi.h, half, q, p.H, p.n)] *
+        lse_r[e] = valid ? p.lse[lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n)] *
                                -1.4426950408889634f
                          : -INFINITY;
         del_r[e] = valid ? -del_bh[static_cast<size_t>(half) * p.n + q] : 0.f;
@@ -275,9 +294,9 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           tma_load_5d(sbase + C::kOffQ + st * C::kQBytes + c * BMQ * 128, &p.tm_q,
-                      BAR(C::BAR_QFULL + st), 64 * c, it.wi.h, qt * BMQ, half, it.wi.b);
+                      BAR(C::BAR_QFULL + st), 64 * c, h, qt * BMQ, half, it.wi.b);
           tma_load_5d(sbase + C::kOffDO + st * C::kQBytes + c * BMQ * 128, &p.tm_do,
-                      BAR(C::BAR_QFULL + st), 64 * c, it.wi.h, qt * BMQ, half, it.wi.b);
+                      BAR(C::BAR_QFULL + st), 64 * c, h, qt * BMQ, half, it.wi.b);
         }
       }
       __syncwarp();
@@ -462,7 +481,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
     const size_t dq_stride = static_cast<size_t>(p.H) * D;
     // dQ^T of the tile whose products completed last: TMEM lane = head dim
     // `row`, columns = queries; added into the float32 accumulator.
-    auto drain_dq = [&](const Bwd2Item& it, int qh, int qs) -> bool {
+    auto drain_dq = [&](const Bwd2Item& it, int h, int qh, int qs) -> bool {
       uint32_t dq[HC];
       tmem_ld_cols<HC>(t_lane + C::kTmemDQ + c0, dq);
       tmem_wait_ld();
@@ -483,7 +502,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && qs + c0 < p.n) {
-          tma_reduce_add_5d(&p.tm_dq, stg, it.dh * DH + 32 * (warp & 3), it.wi.h, qs + c0, qh,
+          tma_reduce_add_5d(&p.tm_dq, stg, it.dh * DH + 32 * (warp & 3), h, qs + c0, qh,
                             it.wi.b);
           bulk_commit_group();
         }
@@ -491,7 +510,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       }
       float* ptr = p.dq_acc +
                    ((static_cast<size_t>(it.wi.b) * L + static_cast<size_t>(qh) * p.n + qs + c0) *
-                        p.H + it.wi.h) * D + it.dh * DH + row;
+                        p.H + h) * D + it.dh * DH + row;
       if (qs + c0 + HC <= p.n) {
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
@@ -521,11 +540,13 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       // the mask does not cut gives the full column mask below).
       const Interval iv0 = query_interval(it.rule0, j, p.n, p.bs);
       const Interval iv1 = query_interval(it.rule1, j, p.n, p.bs);
-      for (int i = 0; i < it.ntiles && ok; ++i) {
+      // (head, half, first row) of the previous tile, for its dQ
+      int prev_h = 0, prev_half = 0, prev_qs = 0;
+      for (int i = 0, hh = 0, l = 0; i < it.ntiles && ok; ++i) {
         const int gg = g + i;
-        const int qt = it.qtile(i);
         const int st = gg % STAGES;
-        const int qs = qt * BMQ;
+        const int qs = it.ltile(l) * BMQ;
+        const bool seg0 = l < it.n0;
         if (!(ok = mbar_wait_warp(BAR(C::BAR_SDPFULL), gg & 1, ab))) break;
         tc_fence_after();
         uint32_t sr[HC], dpr[HC];
@@ -543,7 +564,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         // those in [clo, chi) (all of them on a tile the mask does not cut).
         uint32_t keep;
         {
-          const Interval iv = i < it.n0 ? iv0 : iv1;
+          const Interval iv = seg0 ? iv0 : iv1;
           const int lo = iv.lo - qs - c0, hi = iv.hi - qs - c0;
           const int clo = lo < 0 ? 0 : (lo > HC ? HC : lo);
           const int chi = hi < clo ? clo : (hi > HC ? HC : hi);
@@ -600,7 +621,14 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         tc_fence_before();
         mbar_arrive_warp(BAR(C::BAR_PDSFULL));
         // The previous tile's products are complete (waited above): its dQ.
-        if (i >= 1 && !(ok = drain_dq(it, it.qhalf(i - 1), it.qtile(i - 1) * BMQ))) break;
+        if (i >= 1 && !(ok = drain_dq(it, prev_h, prev_half, prev_qs))) break;
+        prev_h = it.h0 + hh;
+        prev_half = it.lhalf(l);
+        prev_qs = qs;
+        if (++l == it.nth) {
+          l = 0;
+          ++hh;
+        }
       }
       if (!ok) break;
 
@@ -632,7 +660,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       if (j < p.n) {
         const size_t pos = static_cast<size_t>(it.wi.half) * p.n + j;
         const size_t off =
-            ((static_cast<size_t>(it.wi.b) * L + pos) * p.H + it.wi.h) * D + it.dh * DH + d0;
+            ((static_cast<size_t>(it.wi.b) * L + pos) * p.Hk + it.wi.h) * D + it.dh * DH + d0;
         __nv_bfloat16* dst = (is_v ? p.dv : p.dk) + off;
         const float mul = is_v ? 1.f : p.scale;
 #pragma unroll
@@ -645,9 +673,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           st_global_v4(dst + 8 * g8, w[0], w[1], w[2], w[3]);
         }
       }
-      if (it.ntiles > 0 &&
-          !(ok = drain_dq(it, it.qhalf(it.ntiles - 1), it.qtile(it.ntiles - 1) * BMQ)))
-        break;
+      if (it.ntiles > 0 && !(ok = drain_dq(it, prev_h, prev_half, prev_qs))) break;
       g += it.ntiles;
       ++k;
     }
@@ -682,7 +708,7 @@ static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
   if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
   if (fa.numRegs * C::kThreads < C::kRegCtl * 128 + C::kRegCompute * 128 * C::NWG)
     return cudaErrorInvalidConfiguration;
-  const long long items = 2LL * p.B * p.H * p.k_tiles * C::NDH;
+  const long long items = 2LL * p.B * p.Hk * p.k_tiles * C::NDH;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;

@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
   const int n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
   const int ntiles = n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
   const int qs = wi.tile * BM;
+  const int hk = wi.h / p.kv_group;  // key/value head
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::BAR_Q), 1);
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
-                      BAR(C::BAR_KFULL + st), 64 * c, wi.h, kt * BN, seg[s].half, wi.b);
+                      BAR(C::BAR_KFULL + st), 64 * c, hk, kt * BN, seg[s].half, wi.b);
         if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_VEMPTY + st), (round - 1) & 1, ab))) {
           // K of this stage is in flight; account for it while unwinding.
           ++j;
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
-                      BAR(C::BAR_VFULL + st), 64 * c, wi.h, kt * BN, seg[s].half, wi.b);
+                      BAR(C::BAR_VFULL + st), 64 * c, hk, kt * BN, seg[s].half, wi.b);
       }
       if (!ok) {
         // Unwinding: let the copies already issued land before the CTA exits.

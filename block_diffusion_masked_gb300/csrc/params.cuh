@@ -24,6 +24,7 @@ struct FwdParams {
   float* lse;
   unsigned* status;
   int B, n, H, bs, mode;
+  int kv_group;      // query heads per key/value head (1: multi-head)
   int q_tiles;       // tiles per half along the queries
   int group;         // (batch, head) pairs per scheduling group
   float scale_log2;  // softmax scale * log2(e)
@@ -47,8 +48,10 @@ struct BwdParams {
   __nv_bfloat16* dv;
   unsigned* status;
   int B, n, H, bs, mode;
+  int Hk;             // key/value heads (dk, dv are (B, 2n, Hk, d))
+  int kv_group;       // query heads per key/value head, H / Hk
   int k_tiles;        // tiles per half along the keys
-  int group;          // (batch, head) pairs per scheduling group
+  int group;          // (batch, key/value head) pairs per scheduling group
   float scale;        // softmax scale
   float scale_log2;   // scale * log2(e)
   unsigned* sched;    // work counter of a persistent launch (see sched_next)

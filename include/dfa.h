@@ -99,6 +99,28 @@ int dfa_backward(const void *q, const void *k, const void *v, const void *out,
                  dfa_stream_t stream);
 
 /*
+ * Grouped key/value heads (multi-query and grouped-query attention, which
+ * "Fast Diffusion Attention" lists among the supported shapes, with a
+ * "GQA-grouped backward"): k and v (and dk, dv) are (batch, 2n, kv_heads,
+ * headdim) bf16 while q, out, dout, dq are (batch, 2n, heads, headdim) and
+ * lse (batch, heads, 2n).  Query head h reads key/value head
+ * h / (heads / kv_heads) (integer division: consecutive query heads share a
+ * key/value head).  kv_heads must divide heads (1 <= kv_heads <= heads),
+ * otherwise DFA_EINVAL.  dk and dv of a key/value head are the sums of the
+ * gradients through all of its query heads, accumulated on chip (a work
+ * item of the backward walks the query tiles of every query head of its
+ * group).  kv_heads == heads is dfa_forward / dfa_backward.  Scratch and
+ * errors as for dfa_forward / dfa_backward.
+ */
+int dfa_forward_gqa(const void *q, const void *k, const void *v, void *out, float *lse,
+                    int batch, int n, int heads, int kv_heads, int headdim, int block_size,
+                    dfa_stream_t stream);
+int dfa_backward_gqa(const void *q, const void *k, const void *v, const void *out,
+                     const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                     int batch, int n, int heads, int kv_heads, int headdim, int block_size,
+                     dfa_stream_t stream);
+
+/*
  * The yardstick of "Fast Diffusion Attention", section "The right yardstick":
  * causal attention on `batch` independent sequences of length `seqlen`, same
  * layout (batch, seqlen, heads, headdim), lse (batch, heads, seqlen), run by

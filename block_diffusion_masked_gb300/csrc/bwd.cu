@@ -109,13 +109,17 @@ struct BwdItem {
   int n0, nth, ntiles;  // tiles of segment 0, per query head, in all
   int h0;               // first query head of the group
   int half0, rule0, tb0, half1, rule1, tb1;
-  // Tile t is local tile l of query head h0 + hh.
+  // Tile t is local tile l of query head h0 + hh.  Without grouping
+  // (GQA false: one query head per key/value head) l = t and hh = 0.
+  template <bool GQA>
   __device__ __forceinline__ void split(int t, int& hh, int& l) const {
     hh = 0;
     l = t;
-    if (l >= nth) {
-      hh = l / nth;
-      l -= hh * nth;
+    if constexpr (GQA) {
+      if (l >= nth) {
+        hh = l / nth;
+        l -= hh * nth;
+      }
     }
   }
   __device__ __forceinline__ int ltile(int l) const { return l < n0 ? tb0 + l : tb1 + (l - n0); }
@@ -124,18 +128,18 @@ struct BwdItem {
 
 static_assert(sizeof(BwdItem) <= 64, "item ring slot");
 
-template <int BMQ, int BN>
+template <int BMQ, int BN, bool GQA>
 __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   BwdItem it;
   it.v = v;
   if (v < 0) return it;
   it.wi = bwd_work(v, p.mode, p.B, p.Hk, p.k_tiles, p.group);
-  it.h0 = it.wi.h * p.kv_group;
+  it.h0 = GQA ? it.wi.h * p.kv_group : it.wi.h;
   Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
   const int nseg = bwd_segments(p.mode, p.n, p.bs, BMQ, BN, it.wi.half, it.wi.tile, seg);
   it.n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
   it.nth = it.n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
-  it.ntiles = it.nth * p.kv_group;
+  it.ntiles = GQA ? it.nth * p.kv_group : it.nth;
   it.half0 = seg[0].half;
   it.rule0 = seg[0].rule;
   it.tb0 = seg[0].t_begin;
@@ -145,7 +149,7 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   return it;
 }
 
-template <int D, int BMQ>
+template <int D, int BMQ, bool GQA>
 __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D, BMQ>;
   constexpr int BN = C::BN;
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     // into the stage of global tile gg.  Rows past the half: probability 0.
     auto load_q = [&](const BwdItem& it, int t, int gg) -> bool {
       int hh, l;
-      it.split(t, hh, l);
+      it.template split<GQA>(t, hh, l);
       const int qt = it.ltile(l);
       const int half = it.lhalf(l);
       const int h = it.h0 + hh;  // query head
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       int v = -1;
       if (lane == 0) v = sched_next(p.sched, p.items);
       v = __shfl_sync(0xffffffffu, v, 0);
-      const BwdItem it = bwd_item<BMQ, BN>(p, v);
+      const BwdItem it = bwd_item<BMQ, BN, GQA>(p, v);
       if (lane == 0) {
         *ring(k & 3) = it;
         mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       tc_fence_before();
       mbar_arrive_warp(BAR(C::BAR_DQFREE + b));
       int hh, l;
-      it.split(t, hh, l);
+      it.template split<GQA>(t, hh, l);
       const int q = it.ltile(l) * BMQ + row;
       if (q < p.n) {
         const size_t pos = static_cast<size_t>(it.lhalf(l)) * p.n + q;
@@ -566,7 +570,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         const uint32_t nlse_s = sbase + C::kOffLSE + 4 * st * BMQ;
         const uint32_t ndel_s = sbase + C::kOffDEL + 4 * st * BMQ;
         int hh, l;
-        it.split(i, hh, l);
+        it.template split<GQA>(i, hh, l);
         const int qs = it.ltile(l) * BMQ;
         // Columns (queries) that see key j, as a 128-bit mask in 4 words.
         const Interval iv = l < it.n0 ? iv0 : iv1;
@@ -643,10 +647,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int BMQ>
+template <int D, int BMQ, bool GQA>
 static cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D, BMQ>;
-  auto kern = dfa_bwd_kernel<D, BMQ>;
+  auto kern = dfa_bwd_kernel<D, BMQ, GQA>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -666,7 +670,10 @@ static cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream) {
   switch (headdim) {
-    case 64: return launch_bwd_impl<64, 128>(p, stream);
+    // grouped key/value heads have their own instantiation
+    case 64:
+      return p.kv_group > 1 ? launch_bwd_impl<64, 128, true>(p, stream)
+                            : launch_bwd_impl<64, 128, false>(p, stream);
     case 128: return launch_backward_d128(p, stream);
     case 256: return launch_backward_d256(p, stream);
     default: return cudaErrorInvalidValue;

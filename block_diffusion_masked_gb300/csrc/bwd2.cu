@@ -141,13 +141,17 @@ struct Bwd2Item {
   int n0, nth, ntiles;  // tiles of segment 0, per query head, in all
   int h0;               // first query head of the group
   int half0, rule0, tb0, half1, rule1, tb1;
-  // Tile t is local tile l of query head h0 + hh.
+  // Tile t is local tile l of query head h0 + hh.  Without grouping
+  // (GQA false: one query head per key/value head) l = t and hh = 0.
+  template <bool GQA>
   __device__ __forceinline__ void split(int t, int& hh, int& l) const {
     hh = 0;
     l = t;
-    if (l >= nth) {
-      hh = l / nth;
-      l -= hh * nth;
+    if constexpr (GQA) {
+      if (l >= nth) {
+        hh = l / nth;
+        l -= hh * nth;
+      }
     }
   }
   __device__ __forceinline__ int ltile(int l) const { return l < n0 ? tb0 + l : tb1 + (l - n0); }
@@ -156,19 +160,19 @@ struct Bwd2Item {
 
 static_assert(sizeof(Bwd2Item) <= 64, "item ring slot");
 
-template <int NDH, int BMQ, int BN>
+template <int NDH, int BMQ, int BN, bool GQA>
 __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   Bwd2Item it;
   it.v = v;
   if (v < 0) return it;
   it.dh = v % NDH;
   it.wi = bwd_work(v / NDH, p.mode, p.B, p.Hk, p.k_tiles, p.group);
-  it.h0 = it.wi.h * p.kv_group;
+  it.h0 = GQA ? it.wi.h * p.kv_group : it.wi.h;
   Segment seg[2] = {};
   const int nseg = bwd_segments(p.mode, p.n, p.bs, BMQ, BN, it.wi.half, it.wi.tile, seg);
   it.n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
   it.nth = it.n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
-  it.ntiles = it.nth * p.kv_group;
+  it.ntiles = GQA ? it.nth * p.kv_group : it.nth;
   it.half0 = seg[0].half;
   it.rule0 = seg[0].rule;
   it.tb0 = seg[0].t_begin;
@@ -178,7 +182,7 @@ __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   return it;
 }
 
-template <int D_, int STAGES_, int NWG_, int KVBUF_>
+template <int D_, int STAGES_, int NWG_, int KVBUF_, bool GQA>
 __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 1)
     dfa_bwd2_kernel(const __grid_constant__ BwdParams p) {
   using C = Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>;
@@ -259,7 +263,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
     // stage of global tile gg.
     auto load_q = [&](const Bwd2Item& it, int t, int gg) -> bool {
       int hh, l;
-      it.split(t, hh, l);
+      it.template split<GQA>(t, hh, l);
       const int qt = it.ltile(l);
       const int half = it.lhalf(l);
       const int h = it.h0 + hh;  // query head
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       int v = -1;
       if (lane == 0) v = sched_next(p.sched, p.items);
       v = __shfl_sync(0xffffffffu, v, 0);
-      const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN>(p, v);
+      const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN, GQA>(p, v);
       if (lane == 0) {
         *ring(k & 3) = it;
         mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
@@ -540,11 +544,17 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       // the mask does not cut gives the full column mask below).
       const Interval iv0 = query_interval(it.rule0, j, p.n, p.bs);
       const Interval iv1 = query_interval(it.rule1, j, p.n, p.bs);
-      // (head, half, first row) of the previous tile, for its dQ
-      int prev_h = 0, prev_half = 0, prev_qs = 0;
-      for (int i = 0, hh = 0, l = 0; i < it.ntiles && ok; ++i) {
+      // dQ of tile t: query head, half and first row
+      auto drain_tile = [&](int t) -> bool {
+        int hh, l;
+        it.template split<GQA>(t, hh, l);
+        return drain_dq(it, it.h0 + hh, it.lhalf(l), it.ltile(l) * BMQ);
+      };
+      for (int i = 0; i < it.ntiles && ok; ++i) {
         const int gg = g + i;
         const int st = gg % STAGES;
+        int hh, l;
+        it.template split<GQA>(i, hh, l);
         const int qs = it.ltile(l) * BMQ;
         const bool seg0 = l < it.n0;
         if (!(ok = mbar_wait_warp(BAR(C::BAR_SDPFULL), gg & 1, ab))) break;
@@ -621,14 +631,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         tc_fence_before();
         mbar_arrive_warp(BAR(C::BAR_PDSFULL));
         // The previous tile's products are complete (waited above): its dQ.
-        if (i >= 1 && !(ok = drain_dq(it, prev_h, prev_half, prev_qs))) break;
-        prev_h = it.h0 + hh;
-        prev_half = it.lhalf(l);
-        prev_qs = qs;
-        if (++l == it.nth) {
-          l = 0;
-          ++hh;
-        }
+        if (i >= 1 && !(ok = drain_tile(i - 1))) break;
       }
       if (!ok) break;
 
@@ -673,7 +676,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           st_global_v4(dst + 8 * g8, w[0], w[1], w[2], w[3]);
         }
       }
-      if (it.ntiles > 0 && !(ok = drain_dq(it, prev_h, prev_half, prev_qs))) break;
+      if (it.ntiles > 0 && !(ok = drain_tile(it.ntiles - 1))) break;
       g += it.ntiles;
       ++k;
     }
@@ -695,10 +698,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int STAGES, int NWG, int KVBUF>
+template <int D, int STAGES, int NWG, int KVBUF, bool GQA>
 static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
   using C = Bwd2Cfg<D, STAGES, NWG, KVBUF>;
-  auto kern = dfa_bwd2_kernel<D, STAGES, NWG, KVBUF>;
+  auto kern = dfa_bwd2_kernel<D, STAGES, NWG, KVBUF, GQA>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -723,11 +726,15 @@ static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_backward_d128(const BwdParams& p, cudaStream_t stream) {
-  return launch_bwd2_impl<128, 3, kBwd2WarpgroupsD128, 1>(p, stream);
+  // Grouped key/value heads get their own instantiation, so that the
+  // multi-head kernel keeps its tile loop free of head bookkeeping.
+  return p.kv_group > 1 ? launch_bwd2_impl<128, 3, kBwd2WarpgroupsD128, 1, true>(p, stream)
+                        : launch_bwd2_impl<128, 3, kBwd2WarpgroupsD128, 1, false>(p, stream);
 }
 
 cudaError_t launch_backward_d256(const BwdParams& p, cudaStream_t stream) {
-  return launch_bwd2_impl<256, 1, 2, 1>(p, stream);
+  return p.kv_group > 1 ? launch_bwd2_impl<256, 1, 2, 1, true>(p, stream)
+                        : launch_bwd2_impl<256, 1, 2, 1, false>(p, stream);
 }
 
 }  // namespace dfa

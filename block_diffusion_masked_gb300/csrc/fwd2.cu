@@ -89,7 +89,6 @@ struct Fwd2Cfg {
 struct ItemGeom {
   int item;
   WorkItem wi;
-  int hk;  // key/value head of query head wi.h
   int n0, ntiles, qs;
   int half0, rule0, tb0, half1, rule1, tb1;
   __device__ __forceinline__ int ktile(int j) const { return j < n0 ? tb0 + j : tb1 + (j - n0); }
@@ -103,7 +102,6 @@ __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, 
   g->item = item;
   if (item < 0) return;
   g->wi = fwd_work(item, p.mode, p.B, p.H, p.q_tiles, p.group);
-  g->hk = g->wi.h / p.kv_group;
   Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
   const int nseg = fwd_segments(p.mode, p.n, p.bs, bm, bn, g->wi.half, g->wi.tile, seg);
   g->n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
@@ -222,6 +220,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, &p.tm_q,
                       BAR(C::BAR_QFULL + qb), 64 * c, ig.wi.h, ig.qs, ig.wi.half, ig.wi.b);
+        // key/value head of query head wi.h (grouped heads: kv_group > 1)
+        const int hk = p.kv_group == 1 ? ig.wi.h : ig.wi.h / p.kv_group;
         for (int j = 0; j < ig.ntiles; ++j, ++g) {
           const int st = g % STAGES;
           const int round = g / STAGES;
@@ -230,11 +230,11 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
-                        BAR(C::BAR_KFULL + st), 64 * c, ig.hk, ig.ktile(j) * BN, ig.khalf(j),
+                        BAR(C::BAR_KFULL + st), 64 * c, hk, ig.ktile(j) * BN, ig.khalf(j),
                         ig.wi.b);
           if (vg >= 0 && !(ok = load_v())) break;
           vg = g;
-          vh = ig.hk;
+          vh = hk;
           vb = ig.wi.b;
           vkt = ig.ktile(j);
           vkh = ig.khalf(j);

@@ -18,6 +18,8 @@ from .attention import (  # noqa: F401
     masked_attention_backward,
     diffusion_forward,
     diffusion_backward,
+    diffusion_varlen_forward,
+    diffusion_varlen_backward,
     causal_forward,
     causal_backward,
     online_softmax_row,

@@ -236,6 +236,69 @@ def diffusion_backward(q, k, v, dout, block_size, heads=None):
     return dq, dk, dv
 
 
+# --------------------------------------------------------------------------
+# Packed batches of different lengths ("Fast Diffusion Attention": varlen
+# batches; the API is modeled on FlashAttention's varlen call).
+# q, out: (rows, heads, headdim); k, v: (rows, kv_heads, headdim); lse:
+# (heads, rows).  Sample b is rows [cu[b], cu[b+1]), [noisy | clean].
+# --------------------------------------------------------------------------
+
+def _varlen_samples(cu_seqlens, rows):
+    cu = [int(x) for x in cu_seqlens]
+    if not cu or cu[0] != 0 or cu[-1] != rows:
+        raise ValueError("cu_seqlens must start at 0 and end at the packed rows")
+    out = []
+    for b in range(len(cu) - 1):
+        a, e = cu[b], cu[b + 1]
+        if e < a or (e - a) % 2:
+            raise ValueError("every sample length must be even and non-negative")
+        out.append((a, e))
+    return out
+
+
+def diffusion_varlen_forward(q, k, v, cu_seqlens, block_size):
+    """Forward on a packed batch: each sample is attended to on its own.
+
+    Returns out (rows, H, d) and lse (H, rows), float64.  Every sample uses
+    the mask of its own half length, with the same block size.
+    """
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    rows, H, d = q.shape
+    kvh = _kv_head(q[None], k[None])
+    out = np.zeros((rows, H, d))
+    lse = np.zeros((H, rows))
+    for a, e in _varlen_samples(cu_seqlens, rows):
+        if e == a:
+            continue
+        mask = diffusion_mask((e - a) // 2, block_size)
+        for h in range(H):
+            o, s = masked_attention_forward(q[a:e, h], k[a:e, kvh(h)], v[a:e, kvh(h)], mask)
+            out[a:e, h] = o
+            lse[h, a:e] = s
+    return out, lse
+
+
+def diffusion_varlen_backward(q, k, v, dout, cu_seqlens, block_size):
+    """Gradients of a packed batch: dq (rows, H, d), dk, dv (rows, H_kv, d)."""
+    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    rows, H, d = q.shape
+    kvh = _kv_head(q[None], k[None])
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for a, e in _varlen_samples(cu_seqlens, rows):
+        if e == a:
+            continue
+        mask = diffusion_mask((e - a) // 2, block_size)
+        for h in range(H):
+            hk = kvh(h)
+            g = masked_attention_backward(q[a:e, h], k[a:e, hk], v[a:e, hk], dout[a:e, h], mask)
+            dq[a:e, h] = g[0]
+            dk[a:e, hk] += g[1]
+            dv[a:e, hk] += g[2]
+    return dq, dk, dv
+
+
 def causal_forward(q, k, v, heads=None):
     """Causal attention on (Bc, L, H, d): the yardstick of "The right yardstick"."""
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))

@@ -13,13 +13,14 @@ The binding is imported lazily so that ``inputs`` can be used without CUDA.
 
 from __future__ import annotations
 
-__all__ = ["diffusion_attn_func", "causal_attn_func", "binding"]
+__all__ = ["diffusion_attn_func", "diffusion_attn_varlen_func", "causal_attn_func", "binding"]
 
 
 def __getattr__(name):
     import importlib
 
-    if name in ("diffusion_attn_func", "causal_attn_func", "DiffusionAttnFunc", "CausalAttnFunc"):
+    if name in ("diffusion_attn_func", "diffusion_attn_varlen_func", "causal_attn_func",
+                "DiffusionAttnFunc", "DiffusionAttnVarlenFunc", "CausalAttnFunc"):
         return getattr(importlib.import_module(__name__ + ".autograd"), name)
     if name in ("binding", "autograd", "inputs", "build"):
         return importlib.import_module(__name__ + "." + name)

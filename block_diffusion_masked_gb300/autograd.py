@@ -51,6 +51,35 @@ class CausalAttnFunc(torch.autograd.Function):
         return dq, dk, dv
 
 
+class DiffusionAttnVarlenFunc(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, cu_seqlens, block_size):
+        q, k, v = (t.contiguous() for t in (q, k, v))
+        cu = [int(x) for x in (cu_seqlens.tolist() if isinstance(cu_seqlens, torch.Tensor)
+                               else cu_seqlens)]
+        out, lse = binding.dfa_forward_varlen(q, k, v, cu, block_size)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.cu = cu
+        ctx.block_size = block_size
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        dq, dk, dv = binding.dfa_backward_varlen(q, k, v, out, dout.contiguous(), lse, ctx.cu,
+                                                 ctx.block_size)
+        return dq, dk, dv, None, None
+
+
+def diffusion_attn_varlen_func(q, k, v, cu_seqlens, block_size):
+    """Block-diffusion attention on a packed batch (the pages' varlen API).
+
+    q: (rows, heads, headdim), k, v: (rows, kv_heads, headdim) bf16; sample b
+    is rows [cu_seqlens[b], cu_seqlens[b+1]), [noisy | clean], even length.
+    """
+    return DiffusionAttnVarlenFunc.apply(q, k, v, cu_seqlens, block_size)
+
+
 def diffusion_attn_func(q, k, v, block_size):
     """Attention under the block-diffusion mask; differentiable."""
     return DiffusionAttnFunc.apply(q, k, v, block_size)

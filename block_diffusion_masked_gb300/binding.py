@@ -39,6 +39,8 @@ _SIGNATURES = {
     "dfa_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _I, _P]),
     "dfa_forward_gqa": (_I, [_P] * 5 + [_I] * 6 + [_P]),
     "dfa_backward_gqa": (_I, [_P] * 9 + [_I] * 6 + [_P]),
+    "dfa_forward_varlen": (_I, [_P] * 6 + [_I] * 5 + [_P]),
+    "dfa_backward_varlen": (_I, [_P] * 10 + [_I] * 5 + [_P]),
     "dfa_causal_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "dfa_causal_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _P]),
     "dfa_status": (_I, [_P]),
@@ -196,6 +198,67 @@ def dfa_backward_gqa(q, k, v, out, dout, lse, block_size, dq=None, dk=None, dv=N
                                     _ptr(dq), _ptr(dk), _ptr(dv), B, L // 2, H, Hk, d,
                                     int(block_size), _stream_ptr(q))
     _check("dfa_backward_gqa", rc)
+    return dq, dk, dv
+
+
+def _cu_array(cu_seqlens, rows):
+    """Host int32 copy of cu_seqlens (list, NumPy array or tensor) as a ctypes array."""
+    if isinstance(cu_seqlens, torch.Tensor):
+        cu_seqlens = cu_seqlens.detach().cpu().tolist()
+    cu = [int(x) for x in cu_seqlens]
+    if len(cu) < 1 or cu[0] != 0 or cu[-1] != rows:
+        raise ValueError("cu_seqlens must start at 0 and end at the packed rows")
+    return (ctypes.c_int * len(cu))(*cu), len(cu) - 1
+
+
+def _check_packed(q, k, v, *more):
+    for t in (q, k, v) + more:
+        if t.dim() != 3:
+            raise ValueError("expected packed (rows, heads, headdim) tensors")
+    _check_qkv(q[None], *(t[None] for t in more))
+    _check_qkv(k[None], v[None])
+    if k.device != q.device or k.shape[0] != q.shape[0] or k.shape[2] != q.shape[2]:
+        raise ValueError("k and v must be (rows, kv_heads, headdim) like q")
+    if k.shape[1] < 1 or q.shape[1] % k.shape[1]:
+        raise ValueError("kv_heads must divide the query heads")
+    return k.shape[1]
+
+
+def dfa_forward_varlen(q, k, v, cu_seqlens, block_size, out=None, lse=None):
+    """Forward on a packed batch: q (rows, H, d), k, v (rows, Hk, d) bf16 CUDA.
+
+    ``cu_seqlens`` (host: list, array or tensor) holds batch + 1 prefix sums;
+    every sample length is even ([noisy | clean]).  Returns out (rows, H, d)
+    and lse (H, rows) float32.
+    """
+    Hk = _check_packed(q, k, v)
+    rows, H, d = q.shape
+    cu, batch = _cu_array(cu_seqlens, rows)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, rows), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_forward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), cu, batch,
+                                      H, Hk, d, int(block_size), _stream_ptr(q))
+    _check("dfa_forward_varlen", rc)
+    return out, lse
+
+
+def dfa_backward_varlen(q, k, v, out, dout, lse, cu_seqlens, block_size, dq=None, dk=None,
+                        dv=None):
+    """Backward on a packed batch; returns (dq, dk, dv) bf16."""
+    Hk = _check_packed(q, k, v, out, dout)
+    rows, H, d = q.shape
+    if lse.shape != (H, rows) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 (heads, rows)")
+    cu, batch = _cu_array(cu_seqlens, rows)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_backward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
+                                       _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), cu, batch, H, Hk,
+                                       d, int(block_size), _stream_ptr(q))
+    _check("dfa_backward_varlen", rc)
     return dq, dk, dv
 
 

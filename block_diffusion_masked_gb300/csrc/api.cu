@@ -2,9 +2,11 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <initializer_list>
 #include <mutex>
+#include <vector>
 
 #include "dfa.h"
 #include "geometry.cuh"
@@ -115,12 +117,16 @@ unsigned* sched_for_stream(DeviceState* s, cudaStream_t stream) {
 // increasing -- and load boxes of (64, 1, rows, 1, 1) with 128-byte swizzle:
 // `rows` consecutive positions of one half of one head, 64 head dims each.
 // Rows past the end of a half read zero.
-int make_map(CUtensorMap* map, const void* base, int B, int n, int H, int d, int rows) {
+int make_map(CUtensorMap* map, const void* base, int B, int n, int H, int d, int rows,
+             bool packed = false) {
+  // packed (varlen): n is the number of rows of the packed tensor, viewed as
+  // (d, H, rows, 1, 1)
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
-                              static_cast<cuuint64_t>(n), 2, static_cast<cuuint64_t>(B)};
+                              static_cast<cuuint64_t>(n), packed ? 1u : 2u,
+                              packed ? 1u : static_cast<cuuint64_t>(B)};
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(H) * d * 2;
   const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * 2, row_bytes, row_bytes * n,
-                                 row_bytes * 2 * n};
+                                 row_bytes * n * (packed ? 1 : 2)};
   const cuuint32_t box[5] = {64, 1, static_cast<cuuint32_t>(rows), 1, 1};
   const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
@@ -134,12 +140,14 @@ int make_map(CUtensorMap* map, const void* base, int B, int n, int H, int d, int
 // boxes of (32, 1, rows, 1, 1), no swizzle: the target of the backward's
 // bulk reduce-add of one warp's part of a query tile's dQ (rows past the
 // end of a half are skipped by the copy engine).
-int make_map_f32(CUtensorMap* map, const void* base, int B, int n, int H, int d, int rows) {
+int make_map_f32(CUtensorMap* map, const void* base, int B, int n, int H, int d, int rows,
+                 bool packed = false) {
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
-                              static_cast<cuuint64_t>(n), 2, static_cast<cuuint64_t>(B)};
+                              static_cast<cuuint64_t>(n), packed ? 1u : 2u,
+                              packed ? 1u : static_cast<cuuint64_t>(B)};
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(H) * d * 4;
   const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * 4, row_bytes, row_bytes * n,
-                                 row_bytes * 2 * n};
+                                 row_bytes * n * (packed ? 1 : 2)};
   const cuuint32_t box[5] = {32, 1, static_cast<cuuint32_t>(rows), 1, 1};
   const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<void*>(base), dims,
@@ -178,7 +186,7 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   if ((rc = device_state(&ds))) return rc;
   TileShape ts;
   tile_shape_for(d, &ts);
-  FwdParams p;
+  FwdParams p{};
   if ((rc = make_map(&p.tm_q, q, B, n, H, d, ts.fwd_bm))) return rc;
   if ((rc = make_map(&p.tm_k, k, B, n, Hk, d, ts.fwd_bn))) return rc;
   if ((rc = make_map(&p.tm_v, v, B, n, Hk, d, ts.fwd_bn))) return rc;
@@ -226,7 +234,7 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   if ((rc = device_state(&ds))) return rc;
   TileShape ts;
   tile_shape_for(d, &ts);
-  BwdParams p;
+  BwdParams p{};
   if ((rc = make_map(&p.tm_q, q, B, n, H, d, ts.bwd_bm))) return rc;
   if ((rc = make_map(&p.tm_do, dout, B, n, H, d, ts.bwd_bm))) return rc;
   if ((rc = make_map(&p.tm_k, k, B, n, Hk, d, ts.bwd_bn))) return rc;
@@ -323,6 +331,215 @@ int backward_impl(int mode, const void* q, const void* k, const void* v, const v
   return rc;
 }
 
+// ------------------------------------------------------------ varlen
+// Packed batches: sample b is rows [cu[b], cu[b+1]) of the packed tensors,
+// its noisy half first, so every length cu[b+1] - cu[b] is even.  The
+// non-empty samples are scheduled longest first ("Fast Diffusion
+// Attention": varlen batches), one slot each.
+
+// Check cu_seqlens (host, batch + 1 entries) and return the packed rows.
+int varlen_rows(const int* cu, int batch, int* rows) {
+  if (!cu || batch < 0 || cu[0] != 0) return DFA_EINVAL;
+  for (int b = 0; b < batch; ++b) {
+    const long long len = static_cast<long long>(cu[b + 1]) - cu[b];
+    if (len < 0 || (len & 1)) return DFA_EINVAL;
+  }
+  if (cu[batch] > (1 << 30)) return DFA_EINVAL;
+  *rows = cu[batch];
+  return DFA_OK;
+}
+
+// Slots of the non-empty samples, longest first (ties in sample order), for
+// a pass whose work unit is (head, half, tile of `tile` rows): 2 * heads *
+// cdiv(n, tile) units per sample.  `bytes_per_pos` is what one position of
+// one head brings into L2, for the L2 head groups inside a sample.
+int varlen_schedule(const int* cu, int batch, int heads, int tile, long long bytes_per_pos,
+                    long long l2_bytes, std::vector<VarlenSlot>* slots, int* units) {
+  std::vector<int> order;
+  for (int b = 0; b < batch; ++b)
+    if (cu[b + 1] > cu[b]) order.push_back(b);
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+    return cu[a + 1] - cu[a] > cu[b + 1] - cu[b];
+  });
+  slots->clear();
+  long long off = 0;
+  for (int b : order) {
+    const int n = (cu[b + 1] - cu[b]) / 2;
+    VarlenSlot sl;
+    sl.b = b;
+    sl.n = n;
+    sl.row0 = cu[b];
+    sl.group = l2_group(bytes_per_pos * 2 * n, l2_bytes, heads);
+    sl.off = static_cast<int>(off);
+    slots->push_back(sl);
+    off += 2LL * heads * cdiv(n, tile);
+    if (off > 0x7fffffffLL) return DFA_EINVAL;
+  }
+  *units = static_cast<int>(off);
+  return DFA_OK;
+}
+
+// Copy the slot table to stream-ordered device memory (freed by the caller
+// with cudaFreeAsync after the launch that reads it).
+int upload_slots(const std::vector<VarlenSlot>& slots, cudaStream_t stream, VarlenSlot** dptr) {
+  const size_t bytes = slots.size() * sizeof(VarlenSlot);
+  if (cudaMallocAsync(reinterpret_cast<void**>(dptr), bytes, stream) != cudaSuccess)
+    return DFA_ECUDA;
+  if (cudaMemcpyAsync(*dptr, slots.data(), bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+    cudaFreeAsync(*dptr, stream);
+    return DFA_ECUDA;
+  }
+  return DFA_OK;
+}
+
+int check_varlen(int H, int Hk, int d, int bs) {
+  if (H < 1 || bs < 1) return DFA_EINVAL;
+  if (d != 64 && d != 128 && d != 256) return DFA_EUNSUPPORTED;
+  if (kv_group_of(H, Hk) == 0) return DFA_EINVAL;
+  return DFA_OK;
+}
+
+int forward_varlen_impl(const void* q, const void* k, const void* v, void* out, float* lse,
+                        const int* cu, int batch, int H, int Hk, int d, int bs,
+                        cudaStream_t stream) {
+  int rc = check_varlen(H, Hk, d, bs);
+  if (rc) return rc;
+  int rows = 0;
+  if ((rc = varlen_rows(cu, batch, &rows))) return rc;
+  if (rows == 0) return DFA_OK;
+  if (!q || !k || !v || !out || !lse) return DFA_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return DFA_EINVAL;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds))) return rc;
+  TileShape ts;
+  tile_shape_for(d, &ts);
+  std::vector<VarlenSlot> slots;
+  int units = 0;
+  // q, k, v and out of one head
+  if ((rc = varlen_schedule(cu, batch, H, ts.fwd_bm, 8LL * d, ds->l2_bytes, &slots, &units)))
+    return rc;
+  FwdParams p{};
+  if ((rc = make_map(&p.tm_q, q, 1, rows, H, d, ts.fwd_bm, true))) return rc;
+  if ((rc = make_map(&p.tm_k, k, 1, rows, Hk, d, ts.fwd_bn, true))) return rc;
+  if ((rc = make_map(&p.tm_v, v, 1, rows, Hk, d, ts.fwd_bn, true))) return rc;
+  if ((rc = make_map(&p.tm_o, out, 1, rows, H, d, ts.fwd_bm, true))) return rc;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = ds->status;
+  p.B = 1;
+  p.n = 1;  // per sample: the slot table
+  p.H = H;
+  p.kv_group = H / Hk;
+  p.bs = bs;  // clamped per sample by the kernels
+  p.mode = MODE_DIFFUSION;
+  p.q_tiles = 1;
+  p.group = 1;
+  p.sched = sched_for_stream(ds, stream);
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  p.vl_slots = static_cast<int>(slots.size());
+  p.rows = rows;
+  p.items = units;
+  VarlenSlot* dslots = nullptr;
+  if ((rc = upload_slots(slots, stream, &dslots))) return rc;
+  p.vl = dslots;
+  const cudaError_t e = launch_forward(p, d, stream);
+  cudaFreeAsync(dslots, stream);
+  return e == cudaSuccess ? DFA_OK : cuda_fail(e);
+}
+
+int backward_varlen_impl(const void* q, const void* k, const void* v, const void* out,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         const int* cu, int batch, int H, int Hk, int d, int bs,
+                         cudaStream_t stream) {
+  int rc = check_varlen(H, Hk, d, bs);
+  if (rc) return rc;
+  int rows = 0;
+  if ((rc = varlen_rows(cu, batch, &rows))) return rc;
+  if (rows == 0) return DFA_OK;
+  if (!aligned_all({q, k, v, out, dout, dq, dk, dv}) || !lse ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return DFA_EINVAL;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds))) return rc;
+  const int G = H / Hk;
+  TileShape ts;
+  tile_shape_for(d, &ts);
+  std::vector<VarlenSlot> slots;
+  int units = 0;
+  // per key/value head: k, v and, for each of its G query heads, q, dout
+  // (bf16) and the float32 dq accumulator
+  if ((rc = varlen_schedule(cu, batch, Hk, ts.bwd_bn, (4LL + 8LL * G) * d, ds->l2_bytes, &slots,
+                            &units)))
+    return rc;
+  const size_t elems = static_cast<size_t>(rows) * H * d;
+  float* dq_acc = nullptr;
+  float* delta = nullptr;
+  VarlenSlot* dslots = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&dq_acc), elems * sizeof(float), stream) !=
+      cudaSuccess)
+    return DFA_ECUDA;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&delta),
+                      static_cast<size_t>(rows) * H * sizeof(float), stream) != cudaSuccess) {
+    cudaFreeAsync(dq_acc, stream);
+    return DFA_ECUDA;
+  }
+  if ((rc = upload_slots(slots, stream, &dslots))) {
+    cudaFreeAsync(delta, stream);
+    cudaFreeAsync(dq_acc, stream);
+    return rc;
+  }
+  // delta = rowsum(dout * out) as (heads, rows), the layout of lse; dq_acc = 0
+  cudaError_t e = launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(out),
+                                        static_cast<const __nv_bfloat16*>(dout), delta, dq_acc,
+                                        1, rows, H, d, stream);
+  if (e == cudaSuccess) {
+    BwdParams p{};
+    if ((rc = make_map(&p.tm_q, q, 1, rows, H, d, ts.bwd_bm, true)) ||
+        (rc = make_map(&p.tm_do, dout, 1, rows, H, d, ts.bwd_bm, true)) ||
+        (rc = make_map(&p.tm_k, k, 1, rows, Hk, d, ts.bwd_bn, true)) ||
+        (rc = make_map(&p.tm_v, v, 1, rows, Hk, d, ts.bwd_bn, true)) ||
+        (d == 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, 1, rows, H, d,
+                                        ts.bwd_bm / kBwd2WarpgroupsD128, true)))) {
+      cudaFreeAsync(dslots, stream);
+      cudaFreeAsync(delta, stream);
+      cudaFreeAsync(dq_acc, stream);
+      return rc;
+    }
+    p.lse = lse;
+    p.delta = delta;
+    p.dq_acc = dq_acc;
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.status = ds->status;
+    p.B = 1;
+    p.n = 1;  // per sample: the slot table
+    p.H = H;
+    p.Hk = Hk;
+    p.kv_group = G;
+    p.bs = bs;  // clamped per sample by the kernels
+    p.mode = MODE_DIFFUSION;
+    p.k_tiles = 1;
+    p.group = 1;
+    p.sched = sched_for_stream(ds, stream);
+    p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    p.vl = dslots;
+    p.vl_slots = static_cast<int>(slots.size());
+    p.rows = rows;
+    p.units = units;
+    e = launch_backward(p, d, stream);
+  }
+  if (e == cudaSuccess)
+    e = launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), static_cast<long long>(elems),
+                          stream);
+  cudaFreeAsync(dslots, stream);
+  cudaFreeAsync(delta, stream);
+  cudaFreeAsync(dq_acc, stream);
+  return e == cudaSuccess ? DFA_OK : cuda_fail(e);
+}
+
 }  // namespace
 }  // namespace dfa
 
@@ -377,6 +594,21 @@ int dfa_backward_gqa(const void* q, const void* k, const void* v, const void* ou
 // whose halves are consecutive sequences, so the diffusion kernels run it in
 // their causal mode (each half attends causally to itself).  batch must be
 // even, as it is for the yardstick on the 2B halves of B samples.
+int dfa_forward_varlen(const void* q, const void* k, const void* v, void* out, float* lse,
+                       const int* cu_seqlens, int batch, int heads, int kv_heads, int headdim,
+                       int block_size, dfa_stream_t stream) {
+  return forward_varlen_impl(q, k, v, out, lse, cu_seqlens, batch, heads, kv_heads, headdim,
+                             block_size, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_backward_varlen(const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        const int* cu_seqlens, int batch, int heads, int kv_heads, int headdim,
+                        int block_size, dfa_stream_t stream) {
+  return backward_varlen_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens, batch, heads,
+                              kv_heads, headdim, block_size, static_cast<cudaStream_t>(stream));
+}
+
 int dfa_causal_forward(const void* q, const void* k, const void* v, void* out, float* lse,
                        int batch, int seqlen, int heads, int headdim, dfa_stream_t stream) {
   if (batch < 0 || seqlen < 1) return DFA_EINVAL;

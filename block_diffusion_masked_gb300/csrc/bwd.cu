@@ -76,7 +76,7 @@ struct BwdCfg {
     NUM_BARS = BAR_ALL + 1
   };
   static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 decoded items (BwdItem)
-  static constexpr int kOffTmemSlot = kOffItem + 4 * 64;
+  static constexpr int kOffTmemSlot = kOffItem + 4 * 128;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
   static constexpr int kTmemS = 0;          // S[b] at b * BMQ; dQ of the tile after S is read
@@ -109,6 +109,7 @@ struct BwdItem {
   int n0, nth, ntiles;  // tiles of segment 0, per query head, in all
   int h0;               // first query head of the group
   int half0, rule0, tb0, half1, rule1, tb1;
+  int n, bs, row0;  // half length, block size (clamped) and, varlen, first row
   // Tile t is local tile l of query head h0 + hh.  Without grouping
   // (GQA false: one query head per key/value head) l = t and hh = 0.
   template <bool GQA>
@@ -126,17 +127,29 @@ struct BwdItem {
   __device__ __forceinline__ int lhalf(int l) const { return l < n0 ? half0 : half1; }
 };
 
-static_assert(sizeof(BwdItem) <= 64, "item ring slot");
+static_assert(sizeof(BwdItem) <= 128, "item ring slot");
 
-template <int BMQ, int BN, bool GQA>
+template <int BMQ, int BN, bool GQA, bool VARLEN>
 __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   BwdItem it;
   it.v = v;
   if (v < 0) return it;
-  it.wi = bwd_work(v, p.mode, p.B, p.Hk, p.k_tiles, p.group);
+  if constexpr (VARLEN) {
+    const VarlenSlot sl = p.vl[varlen_slot(p.vl, p.vl_slots, v)];
+    it.wi = bwd_work(v - sl.off, MODE_DIFFUSION, 1, p.Hk, cdiv(sl.n, BN), sl.group);
+    it.wi.b = sl.b;
+    it.n = sl.n;
+    it.bs = imin(p.bs, sl.n);
+    it.row0 = sl.row0;
+  } else {
+    it.wi = bwd_work(v, p.mode, p.B, p.Hk, p.k_tiles, p.group);
+    it.n = p.n;
+    it.bs = p.bs;
+    it.row0 = 0;  // unused: batched rows come from wi.b
+  }
   it.h0 = GQA ? it.wi.h * p.kv_group : it.wi.h;
   Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
-  const int nseg = bwd_segments(p.mode, p.n, p.bs, BMQ, BN, it.wi.half, it.wi.tile, seg);
+  const int nseg = bwd_segments(p.mode, it.n, it.bs, BMQ, BN, it.wi.half, it.wi.tile, seg);
   it.n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
   it.nth = it.n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
   it.ntiles = GQA ? it.nth * p.kv_group : it.nth;
@@ -149,7 +162,7 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   return it;
 }
 
-template <int D, int BMQ, bool GQA>
+template <int D, int BMQ, bool GQA, bool VARLEN>
 __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D, BMQ>;
   constexpr int BN = C::BN;
@@ -163,7 +176,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
   // Slot s of the item ring; written by the producer before it arrives on
   // ITEMFULL[s] (release), read by the other roles after their wait (acquire).
-  auto ring = [&](int s) { return reinterpret_cast<BwdItem*>(smem + C::kOffItem + 64 * s); };
+  auto ring = [&](int s) { return reinterpret_cast<BwdItem*>(smem + C::kOffItem + 128 * s); };
   const AbortFlag ab{abort_flag, p.status};
   const size_t L = 2 * static_cast<size_t>(p.n);
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
@@ -230,16 +243,21 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       const int qt = it.ltile(l);
       const int half = it.lhalf(l);
       const int h = it.h0 + hh;  // query head
-      const float* del_bh = p.delta + (static_cast<size_t>(it.wi.b) * p.H + h) * L;
+      // delta (and, varlen, lse): (batch, heads, 2n) or, varlen, (heads, rows)
+      const float* del_bh = VARLEN ? p.delta + static_cast<size_t>(h) * p.rows + it.row0
+                                   : p.delta + (static_cast<size_t>(it.wi.b) * p.H + h) * L;
       float lse_r[kPerLane], del_r[kPerLane];
 #pragma unroll
       for (int e = 0; e < kPerLane; ++e) {
         const int q = qt * BMQ + lane + 32 * e;
-        const bool valid = q < p.n;
-        lse_r[e] = valid ? p.lse[lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n)] *
-                               -1.4426950408889634f
-                         : -INFINITY;
-        del_r[e] = valid ? -del_bh[static_cast<size_t>(half) * p.n + q] : 0.f;
+        const bool valid = q < it.n;
+        const size_t pos = static_cast<size_t>(half) * it.n + q;
+        const float lse =
+            !valid  ? 0.f
+            : VARLEN ? p.lse[static_cast<size_t>(h) * p.rows + it.row0 + pos]
+                     : p.lse[lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n)];
+        lse_r[e] = valid ? lse * -1.4426950408889634f : -INFINITY;
+        del_r[e] = valid ? -del_bh[pos] : 0.f;
       }
       const int st = gg % STAGES;
       const int round = gg / STAGES;
@@ -258,12 +276,13 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(BAR(C::BAR_QFULL + st), 2 * C::kQBytes);
+        const HalfRows qr = half_rows<VARLEN>(it.wi.b, half, it.n, it.row0);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           tma_load_5d(sbase + C::kOffQ + st * C::kQBytes + c * BMQ * 128, &p.tm_q,
-                      BAR(C::BAR_QFULL + st), 64 * c, h, qt * BMQ, half, it.wi.b);
+                      BAR(C::BAR_QFULL + st), 64 * c, h, qr.base + qt * BMQ, qr.c3, qr.c4);
           tma_load_5d(sbase + C::kOffDO + st * C::kQBytes + c * BMQ * 128, &p.tm_do,
-                      BAR(C::BAR_QFULL + st), 64 * c, h, qt * BMQ, half, it.wi.b);
+                      BAR(C::BAR_QFULL + st), 64 * c, h, qr.base + qt * BMQ, qr.c3, qr.c4);
         }
       }
       __syncwarp();
@@ -274,7 +293,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       int v = -1;
       if (lane == 0) v = sched_next(p.sched, p.items);
       v = __shfl_sync(0xffffffffu, v, 0);
-      const BwdItem it = bwd_item<BMQ, BN, GQA>(p, v);
+      const BwdItem it = bwd_item<BMQ, BN, GQA, VARLEN>(p, v);
       if (lane == 0) {
         *ring(k & 3) = it;
         mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
@@ -292,14 +311,15 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
       }
       if (lane == 0) {
-        const int ks = it.wi.tile * BN;
+        const HalfRows kr = half_rows<VARLEN>(it.wi.b, it.wi.half, it.n, it.row0);
+        const int krow = kr.base + it.wi.tile * BN;
         mbar_arrive_expect_tx(BAR(C::BAR_KV), 2 * C::kKVBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           tma_load_5d(sbase + C::kOffK + c * BN * 128, &p.tm_k, BAR(C::BAR_KV), 64 * c, it.wi.h,
-                      ks, it.wi.half, it.wi.b);
+                      krow, kr.c3, kr.c4);
           tma_load_5d(sbase + C::kOffV + c * BN * 128, &p.tm_v, BAR(C::BAR_KV), 64 * c, it.wi.h,
-                      ks, it.wi.half, it.wi.b);
+                      krow, kr.c3, kr.c4);
         }
       }
       __syncwarp();
@@ -478,9 +498,11 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       int hh, l;
       it.template split<GQA>(t, hh, l);
       const int q = it.ltile(l) * BMQ + row;
-      if (q < p.n) {
-        const size_t pos = static_cast<size_t>(it.lhalf(l)) * p.n + q;
-        float* dst = p.dq_acc + ((static_cast<size_t>(it.wi.b) * L + pos) * p.H + it.h0 + hh) * D;
+      const int n = VARLEN ? it.n : p.n;
+      if (q < n) {
+        const size_t pos = static_cast<size_t>(it.lhalf(l)) * n + q;
+        const size_t first = VARLEN ? static_cast<size_t>(it.row0) : it.wi.b * L;
+        float* dst = p.dq_acc + ((first + pos) * p.H + it.h0 + hh) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 4)
           red_add_v4_f32(dst + c, __uint_as_float(dq[c]) * p.scale,
@@ -558,8 +580,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       const int j = ks + row;  // key inside its half
       // Query rows that see key j, per segment of the item: computed once,
       // so a tile needs no division and no per-tile visibility test.
-      const Interval iv0 = query_interval(it.rule0, j, p.n, p.bs);
-      const Interval iv1 = query_interval(it.rule1, j, p.n, p.bs);
+      const int n = VARLEN ? it.n : p.n;
+      const int bs = VARLEN ? it.bs : p.bs;
+      const Interval iv0 = query_interval(it.rule0, j, n, bs);
+      const Interval iv1 = query_interval(it.rule1, j, n, bs);
       for (int i = ((g & 1) == wg) ? 0 : 1; i < it.ntiles && ok; i += 2) {
         const int gg = g + i;
         const int st = gg % STAGES;
@@ -614,9 +638,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       }
       tc_fence_before();
       mbar_arrive_warp(BAR(C::BAR_ACCFREE));
-      if (j < p.n) {
-        const size_t pos = static_cast<size_t>(it.wi.half) * p.n + j;
-        const size_t off = ((static_cast<size_t>(it.wi.b) * L + pos) * p.Hk + it.wi.h) * D;
+      if (j < n) {
+        const size_t pos = static_cast<size_t>(it.wi.half) * n + j;
+        const size_t first = VARLEN ? static_cast<size_t>(it.row0) : it.wi.b * L;
+        const size_t off = ((first + pos) * p.Hk + it.wi.h) * D;
         __nv_bfloat16* dst = (wg == 0 ? p.dv : p.dk) + off;
         const float mul = wg == 0 ? 1.f : p.scale;
 #pragma unroll
@@ -647,14 +672,14 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int BMQ, bool GQA>
+template <int D, int BMQ, bool GQA, bool VARLEN>
 static cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D, BMQ>;
-  auto kern = dfa_bwd_kernel<D, BMQ, GQA>;
+  auto kern = dfa_bwd_kernel<D, BMQ, GQA, VARLEN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long items = 2LL * p.B * p.Hk * p.k_tiles;
+  const long long items = VARLEN ? p.units : 2LL * p.B * p.Hk * p.k_tiles;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -672,8 +697,9 @@ cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream
   switch (headdim) {
     // grouped key/value heads have their own instantiation
     case 64:
-      return p.kv_group > 1 ? launch_bwd_impl<64, 128, true>(p, stream)
-                            : launch_bwd_impl<64, 128, false>(p, stream);
+      if (p.vl) return launch_bwd_impl<64, 128, true, true>(p, stream);
+      return p.kv_group > 1 ? launch_bwd_impl<64, 128, true, false>(p, stream)
+                            : launch_bwd_impl<64, 128, false, false>(p, stream);
     case 128: return launch_backward_d128(p, stream);
     case 256: return launch_backward_d256(p, stream);
     default: return cudaErrorInvalidValue;

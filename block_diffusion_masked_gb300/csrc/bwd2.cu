@@ -112,7 +112,7 @@ struct Bwd2Cfg {
     NUM_BARS = BAR_ALL + 1
   };
   static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 decoded items (Bwd2Item)
-  static constexpr int kOffTmemSlot = kOffItem + 4 * 64;
+  static constexpr int kOffTmemSlot = kOffItem + 4 * 128;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
   static constexpr int kTmemS = 0;
@@ -141,6 +141,7 @@ struct Bwd2Item {
   int n0, nth, ntiles;  // tiles of segment 0, per query head, in all
   int h0;               // first query head of the group
   int half0, rule0, tb0, half1, rule1, tb1;
+  int n, bs, row0;  // half length, block size (clamped) and, varlen, first row
   // Tile t is local tile l of query head h0 + hh.  Without grouping
   // (GQA false: one query head per key/value head) l = t and hh = 0.
   template <bool GQA>
@@ -158,18 +159,31 @@ struct Bwd2Item {
   __device__ __forceinline__ int lhalf(int l) const { return l < n0 ? half0 : half1; }
 };
 
-static_assert(sizeof(Bwd2Item) <= 64, "item ring slot");
+static_assert(sizeof(Bwd2Item) <= 128, "item ring slot");
 
-template <int NDH, int BMQ, int BN, bool GQA>
+template <int NDH, int BMQ, int BN, bool GQA, bool VARLEN>
 __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   Bwd2Item it;
   it.v = v;
   if (v < 0) return it;
   it.dh = v % NDH;
-  it.wi = bwd_work(v / NDH, p.mode, p.B, p.Hk, p.k_tiles, p.group);
+  if constexpr (VARLEN) {
+    const int u = v / NDH;
+    const VarlenSlot sl = p.vl[varlen_slot(p.vl, p.vl_slots, u)];
+    it.wi = bwd_work(u - sl.off, MODE_DIFFUSION, 1, p.Hk, cdiv(sl.n, BN), sl.group);
+    it.wi.b = sl.b;
+    it.n = sl.n;
+    it.bs = imin(p.bs, sl.n);
+    it.row0 = sl.row0;
+  } else {
+    it.wi = bwd_work(v / NDH, p.mode, p.B, p.Hk, p.k_tiles, p.group);
+    it.n = p.n;
+    it.bs = p.bs;
+    it.row0 = 0;  // unused: batched rows come from wi.b
+  }
   it.h0 = GQA ? it.wi.h * p.kv_group : it.wi.h;
   Segment seg[2] = {};
-  const int nseg = bwd_segments(p.mode, p.n, p.bs, BMQ, BN, it.wi.half, it.wi.tile, seg);
+  const int nseg = bwd_segments(p.mode, it.n, it.bs, BMQ, BN, it.wi.half, it.wi.tile, seg);
   it.n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
   it.nth = it.n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
   it.ntiles = GQA ? it.nth * p.kv_group : it.nth;
@@ -182,7 +196,7 @@ __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   return it;
 }
 
-template <int D_, int STAGES_, int NWG_, int KVBUF_, bool GQA>
+template <int D_, int STAGES_, int NWG_, int KVBUF_, bool GQA, bool VARLEN>
 __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 1)
     dfa_bwd2_kernel(const __grid_constant__ BwdParams p) {
   using C = Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>;
@@ -200,9 +214,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
   // Slot s of the item ring; written by the producer before it arrives on
   // ITEMFULL[s] (release), read by the other roles after their wait (acquire).
-  auto ring = [&](int s) { return reinterpret_cast<Bwd2Item*>(smem + C::kOffItem + 64 * s); };
+  auto ring = [&](int s) { return reinterpret_cast<Bwd2Item*>(smem + C::kOffItem + 128 * s); };
   const AbortFlag ab{abort_flag, p.status};
-  const size_t L = 2 * static_cast<size_t>(p.n);
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
 
   if (threadIdx.x == 0) {
@@ -267,16 +280,22 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       const int qt = it.ltile(l);
       const int half = it.lhalf(l);
       const int h = it.h0 + hh;  // query head
-      const float* del_bh = p.delta + (static_cast<size_t>(it.wi.b) * p.H + h) * L;
+      // delta (and, varlen, lse): (batch, heads, 2n) or, varlen, (heads, rows)
+      const size_t L = 2 * static_cast<size_t>(p.n);
+      const float* del_bh = VARLEN ? p.delta + static_cast<size_t>(h) * p.rows + it.row0
+                                   : p.delta + (static_cast<size_t>(it.wi.b) * p.H + h) * L;
       float lse_r[2], del_r[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int q = qt * BMQ + lane + 32 * e;
-        const bool valid = q < p.n;
-        lse_r[e] = valid ? p.lse[lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n)] *
-                               -1.4426950408889634f
-                         : -INFINITY;
-        del_r[e] = valid ? -del_bh[static_cast<size_t>(half) * p.n + q] : 0.f;
+        const bool valid = q < it.n;
+        const size_t pos = static_cast<size_t>(half) * it.n + q;
+        const float lse =
+            !valid  ? 0.f
+            : VARLEN ? p.lse[static_cast<size_t>(h) * p.rows + it.row0 + pos]
+                     : p.lse[lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n)];
+        lse_r[e] = valid ? lse * -1.4426950408889634f : -INFINITY;
+        del_r[e] = valid ? -del_bh[pos] : 0.f;
       }
       const int st = gg % STAGES;
       const int round = gg / STAGES;
@@ -295,12 +314,13 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(BAR(C::BAR_QFULL + st), 2 * C::kQBytes);
+        const HalfRows qr = half_rows<VARLEN>(it.wi.b, half, it.n, it.row0);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           tma_load_5d(sbase + C::kOffQ + st * C::kQBytes + c * BMQ * 128, &p.tm_q,
-                      BAR(C::BAR_QFULL + st), 64 * c, h, qt * BMQ, half, it.wi.b);
+                      BAR(C::BAR_QFULL + st), 64 * c, h, qr.base + qt * BMQ, qr.c3, qr.c4);
           tma_load_5d(sbase + C::kOffDO + st * C::kQBytes + c * BMQ * 128, &p.tm_do,
-                      BAR(C::BAR_QFULL + st), 64 * c, h, qt * BMQ, half, it.wi.b);
+                      BAR(C::BAR_QFULL + st), 64 * c, h, qr.base + qt * BMQ, qr.c3, qr.c4);
         }
       }
       __syncwarp();
@@ -311,7 +331,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       int v = -1;
       if (lane == 0) v = sched_next(p.sched, p.items);
       v = __shfl_sync(0xffffffffu, v, 0);
-      const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN, GQA>(p, v);
+      const Bwd2Item it = bwd2_item<C::NDH, BMQ, BN, GQA, VARLEN>(p, v);
       if (lane == 0) {
         *ring(k & 3) = it;
         mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
@@ -332,15 +352,16 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
       }
       if (lane == 0) {
-        const int ks = it.wi.tile * BN;
+        const HalfRows kr = half_rows<VARLEN>(it.wi.b, it.wi.half, it.n, it.row0);
+        const int krow = kr.base + it.wi.tile * BN;
         const uint32_t full = BAR(C::BAR_KVFULL + kvs);
         mbar_arrive_expect_tx(full, 2 * C::kKVBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           tma_load_5d(sbase + C::kOffK + kvs * C::kKVBytes + c * BN * 128, &p.tm_k, full, 64 * c,
-                      it.wi.h, ks, it.wi.half, it.wi.b);
+                      it.wi.h, krow, kr.c3, kr.c4);
           tma_load_5d(sbase + C::kOffV + kvs * C::kKVBytes + c * BN * 128, &p.tm_v, full, 64 * c,
-                      it.wi.h, ks, it.wi.half, it.wi.b);
+                      it.wi.h, krow, kr.c3, kr.c4);
         }
       }
       __syncwarp();
@@ -505,24 +526,30 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           st_shared_f32(stg + c * 128 + lane * 4, __uint_as_float(dq[c]) * p.scale);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && qs + c0 < p.n) {
-          tma_reduce_add_5d(&p.tm_dq, stg, it.dh * DH + 32 * (warp & 3), h, qs + c0, qh,
-                            it.wi.b);
+        if (lane == 0 && qs + c0 < (VARLEN ? it.n : p.n)) {
+          // Varlen: rows of the box past the half hold exact zeros (no query
+          // row there sees a key), added to the next rows of the packed
+          // accumulator.
+          const HalfRows dr = half_rows<VARLEN>(it.wi.b, qh, it.n, it.row0);
+          tma_reduce_add_5d(&p.tm_dq, stg, it.dh * DH + 32 * (warp & 3), h, dr.base + qs + c0,
+                            dr.c3, dr.c4);
           bulk_commit_group();
         }
         return true;
       }
-      float* ptr = p.dq_acc +
-                   ((static_cast<size_t>(it.wi.b) * L + static_cast<size_t>(qh) * p.n + qs + c0) *
-                        p.H + h) * D + it.dh * DH + row;
-      if (qs + c0 + HC <= p.n) {
+      const int n = VARLEN ? it.n : p.n;
+      const size_t first = VARLEN ? static_cast<size_t>(it.row0)
+                                  : static_cast<size_t>(it.wi.b) * 2 * static_cast<size_t>(p.n);
+      float* ptr = p.dq_acc + ((first + static_cast<size_t>(qh) * n + qs + c0) * p.H + h) * D +
+                   it.dh * DH + row;
+      if (qs + c0 + HC <= n) {
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
           red_add_f32(ptr, __uint_as_float(dq[c]) * p.scale);
           ptr += dq_stride;
         }
       } else {
-        const int qmax = p.n - qs - c0;
+        const int qmax = n - qs - c0;
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
           if (c < qmax) red_add_f32(ptr, __uint_as_float(dq[c]) * p.scale);
@@ -542,8 +569,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       // Query rows that see key j, per segment of the item: computed once,
       // so a tile needs no division and no per-tile visibility test (a tile
       // the mask does not cut gives the full column mask below).
-      const Interval iv0 = query_interval(it.rule0, j, p.n, p.bs);
-      const Interval iv1 = query_interval(it.rule1, j, p.n, p.bs);
+      const int n = VARLEN ? it.n : p.n;
+      const int bs = VARLEN ? it.bs : p.bs;
+      const Interval iv0 = query_interval(it.rule0, j, n, bs);
+      const Interval iv1 = query_interval(it.rule1, j, n, bs);
       // dQ of tile t: query head, half and first row
       auto drain_tile = [&](int t) -> bool {
         int hh, l;
@@ -660,10 +689,11 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       }
       tc_fence_before();
       mbar_arrive_warp(BAR(C::BAR_ACCFREE));
-      if (j < p.n) {
-        const size_t pos = static_cast<size_t>(it.wi.half) * p.n + j;
-        const size_t off =
-            ((static_cast<size_t>(it.wi.b) * L + pos) * p.Hk + it.wi.h) * D + it.dh * DH + d0;
+      if (j < n) {
+        const size_t pos = static_cast<size_t>(it.wi.half) * n + j;
+        const size_t first = VARLEN ? static_cast<size_t>(it.row0)
+                                    : static_cast<size_t>(it.wi.b) * 2 * static_cast<size_t>(p.n);
+        const size_t off = ((first + pos) * p.Hk + it.wi.h) * D + it.dh * DH + d0;
         __nv_bfloat16* dst = (is_v ? p.dv : p.dk) + off;
         const float mul = is_v ? 1.f : p.scale;
 #pragma unroll
@@ -698,10 +728,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int STAGES, int NWG, int KVBUF, bool GQA>
+template <int D, int STAGES, int NWG, int KVBUF, bool GQA, bool VARLEN>
 static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
   using C = Bwd2Cfg<D, STAGES, NWG, KVBUF>;
-  auto kern = dfa_bwd2_kernel<D, STAGES, NWG, KVBUF, GQA>;
+  auto kern = dfa_bwd2_kernel<D, STAGES, NWG, KVBUF, GQA, VARLEN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -711,7 +741,8 @@ static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
   if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
   if (fa.numRegs * C::kThreads < C::kRegCtl * 128 + C::kRegCompute * 128 * C::NWG)
     return cudaErrorInvalidConfiguration;
-  const long long items = 2LL * p.B * p.Hk * p.k_tiles * C::NDH;
+  const long long items =
+      (VARLEN ? static_cast<long long>(p.units) : 2LL * p.B * p.Hk * p.k_tiles) * C::NDH;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -728,13 +759,16 @@ static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
 cudaError_t launch_backward_d128(const BwdParams& p, cudaStream_t stream) {
   // Grouped key/value heads get their own instantiation, so that the
   // multi-head kernel keeps its tile loop free of head bookkeeping.
-  return p.kv_group > 1 ? launch_bwd2_impl<128, 3, kBwd2WarpgroupsD128, 1, true>(p, stream)
-                        : launch_bwd2_impl<128, 3, kBwd2WarpgroupsD128, 1, false>(p, stream);
+  constexpr int W = kBwd2WarpgroupsD128;
+  if (p.vl) return launch_bwd2_impl<128, 3, W, 1, true, true>(p, stream);
+  return p.kv_group > 1 ? launch_bwd2_impl<128, 3, W, 1, true, false>(p, stream)
+                        : launch_bwd2_impl<128, 3, W, 1, false, false>(p, stream);
 }
 
 cudaError_t launch_backward_d256(const BwdParams& p, cudaStream_t stream) {
-  return p.kv_group > 1 ? launch_bwd2_impl<256, 1, 2, 1, true>(p, stream)
-                        : launch_bwd2_impl<256, 1, 2, 1, false>(p, stream);
+  if (p.vl) return launch_bwd2_impl<256, 1, 2, 1, true, true>(p, stream);
+  return p.kv_group > 1 ? launch_bwd2_impl<256, 1, 2, 1, true, false>(p, stream)
+                        : launch_bwd2_impl<256, 1, 2, 1, false, false>(p, stream);
 }
 
 }  // namespace dfa

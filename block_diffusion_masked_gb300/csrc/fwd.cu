@@ -65,7 +65,7 @@ struct FwdCfg {
   static_assert(BN % 64 == 0 && D % 64 == 0, "tile shape");
 };
 
-template <int D, int BN, int STAGES>
+template <int D, int BN, int STAGES, bool VARLEN>
 __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D, BN, STAGES>;
   constexpr int BM = C::BM;
@@ -79,13 +79,29 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
   const AbortFlag ab{abort_flag, p.status};
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
 
-  const WorkItem wi = fwd_work(blockIdx.x, p.mode, p.B, p.H, p.q_tiles, p.group);
+  // The CTA's item.  A varlen item is decoded from the slot table, which
+  // may only be read after grid_dependency_wait below.
+  WorkItem wi;
   Segment seg[2];
-  const int nseg = fwd_segments(p.mode, p.n, p.bs, BM, BN, wi.half, wi.tile, seg);
-  const int n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
-  const int ntiles = n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
-  const int qs = wi.tile * BM;
-  const int hk = wi.h / p.kv_group;  // key/value head
+  int n = p.n, bs = p.bs, row0 = 0, n0 = 0, ntiles = 0, qs = 0, hk = 0;
+  auto decode = [&]() {
+    if constexpr (VARLEN) {
+      const VarlenSlot sl = p.vl[varlen_slot(p.vl, p.vl_slots, blockIdx.x)];
+      n = sl.n;
+      bs = imin(p.bs, n);
+      row0 = sl.row0;
+      wi = fwd_work(blockIdx.x - sl.off, MODE_DIFFUSION, 1, p.H, cdiv(n, BM), sl.group);
+      wi.b = sl.b;
+    } else {
+      wi = fwd_work(blockIdx.x, p.mode, p.B, p.H, p.q_tiles, p.group);
+    }
+    const int nseg = fwd_segments(p.mode, n, bs, BM, BN, wi.half, wi.tile, seg);
+    n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
+    ntiles = n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
+    qs = wi.tile * BM;
+    hk = wi.h / p.kv_group;  // key/value head
+  };
+  if constexpr (!VARLEN) decode();
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::BAR_Q), 1);
@@ -116,6 +132,7 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
   // The prologue above touches only shared memory and TMEM; global memory
   // waits for the stream's previous kernel.
   grid_dependency_wait();
+  if constexpr (VARLEN) decode();
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -124,10 +141,11 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       mbar_arrive_expect_tx(BAR(C::BAR_Q), C::kQBytes);
+      const HalfRows qr = half_rows<VARLEN>(wi.b, wi.half, n, row0);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_5d(sbase + C::kOffQ + c * BM * 128, &p.tm_q, BAR(C::BAR_Q), 64 * c, wi.h, qs,
-                    wi.half, wi.b);
+        tma_load_5d(sbase + C::kOffQ + c * BM * 128, &p.tm_q, BAR(C::BAR_Q), 64 * c, wi.h,
+                    qr.base + qs, qr.c3, qr.c4);
       bool ok = true;
       int j = 0;
       for (; j < ntiles && ok; ++j) {
@@ -137,10 +155,11 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
         const int round = j / STAGES;
         if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_KEMPTY + st), (round - 1) & 1, ab))) break;
         mbar_arrive_expect_tx(BAR(C::BAR_KFULL + st), C::kKVBytes);
+        const HalfRows kr = half_rows<VARLEN>(wi.b, seg[s].half, n, row0);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
-                      BAR(C::BAR_KFULL + st), 64 * c, hk, kt * BN, seg[s].half, wi.b);
+                      BAR(C::BAR_KFULL + st), 64 * c, hk, kr.base + kt * BN, kr.c3, kr.c4);
         if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_VEMPTY + st), (round - 1) & 1, ab))) {
           // K of this stage is in flight; account for it while unwinding.
           ++j;
@@ -150,7 +169,7 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
-                      BAR(C::BAR_VFULL + st), 64 * c, hk, kt * BN, seg[s].half, wi.b);
+                      BAR(C::BAR_VFULL + st), 64 * c, hk, kr.base + kt * BN, kr.c3, kr.c4);
       }
       if (!ok) {
         // Unwinding: let the copies already issued land before the CTA exits.
@@ -245,8 +264,8 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
       mbar_arrive(BAR(C::BAR_SFREE + buf));
 
       const int ks = kt * BN;
-      if (!tile_full(seg[s].rule, p.n, p.bs, qs, BM, ks, BN)) {
-        const Interval iv = key_interval(seg[s].rule, r, p.n, p.bs);
+      if (!tile_full(seg[s].rule, n, bs, qs, BM, ks, BN)) {
+        const Interval iv = key_interval(seg[s].rule, r, n, bs);
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           const int key = ks + c;
@@ -307,10 +326,11 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
     if (ok && ntiles > 0) ok = mbar_wait_warp(BAR(C::BAR_PVDONE), (ntiles - 1) & 1, ab);
     tc_fence_after();
     if (ok) {
-      const size_t L = 2 * static_cast<size_t>(p.n);
-      const size_t pos = static_cast<size_t>(wi.half) * p.n + r;
-      __nv_bfloat16* orow = p.out + ((wi.b * L + pos) * p.H + wi.h) * D;
-      const bool valid = r < p.n;
+      const size_t pos = static_cast<size_t>(wi.half) * n + r;
+      const size_t first =
+          VARLEN ? static_cast<size_t>(row0) : wi.b * 2 * static_cast<size_t>(n);
+      __nv_bfloat16* orow = p.out + ((first + pos) * p.H + wi.h) * D;
+      const bool valid = r < n;
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -338,7 +358,10 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
       if (valid) {
         const float lse = l_run > 0.f ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f
                                       : -INFINITY;
-        p.lse[lse_offset(p.mode, wi.b, wi.h, wi.half, r, p.H, p.n)] = lse;
+        if constexpr (VARLEN)
+          p.lse[static_cast<size_t>(wi.h) * p.rows + row0 + pos] = lse;
+        else
+          p.lse[lse_offset(p.mode, wi.b, wi.h, wi.half, r, p.H, p.n)] = lse;
       }
     }
   }
@@ -352,14 +375,14 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
   }
 }
 
-template <int D, int BN, int STAGES>
+template <int D, int BN, int STAGES, bool VARLEN>
 static cudaError_t launch_fwd_impl(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D, BN, STAGES>;
-  auto kern = dfa_fwd_kernel<D, BN, STAGES>;
+  auto kern = dfa_fwd_kernel<D, BN, STAGES, VARLEN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long blocks = 2LL * p.B * p.H * p.q_tiles;
+  const long long blocks = VARLEN ? p.items : 2LL * p.B * p.H * p.q_tiles;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   return launch_chained(kern, dim3(static_cast<unsigned>(blocks)), dim3(C::kThreads),
@@ -370,7 +393,9 @@ cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream)
   switch (headdim) {
     case 64:
     case 128: return launch_forward_two_warpgroups(p, headdim, stream);
-    case 256: return launch_fwd_impl<256, 64, 2>(p, stream);
+    case 256:
+      return p.vl ? launch_fwd_impl<256, 64, 2, true>(p, stream)
+                  : launch_fwd_impl<256, 64, 2, false>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

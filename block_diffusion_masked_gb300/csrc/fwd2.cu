@@ -91,19 +91,32 @@ struct ItemGeom {
   WorkItem wi;
   int n0, ntiles, qs;
   int half0, rule0, tb0, half1, rule1, tb1;
+  int n, row0;  // varlen: the sample's half length and first row
   __device__ __forceinline__ int ktile(int j) const { return j < n0 ? tb0 + j : tb1 + (j - n0); }
   __device__ __forceinline__ int khalf(int j) const { return j < n0 ? half0 : half1; }
 };
 
 static_assert(sizeof(ItemGeom) <= 64, "item ring slot");
 
+template <bool VARLEN>
 __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, int bn,
                                           ItemGeom* g) {
   g->item = item;
   if (item < 0) return;
-  g->wi = fwd_work(item, p.mode, p.B, p.H, p.q_tiles, p.group);
+  int n = p.n, bs = p.bs;
+  if constexpr (VARLEN) {
+    const VarlenSlot sl = p.vl[varlen_slot(p.vl, p.vl_slots, item)];
+    n = sl.n;
+    bs = imin(p.bs, n);
+    g->wi = fwd_work(item - sl.off, MODE_DIFFUSION, 1, p.H, cdiv(n, bm), sl.group);
+    g->wi.b = sl.b;
+    g->n = n;
+    g->row0 = sl.row0;
+  } else {
+    g->wi = fwd_work(item, p.mode, p.B, p.H, p.q_tiles, p.group);
+  }
   Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
-  const int nseg = fwd_segments(p.mode, p.n, p.bs, bm, bn, g->wi.half, g->wi.tile, seg);
+  const int nseg = fwd_segments(p.mode, n, bs, bm, bn, g->wi.half, g->wi.tile, seg);
   g->n0 = nseg > 0 ? seg[0].t_end - seg[0].t_begin : 0;
   g->ntiles = g->n0 + (nseg > 1 ? seg[1].t_end - seg[1].t_begin : 0);
   g->half0 = seg[0].half;
@@ -115,7 +128,7 @@ __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, 
   g->qs = g->wi.tile * bm;
 }
 
-template <int D, int STAGES>
+template <int D, int STAGES, bool VARLEN>
 __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant__ FwdParams p) {
   using C = Fwd2Cfg<D, STAGES>;
   constexpr int BM = C::BM;
@@ -131,7 +144,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   // ITEMFULL[s] (release), read by the other roles after their wait (acquire).
   auto ring = [&](int s) { return reinterpret_cast<ItemGeom*>(smem + C::kOffItem + 64 * s); };
   const AbortFlag ab{abort_flag, p.status};
-  const int num_items = 2 * p.B * p.H * p.q_tiles;
+  const int num_items = VARLEN ? p.items : 2 * p.B * p.H * p.q_tiles;
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
 
   if (threadIdx.x == 0) {
@@ -187,8 +200,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       bool ok = true;
       int g = 0;  // K/V ring position across items
       // The V tile still to be loaded: ring position vg (< 0: none) and its
-      // coordinates.
-      int vg = -1, vh = 0, vb = 0, vkt = 0, vkh = 0;
+      // tensor-map coordinates.
+      int vg = -1, vh = 0, vc2 = 0, vc3 = 0, vc4 = 0;
       auto load_v = [&]() -> bool {
         const int st = vg % STAGES;
         const int round = vg / STAGES;
@@ -197,7 +210,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
-                      BAR(C::BAR_VFULL + st), 64 * c, vh, vkt * BN, vkh, vb);
+                      BAR(C::BAR_VFULL + st), 64 * c, vh, vc2, vc3, vc4);
         vg = -1;
         return true;
       };
@@ -209,17 +222,18 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         // k - 3's out tile, which exists only after every role has read item
         // k - 4's slot.
         ItemGeom ig;
-        item_geom(p, sched_next(p.sched, num_items), BM, BN, &ig);
+        item_geom<VARLEN>(p, sched_next(p.sched, num_items), BM, BN, &ig);
         *ring(k & 3) = ig;
         mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
         if (ig.item < 0) break;
         const int qb = k & 1;
         if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_QEMPTY + qb), ((k >> 1) - 1) & 1, ab))) break;
         mbar_arrive_expect_tx(BAR(C::BAR_QFULL + qb), C::kQBytes);
+        const HalfRows qr = half_rows<VARLEN>(ig.wi.b, ig.wi.half, ig.n, ig.row0);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, &p.tm_q,
-                      BAR(C::BAR_QFULL + qb), 64 * c, ig.wi.h, ig.qs, ig.wi.half, ig.wi.b);
+                      BAR(C::BAR_QFULL + qb), 64 * c, ig.wi.h, qr.base + ig.qs, qr.c3, qr.c4);
         // key/value head of query head wi.h (grouped heads: kv_group > 1)
         const int hk = p.kv_group == 1 ? ig.wi.h : ig.wi.h / p.kv_group;
         for (int j = 0; j < ig.ntiles; ++j, ++g) {
@@ -227,17 +241,18 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
           const int round = g / STAGES;
           if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_KEMPTY + st), (round - 1) & 1, ab))) break;
           mbar_arrive_expect_tx(BAR(C::BAR_KFULL + st), C::kKVBytes);
+          const HalfRows kr = half_rows<VARLEN>(ig.wi.b, ig.khalf(j), ig.n, ig.row0);
+          const int krow = kr.base + ig.ktile(j) * BN;
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
-                        BAR(C::BAR_KFULL + st), 64 * c, hk, ig.ktile(j) * BN, ig.khalf(j),
-                        ig.wi.b);
+                        BAR(C::BAR_KFULL + st), 64 * c, hk, krow, kr.c3, kr.c4);
           if (vg >= 0 && !(ok = load_v())) break;
           vg = g;
           vh = hk;
-          vb = ig.wi.b;
-          vkt = ig.ktile(j);
-          vkh = ig.khalf(j);
+          vc2 = krow;
+          vc3 = kr.c3;
+          vc4 = kr.c4;
         }
       }
       if (ok && vg >= 0) ok = load_v();
@@ -341,14 +356,37 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       const ItemGeom ig = *ring(k & 3);
       if (ig.item < 0) break;
       if (!(ok = mbar_wait_warp(BAR(C::BAR_OSTAGED + qb), (k >> 1) & 1, ab))) break;
-      if (lane == 0) {
+      const uint32_t stage = sbase + C::kOffQ + qb * C::kQBytes;
+      const HalfRows orr = half_rows<VARLEN>(ig.wi.b, ig.wi.half, ig.n, ig.row0);
+      if (!VARLEN || ig.qs + BM <= ig.n) {
+        if (lane == 0) {
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_store_5d(&p.tm_o, sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, 64 * c,
-                       ig.wi.h, ig.qs, ig.wi.half, ig.wi.b);
-        bulk_commit_group();
-        bulk_wait_read_all();
-        mbar_arrive(BAR(C::BAR_QEMPTY + qb));
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_store_5d(&p.tm_o, stage + c * BM * 128, 64 * c, ig.wi.h, orr.base + ig.qs, orr.c3,
+                         orr.c4);
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(BAR(C::BAR_QEMPTY + qb));
+        }
+      } else {
+        // Varlen, last tile of a half: a box store would run into the next
+        // rows of the packed tensor, so the warp copies the half's rows out
+        // of the staged (swizzled) tile with 16-byte stores.
+        constexpr int kUnits = D / 8;  // 16-byte units per row
+        const int rows = ig.n - ig.qs;
+        __nv_bfloat16* dst0 = p.out + (static_cast<size_t>(orr.base + ig.qs) * p.H + ig.wi.h) * D;
+        for (int idx = lane; idx < rows * kUnits; idx += 32) {
+          const int r = idx / kUnits;
+          const int u = idx - r * kUnits;
+          uint32_t w0, w1, w2, w3;
+          ld_shared_v4(stage + (u >> 3) * (BM * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4), w0,
+                       w1, w2, w3);
+          st_global_v4(dst0 + static_cast<size_t>(r) * p.H * D + 8 * u, w0, w1, w2, w3);
+        }
+        // The producer's next TMA load into this buffer follows these reads.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C::BAR_QEMPTY + qb));
       }
       __syncwarp();
       if (p.zero_dst != nullptr) {
@@ -372,10 +410,9 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     const uint32_t o_col = t_lane + C::kTmemO + w * D;
     const float sl2 = p.scale_log2;
     // ---------------------------------------------------------- merge
-    // Item kk (sample b, head h, half, query tile at qs) ends: the two
+    // Item kk (ig: sample, head, half; query tile at qs) ends: the two
     // warpgroups' partial states are combined with the online-softmax rule.
-    auto merge = [&](int kk, int b, int h, int half, int qs, float m_ref,
-                     float l_run) -> bool {
+    auto merge = [&](int kk, const ItemGeom& ig, int qs, float m_ref, float l_run) -> bool {
       float2* ml = reinterpret_cast<float2*>(smem + C::kOffML) + (kk & 1) * 2 * BM;
       ml[w * BM + row] = make_float2(m_ref, l_run);
       mbar_arrive(BAR(C::BAR_XCHG));
@@ -428,9 +465,12 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       }
       fence_proxy_async_smem();
       mbar_arrive(BAR(C::BAR_OSTAGED + (kk & 1)));
-      if (r < p.n && w == 0) {
+      if (r < (VARLEN ? ig.n : p.n) && w == 0) {
         const float lse = lsum > 0.f ? (m + lg2_approx(lsum)) * 0.69314718055994531f : -INFINITY;
-        p.lse[lse_offset(p.mode, b, h, half, r, p.H, p.n)] = lse;
+        if constexpr (VARLEN)
+          p.lse[static_cast<size_t>(ig.wi.h) * p.rows + ig.row0 + ig.wi.half * ig.n + r] = lse;
+        else
+          p.lse[lse_offset(p.mode, ig.wi.b, ig.wi.h, ig.wi.half, r, p.H, p.n)] = lse;
       }
       tc_fence_before();
       mbar_arrive(BAR(C::BAR_OFREE));
@@ -447,8 +487,10 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       const int r = qs + row;  // row inside the half
       // Keys visible to row r, per segment of the item: computed once, so a
       // tile needs no division (rows past the end of the half see nothing).
-      const Interval kv0 = key_interval(ig.rule0, r, p.n, p.bs);
-      const Interval kv1 = key_interval(ig.rule1, r, p.n, p.bs);
+      const int n = VARLEN ? ig.n : p.n;
+      const int bs = VARLEN ? imin(p.bs, n) : p.bs;
+      const Interval kv0 = key_interval(ig.rule0, r, n, bs);
+      const Interval kv1 = key_interval(ig.rule1, r, n, bs);
       float m_ref = -INFINITY;  // reference maximum, scaled log2 units
       float l_run = 0.f;        // running sum of 2^(s * sl2 - m_ref)
       for (int j = w; j < ig.ntiles; j += 2, ++cnt) {
@@ -543,7 +585,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         mbar_arrive(BAR(C::BAR_PFULL + w));
       }
       if (!ok) break;
-      ok = merge(k, ig.wi.b, ig.wi.h, ig.wi.half, qs, m_ref, l_run);
+      ok = merge(k, ig, qs, m_ref, l_run);
     }
   }
 #undef BAR
@@ -559,14 +601,14 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int STAGES>
+template <int D, int STAGES, bool VARLEN>
 static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
   using C = Fwd2Cfg<D, STAGES>;
-  auto kern = dfa_fwd2_kernel<D, STAGES>;
+  auto kern = dfa_fwd2_kernel<D, STAGES, VARLEN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long items = 2LL * p.B * p.H * p.q_tiles;
+  const long long items = VARLEN ? p.items : 2LL * p.B * p.H * p.q_tiles;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -580,8 +622,12 @@ static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_forward_two_warpgroups(const FwdParams& p, int headdim, cudaStream_t stream) {
   switch (headdim) {
-    case 64: return launch_fwd2_impl<64, 4>(p, stream);
-    case 128: return launch_fwd2_impl<128, 2>(p, stream);
+    case 64:
+      return p.vl ? launch_fwd2_impl<64, 4, true>(p, stream)
+                  : launch_fwd2_impl<64, 4, false>(p, stream);
+    case 128:
+      return p.vl ? launch_fwd2_impl<128, 2, true>(p, stream)
+                  : launch_fwd2_impl<128, 2, false>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -12,9 +12,26 @@ namespace dfa {
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusIndex = 2u;
 
-// Forward kernel parameters.  Tensor maps view q/k/v as 5-D arrays
+// Packed batches of samples of different lengths ("Fast Diffusion
+// Attention": varlen batches, scheduled longest first).  Sample b occupies
+// rows [row0, row0 + 2n) of the packed (rows, heads, headdim) tensors, its
+// noisy half first.  The host lists the non-empty samples longest first, one
+// slot each; `off` counts the work units of the slots before it (units: the
+// items of a pass without the backward's head-dim split).
+struct VarlenSlot {
+  int b;      // sample index (order of the packed tensors)
+  int n;      // length of each half
+  int row0;   // first row of the sample
+  int group;  // heads per L2 scheduling group inside the sample
+  int off;    // first work unit of the slot
+};
+
+// Forward kernel parameters.  Batched: tensor maps view q/k/v as 5-D arrays
 // (headdim, heads, n, half, batch) so that a tile never crosses the
 // noisy/clean boundary and rows past the end of a half read as zeros.
+// Varlen: the same 5-D maps with dims (headdim, heads, rows, 1, 1); rows past
+// the end of a half are the next rows of the packed tensor (finite data the
+// mask hides; only rows past the last sample read as zeros).
 struct FwdParams {
   CUtensorMap tm_q;  // box (64, 1, block_m, 1, 1)
   CUtensorMap tm_k;  // box (64, 1, block_n, 1, 1)
@@ -33,6 +50,13 @@ struct FwdParams {
   // launch alongside its tensor-core work (zero_groups 16-byte groups).
   float4* zero_dst;
   long long zero_groups;
+  // Varlen only (vl == nullptr for a batched launch): the slot table, its
+  // length, the rows of the packed tensors (lse is (heads, rows)) and the
+  // work units of the launch.
+  const VarlenSlot* vl;
+  int vl_slots;
+  int rows;
+  int items;
 };
 
 struct BwdParams {
@@ -56,6 +80,12 @@ struct BwdParams {
   float scale_log2;   // scale * log2(e)
   unsigned* sched;    // work counter of a persistent launch (see sched_next)
   int items;          // work items of the launch
+  // Varlen only (vl == nullptr for a batched launch): the slot table, its
+  // length and the rows of the packed tensors (lse, delta are (heads, rows)).
+  const VarlenSlot* vl;
+  int vl_slots;
+  int rows;
+  int units;          // work units (items without the head-dim split)
 };
 
 #if defined(__CUDACC__)
@@ -67,6 +97,30 @@ __device__ __forceinline__ int sched_next(unsigned* sched, int items) {
   const unsigned w = atomicAdd(sched, 1u);
   return w < static_cast<unsigned>(items) ? static_cast<int>(w) : -1;
 }
+// Slot of work unit u of a varlen launch: the last slot whose first unit is
+// at most u (binary search over the slots' `off`, ascending).
+__device__ __forceinline__ int varlen_slot(const VarlenSlot* vl, int slots, int u) {
+  int lo = 0, hi = slots - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (vl[mid].off <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Tensor-map coordinates (c2, c3, c4) of row `base + r` of one half: batched
+// maps are (headdim, heads, n, half, batch), varlen maps
+// (headdim, heads, rows, 1, 1).
+struct HalfRows {
+  int base, c3, c4;
+};
+template <bool VARLEN>
+__device__ __forceinline__ HalfRows half_rows(int b, int half, int n, int row0) {
+  if constexpr (VARLEN) return {row0 + half * n, 0, 0};
+  else return {0, half, b};
+}
+
 // One thread per CTA, after the CTA's last sched_next.
 __device__ __forceinline__ void sched_finish(unsigned* sched) {
   __threadfence();

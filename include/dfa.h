@@ -121,6 +121,34 @@ int dfa_backward_gqa(const void *q, const void *k, const void *v, const void *ou
                      dfa_stream_t stream);
 
 /*
+ * Packed batches of samples of different lengths ("Fast Diffusion
+ * Attention": varlen batches, the second API, modeled on FlashAttention's
+ * varlen call).  cu_seqlens is a HOST array of batch + 1 int32 prefix sums
+ * (cu_seqlens[0] == 0, non-decreasing): sample b is rows
+ * [cu_seqlens[b], cu_seqlens[b+1]) of the packed tensors, [noisy | clean],
+ * so its length 2 n_b must be even; zero-length samples are allowed.
+ * rows = cu_seqlens[batch] <= 2^30.  Layouts: q, out, dout, dq are
+ * (rows, heads, headdim) bf16, k, v, dk, dv (rows, kv_heads, headdim) bf16
+ * (kv_heads divides heads, as for dfa_forward_gqa), lse (heads, rows)
+ * float32.  block_size applies to every sample (clamped to each n_b).  The
+ * non-empty samples run in one launch per pass, longest first.  A tile may
+ * read rows of the next sample, which the mask hides: the inputs must be
+ * finite everywhere in the packed tensors.  The schedule (20 bytes per
+ * sample) is copied to stream-ordered device memory on `stream`
+ * (cudaMallocAsync, cudaMemcpyAsync from the host array, cudaFreeAsync);
+ * dfa_backward_varlen also takes the scratch of dfa_backward.  Errors:
+ * DFA_EINVAL for a bad cu_seqlens (odd or negative length, cu_seqlens[0] !=
+ * 0, NULL) or head counts, otherwise as dfa_forward / dfa_backward.
+ */
+int dfa_forward_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                       const int *cu_seqlens, int batch, int heads, int kv_heads, int headdim,
+                       int block_size, dfa_stream_t stream);
+int dfa_backward_varlen(const void *q, const void *k, const void *v, const void *out,
+                        const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                        const int *cu_seqlens, int batch, int heads, int kv_heads,
+                        int headdim, int block_size, dfa_stream_t stream);
+
+/*
  * The yardstick of "Fast Diffusion Attention", section "The right yardstick":
  * causal attention on `batch` independent sequences of length `seqlen`, same
  * layout (batch, seqlen, heads, headdim), lse (batch, heads, seqlen), run by

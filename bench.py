@@ -460,6 +460,97 @@ def run_reference(args, w, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+# Half lengths of the packed varlen batch: a mix of sample lengths with the
+# rows of the workload it stands beside (8 x 2048 rows for "small").
+VARLEN_HALVES = (1536, 1280, 1152, 1024, 1024, 896, 768, 512)
+
+
+def run_variant(args, w):
+    """Time the one-call API on a grouped-head or packed version of `w`.
+
+    gqa: k and v with heads // 4 heads; varlen: the samples of VARLEN_HALVES
+    (scaled to the workload's rows) packed along the rows.  One step is the
+    forward and the backward (scratch, preprocess, main, dq convert) through
+    dfa_forward_gqa / dfa_backward_gqa or dfa_forward_varlen /
+    dfa_backward_varlen; FLOPs count the visible pairs of every sample.
+    """
+    import torch
+
+    from block_diffusion_masked_gb300 import binding
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    binding.lib()
+    stream = torch.cuda.current_stream(dev)
+    H, d, bs = w.heads, w.headdim, w.block_size
+    if args.variant == "gqa":
+        Hk = max(1, H // 4)
+        q, _, _, do = inputs.make_workload_inputs(w)
+        _, k, v = inputs.make_inputs(w.batch, w.n, Hk, d, seed=w.seed + 1, with_dout=False)
+        q, k, v, do = (t.to(dev) for t in (q, k, v, do))
+        halves = [w.n] * w.batch
+        fwd = lambda: binding.dfa_forward_gqa(q, k, v, bs)  # noqa: E731
+        bwd = lambda o, l: binding.dfa_backward_gqa(q, k, v, o, do, l, bs)  # noqa: E731
+        shape = {"batch": w.batch, "n": w.n, "heads": H, "kv_heads": Hk}
+    else:
+        scale = w.batch * w.n / sum(VARLEN_HALVES)
+        halves = [max(1, int(round(h * scale))) for h in VARLEN_HALVES]
+        rows = 2 * sum(halves)
+        q, k, v, do = (t[0].to(dev) for t in inputs.make_inputs(1, rows // 2, H, d, seed=w.seed))
+        cu = np.concatenate([[0], np.cumsum([2 * h for h in halves])]).astype(int).tolist()
+        fwd = lambda: binding.dfa_forward_varlen(q, k, v, cu, bs)  # noqa: E731
+        bwd = lambda o, l: binding.dfa_backward_varlen(q, k, v, o, do, l, cu, bs)  # noqa: E731
+        shape = {"halves": halves, "rows": rows, "heads": H}
+    pairs = sum(visible_pairs_per_sample(n, bs) for n in halves)
+    f_fwd = 4.0 * pairs * d * H
+    f_bwd = 2.5 * f_fwd
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        o, l = fwd()
+        if ev is not None:
+            ev[1].record(stream)
+        bwd(o, l)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(end) / args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize(dev)
+    if binding.dfa_status() != 0:
+        raise RuntimeError("device status set during the timed region")
+    split = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in evs]).mean(0)
+    return {
+        "metric": "visible-pair TFLOPS fwd+bwd on 1 GB300 (one-call API, " + args.variant + ")",
+        "variant": args.variant,
+        "value": (f_fwd + f_bwd) / (ms * 1e-3) / 1e12,
+        "unit": "TFLOPS",
+        "ms_per_step": ms,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "fwd_tflops": f_fwd / (split[0] * 1e-3) / 1e12,
+        "bwd_tflops": f_bwd / (split[1] * 1e-3) / 1e12,
+        "kernel_ms": {"fwd": float(split[0]), "bwd": float(split[1])},
+        "dtype": "bf16",
+        "data": "synthetic: i.i.d. N(0,1) bf16 from a seeded CPU generator",
+        "config": dict({"workload": w.name, "headdim": d, "block_size": bs}, **shape),
+        "clocks": clk.summary(),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -471,6 +562,8 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sdpa", action="store_true", help="also time torch SDPA causal (context)")
+    ap.add_argument("--variant", default="mha", choices=["mha", "gqa", "varlen"],
+                    help="gqa / varlen: time the one-call API on that version of the workload")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -481,6 +574,11 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, w, rank, world)), flush=True)
+        return
+
+    if args.variant != "mha":
+        if rank == 0:
+            print(json.dumps(run_variant(args, w)), flush=True)
         return
 
     if world > 1:

@@ -24,6 +24,7 @@ DFA_EUNSUPPORTED = -2
 DFA_ECUDA = -3
 DFA_ETIMEOUT = -4
 DFA_EDEVICE = -5
+DFA_DETERMINISTIC = 1
 MODE_DIFFUSION = 0
 MODE_CAUSAL = 1
 
@@ -41,6 +42,7 @@ _SIGNATURES = {
     "dfa_backward_gqa": (_I, [_P] * 9 + [_I] * 6 + [_P]),
     "dfa_forward_varlen": (_I, [_P] * 6 + [_I] * 5 + [_P]),
     "dfa_backward_varlen": (_I, [_P] * 10 + [_I] * 5 + [_P]),
+    "dfa_backward_ex": (_I, [_P] * 10 + [_I] * 7 + [_P]),
     "dfa_causal_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "dfa_causal_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _P]),
     "dfa_status": (_I, [_P]),
@@ -259,6 +261,40 @@ def dfa_backward_varlen(q, k, v, out, dout, lse, cu_seqlens, block_size, dq=None
                                        _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), cu, batch, H, Hk,
                                        d, int(block_size), _stream_ptr(q))
     _check("dfa_backward_varlen", rc)
+    return dq, dk, dv
+
+
+def dfa_backward_ex(q, k, v, out, dout, lse, block_size, cu_seqlens=None, deterministic=False,
+                    dq=None, dk=None, dv=None):
+    """Backward with options: batched (q 4-D) or packed (q 3-D, ``cu_seqlens``).
+
+    ``deterministic``: dQ contributions are added in a fixed order, so the
+    results are bitwise reproducible.
+    """
+    if cu_seqlens is None:
+        Hk = _check_grouped(q, k, v, out, dout)
+        B, L, H, d = q.shape
+        if lse.shape != (B, H, L):
+            raise ValueError("lse must be (B, H, 2n)")
+        cu, batch, n = None, B, L // 2
+    else:
+        Hk = _check_packed(q, k, v, out, dout)
+        rows, H, d = q.shape
+        if lse.shape != (H, rows):
+            raise ValueError("lse must be (heads, rows)")
+        cu, batch = _cu_array(cu_seqlens, rows)
+        n = 0
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    flags = DFA_DETERMINISTIC if deterministic else 0
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_backward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), cu, batch, n, H, Hk, d,
+                                   int(block_size), flags, _stream_ptr(q))
+    _check("dfa_backward_ex", rc)
     return dq, dk, dv
 
 

@@ -221,7 +221,8 @@ bool aligned_all(std::initializer_list<const void*> ps) {
 // The tensor-core backward step alone: caller-owned delta and dq_acc.
 int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const void* dout,
                   const float* lse, const float* delta, float* dq_acc, void* dk, void* dv, int B,
-                  int n, int H, int Hk, int d, int bs, cudaStream_t stream) {
+                  int n, int H, int Hk, int d, int bs, cudaStream_t stream,
+                  unsigned* dq_sem = nullptr) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
   const int G = kv_group_of(H, Hk);
@@ -261,6 +262,8 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   p.group = l2_group((4LL + 8LL * G) * 2 * n * d, ds->l2_bytes, B * Hk);
   p.sched = sched_for_stream(ds, stream);
   p.items = 0;  // set by the launcher
+  p.dq_sem = dq_sem;
+  p.sem_rows = B * 2 * n;
   p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   const cudaError_t e = launch_backward(p, d, stream);
@@ -297,9 +300,22 @@ int convert_impl(const float* dq_acc, void* dq, int B, int n, int H, int d, cuda
 }
 
 // Full backward: stream-ordered scratch, then the three steps.
+// Counters of the deterministic mode: one per (head-dim part, head, row),
+// zero, stream-ordered.
+int alloc_dq_sem(size_t head_rows, cudaStream_t stream, unsigned** sem) {
+  const size_t bytes = 2 * head_rows * sizeof(unsigned);
+  if (cudaMallocAsync(reinterpret_cast<void**>(sem), bytes, stream) != cudaSuccess)
+    return DFA_ECUDA;
+  if (cudaMemsetAsync(*sem, 0, bytes, stream) != cudaSuccess) {
+    cudaFreeAsync(*sem, stream);
+    return DFA_ECUDA;
+  }
+  return DFA_OK;
+}
+
 int backward_impl(int mode, const void* q, const void* k, const void* v, const void* out,
                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int n,
-                  int H, int Hk, int d, int bs, cudaStream_t stream) {
+                  int H, int Hk, int d, int bs, cudaStream_t stream, bool det = false) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
   if (kv_group_of(H, Hk) == 0) return DFA_EINVAL;
@@ -322,10 +338,18 @@ int backward_impl(int mode, const void* q, const void* k, const void* v, const v
     cudaFreeAsync(dq_acc, stream);
     return DFA_ECUDA;
   }
+  unsigned* sem = nullptr;
+  if (det && (rc = alloc_dq_sem(rows, stream, &sem))) {
+    cudaFreeAsync(delta, stream);
+    cudaFreeAsync(dq_acc, stream);
+    return rc;
+  }
   rc = preprocess_impl(out, dout, delta, dq_acc, B, n, H, d, stream);
   if (!rc)
-    rc = bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, Hk, d, bs, stream);
+    rc = bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, Hk, d, bs, stream,
+                       sem);
   if (!rc) rc = convert_impl(dq_acc, dq, B, n, H, d, stream);
+  if (sem) cudaFreeAsync(sem, stream);
   cudaFreeAsync(delta, stream);
   cudaFreeAsync(dq_acc, stream);
   return rc;
@@ -452,7 +476,7 @@ int forward_varlen_impl(const void* q, const void* k, const void* v, void* out, 
 int backward_varlen_impl(const void* q, const void* k, const void* v, const void* out,
                          const void* dout, const float* lse, void* dq, void* dk, void* dv,
                          const int* cu, int batch, int H, int Hk, int d, int bs,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool det = false) {
   int rc = check_varlen(H, Hk, d, bs);
   if (rc) return rc;
   int rows = 0;
@@ -490,6 +514,13 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
     cudaFreeAsync(dq_acc, stream);
     return rc;
   }
+  unsigned* sem = nullptr;
+  if (det && (rc = alloc_dq_sem(static_cast<size_t>(rows) * H, stream, &sem))) {
+    cudaFreeAsync(dslots, stream);
+    cudaFreeAsync(delta, stream);
+    cudaFreeAsync(dq_acc, stream);
+    return rc;
+  }
   // delta = rowsum(dout * out) as (heads, rows), the layout of lse; dq_acc = 0
   cudaError_t e = launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(out),
                                         static_cast<const __nv_bfloat16*>(dout), delta, dq_acc,
@@ -502,6 +533,7 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
         (rc = make_map(&p.tm_v, v, 1, rows, Hk, d, ts.bwd_bn, true)) ||
         (d == 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, 1, rows, H, d,
                                         ts.bwd_bm / kBwd2WarpgroupsD128, true)))) {
+      if (sem) cudaFreeAsync(sem, stream);
       cudaFreeAsync(dslots, stream);
       cudaFreeAsync(delta, stream);
       cudaFreeAsync(dq_acc, stream);
@@ -529,11 +561,14 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
     p.vl_slots = static_cast<int>(slots.size());
     p.rows = rows;
     p.units = units;
+    p.dq_sem = sem;
+    p.sem_rows = rows;
     e = launch_backward(p, d, stream);
   }
   if (e == cudaSuccess)
     e = launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), static_cast<long long>(elems),
                           stream);
+  if (sem) cudaFreeAsync(sem, stream);
   cudaFreeAsync(dslots, stream);
   cudaFreeAsync(delta, stream);
   cudaFreeAsync(dq_acc, stream);
@@ -607,6 +642,20 @@ int dfa_backward_varlen(const void* q, const void* k, const void* v, const void*
                         int block_size, dfa_stream_t stream) {
   return backward_varlen_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens, batch, heads,
                               kv_heads, headdim, block_size, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_backward_ex(const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                    const int* cu_seqlens, int batch, int n, int heads, int kv_heads, int headdim,
+                    int block_size, int flags, dfa_stream_t stream) {
+  if (flags & ~DFA_DETERMINISTIC) return DFA_EINVAL;
+  const bool det = (flags & DFA_DETERMINISTIC) != 0;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cu_seqlens)
+    return backward_varlen_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens, batch, heads,
+                                kv_heads, headdim, block_size, s, det);
+  return backward_impl(MODE_DIFFUSION, q, k, v, out, dout, lse, dq, dk, dv, batch, n, heads,
+                       kv_heads, headdim, block_size, s, det);
 }
 
 int dfa_causal_forward(const void* q, const void* k, const void* v, void* out, float* lse,

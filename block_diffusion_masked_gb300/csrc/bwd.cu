@@ -162,7 +162,7 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   return it;
 }
 
-template <int D, int BMQ, bool GQA, bool VARLEN>
+template <int D, int BMQ, bool GQA, bool VARLEN, bool DET>
 __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D, BMQ>;
   constexpr int BN = C::BN;
@@ -497,11 +497,22 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       mbar_arrive_warp(BAR(C::BAR_DQFREE + b));
       int hh, l;
       it.template split<GQA>(t, hh, l);
-      const int q = it.ltile(l) * BMQ + row;
+      const int qs = it.ltile(l) * BMQ;
+      const int q = qs + row;
       const int n = VARLEN ? it.n : p.n;
+      const size_t first = VARLEN ? static_cast<size_t>(it.row0) : it.wi.b * L;
+      unsigned* sem = nullptr;
+      if constexpr (DET) {
+        // The 4 warps of this warpgroup add the tile's dQ after the key
+        // tiles the work order takes earlier: wait for them.
+        const int ord = dq_ordinal(p.mode, n, VARLEN ? it.bs : p.bs, BMQ, BN, it.lhalf(l),
+                                   it.ltile(l), it.wi.half, it.wi.tile);
+        sem = p.dq_sem + static_cast<size_t>(it.h0 + hh) * p.sem_rows + first +
+              static_cast<size_t>(it.lhalf(l)) * n + qs;
+        if (!sem_wait_warp(sem, static_cast<unsigned>(4 * ord), ab)) return false;
+      }
       if (q < n) {
         const size_t pos = static_cast<size_t>(it.lhalf(l)) * n + q;
-        const size_t first = VARLEN ? static_cast<size_t>(it.row0) : it.wi.b * L;
         float* dst = p.dq_acc + ((first + pos) * p.H + it.h0 + hh) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 4)
@@ -509,6 +520,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
                          __uint_as_float(dq[c + 1]) * p.scale, __uint_as_float(dq[c + 2]) * p.scale,
                          __uint_as_float(dq[c + 3]) * p.scale);
       }
+      if constexpr (DET) sem_signal_warp(sem);
       return true;
     };
 
@@ -672,10 +684,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int BMQ, bool GQA, bool VARLEN>
+template <int D, int BMQ, bool GQA, bool VARLEN, bool DET = false>
 static cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D, BMQ>;
-  auto kern = dfa_bwd_kernel<D, BMQ, GQA, VARLEN>;
+  auto kern = dfa_bwd_kernel<D, BMQ, GQA, VARLEN, DET>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -697,6 +709,9 @@ cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream
   switch (headdim) {
     // grouped key/value heads have their own instantiation
     case 64:
+      if (p.dq_sem)  // deterministic mode
+        return p.vl ? launch_bwd_impl<64, 128, true, true, true>(p, stream)
+                    : launch_bwd_impl<64, 128, true, false, true>(p, stream);
       if (p.vl) return launch_bwd_impl<64, 128, true, true>(p, stream);
       return p.kv_group > 1 ? launch_bwd_impl<64, 128, true, false>(p, stream)
                             : launch_bwd_impl<64, 128, false, false>(p, stream);

@@ -196,7 +196,7 @@ __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   return it;
 }
 
-template <int D_, int STAGES_, int NWG_, int KVBUF_, bool GQA, bool VARLEN>
+template <int D_, int STAGES_, int NWG_, int KVBUF_, bool GQA, bool VARLEN, bool DET>
 __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 1)
     dfa_bwd2_kernel(const __grid_constant__ BwdParams p) {
   using C = Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>;
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       tmem_pin<HC>(dq);
       tc_fence_before();
       mbar_arrive_warp(BAR(C::BAR_DQFREE));
-      if constexpr (C::kTmaDQ) {
+      if constexpr (C::kTmaDQ && !DET) {
         // Stage the warp's HC queries x 32 head dims (scaled) in its own
         // shared tile and let the copy engine add them into the accumulator.
         // Lane 0 issues the reduce; before the warp rewrites the tile it
@@ -540,6 +540,16 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       const int n = VARLEN ? it.n : p.n;
       const size_t first = VARLEN ? static_cast<size_t>(it.row0)
                                   : static_cast<size_t>(it.wi.b) * 2 * static_cast<size_t>(p.n);
+      unsigned* sem = nullptr;
+      if constexpr (DET) {
+        // This item's contribution to the query tile comes after those of
+        // the key tiles the work order takes earlier: wait for them.
+        const int ord = dq_ordinal(p.mode, n, VARLEN ? it.bs : p.bs, BMQ, BN, qh, qs / BMQ,
+                                   it.wi.half, it.wi.tile);
+        sem = p.dq_sem + (static_cast<size_t>(it.dh) * p.H + h) * p.sem_rows + first +
+              static_cast<size_t>(qh) * n + qs;
+        if (!sem_wait_warp(sem, static_cast<unsigned>(C::kComputeWarps * ord), ab)) return false;
+      }
       float* ptr = p.dq_acc + ((first + static_cast<size_t>(qh) * n + qs + c0) * p.H + h) * D +
                    it.dh * DH + row;
       if (qs + c0 + HC <= n) {
@@ -556,6 +566,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           ptr += dq_stride;
         }
       }
+      if constexpr (DET) sem_signal_warp(sem);
       return true;
     };
     bool ok = true;
@@ -728,10 +739,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int STAGES, int NWG, int KVBUF, bool GQA, bool VARLEN>
+template <int D, int STAGES, int NWG, int KVBUF, bool GQA, bool VARLEN, bool DET = false>
 static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
   using C = Bwd2Cfg<D, STAGES, NWG, KVBUF>;
-  auto kern = dfa_bwd2_kernel<D, STAGES, NWG, KVBUF, GQA, VARLEN>;
+  auto kern = dfa_bwd2_kernel<D, STAGES, NWG, KVBUF, GQA, VARLEN, DET>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -760,12 +771,19 @@ cudaError_t launch_backward_d128(const BwdParams& p, cudaStream_t stream) {
   // Grouped key/value heads get their own instantiation, so that the
   // multi-head kernel keeps its tile loop free of head bookkeeping.
   constexpr int W = kBwd2WarpgroupsD128;
+  // Deterministic mode: its own instantiations (grouped heads, both layouts).
+  if (p.dq_sem)
+    return p.vl ? launch_bwd2_impl<128, 3, W, 1, true, true, true>(p, stream)
+                : launch_bwd2_impl<128, 3, W, 1, true, false, true>(p, stream);
   if (p.vl) return launch_bwd2_impl<128, 3, W, 1, true, true>(p, stream);
   return p.kv_group > 1 ? launch_bwd2_impl<128, 3, W, 1, true, false>(p, stream)
                         : launch_bwd2_impl<128, 3, W, 1, false, false>(p, stream);
 }
 
 cudaError_t launch_backward_d256(const BwdParams& p, cudaStream_t stream) {
+  if (p.dq_sem)
+    return p.vl ? launch_bwd2_impl<256, 1, 2, 1, true, true, true>(p, stream)
+                : launch_bwd2_impl<256, 1, 2, 1, true, false, true>(p, stream);
   if (p.vl) return launch_bwd2_impl<256, 1, 2, 1, true, true>(p, stream);
   return p.kv_group > 1 ? launch_bwd2_impl<256, 1, 2, 1, true, false>(p, stream)
                         : launch_bwd2_impl<256, 1, 2, 1, false, false>(p, stream);

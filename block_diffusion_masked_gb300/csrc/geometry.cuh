@@ -132,6 +132,19 @@ DFA_HD int bwd_segments(int mode, int n, int bs, int bm, int bn, int k_half, int
   return cnt;
 }
 
+// Deterministic dQ: the key tiles that reach query tile qt of half q_half
+// add into its dQ one after another, in the order the backward's work
+// order takes them (clean key tiles before noisy ones, increasing index;
+// the same order fwd_segments lists them).  Position of key tile kt of half
+// k_half in that order (bm: query rows per tile, bn: keys per tile).
+DFA_HD int dq_ordinal(int mode, int n, int bs, int bm, int bn, int q_half, int qt, int k_half,
+                      int kt) {
+  Segment s[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
+  const int cnt = fwd_segments(mode, n, bs, bm, bn, q_half, qt, s);
+  if (cnt > 0 && s[0].half == k_half) return kt - s[0].t_begin;
+  return (s[0].t_end - s[0].t_begin) + kt - s[1].t_begin;
+}
+
 // Offset of the log-sum-exp of row r of half `half` of sample b, head h.
 // Diffusion mode: lse is (B, H, 2n).  Causal mode: the sample is a pair of
 // consecutive sequences (2b, 2b+1) of length n and lse is (2B, H, n).

@@ -86,6 +86,11 @@ struct BwdParams {
   int vl_slots;
   int rows;
   int units;          // work units (items without the head-dim split)
+  // Deterministic mode only (null otherwise): one counter per (head-dim
+  // part, head, first row of a query tile), zero before the launch; rows =
+  // the rows of q (batch * 2n, or the packed rows).
+  unsigned* dq_sem;
+  int sem_rows;
 };
 
 #if defined(__CUDACC__)

@@ -93,6 +93,50 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
   }
 }
 
+// Ordered accumulation across CTAs (deterministic mode).  A counter in
+// global memory records how many contributions to one output region are
+// complete; the warp adding contribution `ord` waits until the counter
+// reaches `per * ord` (per: warps adding one contribution), adds, and counts
+// itself.  Lane 0 polls (bounded, as mbar_wait); returns false when the CTA
+// is aborting.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool sem_wait_warp(const unsigned* sem, unsigned target,
+                                              const AbortFlag& ab) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0 && ld_acquire_gpu(sem) < target) {
+    const unsigned long long t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+      if (ld_acquire_gpu(sem) >= target) break;
+      __nanosleep(32);
+      if ((i & 63u) == 0) {
+        if (*ab.flag) {
+          ok = 0;
+          break;
+        }
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          *ab.flag = 1;
+          atomicOr(ab.status, kStatusTimeout);
+          ok = 0;
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __threadfence();  // the other lanes' adds follow lane 0's acquire
+  return ok != 0;
+}
+// After the warp's adds: make them visible, then count the warp.
+__device__ __forceinline__ void sem_signal_warp(unsigned* sem) {
+  __threadfence();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) atomicAdd(sem, 1u);
+}
+
 // Warp-uniform wait: lane 0 polls (bounded), the verdict is broadcast, and
 // every lane then observes the completed phase itself (acquire).  Keeps the
 // warp converged for the .sync.aligned tcgen05 instructions that follow.

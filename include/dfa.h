@@ -149,6 +149,29 @@ int dfa_backward_varlen(const void *q, const void *k, const void *v, const void 
                         int headdim, int block_size, dfa_stream_t stream);
 
 /*
+ * The backward with options.  cu_seqlens == NULL: the batched layout of
+ * dfa_backward_gqa (batch, n); otherwise the packed layout of
+ * dfa_backward_varlen (n ignored).  flags: 0 or DFA_DETERMINISTIC.
+ *
+ * DFA_DETERMINISTIC ("Fast Diffusion Attention": the deterministic mode
+ * orders the accumulations of dQ with semaphores): the key tiles that reach
+ * a query tile add their share of dQ one after another, in the order the
+ * work counter hands them out, through one counter per (head-dim part,
+ * head, query tile) in global memory; the results are then bitwise the
+ * same from run to run.  dK and dV are summed inside one work item in a
+ * fixed order in every mode (with grouped heads too), so only dQ needs the
+ * counters.  Extra scratch: 2 * heads * rows uint32 counters (rows = batch
+ * * 2n, or the packed rows), zeroed stream-ordered.  Every wait is bounded;
+ * a wait that gives up sets DFA_ETIMEOUT in the status word.  Unknown flag
+ * bits: DFA_EINVAL.
+ */
+#define DFA_DETERMINISTIC 1
+int dfa_backward_ex(const void *q, const void *k, const void *v, const void *out,
+                    const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                    const int *cu_seqlens, int batch, int n, int heads, int kv_heads,
+                    int headdim, int block_size, int flags, dfa_stream_t stream);
+
+/*
  * The yardstick of "Fast Diffusion Attention", section "The right yardstick":
  * causal attention on `batch` independent sequences of length `seqlen`, same
  * layout (batch, seqlen, heads, headdim), lse (batch, heads, seqlen), run by

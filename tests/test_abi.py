@@ -70,6 +70,20 @@ def test_host_side_argument_checks(lib):
     assert lib.dfa_causal_forward(p, p, p, p, p, 3, 64, 2, 64, s) == b.DFA_EINVAL  # odd batch
     # an empty batch is a no-op
     assert lib.dfa_forward(p, p, p, p, p, 0, 64, 2, 64, 4, s) == b.DFA_OK
+    # grouped heads: kv_heads must divide heads
+    assert lib.dfa_forward_gqa(p, p, p, p, p, 1, 64, 4, 3, 64, 4, s) == b.DFA_EINVAL
+    assert lib.dfa_forward_gqa(p, p, p, p, p, 1, 64, 4, 0, 64, 4, s) == b.DFA_EINVAL
+    assert lib.dfa_backward_gqa(p, p, p, p, p, p, p, p, p, 1, 64, 2, 4, 64, 4, s) == b.DFA_EINVAL
+    # varlen: cu_seqlens must start at 0 with even, non-negative lengths
+    cu = lambda *xs: (ctypes.c_int * len(xs))(*xs)  # noqa: E731
+    assert lib.dfa_forward_varlen(p, p, p, p, p, cu(0, 3, 8), 2, 2, 2, 64, 4, s) == b.DFA_EINVAL
+    assert lib.dfa_forward_varlen(p, p, p, p, p, cu(2, 8), 1, 2, 2, 64, 4, s) == b.DFA_EINVAL
+    assert lib.dfa_forward_varlen(p, p, p, p, p, cu(0, 8, 6), 2, 2, 2, 64, 4, s) == b.DFA_EINVAL
+    assert lib.dfa_forward_varlen(p, p, p, p, p, None, 1, 2, 2, 64, 4, s) == b.DFA_EINVAL
+    assert lib.dfa_forward_varlen(p, p, p, p, p, cu(0, 0, 0), 2, 2, 2, 64, 4, s) == b.DFA_OK
+    # backward options: unknown flag bits are refused
+    assert lib.dfa_backward_ex(p, p, p, p, p, p, p, p, p, None, 1, 64, 2, 2, 64, 4, 2,
+                               s) == b.DFA_EINVAL
 
 
 def test_tile_shapes(lib):

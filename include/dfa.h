@@ -153,8 +153,8 @@ int dfa_backward_varlen(const void *q, const void *k, const void *v, const void 
  * dfa_backward_gqa (batch, n); otherwise the packed layout of
  * dfa_backward_varlen (n ignored).  flags: 0 or DFA_DETERMINISTIC.
  *
- * DFA_DETERMINISTIC ("Fast Diffusion Attention": the deterministic mode
- * orders the accumulations of dQ with semaphores): the key tiles that reach
+ * DFA_DETERMINISTIC (the deterministic mode of "Fast Diffusion Attention",
+ * where semaphores fix the order of the dQ sums): the key tiles that reach
  * a query tile add their share of dQ one after another, in the order the
  * work counter hands them out, through one counter per (head-dim part,
  * head, query tile) in global memory; the results are then bitwise the

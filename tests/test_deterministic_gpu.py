@@ -1,7 +1,7 @@
 """Deterministic backward: bitwise reproducible dQ, parity with the oracle.
 
-"Fast Diffusion Attention" offers a deterministic mode that orders the
-accumulations of dQ with semaphores.  Here the key tiles that reach a query
+"Fast Diffusion Attention" has a deterministic mode in which semaphores fix
+the order of the dQ sums.  Here the key tiles that reach a query
 tile add their part of dQ in the work order, through counters in global
 memory.  Checked: repeated runs give bitwise equal dq, dk, dv (batched,
 grouped heads, packed varlen; every head dimension); the results pass the

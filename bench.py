@@ -180,7 +180,7 @@ def cpu_baseline(w: inputs.Workload, budget_s=12.0, max_heads=None):
 # DRAM traffic (read + write bytes) per launch of the dominant kernel from
 # one ncu capture (profiles/dfa_bwd2_kernel_small_b8_n1024_h16_d128_bs16.md),
 # keyed by workload and kernel; any other pair reports null.
-NCU_TRAFFIC = {("small", "dfa_bwd2_kernel<128>"): 804.7e6}
+NCU_TRAFFIC = {("small", "dfa_bwd2_kernel<128>"): 804.9e6}
 
 
 def run_gpu(args, w, rank, world):
@@ -492,6 +492,16 @@ def run_variant(args, w):
         fwd = lambda: binding.dfa_forward_gqa(q, k, v, bs)  # noqa: E731
         bwd = lambda o, l: binding.dfa_backward_gqa(q, k, v, o, do, l, bs)  # noqa: E731
         shape = {"batch": w.batch, "n": w.n, "heads": H, "kv_heads": Hk}
+    elif args.variant == "fp8":
+        # forward only: per-tensor e4m3 quantisation of the workload's q, k, v
+        q, k, v = inputs.make_workload_inputs(w, with_dout=False)
+        qs, ks, vs = (float(t.float().abs().max()) / 448.0 for t in (q, k, v))
+        q, k, v = ((t.float() / s_).to(torch.float8_e4m3fn).to(dev)
+                   for t, s_ in ((q, qs), (k, ks), (v, vs)))
+        halves = [w.n] * w.batch
+        fwd = lambda: binding.dfa_forward_fp8(q, k, v, qs, ks, vs, bs)  # noqa: E731
+        bwd = lambda o, l: None  # noqa: E731
+        shape = {"batch": w.batch, "n": w.n, "heads": H, "inputs": "e4m3, per-tensor descale"}
     else:
         scale = w.batch * w.n / sum(VARLEN_HALVES)
         halves = [max(1, int(round(h * scale))) for h in VARLEN_HALVES]
@@ -503,7 +513,7 @@ def run_variant(args, w):
         shape = {"halves": halves, "rows": rows, "heads": H}
     pairs = sum(visible_pairs_per_sample(n, bs) for n in halves)
     f_fwd = 4.0 * pairs * d * H
-    f_bwd = 2.5 * f_fwd
+    f_bwd = 0.0 if args.variant == "fp8" else 2.5 * f_fwd
 
     def step(ev=None):
         if ev is not None:
@@ -542,7 +552,7 @@ def run_variant(args, w):
         "steps": args.steps,
         "warmup": args.warmup,
         "fwd_tflops": f_fwd / (split[0] * 1e-3) / 1e12,
-        "bwd_tflops": f_bwd / (split[1] * 1e-3) / 1e12,
+        "bwd_tflops": f_bwd / (split[1] * 1e-3) / 1e12 if f_bwd else None,
         "kernel_ms": {"fwd": float(split[0]), "bwd": float(split[1])},
         "dtype": "bf16",
         "data": "synthetic: i.i.d. N(0,1) bf16 from a seeded CPU generator",
@@ -562,8 +572,9 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sdpa", action="store_true", help="also time torch SDPA causal (context)")
-    ap.add_argument("--variant", default="mha", choices=["mha", "gqa", "varlen"],
-                    help="gqa / varlen: time the one-call API on that version of the workload")
+    ap.add_argument("--variant", default="mha", choices=["mha", "gqa", "varlen", "fp8"],
+                    help="gqa / varlen / fp8: time the one-call API on that version of the "
+                    "workload (fp8: the forward alone)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -43,6 +43,7 @@ _SIGNATURES = {
     "dfa_forward_varlen": (_I, [_P] * 6 + [_I] * 5 + [_P]),
     "dfa_backward_varlen": (_I, [_P] * 10 + [_I] * 5 + [_P]),
     "dfa_backward_ex": (_I, [_P] * 10 + [_I] * 7 + [_P]),
+    "dfa_forward_fp8": (_I, [_P] * 5 + [ctypes.c_float] * 3 + [_I] * 6 + [_P]),
     "dfa_causal_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "dfa_causal_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _P]),
     "dfa_status": (_I, [_P]),
@@ -262,6 +263,31 @@ def dfa_backward_varlen(q, k, v, out, dout, lse, cu_seqlens, block_size, dq=None
                                        d, int(block_size), _stream_ptr(q))
     _check("dfa_backward_varlen", rc)
     return dq, dk, dv
+
+
+def dfa_forward_fp8(q, k, v, q_descale, k_descale, v_descale, block_size, out=None, lse=None):
+    """FP8 forward: q (B, 2n, H, 128), k, v (B, 2n, Hk, 128) float8_e4m3fn CUDA tensors.
+
+    The attention of q * q_descale, k * k_descale, v * v_descale; returns
+    out (B, 2n, H, 128) bf16 and lse (B, H, 2n) float32.
+    """
+    for t in (q, k, v):
+        if t.dtype != torch.float8_e4m3fn or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous float8_e4m3fn CUDA tensors")
+    if q.dim() != 4 or k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("q (B, 2n, H, d), k and v (B, 2n, Hk, d)")
+    B, L, H, d = q.shape
+    Hk = k.shape[2]
+    if L % 2 or H % Hk:
+        raise ValueError("even 2n and kv_heads dividing heads required")
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_forward_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                   float(q_descale), float(k_descale), float(v_descale), B, L // 2,
+                                   H, Hk, d, int(block_size), _stream_ptr(q))
+    _check("dfa_forward_fp8", rc)
+    return out, lse
 
 
 def dfa_backward_ex(q, k, v, out, dout, lse, block_size, cu_seqlens=None, deterministic=False,

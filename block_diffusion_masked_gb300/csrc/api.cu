@@ -136,6 +136,41 @@ int make_map(CUtensorMap* map, const void* base, int B, int n, int H, int d, int
   return r == CUDA_SUCCESS ? DFA_OK : DFA_ECUDA;
 }
 
+// An e4m3 (one byte per element) (B, 2n, H, d) tensor as 5-D (d, H, n,
+// half, B) with boxes of (128, 1, rows, 1, 1), 128-byte swizzle: rows of
+// 128 head dims, the same 128-byte rows as the bf16 maps' 64.
+int make_map_u8(CUtensorMap* map, const void* base, int B, int n, int H, int d, int rows) {
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(n), 2, static_cast<cuuint64_t>(B)};
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(H) * d;
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d), row_bytes, row_bytes * n,
+                                 row_bytes * 2 * n};
+  const cuuint32_t box[5] = {128, 1, static_cast<cuuint32_t>(rows), 1, 1};
+  const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFA_OK : DFA_ECUDA;
+}
+
+// The FP8 forward's V^T, (B, H, 128, 2, n_pad) bytes, as 5-D (n, half,
+// 128, H, B) with boxes of (128, 1, 128, 1, 1): 128 keys of one half for
+// all 128 head dims, 128-byte swizzle; keys past n read zero.
+int make_map_vt(CUtensorMap* map, const void* base, int B, int n, int n_pad, int H) {
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(n), 2, 128, static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t np = static_cast<cuuint64_t>(n_pad);
+  const cuuint64_t strides[4] = {np, 2 * np, 256 * np, 256 * np * H};
+  const cuuint32_t box[5] = {128, 1, 128, 1, 1};
+  const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFA_OK : DFA_ECUDA;
+}
+
 // The float32 dQ accumulator (B, 2n, H, d) as 5-D (d, H, n, half, B) with
 // boxes of (32, 1, rows, 1, 1), no swizzle: the target of the backward's
 // bulk reduce-add of one warp's part of a query tile's dQ (rows past the
@@ -209,6 +244,64 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   // B * 2n * H * d floats, d a multiple of 64: whole 16-byte groups
   p.zero_groups = dq_acc ? static_cast<long long>(B) * 2 * n * H * d / 4 : 0;
   const cudaError_t e = launch_forward(p, d, stream);
+  return e == cudaSuccess ? DFA_OK : cuda_fail(e);
+}
+
+// FP8 forward: q, k, v e4m3 with per-tensor descales (x = x8 * x_descale);
+// out bf16, lse as dfa_forward's.  Headdim 128.
+int forward_fp8_impl(const void* q, const void* k, const void* v, void* out, float* lse,
+                     float q_descale, float k_descale, float v_descale, int B, int n, int H,
+                     int Hk, int d, int bs, cudaStream_t stream) {
+  int rc = check_common(B, n, H, d, bs);
+  if (rc) return rc;
+  if (d != 128) return DFA_EUNSUPPORTED;
+  const int G = kv_group_of(H, Hk);
+  if (G == 0) return DFA_EINVAL;
+  if (!(q_descale > 0.f) || !(k_descale > 0.f) || !(v_descale > 0.f) ||
+      !std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale))
+    return DFA_EINVAL;
+  if (B == 0) return DFA_OK;
+  if (!q || !k || !v || !out || !lse) return DFA_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return DFA_EINVAL;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds))) return rc;
+  TileShape ts;
+  tile_shape_for(d, &ts);
+  // V^T in stream-ordered scratch, keys padded to 16 (TMA row strides)
+  const int n_pad = (n + 15) / 16 * 16;
+  uint8_t* vt = nullptr;
+  const size_t vt_bytes = static_cast<size_t>(B) * Hk * 128 * 2 * n_pad;
+  FwdParams p{};
+  if ((rc = make_map_u8(&p.tm_q, q, B, n, H, d, ts.fwd_bm))) return rc;
+  if ((rc = make_map_u8(&p.tm_k, k, B, n, Hk, d, ts.fwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_o, out, B, n, H, d, ts.fwd_bm))) return rc;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&vt), vt_bytes, stream) != cudaSuccess)
+    return DFA_ECUDA;
+  if ((rc = make_map_vt(&p.tm_v, vt, B, n, n_pad, Hk))) {
+    cudaFreeAsync(vt, stream);
+    return rc;
+  }
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = ds->status;
+  p.B = B;
+  p.n = n;
+  p.H = H;
+  p.kv_group = G;
+  p.bs = bs < n ? bs : n;
+  p.mode = MODE_DIFFUSION;
+  p.q_tiles = cdiv(n, ts.fwd_bm);
+  // q, k, v (one byte) and out (two) of one (batch, head)
+  p.group = l2_group(5LL * 2 * n * d, ds->l2_bytes, B * H);
+  p.sched = sched_for_stream(ds, stream);
+  const double scale = static_cast<double>(q_descale) * k_descale / std::sqrt(static_cast<double>(d));
+  p.scale_log2 = static_cast<float>(1.4426950408889634 * scale);
+  p.out_scale = v_descale;
+  cudaError_t e = launch_fp8_v_transpose(static_cast<const uint8_t*>(v), vt, B, n, n_pad, Hk, stream);
+  if (e == cudaSuccess) e = launch_forward_fp8(p, d, stream);
+  cudaFreeAsync(vt, stream);
   return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
 
@@ -642,6 +735,13 @@ int dfa_backward_varlen(const void* q, const void* k, const void* v, const void*
                         int block_size, dfa_stream_t stream) {
   return backward_varlen_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens, batch, heads,
                               kv_heads, headdim, block_size, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_forward_fp8(const void* q, const void* k, const void* v, void* out, float* lse,
+                    float q_descale, float k_descale, float v_descale, int batch, int n,
+                    int heads, int kv_heads, int headdim, int block_size, dfa_stream_t stream) {
+  return forward_fp8_impl(q, k, v, out, lse, q_descale, k_descale, v_descale, batch, n, heads,
+                          kv_heads, headdim, block_size, static_cast<cudaStream_t>(stream));
 }
 
 int dfa_backward_ex(const void* q, const void* k, const void* v, const void* out,

@@ -105,6 +105,70 @@ __global__ void __launch_bounds__(256) dfa_dq_convert_kernel(const float4* __res
   }
 }
 
+// FP8 forward: V^T.  vt[b][h][c][half][j] = v[b][half * n + j][h][c] for
+// e4m3 v (B, 2n, H, 128), with vt rows of n_pad >= n keys, so that the
+// P V product reads V with the keys contiguous (the K-major operand layout).
+// One block per (128 keys of one half, head, batch): the 128 x 128-byte
+// tile goes through shared memory, read and written in 16-byte units.
+__global__ void __launch_bounds__(256) dfa_fp8_v_transpose_kernel(const uint8_t* __restrict__ v,
+                                                                   uint8_t* __restrict__ vt, int n,
+                                                                   int n_pad, int H) {
+  // tile[r][w]: bytes 4w..4w+3 of the head dims of key r (rows padded by a
+  // word against bank conflicts)
+  __shared__ uint32_t tile[128][33];
+  grid_dependency_wait();
+  const int per_half = gridDim.x >> 1;  // 128-key chunks per half
+  const int half = blockIdx.x >= per_half ? 1 : 0;
+  const int jh = (blockIdx.x - half * per_half) * 128;  // first key of the block in its half
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  for (int u = threadIdx.x; u < 128 * 8; u += blockDim.x) {
+    const int r = u >> 3, c16 = u & 7;  // key row, 16-byte unit of the head dims
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (jh + r < n)
+      w = *reinterpret_cast<const uint4*>(
+          v + ((static_cast<size_t>(b) * 2 * n + static_cast<size_t>(half) * n + jh + r) * H + h) *
+                  128 + 16 * c16);
+    tile[r][4 * c16 + 0] = w.x;
+    tile[r][4 * c16 + 1] = w.y;
+    tile[r][4 * c16 + 2] = w.z;
+    tile[r][4 * c16 + 3] = w.w;
+  }
+  __syncthreads();
+  // 4 x 4 byte blocks: keys 4m..4m+3 x head dims 4c4..4c4+3.  A warp takes
+  // the 32 key groups of one head-dim group, so each of its four output
+  // rows is written as 128 contiguous bytes.
+  const int m = threadIdx.x & 31;
+  for (int c4 = threadIdx.x >> 5; c4 < 32; c4 += blockDim.x >> 5) {
+    const uint32_t w0 = tile[4 * m + 0][c4], w1 = tile[4 * m + 1][c4];
+    const uint32_t w2 = tile[4 * m + 2][c4], w3 = tile[4 * m + 3][c4];
+    const uint32_t t0 = __byte_perm(w0, w1, 0x5140), t1 = __byte_perm(w2, w3, 0x5140);
+    const uint32_t t2 = __byte_perm(w0, w1, 0x7362), t3 = __byte_perm(w2, w3, 0x7362);
+    const uint32_t o[4] = {__byte_perm(t0, t1, 0x5410), __byte_perm(t0, t1, 0x7632),
+                           __byte_perm(t2, t3, 0x5410), __byte_perm(t2, t3, 0x7632)};
+    if (jh + 4 * m < n_pad) {
+#pragma unroll
+      for (int jd = 0; jd < 4; ++jd) {
+        const int c = 4 * c4 + jd;  // head dim = output row
+        *reinterpret_cast<uint32_t*>(
+            vt + (((static_cast<size_t>(b) * H + h) * 128 + c) * 2 + half) * n_pad + jh + 4 * m) =
+            o[jd];
+      }
+    }
+  }
+}
+
+cudaError_t launch_fp8_v_transpose(const uint8_t* v, uint8_t* vt, int B, int n, int n_pad, int H,
+                                   cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  // blocks along x: the 128-key chunks of the noisy half, then the clean
+  const int per_half = (n_pad + 127) / 128;
+  const dim3 grid(static_cast<unsigned>(2 * per_half), static_cast<unsigned>(H),
+                  static_cast<unsigned>(B));
+  return launch_chained(dfa_fp8_v_transpose_kernel, grid, dim3(256), 0, stream, v, vt, n, n_pad,
+                        H);
+}
+
 // Failure-detection self-test: one warp waits, through the same bounded
 // wait the attention kernels use, on an mbarrier that nothing arrives on.
 // The wait gives up after `limit_ns`, records the timeout in the status word

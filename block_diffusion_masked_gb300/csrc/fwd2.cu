@@ -39,13 +39,23 @@
 
 namespace dfa {
 
-template <int D, int STAGES>
+// FP8: q, k, v in e4m3 (the FP8 forward of "Fast Diffusion Attention"):
+// 128-byte rows hold 128 elements, a K step of the products is 32 elements,
+// P goes to TMEM as four e4m3 per column; out stays bf16, staged in the
+// query buffer, which keeps the bf16 tile's size.
+template <int D, int STAGES, bool FP8 = false>
 struct Fwd2Cfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
-  static constexpr int kChunks = D / 64;
-  static constexpr int kQBytes = BM * D * 2;
-  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int ES = FP8 ? 1 : 2;           // bytes per q / k / v element
+  static constexpr int kChunkElems = 128 / ES;     // elements per 128-byte row
+  static constexpr int kChunks = D / kChunkElems;  // 128-byte chunks of q, k, v rows
+  static constexpr int kOutChunks = D / 64;        // 128-byte chunks of a bf16 out row
+  static constexpr int kKSteps = D * ES / 32;      // K steps of S = Q K^T (32 bytes each)
+  static constexpr int kPVKeys = 32 / ES;          // keys per step of O += P V
+  static constexpr int kQLoadBytes = BM * D * ES;
+  static constexpr int kQBytes = BM * D * 2;       // query buffer: also the bf16 out tile
+  static constexpr int kKVBytes = BN * D * ES;
   static constexpr int kOffQ = 0;  // 2 buffers
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + STAGES * kKVBytes;
@@ -128,9 +138,9 @@ __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, 
   g->qs = g->wi.tile * bm;
 }
 
-template <int D, int STAGES, bool VARLEN>
+template <int D, int STAGES, bool VARLEN, bool FP8 = false>
 __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant__ FwdParams p) {
-  using C = Fwd2Cfg<D, STAGES>;
+  using C = Fwd2Cfg<D, STAGES, FP8>;
   constexpr int BM = C::BM;
   constexpr int BN = C::BN;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -209,8 +219,12 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         mbar_arrive_expect_tx(BAR(C::BAR_VFULL + st), C::kKVBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
-                      BAR(C::BAR_VFULL + st), 64 * c, vh, vc2, vc3, vc4);
+          if constexpr (FP8)  // V^T (n, half, headdim, heads, batch): keys innermost
+            tma_load_5d(sbase + C::kOffV + st * C::kKVBytes, &p.tm_v, BAR(C::BAR_VFULL + st), vc2,
+                        vc3, 0, vh, vc4);
+          else
+            tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
+                        BAR(C::BAR_VFULL + st), C::kChunkElems * c, vh, vc2, vc3, vc4);
         vg = -1;
         return true;
       };
@@ -228,12 +242,13 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         if (ig.item < 0) break;
         const int qb = k & 1;
         if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_QEMPTY + qb), ((k >> 1) - 1) & 1, ab))) break;
-        mbar_arrive_expect_tx(BAR(C::BAR_QFULL + qb), C::kQBytes);
+        mbar_arrive_expect_tx(BAR(C::BAR_QFULL + qb), C::kQLoadBytes);
         const HalfRows qr = half_rows<VARLEN>(ig.wi.b, ig.wi.half, ig.n, ig.row0);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, &p.tm_q,
-                      BAR(C::BAR_QFULL + qb), 64 * c, ig.wi.h, qr.base + ig.qs, qr.c3, qr.c4);
+                      BAR(C::BAR_QFULL + qb), C::kChunkElems * c, ig.wi.h, qr.base + ig.qs, qr.c3,
+                      qr.c4);
         // key/value head of query head wi.h (grouped heads: kv_group > 1)
         const int hk = p.kv_group == 1 ? ig.wi.h : ig.wi.h / p.kv_group;
         for (int j = 0; j < ig.ntiles; ++j, ++g) {
@@ -246,7 +261,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
-                        BAR(C::BAR_KFULL + st), 64 * c, hk, krow, kr.c3, kr.c4);
+                        BAR(C::BAR_KFULL + st), C::kChunkElems * c, hk, krow, kr.c3, kr.c4);
           if (vg >= 0 && !(ok = load_v())) break;
           vg = g;
           vh = hk;
@@ -274,11 +289,15 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     // for that P V (PVDONE); P V waits for the warpgroup's P (PFULL).
     if (lane == 0) {
       const bool s_warp = warp == 10;
-      constexpr uint32_t kIdS = idesc_bf16(BM, BN, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16(BM, D, false, true);
+      constexpr uint32_t kIdS =
+          FP8 ? idesc_e4m3(BM, BN, false, false) : idesc_bf16(BM, BN, false, false);
+      constexpr uint32_t kIdPV =
+          FP8 ? idesc_e4m3(BM, D, false, false) : idesc_bf16(BM, D, false, true);
       const uint64_t dQ = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
       const uint64_t dK = sdesc_sw128(sbase + C::kOffK, 16, 1024);
-      const uint64_t dV = sdesc_sw128(sbase + C::kOffV, BN * 128, 1024);
+      // V: MN-major (keys = K in rows); FP8 reads V^T, K-major (128 keys a row)
+      const uint64_t dV = FP8 ? sdesc_sw128(sbase + C::kOffV, 16, 1024)
+                              : sdesc_sw128(sbase + C::kOffV, BN * 128, 1024);
       auto adv = [](uint64_t d, uint32_t bytes) { return d + static_cast<uint64_t>(bytes >> 4); };
       bool ok = true;
       int g = 0;            // K/V ring position
@@ -305,11 +324,14 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
             if (c >= 1 && !(ok = mbar_wait(BAR(C::BAR_PVDONE + w), (c - 1) & 1, ab))) break;
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tmem + C::kTmemS + w * BN,
-                     adv(dQ, qb * C::kQBytes + (kk >> 2) * (BM * 128) + (kk & 3) * 32),
-                     adv(dK, st * C::kKVBytes + (kk >> 2) * (BN * 128) + (kk & 3) * 32), kIdS,
-                     kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < C::kKSteps; ++kk) {
+              const uint64_t a = adv(dQ, qb * C::kQBytes + (kk >> 2) * (BM * 128) + (kk & 3) * 32);
+              const uint64_t b = adv(dK, st * C::kKVBytes + (kk >> 2) * (BN * 128) + (kk & 3) * 32);
+              if constexpr (FP8)
+                mma_ss_f8(tmem + C::kTmemS + w * BN, a, b, kIdS, kk > 0 ? 1u : 0u);
+              else
+                mma_ss(tmem + C::kTmemS + w * BN, a, b, kIdS, kk > 0 ? 1u : 0u);
+            }
             mma_commit(BAR(C::BAR_SFULL + w));
             mma_commit(BAR(C::BAR_KEMPTY + st));
           } else {
@@ -317,10 +339,19 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
             if (!(ok = mbar_wait(BAR(C::BAR_VFULL + st), (gg / STAGES) & 1, ab))) break;
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ts(tmem + C::kTmemO + w * D, tmem + C::kTmemS + w * BN + 8 * kk,
-                     adv(dV, st * C::kKVBytes + kk * 16 * 128), kIdPV,
-                     (j >= 2 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BN / C::kPVKeys; ++kk) {
+              // P: 8 TMEM columns per step (bf16 pairs or e4m3 quadruples);
+              // V: 16 key rows of 128 bytes, or (V^T) 32 bytes of 128-key rows
+              const uint64_t b =
+                  adv(dV, st * C::kKVBytes + (FP8 ? kk * 32 : kk * C::kPVKeys * 128));
+              const uint32_t acc = (j >= 2 || kk > 0) ? 1u : 0u;
+              if constexpr (FP8)
+                mma_ts_f8(tmem + C::kTmemO + w * D, tmem + C::kTmemS + w * BN + 8 * kk, b, kIdPV,
+                          acc);
+              else
+                mma_ts(tmem + C::kTmemO + w * D, tmem + C::kTmemS + w * BN + 8 * kk, b, kIdPV,
+                       acc);
+            }
             mma_commit(BAR(C::BAR_VEMPTY + st));
             mma_commit(BAR(C::BAR_PVDONE + w));
           }
@@ -361,7 +392,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       if (!VARLEN || ig.qs + BM <= ig.n) {
         if (lane == 0) {
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
+          for (int c = 0; c < C::kOutChunks; ++c)
             tma_store_5d(&p.tm_o, stage + c * BM * 128, 64 * c, ig.wi.h, orr.base + ig.qs, orr.c3,
                          orr.c4);
           bulk_commit_group();
@@ -425,7 +456,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       const float fa = ma.y > 0.f ? ex2_approx(ma.x - m) : 0.f;
       const float fb = mb.y > 0.f ? ex2_approx(mb.x - m) : 0.f;
       const float lsum = ma.y * fa + mb.y * fb;
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      // FP8: out = (P V8) * v_descale / l
+      const float inv = lsum > 0.f ? (FP8 ? p.out_scale : 1.f) / lsum : 0.f;
       const int r = qs + row;
       // The out tile goes, as bf16, into this item's query buffer (free: the
       // item's last product has completed) in the 128-byte-swizzled layout of
@@ -571,9 +603,17 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
             const float p0 = ex2_approx(x0);
             const float p1 = ex2_approx(x1);
             acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
-            pk[e] = pack_bf16x2(p0, p1);
+            if constexpr (FP8) {
+              const uint32_t h = pack_e4m3x2(p0, p1);
+              pk[e >> 1] = (e & 1) ? (pk[e >> 1] | (h << 16)) : h;
+            } else {
+              pk[e] = pack_bf16x2(p0, p1);
+            }
           }
-          tmem_st16(s_col + 16 * c, pk);
+          if constexpr (FP8)
+            tmem_st8(s_col + 8 * c, pk);
+          else
+            tmem_st16(s_col + 16 * c, pk);
         }
         float a0, a1, b0, b1, c0, c1, d0, d1;
         f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
@@ -601,10 +641,10 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int STAGES, bool VARLEN>
+template <int D, int STAGES, bool VARLEN, bool FP8 = false>
 static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
-  using C = Fwd2Cfg<D, STAGES>;
-  auto kern = dfa_fwd2_kernel<D, STAGES, VARLEN>;
+  using C = Fwd2Cfg<D, STAGES, FP8>;
+  auto kern = dfa_fwd2_kernel<D, STAGES, VARLEN, FP8>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -618,6 +658,12 @@ static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
   const long long grid = items < sms ? items : sms;
   return launch_chained(kern, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads), C::kSmemBytes,
                         stream, p);
+}
+
+// FP8 (e4m3) q, k, v, headdim 128: smaller K / V tiles, so four stages.
+cudaError_t launch_forward_fp8(const FwdParams& p, int headdim, cudaStream_t stream) {
+  if (headdim != 128 || p.vl) return cudaErrorInvalidValue;
+  return launch_fwd2_impl<128, 4, false, true>(p, stream);
 }
 
 cudaError_t launch_forward_two_warpgroups(const FwdParams& p, int headdim, cudaStream_t stream) {

@@ -57,6 +57,7 @@ struct FwdParams {
   int vl_slots;
   int rows;
   int items;
+  float out_scale;  // FP8 forward: v's descale, applied to out
 };
 
 struct BwdParams {
@@ -159,6 +160,7 @@ cudaError_t launch_chained(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t
 // Launchers (one per translation unit).  Return a cudaError_t.
 cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream);
 cudaError_t launch_forward_two_warpgroups(const FwdParams& p, int headdim, cudaStream_t stream);
+cudaError_t launch_forward_fp8(const FwdParams& p, int headdim, cudaStream_t stream);
 cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream);
 cudaError_t launch_backward_d128(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_backward_d256(const BwdParams& p, cudaStream_t stream);
@@ -169,6 +171,8 @@ cudaError_t launch_selftest_wait(unsigned* status, unsigned long long limit_ns,
                                  cudaStream_t stream);
 cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, long long count,
                               cudaStream_t stream);
+cudaError_t launch_fp8_v_transpose(const uint8_t* v, uint8_t* vt, int B, int n, int n_pad, int H,
+                                   cudaStream_t stream);
 
 // Compute warpgroups of the headdim-128 backward kernel; each takes
 // 64 / this query columns of a tile and stages that many rows of dQ.

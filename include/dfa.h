@@ -149,6 +149,22 @@ int dfa_backward_varlen(const void *q, const void *k, const void *v, const void 
                         int headdim, int block_size, dfa_stream_t stream);
 
 /*
+ * FP8 forward ("Fast Diffusion Attention" lists an FP8 forward): q, k, v
+ * are e4m3 (one byte per element; q (batch, 2n, heads, 128), k, v (batch,
+ * 2n, kv_heads, 128)) with per-tensor descales: the attention is that of
+ * q8 * q_descale, k8 * k_descale, v8 * v_descale (descales finite, > 0).
+ * S = Q K^T and O = P V run on the e4m3 tensor-core path with float32
+ * accumulation; P is rounded to e4m3 (round to nearest even) for P V, while
+ * the row sums and lse use the unrounded probabilities, so |out - exact|
+ * <= 2^-4 * max|v| per element, plus the underflow of probabilities below
+ * e4m3's smallest subnormal.  out bf16 (batch, 2n, heads, 128), lse as
+ * dfa_forward.  headdim 128 only (DFA_EUNSUPPORTED otherwise).
+ */
+int dfa_forward_fp8(const void *q, const void *k, const void *v, void *out, float *lse,
+                    float q_descale, float k_descale, float v_descale, int batch, int n,
+                    int heads, int kv_heads, int headdim, int block_size, dfa_stream_t stream);
+
+/*
  * The backward with options.  cu_seqlens == NULL: the batched layout of
  * dfa_backward_gqa (batch, n); otherwise the packed layout of
  * dfa_backward_varlen (n ignored).  flags: 0 or DFA_DETERMINISTIC.

@@ -483,8 +483,10 @@ def run_variant(args, w):
     binding.lib()
     stream = torch.cuda.current_stream(dev)
     H, d, bs = w.heads, w.headdim, w.block_size
-    if args.variant == "gqa":
-        Hk = max(1, H // 4)
+    if args.variant in ("gqa", "onecall"):
+        # onecall: the same one-call path with every head its own key/value
+        # head, the baseline the grouped and packed variants compare with
+        Hk = max(1, H // 4) if args.variant == "gqa" else H
         q, _, _, do = inputs.make_workload_inputs(w)
         _, k, v = inputs.make_inputs(w.batch, w.n, Hk, d, seed=w.seed + 1, with_dout=False)
         q, k, v, do = (t.to(dev) for t in (q, k, v, do))
@@ -572,7 +574,7 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sdpa", action="store_true", help="also time torch SDPA causal (context)")
-    ap.add_argument("--variant", default="mha", choices=["mha", "gqa", "varlen", "fp8"],
+    ap.add_argument("--variant", default="mha", choices=["mha", "onecall", "gqa", "varlen", "fp8"],
                     help="gqa / varlen / fp8: time the one-call API on that version of the "
                     "workload (fp8: the forward alone)")
     args = ap.parse_args()

@@ -137,7 +137,7 @@ __device__ __forceinline__ void sem_signal_warp(unsigned* sem) {
   if ((threadIdx.x & 31) == 0) atomicAdd(sem, 1u);
 }
 
-// Warp-uniform wait: lane 0 polls (bounded), the verdict is broadcast, and
+// Warp-uniform wait: lane 0 polls (bounded), the result is broadcast, and
 // every lane then observes the completed phase itself (acquire).  Keeps the
 // warp converged for the .sync.aligned tcgen05 instructions that follow.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const AbortFlag& ab) {

@@ -14,7 +14,8 @@
 // Per query tile g (counted over the CTA's whole run), b = g % 2:
 //   S^T  = K Q^T                    -> TMEM S[b]
 //   dP^T = V dO^T                   -> TMEM dP (one buffer)
-//   P^T  = exp(scale S^T - LSE)  (0 on hidden pairs), dS^T = P^T (dP^T - D)
+//   P^T  = exp(scale S^T - LSE)  (0 on hidden pairs),
+//   dS^T = scale * P^T (dP^T - D)   (the softmax scale of dQ and dK)
 //        written back as bf16 into the columns of dP, dS^T also to shared
 //   dV  += P^T dO,  dK += dS^T Q    (A operand read from TMEM)
 //   dQ   = dS K                     -> TMEM S[b] (S is consumed by then),
@@ -257,7 +258,8 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
             : VARLEN ? p.lse[static_cast<size_t>(h) * p.rows + it.row0 + pos]
                      : p.lse[lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n)];
         lse_r[e] = valid ? lse * -1.4426950408889634f : -INFINITY;
-        del_r[e] = valid ? -del_bh[pos] : 0.f;
+        // -D * scale: the softmax scale is folded into dS (see the compute)
+        del_r[e] = valid ? -del_bh[pos] * p.scale : 0.f;
       }
       const int st = gg % STAGES;
       const int round = gg / STAGES;
@@ -481,6 +483,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     const int row = (warp & 3) * 32 + lane;  // key row of the tile / TMEM lane
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const float sl2 = p.scale_log2;
+    const uint64_t dscale2 = f2_pack(p.scale, p.scale);
 
     // dQ of global tile gg (TMEM S[gg % 2], lane = query `row` of the tile,
     // columns = head dims), added to dq_acc with 16-byte atomics.
@@ -516,9 +519,8 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         float* dst = p.dq_acc + ((first + pos) * p.H + it.h0 + hh) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 4)
-          red_add_v4_f32(dst + c, __uint_as_float(dq[c]) * p.scale,
-                         __uint_as_float(dq[c + 1]) * p.scale, __uint_as_float(dq[c + 2]) * p.scale,
-                         __uint_as_float(dq[c + 3]) * p.scale);
+          red_add_v4_f32(dst + c, __uint_as_float(dq[c]), __uint_as_float(dq[c + 1]),
+                         __uint_as_float(dq[c + 2]), __uint_as_float(dq[c + 3]));
       }
       if constexpr (DET) sem_signal_warp(sem);
       return true;
@@ -528,7 +530,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     // TMEM loads), bf16 P^T / dS^T back into the dP columns of each 32-query
     // chunk (P^T in its first 16 columns, dS^T in its last 16), dS^T also into
     // the swizzled shared tile.  Pairs of columns go through packed f32x2
-    // arithmetic: x = s * sl2 - lse2, p = 2^x, ds = p * (dp - D); a hidden
+    // arithmetic: x = s * sl2 - lse2, p = 2^x, ds = p * (dp - D) * scale; a hidden
     // pair's p is cleared by AND with its column's mask bit (keep_lo /
     // keep_hi: columns 0-31 / 32-63 of the slice).
     auto slice = [&](int h, uint32_t s_col, uint32_t ds_s, uint32_t nlse_s, uint32_t ndel_s,
@@ -561,8 +563,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
           const float p1 =
               __uint_as_float(__float_as_uint(ex2_approx(x1)) & bit_spread(keep, 2 * e + 1));
           const uint64_t pp = f2_pack(p0, p1);
+          // (dP - D) * scale: dS carries the softmax scale, so dQ and dK
+          // need no scaling afterwards
           const uint64_t dd =
-              f2_add(f2_pack(__uint_as_float(dpr[cl]), __uint_as_float(dpr[cl + 1])),
+              f2_fma(f2_pack(__uint_as_float(dpr[cl]), __uint_as_float(dpr[cl + 1])), dscale2,
                      f2_pack(nd.x, nd.y));
           float d0, d1;
           f2_unpack(f2_mul(pp, dd), d0, d1);
@@ -655,7 +659,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         const size_t first = VARLEN ? static_cast<size_t>(it.row0) : it.wi.b * L;
         const size_t off = ((first + pos) * p.Hk + it.wi.h) * D;
         __nv_bfloat16* dst = (wg == 0 ? p.dv : p.dk) + off;
-        const float mul = wg == 0 ? 1.f : p.scale;
+        const float mul = 1.f;  // dK: the scale is already in dS
 #pragma unroll
         for (int g8 = 0; g8 < D / 8; ++g8) {
           uint32_t w4[4];

@@ -9,7 +9,9 @@
 //
 // Per query tile (tensor cores, accumulators in TMEM):
 //   S^T  = K Q^T     -> TMEM S        dP^T = V dO^T   -> TMEM dP
-//   P^T  = exp(scale S^T - LSE) (0 on hidden pairs),  dS^T = P^T (dP^T - D)
+//   P^T  = exp(scale S^T - LSE) (0 on hidden pairs),
+//   dS^T = scale * P^T (dP^T - D)  (the softmax scale of dQ and dK, taken
+//        here once per element instead of on every dQ and dK element)
 //        bf16 P^T / dS^T -> TMEM PdS, dS^T also -> shared memory
 //   dV  += P^T dO,  dK += dS^T Q       (A operand read from TMEM PdS)
 //   dQ^T = K^T dS^T  -> TMEM DQ, then added to a float32 accumulator in
@@ -295,7 +297,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
             : VARLEN ? p.lse[static_cast<size_t>(h) * p.rows + it.row0 + pos]
                      : p.lse[lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n)];
         lse_r[e] = valid ? lse * -1.4426950408889634f : -INFINITY;
-        del_r[e] = valid ? -del_bh[pos] : 0.f;
+        // -D * scale: the softmax scale is folded into dS (see the compute)
+        del_r[e] = valid ? -del_bh[pos] * p.scale : 0.f;
       }
       const int st = gg % STAGES;
       const int round = gg / STAGES;
@@ -503,6 +506,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const float sl2 = p.scale_log2;
     const uint64_t scale2 = f2_pack(sl2, sl2);
+    const uint64_t dscale2 = f2_pack(p.scale, p.scale);
     const size_t dq_stride = static_cast<size_t>(p.H) * D;
     // dQ^T of the tile whose products completed last: TMEM lane = head dim
     // `row`, columns = queries; added into the float32 accumulator.
@@ -523,7 +527,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < HC; ++c)
-          st_shared_f32(stg + c * 128 + lane * 4, __uint_as_float(dq[c]) * p.scale);
+          st_shared_f32(stg + c * 128 + lane * 4, __uint_as_float(dq[c]));
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && qs + c0 < (VARLEN ? it.n : p.n)) {
@@ -555,14 +559,14 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       if (qs + c0 + HC <= n) {
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
-          red_add_f32(ptr, __uint_as_float(dq[c]) * p.scale);
+          red_add_f32(ptr, __uint_as_float(dq[c]));
           ptr += dq_stride;
         }
       } else {
         const int qmax = n - qs - c0;
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
-          if (c < qmax) red_add_f32(ptr, __uint_as_float(dq[c]) * p.scale);
+          if (c < qmax) red_add_f32(ptr, __uint_as_float(dq[c]));
           ptr += dq_stride;
         }
       }
@@ -623,7 +627,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           keep = below_hi & ~below_lo;
         }
         // P^T and dS^T in packed pairs: x = s * sl2 - lse2, p = 2^x,
-        // ds = p * (dp - D).  A hidden pair's p is cleared by AND with its
+        // ds = p * (dp - D) * scale.  A hidden pair's p is cleared by AND with its
         // column's mask bit spread to a word, so every tile runs the same
         // straight-line code.
         uint32_t wp[HC / 2], wd[HC / 2];
@@ -640,8 +644,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
               __uint_as_float(__float_as_uint(ex2_approx(x0)) & bit_spread(keep, 2 * e));
           const float p1 =
               __uint_as_float(__float_as_uint(ex2_approx(x1)) & bit_spread(keep, 2 * e + 1));
-          const uint64_t dd = f2_add(
-              f2_pack(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1])),
+          // (dP - D) * scale: dS carries the softmax scale, so dQ and dK
+          // need no scaling afterwards
+          const uint64_t dd = f2_fma(
+              f2_pack(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1])), dscale2,
               f2_pack(nd.x, nd.y));
           float d0, d1;
           f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
@@ -706,7 +712,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
                                     : static_cast<size_t>(it.wi.b) * 2 * static_cast<size_t>(p.n);
         const size_t off = ((first + pos) * p.Hk + it.wi.h) * D + it.dh * DH + d0;
         __nv_bfloat16* dst = (is_v ? p.dv : p.dk) + off;
-        const float mul = is_v ? 1.f : p.scale;
+        const float mul = 1.f;  // dK: the scale is already in dS
 #pragma unroll
         for (int g8 = 0; g8 < DW / 8; ++g8) {
           uint32_t w[4];

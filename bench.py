@@ -180,7 +180,7 @@ def cpu_baseline(w: inputs.Workload, budget_s=12.0, max_heads=None):
 # DRAM traffic (read + write bytes) per launch of the dominant kernel from
 # one ncu capture (profiles/dfa_bwd2_kernel_small_b8_n1024_h16_d128_bs16.md),
 # keyed by workload and kernel; any other pair reports null.
-NCU_TRAFFIC = {}  # re-captured after the latest change to the kernel: see profiles/
+NCU_TRAFFIC = {("small", "dfa_bwd2_kernel<128>"): 803.4e6}
 
 
 def run_gpu(args, w, rank, world):

@@ -484,16 +484,35 @@ def run_variant(args, w):
     stream = torch.cuda.current_stream(dev)
     H, d, bs = w.heads, w.headdim, w.block_size
     if args.variant in ("gqa", "onecall"):
-        # onecall: the same one-call path with every head its own key/value
-        # head, the baseline the grouped and packed variants compare with
+        # onecall: the one-call API with every head its own key/value head,
+        # the baseline of the packed line; gqa: the step API (the headline's
+        # path) with a key/value head per 4 query heads
         Hk = max(1, H // 4) if args.variant == "gqa" else H
         q, _, _, do = inputs.make_workload_inputs(w)
         _, k, v = inputs.make_inputs(w.batch, w.n, Hk, d, seed=w.seed + 1, with_dout=False)
         q, k, v, do = (t.to(dev) for t in (q, k, v, do))
         halves = [w.n] * w.batch
-        fwd = lambda: binding.dfa_forward_gqa(q, k, v, bs)  # noqa: E731
-        bwd = lambda o, l: binding.dfa_backward_gqa(q, k, v, o, do, l, bs)  # noqa: E731
         shape = {"batch": w.batch, "n": w.n, "heads": H, "kv_heads": Hk}
+        if args.variant == "onecall":
+            fwd = lambda: binding.dfa_forward_gqa(q, k, v, bs)  # noqa: E731
+            bwd = lambda o, l: binding.dfa_backward_gqa(q, k, v, o, do, l, bs)  # noqa: E731
+        else:
+            B_, L_ = q.shape[0], q.shape[1]
+            out = torch.empty_like(q)
+            lse = torch.empty((B_, H, L_), dtype=torch.float32, device=dev)
+            dq_acc = torch.empty(q.shape, dtype=torch.float32, device=dev)
+            delta = torch.empty((B_, H, L_), dtype=torch.float32, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            shape["api"] = "step (forward zeroing dq_acc, preprocess, main, convert)"
+
+            def fwd():
+                binding.dfa_fwd_main_gqa(q, k, v, out, lse, dq_acc, bs)
+                return out, lse
+
+            def bwd(o, l):
+                binding.dfa_bwd_preprocess(o, do, delta, None)
+                binding.dfa_bwd_main_gqa(q, k, v, do, l, delta, dq_acc, dk, dv, bs)
+                binding.dfa_bwd_dq_convert(dq_acc, dq)
     elif args.variant == "fp8":
         # forward only: per-tensor e4m3 quantisation of the workload's q, k, v
         q, k, v = inputs.make_workload_inputs(w, with_dout=False)
@@ -546,7 +565,7 @@ def run_variant(args, w):
         raise RuntimeError("device status set during the timed region")
     split = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in evs]).mean(0)
     return {
-        "metric": "visible-pair TFLOPS fwd+bwd on 1 GB300 (one-call API, " + args.variant + ")",
+        "metric": "visible-pair TFLOPS fwd+bwd on 1 GB300 (" + args.variant + ")",
         "variant": args.variant,
         "value": (f_fwd + f_bwd) / (ms * 1e-3) / 1e12,
         "unit": "TFLOPS",

@@ -52,6 +52,8 @@ _SIGNATURES = {
     "dfa_bwd_preprocess": (_I, [_P] * 4 + [_I] * 4 + [_P]),
     "dfa_bwd_main": (_I, [_P] * 9 + [_I] * 6 + [_P]),
     "dfa_bwd_dq_convert": (_I, [_P] * 2 + [_I] * 4 + [_P]),
+    "dfa_fwd_main_gqa": (_I, [_P] * 6 + [_I] * 7 + [_P]),
+    "dfa_bwd_main_gqa": (_I, [_P] * 9 + [_I] * 7 + [_P]),
     "dfa_fwd_segments": (_I, [_I] * 7 + [ctypes.POINTER(_I)]),
     "dfa_bwd_segments": (_I, [_I] * 7 + [ctypes.POINTER(_I)]),
     "dfa_tile_full": (_I, [_I] * 7),
@@ -389,6 +391,30 @@ def dfa_bwd_main(q, k, v, dout, lse, delta, dq_acc, dk, dv, block_size, mode=MOD
                                 _ptr(dq_acc), _ptr(dk), _ptr(dv), B, L // 2, H, d,
                                 int(block_size), int(mode), _stream_ptr(q))
     _check("dfa_bwd_main", rc)
+
+
+def dfa_fwd_main_gqa(q, k, v, out, lse, dq_acc, block_size, mode=MODE_DIFFUSION):
+    """dfa_fwd_main with k, v of fewer heads (grouped key/value heads)."""
+    Hk = _check_grouped(q, k, v, out)
+    B, L, H, d = q.shape
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_fwd_main_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                    _ptr_or_null(dq_acc), B, L // 2, H, Hk, d, int(block_size),
+                                    int(mode), _stream_ptr(q))
+    _check("dfa_fwd_main_gqa", rc)
+
+
+def dfa_bwd_main_gqa(q, k, v, dout, lse, delta, dq_acc, dk, dv, block_size, mode=MODE_DIFFUSION):
+    """dfa_bwd_main with k, v, dk, dv of fewer heads (grouped key/value heads)."""
+    Hk = _check_grouped(q, k, v, dout)
+    B, L, H, d = q.shape
+    if dk.shape != k.shape or dv.shape != v.shape:
+        raise ValueError("dk, dv must have the shape of k, v")
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_bwd_main_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse),
+                                    _ptr(delta), _ptr(dq_acc), _ptr(dk), _ptr(dv), B, L // 2, H,
+                                    Hk, d, int(block_size), int(mode), _stream_ptr(q))
+    _check("dfa_bwd_main_gqa", rc)
 
 
 def dfa_bwd_dq_convert(dq_acc, dq):

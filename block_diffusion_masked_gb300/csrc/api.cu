@@ -783,6 +783,24 @@ int dfa_fwd_main(const void* q, const void* k, const void* v, void* out, float* 
                       mode == MODE_CAUSAL ? 1 : block_size, static_cast<cudaStream_t>(stream));
 }
 
+int dfa_fwd_main_gqa(const void* q, const void* k, const void* v, void* out, float* lse,
+                     float* dq_acc, int batch, int n, int heads, int kv_heads, int headdim,
+                     int block_size, int mode, dfa_stream_t stream) {
+  if (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) return DFA_EINVAL;
+  return forward_impl(mode, q, k, v, out, lse, dq_acc, batch, n, heads, kv_heads, headdim,
+                      mode == MODE_CAUSAL ? 1 : block_size, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_bwd_main_gqa(const void* q, const void* k, const void* v, const void* dout,
+                     const float* lse, const float* delta, float* dq_acc, void* dk, void* dv,
+                     int batch, int n, int heads, int kv_heads, int headdim, int block_size,
+                     int mode, dfa_stream_t stream) {
+  if (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) return DFA_EINVAL;
+  return bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, batch, n, heads,
+                       kv_heads, headdim, mode == MODE_CAUSAL ? 1 : block_size,
+                       static_cast<cudaStream_t>(stream));
+}
+
 int dfa_bwd_preprocess(const void* out, const void* dout, float* delta, float* dq_acc, int batch,
                        int n, int heads, int headdim, dfa_stream_t stream) {
   return preprocess_impl(out, dout, delta, dq_acc, batch, n, heads, headdim,

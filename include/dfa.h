@@ -234,6 +234,19 @@ int dfa_bwd_main(const void *q, const void *k, const void *v, const void *dout,
                  dfa_stream_t stream);
 int dfa_bwd_dq_convert(const float *dq_acc, void *dq, int batch, int n, int heads,
                        int headdim, dfa_stream_t stream);
+/*
+ * dfa_fwd_main and dfa_bwd_main with grouped key/value heads: k, v, dk, dv
+ * have kv_heads heads (a divisor of heads), as for dfa_forward_gqa; q, out,
+ * dout, lse, delta and dq_acc keep `heads`.  kv_heads == heads is
+ * dfa_fwd_main / dfa_bwd_main.
+ */
+int dfa_fwd_main_gqa(const void *q, const void *k, const void *v, void *out, float *lse,
+                     float *dq_acc, int batch, int n, int heads, int kv_heads, int headdim,
+                     int block_size, int mode, dfa_stream_t stream);
+int dfa_bwd_main_gqa(const void *q, const void *k, const void *v, const void *dout,
+                     const float *lse, const float *delta, float *dq_acc, void *dk, void *dv,
+                     int batch, int n, int heads, int kv_heads, int headdim, int block_size,
+                     int mode, dfa_stream_t stream);
 
 /*
  * dfa_backward without any allocation.  No passage of the pages has a

@@ -155,3 +155,30 @@ def test_autograd_function_grouped(b):
     errs = _errors({"dq": _np(qd.grad), "dk": _np(kd.grad), "dv": _np(vd.grad)},
                    {"dq": rq, "dk": rk, "dv": rv})
     assert max(errs.values()) <= TOL_GRAD, errs
+
+
+@pytest.mark.parametrize("d,Hk", [(64, 1), (128, 2), (256, 1)])
+def test_grouped_step_api_matches_one_call(b, d, Hk):
+    # dfa_fwd_main_gqa (zeroing the dq accumulator) + preprocess +
+    # dfa_bwd_main_gqa + convert: the same kernels as the one-call API.
+    B, n, H, bs = 2, 150, 4, 8
+    q, k, v, do = _grouped_inputs(B, n, H, Hk, d, seed=88 + d)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    out = torch.empty_like(qd)
+    lse = torch.empty((B, H, 2 * n), dtype=torch.float32, device=dev)
+    dq_acc = torch.full(qd.shape, 1.0e30, dtype=torch.float32, device=dev)
+    delta = torch.empty((B, H, 2 * n), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    b.dfa_fwd_main_gqa(qd, kd, vd, out, lse, dq_acc, bs)
+    b.dfa_bwd_preprocess(out, dod, delta, None)
+    b.dfa_bwd_main_gqa(qd, kd, vd, dod, lse, delta, dq_acc, dk, dv, bs)
+    b.dfa_bwd_dq_convert(dq_acc, dq)
+    ro, rl = b.dfa_forward_gqa(qd, kd, vd, bs)
+    rq, rk, rv = b.dfa_backward_gqa(qd, kd, vd, ro, dod, rl, bs)
+    torch.cuda.synchronize()
+    assert b.dfa_status() == 0
+    assert torch.equal(out, ro) and torch.equal(lse, rl)
+    assert torch.equal(dk, rk) and torch.equal(dv, rv)
+    gap = (dq.float() - rq.float()).abs().max().item()
+    assert gap <= 1e-2 * rq.float().abs().max().item()

@@ -520,9 +520,22 @@ def run_variant(args, w):
         q, k, v = ((t.float() / s_).to(torch.float8_e4m3fn).to(dev)
                    for t, s_ in ((q, qs), (k, ks), (v, vs)))
         halves = [w.n] * w.batch
-        fwd = lambda: binding.dfa_forward_fp8(q, k, v, qs, ks, vs, bs)  # noqa: E731
+        # V^T made once, as a caller that quantises V would (its own cost is
+        # reported as transpose_ms); the timed forward runs on it
+        vt = binding.dfa_fp8_transpose_v(v)
+        fwd = lambda: binding.dfa_forward_fp8_vt(q, k, vt, H, qs, ks, vs, bs)  # noqa: E731
         bwd = lambda o, l: None  # noqa: E731
-        shape = {"batch": w.batch, "n": w.n, "heads": H, "inputs": "e4m3, per-tensor descale"}
+        shape = {"batch": w.batch, "n": w.n, "heads": H, "inputs": "e4m3, per-tensor descale",
+                 "api": "dfa_forward_fp8_vt on a V^T from dfa_fp8_transpose_v"}
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            binding.dfa_fp8_transpose_v(v, vt)
+        t0.record(stream)
+        for _ in range(10):
+            binding.dfa_fp8_transpose_v(v, vt)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        shape["transpose_ms"] = t0.elapsed_time(t1) / 10
     else:
         scale = w.batch * w.n / sum(VARLEN_HALVES)
         halves = [max(1, int(round(h * scale))) for h in VARLEN_HALVES]

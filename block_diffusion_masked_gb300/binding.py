@@ -44,6 +44,9 @@ _SIGNATURES = {
     "dfa_backward_varlen": (_I, [_P] * 10 + [_I] * 5 + [_P]),
     "dfa_backward_ex": (_I, [_P] * 10 + [_I] * 7 + [_P]),
     "dfa_forward_fp8": (_I, [_P] * 5 + [ctypes.c_float] * 3 + [_I] * 6 + [_P]),
+    "dfa_fp8_vt_bytes": (ctypes.c_longlong, [_I] * 4),
+    "dfa_fp8_transpose_v": (_I, [_P] * 2 + [_I] * 4 + [_P]),
+    "dfa_forward_fp8_vt": (_I, [_P] * 5 + [ctypes.c_float] * 3 + [_I] * 6 + [_P]),
     "dfa_causal_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "dfa_causal_backward": (_I, [_P] * 9 + [_I, _I, _I, _I, _P]),
     "dfa_status": (_I, [_P]),
@@ -289,6 +292,38 @@ def dfa_forward_fp8(q, k, v, q_descale, k_descale, v_descale, block_size, out=No
                                    float(q_descale), float(k_descale), float(v_descale), B, L // 2,
                                    H, Hk, d, int(block_size), _stream_ptr(q))
     _check("dfa_forward_fp8", rc)
+    return out, lse
+
+
+def dfa_fp8_transpose_v(v, vt=None):
+    """V^T of an e4m3 v (B, 2n, Hk, 128) for dfa_forward_fp8_vt (a uint8 tensor)."""
+    if v.dtype != torch.float8_e4m3fn or v.dim() != 4 or not v.is_contiguous():
+        raise ValueError("v must be a contiguous float8_e4m3fn (B, 2n, Hk, 128) tensor")
+    B, L, Hk, d = v.shape
+    nbytes = lib().dfa_fp8_vt_bytes(B, L // 2, Hk, d)
+    if nbytes < 0:
+        raise DfaError("dfa_fp8_vt_bytes", int(nbytes))
+    vt = torch.empty(int(nbytes), dtype=torch.uint8, device=v.device) if vt is None else vt
+    with torch.cuda.device(v.device):
+        rc = lib().dfa_fp8_transpose_v(_ptr(v), _ptr(vt), B, L // 2, Hk, d, _stream_ptr(v))
+    _check("dfa_fp8_transpose_v", rc)
+    return vt
+
+
+def dfa_forward_fp8_vt(q, k, vt, kv_heads, q_descale, k_descale, v_descale, block_size,
+                       out=None, lse=None):
+    """dfa_forward_fp8 on a V^T from dfa_fp8_transpose_v (no scratch)."""
+    for t in (q, k):
+        if t.dtype != torch.float8_e4m3fn or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k must be contiguous float8_e4m3fn CUDA tensors")
+    B, L, H, d = q.shape
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_forward_fp8_vt(_ptr(q), _ptr(k), _ptr(vt), _ptr(out), _ptr(lse),
+                                      float(q_descale), float(k_descale), float(v_descale), B,
+                                      L // 2, H, int(kv_heads), d, int(block_size), _stream_ptr(q))
+    _check("dfa_forward_fp8_vt", rc)
     return out, lse
 
 

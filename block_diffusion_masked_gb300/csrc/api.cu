@@ -249,9 +249,11 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
 
 // FP8 forward: q, k, v e4m3 with per-tensor descales (x = x8 * x_descale);
 // out bf16, lse as dfa_forward's.  Headdim 128.
+// vt_in: V^T already in the layout dfa_fp8_transpose_v writes (v unused),
+// or null: V^T goes through stream-ordered scratch.
 int forward_fp8_impl(const void* q, const void* k, const void* v, void* out, float* lse,
                      float q_descale, float k_descale, float v_descale, int B, int n, int H,
-                     int Hk, int d, int bs, cudaStream_t stream) {
+                     int Hk, int d, int bs, cudaStream_t stream, const void* vt_in = nullptr) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
   if (d != 128) return DFA_EUNSUPPORTED;
@@ -261,15 +263,17 @@ int forward_fp8_impl(const void* q, const void* k, const void* v, void* out, flo
       !std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale))
     return DFA_EINVAL;
   if (B == 0) return DFA_OK;
-  if (!q || !k || !v || !out || !lse) return DFA_EINVAL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+  const void* vsrc = vt_in ? vt_in : v;
+  if (!q || !k || !vsrc || !out || !lse) return DFA_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vsrc) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return DFA_EINVAL;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds))) return rc;
   TileShape ts;
   tile_shape_for(d, &ts);
-  // V^T in stream-ordered scratch, keys padded to 16 (TMA row strides)
+  // V^T (given, or in stream-ordered scratch), keys padded to 16 (TMA row
+  // strides)
   const int n_pad = (n + 15) / 16 * 16;
   uint8_t* vt = nullptr;
   const size_t vt_bytes = static_cast<size_t>(B) * Hk * 128 * 2 * n_pad;
@@ -277,11 +281,15 @@ int forward_fp8_impl(const void* q, const void* k, const void* v, void* out, flo
   if ((rc = make_map_u8(&p.tm_q, q, B, n, H, d, ts.fwd_bm))) return rc;
   if ((rc = make_map_u8(&p.tm_k, k, B, n, Hk, d, ts.fwd_bn))) return rc;
   if ((rc = make_map(&p.tm_o, out, B, n, H, d, ts.fwd_bm))) return rc;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&vt), vt_bytes, stream) != cudaSuccess)
-    return DFA_ECUDA;
-  if ((rc = make_map_vt(&p.tm_v, vt, B, n, n_pad, Hk))) {
-    cudaFreeAsync(vt, stream);
-    return rc;
+  if (vt_in) {
+    if ((rc = make_map_vt(&p.tm_v, vt_in, B, n, n_pad, Hk))) return rc;
+  } else {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&vt), vt_bytes, stream) != cudaSuccess)
+      return DFA_ECUDA;
+    if ((rc = make_map_vt(&p.tm_v, vt, B, n, n_pad, Hk))) {
+      cudaFreeAsync(vt, stream);
+      return rc;
+    }
   }
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
@@ -299,9 +307,10 @@ int forward_fp8_impl(const void* q, const void* k, const void* v, void* out, flo
   const double scale = static_cast<double>(q_descale) * k_descale / std::sqrt(static_cast<double>(d));
   p.scale_log2 = static_cast<float>(1.4426950408889634 * scale);
   p.out_scale = v_descale;
-  cudaError_t e = launch_fp8_v_transpose(static_cast<const uint8_t*>(v), vt, B, n, n_pad, Hk, stream);
+  cudaError_t e = cudaSuccess;
+  if (!vt_in) e = launch_fp8_v_transpose(static_cast<const uint8_t*>(v), vt, B, n, n_pad, Hk, stream);
   if (e == cudaSuccess) e = launch_forward_fp8(p, d, stream);
-  cudaFreeAsync(vt, stream);
+  if (vt) cudaFreeAsync(vt, stream);
   return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
 
@@ -742,6 +751,35 @@ int dfa_forward_fp8(const void* q, const void* k, const void* v, void* out, floa
                     int heads, int kv_heads, int headdim, int block_size, dfa_stream_t stream) {
   return forward_fp8_impl(q, k, v, out, lse, q_descale, k_descale, v_descale, batch, n, heads,
                           kv_heads, headdim, block_size, static_cast<cudaStream_t>(stream));
+}
+
+long long dfa_fp8_vt_bytes(int batch, int n, int kv_heads, int headdim) {
+  if (batch < 0 || n < 1 || kv_heads < 1 || headdim != 128) return DFA_EINVAL;
+  return static_cast<long long>(batch) * kv_heads * 128 * 2 * ((n + 15) / 16 * 16);
+}
+
+int dfa_fp8_transpose_v(const void* v, void* vt, int batch, int n, int kv_heads, int headdim,
+                        dfa_stream_t stream) {
+  if (dfa_fp8_vt_bytes(batch, n, kv_heads, headdim) < 0) return DFA_EINVAL;
+  if (batch == 0) return DFA_OK;
+  if (!v || !vt || !aligned16(v) || !aligned16(vt)) return DFA_EINVAL;
+  DeviceState* ds = nullptr;
+  const int rc = device_state(&ds);
+  if (rc) return rc;
+  const cudaError_t e =
+      launch_fp8_v_transpose(static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt), batch, n,
+                             (n + 15) / 16 * 16, kv_heads, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DFA_OK : cuda_fail(e);
+}
+
+int dfa_forward_fp8_vt(const void* q, const void* k, const void* vt, void* out, float* lse,
+                       float q_descale, float k_descale, float v_descale, int batch, int n,
+                       int heads, int kv_heads, int headdim, int block_size,
+                       dfa_stream_t stream) {
+  if (!vt) return DFA_EINVAL;
+  return forward_fp8_impl(q, k, nullptr, out, lse, q_descale, k_descale, v_descale, batch, n,
+                          heads, kv_heads, headdim, block_size,
+                          static_cast<cudaStream_t>(stream), vt);
 }
 
 int dfa_backward_ex(const void* q, const void* k, const void* v, const void* out,

@@ -165,6 +165,24 @@ int dfa_forward_fp8(const void *q, const void *k, const void *v, void *out, floa
                     int heads, int kv_heads, int headdim, int block_size, dfa_stream_t stream);
 
 /*
+ * The FP8 forward in two steps, for callers that produce V^T once (e.g.
+ * while quantising V) and reuse it: dfa_fp8_transpose_v writes the V^T that
+ * dfa_forward_fp8 builds internally -- e4m3 bytes laid out (batch,
+ * kv_heads, 128, 2, n_pad), n_pad = n rounded up to 16, element
+ * [b][h][c][half][j] = v[b][half * n + j][h][c]; keys j >= n unspecified --
+ * into dfa_fp8_vt_bytes(batch, n, kv_heads, 128) bytes of device memory,
+ * and dfa_forward_fp8_vt runs the forward on it (no scratch).  Results as
+ * dfa_forward_fp8.
+ */
+long long dfa_fp8_vt_bytes(int batch, int n, int kv_heads, int headdim);
+int dfa_fp8_transpose_v(const void *v, void *vt, int batch, int n, int kv_heads, int headdim,
+                        dfa_stream_t stream);
+int dfa_forward_fp8_vt(const void *q, const void *k, const void *vt, void *out, float *lse,
+                       float q_descale, float k_descale, float v_descale, int batch, int n,
+                       int heads, int kv_heads, int headdim, int block_size,
+                       dfa_stream_t stream);
+
+/*
  * The backward with options.  cu_seqlens == NULL: the batched layout of
  * dfa_backward_gqa (batch, n); otherwise the packed layout of
  * dfa_backward_varlen (n ignored).  flags: 0 or DFA_DETERMINISTIC.

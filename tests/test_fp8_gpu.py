@@ -69,3 +69,20 @@ def test_fp8_rejects_other_head_dims(b):
     q = torch.zeros((1, 8, 2, 64), dtype=torch.float8_e4m3fn, device="cuda")
     with pytest.raises(DfaError):
         b.dfa_forward_fp8(q, q, q, 1.0, 1.0, 1.0, 2)
+
+
+@pytest.mark.parametrize("n,Hk", [(300, 2), (67, 1)])
+def test_fp8_two_step_equals_one_call(b, n, Hk):
+    # dfa_fp8_transpose_v + dfa_forward_fp8_vt: bitwise the one-call forward
+    B, H, d, bs = 2, 4, 128, 16
+    q, _, _, _ = inputs.make_inputs(B, n, H, d, seed=710 + n)
+    _, k, v = inputs.make_inputs(B, n, Hk, d, seed=711 + n, with_dout=False)
+    (q8, qs), (k8, ks), (v8, vs) = (_quantize(t) for t in (q, k, v))
+    dev = torch.device("cuda", 0)
+    q8, k8, v8 = q8.to(dev), k8.to(dev), v8.to(dev)
+    o1, l1 = b.dfa_forward_fp8(q8, k8, v8, qs, ks, vs, bs)
+    vt = b.dfa_fp8_transpose_v(v8)
+    o2, l2 = b.dfa_forward_fp8_vt(q8, k8, vt, Hk, qs, ks, vs, bs)
+    torch.cuda.synchronize()
+    assert b.dfa_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

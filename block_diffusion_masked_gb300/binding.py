@@ -55,6 +55,8 @@ _SIGNATURES = {
     "dfa_bwd_preprocess": (_I, [_P] * 4 + [_I] * 4 + [_P]),
     "dfa_bwd_main": (_I, [_P] * 9 + [_I] * 6 + [_P]),
     "dfa_bwd_dq_convert": (_I, [_P] * 2 + [_I] * 4 + [_P]),
+    "dfa_bwd_preprocess_ex": (_I, [_P] * 4 + [_I] * 5 + [_P]),
+    "dfa_bwd_dq_convert_ex": (_I, [_P] * 2 + [_I] * 5 + [_P]),
     "dfa_fwd_main_gqa": (_I, [_P] * 6 + [_I] * 7 + [_P]),
     "dfa_bwd_main_gqa": (_I, [_P] * 9 + [_I] * 7 + [_P]),
     "dfa_fwd_segments": (_I, [_I] * 7 + [ctypes.POINTER(_I)]),
@@ -103,6 +105,21 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _check_buf(t, shape, dtype, device, name):
+    """A caller-supplied buffer must be exactly what the library will write."""
+    if (not isinstance(t, torch.Tensor) or tuple(t.shape) != tuple(shape) or t.dtype != dtype
+            or t.device != device or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} "
+                         f"on {device}")
+    return t
+
+
+def _out_or_new(t, shape, dtype, device, name):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    return _check_buf(t, shape, dtype, device, name)
+
+
 def _check_qkv(*ts):
     q = ts[0]
     if q.dim() != 4:
@@ -127,8 +144,8 @@ def dfa_forward(q, k, v, block_size, out=None, lse=None):
     B, L, H, d = q.shape
     if L % 2:
         raise ValueError("the sequence must be [noisy | clean] with an even length 2n")
-    out = torch.empty_like(q) if out is None else out
-    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    out = _out_or_new(out, q.shape, torch.bfloat16, q.device, "out")
+    lse = _out_or_new(lse, (B, H, L), torch.float32, q.device, "lse")
     with torch.cuda.device(q.device):
         rc = lib().dfa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L // 2, H, d,
                                int(block_size), _stream_ptr(q))
@@ -140,11 +157,12 @@ def dfa_backward(q, k, v, out, dout, lse, block_size, dq=None, dk=None, dv=None)
     """Block-diffusion attention backward; returns (dq, dk, dv) bf16."""
     _check_qkv(q, k, v, out, dout)
     B, L, H, d = q.shape
-    if lse.shape != (B, H, L) or lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be contiguous float32 (B, H, 2n)")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    if L % 2:
+        raise ValueError("the sequence must be [noisy | clean] with an even length 2n")
+    _check_buf(lse, (B, H, L), torch.float32, q.device, "lse")
+    dq = _out_or_new(dq, q.shape, torch.bfloat16, q.device, "dq")
+    dk = _out_or_new(dk, k.shape, torch.bfloat16, q.device, "dk")
+    dv = _out_or_new(dv, v.shape, torch.bfloat16, q.device, "dv")
     with torch.cuda.device(q.device):
         rc = lib().dfa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
                                 _ptr(dq), _ptr(dk), _ptr(dv), B, L // 2, H, d, int(block_size),
@@ -180,8 +198,8 @@ def dfa_forward_gqa(q, k, v, block_size, out=None, lse=None):
     B, L, H, d = q.shape
     if L % 2:
         raise ValueError("the sequence must be [noisy | clean] with an even length 2n")
-    out = torch.empty_like(q) if out is None else out
-    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    out = _out_or_new(out, q.shape, torch.bfloat16, q.device, "out")
+    lse = _out_or_new(lse, (B, H, L), torch.float32, q.device, "lse")
     with torch.cuda.device(q.device):
         rc = lib().dfa_forward_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L // 2, H,
                                    Hk, d, int(block_size), _stream_ptr(q))
@@ -196,11 +214,12 @@ def dfa_backward_gqa(q, k, v, out, dout, lse, block_size, dq=None, dk=None, dv=N
     """
     Hk = _check_grouped(q, k, v, out, dout)
     B, L, H, d = q.shape
-    if lse.shape != (B, H, L) or lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be contiguous float32 (B, H, 2n)")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    if L % 2:
+        raise ValueError("the sequence must be [noisy | clean] with an even length 2n")
+    _check_buf(lse, (B, H, L), torch.float32, q.device, "lse")
+    dq = _out_or_new(dq, q.shape, torch.bfloat16, q.device, "dq")
+    dk = _out_or_new(dk, k.shape, torch.bfloat16, q.device, "dk")
+    dv = _out_or_new(dv, v.shape, torch.bfloat16, q.device, "dv")
     with torch.cuda.device(q.device):
         rc = lib().dfa_backward_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
                                     _ptr(dq), _ptr(dk), _ptr(dv), B, L // 2, H, Hk, d,
@@ -242,8 +261,8 @@ def dfa_forward_varlen(q, k, v, cu_seqlens, block_size, out=None, lse=None):
     Hk = _check_packed(q, k, v)
     rows, H, d = q.shape
     cu, batch = _cu_array(cu_seqlens, rows)
-    out = torch.empty_like(q) if out is None else out
-    lse = torch.empty((H, rows), dtype=torch.float32, device=q.device) if lse is None else lse
+    out = _out_or_new(out, q.shape, torch.bfloat16, q.device, "out")
+    lse = _out_or_new(lse, (H, rows), torch.float32, q.device, "lse")
     with torch.cuda.device(q.device):
         rc = lib().dfa_forward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), cu, batch,
                                       H, Hk, d, int(block_size), _stream_ptr(q))
@@ -256,12 +275,11 @@ def dfa_backward_varlen(q, k, v, out, dout, lse, cu_seqlens, block_size, dq=None
     """Backward on a packed batch; returns (dq, dk, dv) bf16."""
     Hk = _check_packed(q, k, v, out, dout)
     rows, H, d = q.shape
-    if lse.shape != (H, rows) or lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be contiguous float32 (heads, rows)")
+    _check_buf(lse, (H, rows), torch.float32, q.device, "lse")
     cu, batch = _cu_array(cu_seqlens, rows)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = _out_or_new(dq, q.shape, torch.bfloat16, q.device, "dq")
+    dk = _out_or_new(dk, k.shape, torch.bfloat16, q.device, "dk")
+    dv = _out_or_new(dv, v.shape, torch.bfloat16, q.device, "dv")
     with torch.cuda.device(q.device):
         rc = lib().dfa_backward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
                                        _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), cu, batch, H, Hk,
@@ -285,8 +303,10 @@ def dfa_forward_fp8(q, k, v, q_descale, k_descale, v_descale, block_size, out=No
     Hk = k.shape[2]
     if L % 2 or H % Hk:
         raise ValueError("even 2n and kv_heads dividing heads required")
-    out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if out is None else out
-    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must live on the same CUDA device")
+    out = _out_or_new(out, q.shape, torch.bfloat16, q.device, "out")
+    lse = _out_or_new(lse, (B, H, L), torch.float32, q.device, "lse")
     with torch.cuda.device(q.device):
         rc = lib().dfa_forward_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                                    float(q_descale), float(k_descale), float(v_descale), B, L // 2,
@@ -296,14 +316,21 @@ def dfa_forward_fp8(q, k, v, q_descale, k_descale, v_descale, block_size, out=No
 
 
 def dfa_fp8_transpose_v(v, vt=None):
-    """V^T of an e4m3 v (B, 2n, Hk, 128) for dfa_forward_fp8_vt (a uint8 tensor)."""
-    if v.dtype != torch.float8_e4m3fn or v.dim() != 4 or not v.is_contiguous():
-        raise ValueError("v must be a contiguous float8_e4m3fn (B, 2n, Hk, 128) tensor")
+    """V^T of an e4m3 v (B, 2n, Hk, 128) for dfa_forward_fp8_vt (a uint8 tensor).
+
+    A caller-supplied ``vt`` must be a contiguous uint8 tensor on v's device
+    with exactly dfa_fp8_vt_bytes(B, n, Hk, 128) elements.
+    """
+    if (v.dtype != torch.float8_e4m3fn or v.dim() != 4 or not v.is_contiguous()
+            or not v.is_cuda):
+        raise ValueError("v must be a contiguous float8_e4m3fn (B, 2n, Hk, 128) CUDA tensor")
     B, L, Hk, d = v.shape
+    if L % 2:
+        raise ValueError("the sequence must be [noisy | clean] with an even length 2n")
     nbytes = lib().dfa_fp8_vt_bytes(B, L // 2, Hk, d)
     if nbytes < 0:
         raise DfaError("dfa_fp8_vt_bytes", int(nbytes))
-    vt = torch.empty(int(nbytes), dtype=torch.uint8, device=v.device) if vt is None else vt
+    vt = _out_or_new(vt, (int(nbytes),), torch.uint8, v.device, "vt")
     with torch.cuda.device(v.device):
         rc = lib().dfa_fp8_transpose_v(_ptr(v), _ptr(vt), B, L // 2, Hk, d, _stream_ptr(v))
     _check("dfa_fp8_transpose_v", rc)
@@ -312,17 +339,36 @@ def dfa_fp8_transpose_v(v, vt=None):
 
 def dfa_forward_fp8_vt(q, k, vt, kv_heads, q_descale, k_descale, v_descale, block_size,
                        out=None, lse=None):
-    """dfa_forward_fp8 on a V^T from dfa_fp8_transpose_v (no scratch)."""
+    """dfa_forward_fp8 on a V^T from dfa_fp8_transpose_v (no scratch).
+
+    ``kv_heads`` must equal k.shape[2]; ``vt`` must be the uint8 tensor
+    dfa_fp8_transpose_v wrote for a v of k's shape.
+    """
     for t in (q, k):
         if t.dtype != torch.float8_e4m3fn or not t.is_cuda or not t.is_contiguous():
             raise ValueError("q, k must be contiguous float8_e4m3fn CUDA tensors")
+    if q.dim() != 4 or k.dim() != 4 or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("q (B, 2n, H, d), k (B, 2n, Hk, d)")
+    if k.device != q.device:
+        raise ValueError("q and k must live on the same CUDA device")
     B, L, H, d = q.shape
-    out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if out is None else out
-    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    if L % 2:
+        raise ValueError("the sequence must be [noisy | clean] with an even length 2n")
+    Hk = k.shape[2]
+    if int(kv_heads) != Hk:
+        raise ValueError(f"kv_heads ({kv_heads}) must equal k.shape[2] ({Hk})")
+    if H % Hk:
+        raise ValueError("kv_heads must divide the query heads")
+    nbytes = lib().dfa_fp8_vt_bytes(B, L // 2, Hk, d)
+    if nbytes < 0:
+        raise DfaError("dfa_fp8_vt_bytes", int(nbytes))
+    _check_buf(vt, (int(nbytes),), torch.uint8, q.device, "vt")
+    out = _out_or_new(out, q.shape, torch.bfloat16, q.device, "out")
+    lse = _out_or_new(lse, (B, H, L), torch.float32, q.device, "lse")
     with torch.cuda.device(q.device):
         rc = lib().dfa_forward_fp8_vt(_ptr(q), _ptr(k), _ptr(vt), _ptr(out), _ptr(lse),
                                       float(q_descale), float(k_descale), float(v_descale), B,
-                                      L // 2, H, int(kv_heads), d, int(block_size), _stream_ptr(q))
+                                      L // 2, H, Hk, d, int(block_size), _stream_ptr(q))
     _check("dfa_forward_fp8_vt", rc)
     return out, lse
 
@@ -362,11 +408,11 @@ def dfa_backward_ex(q, k, v, out, dout, lse, block_size, cu_seqlens=None, determ
 
 
 def dfa_causal_forward(q, k, v, out=None, lse=None):
-    """Causal attention on (Bc, L, H, d) (Bc even): the yardstick."""
+    """Causal attention on (Bc, L, H, d), any Bc: the yardstick."""
     _check_qkv(q, k, v)
     B, L, H, d = q.shape
-    out = torch.empty_like(q) if out is None else out
-    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    out = _out_or_new(out, q.shape, torch.bfloat16, q.device, "out")
+    lse = _out_or_new(lse, (B, H, L), torch.float32, q.device, "lse")
     with torch.cuda.device(q.device):
         rc = lib().dfa_causal_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, H, d,
                                       _stream_ptr(q))
@@ -377,9 +423,10 @@ def dfa_causal_forward(q, k, v, out=None, lse=None):
 def dfa_causal_backward(q, k, v, out, dout, lse, dq=None, dk=None, dv=None):
     _check_qkv(q, k, v, out, dout)
     B, L, H, d = q.shape
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    _check_buf(lse, (B, H, L), torch.float32, q.device, "lse")
+    dq = _out_or_new(dq, q.shape, torch.bfloat16, q.device, "dq")
+    dk = _out_or_new(dk, k.shape, torch.bfloat16, q.device, "dk")
+    dv = _out_or_new(dv, v.shape, torch.bfloat16, q.device, "dv")
     with torch.cuda.device(q.device):
         rc = lib().dfa_causal_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
                                        _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, L, H, d,
@@ -392,38 +439,70 @@ def _ptr_or_null(t):
     return ctypes.c_void_p(None) if t is None else _ptr(t)
 
 
+def _step_shape(q, mode):
+    """(batch, n, rows per batch entry) of a step-API tensor for `mode`.
+
+    Diffusion: q is (B, 2n, H, d); causal: q is (Bc, n, H, d), Bc sequences.
+    """
+    B, L, H, d = q.shape
+    if mode == MODE_CAUSAL:
+        return B, L, L
+    if mode != MODE_DIFFUSION:
+        raise ValueError("mode must be MODE_DIFFUSION or MODE_CAUSAL")
+    if L % 2:
+        raise ValueError("the sequence must be [noisy | clean] with an even length 2n")
+    return B, L // 2, L
+
+
+def _check_scratch(q, lse, delta, dq_acc):
+    B, L, H, d = q.shape
+    if lse is not None:
+        _check_buf(lse, (B, H, L), torch.float32, q.device, "lse")
+    if delta is not None:
+        _check_buf(delta, (B, H, L), torch.float32, q.device, "delta")
+    if dq_acc is not None:
+        _check_buf(dq_acc, q.shape, torch.float32, q.device, "dq_acc")
+
+
 def dfa_fwd_main(q, k, v, out, lse, dq_acc, block_size, mode=MODE_DIFFUSION):
     """The forward step; also zeroes dq_acc (float32, shape of q) unless None.
 
-    q, k, v, out: (B, 2n, H, d) bf16; lse (B, H, 2n) fp32 (in the causal mode
-    the paired view's (2B, H, n) layout, as dfa_causal_forward writes it).
+    Diffusion: q, k, v, out (B, 2n, H, d) bf16, lse (B, H, 2n) fp32.  Causal:
+    q, k, v, out (Bc, n, H, d), lse (Bc, H, n), as dfa_causal_forward.
     """
     _check_qkv(q, k, v, out)
-    B, L, H, d = q.shape
+    B, n, L = _step_shape(q, mode)
+    H, d = q.shape[2], q.shape[3]
+    _check_scratch(q, lse, None, dq_acc)
     with torch.cuda.device(q.device):
         rc = lib().dfa_fwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                                _ptr_or_null(dq_acc), B, L // 2, H, d, int(block_size), int(mode),
+                                _ptr_or_null(dq_acc), B, n, H, d, int(block_size), int(mode),
                                 _stream_ptr(q))
     _check("dfa_fwd_main", rc)
 
 
-def dfa_bwd_preprocess(out, dout, delta, dq_acc):
+def dfa_bwd_preprocess(out, dout, delta, dq_acc, mode=MODE_DIFFUSION):
     """Step 1 of the backward: delta = rowsum(dout * out); dq_acc = 0 unless None."""
     _check_qkv(out, dout)
-    B, L, H, d = out.shape
+    B, n, L = _step_shape(out, mode)
+    H, d = out.shape[2], out.shape[3]
+    _check_scratch(out, None, delta, dq_acc)
     with torch.cuda.device(out.device):
-        rc = lib().dfa_bwd_preprocess(_ptr(out), _ptr(dout), _ptr(delta), _ptr_or_null(dq_acc),
-                                      B, L // 2, H, d, _stream_ptr(out))
-    _check("dfa_bwd_preprocess", rc)
+        rc = lib().dfa_bwd_preprocess_ex(_ptr(out), _ptr(dout), _ptr(delta),
+                                         _ptr_or_null(dq_acc), B, n, H, d, int(mode),
+                                         _stream_ptr(out))
+    _check("dfa_bwd_preprocess_ex", rc)
 
 
 def dfa_bwd_main(q, k, v, dout, lse, delta, dq_acc, dk, dv, block_size, mode=MODE_DIFFUSION):
     """Step 2 of the backward: the tensor-core kernel (dk, dv, dq_acc += dq)."""
     _check_qkv(q, k, v, dout, dk, dv)
-    B, L, H, d = q.shape
+    B, n, L = _step_shape(q, mode)
+    H, d = q.shape[2], q.shape[3]
+    _check_scratch(q, lse, delta, dq_acc)
     with torch.cuda.device(q.device):
         rc = lib().dfa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(delta),
-                                _ptr(dq_acc), _ptr(dk), _ptr(dv), B, L // 2, H, d,
+                                _ptr(dq_acc), _ptr(dk), _ptr(dv), B, n, H, d,
                                 int(block_size), int(mode), _stream_ptr(q))
     _check("dfa_bwd_main", rc)
 
@@ -431,10 +510,12 @@ def dfa_bwd_main(q, k, v, dout, lse, delta, dq_acc, dk, dv, block_size, mode=MOD
 def dfa_fwd_main_gqa(q, k, v, out, lse, dq_acc, block_size, mode=MODE_DIFFUSION):
     """dfa_fwd_main with k, v of fewer heads (grouped key/value heads)."""
     Hk = _check_grouped(q, k, v, out)
-    B, L, H, d = q.shape
+    B, n, L = _step_shape(q, mode)
+    H, d = q.shape[2], q.shape[3]
+    _check_scratch(q, lse, None, dq_acc)
     with torch.cuda.device(q.device):
         rc = lib().dfa_fwd_main_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                                    _ptr_or_null(dq_acc), B, L // 2, H, Hk, d, int(block_size),
+                                    _ptr_or_null(dq_acc), B, n, H, Hk, d, int(block_size),
                                     int(mode), _stream_ptr(q))
     _check("dfa_fwd_main_gqa", rc)
 
@@ -442,22 +523,28 @@ def dfa_fwd_main_gqa(q, k, v, out, lse, dq_acc, block_size, mode=MODE_DIFFUSION)
 def dfa_bwd_main_gqa(q, k, v, dout, lse, delta, dq_acc, dk, dv, block_size, mode=MODE_DIFFUSION):
     """dfa_bwd_main with k, v, dk, dv of fewer heads (grouped key/value heads)."""
     Hk = _check_grouped(q, k, v, dout)
-    B, L, H, d = q.shape
-    if dk.shape != k.shape or dv.shape != v.shape:
-        raise ValueError("dk, dv must have the shape of k, v")
+    B, n, L = _step_shape(q, mode)
+    H, d = q.shape[2], q.shape[3]
+    _check_scratch(q, lse, delta, dq_acc)
+    _check_buf(dk, k.shape, torch.bfloat16, q.device, "dk")
+    _check_buf(dv, v.shape, torch.bfloat16, q.device, "dv")
     with torch.cuda.device(q.device):
         rc = lib().dfa_bwd_main_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse),
-                                    _ptr(delta), _ptr(dq_acc), _ptr(dk), _ptr(dv), B, L // 2, H,
+                                    _ptr(delta), _ptr(dq_acc), _ptr(dk), _ptr(dv), B, n, H,
                                     Hk, d, int(block_size), int(mode), _stream_ptr(q))
     _check("dfa_bwd_main_gqa", rc)
 
 
-def dfa_bwd_dq_convert(dq_acc, dq):
+def dfa_bwd_dq_convert(dq_acc, dq, mode=MODE_DIFFUSION):
     """Step 3 of the backward: dq = bf16(dq_acc)."""
-    B, L, H, d = dq.shape
+    _check_qkv(dq)
+    B, n, L = _step_shape(dq, mode)
+    H, d = dq.shape[2], dq.shape[3]
+    _check_scratch(dq, None, None, dq_acc)
     with torch.cuda.device(dq.device):
-        rc = lib().dfa_bwd_dq_convert(_ptr(dq_acc), _ptr(dq), B, L // 2, H, d, _stream_ptr(dq))
-    _check("dfa_bwd_dq_convert", rc)
+        rc = lib().dfa_bwd_dq_convert_ex(_ptr(dq_acc), _ptr(dq), B, n, H, d, int(mode),
+                                         _stream_ptr(dq))
+    _check("dfa_bwd_dq_convert_ex", rc)
 
 
 def dfa_selftest_wait_timeout(limit_us=20000):

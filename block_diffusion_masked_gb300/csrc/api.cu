@@ -30,6 +30,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;
   bool supported = false;
+  unsigned long long ctx_id = 0;  // context the addresses below belong to
   unsigned* status = nullptr;
   unsigned* sched = nullptr;  // kSchedSlots slots of 8 words
   long long l2_bytes = 0;
@@ -48,15 +49,63 @@ int cuda_fail(cudaError_t e) {
   return DFA_ECUDA;
 }
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
 
-// Per-device set-up on first use: check the architecture (the library holds
-// sm_103a code only) and find the device address of the status word.
+// Driver entry points, resolved once (caller holds g_mu).
+bool resolve_driver() {
+  if (g_encode && g_ctx_current && g_ctx_get_id) return true;
+  auto get = [](const char* name, int version, void** fn) {
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion(name, fn, version, cudaEnableDefault, &q) ==
+               cudaSuccess &&
+           q == cudaDriverEntryPointSuccess && *fn != nullptr;
+  };
+  void* a = nullptr;
+  void* b = nullptr;
+  void* c = nullptr;
+  if (!get("cuTensorMapEncodeTiled", 12000, &a) || !get("cuCtxGetCurrent", 4000, &b) ||
+      !get("cuCtxGetId", 12000, &c))
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(a);
+  g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(b);
+  g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(c);
+  return true;
+}
+
+// Process-unique id of the calling thread's current context, 0 if there is
+// none yet.  cudaDeviceReset destroys a device's primary context; the one
+// the runtime creates next has a new id, and device addresses looked up in
+// the old one are stale.
+unsigned long long ctx_id_now() {
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!g_ctx_current || g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (!g_ctx_get_id || g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Per-device set-up on first use, and again whenever the device's context
+// has changed: check the architecture (the library holds sm_103a code only)
+// and find the device addresses of the status word and the work counters.
 int device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DFA_ECUDA;
   if (dev < 0 || dev >= kMaxDevices) return DFA_EUNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
+  if (!resolve_driver()) return DFA_ECUDA;
   DeviceState& s = g_dev[dev];
+  if (s.ready && s.supported) {
+    // The context may not be current on this thread yet: a symbol lookup
+    // makes the runtime bind its primary context.
+    unsigned long long id = ctx_id_now();
+    if (id == 0) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_dfa_status) != cudaSuccess) return DFA_ECUDA;
+      id = ctx_id_now();
+    }
+    if (id != s.ctx_id) s = DeviceState();  // a new context: set up again
+  }
   if (!s.ready) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -72,15 +121,7 @@ int device_state(DeviceState** out) {
       s.status = static_cast<unsigned*>(addr);
       if (cudaGetSymbolAddress(&addr, g_dfa_sched) != cudaSuccess) return DFA_ECUDA;
       s.sched = static_cast<unsigned*>(addr);
-    }
-    if (!g_encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return DFA_ECUDA;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      s.ctx_id = ctx_id_now();
     }
     s.ready = true;
   }
@@ -113,20 +154,22 @@ unsigned* sched_for_stream(DeviceState* s, cudaStream_t stream) {
   return s->sched + 8 * i;
 }
 
-// View a (B, 2n, H, d) bf16 tensor as 5-D (d, H, n, half, B) -- strides
-// increasing -- and load boxes of (64, 1, rows, 1, 1) with 128-byte swizzle:
-// `rows` consecutive positions of one half of one head, 64 head dims each.
-// Rows past the end of a half read zero.
-int make_map(CUtensorMap* map, const void* base, int B, int n, int H, int d, int rows,
+// View a bf16 tensor of `halves` consecutive halves of n rows, (halves * n,
+// H, d), as 5-D (d, H, n, halves, 1) -- strides increasing -- and load boxes
+// of (64, 1, rows, 1, 1) with 128-byte swizzle: `rows` consecutive positions
+// of one half of one head, 64 head dims each.  Rows past the end of a half
+// read zero.  A (B, 2n, H, d) diffusion tensor has 2B halves (sample b's are
+// 2b and 2b + 1); a causal (Bc, n, H, d) tensor has Bc, one per sequence.
+int make_map(CUtensorMap* map, const void* base, long long halves, int n, int H, int d, int rows,
              bool packed = false) {
   // packed (varlen): n is the number of rows of the packed tensor, viewed as
   // (d, H, rows, 1, 1)
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
-                              static_cast<cuuint64_t>(n), packed ? 1u : 2u,
-                              packed ? 1u : static_cast<cuuint64_t>(B)};
+                              static_cast<cuuint64_t>(n),
+                              packed ? 1u : static_cast<cuuint64_t>(halves), 1u};
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(H) * d * 2;
   const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * 2, row_bytes, row_bytes * n,
-                                 row_bytes * n * (packed ? 1 : 2)};
+                                 row_bytes * n * (packed ? 1 : static_cast<cuuint64_t>(halves))};
   const cuuint32_t box[5] = {64, 1, static_cast<cuuint32_t>(rows), 1, 1};
   const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
@@ -137,14 +180,14 @@ int make_map(CUtensorMap* map, const void* base, int B, int n, int H, int d, int
 }
 
 // An e4m3 (one byte per element) (B, 2n, H, d) tensor as 5-D (d, H, n,
-// half, B) with boxes of (128, 1, rows, 1, 1), 128-byte swizzle: rows of
+// 2B, 1) with boxes of (128, 1, rows, 1, 1), 128-byte swizzle: rows of
 // 128 head dims, the same 128-byte rows as the bf16 maps' 64.
 int make_map_u8(CUtensorMap* map, const void* base, int B, int n, int H, int d, int rows) {
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
-                              static_cast<cuuint64_t>(n), 2, static_cast<cuuint64_t>(B)};
+                              static_cast<cuuint64_t>(n), 2 * static_cast<cuuint64_t>(B), 1};
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(H) * d;
   const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d), row_bytes, row_bytes * n,
-                                 row_bytes * 2 * n};
+                                 row_bytes * 2 * n * B};
   const cuuint32_t box[5] = {128, 1, static_cast<cuuint32_t>(rows), 1, 1};
   const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims,
@@ -171,18 +214,18 @@ int make_map_vt(CUtensorMap* map, const void* base, int B, int n, int n_pad, int
   return r == CUDA_SUCCESS ? DFA_OK : DFA_ECUDA;
 }
 
-// The float32 dQ accumulator (B, 2n, H, d) as 5-D (d, H, n, half, B) with
-// boxes of (32, 1, rows, 1, 1), no swizzle: the target of the backward's
-// bulk reduce-add of one warp's part of a query tile's dQ (rows past the
-// end of a half are skipped by the copy engine).
-int make_map_f32(CUtensorMap* map, const void* base, int B, int n, int H, int d, int rows,
-                 bool packed = false) {
+// The float32 dQ accumulator, laid out as q, as 5-D (d, H, n, halves, 1)
+// with boxes of (32, 1, rows, 1, 1), no swizzle: the target of the
+// backward's bulk reduce-add of one warp's part of a query tile's dQ (rows
+// past the end of a half are skipped by the copy engine).
+int make_map_f32(CUtensorMap* map, const void* base, long long halves, int n, int H, int d,
+                 int rows, bool packed = false) {
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
-                              static_cast<cuuint64_t>(n), packed ? 1u : 2u,
-                              packed ? 1u : static_cast<cuuint64_t>(B)};
+                              static_cast<cuuint64_t>(n),
+                              packed ? 1u : static_cast<cuuint64_t>(halves), 1u};
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(H) * d * 4;
   const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * 4, row_bytes, row_bytes * n,
-                                 row_bytes * n * (packed ? 1 : 2)};
+                                 row_bytes * n * (packed ? 1 : static_cast<cuuint64_t>(halves))};
   const cuuint32_t box[5] = {32, 1, static_cast<cuuint32_t>(rows), 1, 1};
   const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<void*>(base), dims,
@@ -221,11 +264,13 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   if ((rc = device_state(&ds))) return rc;
   TileShape ts;
   tile_shape_for(d, &ts);
+  // Diffusion: B samples of two halves; causal: B sequences of n rows.
+  const long long halves = launch_halves(mode, B);
   FwdParams p{};
-  if ((rc = make_map(&p.tm_q, q, B, n, H, d, ts.fwd_bm))) return rc;
-  if ((rc = make_map(&p.tm_k, k, B, n, Hk, d, ts.fwd_bn))) return rc;
-  if ((rc = make_map(&p.tm_v, v, B, n, Hk, d, ts.fwd_bn))) return rc;
-  if ((rc = make_map(&p.tm_o, out, B, n, H, d, ts.fwd_bm))) return rc;
+  if ((rc = make_map(&p.tm_q, q, halves, n, H, d, ts.fwd_bm))) return rc;
+  if ((rc = make_map(&p.tm_k, k, halves, n, Hk, d, ts.fwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_v, v, halves, n, Hk, d, ts.fwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_o, out, halves, n, H, d, ts.fwd_bm))) return rc;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.status = ds->status;
@@ -236,13 +281,13 @@ int forward_impl(int mode, const void* q, const void* k, const void* v, void* ou
   p.bs = bs < n ? bs : n;
   p.mode = mode;
   p.q_tiles = cdiv(n, ts.fwd_bm);
-  // q, k, v and out of one (batch, head)
-  p.group = l2_group(8LL * 2 * n * d, ds->l2_bytes, B * H);
+  // q, k, v and out of one (batch, head), or of one (sequence, head)
+  p.group = l2_group(8LL * (mode == MODE_CAUSAL ? 1 : 2) * n * d, ds->l2_bytes, B * H);
   p.sched = sched_for_stream(ds, stream);
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   p.zero_dst = reinterpret_cast<float4*>(dq_acc);
-  // B * 2n * H * d floats, d a multiple of 64: whole 16-byte groups
-  p.zero_groups = dq_acc ? static_cast<long long>(B) * 2 * n * H * d / 4 : 0;
+  // halves * n * H * d floats, d a multiple of 64: whole 16-byte groups
+  p.zero_groups = dq_acc ? halves * n * H * d / 4 : 0;
   const cudaError_t e = launch_forward(p, d, stream);
   return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
@@ -280,7 +325,7 @@ int forward_fp8_impl(const void* q, const void* k, const void* v, void* out, flo
   FwdParams p{};
   if ((rc = make_map_u8(&p.tm_q, q, B, n, H, d, ts.fwd_bm))) return rc;
   if ((rc = make_map_u8(&p.tm_k, k, B, n, Hk, d, ts.fwd_bn))) return rc;
-  if ((rc = make_map(&p.tm_o, out, B, n, H, d, ts.fwd_bm))) return rc;
+  if ((rc = make_map(&p.tm_o, out, 2LL * B, n, H, d, ts.fwd_bm))) return rc;
   if (vt_in) {
     if ((rc = make_map_vt(&p.tm_v, vt_in, B, n, n_pad, Hk))) return rc;
   } else {
@@ -337,12 +382,13 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   if ((rc = device_state(&ds))) return rc;
   TileShape ts;
   tile_shape_for(d, &ts);
+  const long long halves = launch_halves(mode, B);
   BwdParams p{};
-  if ((rc = make_map(&p.tm_q, q, B, n, H, d, ts.bwd_bm))) return rc;
-  if ((rc = make_map(&p.tm_do, dout, B, n, H, d, ts.bwd_bm))) return rc;
-  if ((rc = make_map(&p.tm_k, k, B, n, Hk, d, ts.bwd_bn))) return rc;
-  if ((rc = make_map(&p.tm_v, v, B, n, Hk, d, ts.bwd_bn))) return rc;
-  if (d == 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, B, n, H, d,
+  if ((rc = make_map(&p.tm_q, q, halves, n, H, d, ts.bwd_bm))) return rc;
+  if ((rc = make_map(&p.tm_do, dout, halves, n, H, d, ts.bwd_bm))) return rc;
+  if ((rc = make_map(&p.tm_k, k, halves, n, Hk, d, ts.bwd_bn))) return rc;
+  if ((rc = make_map(&p.tm_v, v, halves, n, Hk, d, ts.bwd_bn))) return rc;
+  if (d == 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, halves, n, H, d,
                                       ts.bwd_bm / kBwd2WarpgroupsD128)))
     return rc;
   p.lse = lse;
@@ -359,22 +405,32 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   p.bs = bs < n ? bs : n;
   p.mode = mode;
   p.k_tiles = cdiv(n, ts.bwd_bn);
-  // per (batch, key/value head): k, v (bf16) and, for each of its G query
-  // heads, q, dout (bf16) and the float32 dq accumulator
-  p.group = l2_group((4LL + 8LL * G) * 2 * n * d, ds->l2_bytes, B * Hk);
+  // per (batch, key/value head), or (sequence, key/value head): k, v (bf16)
+  // and, for each of its G query heads, q, dout (bf16) and the float32 dq
+  // accumulator
+  p.group = l2_group((4LL + 8LL * G) * (mode == MODE_CAUSAL ? 1 : 2) * n * d, ds->l2_bytes,
+                     B * Hk);
   p.sched = sched_for_stream(ds, stream);
   p.items = 0;  // set by the launcher
   p.dq_sem = dq_sem;
-  p.sem_rows = B * 2 * n;
+  p.sem_rows = static_cast<int>(halves * n);
   p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   const cudaError_t e = launch_backward(p, d, stream);
   return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
 
-int preprocess_impl(const void* out, const void* dout, float* delta, float* dq_acc, int B, int n,
-                    int H, int d, cudaStream_t stream) {
-  int rc = check_common(B, n, H, d, 1);
+// delta = rowsum(dout * out) over B groups of `rows` rows, laid out (B, H,
+// rows): rows = 2n for diffusion samples, n for causal sequences.
+int check_rows(int B, int rows, int H, int d) {
+  if (B < 0 || rows < 1 || rows > (1 << 30) || H < 1) return DFA_EINVAL;
+  if (d != 64 && d != 128 && d != 256) return DFA_EUNSUPPORTED;
+  return DFA_OK;
+}
+
+int preprocess_impl(const void* out, const void* dout, float* delta, float* dq_acc, int B,
+                    int rows, int H, int d, cudaStream_t stream) {
+  int rc = check_rows(B, rows, H, d);
   if (rc) return rc;
   if (B == 0) return DFA_OK;
   if (!aligned_all({out, dout}) || (dq_acc && !aligned16(dq_acc)) || !delta ||
@@ -384,19 +440,21 @@ int preprocess_impl(const void* out, const void* dout, float* delta, float* dq_a
   if ((rc = device_state(&ds))) return rc;
   const cudaError_t e =
       launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(out),
-                            static_cast<const __nv_bfloat16*>(dout), delta, dq_acc, B, 2 * n, H, d,
+                            static_cast<const __nv_bfloat16*>(dout), delta, dq_acc, B, rows, H, d,
                             stream);
   return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
 
-int convert_impl(const float* dq_acc, void* dq, int B, int n, int H, int d, cudaStream_t stream) {
-  int rc = check_common(B, n, H, d, 1);
+// dq = bf16(dq_acc) over B groups of `rows` rows of H * d elements.
+int convert_impl(const float* dq_acc, void* dq, int B, int rows, int H, int d,
+                 cudaStream_t stream) {
+  int rc = check_rows(B, rows, H, d);
   if (rc) return rc;
   if (B == 0) return DFA_OK;
   if (!aligned_all({dq_acc, dq})) return DFA_EINVAL;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds))) return rc;
-  const long long elems = static_cast<long long>(B) * 2 * n * H * d;
+  const long long elems = static_cast<long long>(B) * rows * H * d;
   const cudaError_t e = launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), elems, stream);
   return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
@@ -427,7 +485,8 @@ int backward_impl(int mode, const void* q, const void* k, const void* v, const v
     return DFA_EINVAL;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds))) return rc;
-  const size_t L = 2 * static_cast<size_t>(n);
+  // rows per sample (two halves) or, causal, per sequence
+  const int L = mode == MODE_CAUSAL ? n : 2 * n;
   const size_t elems = static_cast<size_t>(B) * L * H * d;
   const size_t rows = static_cast<size_t>(B) * H * L;
   float* dq_acc = nullptr;
@@ -446,11 +505,11 @@ int backward_impl(int mode, const void* q, const void* k, const void* v, const v
     cudaFreeAsync(dq_acc, stream);
     return rc;
   }
-  rc = preprocess_impl(out, dout, delta, dq_acc, B, n, H, d, stream);
+  rc = preprocess_impl(out, dout, delta, dq_acc, B, L, H, d, stream);
   if (!rc)
     rc = bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, Hk, d, bs, stream,
                        sem);
-  if (!rc) rc = convert_impl(dq_acc, dq, B, n, H, d, stream);
+  if (!rc) rc = convert_impl(dq_acc, dq, B, L, H, d, stream);
   if (sem) cudaFreeAsync(sem, stream);
   cudaFreeAsync(delta, stream);
   cudaFreeAsync(dq_acc, stream);
@@ -678,6 +737,20 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
 }
 
 }  // namespace
+
+// For the other translation units of the library (see params.cuh).
+int check_device(unsigned long long* ctx_id) {
+  DeviceState* ds = nullptr;
+  const int rc = device_state(&ds);
+  if (rc) return rc;
+  if (ctx_id) *ctx_id = ds->ctx_id;
+  return DFA_OK;
+}
+
+int record_cuda_failure(cudaError_t e) { return cuda_fail(e); }
+
+int check_backward_args(int B, int n, int H, int d, int bs) { return check_common(B, n, H, d, bs); }
+
 }  // namespace dfa
 
 using namespace dfa;
@@ -726,11 +799,6 @@ int dfa_backward_gqa(const void* q, const void* k, const void* v, const void* ou
                        kv_heads, headdim, block_size, static_cast<cudaStream_t>(stream));
 }
 
-// Causal attention on (batch, seqlen, heads, headdim).  A contiguous tensor of
-// that shape is, byte for byte, a (batch/2, 2*seqlen, heads, headdim) tensor
-// whose halves are consecutive sequences, so the diffusion kernels run it in
-// their causal mode (each half attends causally to itself).  batch must be
-// even, as it is for the yardstick on the 2B halves of B samples.
 int dfa_forward_varlen(const void* q, const void* k, const void* v, void* out, float* lse,
                        const int* cu_seqlens, int batch, int heads, int kv_heads, int headdim,
                        int block_size, dfa_stream_t stream) {
@@ -796,11 +864,13 @@ int dfa_backward_ex(const void* q, const void* k, const void* v, const void* out
                        kv_heads, headdim, block_size, s, det);
 }
 
+// Causal attention on (batch, seqlen, heads, headdim): the diffusion kernels
+// in their causal mode, every sequence one "half" of seqlen rows that
+// attends causally to itself.
 int dfa_causal_forward(const void* q, const void* k, const void* v, void* out, float* lse,
                        int batch, int seqlen, int heads, int headdim, dfa_stream_t stream) {
   if (batch < 0 || seqlen < 1) return DFA_EINVAL;
-  if (batch % 2) return DFA_EINVAL;
-  return forward_impl(MODE_CAUSAL, q, k, v, out, lse, nullptr, batch / 2, seqlen, heads, heads,
+  return forward_impl(MODE_CAUSAL, q, k, v, out, lse, nullptr, batch, seqlen, heads, heads,
                       headdim, 1, static_cast<cudaStream_t>(stream));
 }
 
@@ -808,8 +878,7 @@ int dfa_causal_backward(const void* q, const void* k, const void* v, const void*
                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
                         int batch, int seqlen, int heads, int headdim, dfa_stream_t stream) {
   if (batch < 0 || seqlen < 1) return DFA_EINVAL;
-  if (batch % 2) return DFA_EINVAL;
-  return backward_impl(MODE_CAUSAL, q, k, v, out, dout, lse, dq, dk, dv, batch / 2, seqlen, heads,
+  return backward_impl(MODE_CAUSAL, q, k, v, out, dout, lse, dq, dk, dv, batch, seqlen, heads,
                        heads, headdim, 1, static_cast<cudaStream_t>(stream));
 }
 
@@ -841,8 +910,18 @@ int dfa_bwd_main_gqa(const void* q, const void* k, const void* v, const void* do
 
 int dfa_bwd_preprocess(const void* out, const void* dout, float* delta, float* dq_acc, int batch,
                        int n, int heads, int headdim, dfa_stream_t stream) {
-  return preprocess_impl(out, dout, delta, dq_acc, batch, n, heads, headdim,
+  if (n < 1 || n > (1 << 29)) return DFA_EINVAL;
+  return preprocess_impl(out, dout, delta, dq_acc, batch, 2 * n, heads, headdim,
                          static_cast<cudaStream_t>(stream));
+}
+
+int dfa_bwd_preprocess_ex(const void* out, const void* dout, float* delta, float* dq_acc,
+                          int batch, int n, int heads, int headdim, int mode,
+                          dfa_stream_t stream) {
+  if (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) return DFA_EINVAL;
+  if (n < 1 || n > (1 << 29)) return DFA_EINVAL;
+  return preprocess_impl(out, dout, delta, dq_acc, batch, mode == MODE_CAUSAL ? n : 2 * n, heads,
+                         headdim, static_cast<cudaStream_t>(stream));
 }
 
 int dfa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse,
@@ -856,7 +935,16 @@ int dfa_bwd_main(const void* q, const void* k, const void* v, const void* dout, 
 
 int dfa_bwd_dq_convert(const float* dq_acc, void* dq, int batch, int n, int heads, int headdim,
                        dfa_stream_t stream) {
-  return convert_impl(dq_acc, dq, batch, n, heads, headdim, static_cast<cudaStream_t>(stream));
+  if (n < 1 || n > (1 << 29)) return DFA_EINVAL;
+  return convert_impl(dq_acc, dq, batch, 2 * n, heads, headdim, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_bwd_dq_convert_ex(const float* dq_acc, void* dq, int batch, int n, int heads,
+                          int headdim, int mode, dfa_stream_t stream) {
+  if (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) return DFA_EINVAL;
+  if (n < 1 || n > (1 << 29)) return DFA_EINVAL;
+  return convert_impl(dq_acc, dq, batch, mode == MODE_CAUSAL ? n : 2 * n, heads, headdim,
+                      static_cast<cudaStream_t>(stream));
 }
 
 int dfa_selftest_wait_timeout(int limit_us, dfa_stream_t stream) {
@@ -949,7 +1037,7 @@ int dfa_work_item(int pass, int mode, int w, int batch, int heads, int tiles, in
   if ((pass != 0 && pass != 1) || (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) || batch < 1 ||
       heads < 1 || tiles < 1 || group < 1 || !item)
     return DFA_EINVAL;
-  const long long items = 2LL * batch * heads * tiles;
+  const long long items = pass_items(mode, batch, heads, tiles);
   if (items > 0x7fffffffLL || w < 0 || w >= items) return DFA_EINVAL;
   const WorkItem it = pass == 0 ? fwd_work(w, mode, batch, heads, tiles, group)
                                 : bwd_work(w, mode, batch, heads, tiles, group);

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
   // ITEMFULL[s] (release), read by the other roles after their wait (acquire).
   auto ring = [&](int s) { return reinterpret_cast<BwdItem*>(smem + C::kOffItem + 128 * s); };
   const AbortFlag ab{abort_flag, p.status};
-  const size_t L = 2 * static_cast<size_t>(p.n);
+  const size_t L = 2 * static_cast<size_t>(p.n);  // rows of one sample (two halves)
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
 
   if (threadIdx.x == 0) {
@@ -244,22 +244,19 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       const int qt = it.ltile(l);
       const int half = it.lhalf(l);
       const int h = it.h0 + hh;  // query head
-      // delta (and, varlen, lse): (batch, heads, 2n) or, varlen, (heads, rows)
-      const float* del_bh = VARLEN ? p.delta + static_cast<size_t>(h) * p.rows + it.row0
-                                   : p.delta + (static_cast<size_t>(it.wi.b) * p.H + h) * L;
+      // lse and delta: laid out alike, (batch, heads, 2n) (causal:
+      // (sequences, heads, n)) or, varlen, (heads, rows)
       float lse_r[kPerLane], del_r[kPerLane];
 #pragma unroll
       for (int e = 0; e < kPerLane; ++e) {
         const int q = qt * BMQ + lane + 32 * e;
         const bool valid = q < it.n;
-        const size_t pos = static_cast<size_t>(half) * it.n + q;
-        const float lse =
-            !valid  ? 0.f
-            : VARLEN ? p.lse[static_cast<size_t>(h) * p.rows + it.row0 + pos]
-                     : p.lse[lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n)];
-        lse_r[e] = valid ? lse * -1.4426950408889634f : -INFINITY;
+        const long long off =
+            VARLEN ? static_cast<long long>(h) * p.rows + it.row0 + static_cast<long long>(half) * it.n + q
+                   : lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n);
+        lse_r[e] = valid ? p.lse[off] * -1.4426950408889634f : -INFINITY;
         // -D * scale: the softmax scale is folded into dS (see the compute)
-        del_r[e] = valid ? -del_bh[pos] * p.scale : 0.f;
+        del_r[e] = valid ? -p.delta[off] * p.scale : 0.f;
       }
       const int st = gg % STAGES;
       const int round = gg / STAGES;
@@ -695,7 +692,7 @@ static cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long items = VARLEN ? p.units : 2LL * p.B * p.Hk * p.k_tiles;
+  const long long items = VARLEN ? p.units : pass_items(p.mode, p.B, p.Hk, p.k_tiles);
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;

@@ -282,23 +282,19 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       const int qt = it.ltile(l);
       const int half = it.lhalf(l);
       const int h = it.h0 + hh;  // query head
-      // delta (and, varlen, lse): (batch, heads, 2n) or, varlen, (heads, rows)
-      const size_t L = 2 * static_cast<size_t>(p.n);
-      const float* del_bh = VARLEN ? p.delta + static_cast<size_t>(h) * p.rows + it.row0
-                                   : p.delta + (static_cast<size_t>(it.wi.b) * p.H + h) * L;
+      // lse and delta: laid out alike, (batch, heads, 2n) (causal:
+      // (sequences, heads, n)) or, varlen, (heads, rows)
       float lse_r[2], del_r[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int q = qt * BMQ + lane + 32 * e;
         const bool valid = q < it.n;
-        const size_t pos = static_cast<size_t>(half) * it.n + q;
-        const float lse =
-            !valid  ? 0.f
-            : VARLEN ? p.lse[static_cast<size_t>(h) * p.rows + it.row0 + pos]
-                     : p.lse[lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n)];
-        lse_r[e] = valid ? lse * -1.4426950408889634f : -INFINITY;
+        const long long off =
+            VARLEN ? static_cast<long long>(h) * p.rows + it.row0 + static_cast<long long>(half) * it.n + q
+                   : lse_offset(p.mode, it.wi.b, h, half, q, p.H, p.n);
+        lse_r[e] = valid ? p.lse[off] * -1.4426950408889634f : -INFINITY;
         // -D * scale: the softmax scale is folded into dS (see the compute)
-        del_r[e] = valid ? -del_bh[pos] * p.scale : 0.f;
+        del_r[e] = valid ? -p.delta[off] * p.scale : 0.f;
       }
       const int st = gg % STAGES;
       const int round = gg / STAGES;
@@ -759,7 +755,7 @@ static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
   if (fa.numRegs * C::kThreads < C::kRegCtl * 128 + C::kRegCompute * 128 * C::NWG)
     return cudaErrorInvalidConfiguration;
   const long long items =
-      (VARLEN ? static_cast<long long>(p.units) : 2LL * p.B * p.Hk * p.k_tiles) * C::NDH;
+      (VARLEN ? static_cast<long long>(p.units) : pass_items(p.mode, p.B, p.Hk, p.k_tiles)) * C::NDH;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;

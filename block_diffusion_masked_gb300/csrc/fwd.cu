@@ -382,7 +382,7 @@ static cudaError_t launch_fwd_impl(const FwdParams& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long blocks = VARLEN ? p.items : 2LL * p.B * p.H * p.q_tiles;
+  const long long blocks = VARLEN ? p.items : pass_items(p.mode, p.B, p.H, p.q_tiles);
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   return launch_chained(kern, dim3(static_cast<unsigned>(blocks)), dim3(C::kThreads),

@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   // ITEMFULL[s] (release), read by the other roles after their wait (acquire).
   auto ring = [&](int s) { return reinterpret_cast<ItemGeom*>(smem + C::kOffItem + 64 * s); };
   const AbortFlag ab{abort_flag, p.status};
-  const int num_items = VARLEN ? p.items : 2 * p.B * p.H * p.q_tiles;
+  const int num_items = VARLEN ? p.items : static_cast<int>(pass_items(p.mode, p.B, p.H, p.q_tiles));
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
 
   if (threadIdx.x == 0) {
@@ -219,9 +219,10 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         mbar_arrive_expect_tx(BAR(C::BAR_VFULL + st), C::kKVBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          if constexpr (FP8)  // V^T (n, half, headdim, heads, batch): keys innermost
+          if constexpr (FP8)  // V^T (n, half, headdim, heads, batch): keys innermost;
+                              // vc3 = 2 * batch + half (batched coordinates)
             tma_load_5d(sbase + C::kOffV + st * C::kKVBytes, &p.tm_v, BAR(C::BAR_VFULL + st), vc2,
-                        vc3, 0, vh, vc4);
+                        vc3 & 1, 0, vh, vc3 >> 1);
           else
             tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
                         BAR(C::BAR_VFULL + st), C::kChunkElems * c, vh, vc2, vc3, vc4);
@@ -648,7 +649,7 @@ static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long items = VARLEN ? p.items : 2LL * p.B * p.H * p.q_tiles;
+  const long long items = VARLEN ? p.items : pass_items(p.mode, p.B, p.H, p.q_tiles);
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;

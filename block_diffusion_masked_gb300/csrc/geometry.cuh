@@ -145,13 +145,26 @@ DFA_HD int dq_ordinal(int mode, int n, int bs, int bm, int bn, int q_half, int q
   return (s[0].t_end - s[0].t_begin) + kt - s[1].t_begin;
 }
 
-// Offset of the log-sum-exp of row r of half `half` of sample b, head h.
-// Diffusion mode: lse is (B, H, 2n).  Causal mode: the sample is a pair of
-// consecutive sequences (2b, 2b+1) of length n and lse is (2B, H, n).
+// Offset of the log-sum-exp (and of D = rowsum(dO * O), laid out alike) of
+// row r of half `half` of sample b, head h.  Diffusion mode: lse is
+// (B, H, 2n).  Causal mode: sequence s of length n is half s % 2 of
+// "sample" s / 2 (so that its rows start at (2b + half) * n as a half's
+// do), and lse is (sequences, H, n).
 DFA_HD long long lse_offset(int mode, int b, int h, int half, int r, int H, int n) {
   if (mode == MODE_CAUSAL)
     return ((2LL * b + half) * H + h) * static_cast<long long>(n) + r;
   return (static_cast<long long>(b) * H + h) * (2LL * n) + static_cast<long long>(half) * n + r;
+}
+
+// Halves of a batched launch: every sample has two (noisy, clean); in the
+// causal mode B counts sequences, each one "half".
+DFA_HD long long launch_halves(int mode, int B) {
+  return mode == MODE_CAUSAL ? static_cast<long long>(B) : 2LL * B;
+}
+
+// Work items of a batched pass over `tiles` tiles per half.
+DFA_HD long long pass_items(int mode, int B, int H, int tiles) {
+  return launch_halves(mode, B) * H * tiles;
 }
 
 // Work decoding.  An item's "rank" orders the items of one (batch, head)
@@ -168,8 +181,10 @@ DFA_HD long long lse_offset(int mode, int b, int h, int half, int r, int H, int 
 // half form the tail.  Backward: key tiles; in the diffusion mode the clean
 // key tiles (seen by clean and noisy queries) in increasing index, then the
 // noisy key tiles (seen only by their own noisy blocks), which form the
-// tail; in the causal mode key tiles in increasing index, halves side by
-// side, the last two tiles of each half forming the tail.
+// tail; in the causal mode key tiles in increasing index.  In the causal
+// mode B counts sequences and the (sequence, head) pairs take the place of
+// the (batch, head) pairs, one half each; the last two tiles of each
+// sequence form the tail.
 struct WorkItem {
   int b, h, half, tile;
 };
@@ -199,19 +214,36 @@ DFA_HD void work_split(int w, int BH, int group, int ranks, int tail, int* rank,
   *bh = static_cast<int>(t % BH);
 }
 
+// Ranks per (batch, head) pair, or per (sequence, head) pair in the causal
+// mode, and how many of them form the tail.
+DFA_HD int pass_ranks(int mode, int tiles) { return mode == MODE_CAUSAL ? tiles : 2 * tiles; }
+
 DFA_HD int fwd_tail_ranks(int mode, int tiles) {
-  (void)mode;
-  return imin(2 * tiles, 4);
+  return mode == MODE_CAUSAL ? imin(tiles, 2) : imin(2 * tiles, 4);
 }
 
 DFA_HD int bwd_tail_ranks(int mode, int tiles) {
-  return mode == MODE_CAUSAL ? imin(2 * tiles, 4) : tiles;
+  return mode == MODE_CAUSAL ? imin(tiles, 2) : tiles;
+}
+
+// Causal mode: pair index bh = s * H + h of sequence s -> sample s / 2,
+// half s % 2.
+DFA_HD void causal_split(int bh, int H, WorkItem* it) {
+  const int s = bh / H;
+  it->b = s >> 1;
+  it->half = s & 1;
+  it->h = bh % H;
 }
 
 DFA_HD WorkItem fwd_work(int w, int mode, int B, int H, int tiles, int group) {
   int rank, bh;
-  work_split(w, B * H, group, 2 * tiles, fwd_tail_ranks(mode, tiles), &rank, &bh);
+  work_split(w, B * H, group, pass_ranks(mode, tiles), fwd_tail_ranks(mode, tiles), &rank, &bh);
   WorkItem it;
+  if (mode == MODE_CAUSAL) {
+    it.tile = tiles - 1 - rank;
+    causal_split(bh, H, &it);
+    return it;
+  }
   it.tile = tiles - 1 - (rank >> 1);
   it.half = rank & 1;
   it.b = bh / H;
@@ -221,12 +253,14 @@ DFA_HD WorkItem fwd_work(int w, int mode, int B, int H, int tiles, int group) {
 
 DFA_HD WorkItem bwd_work(int w, int mode, int B, int H, int tiles, int group) {
   int rank, bh;
-  work_split(w, B * H, group, 2 * tiles, bwd_tail_ranks(mode, tiles), &rank, &bh);
+  work_split(w, B * H, group, pass_ranks(mode, tiles), bwd_tail_ranks(mode, tiles), &rank, &bh);
   WorkItem it;
   if (mode == MODE_CAUSAL) {
-    it.tile = rank >> 1;
-    it.half = rank & 1;
-  } else if (rank < tiles) {
+    it.tile = rank;
+    causal_split(bh, H, &it);
+    return it;
+  }
+  if (rank < tiles) {
     it.half = HALF_CLEAN;
     it.tile = rank;
   } else {

@@ -12,13 +12,16 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it (kNoallocScratchBytes) until the process exits.  Host code
 // must not use the array's name as an address (on the host it only names a
-// stand-in); its device address is fetched once per device with
-// cudaGetSymbolAddress, with that device current, on the first call there.
+// stand-in); its device address is fetched with cudaGetSymbolAddress, with
+// the device current, on the first call there, and fetched again if the
+// device's context has been destroyed and re-created since (for instance by
+// cudaDeviceReset), because the old address then belongs to a dead context.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "dfa.h"
+#include "params.cuh"
 
 namespace {
 
@@ -26,8 +29,13 @@ constexpr size_t kNoallocScratchBytes = size_t(32) << 20;  // 32 MiB per device
 constexpr size_t kNoallocScratchFloats = kNoallocScratchBytes / sizeof(float);
 constexpr int kMaxDevices = 64;
 
+struct NoallocSlot {
+  float* ptr = nullptr;
+  unsigned long long ctx_id = 0;  // context `ptr` was looked up in
+};
+
 std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kMaxDevices] = {};
+NoallocSlot g_noalloc[kMaxDevices];
 
 }  // namespace
 
@@ -37,7 +45,10 @@ extern "C" int dfa_backward_noalloc(const void* q, const void* k, const void* v,
                                     const void* dout, const float* lse, void* dq, void* dk,
                                     void* dv, int batch, int n, int heads, int headdim,
                                     int block_size, dfa_stream_t stream) {
-  if (batch < 0 || n < 1 || heads < 1 || headdim < 1 || block_size < 1) return DFA_EINVAL;
+  // The checks of dfa_backward come first, in its order: arguments, then
+  // the device (an unsupported device is DFA_EUNSUPPORTED, as there).
+  int rc = dfa::check_backward_args(batch, n, heads, headdim, block_size);
+  if (rc) return rc;
   if (batch == 0) return DFA_OK;
   // Scratch: dq_acc (batch * 2n * heads * headdim floats), then delta
   // (batch * heads * 2n floats).  headdim is a multiple of 64, so delta
@@ -45,6 +56,8 @@ extern "C" int dfa_backward_noalloc(const void* q, const void* k, const void* v,
   const size_t rows = static_cast<size_t>(batch) * heads * 2 * static_cast<size_t>(n);
   const size_t elems = rows * static_cast<size_t>(headdim);
   if (elems + rows > kNoallocScratchFloats) return DFA_EINVAL;
+  unsigned long long ctx = 0;
+  if ((rc = dfa::check_device(&ctx))) return rc;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DFA_ECUDA;
@@ -52,19 +65,22 @@ extern "C" int dfa_backward_noalloc(const void* q, const void* k, const void* v,
   float* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    NoallocSlot& slot = g_noalloc[dev];
+    if (!slot.ptr || slot.ctx_id != ctx) {
       void* addr = nullptr;
-      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
-        return DFA_ECUDA;
-      g_noalloc_ptr[dev] = static_cast<float*>(addr);
+      const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+      if (e != cudaSuccess) return dfa::record_cuda_failure(e);
+      if (addr == nullptr) return DFA_ECUDA;
+      slot.ptr = static_cast<float*>(addr);
+      slot.ctx_id = ctx;
     }
-    base = g_noalloc_ptr[dev];
+    base = slot.ptr;
   }
   float* dq_acc = base;
   float* delta = base + elems;
   // The preprocess step zeroes dq_acc, so a previous call's contents never
   // leak into this one.
-  int rc = dfa_bwd_preprocess(out, dout, delta, dq_acc, batch, n, heads, headdim, stream);
+  rc = dfa_bwd_preprocess(out, dout, delta, dq_acc, batch, n, heads, headdim, stream);
   if (rc) return rc;
   rc = dfa_bwd_main(q, k, v, dout, lse, delta, dq_acc, dk, dv, batch, n, heads, headdim,
                     block_size, DFA_MODE_DIFFUSION, stream);

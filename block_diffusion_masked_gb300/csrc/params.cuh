@@ -27,8 +27,10 @@ struct VarlenSlot {
 };
 
 // Forward kernel parameters.  Batched: tensor maps view q/k/v as 5-D arrays
-// (headdim, heads, n, half, batch) so that a tile never crosses the
-// noisy/clean boundary and rows past the end of a half read as zeros.
+// (headdim, heads, n, halves, 1), halves = 2 * batch (sample b's noisy half
+// is half 2b, its clean half 2b + 1; in the causal mode every sequence is
+// one half), so that a tile never crosses the noisy/clean boundary and rows
+// past the end of a half read as zeros.
 // Varlen: the same 5-D maps with dims (headdim, heads, rows, 1, 1); rows past
 // the end of a half are the next rows of the packed tensor (finite data the
 // mask hides; only rows past the last sample read as zeros).
@@ -116,7 +118,7 @@ __device__ __forceinline__ int varlen_slot(const VarlenSlot* vl, int slots, int 
 }
 
 // Tensor-map coordinates (c2, c3, c4) of row `base + r` of one half: batched
-// maps are (headdim, heads, n, half, batch), varlen maps
+// maps are (headdim, heads, n, halves, 1), varlen maps
 // (headdim, heads, rows, 1, 1).
 struct HalfRows {
   int base, c3, c4;
@@ -124,7 +126,7 @@ struct HalfRows {
 template <bool VARLEN>
 __device__ __forceinline__ HalfRows half_rows(int b, int half, int n, int row0) {
   if constexpr (VARLEN) return {row0 + half * n, 0, 0};
-  else return {0, half, b};
+  else return {0, 2 * b + half, 0};
 }
 
 // One thread per CTA, after the CTA's last sched_next.
@@ -156,6 +158,17 @@ cudaError_t launch_chained(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
+
+// Host helpers of the C ABI layer (api.cu) for the other translation units.
+// check_device: the per-device set-up and architecture check every entry
+// point runs first (DFA_OK, DFA_EUNSUPPORTED or DFA_ECUDA); *ctx_id receives
+// the id of the device's current context, which changes when the context is
+// destroyed and re-created.  record_cuda_failure: remember a failing CUDA
+// call for dfa_last_cuda_error and return DFA_ECUDA.  check_backward_args:
+// the shape checks of dfa_backward.
+int check_device(unsigned long long* ctx_id);
+int record_cuda_failure(cudaError_t e);
+int check_backward_args(int B, int n, int H, int d, int bs);
 
 // Launchers (one per translation unit).  Return a cudaError_t.
 cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream);

@@ -207,13 +207,13 @@ int dfa_backward_ex(const void *q, const void *k, const void *v, const void *out
 
 /*
  * The yardstick of "Fast Diffusion Attention", section "The right yardstick":
- * causal attention on `batch` independent sequences of length `seqlen`, same
- * layout (batch, seqlen, heads, headdim), lse (batch, heads, seqlen), run by
- * the same kernels with causal tile enumeration.  Viewing a (B, 2n, H, d)
- * tensor as (2B, n, H, d) gives causal attention on the 2B halves.  batch
- * must be even (DFA_EINVAL otherwise): the kernels pair consecutive sequences
- * as the two halves of one sample.  Scratch of dfa_causal_backward as for
- * dfa_backward.
+ * causal attention on `batch` (>= 0, any number) independent sequences of
+ * length `seqlen` (>= 1), same layout (batch, seqlen, heads, headdim), lse
+ * (batch, heads, seqlen), run by the same kernels with causal tile
+ * enumeration: each sequence takes the place of one half of a sample.
+ * Viewing a (B, 2n, H, d) tensor as (2B, n, H, d) gives causal attention on
+ * the 2B halves.  Scratch of dfa_causal_backward as for dfa_backward (delta
+ * laid out (batch, heads, seqlen)).
  */
 int dfa_causal_forward(const void *q, const void *k, const void *v, void *out, float *lse,
                        int batch, int seqlen, int heads, int headdim, dfa_stream_t stream);
@@ -224,21 +224,23 @@ int dfa_causal_backward(const void *q, const void *k, const void *v, const void 
 /*
  * The forward and the three steps dfa_backward runs, for callers that own
  * the scratch or time the steps one by one.  `mode` is DFA_MODE_DIFFUSION or
- * DFA_MODE_CAUSAL; in the causal mode (batch, n) describe the paired view
- * (batch samples of two consecutive sequences of length n), block_size is
- * ignored and lse is laid out (2*batch, heads, n) as dfa_causal_forward
- * writes it.  delta is always (batch, heads, 2n).
- *   dfa_fwd_main: dfa_forward (or, in the causal mode, dfa_causal_forward
- *     on the paired view); if dq_acc is not NULL the same launch also sets
- *     dq_acc (float32, shape of q) to zero, with stores issued alongside
- *     the tensor-core work by warps that are not on its critical path, so
- *     that the backward needs no separate pass over it.
+ * DFA_MODE_CAUSAL.  Diffusion: tensors (batch, 2n, heads, headdim), lse and
+ * delta (batch, heads, 2n).  Causal: `batch` sequences of length n, tensors
+ * (batch, n, heads, headdim), lse and delta (batch, heads, n), block_size
+ * ignored -- dfa_causal_forward / dfa_causal_backward in steps.
+ *   dfa_fwd_main: dfa_forward (or, in the causal mode, dfa_causal_forward);
+ *     if dq_acc is not NULL the same launch also sets dq_acc (float32, shape
+ *     of q) to zero, with stores issued alongside the tensor-core work by
+ *     warps that are not on its critical path, so that the backward needs no
+ *     separate pass over it.
  *   dfa_bwd_preprocess: delta = rowsum(dout * out), float32 (batch, heads, 2n);
  *     dq_acc (float32, shape of q) set to zero unless dq_acc is NULL (then
  *     the caller zeroed it, e.g. through dfa_fwd_main).
+ *     dfa_bwd_preprocess_ex: the same with `mode` (causal: rows of n).
  *   dfa_bwd_main: the tensor-core backward: writes dk, dv (bf16) and adds
- *     dq (already scaled) into dq_acc with float32 atomics.
+ *     dq (already scaled) into dq_acc (float32 atomics or bulk reduce-adds).
  *   dfa_bwd_dq_convert: dq = bf16(dq_acc), round to nearest even.
+ *     dfa_bwd_dq_convert_ex: the same with `mode` (causal: rows of n).
  * dq_acc and delta are device buffers the caller allocated (16-byte aligned).
  */
 int dfa_fwd_main(const void *q, const void *k, const void *v, void *out, float *lse,
@@ -252,6 +254,11 @@ int dfa_bwd_main(const void *q, const void *k, const void *v, const void *dout,
                  dfa_stream_t stream);
 int dfa_bwd_dq_convert(const float *dq_acc, void *dq, int batch, int n, int heads,
                        int headdim, dfa_stream_t stream);
+int dfa_bwd_preprocess_ex(const void *out, const void *dout, float *delta, float *dq_acc,
+                          int batch, int n, int heads, int headdim, int mode,
+                          dfa_stream_t stream);
+int dfa_bwd_dq_convert_ex(const float *dq_acc, void *dq, int batch, int n, int heads,
+                          int headdim, int mode, dfa_stream_t stream);
 /*
  * dfa_fwd_main and dfa_bwd_main with grouped key/value heads: k, v, dk, dv
  * have kv_heads heads (a divisor of heads), as for dfa_forward_gqa; q, out,
@@ -335,10 +342,13 @@ long long dfa_tile_visits(int mode, int n, int block_size, int block_m, int bloc
 
 /*
  * Work order of the kernels, host side, for tests and schedulers: the w-th
- * work item (0 <= w < 2 * batch * heads * tiles) of the forward (pass 0,
- * one item per query tile) or backward (pass 1, one item per key tile)
- * enumeration, for `tiles` tiles per half and scheduling groups of `group`
- * (batch, head) pairs.  Writes (batch, head, half, tile) into item[4].
+ * work item (0 <= w < 2 * batch * heads * tiles; causal mode: batch counts
+ * sequences, w < batch * heads * tiles) of the forward (pass 0, one item per
+ * query tile) or backward (pass 1, one item per key tile) enumeration, for
+ * `tiles` tiles per half and scheduling groups of `group` (batch, head)
+ * pairs ((sequence, head) pairs in the causal mode).  Writes (batch, head,
+ * half, tile) into item[4]; in the causal mode sequence s is reported as
+ * (s / 2, head, s % 2, tile).
  * Inside a group the items of a (batch, head) go longest first; the
  * shortest ones of all pairs come last ("Fast Diffusion Attention",
  * "Hopper" and "Ampere and Ada": longest-first, L2-aware order).  The

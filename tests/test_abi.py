@@ -67,7 +67,14 @@ def test_host_side_argument_checks(lib):
     assert lib.dfa_backward(p, p, p, p, p, p, p, p, null, 1, 64, 2, 64, 4, s) == b.DFA_EINVAL
     assert lib.dfa_backward(p, p, p, p, p, p, p, p, p, 1, 64, 2, 80, 4, s) == b.DFA_EUNSUPPORTED
     assert lib.dfa_backward(p, p, p, p, p, p, p, p, p, 1, 64, 2, 96, 4, s) == b.DFA_EUNSUPPORTED
-    assert lib.dfa_causal_forward(p, p, p, p, p, 3, 64, 2, 64, s) == b.DFA_EINVAL  # odd batch
+    # the causal yardstick takes any number of sequences; bad sizes are refused
+    assert lib.dfa_causal_forward(p, p, p, p, p, -1, 64, 2, 64, s) == b.DFA_EINVAL
+    assert lib.dfa_causal_forward(p, p, p, p, p, 3, 0, 2, 64, s) == b.DFA_EINVAL
+    assert lib.dfa_causal_forward(p, p, p, p, p, 0, 64, 2, 64, s) == b.DFA_OK
+    assert lib.dfa_causal_backward(p, p, p, p, p, p, p, p, null, 3, 64, 2, 64, s) == b.DFA_EINVAL
+    # step API: unknown mode
+    assert lib.dfa_bwd_preprocess_ex(p, p, p, p, 1, 64, 2, 64, 2, s) == b.DFA_EINVAL
+    assert lib.dfa_bwd_dq_convert_ex(p, p, 1, 64, 2, 64, 5, s) == b.DFA_EINVAL
     # an empty batch is a no-op
     assert lib.dfa_forward(p, p, p, p, p, 0, 64, 2, 64, 4, s) == b.DFA_OK
     # grouped heads: kv_heads must divide heads

@@ -5,7 +5,10 @@ the order of the dQ sums.  Here the key tiles that reach a query
 tile add their part of dQ in the work order, through counters in global
 memory.  Checked: repeated runs give bitwise equal dq, dk, dv (batched,
 grouped heads, packed varlen; every head dimension); the results pass the
-oracle's bars; dk and dv equal those of the default mode bitwise.
+oracle's bars; dk and dv equal those of the default mode bitwise; and,
+with the schedule perturbed by kernels running on a second stream, the
+deterministic dq stays bitwise the same while the default mode's dq (added
+with float32 atomics in arrival order) is seen to change.
 """
 
 import numpy as np
@@ -105,3 +108,48 @@ def test_flags_are_checked(b):
     assert rc == b.DFA_EINVAL
     with pytest.raises(DfaError):
         b._check("dfa_backward_ex", rc)
+
+
+def test_schedule_perturbation(b):
+    """Kernels queued on a second stream take SMs away at varying times, so
+    the backward's CTAs reach the dQ accumulator in varying orders.  The
+    deterministic mode must not change a bit; the default mode must be seen
+    to change (otherwise this test would not show the counters doing
+    anything)."""
+    B, n, H, d, bs = 2, 1024, 8, 128, 16
+    q, k, v, do = inputs.make_inputs(B, n, H, d, seed=990)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    out, lse = b.dfa_forward(qd, kd, vd, bs)
+    side = torch.cuda.Stream(dev)
+    x0 = torch.randn(1024, 1024, device=dev, dtype=torch.bfloat16)
+
+    def perturbed(det, i):
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(side):
+            x = x0
+            for _ in range(5 + 7 * (i % 5)):  # small GEMMs, a different count each run
+                x = torch.tanh(x @ x)
+        if det:
+            g = b.dfa_backward_ex(qd, kd, vd, out, dod, lse, bs, deterministic=True)
+        else:
+            g = b.dfa_backward(qd, kd, vd, out, dod, lse, bs)
+        torch.cuda.synchronize(dev)
+        return g[0].clone()
+
+    det = [perturbed(True, i) for i in range(6)]
+    assert b.dfa_status() == 0
+    for x in det[1:]:
+        assert torch.equal(det[0], x)
+    first = perturbed(False, 0)
+    changed = False
+    for i in range(1, 20):
+        if not torch.equal(first, perturbed(False, i)):
+            changed = True
+            break
+    assert b.dfa_status() == 0
+    assert changed, "default-mode dq never changed under a perturbed schedule"
+    qn, kn, vn, don = (_np(t) for t in (q, k, v, do))
+    heads = [(1, 7)]
+    rq, _, _ = oracle.diffusion_backward(qn, kn, vn, don, bs, heads=heads)
+    assert _rel(_np(det[0])[1, :, 7], rq[1, :, 7]) <= TOL_GRAD

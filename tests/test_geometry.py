@@ -132,34 +132,48 @@ def _visits(b, pass_, mode, n, bs, half, tile, bm, bn):
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("batch,heads,n,bs,group", [
     (1, 1, 300, 16, 1), (2, 3, 700, 1, 2), (3, 5, 1024, 64, 4), (2, 4, 512, 512, 3),
-    (1, 7, 129, 7, 7), (4, 2, 2048, 16, 3),
+    (1, 7, 129, 7, 7), (4, 2, 2048, 16, 3), (3, 2, 640, 1, 2),
 ])
 def test_work_order_is_longest_first_with_short_tail(b, pass_, mode, batch, heads, n, bs, group):
     """The persistent kernels take items in this order from a counter: it must
     cover every (batch, head, half, tile) once, go longest first for each
-    (batch, head) inside the grouped part, and end on the shortest items."""
+    (batch, head) inside the grouped part, and end on the shortest items.
+    In the causal mode `batch` counts sequences (any number, odd included):
+    sequence s is reported as half s % 2 of sample s // 2, and the
+    (sequence, head) pairs take the place of the (batch, head) pairs."""
     bm, bn = (128, 128) if pass_ == 0 else (64, 128)
     tiles = -(-n // (bm if pass_ == 0 else bn))
     BH = batch * heads
-    total = 2 * BH * tiles
+    per_pair = tiles if mode == 1 else 2 * tiles
+    total = BH * per_pair
     order = [b.dfa_work_item(pass_, mode, w, batch, heads, tiles, group) for w in range(total)]
-    assert sorted(order) == sorted((x, y, h, t) for x in range(batch) for y in range(heads)
-                                   for h in range(2) for t in range(tiles))
+    if mode == 1:
+        expect = [(s // 2, y, s % 2, t) for s in range(batch) for y in range(heads)
+                  for t in range(tiles)]
+    else:
+        expect = [(x, y, h, t) for x in range(batch) for y in range(heads) for h in range(2)
+                  for t in range(tiles)]
+    assert sorted(order) == sorted(expect)
+    pair = (lambda x, y, h: (2 * x + h, y)) if mode == 1 else (lambda x, y, h: (x, y))
     bs_eff = min(bs, n)
     vis = [_visits(b, pass_, mode, n, bs_eff, h, t, bm, bn) for (_, _, h, t) in order]
-    tail = min(2 * tiles, 4) if (pass_ == 0 or mode == 1) else tiles
+    if mode == 1:
+        tail = min(tiles, 2)
+    else:
+        tail = min(2 * tiles, 4) if pass_ == 0 else tiles
     head = total - BH * tail
     if head > 0:
         if n % 128 == 0:  # a ragged last tile can be shorter than a tail item
             assert max(vis[head:]) <= min(vis[:head])
         seen = {}
-        for (x, y, _, _), c in zip(order[:head], vis[:head]):
-            assert c <= seen.get((x, y), c)
-            seen[(x, y)] = c
+        for (x, y, h, _), c in zip(order[:head], vis[:head]):
+            key = pair(x, y, h)
+            assert c <= seen.get(key, c)
+            seen[key] = c
     # tail: rank by rank over all pairs, each rank covering every pair once
+    pairs = sorted({pair(x, y, h) for (x, y, h, _) in expect})
     for r in range(tail):
         chunk = order[head + r * BH: head + (r + 1) * BH]
-        assert sorted((x, y) for (x, y, _, _) in chunk) == [(x, y) for x in range(batch)
-                                                            for y in range(heads)]
+        assert sorted(pair(x, y, h) for (x, y, h, _) in chunk) == pairs
     with pytest.raises(b.DfaError):
         b.dfa_work_item(pass_, mode, total, batch, heads, tiles, group)

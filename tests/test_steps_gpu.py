@@ -30,6 +30,7 @@ def b():
 
 
 def _steps(b, q, k, v, do, bs, mode):
+    """The step API on q (B, 2n, H, d) (diffusion) or (Bc, n, H, d) (causal)."""
     B, L, H, d = q.shape
     dev = q.device
     out = torch.empty_like(q)
@@ -40,23 +41,19 @@ def _steps(b, q, k, v, do, bs, mode):
     torch.cuda.synchronize()
     zeroed = bool((dq_acc == 0).all())
     dk, dv, dq = torch.empty_like(k), torch.empty_like(v), torch.empty_like(q)
-    b.dfa_bwd_preprocess(out, do, delta, None)
+    b.dfa_bwd_preprocess(out, do, delta, None, mode=mode)
     b.dfa_bwd_main(q, k, v, do, lse, delta, dq_acc, dk, dv, bs, mode=mode)
-    b.dfa_bwd_dq_convert(dq_acc, dq)
+    b.dfa_bwd_dq_convert(dq_acc, dq, mode=mode)
     torch.cuda.synchronize()
     assert b.dfa_status() == b.DFA_OK
     return zeroed, out, lse, dq, dk, dv
 
 
 def _one_call(b, q, k, v, do, bs, mode):
-    B, L, H, d = q.shape
     if mode == b.MODE_CAUSAL:
-        n = L // 2
-        qc, kc, vc, doc = (t.view(2 * B, n, H, d) for t in (q, k, v, do))
-        out, lse = b.dfa_causal_forward(qc, kc, vc)
-        dq, dk, dv = b.dfa_causal_backward(qc, kc, vc, out, doc, lse)
-        res = (out, lse, dq, dk, dv)
-        return tuple(t.view(B, L, H, d) if t.dim() == 4 else t for t in res)
+        out, lse = b.dfa_causal_forward(q, k, v)
+        dq, dk, dv = b.dfa_causal_backward(q, k, v, out, do, lse)
+        return out, lse, dq, dk, dv
     out, lse = b.dfa_forward(q, k, v, bs)
     dq, dk, dv = b.dfa_backward(q, k, v, out, do, lse, bs)
     return out, lse, dq, dk, dv
@@ -64,11 +61,16 @@ def _one_call(b, q, k, v, do, bs, mode):
 
 @pytest.mark.parametrize("mode_name", ["diffusion", "causal"])
 @pytest.mark.parametrize("B,n,H,d,bs", [(2, 300, 3, 64, 16), (2, 256, 4, 128, 32),
-                                        (2, 200, 2, 256, 8)])
+                                        (2, 200, 2, 256, 8), (1, 129, 2, 128, 4)])
 def test_steps_match_one_call(b, mode_name, B, n, H, d, bs):
+    """Diffusion on (B, 2n); causal on the 2B sequences of length n and, for
+    an odd count, on the first 2B - 1 of them."""
     mode = b.MODE_DIFFUSION if mode_name == "diffusion" else b.MODE_CAUSAL
     dev = torch.device("cuda", 0)
     q, k, v, do = (t.to(dev) for t in inputs.make_inputs(B, n, H, d, seed=21))
+    if mode == b.MODE_CAUSAL:
+        Bc = 2 * B - 1 if B > 1 else 2 * B
+        q, k, v, do = (t.view(2 * B, n, H, d)[:Bc].contiguous() for t in (q, k, v, do))
     zeroed, *got = _steps(b, q, k, v, do, bs, mode)
     assert zeroed, "the forward left part of the dq accumulator unzeroed"
     ref = _one_call(b, q, k, v, do, bs, mode)
@@ -94,3 +96,35 @@ def test_steps_dq_against_oracle(b):
     rq, _, _ = oracle.diffusion_backward(as64(qh), as64(kh), as64(vh), as64(doh), bs)
     got = as64(dq)
     assert np.abs(got - rq).max() / np.abs(rq).max() < 2e-2
+
+
+@pytest.mark.parametrize("Bc,n,H,Hk,d", [(3, 200, 4, 2, 128), (2, 129, 6, 2, 64),
+                                         (1, 150, 2, 1, 256)])
+def test_causal_grouped_heads_step_api(b, Bc, n, H, Hk, d):
+    """The step API in the causal mode with grouped key/value heads (query
+    head h reads key/value head h // (H / Hk)) against the oracle's causal
+    attention with the same head map."""
+    dev = torch.device("cuda", 0)
+    g = torch.Generator().manual_seed(31 + Bc)
+    mk = lambda h: torch.randn(Bc, n, h, d, generator=g).to(torch.bfloat16)  # noqa: E731
+    qh, kh, vh, doh = mk(H), mk(Hk), mk(Hk), mk(H)
+    q, k, v, do = (t.to(dev) for t in (qh, kh, vh, doh))
+    out = torch.empty_like(q)
+    lse = torch.empty((Bc, H, n), dtype=torch.float32, device=dev)
+    dq_acc = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    delta = torch.empty((Bc, H, n), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    b.dfa_fwd_main_gqa(q, k, v, out, lse, dq_acc, 1, mode=b.MODE_CAUSAL)
+    b.dfa_bwd_preprocess(out, do, delta, None, mode=b.MODE_CAUSAL)
+    b.dfa_bwd_main_gqa(q, k, v, do, lse, delta, dq_acc, dk, dv, 1, mode=b.MODE_CAUSAL)
+    b.dfa_bwd_dq_convert(dq_acc, dq, mode=b.MODE_CAUSAL)
+    torch.cuda.synchronize()
+    assert b.dfa_status() == b.DFA_OK
+    as64 = lambda t: t.float().cpu().double().numpy()  # noqa: E731
+    ro, rl = oracle.causal_forward(as64(qh), as64(kh), as64(vh))
+    rq, rk, rv = oracle.causal_backward(as64(qh), as64(kh), as64(vh), as64(doh))
+    nw = lambda a, r: np.abs(a - r).max() / np.abs(r).max()  # noqa: E731
+    assert nw(as64(out), ro) <= 1e-2
+    assert np.abs(as64(lse) - rl).max() <= 1e-3
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert nw(as64(got), ref) <= 2e-2

@@ -4,8 +4,9 @@ for every byte, or a latency-critical step where an allocation could block
 or fail).  Its scratch lives in a fixed array inside the library.
 
 Checked through the C ABI against dfa_backward on two calls in a row (the
-second on different data, so stale scratch from the first would show).
-Kept in its own file, collected last.
+second on different data, so stale scratch from the first would show), and
+the second call also against the float64 oracle.  Kept in its own file,
+collected last.
 """
 
 import ctypes
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from block_diffusion_masked_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -63,6 +65,12 @@ def test_noalloc_backward_matches_backward(lib, B, n, H, d, bs, seed):
         for g, r in zip(got, ref):
             assert torch.isfinite(g).all()
             assert _normwise(g, r) <= TOL_GRAD
+    # the second call's gradients against the oracle
+    f64 = lambda t: t.float().cpu().double().numpy()  # noqa: E731
+    refs = oracle.diffusion_backward(f64(q), f64(k), f64(v), f64(do), bs)
+    floor = 1e-3 * max(np.abs(r).max() for r in refs)
+    for g, r in zip(got, refs):
+        assert np.abs(f64(g) - r).max() / max(np.abs(r).max(), floor) <= TOL_GRAD
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(lib):

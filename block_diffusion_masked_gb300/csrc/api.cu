@@ -6,6 +6,7 @@
 #include <cmath>
 #include <initializer_list>
 #include <mutex>
+#include <cstring>
 #include <vector>
 
 #include "dfa.h"
@@ -564,16 +565,58 @@ int varlen_schedule(const int* cu, int batch, int heads, int tile, long long byt
   return DFA_OK;
 }
 
-// Copy the slot table to stream-ordered device memory (freed by the caller
-// with cudaFreeAsync after the launch that reads it).
-int upload_slots(const std::vector<VarlenSlot>& slots, cudaStream_t stream, VarlenSlot** dptr) {
-  const size_t bytes = slots.size() * sizeof(VarlenSlot);
-  if (cudaMallocAsync(reinterpret_cast<void**>(dptr), bytes, stream) != cudaSuccess)
-    return DFA_ECUDA;
-  if (cudaMemcpyAsync(*dptr, slots.data(), bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
-    cudaFreeAsync(*dptr, stream);
+// Tensor maps of every slot's sample: (d, H, n, 2, 1) views starting at
+// the sample's first row, so that rows past the end of a half read zero.
+// Forward: q (box bm rows), k, v (box bn rows); backward also dout (bm) and,
+// if dq_acc is given, the float32 accumulator (box dq_rows rows of 32).
+int varlen_maps(const std::vector<VarlenSlot>& slots, const void* q, const void* k,
+                const void* v, const void* dout, int H, int Hk, int d, int bm, int bn,
+                std::vector<VarlenMaps>* maps, const float* dq_acc = nullptr, int dq_rows = 0) {
+  maps->assign(slots.size(), VarlenMaps{});
+  const size_t qrow = static_cast<size_t>(H) * d * 2, krow = static_cast<size_t>(Hk) * d * 2;
+  for (size_t i = 0; i < slots.size(); ++i) {
+    const VarlenSlot& sl = slots[i];
+    VarlenMaps& m = (*maps)[i];
+    const char* qb = static_cast<const char*>(q) + sl.row0 * qrow;
+    int rc;
+    if ((rc = make_map(&m.q, qb, 2, sl.n, H, d, bm))) return rc;
+    if ((rc = make_map(&m.k, static_cast<const char*>(k) + sl.row0 * krow, 2, sl.n, Hk, d, bn)))
+      return rc;
+    if ((rc = make_map(&m.v, static_cast<const char*>(v) + sl.row0 * krow, 2, sl.n, Hk, d, bn)))
+      return rc;
+    if (dout &&
+        (rc = make_map(&m.dout, static_cast<const char*>(dout) + sl.row0 * qrow, 2, sl.n, H, d,
+                       bm)))
+      return rc;
+    if (dq_acc && (rc = make_map_f32(&m.dq, dq_acc + static_cast<size_t>(sl.row0) * H * d, 2,
+                                     sl.n, H, d, dq_rows)))
+      return rc;
+  }
+  return DFA_OK;
+}
+
+// Copy the slot table and the slots' tensor maps to stream-ordered device
+// memory: maps first (at the allocation's 256-byte aligned start), then the table.  One allocation,
+// freed by the caller with cudaFreeAsync(*dmaps) after the launch that reads
+// it.
+int upload_slots(const std::vector<VarlenSlot>& slots, const std::vector<VarlenMaps>& maps,
+                 cudaStream_t stream, VarlenMaps** dmaps, VarlenSlot** dslots) {
+  const size_t mbytes = maps.size() * sizeof(VarlenMaps);
+  const size_t sbytes = slots.size() * sizeof(VarlenSlot);
+  std::vector<char> host(mbytes + sbytes);
+  std::memcpy(host.data(), maps.data(), mbytes);
+  std::memcpy(host.data() + mbytes, slots.data(), sbytes);
+  void* d = nullptr;
+  if (cudaMallocAsync(&d, host.size(), stream) != cudaSuccess) return DFA_ECUDA;
+  if (cudaMemcpyAsync(d, host.data(), host.size(), cudaMemcpyHostToDevice, stream) !=
+      cudaSuccess) {
+    cudaFreeAsync(d, stream);
     return DFA_ECUDA;
   }
+  // From pageable memory the copy has staged the host buffer by the time it
+  // returns, so the buffer may go out of scope now.
+  *dmaps = static_cast<VarlenMaps*>(d);
+  *dslots = reinterpret_cast<VarlenSlot*>(static_cast<char*>(d) + mbytes);
   return DFA_OK;
 }
 
@@ -605,10 +648,11 @@ int forward_varlen_impl(const void* q, const void* k, const void* v, void* out, 
   // q, k, v and out of one head
   if ((rc = varlen_schedule(cu, batch, H, ts.fwd_bm, 8LL * d, ds->l2_bytes, &slots, &units)))
     return rc;
+  // q, k, v through per-sample maps; out through a map of the packed tensor
+  std::vector<VarlenMaps> maps;
+  if ((rc = varlen_maps(slots, q, k, v, nullptr, H, Hk, d, ts.fwd_bm, ts.fwd_bn, &maps)))
+    return rc;
   FwdParams p{};
-  if ((rc = make_map(&p.tm_q, q, 1, rows, H, d, ts.fwd_bm, true))) return rc;
-  if ((rc = make_map(&p.tm_k, k, 1, rows, Hk, d, ts.fwd_bn, true))) return rc;
-  if ((rc = make_map(&p.tm_v, v, 1, rows, Hk, d, ts.fwd_bn, true))) return rc;
   if ((rc = make_map(&p.tm_o, out, 1, rows, H, d, ts.fwd_bm, true))) return rc;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
@@ -627,10 +671,12 @@ int forward_varlen_impl(const void* q, const void* k, const void* v, void* out, 
   p.rows = rows;
   p.items = units;
   VarlenSlot* dslots = nullptr;
-  if ((rc = upload_slots(slots, stream, &dslots))) return rc;
+  VarlenMaps* dmaps = nullptr;
+  if ((rc = upload_slots(slots, maps, stream, &dmaps, &dslots))) return rc;
   p.vl = dslots;
+  p.vl_maps = dmaps;
   const cudaError_t e = launch_forward(p, d, stream);
-  cudaFreeAsync(dslots, stream);
+  cudaFreeAsync(dmaps, stream);
   return e == cudaSuccess ? DFA_OK : cuda_fail(e);
 }
 
@@ -662,6 +708,7 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
   float* dq_acc = nullptr;
   float* delta = nullptr;
   VarlenSlot* dslots = nullptr;
+  VarlenMaps* dmaps = nullptr;
   if (cudaMallocAsync(reinterpret_cast<void**>(&dq_acc), elems * sizeof(float), stream) !=
       cudaSuccess)
     return DFA_ECUDA;
@@ -670,14 +717,19 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
     cudaFreeAsync(dq_acc, stream);
     return DFA_ECUDA;
   }
-  if ((rc = upload_slots(slots, stream, &dslots))) {
+  // q, dout, k, v and the dq accumulator through per-sample maps (rows past
+  // a half read zero; reduce-adds past a half are skipped)
+  std::vector<VarlenMaps> maps;
+  if ((rc = varlen_maps(slots, q, k, v, dout, H, Hk, d, ts.bwd_bm, ts.bwd_bn, &maps,
+                        d == 128 ? dq_acc : nullptr, ts.bwd_bm / kBwd2WarpgroupsD128)) ||
+      (rc = upload_slots(slots, maps, stream, &dmaps, &dslots))) {
     cudaFreeAsync(delta, stream);
     cudaFreeAsync(dq_acc, stream);
     return rc;
   }
   unsigned* sem = nullptr;
   if (det && (rc = alloc_dq_sem(static_cast<size_t>(rows) * H, stream, &sem))) {
-    cudaFreeAsync(dslots, stream);
+    cudaFreeAsync(dmaps, stream);
     cudaFreeAsync(delta, stream);
     cudaFreeAsync(dq_acc, stream);
     return rc;
@@ -688,18 +740,6 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
                                         1, rows, H, d, stream);
   if (e == cudaSuccess) {
     BwdParams p{};
-    if ((rc = make_map(&p.tm_q, q, 1, rows, H, d, ts.bwd_bm, true)) ||
-        (rc = make_map(&p.tm_do, dout, 1, rows, H, d, ts.bwd_bm, true)) ||
-        (rc = make_map(&p.tm_k, k, 1, rows, Hk, d, ts.bwd_bn, true)) ||
-        (rc = make_map(&p.tm_v, v, 1, rows, Hk, d, ts.bwd_bn, true)) ||
-        (d == 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, 1, rows, H, d,
-                                        ts.bwd_bm / kBwd2WarpgroupsD128, true)))) {
-      if (sem) cudaFreeAsync(sem, stream);
-      cudaFreeAsync(dslots, stream);
-      cudaFreeAsync(delta, stream);
-      cudaFreeAsync(dq_acc, stream);
-      return rc;
-    }
     p.lse = lse;
     p.delta = delta;
     p.dq_acc = dq_acc;
@@ -719,6 +759,7 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
     p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     p.vl = dslots;
+    p.vl_maps = dmaps;
     p.vl_slots = static_cast<int>(slots.size());
     p.rows = rows;
     p.units = units;
@@ -730,7 +771,7 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
     e = launch_dq_convert(dq_acc, static_cast<__nv_bfloat16*>(dq), static_cast<long long>(elems),
                           stream);
   if (sem) cudaFreeAsync(sem, stream);
-  cudaFreeAsync(dslots, stream);
+  cudaFreeAsync(dmaps, stream);
   cudaFreeAsync(delta, stream);
   cudaFreeAsync(dq_acc, stream);
   return e == cudaSuccess ? DFA_OK : cuda_fail(e);

@@ -111,6 +111,7 @@ struct BwdItem {
   int h0;               // first query head of the group
   int half0, rule0, tb0, half1, rule1, tb1;
   int n, bs, row0;  // half length, block size (clamped) and, varlen, first row
+  int slot;         // varlen: the sample's slot (its tensor maps)
   // Tile t is local tile l of query head h0 + hh.  Without grouping
   // (GQA false: one query head per key/value head) l = t and hh = 0.
   template <bool GQA>
@@ -136,7 +137,8 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
   it.v = v;
   if (v < 0) return it;
   if constexpr (VARLEN) {
-    const VarlenSlot sl = p.vl[varlen_slot(p.vl, p.vl_slots, v)];
+    it.slot = varlen_slot(p.vl, p.vl_slots, v);
+    const VarlenSlot sl = p.vl[it.slot];
     it.wi = bwd_work(v - sl.off, MODE_DIFFUSION, 1, p.Hk, cdiv(sl.n, BN), sl.group);
     it.wi.b = sl.b;
     it.n = sl.n;
@@ -147,6 +149,7 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
     it.n = p.n;
     it.bs = p.bs;
     it.row0 = 0;  // unused: batched rows come from wi.b
+    it.slot = 0;
   }
   it.h0 = GQA ? it.wi.h * p.kv_group : it.wi.h;
   Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
    if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ loads
-    if (lane == 0) {
+    if (lane == 0 && !VARLEN) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_do);
       tma_prefetch_desc(&p.tm_k);
@@ -275,12 +278,15 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(BAR(C::BAR_QFULL + st), 2 * C::kQBytes);
-        const HalfRows qr = half_rows<VARLEN>(it.wi.b, half, it.n, it.row0);
+        // Varlen: the sample's own maps (rows past its halves read zero).
+        const CUtensorMap* mq = VARLEN ? &p.vl_maps[it.slot].q : &p.tm_q;
+        const CUtensorMap* mdo = VARLEN ? &p.vl_maps[it.slot].dout : &p.tm_do;
+        const HalfRows qr = in_rows<VARLEN>(it.wi.b, half);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_5d(sbase + C::kOffQ + st * C::kQBytes + c * BMQ * 128, &p.tm_q,
+          tma_load_5d(sbase + C::kOffQ + st * C::kQBytes + c * BMQ * 128, mq,
                       BAR(C::BAR_QFULL + st), 64 * c, h, qr.base + qt * BMQ, qr.c3, qr.c4);
-          tma_load_5d(sbase + C::kOffDO + st * C::kQBytes + c * BMQ * 128, &p.tm_do,
+          tma_load_5d(sbase + C::kOffDO + st * C::kQBytes + c * BMQ * 128, mdo,
                       BAR(C::BAR_QFULL + st), 64 * c, h, qr.base + qt * BMQ, qr.c3, qr.c4);
         }
       }
@@ -298,6 +304,13 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
       }
       if (v < 0) break;
+      if (VARLEN && lane == 0) {
+        // this launch's maps of the item's sample, as memory holds them
+        tensormap_acquire(&p.vl_maps[it.slot].q);
+        tensormap_acquire(&p.vl_maps[it.slot].dout);
+        tensormap_acquire(&p.vl_maps[it.slot].k);
+        tensormap_acquire(&p.vl_maps[it.slot].v);
+      }
       // The first query tiles only need stages the current item frees before
       // its last products, so they go ahead of the K / V load, which waits
       // for the whole item.
@@ -310,14 +323,16 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
       }
       if (lane == 0) {
-        const HalfRows kr = half_rows<VARLEN>(it.wi.b, it.wi.half, it.n, it.row0);
+        const CUtensorMap* mk = VARLEN ? &p.vl_maps[it.slot].k : &p.tm_k;
+        const CUtensorMap* mv = VARLEN ? &p.vl_maps[it.slot].v : &p.tm_v;
+        const HalfRows kr = in_rows<VARLEN>(it.wi.b, it.wi.half);
         const int krow = kr.base + it.wi.tile * BN;
         mbar_arrive_expect_tx(BAR(C::BAR_KV), 2 * C::kKVBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_5d(sbase + C::kOffK + c * BN * 128, &p.tm_k, BAR(C::BAR_KV), 64 * c, it.wi.h,
+          tma_load_5d(sbase + C::kOffK + c * BN * 128, mk, BAR(C::BAR_KV), 64 * c, it.wi.h,
                       krow, kr.c3, kr.c4);
-          tma_load_5d(sbase + C::kOffV + c * BN * 128, &p.tm_v, BAR(C::BAR_KV), 64 * c, it.wi.h,
+          tma_load_5d(sbase + C::kOffV + c * BN * 128, mv, BAR(C::BAR_KV), 64 * c, it.wi.h,
                       krow, kr.c3, kr.c4);
         }
       }

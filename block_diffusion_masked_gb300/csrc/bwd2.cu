@@ -144,6 +144,7 @@ struct Bwd2Item {
   int h0;               // first query head of the group
   int half0, rule0, tb0, half1, rule1, tb1;
   int n, bs, row0;  // half length, block size (clamped) and, varlen, first row
+  int slot;         // varlen: the sample's slot (its tensor maps)
   // Tile t is local tile l of query head h0 + hh.  Without grouping
   // (GQA false: one query head per key/value head) l = t and hh = 0.
   template <bool GQA>
@@ -171,7 +172,8 @@ __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   it.dh = v % NDH;
   if constexpr (VARLEN) {
     const int u = v / NDH;
-    const VarlenSlot sl = p.vl[varlen_slot(p.vl, p.vl_slots, u)];
+    it.slot = varlen_slot(p.vl, p.vl_slots, u);
+    const VarlenSlot sl = p.vl[it.slot];
     it.wi = bwd_work(u - sl.off, MODE_DIFFUSION, 1, p.Hk, cdiv(sl.n, BN), sl.group);
     it.wi.b = sl.b;
     it.n = sl.n;
@@ -182,6 +184,7 @@ __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
     it.n = p.n;
     it.bs = p.bs;
     it.row0 = 0;  // unused: batched rows come from wi.b
+    it.slot = 0;
   }
   it.h0 = GQA ? it.wi.h * p.kv_group : it.wi.h;
   Segment seg[2] = {};
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegCtl));
    if (warp == C::kWarpLoad) {
     // ------------------------------------------------------------ loads
-    if (lane == 0) {
+    if (lane == 0 && !VARLEN) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_do);
       tma_prefetch_desc(&p.tm_k);
@@ -313,12 +316,15 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(BAR(C::BAR_QFULL + st), 2 * C::kQBytes);
-        const HalfRows qr = half_rows<VARLEN>(it.wi.b, half, it.n, it.row0);
+        // Varlen: the sample's own maps (rows past its halves read zero).
+        const CUtensorMap* mq = VARLEN ? &p.vl_maps[it.slot].q : &p.tm_q;
+        const CUtensorMap* mdo = VARLEN ? &p.vl_maps[it.slot].dout : &p.tm_do;
+        const HalfRows qr = in_rows<VARLEN>(it.wi.b, half);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_5d(sbase + C::kOffQ + st * C::kQBytes + c * BMQ * 128, &p.tm_q,
+          tma_load_5d(sbase + C::kOffQ + st * C::kQBytes + c * BMQ * 128, mq,
                       BAR(C::BAR_QFULL + st), 64 * c, h, qr.base + qt * BMQ, qr.c3, qr.c4);
-          tma_load_5d(sbase + C::kOffDO + st * C::kQBytes + c * BMQ * 128, &p.tm_do,
+          tma_load_5d(sbase + C::kOffDO + st * C::kQBytes + c * BMQ * 128, mdo,
                       BAR(C::BAR_QFULL + st), 64 * c, h, qr.base + qt * BMQ, qr.c3, qr.c4);
         }
       }
@@ -336,6 +342,13 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         mbar_arrive(BAR(C::BAR_ITEMFULL + (k & 3)));
       }
       if (v < 0) break;
+      if (VARLEN && lane == 0) {
+        // this launch's maps of the item's sample, as memory holds them
+        tensormap_acquire(&p.vl_maps[it.slot].q);
+        tensormap_acquire(&p.vl_maps[it.slot].dout);
+        tensormap_acquire(&p.vl_maps[it.slot].k);
+        tensormap_acquire(&p.vl_maps[it.slot].v);
+      }
       // K / V buffer `kvs` was last used by item k - KVBUF.  With one buffer
       // the first query tiles only need stages that the current item frees
       // before its last product, so they go ahead of the K / V load, which
@@ -351,15 +364,17 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
       }
       if (lane == 0) {
-        const HalfRows kr = half_rows<VARLEN>(it.wi.b, it.wi.half, it.n, it.row0);
+        const CUtensorMap* mk = VARLEN ? &p.vl_maps[it.slot].k : &p.tm_k;
+        const CUtensorMap* mv = VARLEN ? &p.vl_maps[it.slot].v : &p.tm_v;
+        const HalfRows kr = in_rows<VARLEN>(it.wi.b, it.wi.half);
         const int krow = kr.base + it.wi.tile * BN;
         const uint32_t full = BAR(C::BAR_KVFULL + kvs);
         mbar_arrive_expect_tx(full, 2 * C::kKVBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_5d(sbase + C::kOffK + kvs * C::kKVBytes + c * BN * 128, &p.tm_k, full, 64 * c,
+          tma_load_5d(sbase + C::kOffK + kvs * C::kKVBytes + c * BN * 128, mk, full, 64 * c,
                       it.wi.h, krow, kr.c3, kr.c4);
-          tma_load_5d(sbase + C::kOffV + kvs * C::kKVBytes + c * BN * 128, &p.tm_v, full, 64 * c,
+          tma_load_5d(sbase + C::kOffV + kvs * C::kKVBytes + c * BN * 128, mv, full, 64 * c,
                       it.wi.h, krow, kr.c3, kr.c4);
         }
       }
@@ -527,12 +542,12 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && qs + c0 < (VARLEN ? it.n : p.n)) {
-          // Varlen: rows of the box past the half hold exact zeros (no query
-          // row there sees a key), added to the next rows of the packed
-          // accumulator.
-          const HalfRows dr = half_rows<VARLEN>(it.wi.b, qh, it.n, it.row0);
-          tma_reduce_add_5d(&p.tm_dq, stg, it.dh * DH + 32 * (warp & 3), h, dr.base + qs + c0,
-                            dr.c3, dr.c4);
+          // Varlen: through the sample's own map, so that rows of the box
+          // past the half are skipped rather than added to the next sample.
+          const CUtensorMap* mdq = VARLEN ? &p.vl_maps[it.slot].dq : &p.tm_dq;
+          const HalfRows dr = in_rows<VARLEN>(it.wi.b, qh);
+          tma_reduce_add_5d(mdq, stg, it.dh * DH + 32 * (warp & 3), h, dr.base + qs + c0, dr.c3,
+                            dr.c4);
           bulk_commit_group();
         }
         return true;
@@ -575,6 +590,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
       const Bwd2Item it = *ring(k & 3);
       if (it.v < 0) break;
+      if constexpr (VARLEN && C::kTmaDQ && !DET) {
+        // this launch's dq map of the item's sample, as memory holds it
+        if (lane == 0) tensormap_acquire(&p.vl_maps[it.slot].dq);
+      }
       const int ks = it.wi.tile * BN;
       const int j = ks + row;  // key inside its half
       // Query rows that see key j, per segment of the item: computed once,

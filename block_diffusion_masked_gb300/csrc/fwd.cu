@@ -83,10 +83,11 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
   // may only be read after grid_dependency_wait below.
   WorkItem wi;
   Segment seg[2];
-  int n = p.n, bs = p.bs, row0 = 0, n0 = 0, ntiles = 0, qs = 0, hk = 0;
+  int n = p.n, bs = p.bs, row0 = 0, n0 = 0, ntiles = 0, qs = 0, hk = 0, slot = 0;
   auto decode = [&]() {
     if constexpr (VARLEN) {
-      const VarlenSlot sl = p.vl[varlen_slot(p.vl, p.vl_slots, blockIdx.x)];
+      slot = varlen_slot(p.vl, p.vl_slots, blockIdx.x);
+      const VarlenSlot sl = p.vl[slot];
       n = sl.n;
       bs = imin(p.bs, n);
       row0 = sl.row0;
@@ -137,14 +138,26 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
+      // Varlen: the sample's own maps (rows past its halves read zero).
+      const CUtensorMap* mq = &p.tm_q;
+      const CUtensorMap* mk = &p.tm_k;
+      const CUtensorMap* mv = &p.tm_v;
+      if constexpr (VARLEN) {
+        mq = &p.vl_maps[slot].q;
+        mk = &p.vl_maps[slot].k;
+        mv = &p.vl_maps[slot].v;
+        tensormap_acquire(mq);
+        tensormap_acquire(mk);
+        tensormap_acquire(mv);
+      }
+      tma_prefetch_desc(mq);
+      tma_prefetch_desc(mk);
+      tma_prefetch_desc(mv);
       mbar_arrive_expect_tx(BAR(C::BAR_Q), C::kQBytes);
-      const HalfRows qr = half_rows<VARLEN>(wi.b, wi.half, n, row0);
+      const HalfRows qr = in_rows<VARLEN>(wi.b, wi.half);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_5d(sbase + C::kOffQ + c * BM * 128, &p.tm_q, BAR(C::BAR_Q), 64 * c, wi.h,
+        tma_load_5d(sbase + C::kOffQ + c * BM * 128, mq, BAR(C::BAR_Q), 64 * c, wi.h,
                     qr.base + qs, qr.c3, qr.c4);
       bool ok = true;
       int j = 0;
@@ -155,10 +168,10 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
         const int round = j / STAGES;
         if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_KEMPTY + st), (round - 1) & 1, ab))) break;
         mbar_arrive_expect_tx(BAR(C::BAR_KFULL + st), C::kKVBytes);
-        const HalfRows kr = half_rows<VARLEN>(wi.b, seg[s].half, n, row0);
+        const HalfRows kr = in_rows<VARLEN>(wi.b, seg[s].half);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
+          tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, mk,
                       BAR(C::BAR_KFULL + st), 64 * c, hk, kr.base + kt * BN, kr.c3, kr.c4);
         if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_VEMPTY + st), (round - 1) & 1, ab))) {
           // K of this stage is in flight; account for it while unwinding.
@@ -168,7 +181,7 @@ __global__ void __launch_bounds__(224, 1) dfa_fwd_kernel(const __grid_constant__
         mbar_arrive_expect_tx(BAR(C::BAR_VFULL + st), C::kKVBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
+          tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, mv,
                       BAR(C::BAR_VFULL + st), 64 * c, hk, kr.base + kt * BN, kr.c3, kr.c4);
       }
       if (!ok) {

@@ -80,7 +80,7 @@ struct Fwd2Cfg {
     NUM_BARS = BAR_ALL + 1
   };
   static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 decoded items (ItemGeom)
-  static constexpr int kOffTmemSlot = kOffItem + 4 * 64;
+  static constexpr int kOffTmemSlot = kOffItem + 4 * 128;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
   static constexpr int kTmemS = 0;       // S[w] at w * BN; P[w] in its first BN / 2 columns
@@ -102,11 +102,12 @@ struct ItemGeom {
   int n0, ntiles, qs;
   int half0, rule0, tb0, half1, rule1, tb1;
   int n, row0;  // varlen: the sample's half length and first row
+  int slot;     // varlen: the sample's slot (its tensor maps)
   __device__ __forceinline__ int ktile(int j) const { return j < n0 ? tb0 + j : tb1 + (j - n0); }
   __device__ __forceinline__ int khalf(int j) const { return j < n0 ? half0 : half1; }
 };
 
-static_assert(sizeof(ItemGeom) <= 64, "item ring slot");
+static_assert(sizeof(ItemGeom) <= 128, "item ring slot");
 
 template <bool VARLEN>
 __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, int bn,
@@ -115,7 +116,8 @@ __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, 
   if (item < 0) return;
   int n = p.n, bs = p.bs;
   if constexpr (VARLEN) {
-    const VarlenSlot sl = p.vl[varlen_slot(p.vl, p.vl_slots, item)];
+    g->slot = varlen_slot(p.vl, p.vl_slots, item);
+    const VarlenSlot sl = p.vl[g->slot];
     n = sl.n;
     bs = imin(p.bs, n);
     g->wi = fwd_work(item - sl.off, MODE_DIFFUSION, 1, p.H, cdiv(n, bm), sl.group);
@@ -124,6 +126,7 @@ __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, 
     g->row0 = sl.row0;
   } else {
     g->wi = fwd_work(item, p.mode, p.B, p.H, p.q_tiles, p.group);
+    g->slot = 0;
   }
   Segment seg[2] = {{0, RULE_NONE, 0, 0}, {0, RULE_NONE, 0, 0}};
   const int nseg = fwd_segments(p.mode, n, bs, bm, bn, g->wi.half, g->wi.tile, seg);
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
   // Slot s of the item ring; written by warp 8 before it arrives on
   // ITEMFULL[s] (release), read by the other roles after their wait (acquire).
-  auto ring = [&](int s) { return reinterpret_cast<ItemGeom*>(smem + C::kOffItem + 64 * s); };
+  auto ring = [&](int s) { return reinterpret_cast<ItemGeom*>(smem + C::kOffItem + 128 * s); };
   const AbortFlag ab{abort_flag, p.status};
   const int num_items = VARLEN ? p.items : static_cast<int>(pass_items(p.mode, p.B, p.H, p.q_tiles));
 #define BAR(i) (sbase + C::kOffBar + 8 * (i))
@@ -204,14 +207,17 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     // load of a tile is issued after the K load of the next one, so that a K
     // tile (needed first, by S) never waits behind a V slot.
     if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
+      if constexpr (!VARLEN) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+      }
       bool ok = true;
       int g = 0;  // K/V ring position across items
-      // The V tile still to be loaded: ring position vg (< 0: none) and its
-      // tensor-map coordinates.
+      // The V tile still to be loaded: ring position vg (< 0: none), its
+      // tensor map and coordinates.
       int vg = -1, vh = 0, vc2 = 0, vc3 = 0, vc4 = 0;
+      const CUtensorMap* vmap = &p.tm_v;
       auto load_v = [&]() -> bool {
         const int st = vg % STAGES;
         const int round = vg / STAGES;
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
             tma_load_5d(sbase + C::kOffV + st * C::kKVBytes, &p.tm_v, BAR(C::BAR_VFULL + st), vc2,
                         vc3 & 1, 0, vh, vc3 >> 1);
           else
-            tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, &p.tm_v,
+            tma_load_5d(sbase + C::kOffV + st * C::kKVBytes + c * BN * 128, vmap,
                         BAR(C::BAR_VFULL + st), C::kChunkElems * c, vh, vc2, vc3, vc4);
         vg = -1;
         return true;
@@ -243,11 +249,23 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         if (ig.item < 0) break;
         const int qb = k & 1;
         if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_QEMPTY + qb), ((k >> 1) - 1) & 1, ab))) break;
+        // Varlen: the sample's own maps (rows past its halves read zero).
+        const CUtensorMap* mq = &p.tm_q;
+        const CUtensorMap* mk = &p.tm_k;
+        const CUtensorMap* mv = &p.tm_v;
+        if constexpr (VARLEN) {
+          mq = &p.vl_maps[ig.slot].q;
+          mk = &p.vl_maps[ig.slot].k;
+          mv = &p.vl_maps[ig.slot].v;
+          tensormap_acquire(mq);
+          tensormap_acquire(mk);
+          tensormap_acquire(mv);
+        }
         mbar_arrive_expect_tx(BAR(C::BAR_QFULL + qb), C::kQLoadBytes);
-        const HalfRows qr = half_rows<VARLEN>(ig.wi.b, ig.wi.half, ig.n, ig.row0);
+        const HalfRows qr = in_rows<VARLEN>(ig.wi.b, ig.wi.half);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, &p.tm_q,
+          tma_load_5d(sbase + C::kOffQ + qb * C::kQBytes + c * BM * 128, mq,
                       BAR(C::BAR_QFULL + qb), C::kChunkElems * c, ig.wi.h, qr.base + ig.qs, qr.c3,
                       qr.c4);
         // key/value head of query head wi.h (grouped heads: kv_group > 1)
@@ -257,14 +275,15 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
           const int round = g / STAGES;
           if (round > 0 && !(ok = mbar_wait(BAR(C::BAR_KEMPTY + st), (round - 1) & 1, ab))) break;
           mbar_arrive_expect_tx(BAR(C::BAR_KFULL + st), C::kKVBytes);
-          const HalfRows kr = half_rows<VARLEN>(ig.wi.b, ig.khalf(j), ig.n, ig.row0);
+          const HalfRows kr = in_rows<VARLEN>(ig.wi.b, ig.khalf(j));
           const int krow = kr.base + ig.ktile(j) * BN;
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, &p.tm_k,
+            tma_load_5d(sbase + C::kOffK + st * C::kKVBytes + c * BN * 128, mk,
                         BAR(C::BAR_KFULL + st), C::kChunkElems * c, hk, krow, kr.c3, kr.c4);
           if (vg >= 0 && !(ok = load_v())) break;
           vg = g;
+          vmap = mv;
           vh = hk;
           vc2 = krow;
           vc3 = kr.c3;

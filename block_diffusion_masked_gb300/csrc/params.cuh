@@ -26,14 +26,24 @@ struct VarlenSlot {
   int off;    // first work unit of the slot
 };
 
+// Varlen: tensor maps of one sample (rows [row0, row0 + 2n) of the packed
+// tensors) viewed as (headdim, heads, n, 2, 1) -- the batched view of a
+// batch of one -- so that rows past the end of either half read as zeros
+// instead of the next sample's rows, and reduce-adds skip them: no value of
+// one sample, finite or not, reaches another sample's tiles or results.
+// The forward uses q, k, v; the backward q, k, v, dout and (headdim 128)
+// dq, the float32 accumulator.
+struct VarlenMaps {  // CUtensorMap carries its own (128-byte) alignment
+  CUtensorMap q, k, v, dout, dq;
+};
+
 // Forward kernel parameters.  Batched: tensor maps view q/k/v as 5-D arrays
 // (headdim, heads, n, halves, 1), halves = 2 * batch (sample b's noisy half
 // is half 2b, its clean half 2b + 1; in the causal mode every sequence is
 // one half), so that a tile never crosses the noisy/clean boundary and rows
 // past the end of a half read as zeros.
-// Varlen: the same 5-D maps with dims (headdim, heads, rows, 1, 1); rows past
-// the end of a half are the next rows of the packed tensor (finite data the
-// mask hides; only rows past the last sample read as zeros).
+// Varlen: q, k, v are read through per-sample maps (VarlenMaps); tm_o is a
+// map of the packed output, (headdim, heads, rows, 1, 1).
 struct FwdParams {
   CUtensorMap tm_q;  // box (64, 1, block_m, 1, 1)
   CUtensorMap tm_k;  // box (64, 1, block_n, 1, 1)
@@ -56,6 +66,7 @@ struct FwdParams {
   // length, the rows of the packed tensors (lse is (heads, rows)) and the
   // work units of the launch.
   const VarlenSlot* vl;
+  const VarlenMaps* vl_maps;  // one per slot
   int vl_slots;
   int rows;
   int items;
@@ -86,6 +97,7 @@ struct BwdParams {
   // Varlen only (vl == nullptr for a batched launch): the slot table, its
   // length and the rows of the packed tensors (lse, delta are (heads, rows)).
   const VarlenSlot* vl;
+  const VarlenMaps* vl_maps;  // one per slot
   int vl_slots;
   int rows;
   int units;          // work units (items without the head-dim split)
@@ -118,14 +130,22 @@ __device__ __forceinline__ int varlen_slot(const VarlenSlot* vl, int slots, int 
 }
 
 // Tensor-map coordinates (c2, c3, c4) of row `base + r` of one half: batched
-// maps are (headdim, heads, n, halves, 1), varlen maps
-// (headdim, heads, rows, 1, 1).
+// maps are (headdim, heads, n, halves, 1), packed varlen maps (the output
+// and dq maps) (headdim, heads, rows, 1, 1).
 struct HalfRows {
   int base, c3, c4;
 };
 template <bool VARLEN>
 __device__ __forceinline__ HalfRows half_rows(int b, int half, int n, int row0) {
   if constexpr (VARLEN) return {row0 + half * n, 0, 0};
+  else return {0, 2 * b + half, 0};
+}
+// Coordinates of the input maps (q, k, v, dout): batched maps as above;
+// varlen inputs are read through the sample's own maps (VarlenMaps), whose
+// half index is the half itself.
+template <bool VARLEN>
+__device__ __forceinline__ HalfRows in_rows(int b, int half) {
+  if constexpr (VARLEN) return {0, half, 0};
   else return {0, 2 * b + half, 0};
 }
 

@@ -131,11 +131,13 @@ int dfa_backward_gqa(const void *q, const void *k, const void *v, const void *ou
  * (rows, heads, headdim) bf16, k, v, dk, dv (rows, kv_heads, headdim) bf16
  * (kv_heads divides heads, as for dfa_forward_gqa), lse (heads, rows)
  * float32.  block_size applies to every sample (clamped to each n_b).  The
- * non-empty samples run in one launch per pass, longest first.  A tile may
- * read rows of the next sample, which the mask hides: the inputs must be
- * finite everywhere in the packed tensors.  The schedule (20 bytes per
- * sample) is copied to stream-ordered device memory on `stream`
- * (cudaMallocAsync, cudaMemcpyAsync from the host array, cudaFreeAsync);
+ * non-empty samples run in one launch per pass, longest first.  Every
+ * sample is read through tensor maps of its own, so rows past the end of a
+ * half read as zeros: no value of one sample -- finite or not -- reaches
+ * another sample's results.  The schedule (20 bytes and four 128-byte
+ * tensor maps per sample) is copied to stream-ordered device memory on
+ * `stream` (cudaMallocAsync, cudaMemcpyAsync from a host array,
+ * cudaFreeAsync);
  * dfa_backward_varlen also takes the scratch of dfa_backward.  Errors:
  * DFA_EINVAL for a bad cu_seqlens (odd or negative length, cu_seqlens[0] !=
  * 0, NULL) or head counts, otherwise as dfa_forward / dfa_backward.

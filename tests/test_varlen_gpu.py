@@ -141,3 +141,49 @@ def test_autograd_varlen_function(b):
     errs = _errors({"dq": _np(qd.grad), "dk": _np(kd.grad), "dv": _np(vd.grad)},
                    {"dq": rq, "dk": rk, "dv": rv})
     assert max(errs.values()) <= TOL_GRAD, errs
+
+
+@pytest.mark.parametrize("d,det", [(64, False), (128, False), (256, False), (128, True)])
+def test_neighbour_samples_do_not_leak(b, d, det):
+    """Non-finite values in one sample must not reach another sample's
+    results: every sample is read through its own tensor maps, so rows past
+    the end of a half read zero instead of the next sample's rows.  Sample 1
+    (and the empty sample 2) sit between samples 0 and 3; inf and NaN are
+    planted in all of sample 1's q, k, v, dout.  Samples 0 and 3 (ragged
+    halves, so their last tiles run into the neighbours) must match the
+    oracle on their own rows, finite everywhere."""
+    halves = [67, 45, 0, 130]
+    H, Hk, bs = 2, 1, 5
+    q, k, v, do, cu = _packed(halves, H, Hk, d, seed=640 + d)
+    a1, e1 = cu[1], cu[2]  # sample 1's rows
+    for t, val in ((q, float("inf")), (k, float("nan")), (v, float("-inf")), (do, float("nan"))):
+        t[a1:e1] = val
+        t[a1 + 1] = float("inf")
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    out, lse = b.dfa_forward_varlen(qd, kd, vd, cu, bs)
+    if det:
+        dq, dk, dv = b.dfa_backward_ex(qd, kd, vd, out, dod, lse, bs, cu_seqlens=cu,
+                                       deterministic=True)
+    else:
+        dq, dk, dv = b.dfa_backward_varlen(qd, kd, vd, out, dod, lse, cu, bs)
+    torch.cuda.synchronize()
+    assert b.dfa_status() == 0
+    qn, kn, vn, don = (_np(t) for t in (q, k, v, do))
+    for s in (0, 3):
+        a, e = cu[s], cu[s + 1]
+        sub = [0, e - a]
+        ro, rl = oracle.diffusion_varlen_forward(qn[a:e], kn[a:e], vn[a:e], sub, bs)
+        rq, rk, rv = oracle.diffusion_varlen_backward(qn[a:e], kn[a:e], vn[a:e], don[a:e], sub,
+                                                      bs)
+        got = {"out": _np(out[a:e]), "dq": _np(dq[a:e]), "dk": _np(dk[a:e]),
+               "dv": _np(dv[a:e])}
+        for name, t in got.items():
+            assert np.isfinite(t).all(), (s, name)
+        g_lse = lse[:, a:e].cpu().double().numpy()
+        assert np.isfinite(g_lse).all()
+        assert np.abs(g_lse - rl).max() <= TOL_LSE
+        errs = _errors(got, {"out": ro, "dq": rq, "dk": rk, "dv": rv})
+        assert errs["out"] <= TOL_OUT, (s, errs)
+        for name in ("dq", "dk", "dv"):
+            assert errs[name] <= TOL_GRAD, (s, errs)

@@ -83,11 +83,25 @@ struct Bwd2Cfg {
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int kQBytes = BMQ * D * 2;
   static constexpr int kDSBytes = BN * BMQ * 2;
+  // Headdim 256: Q and dO go through two rings of 64-dim chunks instead of
+  // whole-tile stages.  An item needs the chunks of the other head-dim half
+  // only for S^T and dP^T, those of its own half also for dV and dK; so the
+  // other half's chunks (OH ring, 2 slots) are released as soon as S^T and
+  // dP^T complete and the own half's (DH ring, 3 slots) after dV and dK,
+  // and the next tile's chunks load while the current tile is still at work
+  // -- K and V (128 KB) leave room for five chunk slots, not two stages.
+  static constexpr bool kChunkRing = D == 256;
+  static constexpr int kOhSlots = 2;
+  static constexpr int kDhSlots = 3;
+  static constexpr int kSlotBytes = 2 * BMQ * 128;  // a Q chunk, then a dO chunk
+  static constexpr int kQBars = kChunkRing ? kOhSlots + kDhSlots : STAGES;
+  static constexpr int kLseBufs = kChunkRing ? 2 : STAGES;  // -LSE, -D buffers
   static constexpr int kOffK = 0;                          // [KVBUF]
   static constexpr int kOffV = kOffK + KVBUF * kKVBytes;   // [KVBUF]
-  static constexpr int kOffQ = kOffV + KVBUF * kKVBytes;
-  static constexpr int kOffDO = kOffQ + STAGES * kQBytes;
-  static constexpr int kOffDS = kOffDO + STAGES * kQBytes;
+  static constexpr int kOffQ = kOffV + KVBUF * kKVBytes;   // ring: the chunk slots
+  static constexpr int kOffDO = kOffQ + STAGES * kQBytes;  // (no ring)
+  static constexpr int kOffDS =
+      kChunkRing ? kOffQ + (kOhSlots + kDhSlots) * kSlotBytes : kOffDO + STAGES * kQBytes;
   // dQ staging, one tile per compute warp: float32 [HC queries][32 head
   // dims], the source of that warp's bulk reduce-add into the accumulator
   // (headdim 128; with 256 the shared memory is full and dQ goes out with
@@ -95,14 +109,14 @@ struct Bwd2Cfg {
   static constexpr bool kTmaDQ = D == 128 && KVBUF == 1;
   static constexpr int kDQSBytes = HC * 32 * 4;
   static constexpr int kOffDQS = kOffDS + kDSBytes;
-  static constexpr int kOffLSE = kOffDQS + (kTmaDQ ? kComputeWarps * kDQSBytes : 0);  // STAGES x BMQ floats
-  static constexpr int kOffDEL = kOffLSE + STAGES * BMQ * 4;  // STAGES x BMQ floats
-  static constexpr int kOffBar = kOffDEL + STAGES * BMQ * 4;
+  static constexpr int kOffLSE = kOffDQS + (kTmaDQ ? kComputeWarps * kDQSBytes : 0);  // kLseBufs x BMQ floats
+  static constexpr int kOffDEL = kOffLSE + kLseBufs * BMQ * 4;  // kLseBufs x BMQ floats
+  static constexpr int kOffBar = kOffDEL + kLseBufs * BMQ * 4;
   enum {
     BAR_KVFULL = 0,  // [KVBUF] K and V of an item loaded
-    BAR_QFULL = KVBUF,
-    BAR_QEMPTY = BAR_QFULL + STAGES,
-    BAR_SDPFULL = BAR_QEMPTY + STAGES,  // S^T and dP^T of a tile computed
+    BAR_QFULL = KVBUF,  // [kQBars] per stage, or per ring slot (OH slots first)
+    BAR_QEMPTY = BAR_QFULL + kQBars,
+    BAR_SDPFULL = BAR_QEMPTY + kQBars,  // S^T and dP^T of a tile computed
     BAR_SDPFREE = BAR_SDPFULL + 1,      // S^T / dP^T read into registers
     BAR_PDSFULL = BAR_SDPFREE + 1,      // P^T / dS^T of a tile in place
     BAR_MMA2 = BAR_PDSFULL + 1,         // dV, dK, dQ of a tile done
@@ -228,9 +242,11 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       mbar_init(BAR(C::BAR_KVFULL + s), 1);
       mbar_init(BAR(C::BAR_ITEMDONE + s), 1);  // the warp issuing dV / dK and dQ
     }
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::kQBars; ++s) {
       mbar_init(BAR(C::BAR_QFULL + s), 1);
-      mbar_init(BAR(C::BAR_QEMPTY + s), 1);
+      // ring: an OH slot is released by the S^T and the dP^T warps, a DH
+      // slot (like a stage) by the warp issuing dV / dK
+      mbar_init(BAR(C::BAR_QEMPTY + s), C::kChunkRing && s < C::kOhSlots ? 2 : 1);
     }
     mbar_init(BAR(C::BAR_SDPFULL), 2);  // the S^T and the dP^T warps
     mbar_init(BAR(C::BAR_SDPFREE), C::kComputeWarps);
@@ -277,9 +293,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
     }
     bool ok = true;
     int g = 0, k = 0, q_issued = 0, kv_issued = 0;
-    // Q, dO, -LSE * log2(e) and -D of the item's t-th query tile into the
-    // stage of global tile gg.
-    auto load_q = [&](const Bwd2Item& it, int t, int gg) -> bool {
+    // -LSE * log2(e) and -D of the item's t-th query tile, read into
+    // registers (stage_rows) and stored into buffer `buf` (store_rows).
+    float lse_r[2], del_r[2];
+    auto stage_rows = [&](const Bwd2Item& it, int t) {
       int hh, l;
       it.template split<GQA>(t, hh, l);
       const int qt = it.ltile(l);
@@ -287,7 +304,6 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       const int h = it.h0 + hh;  // query head
       // lse and delta: laid out alike, (batch, heads, 2n) (causal:
       // (sequences, heads, n)) or, varlen, (heads, rows)
-      float lse_r[2], del_r[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int q = qt * BMQ + lane + 32 * e;
@@ -299,21 +315,36 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
         // -D * scale: the softmax scale is folded into dS (see the compute)
         del_r[e] = valid ? -p.delta[off] * p.scale : 0.f;
       }
-      const int st = gg % STAGES;
-      const int round = gg / STAGES;
-      if (round > 0) {
-        int w = 0;
-        if (lane == 0) w = mbar_wait(BAR(C::BAR_QEMPTY + st), (round - 1) & 1, ab) ? 1 : 0;
-        if (__shfl_sync(0xffffffffu, w, 0) == 0) return false;
-      }
-      float* lse_s = reinterpret_cast<float*>(smem + C::kOffLSE) + st * BMQ;
-      float* del_s = reinterpret_cast<float*>(smem + C::kOffDEL) + st * BMQ;
+    };
+    auto store_rows = [&](int buf) {
+      float* lse_s = reinterpret_cast<float*>(smem + C::kOffLSE) + buf * BMQ;
+      float* del_s = reinterpret_cast<float*>(smem + C::kOffDEL) + buf * BMQ;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         lse_s[lane + 32 * e] = lse_r[e];
         del_s[lane + 32 * e] = del_r[e];
       }
       __syncwarp();
+    };
+    // Lane 0 waits on `bar` for `parity`; false when the wait gave up.
+    auto warp_wait = [&](uint32_t bar, int parity) -> bool {
+      int w = 0;
+      if (lane == 0) w = mbar_wait(bar, parity, ab) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, w, 0) != 0;
+    };
+    // Q, dO, -LSE * log2(e) and -D of the item's t-th query tile into the
+    // stage of global tile gg.
+    auto load_q = [&](const Bwd2Item& it, int t, int gg) -> bool {
+      int hh, l;
+      it.template split<GQA>(t, hh, l);
+      const int qt = it.ltile(l);
+      const int half = it.lhalf(l);
+      const int h = it.h0 + hh;  // query head
+      stage_rows(it, t);
+      const int st = gg % STAGES;
+      const int round = gg / STAGES;
+      if (round > 0 && !warp_wait(BAR(C::BAR_QEMPTY + st), (round - 1) & 1)) return false;
+      store_rows(st);
       if (lane == 0) {
         mbar_arrive_expect_tx(BAR(C::BAR_QFULL + st), 2 * C::kQBytes);
         // Varlen: the sample's own maps (rows past its halves read zero).
@@ -330,6 +361,60 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       }
       __syncwarp();
       q_issued = gg + 1;
+      return true;
+    };
+    // Ring (headdim 256): the Q and dO chunks c of the item's t-th query
+    // tile into ring slot `slot` (lane 0).
+    int oh_last = -1, dh_last = -1;  // last tile with OH chunks, last DH chunk issued
+    auto ring_chunk = [&](const Bwd2Item& it, int t, int c, int slot) {
+      int hh, l;
+      it.template split<GQA>(t, hh, l);
+      const int qt = it.ltile(l);
+      const int h = it.h0 + hh;
+      const CUtensorMap* mq = VARLEN ? &p.vl_maps[it.slot].q : &p.tm_q;
+      const CUtensorMap* mdo = VARLEN ? &p.vl_maps[it.slot].dout : &p.tm_do;
+      const HalfRows qr = in_rows<VARLEN>(it.wi.b, it.lhalf(l));
+      const uint32_t dst = sbase + C::kOffQ + slot * C::kSlotBytes;
+      mbar_arrive_expect_tx(BAR(C::BAR_QFULL + slot), C::kSlotBytes);
+      tma_load_5d(dst, mq, BAR(C::BAR_QFULL + slot), 64 * c, h, qr.base + qt * BMQ, qr.c3, qr.c4);
+      tma_load_5d(dst + BMQ * 128, mdo, BAR(C::BAR_QFULL + slot), 64 * c, h, qr.base + qt * BMQ,
+                  qr.c3, qr.c4);
+    };
+    // Tile gg's first own-half chunk (with its -LSE, -D rows) and its two
+    // other-half chunks.  DH chunk s = 2 gg + j goes to slot kOhSlots + s % 3;
+    // that slot last held chunk s - 3, of tile gg - 2 (j = 0), whose dV / dK
+    // are then complete -- and with them the compute that read the rows
+    // buffer gg & 1.  The OH slots last held tile gg - 1's chunks, free once
+    // its S^T and dP^T are complete.
+    auto ring_first = [&](const Bwd2Item& it, int t, int gg) -> bool {
+      const int s0 = 2 * gg;
+      const int slot0 = C::kOhSlots + s0 % C::kDhSlots;
+      stage_rows(it, t);
+      if (s0 >= C::kDhSlots &&
+          !warp_wait(BAR(C::BAR_QEMPTY + slot0), (s0 / C::kDhSlots - 1) & 1))
+        return false;
+      store_rows(gg & 1);
+      if (lane == 0) ring_chunk(it, t, 2 * it.dh, slot0);
+      dh_last = s0;
+      for (int i = 0; i < C::kOhSlots; ++i) {
+        if (gg >= 1 && !warp_wait(BAR(C::BAR_QEMPTY + i), (gg - 1) & 1)) return false;
+        if (lane == 0) ring_chunk(it, t, 2 * (1 - it.dh) + i, i);
+      }
+      oh_last = gg;
+      __syncwarp();
+      return true;
+    };
+    // Tile gg's second own-half chunk: its slot last held chunk 2 gg - 2, of
+    // tile gg - 1.
+    auto ring_last = [&](const Bwd2Item& it, int t, int gg) -> bool {
+      const int s1 = 2 * gg + 1;
+      const int slot1 = C::kOhSlots + s1 % C::kDhSlots;
+      if (s1 >= C::kDhSlots &&
+          !warp_wait(BAR(C::BAR_QEMPTY + slot1), (s1 / C::kDhSlots - 1) & 1))
+        return false;
+      if (lane == 0) ring_chunk(it, t, 2 * it.dh + 1, slot1);
+      dh_last = s1;
+      __syncwarp();
       return true;
     };
     while (ok) {
@@ -355,7 +440,13 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       // waits for the whole item; with two the K / V load goes first.
       const int kvs = k % C::KVBUF;
       const int pre = C::KVBUF == 1 ? imin(it.ntiles, STAGES - 1) : 0;
-      for (int t = 0; t < pre && ok; ++t) ok = load_q(it, t, g + t);
+      if constexpr (C::kChunkRing) {
+        // the first tile's chunks that the current item frees before its
+        // last products go ahead of the K / V load
+        if (it.ntiles > 0) ok = ring_first(it, 0, g);
+      } else {
+        for (int t = 0; t < pre && ok; ++t) ok = load_q(it, t, g + t);
+      }
       if (!ok) break;
       if (k >= C::KVBUF) {
         int w = 0;
@@ -380,7 +471,14 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       }
       __syncwarp();
       kv_issued = k + 1;
-      for (int t = pre; t < it.ntiles && ok; ++t) ok = load_q(it, t, g + t);
+      if constexpr (C::kChunkRing) {
+        for (int t = 0; t < it.ntiles && ok; ++t) {
+          if (t > 0) ok = ring_first(it, t, g + t);
+          if (ok) ok = ring_last(it, t, g + t);
+        }
+      } else {
+        for (int t = pre; t < it.ntiles && ok; ++t) ok = load_q(it, t, g + t);
+      }
       g += it.ntiles;
       ++k;
     }
@@ -389,8 +487,17 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       if (kv_issued > 0)
         mbar_wait_limited(BAR(C::BAR_KVFULL + (kv_issued - 1) % C::KVBUF),
                           ((kv_issued - 1) / C::KVBUF) & 1, 100000000ull);
-      for (int t = (q_issued > STAGES ? q_issued - STAGES : 0); t < q_issued; ++t)
-        mbar_wait_limited(BAR(C::BAR_QFULL + t % STAGES), (t / STAGES) & 1, 100000000ull);
+      if constexpr (C::kChunkRing) {
+        if (oh_last >= 0)
+          for (int i = 0; i < C::kOhSlots; ++i)
+            mbar_wait_limited(BAR(C::BAR_QFULL + i), oh_last & 1, 100000000ull);
+        for (int s = (dh_last >= C::kDhSlots ? dh_last - C::kDhSlots + 1 : 0); s <= dh_last; ++s)
+          mbar_wait_limited(BAR(C::BAR_QFULL + C::kOhSlots + s % C::kDhSlots),
+                            (s / C::kDhSlots) & 1, 100000000ull);
+      } else {
+        for (int t = (q_issued > STAGES ? q_issued - STAGES : 0); t < q_issued; ++t)
+          mbar_wait_limited(BAR(C::BAR_QFULL + t % STAGES), (t / STAGES) & 1, 100000000ull);
+      }
     }
     __syncwarp();
    } else {
@@ -423,6 +530,42 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           const uint64_t dK_kmaj = adv(dK_kmaj0, kvs * C::kKVBytes);
           const uint64_t dV_kmaj = adv(dV_kmaj0, kvs * C::kKVBytes);
           if (!(ok = mbar_wait(BAR(C::BAR_KVFULL + kvs), (k / C::KVBUF) & 1, ab))) break;
+          if constexpr (C::kChunkRing) {
+            // S^T = K Q^T or dP^T = V dO^T chunk by chunk, in the order the
+            // chunks arrive: own-half chunk 0, the other half's two (whose
+            // slots are then released), own-half chunk 1.
+            const uint32_t acc = dp ? C::kTmemDP : C::kTmemS;
+            const uint64_t a0 = dp ? dV_kmaj : dK_kmaj;
+            auto chunk = [&](int c, int slot, bool first) {
+              const uint64_t b = sdesc_sw128(
+                  sbase + C::kOffQ + slot * C::kSlotBytes + (dp ? BMQ * 128 : 0), 16, 1024);
+#pragma unroll
+              for (int sub = 0; sub < 4; ++sub)
+                mma_ss(tmem + acc, adv(a0, c * (BN * 128) + sub * 32), adv(b, sub * 32), kIdS,
+                       (first && sub == 0) ? 0u : 1u);
+            };
+            for (int i = 0; i < it.ntiles && ok; ++i) {
+              const int gg = g + i;
+              const int s0 = 2 * gg, s1 = s0 + 1;
+              const int slot0 = C::kOhSlots + s0 % C::kDhSlots;
+              const int slot1 = C::kOhSlots + s1 % C::kDhSlots;
+              if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_SDPFREE), (gg - 1) & 1, ab))) break;
+              if (!(ok = mbar_wait(BAR(C::BAR_QFULL + slot0), (s0 / C::kDhSlots) & 1, ab))) break;
+              tc_fence_after();
+              chunk(2 * it.dh, slot0, true);
+              for (int j = 0; j < C::kOhSlots && ok; ++j) {
+                if (!(ok = mbar_wait(BAR(C::BAR_QFULL + j), gg & 1, ab))) break;
+                tc_fence_after();
+                chunk(2 * (1 - it.dh) + j, j, false);
+              }
+              if (!ok) break;
+              for (int j = 0; j < C::kOhSlots; ++j) mma_commit(BAR(C::BAR_QEMPTY + j));
+              if (!(ok = mbar_wait(BAR(C::BAR_QFULL + slot1), (s1 / C::kDhSlots) & 1, ab))) break;
+              tc_fence_after();
+              chunk(2 * it.dh + 1, slot1, false);
+              mma_commit(BAR(C::BAR_SDPFULL));
+            }
+          } else {
           for (int i = 0; i < it.ntiles && ok; ++i) {
             const int gg = g + i;
             const int st = gg % STAGES;
@@ -442,6 +585,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
               mma_ss(tmem + acc, adv(a0, koff), adv(b0, st_off + qoff), kIdS, kk > 0 ? 1u : 0u);
             }
             mma_commit(BAR(C::BAR_SDPFULL));
+          }
           }
           g += it.ntiles;
           ++k;
@@ -471,18 +615,43 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
             if (!(ok = mbar_wait(BAR(C::BAR_PDSFULL), gg & 1, ab))) break;
             tc_fence_after();
             const uint32_t pds = tmem + C::kTmemPDS;
+            if constexpr (C::kChunkRing) {
+              // dV, dK of the item's head-dim half, 64 dims (one chunk of dO
+              // and of Q, in its ring slot) at a time; then both slots are free.
+              constexpr uint32_t kIdKV64 = idesc_bf16(BN, 64, false, true);
 #pragma unroll
-            for (int kk = 0; kk < BMQ / 16; ++kk) {
-              // queries [16kk, 16kk+16): chunk kk/2, P^T first 16 columns, dS^T last 16
-              const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
-              const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-              mma_ts(tmem + C::kTmemDV, pds + col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV,
-                     acc);
-              mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128),
-                     kIdKV, acc);
+              for (int j = 0; j < 2; ++j) {
+                const uint32_t slot_base =
+                    sbase + C::kOffQ +
+                    (C::kOhSlots + (2 * gg + j) % C::kDhSlots) * C::kSlotBytes;
+                const uint64_t q_mn = sdesc_sw128(slot_base, BMQ * 128, 1024);
+                const uint64_t o_mn = sdesc_sw128(slot_base + BMQ * 128, BMQ * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BMQ / 16; ++kk) {
+                  const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+                  const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                  mma_ts(tmem + C::kTmemDV + 64 * j, pds + col, adv(o_mn, kk * 16 * 128), kIdKV64,
+                         acc);
+                  mma_ts(tmem + C::kTmemDK + 64 * j, pds + col + 16, adv(q_mn, kk * 16 * 128),
+                         kIdKV64, acc);
+                }
+              }
+              mma_commit(BAR(C::BAR_QEMPTY + C::kOhSlots + (2 * gg) % C::kDhSlots));
+              mma_commit(BAR(C::BAR_QEMPTY + C::kOhSlots + (2 * gg + 1) % C::kDhSlots));
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < BMQ / 16; ++kk) {
+                // queries [16kk, 16kk+16): chunk kk/2, P^T first 16 columns, dS^T last 16
+                const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                mma_ts(tmem + C::kTmemDV, pds + col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV,
+                       acc);
+                mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128),
+                       kIdKV, acc);
+              }
+              // dQ^T reads no Q / dO: the stage is free once dV / dK are done.
+              mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
             }
-            // dQ^T reads no Q / dO: the stage is free once dV / dK are done.
-            mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
             // The DQ columns still hold dQ of tile gg-1 until it has been read out.
             if (gg >= 1 && !(ok = mbar_wait(BAR(C::BAR_DQFREE), (gg - 1) & 1, ab))) break;
             tc_fence_after();
@@ -611,7 +780,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       };
       for (int i = 0; i < it.ntiles && ok; ++i) {
         const int gg = g + i;
-        const int st = gg % STAGES;
+        const int st = C::kChunkRing ? (gg & 1) : gg % STAGES;  // -LSE, -D buffer
         int hh, l;
         it.template split<GQA>(i, hh, l);
         const int qs = it.ltile(l) * BMQ;

@@ -27,10 +27,14 @@
 // current item ends, and K / V reload once the current item's products are
 // done.  At the end of an item warpgroup 0 writes dV and warpgroup 1 dK; the
 // next item's first dV / dK products wait until both have been read out.
-// Warp roles (384 threads): two compute warpgroups, warpgroup b handling the
-// query tiles with g % 2 == b (thread t of a warpgroup owns key row t of the
-// tile, TMEM lane t), so that the MMAs of one tile overlap the
-// softmax-gradient work of the other; warp 8 loads (TMA for Q/dO, plain loads
+// Warp roles (384 threads): two compute warpgroups that both work on every
+// query tile, warpgroup b on its query columns [64 b, 64 b + 64) (thread t
+// of a warpgroup owns key row t of the tile, TMEM lane t): with one dP
+// buffer, dP^T of a tile waits for the dV / dK products of the tile before
+// it, so tiles follow one another and the softmax-gradient work of a tile
+// is split between the warpgroups rather than alternated; the dQ of a tile
+// is added during the next tile's turn, each warpgroup adding 32 of its head
+// dims.  Warp 8 loads (TMA for Q/dO, plain loads
 // for LSE/D); warp 9 issues S^T, warp 10 dP^T, dV and dK, warp 11 dQ (on
 // three schedulers, so that the busy compute warps sharing a scheduler with
 // one of them do not starve the tensor pipe).  The load/MMA
@@ -194,9 +198,9 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(C::BAR_SFULL + b), 1);
       mbar_init(BAR(C::BAR_DPFULL + b), 1);
-      mbar_init(BAR(C::BAR_PDS + b), 4);    // warps of the tile's warpgroup
+      mbar_init(BAR(C::BAR_PDS + b), 8);    // every compute warp
       mbar_init(BAR(C::BAR_MMA2 + b), 1);
-      mbar_init(BAR(C::BAR_DQFREE + b), 4);
+      mbar_init(BAR(C::BAR_DQFREE + b), 8);
     }
     mbar_init(BAR(C::BAR_ITEMDONE), 2);  // warps 10 and 11
     mbar_init(BAR(C::BAR_ACCFREE), 8);
@@ -498,16 +502,17 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     const uint64_t dscale2 = f2_pack(p.scale, p.scale);
 
     // dQ of global tile gg (TMEM S[gg % 2], lane = query `row` of the tile,
-    // columns = head dims), added to dq_acc with 16-byte atomics.
+    // columns = head dims), added to dq_acc with 16-byte atomics; warpgroup
+    // wg adds head dims [32 wg, 32 wg + 32) of every query row.
     auto drain_dq = [&](const BwdItem& it, int gg, int t) -> bool {
+      constexpr int DW = D / 2;  // head dims per warpgroup
       const int b = gg & 1;
       if (!mbar_wait_warp(BAR(C::BAR_MMA2 + b), (gg >> 1) & 1, ab)) return false;
       tc_fence_after();
-      uint32_t dq[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(t_lane + C::kTmemS + b * BMQ + 32 * c, dq + 32 * c);
+      uint32_t dq[DW];
+      tmem_ld32(t_lane + C::kTmemS + b * BMQ + DW * wg, dq);
       tmem_wait_ld();
-      tmem_pin<D>(dq);
+      tmem_pin<DW>(dq);
       tc_fence_before();
       mbar_arrive_warp(BAR(C::BAR_DQFREE + b));
       int hh, l;
@@ -524,13 +529,14 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
                                    it.ltile(l), it.wi.half, it.wi.tile);
         sem = p.dq_sem + static_cast<size_t>(it.h0 + hh) * p.sem_rows + first +
               static_cast<size_t>(it.lhalf(l)) * n + qs;
-        if (!sem_wait_warp(sem, static_cast<unsigned>(4 * ord), ab)) return false;
+        // the 8 compute warps of every earlier contribution have signalled
+        if (!sem_wait_warp(sem, static_cast<unsigned>(8 * ord), ab)) return false;
       }
       if (q < n) {
         const size_t pos = static_cast<size_t>(it.lhalf(l)) * n + q;
-        float* dst = p.dq_acc + ((first + pos) * p.H + it.h0 + hh) * D;
+        float* dst = p.dq_acc + ((first + pos) * p.H + it.h0 + hh) * D + DW * wg;
 #pragma unroll
-        for (int c = 0; c < D; c += 4)
+        for (int c = 0; c < DW; c += 4)
           red_add_v4_f32(dst + c, __uint_as_float(dq[c]), __uint_as_float(dq[c + 1]),
                          __uint_as_float(dq[c + 2]), __uint_as_float(dq[c + 3]));
       }
@@ -612,7 +618,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       const int bs = VARLEN ? it.bs : p.bs;
       const Interval iv0 = query_interval(it.rule0, j, n, bs);
       const Interval iv1 = query_interval(it.rule1, j, n, bs);
-      for (int i = ((g & 1) == wg) ? 0 : 1; i < it.ntiles && ok; i += 2) {
+      // Both warpgroups work on every tile, warpgroup wg on query columns
+      // [64 wg, 64 wg + 64); a tile's dQ is added during the next tile's
+      // turn, so its product has completed by then.
+      for (int i = 0; i < it.ntiles && ok; ++i) {
         const int gg = g + i;
         const int st = gg % STAGES;
         const int b = gg & 1;
@@ -638,15 +647,18 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         }
         const uint32_t s_col = t_lane + C::kTmemS + b * BMQ;
         const uint32_t ds_s = sbase + C::kOffDS + b * C::kDSBytes;
-        slice(0, s_col, ds_s, nlse_s, ndel_s, keep[0], keep[1]);
-        slice(1, s_col, ds_s, nlse_s, ndel_s, keep[2], keep[3]);
+        if (wg == 0)
+          slice(0, s_col, ds_s, nlse_s, ndel_s, keep[0], keep[1]);
+        else
+          slice(1, s_col, ds_s, nlse_s, ndel_s, keep[2], keep[3]);
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive_warp(BAR(C::BAR_PDS + b));
-        if (!(ok = drain_dq(it, gg, i))) break;
+        if (i >= 1 && !(ok = drain_dq(it, gg - 1, i - 1))) break;
       }
       if (!ok) break;
+      if (it.ntiles > 0 && !(ok = drain_dq(it, g + it.ntiles - 1, it.ntiles - 1))) break;
 
       // -------------------------------------------------------- item epilogue
       // Warpgroup 0 writes dV, warpgroup 1 writes dK, once the item's MMAs

@@ -617,13 +617,14 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
             const uint32_t pds = tmem + C::kTmemPDS;
             if constexpr (C::kChunkRing) {
               // dV, dK of the item's head-dim half, 64 dims (one chunk of dO
-              // and of Q, in its ring slot) at a time; then both slots are free.
+              // and of Q, in its ring slot) at a time; each slot is released
+              // once its own products complete (the next tile's second chunk
+              // goes into the first one's slot).
               constexpr uint32_t kIdKV64 = idesc_bf16(BN, 64, false, true);
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
-                const uint32_t slot_base =
-                    sbase + C::kOffQ +
-                    (C::kOhSlots + (2 * gg + j) % C::kDhSlots) * C::kSlotBytes;
+                const int slot = C::kOhSlots + (2 * gg + j) % C::kDhSlots;
+                const uint32_t slot_base = sbase + C::kOffQ + slot * C::kSlotBytes;
                 const uint64_t q_mn = sdesc_sw128(slot_base, BMQ * 128, 1024);
                 const uint64_t o_mn = sdesc_sw128(slot_base + BMQ * 128, BMQ * 128, 1024);
 #pragma unroll
@@ -635,9 +636,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
                   mma_ts(tmem + C::kTmemDK + 64 * j, pds + col + 16, adv(q_mn, kk * 16 * 128),
                          kIdKV64, acc);
                 }
+                mma_commit(BAR(C::BAR_QEMPTY + slot));
               }
-              mma_commit(BAR(C::BAR_QEMPTY + C::kOhSlots + (2 * gg) % C::kDhSlots));
-              mma_commit(BAR(C::BAR_QEMPTY + C::kOhSlots + (2 * gg + 1) % C::kDhSlots));
             } else {
 #pragma unroll
               for (int kk = 0; kk < BMQ / 16; ++kk) {

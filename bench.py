@@ -61,6 +61,7 @@ PER_CONFIG = ("tiny", "small", "long", "hd256_bs1", "hd256_bs64", "hd256_bs128")
 ROUND_MS = 300.0
 ROUNDS = 10
 L2_FLUSH_BYTES = 512 << 20
+GB300_L2_BYTES = 126 << 20  # nominal; the GPU arm uses the device's own figure
 FLUSHED_STEPS = 100
 CSRC = os.path.join(ROOT, "block_diffusion_masked_gb300", "csrc")
 PROFILES = os.path.join(ROOT, "profiles")
@@ -374,6 +375,7 @@ def time_workload(args, w, dev, world):
     st = Steps(w, dev)
     stream = _stream(st.q)
     flush = st.input_bytes < torch.cuda.get_device_properties(dev).L2_cache_size
+    l2 = l2_note(st.input_bytes, flush)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     arms = (("diff", st.diff), ("causal", st.causal))
 
@@ -465,10 +467,7 @@ def time_workload(args, w, dev, world):
                    "round_ms_median": {k_: float(np.median(v_)) * spr[k_]
                                        for k_, v_ in rounds.items()},
                    "spread_pct": 100.0 * (max(rounds["diff"]) - min(rounds["diff"])) / ms,
-                   "l2": ("inputs fit in L2: 512 MB flush before every step, outside the timed "
-                          "interval" if flush else
-                          f"inputs ({st.input_bytes / 1e6:.0f} MB of q/k/v/dout) larger than "
-                          f"L2: no flush")},
+                   "l2": l2},
         "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
         "bwd_tflops": f_bwd / ((pre_ms + main_ms + conv_ms) * 1e-3) / 1e12,
         "kernel_ms": dict(zip(names, kparts["diff"])),
@@ -593,6 +592,13 @@ def sdpa_causal(qc, kc, vc, doc, warmup, steps):
     return e0.elapsed_time(e1) / steps
 
 
+def l2_note(input_bytes, flush):
+    """How the timed steps treat L2 (the same text on both arms)."""
+    if flush:
+        return "inputs fit in L2: 512 MB flush before every step, outside the timed interval"
+    return f"inputs ({input_bytes / 1e6:.0f} MB of q/k/v/dout) larger than L2: no flush"
+
+
 def _config(w, world, l2):
     return {"workload": w.name, "batch": w.batch, "n": w.n, "seqlen": 2 * w.n,
             "heads": w.heads, "headdim": w.headdim, "block_size": w.block_size,
@@ -674,6 +680,19 @@ def run_profile(args):
     print(json.dumps({"profiled": args.profile_workload, "steps": args.profile_steps}))
 
 
+def algorithmic_bytes(w, backward):
+    """Bytes a launch must move at least, as the step runs it: forward reads
+    q, k, v, writes out and lse, and zeroes the float32 dq accumulator;
+    backward main reads q, k, v, dout, lse, D, writes dk, dv and reads and
+    writes the float32 dq accumulator once."""
+    T = w.batch * 2 * w.n * w.heads * w.headdim  # elements of one tensor
+    rows = w.batch * w.heads * 2 * w.n
+    if backward:
+        return 4 * 2 * T + 2 * 4 * rows + 2 * 2 * T + 2 * 4 * T, \
+            "q, k, v, dout, lse, D read; dk, dv written; dq accumulator read and written"
+    return 4 * 2 * T + 4 * rows + 4 * T, "q, k, v read; out, lse written; dq accumulator zeroed"
+
+
 def summarize_ncu(args):
     """Write a profiles/ summary of an ncu --csv capture of one kernel.
 
@@ -714,7 +733,9 @@ def summarize_ncu(args):
     tens = val("sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active", scale)
     w = inputs.WORKLOADS[args.workload]
     f_fwd, f_bwd = flops(w)
-    algo = f_bwd if "bwd" in args.kernel else f_fwd
+    is_bwd = "bwd" in args.kernel
+    algo = f_bwd if is_bwd else f_fwd
+    algo_bytes, algo_what = algorithmic_bytes(w, is_bwd)
     lines = [f"# {args.kernel} on {args.workload}", "",
              f"Workload: B {w.batch}, n {w.n}, H {w.heads}, d {w.headdim}, bs {w.block_size}.",
              f"Launches captured: {len(rd)}.", "",
@@ -723,14 +744,16 @@ def summarize_ncu(args):
              f"- source_sha256: {source_hash(args.kernel)}",
              f"- dram_bytes_per_launch: {traffic:.6g}",
              f"- dram_read_bytes: {np.mean(rd):.6g}",
-             f"- dram_write_bytes: {np.mean(wr):.6g}"]
+             f"- dram_write_bytes: {np.mean(wr):.6g}",
+             f"- algorithmic_bytes: {algo_bytes:.6g} ({algo_what})",
+             f"- traffic / algorithmic: {traffic / algo_bytes:.2f}"]
     if dur:
         lines.append(f"- ncu_duration_us (serialised, cold): {np.mean(dur) * 1e6:.1f}")
         lines.append(f"- algorithmic_tflops_at_ncu_duration: {algo / np.mean(dur) / 1e12:.1f}")
     if tens:
         lines.append(f"- tensor_pipe_active_pct: {np.mean(tens):.1f}")
-    lines += ["", "Command (GB300, under gpurun-style remote execution of committed files):", "",
-              "```", args.command or "(not given)", "```", ""]
+    lines += ["", "Command (one GB300, from the repository root; the plain run must exit 0 "
+              "before the capture):", "", "```", args.command or "(not given)", "```", ""]
     with open(args.out, "w") as f:
         f.write("\n".join(lines))
     print(args.out, traffic)
@@ -749,7 +772,8 @@ def run_reference(args, rank, world):
     value = float(np.median(per_step))
     base = dict(base)
     base["value"] = value
-    cfg = _config(w, world, "n/a: host CPU")
+    nbytes = 4 * w.batch * 2 * w.n * w.heads * w.headdim * 2
+    cfg = _config(w, world, l2_note(nbytes, nbytes < GB300_L2_BYTES))
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
             "n_gpus": world, "steps": len(per_step), "warmup": args.warmup,
             "ms_per_step": None, "higher_is_better": True, "scaling": "weak",

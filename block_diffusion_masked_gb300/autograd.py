@@ -86,5 +86,5 @@ def diffusion_attn_func(q, k, v, block_size):
 
 
 def causal_attn_func(q, k, v):
-    """Causal attention on (Bc, L, H, d), Bc even; the yardstick kernels."""
+    """Causal attention on (Bc, L, H, d), any Bc; the yardstick kernels."""
     return CausalAttnFunc.apply(q, k, v)

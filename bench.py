@@ -793,7 +793,9 @@ def run_variant(args, w):
 
     gqa: k and v with heads // 4 heads (the step API); step: the same step
     API with every head its own key/value head (the baseline of gqa);
-    onecall: the one-call API, multi-head; varlen: the samples of
+    onecall: the one-call API, multi-head; diagpass: the step API with the
+    noisy-diagonal backward option (DFA_NOISY_DIAG_PASS; step is its
+    baseline); varlen: the samples of
     VARLEN_HALVES (scaled to the workload's rows) packed along the rows;
     fp8: the FP8 forward.  FLOPs count the visible pairs of every sample.
     """
@@ -806,7 +808,7 @@ def run_variant(args, w):
     binding.lib()
     stream = torch.cuda.current_stream(dev)
     H, d, bs = w.heads, w.headdim, w.block_size
-    if args.variant in ("gqa", "onecall", "step"):
+    if args.variant in ("gqa", "onecall", "step", "diagpass"):
         Hk = max(1, H // 4) if args.variant == "gqa" else H
         q, _, _, do = inputs.make_workload_inputs(w)
         _, k, v = inputs.make_inputs(w.batch, w.n, Hk, d, seed=w.seed + 1, with_dout=False)
@@ -825,6 +827,9 @@ def run_variant(args, w):
             delta = torch.empty((B_, H, L_), dtype=torch.float32, device=dev)
             dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
             shape["api"] = "step (forward zeroing dq_acc, preprocess, main, convert)"
+            diag = args.variant == "diagpass"
+            if diag:
+                shape["api"] += ", noisy-diagonal pass"
 
             def fwd():
                 binding.dfa_fwd_main_gqa(q, k, v, out, lse, dq_acc, bs)
@@ -832,7 +837,8 @@ def run_variant(args, w):
 
             def bwd(o, l):
                 binding.dfa_bwd_preprocess(o, do, delta, None)
-                binding.dfa_bwd_main_gqa(q, k, v, do, l, delta, dq_acc, dk, dv, bs)
+                binding.dfa_bwd_main_ex(q, k, v, do, l, delta, dq_acc, dk, dv, bs,
+                                        noisy_diag_pass=diag)
                 binding.dfa_bwd_dq_convert(dq_acc, dq)
     elif args.variant == "fp8":
         # forward only: per-tensor e4m3 quantisation of the workload's q, k, v
@@ -933,9 +939,9 @@ def main():
     ap.add_argument("--headline-only", action="store_true", help="skip the per_config workloads")
     ap.add_argument("--sdpa", action="store_true", help="also time torch SDPA causal (context)")
     ap.add_argument("--variant", default="mha",
-                    choices=["mha", "onecall", "step", "gqa", "varlen", "fp8"],
-                    help="gqa / step / onecall / varlen / fp8: time that API on that version "
-                    "of the workload (fp8: the forward alone)")
+                    choices=["mha", "onecall", "step", "diagpass", "gqa", "varlen", "fp8"],
+                    help="gqa / step / diagpass / onecall / varlen / fp8: time that API on that "
+                    "version of the workload (fp8: the forward alone)")
     ap.add_argument("--profile-workload", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--profile-steps", type=int, default=3)
     ap.add_argument("--summarize-ncu")

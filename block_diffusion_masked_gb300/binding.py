@@ -25,6 +25,7 @@ DFA_ECUDA = -3
 DFA_ETIMEOUT = -4
 DFA_EDEVICE = -5
 DFA_DETERMINISTIC = 1
+DFA_NOISY_DIAG_PASS = 2
 MODE_DIFFUSION = 0
 MODE_CAUSAL = 1
 
@@ -59,6 +60,7 @@ _SIGNATURES = {
     "dfa_bwd_dq_convert_ex": (_I, [_P] * 2 + [_I] * 5 + [_P]),
     "dfa_fwd_main_gqa": (_I, [_P] * 6 + [_I] * 7 + [_P]),
     "dfa_bwd_main_gqa": (_I, [_P] * 9 + [_I] * 7 + [_P]),
+    "dfa_bwd_main_ex": (_I, [_P] * 9 + [_I] * 8 + [_P]),
     "dfa_fwd_segments": (_I, [_I] * 7 + [ctypes.POINTER(_I)]),
     "dfa_bwd_segments": (_I, [_I] * 7 + [ctypes.POINTER(_I)]),
     "dfa_tile_full": (_I, [_I] * 7),
@@ -374,11 +376,13 @@ def dfa_forward_fp8_vt(q, k, vt, kv_heads, q_descale, k_descale, v_descale, bloc
 
 
 def dfa_backward_ex(q, k, v, out, dout, lse, block_size, cu_seqlens=None, deterministic=False,
-                    dq=None, dk=None, dv=None):
+                    dq=None, dk=None, dv=None, noisy_diag_pass=False):
     """Backward with options: batched (q 4-D) or packed (q 3-D, ``cu_seqlens``).
 
     ``deterministic``: dQ contributions are added in a fixed order, so the
-    results are bitwise reproducible.
+    results are bitwise reproducible.  ``noisy_diag_pass``: the noisy key
+    tiles in a launch of their own before the clean ones, where the block
+    size allows it (DFA_NOISY_DIAG_PASS).
     """
     if cu_seqlens is None:
         Hk = _check_grouped(q, k, v, out, dout)
@@ -398,7 +402,8 @@ def dfa_backward_ex(q, k, v, out, dout, lse, block_size, cu_seqlens=None, determ
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    flags = DFA_DETERMINISTIC if deterministic else 0
+    flags = (DFA_DETERMINISTIC if deterministic else 0) | \
+        (DFA_NOISY_DIAG_PASS if noisy_diag_pass else 0)
     with torch.cuda.device(q.device):
         rc = lib().dfa_backward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
                                    _ptr(dq), _ptr(dk), _ptr(dv), cu, batch, n, H, Hk, d,
@@ -533,6 +538,23 @@ def dfa_bwd_main_gqa(q, k, v, dout, lse, delta, dq_acc, dk, dv, block_size, mode
                                     _ptr(delta), _ptr(dq_acc), _ptr(dk), _ptr(dv), B, n, H,
                                     Hk, d, int(block_size), int(mode), _stream_ptr(q))
     _check("dfa_bwd_main_gqa", rc)
+
+
+def dfa_bwd_main_ex(q, k, v, dout, lse, delta, dq_acc, dk, dv, block_size, mode=MODE_DIFFUSION,
+                    noisy_diag_pass=False):
+    """dfa_bwd_main_gqa with flags (``noisy_diag_pass``: DFA_NOISY_DIAG_PASS)."""
+    Hk = _check_grouped(q, k, v, dout)
+    B, n, L = _step_shape(q, mode)
+    H, d = q.shape[2], q.shape[3]
+    _check_scratch(q, lse, delta, dq_acc)
+    _check_buf(dk, k.shape, torch.bfloat16, q.device, "dk")
+    _check_buf(dv, v.shape, torch.bfloat16, q.device, "dv")
+    flags = DFA_NOISY_DIAG_PASS if noisy_diag_pass else 0
+    with torch.cuda.device(q.device):
+        rc = lib().dfa_bwd_main_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse),
+                                   _ptr(delta), _ptr(dq_acc), _ptr(dk), _ptr(dv), B, n, H,
+                                   Hk, d, int(block_size), int(mode), flags, _stream_ptr(q))
+    _check("dfa_bwd_main_ex", rc)
 
 
 def dfa_bwd_dq_convert(dq_acc, dq, mode=MODE_DIFFUSION):

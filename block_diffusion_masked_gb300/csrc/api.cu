@@ -370,7 +370,7 @@ bool aligned_all(std::initializer_list<const void*> ps) {
 int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const void* dout,
                   const float* lse, const float* delta, float* dq_acc, void* dk, void* dv, int B,
                   int n, int H, int Hk, int d, int bs, cudaStream_t stream,
-                  unsigned* dq_sem = nullptr) {
+                  unsigned* dq_sem = nullptr, int pass = 0) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
   const int G = kv_group_of(H, Hk);
@@ -415,6 +415,7 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   p.items = 0;  // set by the launcher
   p.dq_sem = dq_sem;
   p.sem_rows = static_cast<int>(halves * n);
+  p.pass = pass;
   p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   const cudaError_t e = launch_backward(p, d, stream);
@@ -427,6 +428,28 @@ int check_rows(int B, int rows, int H, int d) {
   if (B < 0 || rows < 1 || rows > (1 << 30) || H < 1) return DFA_EINVAL;
   if (d != 64 && d != 128 && d != 256) return DFA_EUNSUPPORTED;
   return DFA_OK;
+}
+
+// The tensor-core backward step, with the noisy-diagonal specialisation
+// when asked and applicable (diffusion mode, no block crossing a key tile):
+// the pass over the noisy key tiles, which stores the noisy queries' first
+// dQ contribution, then the pass over the clean key tiles; otherwise the
+// single pass over every key tile.
+int bwd_main_passes(int mode, const void* q, const void* k, const void* v, const void* dout,
+                    const float* lse, const float* delta, float* dq_acc, void* dk, void* dv,
+                    int B, int n, int H, int Hk, int d, int bs, cudaStream_t stream, bool diag,
+                    unsigned* dq_sem = nullptr) {
+  TileShape ts;
+  if (diag && !dq_sem && mode == MODE_DIFFUSION && n >= 1 && bs >= 1 && tile_shape_for(d, &ts) &&
+      diag_pass_applies(n, bs < n ? bs : n, ts.bwd_bn)) {
+    int rc = bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, Hk, d, bs,
+                           stream, nullptr, 2);
+    if (rc) return rc;
+    return bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, Hk, d, bs,
+                         stream, nullptr, 1);
+  }
+  return bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, Hk, d, bs, stream,
+                       dq_sem, 0);
 }
 
 int preprocess_impl(const void* out, const void* dout, float* delta, float* dq_acc, int B,
@@ -476,7 +499,8 @@ int alloc_dq_sem(size_t head_rows, cudaStream_t stream, unsigned** sem) {
 
 int backward_impl(int mode, const void* q, const void* k, const void* v, const void* out,
                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int n,
-                  int H, int Hk, int d, int bs, cudaStream_t stream, bool det = false) {
+                  int H, int Hk, int d, int bs, cudaStream_t stream, bool det = false,
+                  bool diag = false) {
   int rc = check_common(B, n, H, d, bs);
   if (rc) return rc;
   if (kv_group_of(H, Hk) == 0) return DFA_EINVAL;
@@ -508,8 +532,8 @@ int backward_impl(int mode, const void* q, const void* k, const void* v, const v
   }
   rc = preprocess_impl(out, dout, delta, dq_acc, B, L, H, d, stream);
   if (!rc)
-    rc = bwd_main_impl(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, Hk, d, bs, stream,
-                       sem);
+    rc = bwd_main_passes(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, B, n, H, Hk, d, bs,
+                         stream, diag, sem);
   if (!rc) rc = convert_impl(dq_acc, dq, B, L, H, d, stream);
   if (sem) cudaFreeAsync(sem, stream);
   cudaFreeAsync(delta, stream);
@@ -895,14 +919,15 @@ int dfa_backward_ex(const void* q, const void* k, const void* v, const void* out
                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
                     const int* cu_seqlens, int batch, int n, int heads, int kv_heads, int headdim,
                     int block_size, int flags, dfa_stream_t stream) {
-  if (flags & ~DFA_DETERMINISTIC) return DFA_EINVAL;
+  if (flags & ~(DFA_DETERMINISTIC | DFA_NOISY_DIAG_PASS)) return DFA_EINVAL;
   const bool det = (flags & DFA_DETERMINISTIC) != 0;
+  const bool diag = (flags & DFA_NOISY_DIAG_PASS) != 0;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cu_seqlens)
     return backward_varlen_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens, batch, heads,
                                 kv_heads, headdim, block_size, s, det);
   return backward_impl(MODE_DIFFUSION, q, k, v, out, dout, lse, dq, dk, dv, batch, n, heads,
-                       kv_heads, headdim, block_size, s, det);
+                       kv_heads, headdim, block_size, s, det, diag);
 }
 
 // Causal attention on (batch, seqlen, heads, headdim): the diffusion kernels
@@ -937,6 +962,17 @@ int dfa_fwd_main_gqa(const void* q, const void* k, const void* v, void* out, flo
   if (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) return DFA_EINVAL;
   return forward_impl(mode, q, k, v, out, lse, dq_acc, batch, n, heads, kv_heads, headdim,
                       mode == MODE_CAUSAL ? 1 : block_size, static_cast<cudaStream_t>(stream));
+}
+
+int dfa_bwd_main_ex(const void* q, const void* k, const void* v, const void* dout,
+                    const float* lse, const float* delta, float* dq_acc, void* dk, void* dv,
+                    int batch, int n, int heads, int kv_heads, int headdim, int block_size,
+                    int mode, int flags, dfa_stream_t stream) {
+  if (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) return DFA_EINVAL;
+  if (flags & ~DFA_NOISY_DIAG_PASS) return DFA_EINVAL;
+  return bwd_main_passes(mode, q, k, v, dout, lse, delta, dq_acc, dk, dv, batch, n, heads,
+                         kv_heads, headdim, mode == MODE_CAUSAL ? 1 : block_size,
+                         static_cast<cudaStream_t>(stream), (flags & DFA_NOISY_DIAG_PASS) != 0);
 }
 
 int dfa_bwd_main_gqa(const void* q, const void* k, const void* v, const void* dout,
@@ -1075,13 +1111,16 @@ long long dfa_tile_visits(int mode, int n, int block_size, int block_m, int bloc
 
 int dfa_work_item(int pass, int mode, int w, int batch, int heads, int tiles, int group,
                   int* item) {
-  if ((pass != 0 && pass != 1) || (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) || batch < 1 ||
+  if (pass < 0 || pass > 3 || (mode != MODE_DIFFUSION && mode != MODE_CAUSAL) || batch < 1 ||
       heads < 1 || tiles < 1 || group < 1 || !item)
     return DFA_EINVAL;
-  const long long items = pass_items(mode, batch, heads, tiles);
+  if (pass >= 2 && mode != MODE_DIFFUSION) return DFA_EINVAL;
+  const long long items = pass >= 2 ? static_cast<long long>(batch) * heads * tiles
+                                    : pass_items(mode, batch, heads, tiles);
   if (items > 0x7fffffffLL || w < 0 || w >= items) return DFA_EINVAL;
-  const WorkItem it = pass == 0 ? fwd_work(w, mode, batch, heads, tiles, group)
-                                : bwd_work(w, mode, batch, heads, tiles, group);
+  const WorkItem it = pass == 0   ? fwd_work(w, mode, batch, heads, tiles, group)
+                      : pass == 1 ? bwd_work(w, mode, batch, heads, tiles, group)
+                                  : bwd_work_pass(w, pass - 1, batch, heads, tiles, group);
   item[0] = it.b;
   item[1] = it.h;
   item[2] = it.half;

@@ -149,7 +149,8 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int v) {
     it.bs = imin(p.bs, sl.n);
     it.row0 = sl.row0;
   } else {
-    it.wi = bwd_work(v, p.mode, p.B, p.Hk, p.k_tiles, p.group);
+    it.wi = p.pass ? bwd_work_pass(v, p.pass, p.B, p.Hk, p.k_tiles, p.group)
+                   : bwd_work(v, p.mode, p.B, p.Hk, p.k_tiles, p.group);
     it.n = p.n;
     it.bs = p.bs;
     it.row0 = 0;  // unused: batched rows come from wi.b
@@ -535,10 +536,16 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       if (q < n) {
         const size_t pos = static_cast<size_t>(it.lhalf(l)) * n + q;
         float* dst = p.dq_acc + ((first + pos) * p.H + it.h0 + hh) * D + DW * wg;
+        if (p.pass == 2) {
+          // noisy-diagonal pass: this item's contribution is the row's first
 #pragma unroll
-        for (int c = 0; c < DW; c += 4)
-          red_add_v4_f32(dst + c, __uint_as_float(dq[c]), __uint_as_float(dq[c + 1]),
-                         __uint_as_float(dq[c + 2]), __uint_as_float(dq[c + 3]));
+          for (int c = 0; c < DW; c += 4) st_global_v4(dst + c, dq[c], dq[c + 1], dq[c + 2], dq[c + 3]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < DW; c += 4)
+            red_add_v4_f32(dst + c, __uint_as_float(dq[c]), __uint_as_float(dq[c + 1]),
+                           __uint_as_float(dq[c + 2]), __uint_as_float(dq[c + 3]));
+        }
       }
       if constexpr (DET) sem_signal_warp(sem);
       return true;
@@ -719,7 +726,10 @@ static cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long items = VARLEN ? p.units : pass_items(p.mode, p.B, p.Hk, p.k_tiles);
+  // the noisy-diagonal passes take the key tiles of one half only
+  const long long items = VARLEN ? p.units
+                          : p.pass ? static_cast<long long>(p.B) * p.Hk * p.k_tiles
+                                   : pass_items(p.mode, p.B, p.Hk, p.k_tiles);
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;

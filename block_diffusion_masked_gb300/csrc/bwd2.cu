@@ -194,7 +194,8 @@ __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
     it.bs = imin(p.bs, sl.n);
     it.row0 = sl.row0;
   } else {
-    it.wi = bwd_work(v / NDH, p.mode, p.B, p.Hk, p.k_tiles, p.group);
+    it.wi = p.pass ? bwd_work_pass(v / NDH, p.pass, p.B, p.Hk, p.k_tiles, p.group)
+                   : bwd_work(v / NDH, p.mode, p.B, p.Hk, p.k_tiles, p.group);
     it.n = p.n;
     it.bs = p.bs;
     it.row0 = 0;  // unused: batched rows come from wi.b
@@ -715,8 +716,12 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           // past the half are skipped rather than added to the next sample.
           const CUtensorMap* mdq = VARLEN ? &p.vl_maps[it.slot].dq : &p.tm_dq;
           const HalfRows dr = in_rows<VARLEN>(it.wi.b, qh);
-          tma_reduce_add_5d(mdq, stg, it.dh * DH + 32 * (warp & 3), h, dr.base + qs + c0, dr.c3,
-                            dr.c4);
+          if (p.pass == 2)  // noisy-diagonal pass: the rows' first contribution
+            tma_store_5d(mdq, stg, it.dh * DH + 32 * (warp & 3), h, dr.base + qs + c0, dr.c3,
+                         dr.c4);
+          else
+            tma_reduce_add_5d(mdq, stg, it.dh * DH + 32 * (warp & 3), h, dr.base + qs + c0, dr.c3,
+                              dr.c4);
           bulk_commit_group();
         }
         return true;
@@ -736,14 +741,21 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       }
       float* ptr = p.dq_acc + ((first + static_cast<size_t>(qh) * n + qs + c0) * p.H + h) * D +
                    it.dh * DH + row;
-      if (qs + c0 + HC <= n) {
+      const int qmax = n - qs - c0;
+      if (p.pass == 2) {
+        // noisy-diagonal pass: this item's contribution is the rows' first
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+          if (c < qmax) *ptr = __uint_as_float(dq[c]);
+          ptr += dq_stride;
+        }
+      } else if (qmax >= HC) {
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
           red_add_f32(ptr, __uint_as_float(dq[c]));
           ptr += dq_stride;
         }
       } else {
-        const int qmax = n - qs - c0;
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
           if (c < qmax) red_add_f32(ptr, __uint_as_float(dq[c]));
@@ -943,7 +955,10 @@ static cudaError_t launch_bwd2_impl(const BwdParams& p, cudaStream_t stream) {
   if (fa.numRegs * C::kThreads < C::kRegCtl * 128 + C::kRegCompute * 128 * C::NWG)
     return cudaErrorInvalidConfiguration;
   const long long items =
-      (VARLEN ? static_cast<long long>(p.units) : pass_items(p.mode, p.B, p.Hk, p.k_tiles)) * C::NDH;
+      (VARLEN  ? static_cast<long long>(p.units)
+       : p.pass ? static_cast<long long>(p.B) * p.Hk * p.k_tiles  // one key half per pass
+                : pass_items(p.mode, p.B, p.Hk, p.k_tiles)) *
+      C::NDH;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;

@@ -272,6 +272,32 @@ DFA_HD WorkItem bwd_work(int w, int mode, int B, int H, int tiles, int group) {
   return it;
 }
 
+// Backward items of one key half only (the two passes of the noisy-diagonal
+// specialisation, "Fast Diffusion Attention", "Hopper": a dedicated pass
+// over the noisy diagonal, then the main pass over the clean key tiles).
+// Clean key tiles longest first (increasing index) with the last two ranks
+// of every pair as the tail; noisy key tiles, all equally short, rank by
+// rank over all pairs.  `pass`: 1 clean key tiles, 2 noisy key tiles.
+DFA_HD WorkItem bwd_work_pass(int w, int pass, int B, int H, int tiles, int group) {
+  int rank, bh;
+  const int tail = pass == 1 ? imin(tiles, 2) : tiles;
+  work_split(w, B * H, group, tiles, tail, &rank, &bh);
+  WorkItem it;
+  it.half = pass == 1 ? HALF_CLEAN : HALF_NOISY;
+  it.tile = rank;
+  it.b = bh / H;
+  it.h = bh % H;
+  return it;
+}
+
+// The noisy-diagonal pass may store the noisy queries' dQ instead of adding
+// it when every noisy query row is seen by the noisy keys of one key tile
+// only: no block crosses a tile boundary (block size divides the tile) or
+// the half is a single tile.
+DFA_HD bool diag_pass_applies(int n, int bs, int tile) {
+  return tile % bs == 0 || n <= tile;
+}
+
 // Heads per group: the group's working set (bytes_per_bh each) kept within
 // about half of L2, and the heads spread evenly over the fewest groups that
 // allows.  Even groups matter: a group's longest items start when the group

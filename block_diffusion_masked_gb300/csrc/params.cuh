@@ -106,6 +106,11 @@ struct BwdParams {
   // the rows of q (batch * 2n, or the packed rows).
   unsigned* dq_sem;
   int sem_rows;
+  // Passes of the noisy-diagonal specialisation (diffusion mode, batched):
+  // 0 every key tile; 1 clean key tiles only; 2 noisy key tiles only, dQ
+  // stored into the accumulator (each noisy query row gets its one noisy
+  // diagonal contribution) instead of added.
+  int pass;
 };
 
 #if defined(__CUDACC__)

@@ -187,7 +187,8 @@ int dfa_forward_fp8_vt(const void *q, const void *k, const void *vt, void *out, 
 /*
  * The backward with options.  cu_seqlens == NULL: the batched layout of
  * dfa_backward_gqa (batch, n); otherwise the packed layout of
- * dfa_backward_varlen (n ignored).  flags: 0 or DFA_DETERMINISTIC.
+ * dfa_backward_varlen (n ignored).  flags: 0, DFA_DETERMINISTIC,
+ * DFA_NOISY_DIAG_PASS, or both (then DFA_DETERMINISTIC alone applies).
  *
  * DFA_DETERMINISTIC (the deterministic mode of "Fast Diffusion Attention",
  * where semaphores fix the order of the dQ sums): the key tiles that reach
@@ -202,6 +203,21 @@ int dfa_forward_fp8_vt(const void *q, const void *k, const void *vt, void *out, 
  * bits: DFA_EINVAL.
  */
 #define DFA_DETERMINISTIC 1
+/*
+ * DFA_NOISY_DIAG_PASS (the dedicated noisy-diagonal pass of the backward,
+ * "Fast Diffusion Attention", "Hopper: the FlashAttention-3 generation"):
+ * the tensor-core backward runs as two launches on `stream`, first over the
+ * noisy key tiles only -- the complete dK / dV of the noisy keys, and the
+ * noisy queries' dQ from their own block STORED into the accumulator --
+ * then over the clean key tiles, which add the rest of dQ.  It applies to
+ * the batched layout when the block size divides the 128-key tile or a
+ * half fits in one tile (min(block_size, n) divides 128, or n <= 128), so
+ * that every noisy query row meets the noisy keys of one key tile only; in
+ * every other case (varlen, DFA_DETERMINISTIC, other block sizes) the
+ * single launch runs.  Results equal the single launch's up to the order
+ * of float32 dQ additions; dK and dV are bitwise the same.
+ */
+#define DFA_NOISY_DIAG_PASS 2
 int dfa_backward_ex(const void *q, const void *k, const void *v, const void *out,
                     const void *dout, const float *lse, void *dq, void *dk, void *dv,
                     const int *cu_seqlens, int batch, int n, int heads, int kv_heads,
@@ -243,6 +259,10 @@ int dfa_causal_backward(const void *q, const void *k, const void *v, const void 
  *     dq (already scaled) into dq_acc (float32 atomics or bulk reduce-adds).
  *   dfa_bwd_dq_convert: dq = bf16(dq_acc), round to nearest even.
  *     dfa_bwd_dq_convert_ex: the same with `mode` (causal: rows of n).
+ *   dfa_bwd_main_ex: dfa_bwd_main_gqa with flags, 0 or DFA_NOISY_DIAG_PASS
+ *     (see dfa_backward_ex; causal mode: the flag is ignored).  Where the
+ *     noisy-diagonal pass applies, the noisy rows of dq_acc are overwritten
+ *     rather than added to: their prior contents do not matter.
  * dq_acc and delta are device buffers the caller allocated (16-byte aligned).
  */
 int dfa_fwd_main(const void *q, const void *k, const void *v, void *out, float *lse,
@@ -274,6 +294,10 @@ int dfa_bwd_main_gqa(const void *q, const void *k, const void *v, const void *do
                      const float *lse, const float *delta, float *dq_acc, void *dk, void *dv,
                      int batch, int n, int heads, int kv_heads, int headdim, int block_size,
                      int mode, dfa_stream_t stream);
+int dfa_bwd_main_ex(const void *q, const void *k, const void *v, const void *dout,
+                    const float *lse, const float *delta, float *dq_acc, void *dk, void *dv,
+                    int batch, int n, int heads, int kv_heads, int headdim, int block_size,
+                    int mode, int flags, dfa_stream_t stream);
 
 /*
  * dfa_backward without any allocation.  No passage of the pages has a
@@ -351,6 +375,9 @@ long long dfa_tile_visits(int mode, int n, int block_size, int block_m, int bloc
  * pairs ((sequence, head) pairs in the causal mode).  Writes (batch, head,
  * half, tile) into item[4]; in the causal mode sequence s is reported as
  * (s / 2, head, s % 2, tile).
+ * Passes 2 and 3 (diffusion mode only, w < batch * heads * tiles) are the
+ * two launches of DFA_NOISY_DIAG_PASS: 2 the clean key tiles, 3 the noisy
+ * key tiles.
  * Inside a group the items of a (batch, head) go longest first; the
  * shortest ones of all pairs come last ("Fast Diffusion Attention",
  * "Hopper" and "Ampere and Ada": longest-first, L2-aware order).  The

@@ -89,7 +89,11 @@ def test_host_side_argument_checks(lib):
     assert lib.dfa_forward_varlen(p, p, p, p, p, None, 1, 2, 2, 64, 4, s) == b.DFA_EINVAL
     assert lib.dfa_forward_varlen(p, p, p, p, p, cu(0, 0, 0), 2, 2, 2, 64, 4, s) == b.DFA_OK
     # backward options: unknown flag bits are refused
-    assert lib.dfa_backward_ex(p, p, p, p, p, p, p, p, p, None, 1, 64, 2, 2, 64, 4, 2,
+    assert lib.dfa_backward_ex(p, p, p, p, p, p, p, p, p, None, 1, 64, 2, 2, 64, 4, 4,
+                               s) == b.DFA_EINVAL
+    assert lib.dfa_bwd_main_ex(p, p, p, p, p, p, p, p, p, 1, 64, 2, 2, 64, 4, 0, 4,
+                               s) == b.DFA_EINVAL
+    assert lib.dfa_bwd_main_ex(p, p, p, p, p, p, p, p, p, 1, 64, 2, 2, 64, 4, 3, 2,
                                s) == b.DFA_EINVAL
 
 

@@ -177,3 +177,54 @@ def test_work_order_is_longest_first_with_short_tail(b, pass_, mode, batch, head
         assert sorted(pair(x, y, h) for (x, y, h, _) in chunk) == pairs
     with pytest.raises(b.DfaError):
         b.dfa_work_item(pass_, mode, total, batch, heads, tiles, group)
+
+
+@pytest.mark.parametrize("batch,heads,n,bs,group", [
+    (1, 1, 300, 16, 1), (2, 3, 700, 4, 2), (3, 5, 1024, 64, 4), (1, 7, 129, 128, 7),
+    (4, 2, 2048, 16, 3), (2, 2, 100, 512, 1),
+])
+def test_noisy_diag_passes_split_the_backward(b, batch, heads, n, bs, group):
+    """The two launches of the noisy-diagonal option ("Fast Diffusion
+    Attention", "Hopper": a dedicated pass over the noisy diagonal, the main
+    pass over the clean key tiles): together they cover exactly the items of
+    the single backward pass; the clean pass goes longest first per pair and
+    ends on its two shortest ranks; every noisy item visits only the query
+    rows of its own key tile when the block size divides the tile."""
+    bm, bn = 64, 128
+    tiles = -(-n // bn)
+    BH = batch * heads
+    total = BH * tiles
+    clean = [b.dfa_work_item(2, 0, w, batch, heads, tiles, group) for w in range(total)]
+    noisy = [b.dfa_work_item(3, 0, w, batch, heads, tiles, group) for w in range(total)]
+    single = [b.dfa_work_item(1, 0, w, batch, heads, tiles, group) for w in range(2 * total)]
+    assert all(h == 1 for (_, _, h, _) in clean)
+    assert all(h == 0 for (_, _, h, _) in noisy)
+    assert sorted(clean + noisy) == sorted(single)
+    assert len(set(clean)) == total and len(set(noisy)) == total
+    bs_eff = min(bs, n)
+    vis = [_visits(b, 1, 0, n, bs_eff, h, t, bm, bn) for (_, _, h, t) in clean]
+    tail = min(tiles, 2)
+    head = total - BH * tail
+    seen = {}
+    for (x, y, _, _), c in zip(clean[:head], vis[:head]):
+        assert c <= seen.get((x, y), c)
+        seen[(x, y)] = c
+    pairs = sorted({(x, y) for (x, y, _, _) in clean})
+    for r in range(tail):
+        chunk = clean[head + r * BH: head + (r + 1) * BH]
+        assert sorted((x, y) for (x, y, _, _) in chunk) == pairs
+    if bn % bs_eff == 0 or n <= bn:
+        # each noisy query row is visited by exactly one noisy key tile
+        rows = []
+        for t in range(tiles):
+            for (qh, _, s, e) in b.dfa_bwd_segments(0, n, bs_eff, bm, bn, 0, t):
+                assert qh == 0
+                lo, hi = s * bm, min(e * bm, n)
+                assert t * bn <= lo and hi <= (t + 1) * bn
+                rows += range(lo, hi)
+        assert sorted(rows) == list(range(n))
+    for pass_ in (2, 3):
+        with pytest.raises(b.DfaError):
+            b.dfa_work_item(pass_, 0, total, batch, heads, tiles, group)
+        with pytest.raises(b.DfaError):
+            b.dfa_work_item(pass_, 1, 0, batch, heads, tiles, group)

@@ -9,28 +9,32 @@
 // Attention Without Materialization", section 5.1, with the online softmax of
 // section 4.2.
 //
-// Two softmax warpgroups share the query tile: warpgroup w takes the key tiles
-// j with j % 2 == w and keeps its own running maximum, running sum and output
-// accumulator O[w] in TMEM, so the warpgroups never wait for each other
-// inside the loop; at the end of the item the two partial states are merged
-// with the online-softmax rescaling rule (exact).  Scores S[w] = Q K^T land in
-// TMEM; probabilities are written back as bf16 into the same TMEM columns and
-// feed O[w] += P V as the MMA's A operand.  A row's reference maximum is only
-// moved (O and the sum rescaled) when a tile maximum exceeds it by more than
-// 2^8: exact in real arithmetic, and probabilities stay below 256.
+// Two softmax warpgroups share every key tile of the item: warpgroup w takes
+// the tile's key columns [64 w, 64 w + 64) of every row.  The row's
+// reference maximum is common to both (one exchange of half-row maxima
+// through shared memory per tile), so the probabilities of the two halves
+// feed a single output accumulator O in TMEM and nothing is merged at the
+// end of an item.  Scores S = Q K^T land in one of two TMEM buffers, so the
+// scores of the next tile are computed while the softmax of this one runs;
+// each warpgroup writes its probabilities as bf16 back into the first half
+// of its own columns of the buffer, where O += P V reads them as the MMA's A
+// operand.  A row's reference maximum is only moved (O and the sum
+// rescaled) when a tile maximum exceeds it by more than 2^8: exact in real
+// arithmetic, and probabilities stay below 256.  O is double-buffered by
+// item, so the next item's first products need not wait for the read-out of
+// this one.
 //
 // The K/V ring, the query double buffer and all barrier phases run on across
-// items, so the loads and S products of the next item overlap the merge and
-// stores of the current one.
+// items, so the loads and S products of the next item overlap the read-out
+// and stores of the current one.
 // Warps 0-7 softmax; warp 8 takes the items and loads Q, K and V; warp 10
 // issues S = Q K^T and warp 9 O += P V; warp 11 stores the out tiles (staged
 // by the softmax warpgroups in the item's query buffer) with TMA and zeroes
 // the backward's float32 dq accumulator when the caller asks for it.
-// The load/MMA warpgroup
-// hands registers to the softmax warpgroups (setmaxnreg): launched with 168
-// per thread, it drops to 56 and the softmax warpgroups rise to 224, which
-// keeps a row's 128 scores in registers.  256 * (224 - 168) == 128 * (168 -
-// 56): the pool balances.
+// The load/MMA warpgroup hands registers to the softmax warpgroups
+// (setmaxnreg): launched with 168 per thread, it drops to 56 and the softmax
+// warpgroups rise to 224.  256 * (224 - 168) == 128 * (168 - 56): the pool
+// balances.
 #include <cuda_bf16.h>
 
 #include "geometry.cuh"
@@ -59,8 +63,9 @@ struct Fwd2Cfg {
   static constexpr int kOffQ = 0;  // 2 buffers
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + STAGES * kKVBytes;
-  static constexpr int kOffML = kOffV + STAGES * kKVBytes;  // [item % 2][warpgroup][row] (m, l)
-  static constexpr int kOffBar = kOffML + 2 * 2 * BM * 8;
+  // exchange slots of the two softmax warpgroups: [round % 2][warpgroup][row]
+  static constexpr int kOffX = kOffV + STAGES * kKVBytes;
+  static constexpr int kOffBar = kOffX + 2 * 2 * BM * 4;
   enum {
     BAR_QFULL = 0,                    // [2]
     BAR_QEMPTY = BAR_QFULL + 2,       // [2]
@@ -68,12 +73,11 @@ struct Fwd2Cfg {
     BAR_KEMPTY = BAR_KFULL + STAGES,  // [STAGES]
     BAR_VFULL = BAR_KEMPTY + STAGES,  // [STAGES]
     BAR_VEMPTY = BAR_VFULL + STAGES,  // [STAGES]
-    BAR_SFULL = BAR_VEMPTY + STAGES,  // [2] per warpgroup
-    BAR_PFULL = BAR_SFULL + 2,        // [2] per warpgroup
-    BAR_PVDONE = BAR_PFULL + 2,       // [2] per warpgroup: its last P V complete
-    BAR_ITEMDONE = BAR_PVDONE + 2,    // every product of an item complete
-    BAR_OFREE = BAR_ITEMDONE + 1,     // both O accumulators read out
-    BAR_XCHG = BAR_OFREE + 1,         // both warpgroups' (m, l) in shared memory
+    BAR_SFULL = BAR_VEMPTY + STAGES,  // [2] per S buffer: S of its tile complete
+    BAR_PFULL = BAR_SFULL + 2,        // [2] per S buffer: P of its tile written (8 warps)
+    BAR_SFREE = BAR_PFULL + 2,        // [2] per S buffer: P V of its tile complete
+    BAR_OFREE = BAR_SFREE + 2,        // [2] per O buffer: read out (8 warps)
+    BAR_XCHG = BAR_OFREE + 2,         // one exchange round of the softmax warps (8 warps)
     BAR_ITEMFULL = BAR_XCHG + 1,      // [4] item published
     BAR_OSTAGED = BAR_ITEMFULL + 4,   // [2] per query buffer: the item's out tile staged in it
     BAR_ALL = BAR_OSTAGED + 2,        // every MMA of the CTA complete
@@ -83,8 +87,9 @@ struct Fwd2Cfg {
   static constexpr int kOffTmemSlot = kOffItem + 4 * 128;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
-  static constexpr int kTmemS = 0;       // S[w] at w * BN; P[w] in its first BN / 2 columns
-  static constexpr int kTmemO = 2 * BN;  // O[w] at kTmemO + w * D
+  // S[b] at b * BN; warpgroup w's P in columns [64 w, 64 w + 32) of it
+  static constexpr int kTmemS = 0;
+  static constexpr int kTmemO = 2 * BN;  // O[item % 2] at kTmemO + (item % 2) * D
   static constexpr int kTmemCols = 512;
   static constexpr int kThreads = 384;
   static constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -163,10 +168,12 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(C::BAR_QFULL + b), 1);
-      mbar_init(BAR(C::BAR_SFULL + b), 1);
-      mbar_init(BAR(C::BAR_PFULL + b), 128);
       mbar_init(BAR(C::BAR_QEMPTY + b), 1);
-      mbar_init(BAR(C::BAR_PVDONE + b), 1);
+      mbar_init(BAR(C::BAR_SFULL + b), 1);
+      mbar_init(BAR(C::BAR_PFULL + b), 8);
+      mbar_init(BAR(C::BAR_SFREE + b), 1);
+      mbar_init(BAR(C::BAR_OFREE + b), 8);
+      mbar_init(BAR(C::BAR_OSTAGED + b), 8);
     }
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(BAR(C::BAR_KFULL + s), 1);
@@ -174,12 +181,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       mbar_init(BAR(C::BAR_VFULL + s), 1);
       mbar_init(BAR(C::BAR_VEMPTY + s), 1);
     }
-    mbar_init(BAR(C::BAR_ITEMDONE), 1);
-    mbar_init(BAR(C::BAR_OFREE), 256);
-    mbar_init(BAR(C::BAR_XCHG), 256);
+    mbar_init(BAR(C::BAR_XCHG), 8);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
-    mbar_init(BAR(C::BAR_OSTAGED + 0), 256);
-    mbar_init(BAR(C::BAR_OSTAGED + 1), 256);
     mbar_init(BAR(C::BAR_ALL), 2);  // both MMA-issuing warps
     *abort_flag = 0;
     fence_mbar_init();
@@ -304,15 +307,17 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     // Warp 10 issues S = Q K^T, warp 9 O += P V.  Issued from one warp, the
     // products slow down while the softmax warps that share its scheduler are
     // busy; from two warps on two schedulers they keep the tensor pipe fed.
-    // The two streams meet only through barriers: S of a warpgroup's tile
-    // overwrites the TMEM columns its previous P was read from, so it waits
-    // for that P V (PVDONE); P V waits for the warpgroup's P (PFULL).
+    // The two streams meet only through barriers: S of tile g goes into
+    // buffer g % 2 once P V of tile g - 2 (whose P it held) has completed
+    // (SFREE); P V of a tile waits for both warpgroups' P (PFULL), and the
+    // first P V of an item for the read-out of the O buffer it reuses (OFREE).
     if (lane == 0) {
       const bool s_warp = warp == 10;
       constexpr uint32_t kIdS =
           FP8 ? idesc_e4m3(BM, BN, false, false) : idesc_bf16(BM, BN, false, false);
       constexpr uint32_t kIdPV =
           FP8 ? idesc_e4m3(BM, D, false, false) : idesc_bf16(BM, D, false, true);
+      constexpr int kPVSteps = BN / C::kPVKeys;
       const uint64_t dQ = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
       const uint64_t dK = sdesc_sw128(sbase + C::kOffK, 16, 1024);
       // V: MN-major (keys = K in rows); FP8 reads V^T, K-major (128 keys a row)
@@ -320,8 +325,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
                               : sdesc_sw128(sbase + C::kOffV, BN * 128, 1024);
       auto adv = [](uint64_t d, uint32_t bytes) { return d + static_cast<uint64_t>(bytes >> 4); };
       bool ok = true;
-      int g = 0;            // K/V ring position
-      int cnt[2] = {0, 0};  // tiles handed to each warpgroup so far
+      int g = 0;  // tiles of earlier items (K/V ring and S buffer position)
       for (int k = 0; ok; ++k) {
         if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
         const ItemGeom ig = *ring(k & 3);
@@ -330,60 +334,57 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         if (s_warp) {
           if (!(ok = mbar_wait(BAR(C::BAR_QFULL + qb), (k >> 1) & 1, ab))) break;
         } else {
-          // The O accumulators still hold the previous item until it is read out.
-          if (k >= 1 && !(ok = mbar_wait(BAR(C::BAR_OFREE), (k - 1) & 1, ab))) break;
+          // O buffer k % 2 still holds item k - 2 until it is read out.
+          if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_OFREE + qb), ((k >> 1) - 1) & 1, ab))) break;
         }
         tc_fence_after();
         for (int j = 0; j < ig.ntiles && ok; ++j) {
-          const int w = j & 1;
-          const int c = cnt[w] + (j >> 1);  // this warpgroup's tile count
           const int gg = g + j;
           const int st = gg % STAGES;
+          const int sb = gg & 1;
           if (s_warp) {
             if (!(ok = mbar_wait(BAR(C::BAR_KFULL + st), (gg / STAGES) & 1, ab))) break;
-            if (c >= 1 && !(ok = mbar_wait(BAR(C::BAR_PVDONE + w), (c - 1) & 1, ab))) break;
+            if (gg >= 2 && !(ok = mbar_wait(BAR(C::BAR_SFREE + sb), ((gg >> 1) - 1) & 1, ab)))
+              break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < C::kKSteps; ++kk) {
               const uint64_t a = adv(dQ, qb * C::kQBytes + (kk >> 2) * (BM * 128) + (kk & 3) * 32);
               const uint64_t b = adv(dK, st * C::kKVBytes + (kk >> 2) * (BN * 128) + (kk & 3) * 32);
               if constexpr (FP8)
-                mma_ss_f8(tmem + C::kTmemS + w * BN, a, b, kIdS, kk > 0 ? 1u : 0u);
+                mma_ss_f8(tmem + C::kTmemS + sb * BN, a, b, kIdS, kk > 0 ? 1u : 0u);
               else
-                mma_ss(tmem + C::kTmemS + w * BN, a, b, kIdS, kk > 0 ? 1u : 0u);
+                mma_ss(tmem + C::kTmemS + sb * BN, a, b, kIdS, kk > 0 ? 1u : 0u);
             }
-            mma_commit(BAR(C::BAR_SFULL + w));
+            mma_commit(BAR(C::BAR_SFULL + sb));
             mma_commit(BAR(C::BAR_KEMPTY + st));
           } else {
-            if (!(ok = mbar_wait(BAR(C::BAR_PFULL + w), c & 1, ab))) break;
+            if (!(ok = mbar_wait(BAR(C::BAR_PFULL + sb), (gg >> 1) & 1, ab))) break;
             if (!(ok = mbar_wait(BAR(C::BAR_VFULL + st), (gg / STAGES) & 1, ab))) break;
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < BN / C::kPVKeys; ++kk) {
-              // P: 8 TMEM columns per step (bf16 pairs or e4m3 quadruples);
-              // V: 16 key rows of 128 bytes, or (V^T) 32 bytes of 128-key rows
+            for (int kk = 0; kk < kPVSteps; ++kk) {
+              // P of keys [kPVKeys kk, kPVKeys (kk + 1)): in the columns of the
+              // warpgroup that owns them, 8 columns per step (bf16 pairs or
+              // e4m3 quadruples); V: 16 key rows of 128 bytes, or (V^T) 32
+              // bytes of 128-key rows
+              constexpr int kStepsPerHalf = kPVSteps / 2;
+              const uint32_t pcol =
+                  C::kTmemS + sb * BN + 64 * (kk / kStepsPerHalf) + 8 * (kk % kStepsPerHalf);
               const uint64_t b =
                   adv(dV, st * C::kKVBytes + (FP8 ? kk * 32 : kk * C::kPVKeys * 128));
-              const uint32_t acc = (j >= 2 || kk > 0) ? 1u : 0u;
+              const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
               if constexpr (FP8)
-                mma_ts_f8(tmem + C::kTmemO + w * D, tmem + C::kTmemS + w * BN + 8 * kk, b, kIdPV,
-                          acc);
+                mma_ts_f8(tmem + C::kTmemO + qb * D, tmem + pcol, b, kIdPV, acc);
               else
-                mma_ts(tmem + C::kTmemO + w * D, tmem + C::kTmemS + w * BN + 8 * kk, b, kIdPV,
-                       acc);
+                mma_ts(tmem + C::kTmemO + qb * D, tmem + pcol, b, kIdPV, acc);
             }
             mma_commit(BAR(C::BAR_VEMPTY + st));
-            mma_commit(BAR(C::BAR_PVDONE + w));
+            mma_commit(BAR(C::BAR_SFREE + sb));
           }
         }
         if (!ok) break;
-        // Every S of the item precedes its P, so the last P V completes the
-        // item.  Its query buffer is released by warp 11, once the item's out
-        // tile, staged in it, has been stored.
-        if (!s_warp) mma_commit(BAR(C::BAR_ITEMDONE));
         g += ig.ntiles;
-        cnt[0] += (ig.ntiles + 1) >> 1;
-        cnt[1] += ig.ntiles >> 1;
       }
       mma_commit(BAR(C::BAR_ALL));
     }
@@ -454,87 +455,32 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
     // ------------------------------------------------------------ softmax
+    // Warpgroup w, thread `row`: key columns [64 w, 64 w + 64) of every tile
+    // of the item for query row `row` of the tile.
     const int w = warp >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t s_col = t_lane + C::kTmemS + w * BN;
-    const uint32_t o_col = t_lane + C::kTmemO + w * D;
     const float sl2 = p.scale_log2;
-    // ---------------------------------------------------------- merge
-    // Item kk (ig: sample, head, half; query tile at qs) ends: the two
-    // warpgroups' partial states are combined with the online-softmax rule.
-    auto merge = [&](int kk, const ItemGeom& ig, int qs, float m_ref, float l_run) -> bool {
-      float2* ml = reinterpret_cast<float2*>(smem + C::kOffML) + (kk & 1) * 2 * BM;
-      ml[w * BM + row] = make_float2(m_ref, l_run);
-      mbar_arrive(BAR(C::BAR_XCHG));
-      if (!mbar_wait_warp(BAR(C::BAR_ITEMDONE), kk & 1, ab)) return false;
-      if (!mbar_wait_warp(BAR(C::BAR_XCHG), kk & 1, ab)) return false;
-      tc_fence_after();
-      const float2 ma = ml[row];       // warpgroup 0
-      const float2 mb = ml[BM + row];  // warpgroup 1
-      const float m = fmaxf(ma.x, mb.x);
-      const float fa = ma.y > 0.f ? ex2_approx(ma.x - m) : 0.f;
-      const float fb = mb.y > 0.f ? ex2_approx(mb.x - m) : 0.f;
-      const float lsum = ma.y * fa + mb.y * fb;
-      // FP8: out = (P V8) * v_descale / l
-      const float inv = lsum > 0.f ? (FP8 ? p.out_scale : 1.f) / lsum : 0.f;
-      const int r = qs + row;
-      // The out tile goes, as bf16, into this item's query buffer (free: the
-      // item's last product has completed) in the 128-byte-swizzled layout of
-      // a TMA box, for the producer to store; rows past the end of the half are
-      // dropped by the copy.  Warpgroup w stages head dims
-      // [w * D / 2, (w + 1) * D / 2).
-      const uint32_t stage = sbase + C::kOffQ + (kk & 1) * C::kQBytes;
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = w * (D / 2) + 32 * c;
-        uint32_t oa[32], ob[32];
-        tmem_ld32(t_lane + C::kTmemO + col, oa);
-        tmem_ld32(t_lane + C::kTmemO + D + col, ob);
-        tmem_wait_ld();
-        tmem_pin<32>(oa);
-        tmem_pin<32>(ob);
-#pragma unroll
-        for (int gq = 0; gq < 4; ++gq) {
-          uint32_t wv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float v2[2];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int q8 = gq * 8 + 2 * e + h2;
-              const float x = (fa > 0.f ? __uint_as_float(oa[q8]) * fa : 0.f) +
-                              (fb > 0.f ? __uint_as_float(ob[q8]) * fb : 0.f);
-              v2[h2] = x * inv;
-            }
-            wv[e] = pack_bf16x2(v2[0], v2[1]);
-          }
-          const int unit = col / 8 + gq;  // 16-byte unit of the row
-          st_shared_v4(stage + (unit >> 3) * (BM * 128) + row * 128 +
-                           (((unit & 7) ^ (row & 7)) << 4),
-                       wv[0], wv[1], wv[2], wv[3]);
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(BAR(C::BAR_OSTAGED + (kk & 1)));
-      if (r < (VARLEN ? ig.n : p.n) && w == 0) {
-        const float lse = lsum > 0.f ? (m + lg2_approx(lsum)) * 0.69314718055994531f : -INFINITY;
-        if constexpr (VARLEN)
-          p.lse[static_cast<size_t>(ig.wi.h) * p.rows + ig.row0 + ig.wi.half * ig.n + r] = lse;
-        else
-          p.lse[lse_offset(p.mode, ig.wi.b, ig.wi.h, ig.wi.half, r, p.H, p.n)] = lse;
-      }
-      tc_fence_before();
-      mbar_arrive(BAR(C::BAR_OFREE));
+    float* const xslots = reinterpret_cast<float*>(smem + C::kOffX);
+    int xc = 0;  // exchange rounds so far (the same sequence in both warpgroups)
+    // One exchange round: this thread's value for its row goes to the other
+    // warpgroup, whose value for the same row comes back.
+    auto exchange = [&](float mine, float* theirs) -> bool {
+      float* xs = xslots + (xc & 1) * 2 * BM;
+      xs[w * BM + row] = mine;
+      mbar_arrive_warp(BAR(C::BAR_XCHG));
+      if (!mbar_wait_warp(BAR(C::BAR_XCHG), xc & 1, ab)) return false;
+      *theirs = xs[(1 - w) * BM + row];
+      ++xc;
       return true;
     };
     bool ok = true;
-    int cnt = 0;  // tiles this warpgroup has processed so far
-    int k = 0;
-    for (; ok; ++k) {
+    int g = 0;  // tiles of earlier items
+    for (int k = 0; ok; ++k) {
       if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
       const ItemGeom ig = *ring(k & 3);
       if (ig.item < 0) break;
+      const int qb = k & 1;  // query buffer and O buffer of the item
       const int qs = ig.qs;
       const int r = qs + row;  // row inside the half
       // Keys visible to row r, per segment of the item: computed once, so a
@@ -543,31 +489,35 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       const int bs = VARLEN ? imin(p.bs, n) : p.bs;
       const Interval kv0 = key_interval(ig.rule0, r, n, bs);
       const Interval kv1 = key_interval(ig.rule1, r, n, bs);
+      const uint32_t o_col = t_lane + C::kTmemO + qb * D + w * (D / 2);
       float m_ref = -INFINITY;  // reference maximum, scaled log2 units
-      float l_run = 0.f;        // running sum of 2^(s * sl2 - m_ref)
-      for (int j = w; j < ig.ntiles; j += 2, ++cnt) {
-        const int s = j < ig.n0 ? 0 : 1;
+      float l_run = 0.f;        // running sum of 2^(s * sl2 - m_ref) over this half's keys
+      for (int j = 0; j < ig.ntiles; ++j) {
+        const int gg = g + j;
+        const int sb = gg & 1;
+        const int seg = j < ig.n0 ? 0 : 1;
         const int kt = ig.ktile(j);
-        if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + w), cnt & 1, ab))) break;
+        const uint32_t s_col = t_lane + C::kTmemS + sb * BN + 64 * w;
+        if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + sb), (gg >> 1) & 1, ab))) break;
         tc_fence_after();
-        const int ks = kt * BN;
-        const Interval iv = s ? kv1 : kv0;
+        const int ks = kt * BN + 64 * w;
+        const Interval iv = seg ? kv1 : kv0;
         const int clo = iv.lo - ks, chi = iv.hi - ks;
         // The warp masks element by element only if one of its rows needs it.
-        const bool full = __all_sync(0xffffffffu, clo <= 0 && chi >= BN);
-        // The tile's score row in registers; hidden keys -> -inf, so they
+        const bool full = __all_sync(0xffffffffu, clo <= 0 && chi >= 64);
+        // This half's score row in registers; hidden keys -> -inf, so they
         // drop out of the maximum and get probability 0.
-        uint32_t sr[BN];
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_col + 32 * c, sr + 32 * c);
+        uint32_t sr[64];
+        tmem_ld32(s_col, sr);
+        tmem_ld32(s_col + 32, sr + 32);
         tmem_wait_ld();
-        tmem_pin<BN>(sr);
+        tmem_pin<64>(sr);
         if (!full) {
-          // Keys [clo, chi) of the tile are visible to row r: a 32-bit mask
+          // Keys [clo, chi) of the half are visible to row r: a 32-bit mask
           // per 32 columns, hidden scores set to -inf with one AND / OR each,
           // in straight-line code.
 #pragma unroll
-          for (int c32 = 0; c32 < BN / 32; ++c32) {
+          for (int c32 = 0; c32 < 2; ++c32) {
             const int lo = clo - 32 * c32 < 0 ? 0 : (clo - 32 * c32 > 32 ? 32 : clo - 32 * c32);
             const int hi = chi - 32 * c32 < lo ? lo : (chi - 32 * c32 > 32 ? 32 : chi - 32 * c32);
             const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
@@ -580,7 +530,12 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
             }
           }
         }
-        const float m_tile = max_tree<BN>(sr) * sl2;
+        // The row's tile maximum from both halves: both warpgroups then take
+        // the same decision on the common reference maximum.
+        const float mh = max_tree<64>(sr);
+        float mo;
+        if (!(ok = exchange(mh, &mo))) break;
+        const float m_tile = fmaxf(mh, mo) * sl2;
         const bool move = m_tile > m_ref + C::kRescaleThreshold;
         float corr = 1.f;
         if (move) {
@@ -588,11 +543,15 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
           l_run *= corr;
           m_ref = m_tile;
         }
-        // O[w] holds this warpgroup's earlier products of the item (complete:
-        // S of this tile was issued after them).
-        if (j >= 2 && __any_sync(0xffffffffu, move)) {
+        // O holds the item's products of tiles 0 .. j - 1; once the last of
+        // them has completed, this warpgroup rescales its half of the head
+        // dims (the other warpgroup, deciding alike, takes the other half).
+        if (j >= 1 && __any_sync(0xffffffffu, move)) {
+          const int gp = gg - 1;
+          if (!(ok = mbar_wait_warp(BAR(C::BAR_SFREE + (gp & 1)), (gp >> 1) & 1, ab))) break;
+          tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < D / 64; ++c) {
             uint32_t o[32];
             tmem_ld32(o_col + 32 * c, o);
             tmem_wait_ld();
@@ -605,13 +564,14 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         // Probabilities 2^(s * sl2 - m_use), two lanes per instruction for
         // the scaling and the sums (four independent pair accumulators),
-        // written back as bf16 pairs into columns [16c, 16c + 16) -- the
-        // scores there are already in registers.
+        // written back as bf16 pairs (e4m3 quadruples) into the first half of
+        // this warpgroup's columns -- the scores there are already in
+        // registers.
         const uint64_t scale2 = f2_pack(sl2, sl2);
         const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -635,17 +595,67 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
           else
             tmem_st16(s_col + 16 * c, pk);
         }
-        float a0, a1, b0, b1, c0, c1, d0, d1;
+        float a0, a1, b0, b1;
         f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
         f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
-        (void)c0; (void)c1; (void)d0; (void)d1;
         l_run += (a0 + a1) + (b0 + b1);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(BAR(C::BAR_PFULL + w));
+        mbar_arrive_warp(BAR(C::BAR_PFULL + sb));
       }
       if (!ok) break;
-      ok = merge(k, ig, qs, m_ref, l_run);
+      // ---------------------------------------------------------- read-out
+      // Once the item's last P V has completed: the row sum of both halves,
+      // then this warpgroup's half of the head dims of O, normalised, as
+      // bf16 into the item's query buffer (its last S product has completed)
+      // in the 128-byte-swizzled layout of a TMA box, for warp 11 to store;
+      // rows past the end of the half are dropped by the copy.
+      if (ig.ntiles > 0) {
+        const int gl = g + ig.ntiles - 1;
+        if (!(ok = mbar_wait_warp(BAR(C::BAR_SFREE + (gl & 1)), (gl >> 1) & 1, ab))) break;
+      }
+      tc_fence_after();
+      float l_other;
+      if (!(ok = exchange(l_run, &l_other))) break;
+      const float lsum = l_run + l_other;
+      // FP8: out = (P V8) * v_descale / l
+      const float inv = lsum > 0.f ? (FP8 ? p.out_scale : 1.f) / lsum : 0.f;
+      const uint32_t stage = sbase + C::kOffQ + qb * C::kQBytes;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = w * (D / 2) + 32 * c;
+        uint32_t oa[32];
+        tmem_ld32(o_col + 32 * c, oa);
+        tmem_wait_ld();
+        tmem_pin<32>(oa);
+#pragma unroll
+        for (int gq = 0; gq < 4; ++gq) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = lsum > 0.f ? __uint_as_float(oa[gq * 8 + 2 * e]) * inv : 0.f;
+            const float x1 = lsum > 0.f ? __uint_as_float(oa[gq * 8 + 2 * e + 1]) * inv : 0.f;
+            wv[e] = pack_bf16x2(x0, x1);
+          }
+          const int unit = col / 8 + gq;  // 16-byte unit of the row
+          st_shared_v4(stage + (unit >> 3) * (BM * 128) + row * 128 +
+                           (((unit & 7) ^ (row & 7)) << 4),
+                       wv[0], wv[1], wv[2], wv[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive_warp(BAR(C::BAR_OSTAGED + qb));
+      if (r < n && w == 0) {
+        const float lse =
+            lsum > 0.f ? (m_ref + lg2_approx(lsum)) * 0.69314718055994531f : -INFINITY;
+        if constexpr (VARLEN)
+          p.lse[static_cast<size_t>(ig.wi.h) * p.rows + ig.row0 + ig.wi.half * ig.n + r] = lse;
+        else
+          p.lse[lse_offset(p.mode, ig.wi.b, ig.wi.h, ig.wi.half, r, p.H, p.n)] = lse;
+      }
+      tc_fence_before();
+      mbar_arrive_warp(BAR(C::BAR_OFREE + qb));
+      g += ig.ntiles;
     }
   }
 #undef BAR

@@ -128,3 +128,32 @@ def test_causal_grouped_heads_step_api(b, Bc, n, H, Hk, d):
     assert np.abs(as64(lse) - rl).max() <= 1e-3
     for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
         assert nw(as64(got), ref) <= 2e-2
+
+
+@pytest.mark.parametrize("B,L,H,d", [(2, 600, 3, 64), (1, 2050, 32, 128), (3, 70, 8, 256),
+                                     (1, 10, 2100, 64), (2, 9, 1, 128), (1, 1, 5, 256)])
+@pytest.mark.parametrize("zero", [False, True])
+def test_preprocess_delta_and_zeroing(b, B, L, H, d, zero):
+    """D = rowsum(dout * out) ("FlashAttention: Exact Attention Without
+    Materialization", section 4.5), laid out (batch, head, position), for
+    few and very many heads (the latter stored without shared-memory
+    staging), ragged position counts, every head dimension; and the dq
+    accumulator zeroed when passed.  Compared with the float64 sum of the
+    same bf16 products."""
+    dev = torch.device("cuda", 0)
+    g = torch.Generator().manual_seed(31 + L + H + d)
+    out = torch.randn(B, L, H, d, generator=g).to(torch.bfloat16)
+    dout = torch.randn(B, L, H, d, generator=g).to(torch.bfloat16)
+    ref = (out.double() * dout.double()).sum(-1).permute(0, 2, 1).contiguous()  # (B, H, L)
+    delta = torch.full((B, H, L), float("nan"), dtype=torch.float32, device=dev)
+    acc = torch.full((B, L, H, d), 7.0, dtype=torch.float32, device=dev) if zero else None
+    mode = b.MODE_CAUSAL  # rows of L positions per batch entry, L odd allowed
+    b.dfa_bwd_preprocess(out.to(dev), dout.to(dev), delta, acc, mode=mode)
+    torch.cuda.synchronize()
+    assert b.dfa_status() == b.DFA_OK
+    got = delta.cpu().double()
+    assert bool(torch.isfinite(got).all())
+    bar = 1e-5 * (out.double().abs() * dout.double().abs()).sum(-1).permute(0, 2, 1) + 1e-6
+    assert bool(((got - ref).abs() <= bar).all()), float((got - ref).abs().max())
+    if zero:
+        assert bool((acc == 0).all())

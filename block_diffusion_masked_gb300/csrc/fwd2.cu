@@ -14,15 +14,17 @@
 // reference maximum is common to both (one exchange of half-row maxima
 // through shared memory per tile), so the probabilities of the two halves
 // feed a single output accumulator O in TMEM and nothing is merged at the
-// end of an item.  Scores S = Q K^T land in one of two TMEM buffers, so the
-// scores of the next tile are computed while the softmax of this one runs;
+// end of an item.  Scores S = Q K^T land in one of three TMEM buffers, so the
+// scores of the next two tiles are computed while the softmax of this one
+// runs (a tile's products and softmax form a chain of about three times the
+// tensor-core time of a tile, most of it latency);
 // each warpgroup writes its probabilities as bf16 back into the first half
 // of its own columns of the buffer, where O += P V reads them as the MMA's A
 // operand.  A row's reference maximum is only moved (O and the sum
 // rescaled) when a tile maximum exceeds it by more than 2^8: exact in real
-// arithmetic, and probabilities stay below 256.  O is double-buffered by
-// item, so the next item's first products need not wait for the read-out of
-// this one.
+// arithmetic, and probabilities stay below 256.  With headdim 64 O is also
+// double-buffered by item, so the next item's first products need not wait
+// for the read-out of this one.
 //
 // The K/V ring, the query double buffer and all barrier phases run on across
 // items, so the loads and S products of the next item overlap the read-out
@@ -63,6 +65,8 @@ struct Fwd2Cfg {
   static constexpr int kOffQ = 0;  // 2 buffers
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + STAGES * kKVBytes;
+  // TMEM buffers of S (tiles in flight between the S product and P V)
+  static constexpr int kSBufs = 3;
   // exchange slots of the two softmax warpgroups: [round % 2][warpgroup][row]
   static constexpr int kOffX = kOffV + STAGES * kKVBytes;
   static constexpr int kOffBar = kOffX + 2 * 2 * BM * 4;
@@ -73,10 +77,10 @@ struct Fwd2Cfg {
     BAR_KEMPTY = BAR_KFULL + STAGES,  // [STAGES]
     BAR_VFULL = BAR_KEMPTY + STAGES,  // [STAGES]
     BAR_VEMPTY = BAR_VFULL + STAGES,  // [STAGES]
-    BAR_SFULL = BAR_VEMPTY + STAGES,  // [2] per S buffer: S of its tile complete
-    BAR_PFULL = BAR_SFULL + 2,        // [2] per S buffer: P of its tile written (8 warps)
-    BAR_SFREE = BAR_PFULL + 2,        // [2] per S buffer: P V of its tile complete
-    BAR_OFREE = BAR_SFREE + 2,        // [2] per O buffer: read out (8 warps)
+    BAR_SFULL = BAR_VEMPTY + STAGES,    // [kSBufs] per S buffer: S of its tile complete
+    BAR_PFULL = BAR_SFULL + kSBufs,     // [kSBufs] per S buffer: P of its tile written (8 warps)
+    BAR_SFREE = BAR_PFULL + kSBufs,     // [kSBufs] per S buffer: P V of its tile complete
+    BAR_OFREE = BAR_SFREE + kSBufs,     // [2] per O buffer: read out (8 warps)
     BAR_XCHG = BAR_OFREE + 2,         // one exchange round of the softmax warps (8 warps)
     BAR_ITEMFULL = BAR_XCHG + 1,      // [4] item published
     BAR_OSTAGED = BAR_ITEMFULL + 4,   // [2] per query buffer: the item's out tile staged in it
@@ -87,13 +91,15 @@ struct Fwd2Cfg {
   static constexpr int kOffTmemSlot = kOffItem + 4 * 128;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
-  // S[b] at b * BN; warpgroup w's P in columns [64 w, 64 w + 32) of it
+  // S[b] at b * BN (tile g in buffer g % kSBufs); warpgroup w's P in
+  // columns [64 w, 64 w + 32) of it.  O[item % kOBufs] after the S buffers.
   static constexpr int kTmemS = 0;
-  static constexpr int kTmemO = 2 * BN;  // O[item % 2] at kTmemO + (item % 2) * D
+  static constexpr int kTmemO = kSBufs * BN;
+  static constexpr int kOBufs = kSBufs * BN + 2 * D <= 512 ? 2 : 1;
   static constexpr int kTmemCols = 512;
   static constexpr int kThreads = 384;
   static constexpr float kRescaleThreshold = 8.0f;  // log2 units
-  static_assert(2 * BN + 2 * D <= kTmemCols, "TMEM budget");
+  static_assert(kTmemO + kOBufs * D <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -169,11 +175,13 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(C::BAR_QFULL + b), 1);
       mbar_init(BAR(C::BAR_QEMPTY + b), 1);
+      mbar_init(BAR(C::BAR_OFREE + b), 8);
+      mbar_init(BAR(C::BAR_OSTAGED + b), 8);
+    }
+    for (int b = 0; b < C::kSBufs; ++b) {
       mbar_init(BAR(C::BAR_SFULL + b), 1);
       mbar_init(BAR(C::BAR_PFULL + b), 8);
       mbar_init(BAR(C::BAR_SFREE + b), 1);
-      mbar_init(BAR(C::BAR_OFREE + b), 8);
-      mbar_init(BAR(C::BAR_OSTAGED + b), 8);
     }
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(BAR(C::BAR_KFULL + s), 1);
@@ -308,9 +316,10 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     // products slow down while the softmax warps that share its scheduler are
     // busy; from two warps on two schedulers they keep the tensor pipe fed.
     // The two streams meet only through barriers: S of tile g goes into
-    // buffer g % 2 once P V of tile g - 2 (whose P it held) has completed
-    // (SFREE); P V of a tile waits for both warpgroups' P (PFULL), and the
-    // first P V of an item for the read-out of the O buffer it reuses (OFREE).
+    // buffer g % kSBufs once P V of tile g - kSBufs (whose P it held) has
+    // completed (SFREE); P V of a tile waits for both warpgroups' P (PFULL),
+    // and the first P V of an item for the read-out of the O buffer it reuses
+    // (OFREE).
     if (lane == 0) {
       const bool s_warp = warp == 10;
       constexpr uint32_t kIdS =
@@ -331,21 +340,24 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         const ItemGeom ig = *ring(k & 3);
         if (ig.item < 0) break;
         const int qb = k & 1;
+        const int ob = k % C::kOBufs;
         if (s_warp) {
           if (!(ok = mbar_wait(BAR(C::BAR_QFULL + qb), (k >> 1) & 1, ab))) break;
         } else {
-          // O buffer k % 2 still holds item k - 2 until it is read out.
-          if (k >= 2 && !(ok = mbar_wait(BAR(C::BAR_OFREE + qb), ((k >> 1) - 1) & 1, ab))) break;
+          // O buffer ob still holds item k - kOBufs until it is read out.
+          if (k >= C::kOBufs &&
+              !(ok = mbar_wait(BAR(C::BAR_OFREE + ob), ((k / C::kOBufs) - 1) & 1, ab)))
+            break;
         }
         tc_fence_after();
         for (int j = 0; j < ig.ntiles && ok; ++j) {
           const int gg = g + j;
           const int st = gg % STAGES;
-          const int sb = gg & 1;
+          const int sb = gg % C::kSBufs;
+          const int su = gg / C::kSBufs;  // earlier tiles in buffer sb
           if (s_warp) {
             if (!(ok = mbar_wait(BAR(C::BAR_KFULL + st), (gg / STAGES) & 1, ab))) break;
-            if (gg >= 2 && !(ok = mbar_wait(BAR(C::BAR_SFREE + sb), ((gg >> 1) - 1) & 1, ab)))
-              break;
+            if (su >= 1 && !(ok = mbar_wait(BAR(C::BAR_SFREE + sb), (su - 1) & 1, ab))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < C::kKSteps; ++kk) {
@@ -359,7 +371,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
             mma_commit(BAR(C::BAR_SFULL + sb));
             mma_commit(BAR(C::BAR_KEMPTY + st));
           } else {
-            if (!(ok = mbar_wait(BAR(C::BAR_PFULL + sb), (gg >> 1) & 1, ab))) break;
+            if (!(ok = mbar_wait(BAR(C::BAR_PFULL + sb), su & 1, ab))) break;
             if (!(ok = mbar_wait(BAR(C::BAR_VFULL + st), (gg / STAGES) & 1, ab))) break;
             tc_fence_after();
 #pragma unroll
@@ -375,9 +387,9 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
                   adv(dV, st * C::kKVBytes + (FP8 ? kk * 32 : kk * C::kPVKeys * 128));
               const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
               if constexpr (FP8)
-                mma_ts_f8(tmem + C::kTmemO + qb * D, tmem + pcol, b, kIdPV, acc);
+                mma_ts_f8(tmem + C::kTmemO + ob * D, tmem + pcol, b, kIdPV, acc);
               else
-                mma_ts(tmem + C::kTmemO + qb * D, tmem + pcol, b, kIdPV, acc);
+                mma_ts(tmem + C::kTmemO + ob * D, tmem + pcol, b, kIdPV, acc);
             }
             mma_commit(BAR(C::BAR_VEMPTY + st));
             mma_commit(BAR(C::BAR_SFREE + sb));
@@ -464,13 +476,14 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     float* const xslots = reinterpret_cast<float*>(smem + C::kOffX);
     int xc = 0;  // exchange rounds so far (the same sequence in both warpgroups)
     // One exchange round: this thread's value for its row goes to the other
-    // warpgroup, whose value for the same row comes back.
-    auto exchange = [&](float mine, float* theirs) -> bool {
-      float* xs = xslots + (xc & 1) * 2 * BM;
-      xs[w * BM + row] = mine;
+    // warpgroup (post), whose value for the same row comes back (collect).
+    auto exchange_post = [&](float mine) {
+      xslots[(xc & 1) * 2 * BM + w * BM + row] = mine;
       mbar_arrive_warp(BAR(C::BAR_XCHG));
+    };
+    auto exchange_collect = [&](float* theirs) -> bool {
       if (!mbar_wait_warp(BAR(C::BAR_XCHG), xc & 1, ab)) return false;
-      *theirs = xs[(1 - w) * BM + row];
+      *theirs = xslots[(xc & 1) * 2 * BM + (1 - w) * BM + row];
       ++xc;
       return true;
     };
@@ -480,7 +493,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
       const ItemGeom ig = *ring(k & 3);
       if (ig.item < 0) break;
-      const int qb = k & 1;  // query buffer and O buffer of the item
+      const int qb = k & 1;  // query buffer of the item
+      const int ob = k % C::kOBufs;
       const int qs = ig.qs;
       const int r = qs + row;  // row inside the half
       // Keys visible to row r, per segment of the item: computed once, so a
@@ -489,16 +503,16 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       const int bs = VARLEN ? imin(p.bs, n) : p.bs;
       const Interval kv0 = key_interval(ig.rule0, r, n, bs);
       const Interval kv1 = key_interval(ig.rule1, r, n, bs);
-      const uint32_t o_col = t_lane + C::kTmemO + qb * D + w * (D / 2);
+      const uint32_t o_col = t_lane + C::kTmemO + ob * D + w * (D / 2);
       float m_ref = -INFINITY;  // reference maximum, scaled log2 units
       float l_run = 0.f;        // running sum of 2^(s * sl2 - m_ref) over this half's keys
       for (int j = 0; j < ig.ntiles; ++j) {
         const int gg = g + j;
-        const int sb = gg & 1;
+        const int sb = gg % C::kSBufs;
         const int seg = j < ig.n0 ? 0 : 1;
         const int kt = ig.ktile(j);
         const uint32_t s_col = t_lane + C::kTmemS + sb * BN + 64 * w;
-        if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + sb), (gg >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + sb), (gg / C::kSBufs) & 1, ab))) break;
         tc_fence_after();
         const int ks = kt * BN + 64 * w;
         const Interval iv = seg ? kv1 : kv0;
@@ -534,7 +548,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         // the same decision on the common reference maximum.
         const float mh = max_tree<64>(sr);
         float mo;
-        if (!(ok = exchange(mh, &mo))) break;
+        exchange_post(mh);
+        if (!(ok = exchange_collect(&mo))) break;
         const float m_tile = fmaxf(mh, mo) * sl2;
         const bool move = m_tile > m_ref + C::kRescaleThreshold;
         float corr = 1.f;
@@ -548,7 +563,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         // dims (the other warpgroup, deciding alike, takes the other half).
         if (j >= 1 && __any_sync(0xffffffffu, move)) {
           const int gp = gg - 1;
-          if (!(ok = mbar_wait_warp(BAR(C::BAR_SFREE + (gp & 1)), (gp >> 1) & 1, ab))) break;
+          if (!(ok = mbar_wait_warp(BAR(C::BAR_SFREE + gp % C::kSBufs), (gp / C::kSBufs) & 1, ab)))
+            break;
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
@@ -612,11 +628,13 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       // rows past the end of the half are dropped by the copy.
       if (ig.ntiles > 0) {
         const int gl = g + ig.ntiles - 1;
-        if (!(ok = mbar_wait_warp(BAR(C::BAR_SFREE + (gl & 1)), (gl >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(BAR(C::BAR_SFREE + gl % C::kSBufs), (gl / C::kSBufs) & 1, ab)))
+          break;
       }
       tc_fence_after();
       float l_other;
-      if (!(ok = exchange(l_run, &l_other))) break;
+      exchange_post(l_run);
+      if (!(ok = exchange_collect(&l_other))) break;
       const float lsum = l_run + l_other;
       // FP8: out = (P V8) * v_descale / l
       const float inv = lsum > 0.f ? (FP8 ? p.out_scale : 1.f) / lsum : 0.f;
@@ -654,7 +672,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
           p.lse[lse_offset(p.mode, ig.wi.b, ig.wi.h, ig.wi.half, r, p.H, p.n)] = lse;
       }
       tc_fence_before();
-      mbar_arrive_warp(BAR(C::BAR_OFREE + qb));
+      mbar_arrive_warp(BAR(C::BAR_OFREE + ob));
       g += ig.ntiles;
     }
   }

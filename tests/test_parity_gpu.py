@@ -113,6 +113,29 @@ def test_edge_cases(b, B, n, H, d, bs):
     _check(res, q, k, v, do, bs)
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("step", [0.5, 2.0])
+def test_rising_scores_move_the_reference(b, d, step):
+    """Scores that rise from one 64-key half-tile to the next by about 2^8
+    or more in the softmax's base-2 units ("FlashAttention: Exact Attention
+    Without Materialization", section 4.2: the online softmax rescales its
+    running sum and output whenever the maximum grows): the kernels' reference
+    maximum then moves on almost every tile, with the two halves of a tile
+    disagreeing, and O and the row sum are rescaled.  out and lse must stay
+    within the bars against the oracle.  (The backward, which reads the
+    stored LSE and has no running maximum, is not compared here: on these
+    inputs dQ sums large cancelling terms against K entries up to 32, so its
+    normwise error measures bf16 rounding of dS rather than the kernel.)"""
+    B, n, H, bs = 1, 300, 2, 16
+    q, k, v, do = inputs.make_inputs(B, n, H, d, seed=900 + d)
+    pos = torch.arange(2 * n) % n
+    ramp = (pos // 64).float() * 16.0 * step
+    q[..., 0] = 8.0
+    k[..., 0] = ramp.view(1, -1, 1).to(k.dtype)
+    res = _run_gpu(b, q, k, v, do, bs, backward=False)
+    _check(res, q, k, v, do, bs, backward=False)
+
+
 @pytest.mark.parametrize("n,bs", [(67, 3), (256, 64), (300, 1)])
 def test_headdim_256(b, n, bs):
     q, k, v, do = inputs.make_inputs(1, n, 2, 256, seed=7 + n)

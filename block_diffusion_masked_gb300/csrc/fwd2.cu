@@ -49,7 +49,9 @@ namespace dfa {
 // 128-byte rows hold 128 elements, a K step of the products is 32 elements,
 // P goes to TMEM as four e4m3 per column; out stays bf16, staged in the
 // query buffer, which keeps the bf16 tile's size.
-template <int D, int STAGES, bool FP8 = false>
+// STAGES K tiles and VSTAGES V tiles in flight (a K tile is needed first,
+// by S, a V tile a softmax later, by P V).
+template <int D, int STAGES, int VSTAGES, bool FP8 = false>
 struct Fwd2Cfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
@@ -64,20 +66,20 @@ struct Fwd2Cfg {
   static constexpr int kKVBytes = BN * D * ES;
   static constexpr int kOffQ = 0;  // 2 buffers
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
-  static constexpr int kOffV = kOffK + STAGES * kKVBytes;
+  static constexpr int kOffV = kOffK + STAGES * kKVBytes;  // [VSTAGES]
   // TMEM buffers of S (tiles in flight between the S product and P V)
   static constexpr int kSBufs = 3;
   // exchange slots of the two softmax warpgroups: [round % 2][warpgroup][row]
-  static constexpr int kOffX = kOffV + STAGES * kKVBytes;
+  static constexpr int kOffX = kOffV + VSTAGES * kKVBytes;
   static constexpr int kOffBar = kOffX + 2 * 2 * BM * 4;
   enum {
     BAR_QFULL = 0,                    // [2]
     BAR_QEMPTY = BAR_QFULL + 2,       // [2]
-    BAR_KFULL = BAR_QEMPTY + 2,       // [STAGES]
-    BAR_KEMPTY = BAR_KFULL + STAGES,  // [STAGES]
-    BAR_VFULL = BAR_KEMPTY + STAGES,  // [STAGES]
-    BAR_VEMPTY = BAR_VFULL + STAGES,  // [STAGES]
-    BAR_SFULL = BAR_VEMPTY + STAGES,    // [kSBufs] per S buffer: S of its tile complete
+    BAR_KFULL = BAR_QEMPTY + 2,        // [STAGES]
+    BAR_KEMPTY = BAR_KFULL + STAGES,   // [STAGES]
+    BAR_VFULL = BAR_KEMPTY + STAGES,   // [VSTAGES]
+    BAR_VEMPTY = BAR_VFULL + VSTAGES,  // [VSTAGES]
+    BAR_SFULL = BAR_VEMPTY + VSTAGES,   // [kSBufs] per S buffer: S of its tile complete
     BAR_PFULL = BAR_SFULL + kSBufs,     // [kSBufs] per S buffer: P of its tile written (8 warps)
     BAR_SFREE = BAR_PFULL + kSBufs,     // [kSBufs] per S buffer: P V of its tile complete
     BAR_OFREE = BAR_SFREE + kSBufs,     // [2] per O buffer: read out (8 warps)
@@ -90,7 +92,9 @@ struct Fwd2Cfg {
   static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 decoded items (ItemGeom)
   static constexpr int kOffTmemSlot = kOffItem + 4 * 128;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
-  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
+  // The dynamic shared memory starts 1024-byte aligned (the kernel checks
+  // this, for the 128-byte swizzle of the TMA boxes and MMA operands).
+  static constexpr int kSmemBytes = kOffAbort + 4;
   // S[b] at b * BN (tile g in buffer g % kSBufs); warpgroup w's P in
   // columns [64 w, 64 w + 32) of it.  O[item % kOBufs] after the S buffers.
   static constexpr int kTmemS = 0;
@@ -152,14 +156,21 @@ __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, 
   g->qs = g->wi.tile * bm;
 }
 
-template <int D, int STAGES, bool VARLEN, bool FP8 = false>
+template <int D, int STAGES, int VSTAGES, bool VARLEN, bool FP8 = false>
 __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant__ FwdParams p) {
-  using C = Fwd2Cfg<D, STAGES, FP8>;
+  using C = Fwd2Cfg<D, STAGES, VSTAGES, FP8>;
   constexpr int BM = C::BM;
   constexpr int BN = C::BN;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem_raw) & 1023u) {
+    // not the layout this kernel was built for: report, take no work
+    if (threadIdx.x == 0) {
+      atomicOr(p.status, kStatusIndex);
+      sched_finish(p.sched);
+    }
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -186,6 +197,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(BAR(C::BAR_KFULL + s), 1);
       mbar_init(BAR(C::BAR_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < VSTAGES; ++s) {
       mbar_init(BAR(C::BAR_VFULL + s), 1);
       mbar_init(BAR(C::BAR_VEMPTY + s), 1);
     }
@@ -230,8 +243,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       int vg = -1, vh = 0, vc2 = 0, vc3 = 0, vc4 = 0;
       const CUtensorMap* vmap = &p.tm_v;
       auto load_v = [&]() -> bool {
-        const int st = vg % STAGES;
-        const int round = vg / STAGES;
+        const int st = vg % VSTAGES;
+        const int round = vg / VSTAGES;
         if (round > 0 && !mbar_wait(BAR(C::BAR_VEMPTY + st), (round - 1) & 1, ab)) return false;
         mbar_arrive_expect_tx(BAR(C::BAR_VFULL + st), C::kKVBytes);
 #pragma unroll
@@ -372,7 +385,8 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
             mma_commit(BAR(C::BAR_KEMPTY + st));
           } else {
             if (!(ok = mbar_wait(BAR(C::BAR_PFULL + sb), su & 1, ab))) break;
-            if (!(ok = mbar_wait(BAR(C::BAR_VFULL + st), (gg / STAGES) & 1, ab))) break;
+            const int vs = gg % VSTAGES;
+            if (!(ok = mbar_wait(BAR(C::BAR_VFULL + vs), (gg / VSTAGES) & 1, ab))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kPVSteps; ++kk) {
@@ -384,14 +398,14 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
               const uint32_t pcol =
                   C::kTmemS + sb * BN + 64 * (kk / kStepsPerHalf) + 8 * (kk % kStepsPerHalf);
               const uint64_t b =
-                  adv(dV, st * C::kKVBytes + (FP8 ? kk * 32 : kk * C::kPVKeys * 128));
+                  adv(dV, vs * C::kKVBytes + (FP8 ? kk * 32 : kk * C::kPVKeys * 128));
               const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
               if constexpr (FP8)
                 mma_ts_f8(tmem + C::kTmemO + ob * D, tmem + pcol, b, kIdPV, acc);
               else
                 mma_ts(tmem + C::kTmemO + ob * D, tmem + pcol, b, kIdPV, acc);
             }
-            mma_commit(BAR(C::BAR_VEMPTY + st));
+            mma_commit(BAR(C::BAR_VEMPTY + vs));
             mma_commit(BAR(C::BAR_SFREE + sb));
           }
         }
@@ -689,10 +703,10 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int STAGES, bool VARLEN, bool FP8 = false>
+template <int D, int STAGES, int VSTAGES, bool VARLEN, bool FP8 = false>
 static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
-  using C = Fwd2Cfg<D, STAGES, FP8>;
-  auto kern = dfa_fwd2_kernel<D, STAGES, VARLEN, FP8>;
+  using C = Fwd2Cfg<D, STAGES, VSTAGES, FP8>;
+  auto kern = dfa_fwd2_kernel<D, STAGES, VSTAGES, VARLEN, FP8>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -708,20 +722,22 @@ static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
                         stream, p);
 }
 
-// FP8 (e4m3) q, k, v, headdim 128: smaller K / V tiles, so four stages.
+// FP8 (e4m3) q, k, v, headdim 128: smaller K / V tiles, so more stages.
 cudaError_t launch_forward_fp8(const FwdParams& p, int headdim, cudaStream_t stream) {
   if (headdim != 128 || p.vl) return cudaErrorInvalidValue;
-  return launch_fwd2_impl<128, 4, false, true>(p, stream);
+  return launch_fwd2_impl<128, 5, 4, false, true>(p, stream);
 }
 
+// K / V stages per head dimension: as many K tiles in flight as the shared
+// memory holds beside two query tiles and the V ring.
 cudaError_t launch_forward_two_warpgroups(const FwdParams& p, int headdim, cudaStream_t stream) {
   switch (headdim) {
     case 64:
-      return p.vl ? launch_fwd2_impl<64, 4, true>(p, stream)
-                  : launch_fwd2_impl<64, 4, false>(p, stream);
+      return p.vl ? launch_fwd2_impl<64, 6, 4, true>(p, stream)
+                  : launch_fwd2_impl<64, 6, 4, false>(p, stream);
     case 128:
-      return p.vl ? launch_fwd2_impl<128, 2, true>(p, stream)
-                  : launch_fwd2_impl<128, 2, false>(p, stream);
+      return p.vl ? launch_fwd2_impl<128, 3, 2, true>(p, stream)
+                  : launch_fwd2_impl<128, 3, 2, false>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

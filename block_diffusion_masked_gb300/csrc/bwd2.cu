@@ -902,20 +902,32 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       }
       tc_fence_before();
       mbar_arrive_warp(BAR(C::BAR_ACCFREE));
-      if (j < n) {
+      const size_t first = VARLEN ? static_cast<size_t>(it.row0)
+                                  : static_cast<size_t>(it.wi.b) * 2 * static_cast<size_t>(p.n);
+      if constexpr (C::kTmaDQ) {
+        // The warp's 32 key rows (dK needs no scale: it is already in dS),
+        // through the warp's dQ staging tile (once its last reduce has read
+        // it), so that the stores coalesce: a row of the item's 128 dims is
+        // 256 bytes, 8 KB or so from the next.
+        const int j0 = ks + (warp & 3) * 32;  // the warp's first key
+        const size_t row0 = first + static_cast<size_t>(it.wi.half) * n + j0;
+        __nv_bfloat16* dst0 = (is_v ? p.dv : p.dk) + (row0 * p.Hk + it.wi.h) * D + it.dh * DH + d0;
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        store_rows_staged<DW, 128>(o, dst0, static_cast<size_t>(p.Hk) * D, n - j0,
+                                   sbase + C::kOffDQS + warp * C::kDQSBytes, lane);
+      } else if (j < n) {
+        // headdim 256 (no staging tile left): each thread its own row
         const size_t pos = static_cast<size_t>(it.wi.half) * n + j;
-        const size_t first = VARLEN ? static_cast<size_t>(it.row0)
-                                    : static_cast<size_t>(it.wi.b) * 2 * static_cast<size_t>(p.n);
         const size_t off = ((first + pos) * p.Hk + it.wi.h) * D + it.dh * DH + d0;
         __nv_bfloat16* dst = (is_v ? p.dv : p.dk) + off;
-        const float mul = 1.f;  // dK: the scale is already in dS
 #pragma unroll
         for (int g8 = 0; g8 < DW / 8; ++g8) {
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(o[g8 * 8 + 2 * e]) * mul,
-                               __uint_as_float(o[g8 * 8 + 2 * e + 1]) * mul);
+            w[e] = pack_bf16x2(__uint_as_float(o[g8 * 8 + 2 * e]),
+                               __uint_as_float(o[g8 * 8 + 2 * e + 1]));
           st_global_v4(dst + 8 * g8, w[0], w[1], w[2], w[3]);
         }
       }

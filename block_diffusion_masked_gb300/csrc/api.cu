@@ -392,6 +392,9 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   if (d == 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, halves, n, H, d,
                                       ts.bwd_bm / kBwd2WarpgroupsD128)))
     return rc;
+  if (d == 128 && ((rc = make_map(&p.tm_dk, dk, halves, n, Hk, d, 32)) ||
+                   (rc = make_map(&p.tm_dv, dv, halves, n, Hk, d, 32))))
+    return rc;
   p.lse = lse;
   p.delta = delta;
   p.dq_acc = dq_acc;
@@ -592,10 +595,12 @@ int varlen_schedule(const int* cu, int batch, int heads, int tile, long long byt
 // Tensor maps of every slot's sample: (d, H, n, 2, 1) views starting at
 // the sample's first row, so that rows past the end of a half read zero.
 // Forward: q (box bm rows), k, v (box bn rows); backward also dout (bm) and,
-// if dq_acc is given, the float32 accumulator (box dq_rows rows of 32).
+// if dq_acc is given, the float32 accumulator (box dq_rows rows of 32); if
+// dk / dv are given, those (box 32 rows), which the stores go through.
 int varlen_maps(const std::vector<VarlenSlot>& slots, const void* q, const void* k,
                 const void* v, const void* dout, int H, int Hk, int d, int bm, int bn,
-                std::vector<VarlenMaps>* maps, const float* dq_acc = nullptr, int dq_rows = 0) {
+                std::vector<VarlenMaps>* maps, const float* dq_acc = nullptr, int dq_rows = 0,
+                const void* dk = nullptr, const void* dv = nullptr) {
   maps->assign(slots.size(), VarlenMaps{});
   const size_t qrow = static_cast<size_t>(H) * d * 2, krow = static_cast<size_t>(Hk) * d * 2;
   for (size_t i = 0; i < slots.size(); ++i) {
@@ -614,6 +619,12 @@ int varlen_maps(const std::vector<VarlenSlot>& slots, const void* q, const void*
       return rc;
     if (dq_acc && (rc = make_map_f32(&m.dq, dq_acc + static_cast<size_t>(sl.row0) * H * d, 2,
                                      sl.n, H, d, dq_rows)))
+      return rc;
+    if (dk && (rc = make_map(&m.dk, static_cast<const char*>(dk) + sl.row0 * krow, 2, sl.n, Hk,
+                             d, 32)))
+      return rc;
+    if (dv && (rc = make_map(&m.dv, static_cast<const char*>(dv) + sl.row0 * krow, 2, sl.n, Hk,
+                             d, 32)))
       return rc;
   }
   return DFA_OK;
@@ -741,11 +752,13 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
     cudaFreeAsync(dq_acc, stream);
     return DFA_ECUDA;
   }
-  // q, dout, k, v and the dq accumulator through per-sample maps (rows past
-  // a half read zero; reduce-adds past a half are skipped)
+  // q, dout, k, v, the dq accumulator and (headdim 128) dk, dv through
+  // per-sample maps (rows past a half read zero; reduce-adds and stores past
+  // a half are skipped)
   std::vector<VarlenMaps> maps;
   if ((rc = varlen_maps(slots, q, k, v, dout, H, Hk, d, ts.bwd_bm, ts.bwd_bn, &maps,
-                        d == 128 ? dq_acc : nullptr, ts.bwd_bm / kBwd2WarpgroupsD128)) ||
+                        d == 128 ? dq_acc : nullptr, ts.bwd_bm / kBwd2WarpgroupsD128,
+                        d == 128 ? dk : nullptr, d == 128 ? dv : nullptr)) ||
       (rc = upload_slots(slots, maps, stream, &dmaps, &dslots))) {
     cudaFreeAsync(delta, stream);
     cudaFreeAsync(dq_acc, stream);

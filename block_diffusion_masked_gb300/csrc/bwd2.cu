@@ -12,11 +12,18 @@
 //   P^T  = exp(scale S^T - LSE) (0 on hidden pairs),
 //   dS^T = scale * P^T (dP^T - D)  (the softmax scale of dQ and dK, taken
 //        here once per element instead of on every dQ and dK element)
-//        bf16 P^T / dS^T -> TMEM PdS, dS^T also -> shared memory
-//   dV  += P^T dO,  dK += dS^T Q       (A operand read from TMEM PdS)
+//        bf16 P^T -> TMEM (two buffers), dS^T -> a shared-memory tile
+//        (two; headdim 256: one, and dS^T also -> TMEM beside P^T)
+//   dV  += P^T dO  (A operand read from TMEM),
+//   dK  += dS^T Q  (A operand read from the shared dS^T tile; headdim 256:
+//        from TMEM)
 //   dQ^T = K^T dS^T  -> TMEM DQ, then added to a float32 accumulator in
 //        device memory (each warp covers 32 consecutive head dims of a query)
-// TMEM (512 columns): S 64 | dP 64 | PdS 64 | DQ 64 | dK 128 | dV 128.
+// TMEM (512 columns): S 64 | dP 64 | P 2 x 32 (headdim 256: P / dS 64) |
+// DQ 64 | dK 128 | dV 128.  With two P^T buffers and two dS^T tiles a
+// tile's P^T / dS^T are written while the tile before is still in its
+// products: the compute warpgroups wait only for the products of the tile
+// before that.
 // With headdim 256 the dK and dV accumulators of all head dims would need
 // every TMEM column, so an item covers one 128-wide half of the head
 // dimension of its key tile: it recomputes S^T and dP^T in full (their
@@ -100,6 +107,11 @@ struct Bwd2Cfg {
   static constexpr int kOffV = kOffK + KVBUF * kKVBytes;   // [KVBUF]
   static constexpr int kOffQ = kOffV + KVBUF * kKVBytes;   // ring: the chunk slots
   static constexpr int kOffDO = kOffQ + STAGES * kQBytes;  // (no ring)
+  // dS^T tiles in shared memory (the A operand of dK += dS^T Q and the B
+  // operand of dQ^T = K^T dS^T): two with headdim 128, so that a tile's dS^T
+  // is written while the tile before is still in its products; one with
+  // 256 (no room for a second).
+  static constexpr int kDSBufs = kChunkRing ? 1 : 2;
   static constexpr int kOffDS =
       kChunkRing ? kOffQ + (kOhSlots + kDhSlots) * kSlotBytes : kOffDO + STAGES * kQBytes;
   // dQ staging, one tile per compute warp: float32 [HC queries][32 head
@@ -108,7 +120,7 @@ struct Bwd2Cfg {
   // per-thread atomics).
   static constexpr bool kTmaDQ = D == 128 && KVBUF == 1;
   static constexpr int kDQSBytes = HC * 32 * 4;
-  static constexpr int kOffDQS = kOffDS + kDSBytes;
+  static constexpr int kOffDQS = kOffDS + kDSBufs * kDSBytes;
   static constexpr int kOffLSE = kOffDQS + (kTmaDQ ? kComputeWarps * kDQSBytes : 0);  // kLseBufs x BMQ floats
   static constexpr int kOffDEL = kOffLSE + kLseBufs * BMQ * 4;  // kLseBufs x BMQ floats
   static constexpr int kOffBar = kOffDEL + kLseBufs * BMQ * 4;
@@ -118,9 +130,9 @@ struct Bwd2Cfg {
     BAR_QEMPTY = BAR_QFULL + kQBars,
     BAR_SDPFULL = BAR_QEMPTY + kQBars,  // S^T and dP^T of a tile computed
     BAR_SDPFREE = BAR_SDPFULL + 1,      // S^T / dP^T read into registers
-    BAR_PDSFULL = BAR_SDPFREE + 1,      // P^T / dS^T of a tile in place
-    BAR_MMA2 = BAR_PDSFULL + 1,         // dV, dK, dQ of a tile done
-    BAR_DQFREE = BAR_MMA2 + 1,          // dQ of a tile read out of TMEM
+    BAR_PDSFULL = BAR_SDPFREE + 1,      // [2] per tile parity: P^T / dS^T of a tile in place
+    BAR_MMA2 = BAR_PDSFULL + 2,         // [kDSBufs] per dS^T tile: dV, dK, dQ of a tile done
+    BAR_DQFREE = BAR_MMA2 + 2,          // dQ of a tile read out of TMEM
     BAR_ITEMDONE = BAR_DQFREE + 1,      // [KVBUF] every MMA of an item done
     BAR_ACCFREE = BAR_ITEMDONE + KVBUF, // dK / dV of an item read out of TMEM
     BAR_ITEMFULL = BAR_ACCFREE + 1,     // [4] item index published
@@ -130,10 +142,18 @@ struct Bwd2Cfg {
   static constexpr int kOffItem = kOffBar + NUM_BARS * 8;  // 4 decoded items (Bwd2Item)
   static constexpr int kOffTmemSlot = kOffItem + 4 * 128;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
-  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;
+  // The dynamic shared memory starts 1024-byte aligned (the kernel checks
+  // this, for the 128-byte swizzle of the TMA boxes and MMA operands).
+  static constexpr int kSmemBytes = kOffAbort + 4;
   static constexpr int kTmemS = 0;
   static constexpr int kTmemDP = 64;
-  static constexpr int kTmemPDS = 128;
+  // Headdim 128: P^T of tile g at kTmemP + 32 (g % 2) (64 queries, bf16
+  // pairs).  Headdim 256: one buffer of P^T and dS^T together, 32-column
+  // chunk c holding P^T of queries [32 c, 32 c + 32) in its first 16 columns
+  // and dS^T in the last 16 (both A operands read from TMEM: with a single
+  // dS^T tile, reading it from shared memory buys no overlap and costs the
+  // ring's shared-memory bandwidth).
+  static constexpr int kTmemP = 128;
   static constexpr int kTmemDQ = 192;
   static constexpr int kTmemDK = 256;
   static constexpr int kTmemDV = 384;
@@ -226,8 +246,15 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
   constexpr int BMQ = C::BMQ;
   constexpr int STAGES = C::STAGES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem_raw) & 1023u) {
+    // not the layout this kernel was built for: report, take no work
+    if (threadIdx.x == 0) {
+      atomicOr(p.status, kStatusIndex);
+      sched_finish(p.sched);
+    }
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -251,8 +278,10 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
     }
     mbar_init(BAR(C::BAR_SDPFULL), 2);  // the S^T and the dP^T warps
     mbar_init(BAR(C::BAR_SDPFREE), C::kComputeWarps);
-    mbar_init(BAR(C::BAR_PDSFULL), C::kComputeWarps);
-    mbar_init(BAR(C::BAR_MMA2), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(BAR(C::BAR_PDSFULL + b), C::kComputeWarps);
+      mbar_init(BAR(C::BAR_MMA2 + b), 1);  // (the second unused with one dS^T tile)
+    }
     mbar_init(BAR(C::BAR_DQFREE), C::kComputeWarps);
     mbar_init(BAR(C::BAR_ACCFREE), C::kComputeWarps);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
@@ -592,7 +621,6 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           ++k;
         }
       } else {
-        const uint64_t dDS_mn = sdesc_sw128(sbase + C::kOffDS, BN * 128, 1024);
         while (ok) {
           if (!(ok = mbar_wait(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
           const Bwd2Item it = *ring(k & 3);
@@ -610,12 +638,16 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           // ACCFREE(k - 1)).
           if (k >= 1 && !(ok = mbar_wait(BAR(C::BAR_ACCFREE), (k - 1) & 1, ab))) break;
           for (int i = 0; i < it.ntiles && ok; ++i) {
-            // dV, dK, dQ of tile gg once its P^T / dS^T are in place.
+            // dV, dK, dQ of tile gg once its P^T / dS^T are in place: P^T in
+            // TMEM buffer gg % 2 (the A operand of dV += P^T dO), dS^T in
+            // shared tile gg % kDSBufs, as a K-major A operand (dK += dS^T Q)
+            // and an MN-major B operand (dQ^T = K^T dS^T).
             const int gg = g + i;
             const uint32_t st_off = (gg % STAGES) * C::kQBytes;
-            if (!(ok = mbar_wait(BAR(C::BAR_PDSFULL), gg & 1, ab))) break;
+            if (!(ok = mbar_wait(BAR(C::BAR_PDSFULL + (gg & 1)), (gg >> 1) & 1, ab))) break;
             tc_fence_after();
-            const uint32_t pds = tmem + C::kTmemPDS;
+            const uint32_t ds_base = sbase + C::kOffDS + (gg % C::kDSBufs) * C::kDSBytes;
+            const uint64_t dDS_mn = sdesc_sw128(ds_base, BN * 128, 1024);
             if constexpr (C::kChunkRing) {
               // dV, dK of the item's head-dim half, 64 dims (one chunk of dO
               // and of Q, in its ring slot) at a time; each slot is released
@@ -630,24 +662,25 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
                 const uint64_t o_mn = sdesc_sw128(slot_base + BMQ * 128, BMQ * 128, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BMQ / 16; ++kk) {
-                  const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+                  // queries [16kk, 16kk+16): chunk kk/2, P^T first 16 columns, dS^T last 16
+                  const uint32_t col = tmem + C::kTmemP + 32 * (kk >> 1) + 8 * (kk & 1);
                   const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                  mma_ts(tmem + C::kTmemDV + 64 * j, pds + col, adv(o_mn, kk * 16 * 128), kIdKV64,
+                  mma_ts(tmem + C::kTmemDV + 64 * j, col, adv(o_mn, kk * 16 * 128), kIdKV64, acc);
+                  mma_ts(tmem + C::kTmemDK + 64 * j, col + 16, adv(q_mn, kk * 16 * 128), kIdKV64,
                          acc);
-                  mma_ts(tmem + C::kTmemDK + 64 * j, pds + col + 16, adv(q_mn, kk * 16 * 128),
-                         kIdKV64, acc);
                 }
                 mma_commit(BAR(C::BAR_QEMPTY + slot));
               }
             } else {
+              const uint32_t pcol = tmem + C::kTmemP + 32 * (gg & 1);
+              const uint64_t dDS_k = sdesc_sw128(ds_base, 16, 1024);
 #pragma unroll
               for (int kk = 0; kk < BMQ / 16; ++kk) {
-                // queries [16kk, 16kk+16): chunk kk/2, P^T first 16 columns, dS^T last 16
-                const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+                // queries [16kk, 16kk+16): 8 columns of P^T, 32 bytes of each dS^T row
                 const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                mma_ts(tmem + C::kTmemDV, pds + col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV,
+                mma_ts(tmem + C::kTmemDV, pcol + 8 * kk, adv(dO_mn, st_off + kk * 16 * 128), kIdKV,
                        acc);
-                mma_ts(tmem + C::kTmemDK, pds + col + 16, adv(dQ_mn, st_off + kk * 16 * 128),
+                mma_ss(tmem + C::kTmemDK, adv(dDS_k, kk * 32), adv(dQ_mn, st_off + kk * 16 * 128),
                        kIdKV, acc);
               }
               // dQ^T reads no Q / dO: the stage is free once dV / dK are done.
@@ -660,7 +693,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
             for (int kk = 0; kk < BN / 16; ++kk)
               mma_ss(tmem + C::kTmemDQ, adv(dK_mn, kk * 16 * 128), adv(dDS_mn, kk * 16 * 128),
                      kIdDQ, kk > 0 ? 1u : 0u);
-            mma_commit(BAR(C::BAR_MMA2));
+            mma_commit(BAR(C::BAR_MMA2 + gg % C::kDSBufs));
           }
           if (!ok) break;
           mma_commit(BAR(C::BAR_ITEMDONE + k % C::KVBUF));
@@ -771,9 +804,14 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
       const Bwd2Item it = *ring(k & 3);
       if (it.v < 0) break;
-      if constexpr (VARLEN && C::kTmaDQ && !DET) {
-        // this launch's dq map of the item's sample, as memory holds it
-        if (lane == 0) tensormap_acquire(&p.vl_maps[it.slot].dq);
+      if constexpr (VARLEN && C::kTmaDQ) {
+        // this launch's dq, dk, dv maps of the item's sample, as memory
+        // holds them
+        if (lane == 0) {
+          if constexpr (!DET) tensormap_acquire(&p.vl_maps[it.slot].dq);
+          tensormap_acquire(&p.vl_maps[it.slot].dk);
+          tensormap_acquire(&p.vl_maps[it.slot].dv);
+        }
       }
       const int ks = it.wi.tile * BN;
       const int j = ks + row;  // key inside its half
@@ -850,30 +888,45 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           wp[e] = pack_bf16x2(p0, p1);
           wd[e] = pack_bf16x2(d0, d1);
         }
-        // PdS (TMEM) and the dS^T shared tile still feed the previous tile's
-        // products until they complete.
-        if (gg >= 1 && !(ok = mbar_wait_warp(BAR(C::BAR_MMA2), (gg - 1) & 1, ab))) break;
+        // P^T buffer gg % 2 and dS^T tile gg % kDSBufs still feed the
+        // products of tile gg - kDSBufs (headdim 128: the tile before the
+        // previous one) until they complete.
+        if (gg >= C::kDSBufs &&
+            !(ok = mbar_wait_warp(BAR(C::BAR_MMA2 + (gg % C::kDSBufs)),
+                                  ((gg / C::kDSBufs) - 1) & 1, ab)))
+          break;
         tc_fence_after();
-        // PdS chunk c0 / 32 holds P^T of its 32 queries in its first 16
-        // columns and dS^T in the last 16; this warpgroup's HC / 2 words of
-        // each start at word (c0 % 32) / 2.
-        const uint32_t pds_col = C::kTmemPDS + 32 * (c0 / 32) + (c0 % 32) / 2;
-        tmem_st_cols<HC / 2>(t_lane + pds_col, wp);
-        tmem_st_cols<HC / 2>(t_lane + pds_col + 16, wd);
+        if constexpr (C::kChunkRing) {
+          // chunk c0 / 32: P^T in its first 16 columns, dS^T in the last 16;
+          // this warpgroup's HC / 2 words of each start at word (c0 % 32) / 2
+          const uint32_t pds_col = C::kTmemP + 32 * (c0 / 32) + (c0 % 32) / 2;
+          tmem_st_cols<HC / 2>(t_lane + pds_col, wp);
+          tmem_st_cols<HC / 2>(t_lane + pds_col + 16, wd);
+        } else {
+          // this warpgroup's HC queries: HC / 2 words of P^T from column c0 / 2
+          tmem_st_cols<HC / 2>(t_lane + C::kTmemP + 32 * (gg & 1) + c0 / 2, wp);
+        }
         // dS^T row `row` of the shared tile: 16-byte units c0 / 8 onwards.
+        const uint32_t ds_s = sbase + C::kOffDS + (gg % C::kDSBufs) * C::kDSBytes;
 #pragma unroll
         for (int u4 = 0; u4 < HC / 8; ++u4) {
           const int u = c0 / 8 + u4;
           const uint32_t off = row * 128 + ((u ^ (row & 7)) << 4);
-          st_shared_v4(sbase + C::kOffDS + off, wd[4 * u4], wd[4 * u4 + 1], wd[4 * u4 + 2],
-                       wd[4 * u4 + 3]);
+          st_shared_v4(ds_s + off, wd[4 * u4], wd[4 * u4 + 1], wd[4 * u4 + 2], wd[4 * u4 + 3]);
         }
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive_warp(BAR(C::BAR_PDSFULL));
-        // The previous tile's products are complete (waited above): its dQ.
-        if (i >= 1 && !(ok = drain_tile(i - 1))) break;
+        mbar_arrive_warp(BAR(C::BAR_PDSFULL + (gg & 1)));
+        // The previous tile's dQ, once its products are complete (with one
+        // dS^T tile that was waited for above).
+        if (i >= 1) {
+          if (C::kDSBufs == 2 &&
+              !(ok = mbar_wait_warp(BAR(C::BAR_MMA2 + ((gg - 1) & 1)), ((gg - 1) >> 1) & 1, ab)))
+            break;
+          tc_fence_after();
+          if (!(ok = drain_tile(i - 1))) break;
+        }
       }
       if (!ok) break;
 
@@ -906,16 +959,36 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
                                   : static_cast<size_t>(it.wi.b) * 2 * static_cast<size_t>(p.n);
       if constexpr (C::kTmaDQ) {
         // The warp's 32 key rows (dK needs no scale: it is already in dS),
-        // through the warp's dQ staging tile (once its last reduce has read
-        // it), so that the stores coalesce: a row of the item's 128 dims is
-        // 256 bytes, 8 KB or so from the next.
-        const int j0 = ks + (warp & 3) * 32;  // the warp's first key
-        const size_t row0 = first + static_cast<size_t>(it.wi.half) * n + j0;
-        __nv_bfloat16* dst0 = (is_v ? p.dv : p.dk) + (row0 * p.Hk + it.wi.h) * D + it.dh * DH + d0;
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-        store_rows_staged<DW, 128>(o, dst0, static_cast<size_t>(p.Hk) * D, n - j0,
-                                   sbase + C::kOffDQS + warp * C::kDQSBytes, lane);
+        // 64 head dims at a time through the warp's staging tile (once the
+        // copy before has read it), in the 128-byte-swizzled layout of a TMA
+        // box, and out with a bulk tensor store: rows past the half are
+        // dropped by the copy, and the warp does not wait for the stores.
+        static_assert(DW % 64 == 0, "whole 64-dim boxes");
+        const uint32_t stg = sbase + C::kOffDQS + warp * C::kDQSBytes;
+        const CUtensorMap* mkv = VARLEN ? (is_v ? &p.vl_maps[it.slot].dv : &p.vl_maps[it.slot].dk)
+                                        : (is_v ? &p.tm_dv : &p.tm_dk);
+        const HalfRows kr = in_rows<VARLEN>(it.wi.b, it.wi.half);
+#pragma unroll
+        for (int rd = 0; rd < DW / 64; ++rd) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int e0 = 64 * rd + 8 * u;
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(o[e0 + 2 * e]), __uint_as_float(o[e0 + 2 * e + 1]));
+            st_shared_v4(stg + lane * 128 + ((u ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_5d(mkv, stg, it.dh * DH + d0 + 64 * rd, it.wi.h,
+                         kr.base + ks + (warp & 3) * 32, kr.c3, kr.c4);
+            bulk_commit_group();
+          }
+        }
       } else if (j < n) {
         // headdim 256 (no staging tile left): each thread its own row
         const size_t pos = static_cast<size_t>(it.wi.half) * n + j;

@@ -34,7 +34,7 @@ struct VarlenSlot {
 // The forward uses q, k, v; the backward q, k, v, dout and (headdim 128)
 // dq, the float32 accumulator.
 struct VarlenMaps {  // CUtensorMap carries its own (128-byte) alignment
-  CUtensorMap q, k, v, dout, dq;
+  CUtensorMap q, k, v, dout, dq, dk, dv;
 };
 
 // Forward kernel parameters.  Batched: tensor maps view q/k/v as 5-D arrays
@@ -79,6 +79,8 @@ struct BwdParams {
   CUtensorMap tm_k;   // box (64, 1, block_n, 1, 1)
   CUtensorMap tm_v;   // box (64, 1, block_n, 1, 1)
   CUtensorMap tm_dq;  // float32 dq_acc, box (32, 1, query columns per warpgroup, 1, 1); headdim 128
+  CUtensorMap tm_dk;  // dk, box (64, 1, 32, 1, 1): one warp's key rows; headdim 128
+  CUtensorMap tm_dv;  // dv, the same
   const float* lse;   // (B, H, 2n)
   const float* delta; // (B, H, 2n): rowsum(dout * out)
   float* dq_acc;      // (B, 2n, H, d) fp32, zeroed before the kernel

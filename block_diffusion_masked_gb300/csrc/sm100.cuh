@@ -594,50 +594,6 @@ struct ZeroShare {
   }
 };
 
-// A warp's 32 consecutive rows (lane i holds row i: kDims float32 values in
-// o) stored as bf16 into rows dst0 + i * stride (elements), rows i >= nrows
-// skipped, through the warp's shared staging tile `stg` of 32 x kRowBytes
-// bytes: each round stages kRowBytes / 2 elements of every row, then each
-// store instruction writes whole kRowBytes-byte segments of 32 * 16 /
-// kRowBytes rows, instead of 16 bytes of each of 32 rows 8 KB or so apart.
-// The units of a staged row are permuted (XOR with a function of the row)
-// so that both the row-per-lane writes and the unit-per-lane reads spread
-// over all banks.  The tile must be free on entry; it is free on return.
-template <int kDims, int kRowBytes>
-__device__ __forceinline__ void store_rows_staged(const uint32_t* o, __nv_bfloat16* dst0,
-                                                  size_t stride, int nrows, uint32_t stg,
-                                                  int lane) {
-  constexpr int kUnits = kRowBytes / 16;  // 16-byte units of a staged row: 4 or 8
-  constexpr int kRounds = kDims * 2 / kRowBytes;
-  constexpr int kRowsPerInst = 32 / kUnits;
-  static_assert(kUnits == 4 || kUnits == 8, "staged row of 64 or 128 bytes");
-  static_assert(kDims * 2 % kRowBytes == 0, "whole rounds");
-#pragma unroll
-  for (int rd = 0; rd < kRounds; ++rd) {
-#pragma unroll
-    for (int u = 0; u < kUnits; ++u) {
-      const int e0 = rd * (kRowBytes / 2) + 8 * u;
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        w[e] = pack_bf16x2(__uint_as_float(o[e0 + 2 * e]), __uint_as_float(o[e0 + 2 * e + 1]));
-      const int sw = kUnits == 8 ? (lane & 7) : ((lane >> 1) & 3);
-      st_shared_v4(stg + lane * kRowBytes + ((u ^ sw) << 4), w[0], w[1], w[2], w[3]);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < kUnits; ++i) {
-      const int r = i * kRowsPerInst + lane / kUnits;
-      const int u = lane % kUnits;
-      const int sw = kUnits == 8 ? (r & 7) : ((r >> 1) & 3);
-      uint32_t a, b, c, d;
-      ld_shared_v4(stg + r * kRowBytes + ((u ^ sw) << 4), a, b, c, d);
-      if (r < nrows) st_global_v4(dst0 + r * stride + rd * (kRowBytes / 2) + 8 * u, a, b, c, d);
-    }
-    __syncwarp();
-  }
-}
-
 __device__ __forceinline__ void red_add_f32(float* ptr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(ptr), "f"(v) : "memory");
 }

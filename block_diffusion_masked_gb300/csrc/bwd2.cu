@@ -957,7 +957,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       mbar_arrive_warp(BAR(C::BAR_ACCFREE));
       const size_t first = VARLEN ? static_cast<size_t>(it.row0)
                                   : static_cast<size_t>(it.wi.b) * 2 * static_cast<size_t>(p.n);
-      if constexpr (C::kTmaDQ) {
+      if constexpr (C::kTmaDQ && C::kDQSBytes >= 4096) {
         // The warp's 32 key rows (dK needs no scale: it is already in dS),
         // 64 head dims at a time through the warp's staging tile (once the
         // copy before has read it), in the 128-byte-swizzled layout of a TMA
@@ -990,7 +990,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           }
         }
       } else if (j < n) {
-        // headdim 256 (no staging tile left): each thread its own row
+        // headdim 256 (no staging tile left) or a staging tile too small for
+        // a box: each thread its own row
         const size_t pos = static_cast<size_t>(it.wi.half) * n + j;
         const size_t off = ((first + pos) * p.Hk + it.wi.h) * D + it.dh * DH + d0;
         __nv_bfloat16* dst = (is_v ? p.dv : p.dk) + off;

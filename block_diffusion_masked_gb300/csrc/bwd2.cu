@@ -52,6 +52,8 @@
 // warpgroups (setmaxnreg) within the pool the launch provides.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "geometry.cuh"
 #include "params.cuh"
 #include "sm100.cuh"
@@ -861,33 +863,48 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           keep = below_hi & ~below_lo;
         }
         // P^T and dS^T in packed pairs: x = s * sl2 - lse2, p = 2^x,
-        // ds = p * (dp - D) * scale.  A hidden pair's p is cleared by AND with its
-        // column's mask bit spread to a word, so every tile runs the same
-        // straight-line code.
+        // ds = p * (dp - D) * scale.  On a tile the mask cuts, a hidden
+        // pair's p is cleared by AND with its column's mask bit spread to a
+        // word; -LSE and -D of four columns come in one shared load.
         uint32_t wp[HC / 2], wd[HC / 2];
+        auto pds = [&](auto masked) {
 #pragma unroll
-        for (int e = 0; e < HC / 2; ++e) {
-          const float2 nl = ld_shared_v2_f32(nlse_s + 8 * e);
-          const float2 nd = ld_shared_v2_f32(ndel_s + 8 * e);
-          const uint64_t x = f2_fma(
-              f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), scale2,
-              f2_pack(nl.x, nl.y));
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          const float p0 =
-              __uint_as_float(__float_as_uint(ex2_approx(x0)) & bit_spread(keep, 2 * e));
-          const float p1 =
-              __uint_as_float(__float_as_uint(ex2_approx(x1)) & bit_spread(keep, 2 * e + 1));
-          // (dP - D) * scale: dS carries the softmax scale, so dQ and dK
-          // need no scaling afterwards
-          const uint64_t dd = f2_fma(
-              f2_pack(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1])), dscale2,
-              f2_pack(nd.x, nd.y));
-          float d0, d1;
-          f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
-          wp[e] = pack_bf16x2(p0, p1);
-          wd[e] = pack_bf16x2(d0, d1);
-        }
+          for (int e4 = 0; e4 < HC / 4; ++e4) {
+            uint32_t la, lb, lc, ld, da, db, dc, dd4;
+            ld_shared_v4(nlse_s + 16 * e4, la, lb, lc, ld);
+            ld_shared_v4(ndel_s + 16 * e4, da, db, dc, dd4);
+            const uint32_t nl[4] = {la, lb, lc, ld};
+            const uint32_t nd[4] = {da, db, dc, dd4};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 2 * e4 + h;
+              const uint64_t x = f2_fma(
+                  f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), scale2,
+                  f2_pack(__uint_as_float(nl[2 * h]), __uint_as_float(nl[2 * h + 1])));
+              float x0, x1;
+              f2_unpack(x, x0, x1);
+              float p0 = ex2_approx(x0);
+              float p1 = ex2_approx(x1);
+              if constexpr (decltype(masked)::value) {
+                p0 = __uint_as_float(__float_as_uint(p0) & bit_spread(keep, 2 * e));
+                p1 = __uint_as_float(__float_as_uint(p1) & bit_spread(keep, 2 * e + 1));
+              }
+              // (dP - D) * scale: dS carries the softmax scale, so dQ and dK
+              // need no scaling afterwards
+              const uint64_t dd = f2_fma(
+                  f2_pack(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1])), dscale2,
+                  f2_pack(__uint_as_float(nd[2 * h]), __uint_as_float(nd[2 * h + 1])));
+              float d0, d1;
+              f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
+              wp[e] = pack_bf16x2(p0, p1);
+              wd[e] = pack_bf16x2(d0, d1);
+            }
+          }
+        };
+        if (__all_sync(0xffffffffu, keep == 0xffffffffu))
+          pds(std::false_type{});
+        else
+          pds(std::true_type{});
         // P^T buffer gg % 2 and dS^T tile gg % kDSBufs still feed the
         // products of tile gg - kDSBufs (headdim 128: the tile before the
         // previous one) until they complete.

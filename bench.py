@@ -126,7 +126,6 @@ KERNEL_SOURCES = {
     "dfa_fwd_kernel": "fwd.cu",
     "dfa_bwd2_kernel": "bwd2.cu",
     "dfa_bwd_kernel": "bwd.cu",
-    "dfa_bwd_diag_kernel": "diag.cu",
 }
 
 

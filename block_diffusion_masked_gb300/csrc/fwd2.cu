@@ -29,8 +29,8 @@
 // The K/V ring, the query double buffer and all barrier phases run on across
 // items, so the loads and S products of the next item overlap the read-out
 // and stores of the current one.
-// Warps 0-7 softmax; warp 8 takes the items and loads Q, K and V; warp 10
-// issues S = Q K^T and warp 9 O += P V; warp 11 stores the out tiles (staged
+// The softmax warps first; then one warp takes the items and loads Q, K and
+// V, one issues O += P V and one S = Q K^T, and one stores the out tiles (staged
 // by the softmax warpgroups in the item's query buffer) with TMA and zeroes
 // the backward's float32 dq accumulator when the caller asks for it.
 // The load/MMA warpgroup hands registers to the softmax warpgroups
@@ -51,10 +51,30 @@ namespace dfa {
 // query buffer, which keeps the bf16 tile's size.
 // STAGES K tiles and VSTAGES V tiles in flight (a K tile is needed first,
 // by S, a V tile a softmax later, by P V).
-template <int D, int STAGES, int VSTAGES, bool FP8 = false>
+// NSW softmax warpgroups, each on kCols = 128 / NSW key columns of every
+// tile and kDCols = D / NSW head dims of O.  Two: four warpgroups of 32
+// columns measured slower (their extra exchange partners and the smaller
+// share of work per warp cost more than the halved per-warp chains gain).
+template <int D, int STAGES, int VSTAGES, bool FP8 = false, int NSW = 2>
 struct Fwd2Cfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
+  static constexpr int kCols = BN / NSW;
+  static constexpr int kDCols = D / NSW;
+  static constexpr int kSoftWarps = 4 * NSW;
+  static constexpr int kWarpLoad = kSoftWarps;       // items, Q / K / V loads
+  static constexpr int kWarpPV = kSoftWarps + 1;     // O += P V; owns TMEM
+  static constexpr int kWarpS = kSoftWarps + 2;      // S = Q K^T
+  static constexpr int kWarpStore = kSoftWarps + 3;  // out stores, dq zeroing
+  static constexpr int kThreads = 32 * (kSoftWarps + 4);
+  // setmaxnreg split within the launch's pool: the load / MMA / store warps
+  // drop to kRegCtl, the softmax warps rise to kRegSoft.
+  static constexpr int kRegLaunch = NSW == 2 ? 168 : 96;
+  static constexpr int kRegCtl = 56;
+  static constexpr int kRegSoft = NSW == 2 ? 224 : 104;
+  static_assert(kRegCtl * 128 + kRegSoft * 128 * NSW <= kRegLaunch * kThreads,
+                "register split exceeds the launch pool");
+  static_assert(kCols % 32 == 0 && kDCols % 16 == 0, "column split");
   static constexpr int ES = FP8 ? 1 : 2;           // bytes per q / k / v element
   static constexpr int kChunkElems = 128 / ES;     // elements per 128-byte row
   static constexpr int kChunks = D / kChunkElems;  // 128-byte chunks of q, k, v rows
@@ -69,9 +89,9 @@ struct Fwd2Cfg {
   static constexpr int kOffV = kOffK + STAGES * kKVBytes;  // [VSTAGES]
   // TMEM buffers of S (tiles in flight between the S product and P V)
   static constexpr int kSBufs = 3;
-  // exchange slots of the two softmax warpgroups: [round % 2][warpgroup][row]
+  // exchange slots of the softmax warpgroups: [round % 2][warpgroup][row]
   static constexpr int kOffX = kOffV + VSTAGES * kKVBytes;
-  static constexpr int kOffBar = kOffX + 2 * 2 * BM * 4;
+  static constexpr int kOffBar = kOffX + 2 * NSW * BM * 4;
   enum {
     BAR_QFULL = 0,                    // [2]
     BAR_QEMPTY = BAR_QFULL + 2,       // [2]
@@ -101,7 +121,6 @@ struct Fwd2Cfg {
   static constexpr int kTmemO = kSBufs * BN;
   static constexpr int kOBufs = kSBufs * BN + 2 * D <= 512 ? 2 : 1;
   static constexpr int kTmemCols = 512;
-  static constexpr int kThreads = 384;
   static constexpr float kRescaleThreshold = 8.0f;  // log2 units
   static_assert(kTmemO + kOBufs * D <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -156,9 +175,10 @@ __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, 
   g->qs = g->wi.tile * bm;
 }
 
-template <int D, int STAGES, int VSTAGES, bool VARLEN, bool FP8 = false>
-__global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant__ FwdParams p) {
-  using C = Fwd2Cfg<D, STAGES, VSTAGES, FP8>;
+template <int D, int STAGES, int VSTAGES, bool VARLEN, bool FP8 = false, int NSW = 2>
+__global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThreads, 1)
+    dfa_fwd2_kernel(const __grid_constant__ FwdParams p) {
+  using C = Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>;
   constexpr int BM = C::BM;
   constexpr int BN = C::BN;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -175,7 +195,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
-  // Slot s of the item ring; written by warp 8 before it arrives on
+  // Slot s of the item ring; written by the load warp before it arrives on
   // ITEMFULL[s] (release), read by the other roles after their wait (acquire).
   auto ring = [&](int s) { return reinterpret_cast<ItemGeom*>(smem + C::kOffItem + 128 * s); };
   const AbortFlag ab{abort_flag, p.status};
@@ -186,12 +206,12 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(C::BAR_QFULL + b), 1);
       mbar_init(BAR(C::BAR_QEMPTY + b), 1);
-      mbar_init(BAR(C::BAR_OFREE + b), 8);
-      mbar_init(BAR(C::BAR_OSTAGED + b), 8);
+      mbar_init(BAR(C::BAR_OFREE + b), C::kSoftWarps);
+      mbar_init(BAR(C::BAR_OSTAGED + b), C::kSoftWarps);
     }
     for (int b = 0; b < C::kSBufs; ++b) {
       mbar_init(BAR(C::BAR_SFULL + b), 1);
-      mbar_init(BAR(C::BAR_PFULL + b), 8);
+      mbar_init(BAR(C::BAR_PFULL + b), C::kSoftWarps);
       mbar_init(BAR(C::BAR_SFREE + b), 1);
     }
     for (int s = 0; s < STAGES; ++s) {
@@ -202,13 +222,13 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       mbar_init(BAR(C::BAR_VFULL + s), 1);
       mbar_init(BAR(C::BAR_VEMPTY + s), 1);
     }
-    mbar_init(BAR(C::BAR_XCHG), 8);
+    mbar_init(BAR(C::BAR_XCHG), C::kSoftWarps);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
     mbar_init(BAR(C::BAR_ALL), 2);  // both MMA-issuing warps
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == C::kWarpPV) {
     tmem_alloc(sbase + C::kOffTmemSlot, C::kTmemCols);
     tmem_relinquish();
   }
@@ -223,9 +243,9 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   grid_dependency_wait();
   grid_launch_dependents();
 
-  if (warp >= 8) {
-   asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
-   if (warp == 8) {
+  if (warp >= C::kSoftWarps) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegCtl));
+   if (warp == C::kWarpLoad) {
     // ------------------------------------------------------------ producer
     // Takes items, publishes them and loads Q and the K and V rings.  The V
     // load of a tile is issued after the K load of the next one, so that a K
@@ -263,7 +283,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         // Items come from the work counter and are published, decoded, to the
         // other roles through slot k % 4 of the item ring.  The slot last held
         // item k - 4, whose readers are all done: for item k - 1's query
-        // buffer this loader has already waited until warp 11 stored item
+        // buffer this loader has already waited until the store warp stored item
         // k - 3's out tile, which exists only after every role has read item
         // k - 4's slot.
         ItemGeom ig;
@@ -323,9 +343,9 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       }
     }
     __syncwarp();
-   } else if (warp == 9 || warp == 10) {
+   } else if (warp == C::kWarpPV || warp == C::kWarpS) {
     // ------------------------------------------------------------ MMA issuers
-    // Warp 10 issues S = Q K^T, warp 9 O += P V.  Issued from one warp, the
+    // One warp issues S = Q K^T, another O += P V.  Issued from one warp, the
     // products slow down while the softmax warps that share its scheduler are
     // busy; from two warps on two schedulers they keep the tensor pipe fed.
     // The two streams meet only through barriers: S of tile g goes into
@@ -334,7 +354,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     // and the first P V of an item for the read-out of the O buffer it reuses
     // (OFREE).
     if (lane == 0) {
-      const bool s_warp = warp == 10;
+      const bool s_warp = warp == C::kWarpS;
       constexpr uint32_t kIdS =
           FP8 ? idesc_e4m3(BM, BN, false, false) : idesc_bf16(BM, BN, false, false);
       constexpr uint32_t kIdPV =
@@ -394,9 +414,9 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
               // warpgroup that owns them, 8 columns per step (bf16 pairs or
               // e4m3 quadruples); V: 16 key rows of 128 bytes, or (V^T) 32
               // bytes of 128-key rows
-              constexpr int kStepsPerHalf = kPVSteps / 2;
+              constexpr int kStepsPerWG = C::kCols / C::kPVKeys;
               const uint32_t pcol =
-                  C::kTmemS + sb * BN + 64 * (kk / kStepsPerHalf) + 8 * (kk % kStepsPerHalf);
+                  C::kTmemS + sb * BN + C::kCols * (kk / kStepsPerWG) + 8 * (kk % kStepsPerWG);
               const uint64_t b =
                   adv(dV, vs * C::kKVBytes + (FP8 ? kk * 32 : kk * C::kPVKeys * 128));
               const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
@@ -479,25 +499,34 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
     __syncwarp();
    }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegSoft));
     // ------------------------------------------------------------ softmax
-    // Warpgroup w, thread `row`: key columns [64 w, 64 w + 64) of every tile
-    // of the item for query row `row` of the tile.
+    // Warpgroup w, thread `row`: key columns [kCols w, kCols (w + 1)) of
+    // every tile of the item for query row `row` of the tile.
+    constexpr int KC = C::kCols;
+    constexpr int DC = C::kDCols;
     const int w = warp >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const float sl2 = p.scale_log2;
     float* const xslots = reinterpret_cast<float*>(smem + C::kOffX);
-    int xc = 0;  // exchange rounds so far (the same sequence in both warpgroups)
+    int xc = 0;  // exchange rounds so far (the same sequence in every warpgroup)
     // One exchange round: this thread's value for its row goes to the other
-    // warpgroup (post), whose value for the same row comes back (collect).
+    // warpgroups (post); the maximum or the sum of all warpgroups' values for
+    // the same row comes back (collect).
     auto exchange_post = [&](float mine) {
-      xslots[(xc & 1) * 2 * BM + w * BM + row] = mine;
+      xslots[(xc & 1) * NSW * BM + w * BM + row] = mine;
       mbar_arrive_warp(BAR(C::BAR_XCHG));
     };
-    auto exchange_collect = [&](float* theirs) -> bool {
+    auto exchange_collect = [&](float mine, bool sum, float* all) -> bool {
       if (!mbar_wait_warp(BAR(C::BAR_XCHG), xc & 1, ab)) return false;
-      *theirs = xslots[(xc & 1) * 2 * BM + (1 - w) * BM + row];
+      float a = mine;
+#pragma unroll
+      for (int o = 1; o < NSW; ++o) {
+        const float t = xslots[(xc & 1) * NSW * BM + ((w + o) % NSW) * BM + row];
+        a = sum ? a + t : fmaxf(a, t);
+      }
+      *all = a;
       ++xc;
       return true;
     };
@@ -517,7 +546,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       const int bs = VARLEN ? imin(p.bs, n) : p.bs;
       const Interval kv0 = key_interval(ig.rule0, r, n, bs);
       const Interval kv1 = key_interval(ig.rule1, r, n, bs);
-      const uint32_t o_col = t_lane + C::kTmemO + ob * D + w * (D / 2);
+      const uint32_t o_col = t_lane + C::kTmemO + ob * D + w * DC;
       float m_ref = -INFINITY;  // reference maximum, scaled log2 units
       float l_run = 0.f;        // running sum of 2^(s * sl2 - m_ref) over this half's keys
       for (int j = 0; j < ig.ntiles; ++j) {
@@ -525,27 +554,27 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         const int sb = gg % C::kSBufs;
         const int seg = j < ig.n0 ? 0 : 1;
         const int kt = ig.ktile(j);
-        const uint32_t s_col = t_lane + C::kTmemS + sb * BN + 64 * w;
+        const uint32_t s_col = t_lane + C::kTmemS + sb * BN + KC * w;
         if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + sb), (gg / C::kSBufs) & 1, ab))) break;
         tc_fence_after();
-        const int ks = kt * BN + 64 * w;
+        const int ks = kt * BN + KC * w;
         const Interval iv = seg ? kv1 : kv0;
         const int clo = iv.lo - ks, chi = iv.hi - ks;
         // The warp masks element by element only if one of its rows needs it.
-        const bool full = __all_sync(0xffffffffu, clo <= 0 && chi >= 64);
-        // This half's score row in registers; hidden keys -> -inf, so they
-        // drop out of the maximum and get probability 0.
-        uint32_t sr[64];
-        tmem_ld32(s_col, sr);
-        tmem_ld32(s_col + 32, sr + 32);
+        const bool full = __all_sync(0xffffffffu, clo <= 0 && chi >= KC);
+        // This warpgroup's part of the score row in registers; hidden keys ->
+        // -inf, so they drop out of the maximum and get probability 0.
+        uint32_t sr[KC];
+#pragma unroll
+        for (int c = 0; c < KC / 32; ++c) tmem_ld32(s_col + 32 * c, sr + 32 * c);
         tmem_wait_ld();
-        tmem_pin<64>(sr);
+        tmem_pin<KC>(sr);
         if (!full) {
-          // Keys [clo, chi) of the half are visible to row r: a 32-bit mask
+          // Keys [clo, chi) of the part are visible to row r: a 32-bit mask
           // per 32 columns, hidden scores set to -inf with one AND / OR each,
           // in straight-line code.
 #pragma unroll
-          for (int c32 = 0; c32 < 2; ++c32) {
+          for (int c32 = 0; c32 < KC / 32; ++c32) {
             const int lo = clo - 32 * c32 < 0 ? 0 : (clo - 32 * c32 > 32 ? 32 : clo - 32 * c32);
             const int hi = chi - 32 * c32 < lo ? lo : (chi - 32 * c32 > 32 ? 32 : chi - 32 * c32);
             const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
@@ -558,13 +587,14 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
             }
           }
         }
-        // The row's tile maximum from both halves: both warpgroups then take
-        // the same decision on the common reference maximum.
-        const float mh = max_tree<64>(sr);
-        float mo;
+        // The row's tile maximum over all warpgroups' parts: every
+        // warpgroup then takes the same decision on the common reference
+        // maximum.
+        const float mh = max_tree<KC>(sr);
+        float mall;
         exchange_post(mh);
-        if (!(ok = exchange_collect(&mo))) break;
-        const float m_tile = fmaxf(mh, mo) * sl2;
+        if (!(ok = exchange_collect(mh, false, &mall))) break;
+        const float m_tile = mall * sl2;
         const bool move = m_tile > m_ref + C::kRescaleThreshold;
         float corr = 1.f;
         if (move) {
@@ -573,22 +603,23 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
           m_ref = m_tile;
         }
         // O holds the item's products of tiles 0 .. j - 1; once the last of
-        // them has completed, this warpgroup rescales its half of the head
-        // dims (the other warpgroup, deciding alike, takes the other half).
+        // them has completed, this warpgroup rescales its DC head dims (the
+        // others, deciding alike, take theirs).
         if (j >= 1 && __any_sync(0xffffffffu, move)) {
           const int gp = gg - 1;
           if (!(ok = mbar_wait_warp(BAR(C::BAR_SFREE + gp % C::kSBufs), (gp / C::kSBufs) & 1, ab)))
             break;
           tc_fence_after();
+          constexpr int OW = DC < 32 ? DC : 32;  // columns per TMEM access
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            uint32_t o[32];
-            tmem_ld32(o_col + 32 * c, o);
+          for (int c = 0; c < DC / OW; ++c) {
+            uint32_t o[OW];
+            tmem_ld_cols<OW>(o_col + OW * c, o);
             tmem_wait_ld();
-            tmem_pin<32>(o);
+            tmem_pin<OW>(o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-            tmem_st32(o_col + 32 * c, o);
+            for (int e = 0; e < OW; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st_cols<OW>(o_col + OW * c, o);
           }
         }
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
@@ -601,7 +632,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
         const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < KC / 32; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -638,7 +669,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
       // Once the item's last P V has completed: the row sum of both halves,
       // then this warpgroup's half of the head dims of O, normalised, as
       // bf16 into the item's query buffer (its last S product has completed)
-      // in the 128-byte-swizzled layout of a TMA box, for warp 11 to store;
+      // in the 128-byte-swizzled layout of a TMA box, for the store warp;
       // rows past the end of the half are dropped by the copy.
       if (ig.ntiles > 0) {
         const int gl = g + ig.ntiles - 1;
@@ -646,22 +677,22 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
           break;
       }
       tc_fence_after();
-      float l_other;
+      float lsum;
       exchange_post(l_run);
-      if (!(ok = exchange_collect(&l_other))) break;
-      const float lsum = l_run + l_other;
+      if (!(ok = exchange_collect(l_run, true, &lsum))) break;
       // FP8: out = (P V8) * v_descale / l
       const float inv = lsum > 0.f ? (FP8 ? p.out_scale : 1.f) / lsum : 0.f;
       const uint32_t stage = sbase + C::kOffQ + qb * C::kQBytes;
+      constexpr int RW = DC < 32 ? DC : 32;  // columns per TMEM read
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = w * (D / 2) + 32 * c;
-        uint32_t oa[32];
-        tmem_ld32(o_col + 32 * c, oa);
+      for (int c = 0; c < DC / RW; ++c) {
+        const int col = w * DC + RW * c;
+        uint32_t oa[RW];
+        tmem_ld_cols<RW>(o_col + RW * c, oa);
         tmem_wait_ld();
-        tmem_pin<32>(oa);
+        tmem_pin<RW>(oa);
 #pragma unroll
-        for (int gq = 0; gq < 4; ++gq) {
+        for (int gq = 0; gq < RW / 8; ++gq) {
           uint32_t wv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -694,7 +725,7 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::kWarpPV) {
     if (lane == 0) mbar_wait_limited(sbase + C::kOffBar + 8 * C::BAR_ALL, 0, 1000000000ull);
     __syncwarp();
     tc_fence_after();
@@ -703,13 +734,19 @@ __global__ void __launch_bounds__(384, 1) dfa_fwd2_kernel(const __grid_constant_
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int STAGES, int VSTAGES, bool VARLEN, bool FP8 = false>
+template <int D, int STAGES, int VSTAGES, bool VARLEN, bool FP8 = false, int NSW = 2>
 static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
-  using C = Fwd2Cfg<D, STAGES, VSTAGES, FP8>;
-  auto kern = dfa_fwd2_kernel<D, STAGES, VSTAGES, VARLEN, FP8>;
+  using C = Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>;
+  auto kern = dfa_fwd2_kernel<D, STAGES, VSTAGES, VARLEN, FP8, NSW>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  // The setmaxnreg split must fit the registers the kernel is launched with,
+  // or the softmax warps' increase would never be granted: refuse to launch.
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+  if (fa.numRegs * C::kThreads < C::kRegCtl * 128 + C::kRegSoft * 128 * NSW)
+    return cudaErrorInvalidConfiguration;
   const long long items = VARLEN ? p.items : pass_items(p.mode, p.B, p.H, p.q_tiles);
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

@@ -325,11 +325,16 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
                : "memory");
 }
 
-// N (8 or 16) consecutive 32-bit columns of the thread's own lane.
+// N (8, 16 or 32) consecutive 32-bit columns of the thread's own lane.
 template <int N>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
-  static_assert(N == 8 || N == 16, "tmem_st_cols: 8 or 16 columns");
-  if constexpr (N == 16) tmem_st16(taddr, r); else tmem_st8(taddr, r);
+  static_assert(N == 8 || N == 16 || N == 32, "tmem_st_cols: 8, 16 or 32 columns");
+  if constexpr (N == 32)
+    tmem_st32(taddr, r);
+  else if constexpr (N == 16)
+    tmem_st16(taddr, r);
+  else
+    tmem_st8(taddr, r);
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

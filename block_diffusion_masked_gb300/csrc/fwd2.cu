@@ -9,18 +9,21 @@
 // Attention Without Materialization", section 5.1, with the online softmax of
 // section 4.2.
 //
-// Two softmax warpgroups share every key tile of the item: warpgroup w takes
-// the tile's key columns [64 w, 64 w + 64) of every row.  The row's
-// reference maximum is common to both (one exchange of half-row maxima
-// through shared memory per tile), so the probabilities of the two halves
-// feed a single output accumulator O in TMEM and nothing is merged at the
-// end of an item.  Scores S = Q K^T land in one of three TMEM buffers, so the
+// Eight softmax warps share every key tile of the item, each on 16 of its
+// 128 rows: TMEM is read and written in the 16-lane shape, which gives
+// thread t of the warp row t % 16 of the warp's 16 and key columns
+// [64 (t / 16), 64 (t / 16) + 64) of it, so the two halves of a row sit in
+// threads t and t ^ 16 of one warp and their maxima and sums meet in one
+// shuffle.  Every row's reference maximum is thus common to both halves,
+// the probabilities of the whole tile feed a single output accumulator O in
+// TMEM and nothing is merged at the end of an item.  Scores S = Q K^T land
+// in one of three TMEM buffers, so the
 // scores of the next two tiles are computed while the softmax of this one
 // runs (a tile's products and softmax form a chain of about three times the
 // tensor-core time of a tile, most of it latency);
-// each warpgroup writes its probabilities as bf16 back into the first half
-// of its own columns of the buffer, where O += P V reads them as the MMA's A
-// operand.  A row's reference maximum is only moved (O and the sum
+// the probabilities of each half row go as bf16 back into the first half of
+// that half's columns of the buffer, where O += P V reads them as the MMA's
+// A operand.  A row's reference maximum is only moved (O and the sum
 // rescaled) when a tile maximum exceeds it by more than 2^8: exact in real
 // arithmetic, and probabilities stay below 256.  With headdim 64 O is also
 // double-buffered by item, so the next item's first products need not wait
@@ -33,10 +36,9 @@
 // V, one issues O += P V and one S = Q K^T, and one stores the out tiles (staged
 // by the softmax warpgroups in the item's query buffer) with TMA and zeroes
 // the backward's float32 dq accumulator when the caller asks for it.
-// The load/MMA warpgroup hands registers to the softmax warpgroups
-// (setmaxnreg): launched with 168 per thread, it drops to 56 and the softmax
-// warpgroups rise to 224.  256 * (224 - 168) == 128 * (168 - 56): the pool
-// balances.
+// The load/MMA warpgroup hands registers to the softmax warps (setmaxnreg):
+// launched with 168 per thread, it drops to 56 and the softmax warps rise to
+// 224.  256 * (224 - 168) == 128 * (168 - 56): the pool balances.
 #include <cuda_bf16.h>
 
 #include "geometry.cuh"
@@ -51,17 +53,15 @@ namespace dfa {
 // query buffer, which keeps the bf16 tile's size.
 // STAGES K tiles and VSTAGES V tiles in flight (a K tile is needed first,
 // by S, a V tile a softmax later, by P V).
-// NSW softmax warpgroups, each on kCols = 128 / NSW key columns of every
-// tile and kDCols = D / NSW head dims of O.  Two: four warpgroups of 32
-// columns measured slower (their extra exchange partners and the smaller
-// share of work per warp cost more than the halved per-warp chains gain).
-template <int D, int STAGES, int VSTAGES, bool FP8 = false, int NSW = 2>
+// Eight softmax warps, each thread on kCols = 64 key columns of a row of
+// every tile and kDCols = D / 2 head dims of its row of O.
+template <int D, int STAGES, int VSTAGES, bool FP8 = false>
 struct Fwd2Cfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
-  static constexpr int kCols = BN / NSW;
-  static constexpr int kDCols = D / NSW;
-  static constexpr int kSoftWarps = 4 * NSW;
+  static constexpr int kCols = BN / 2;
+  static constexpr int kDCols = D / 2;
+  static constexpr int kSoftWarps = 8;
   static constexpr int kWarpLoad = kSoftWarps;       // items, Q / K / V loads
   static constexpr int kWarpPV = kSoftWarps + 1;     // O += P V; owns TMEM
   static constexpr int kWarpS = kSoftWarps + 2;      // S = Q K^T
@@ -69,10 +69,10 @@ struct Fwd2Cfg {
   static constexpr int kThreads = 32 * (kSoftWarps + 4);
   // setmaxnreg split within the launch's pool: the load / MMA / store warps
   // drop to kRegCtl, the softmax warps rise to kRegSoft.
-  static constexpr int kRegLaunch = NSW == 2 ? 168 : 96;
+  static constexpr int kRegLaunch = 168;
   static constexpr int kRegCtl = 56;
-  static constexpr int kRegSoft = NSW == 2 ? 224 : 104;
-  static_assert(kRegCtl * 128 + kRegSoft * 128 * NSW <= kRegLaunch * kThreads,
+  static constexpr int kRegSoft = 224;
+  static_assert(kRegCtl * 128 + kRegSoft * 32 * kSoftWarps <= kRegLaunch * kThreads,
                 "register split exceeds the launch pool");
   static_assert(kCols % 32 == 0 && kDCols % 16 == 0, "column split");
   static constexpr int ES = FP8 ? 1 : 2;           // bytes per q / k / v element
@@ -89,9 +89,7 @@ struct Fwd2Cfg {
   static constexpr int kOffV = kOffK + STAGES * kKVBytes;  // [VSTAGES]
   // TMEM buffers of S (tiles in flight between the S product and P V)
   static constexpr int kSBufs = 3;
-  // exchange slots of the softmax warpgroups: [round % 2][warpgroup][row]
-  static constexpr int kOffX = kOffV + VSTAGES * kKVBytes;
-  static constexpr int kOffBar = kOffX + 2 * NSW * BM * 4;
+  static constexpr int kOffBar = kOffV + VSTAGES * kKVBytes;
   enum {
     BAR_QFULL = 0,                    // [2]
     BAR_QEMPTY = BAR_QFULL + 2,       // [2]
@@ -103,8 +101,7 @@ struct Fwd2Cfg {
     BAR_PFULL = BAR_SFULL + kSBufs,     // [kSBufs] per S buffer: P of its tile written (8 warps)
     BAR_SFREE = BAR_PFULL + kSBufs,     // [kSBufs] per S buffer: P V of its tile complete
     BAR_OFREE = BAR_SFREE + kSBufs,     // [2] per O buffer: read out (8 warps)
-    BAR_XCHG = BAR_OFREE + 2,         // one exchange round of the softmax warps (8 warps)
-    BAR_ITEMFULL = BAR_XCHG + 1,      // [4] item published
+    BAR_ITEMFULL = BAR_OFREE + 2,     // [4] item published
     BAR_OSTAGED = BAR_ITEMFULL + 4,   // [2] per query buffer: the item's out tile staged in it
     BAR_ALL = BAR_OSTAGED + 2,        // every MMA of the CTA complete
     NUM_BARS = BAR_ALL + 1
@@ -115,8 +112,9 @@ struct Fwd2Cfg {
   // The dynamic shared memory starts 1024-byte aligned (the kernel checks
   // this, for the 128-byte swizzle of the TMA boxes and MMA operands).
   static constexpr int kSmemBytes = kOffAbort + 4;
-  // S[b] at b * BN (tile g in buffer g % kSBufs); warpgroup w's P in
-  // columns [64 w, 64 w + 32) of it.  O[item % kOBufs] after the S buffers.
+  // S[b] at b * BN (tile g in buffer g % kSBufs); P of key columns
+  // [64 h, 64 h + 64) in its columns [64 h, 64 h + 32).  O[item % kOBufs]
+  // after the S buffers.
   static constexpr int kTmemS = 0;
   static constexpr int kTmemO = kSBufs * BN;
   static constexpr int kOBufs = kSBufs * BN + 2 * D <= 512 ? 2 : 1;
@@ -175,10 +173,10 @@ __device__ __forceinline__ void item_geom(const FwdParams& p, int item, int bm, 
   g->qs = g->wi.tile * bm;
 }
 
-template <int D, int STAGES, int VSTAGES, bool VARLEN, bool FP8 = false, int NSW = 2>
-__global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThreads, 1)
+template <int D, int STAGES, int VSTAGES, bool VARLEN, bool FP8 = false>
+__global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8>::kThreads, 1)
     dfa_fwd2_kernel(const __grid_constant__ FwdParams p) {
-  using C = Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>;
+  using C = Fwd2Cfg<D, STAGES, VSTAGES, FP8>;
   constexpr int BM = C::BM;
   constexpr int BN = C::BN;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -222,7 +220,6 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
       mbar_init(BAR(C::BAR_VFULL + s), 1);
       mbar_init(BAR(C::BAR_VEMPTY + s), 1);
     }
-    mbar_init(BAR(C::BAR_XCHG), C::kSoftWarps);
     for (int s = 0; s < 4; ++s) mbar_init(BAR(C::BAR_ITEMFULL + s), 1);
     mbar_init(BAR(C::BAR_ALL), 2);  // both MMA-issuing warps
     *abort_flag = 0;
@@ -501,35 +498,17 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegSoft));
     // ------------------------------------------------------------ softmax
-    // Warpgroup w, thread `row`: key columns [kCols w, kCols (w + 1)) of
-    // every tile of the item for query row `row` of the tile.
+    // Warp `warp`: rows [lb, lb + 16) of every tile of the item, lb = 32
+    // (warp % 4) + 16 (warp / 4), the TMEM lanes of the half of its quarter;
+    // thread t: row lb + t % 16, key columns [kCols h, kCols (h + 1)) of each
+    // tile and head dims [kDCols h, kDCols (h + 1)) of O, h = t / 16.
     constexpr int KC = C::kCols;
     constexpr int DC = C::kDCols;
-    const int w = warp >> 2;
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const int w = lane >> 4;  // column half of the thread's row
+    const int lb = (warp & 3) * 32 + (warp >> 2) * 16;
+    const int row = lb + (lane & 15);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(lb) << 16);
     const float sl2 = p.scale_log2;
-    float* const xslots = reinterpret_cast<float*>(smem + C::kOffX);
-    int xc = 0;  // exchange rounds so far (the same sequence in every warpgroup)
-    // One exchange round: this thread's value for its row goes to the other
-    // warpgroups (post); the maximum or the sum of all warpgroups' values for
-    // the same row comes back (collect).
-    auto exchange_post = [&](float mine) {
-      xslots[(xc & 1) * NSW * BM + w * BM + row] = mine;
-      mbar_arrive_warp(BAR(C::BAR_XCHG));
-    };
-    auto exchange_collect = [&](float mine, bool sum, float* all) -> bool {
-      if (!mbar_wait_warp(BAR(C::BAR_XCHG), xc & 1, ab)) return false;
-      float a = mine;
-#pragma unroll
-      for (int o = 1; o < NSW; ++o) {
-        const float t = xslots[(xc & 1) * NSW * BM + ((w + o) % NSW) * BM + row];
-        a = sum ? a + t : fmaxf(a, t);
-      }
-      *all = a;
-      ++xc;
-      return true;
-    };
     bool ok = true;
     int g = 0;  // tiles of earlier items
     for (int k = 0; ok; ++k) {
@@ -546,7 +525,7 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
       const int bs = VARLEN ? imin(p.bs, n) : p.bs;
       const Interval kv0 = key_interval(ig.rule0, r, n, bs);
       const Interval kv1 = key_interval(ig.rule1, r, n, bs);
-      const uint32_t o_col = t_lane + C::kTmemO + ob * D + w * DC;
+      const uint32_t o_col = t_lane + C::kTmemO + ob * D;  // + DC w, through the split
       float m_ref = -INFINITY;  // reference maximum, scaled log2 units
       float l_run = 0.f;        // running sum of 2^(s * sl2 - m_ref) over this half's keys
       for (int j = 0; j < ig.ntiles; ++j) {
@@ -554,7 +533,7 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
         const int sb = gg % C::kSBufs;
         const int seg = j < ig.n0 ? 0 : 1;
         const int kt = ig.ktile(j);
-        const uint32_t s_col = t_lane + C::kTmemS + sb * BN + KC * w;
+        const uint32_t s_col = t_lane + C::kTmemS + sb * BN;  // + KC w, through the split
         if (!(ok = mbar_wait_warp(BAR(C::BAR_SFULL + sb), (gg / C::kSBufs) & 1, ab))) break;
         tc_fence_after();
         const int ks = kt * BN + KC * w;
@@ -562,11 +541,11 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
         const int clo = iv.lo - ks, chi = iv.hi - ks;
         // The warp masks element by element only if one of its rows needs it.
         const bool full = __all_sync(0xffffffffu, clo <= 0 && chi >= KC);
-        // This warpgroup's part of the score row in registers; hidden keys ->
+        // The thread's half of the score row in registers; hidden keys ->
         // -inf, so they drop out of the maximum and get probability 0.
         uint32_t sr[KC];
 #pragma unroll
-        for (int c = 0; c < KC / 32; ++c) tmem_ld32(s_col + 32 * c, sr + 32 * c);
+        for (int c = 0; c < KC / 32; ++c) tmem_ld_half<32, KC>(s_col + 32 * c, sr + 32 * c);
         tmem_wait_ld();
         tmem_pin<KC>(sr);
         if (!full) {
@@ -587,13 +566,10 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
             }
           }
         }
-        // The row's tile maximum over all warpgroups' parts: every
-        // warpgroup then takes the same decision on the common reference
-        // maximum.
+        // The row's tile maximum over both halves: the two threads of the
+        // row then take the same decision on the common reference maximum.
         const float mh = max_tree<KC>(sr);
-        float mall;
-        exchange_post(mh);
-        if (!(ok = exchange_collect(mh, false, &mall))) break;
+        const float mall = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 16));
         const float m_tile = mall * sl2;
         const bool move = m_tile > m_ref + C::kRescaleThreshold;
         float corr = 1.f;
@@ -603,8 +579,8 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
           m_ref = m_tile;
         }
         // O holds the item's products of tiles 0 .. j - 1; once the last of
-        // them has completed, this warpgroup rescales its DC head dims (the
-        // others, deciding alike, take theirs).
+        // them has completed, each thread rescales its DC head dims of the
+        // row (the row's other thread, deciding alike, takes the others).
         if (j >= 1 && __any_sync(0xffffffffu, move)) {
           const int gp = gg - 1;
           if (!(ok = mbar_wait_warp(BAR(C::BAR_SFREE + gp % C::kSBufs), (gp / C::kSBufs) & 1, ab)))
@@ -614,20 +590,20 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
 #pragma unroll
           for (int c = 0; c < DC / OW; ++c) {
             uint32_t o[OW];
-            tmem_ld_cols<OW>(o_col + OW * c, o);
+            tmem_ld_half<OW, DC>(o_col + OW * c, o);
             tmem_wait_ld();
             tmem_pin<OW>(o);
 #pragma unroll
             for (int e = 0; e < OW; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-            tmem_st_cols<OW>(o_col + OW * c, o);
+            tmem_st_half<OW, DC>(o_col + OW * c, o);
           }
         }
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         // Probabilities 2^(s * sl2 - m_use), two lanes per instruction for
         // the scaling and the sums (four independent pair accumulators),
         // written back as bf16 pairs (e4m3 quadruples) into the first half of
-        // this warpgroup's columns -- the scores there are already in
-        // registers.
+        // the columns of the thread's half row -- the scores there are
+        // already in registers.
         const uint64_t scale2 = f2_pack(sl2, sl2);
         const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -652,9 +628,9 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
             }
           }
           if constexpr (FP8)
-            tmem_st8(s_col + 8 * c, pk);
+            tmem_st_half<8, KC>(s_col + 8 * c, pk);
           else
-            tmem_st16(s_col + 16 * c, pk);
+            tmem_st_half<16, KC>(s_col + 16 * c, pk);
         }
         float a0, a1, b0, b1;
         f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
@@ -667,19 +643,17 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
       if (!ok) break;
       // ---------------------------------------------------------- read-out
       // Once the item's last P V has completed: the row sum of both halves,
-      // then this warpgroup's half of the head dims of O, normalised, as
-      // bf16 into the item's query buffer (its last S product has completed)
-      // in the 128-byte-swizzled layout of a TMA box, for the store warp;
-      // rows past the end of the half are dropped by the copy.
+      // then the thread's half of the head dims of its row of O, normalised,
+      // as bf16 into the item's query buffer (its last S product has
+      // completed) in the 128-byte-swizzled layout of a TMA box, for the
+      // store warp; rows past the end of the half are dropped by the copy.
       if (ig.ntiles > 0) {
         const int gl = g + ig.ntiles - 1;
         if (!(ok = mbar_wait_warp(BAR(C::BAR_SFREE + gl % C::kSBufs), (gl / C::kSBufs) & 1, ab)))
           break;
       }
       tc_fence_after();
-      float lsum;
-      exchange_post(l_run);
-      if (!(ok = exchange_collect(l_run, true, &lsum))) break;
+      const float lsum = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
       // FP8: out = (P V8) * v_descale / l
       const float inv = lsum > 0.f ? (FP8 ? p.out_scale : 1.f) / lsum : 0.f;
       const uint32_t stage = sbase + C::kOffQ + qb * C::kQBytes;
@@ -688,7 +662,7 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
       for (int c = 0; c < DC / RW; ++c) {
         const int col = w * DC + RW * c;
         uint32_t oa[RW];
-        tmem_ld_cols<RW>(o_col + RW * c, oa);
+        tmem_ld_half<RW, DC>(o_col + RW * c, oa);
         tmem_wait_ld();
         tmem_pin<RW>(oa);
 #pragma unroll
@@ -734,10 +708,10 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>::kThread
   if (threadIdx.x == 0) sched_finish(p.sched);
 }
 
-template <int D, int STAGES, int VSTAGES, bool VARLEN, bool FP8 = false, int NSW = 2>
+template <int D, int STAGES, int VSTAGES, bool VARLEN, bool FP8 = false>
 static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
-  using C = Fwd2Cfg<D, STAGES, VSTAGES, FP8, NSW>;
-  auto kern = dfa_fwd2_kernel<D, STAGES, VSTAGES, VARLEN, FP8, NSW>;
+  using C = Fwd2Cfg<D, STAGES, VSTAGES, FP8>;
+  auto kern = dfa_fwd2_kernel<D, STAGES, VSTAGES, VARLEN, FP8>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -745,7 +719,7 @@ static cudaError_t launch_fwd2_impl(const FwdParams& p, cudaStream_t stream) {
   // or the softmax warps' increase would never be granted: refuse to launch.
   cudaFuncAttributes fa;
   if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-  if (fa.numRegs * C::kThreads < C::kRegCtl * 128 + C::kRegSoft * 128 * NSW)
+  if (fa.numRegs * C::kThreads < C::kRegCtl * 128 + C::kRegSoft * 32 * C::kSoftWarps)
     return cudaErrorInvalidConfiguration;
   const long long items = VARLEN ? p.items : pass_items(p.mode, p.B, p.H, p.q_tiles);
   if (items <= 0) return cudaSuccess;

@@ -43,6 +43,8 @@
 // slice of S^T and dP^T is read from TMEM in one batch.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "geometry.cuh"
 #include "params.cuh"
 #include "sm100.cuh"
@@ -555,11 +557,13 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     // TMEM loads), bf16 P^T / dS^T back into the dP columns of each 32-query
     // chunk (P^T in its first 16 columns, dS^T in its last 16), dS^T also into
     // the swizzled shared tile.  Pairs of columns go through packed f32x2
-    // arithmetic: x = s * sl2 - lse2, p = 2^x, ds = p * (dp - D) * scale; a hidden
+    // arithmetic: x = s * sl2 - lse2, p = 2^x, ds = p * (dp - D) * scale; -LSE
+    // and -D of four columns come in one shared load.  `masked`: a hidden
     // pair's p is cleared by AND with its column's mask bit (keep_lo /
-    // keep_hi: columns 0-31 / 32-63 of the slice).
+    // keep_hi: columns 0-31 / 32-63 of the slice); a slice the mask does not
+    // cut skips that.
     auto slice = [&](int h, uint32_t s_col, uint32_t ds_s, uint32_t nlse_s, uint32_t ndel_s,
-                     uint32_t keep_lo, uint32_t keep_hi) {
+                     uint32_t keep_lo, uint32_t keep_hi, auto masked) {
       uint32_t sr[64], dpr[64];
       tmem_ld32(s_col + 64 * h, sr);
       tmem_ld32(s_col + 64 * h + 32, sr + 32);
@@ -575,28 +579,38 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         const uint32_t keep = cc ? keep_hi : keep_lo;
         uint32_t wp[16], wd[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int cl = 32 * cc + 2 * e;  // column inside the slice
-          const float2 nl = ld_shared_v2_f32(nlse_s + 4 * (cbase + 2 * e));
-          const float2 nd = ld_shared_v2_f32(ndel_s + 4 * (cbase + 2 * e));
-          const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[cl]), __uint_as_float(sr[cl + 1])),
-                                    scale2, f2_pack(nl.x, nl.y));
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          const float p0 =
-              __uint_as_float(__float_as_uint(ex2_approx(x0)) & bit_spread(keep, 2 * e));
-          const float p1 =
-              __uint_as_float(__float_as_uint(ex2_approx(x1)) & bit_spread(keep, 2 * e + 1));
-          const uint64_t pp = f2_pack(p0, p1);
-          // (dP - D) * scale: dS carries the softmax scale, so dQ and dK
-          // need no scaling afterwards
-          const uint64_t dd =
-              f2_fma(f2_pack(__uint_as_float(dpr[cl]), __uint_as_float(dpr[cl + 1])), dscale2,
-                     f2_pack(nd.x, nd.y));
-          float d0, d1;
-          f2_unpack(f2_mul(pp, dd), d0, d1);
-          wp[e] = pack_bf16x2(p0, p1);
-          wd[e] = pack_bf16x2(d0, d1);
+        for (int e4 = 0; e4 < 8; ++e4) {
+          uint32_t la, lb, lc, ld, da, db, dc, dd4;
+          ld_shared_v4(nlse_s + 4 * (cbase + 4 * e4), la, lb, lc, ld);
+          ld_shared_v4(ndel_s + 4 * (cbase + 4 * e4), da, db, dc, dd4);
+          const uint32_t nl[4] = {la, lb, lc, ld};
+          const uint32_t nd[4] = {da, db, dc, dd4};
+#pragma unroll
+          for (int hp = 0; hp < 2; ++hp) {
+            const int e = 2 * e4 + hp;       // pair inside the chunk
+            const int cl = 32 * cc + 2 * e;  // column inside the slice
+            const uint64_t x =
+                f2_fma(f2_pack(__uint_as_float(sr[cl]), __uint_as_float(sr[cl + 1])), scale2,
+                       f2_pack(__uint_as_float(nl[2 * hp]), __uint_as_float(nl[2 * hp + 1])));
+            float x0, x1;
+            f2_unpack(x, x0, x1);
+            float p0 = ex2_approx(x0);
+            float p1 = ex2_approx(x1);
+            if constexpr (decltype(masked)::value) {
+              p0 = __uint_as_float(__float_as_uint(p0) & bit_spread(keep, 2 * e));
+              p1 = __uint_as_float(__float_as_uint(p1) & bit_spread(keep, 2 * e + 1));
+            }
+            const uint64_t pp = f2_pack(p0, p1);
+            // (dP - D) * scale: dS carries the softmax scale, so dQ and dK
+            // need no scaling afterwards
+            const uint64_t dd =
+                f2_fma(f2_pack(__uint_as_float(dpr[cl]), __uint_as_float(dpr[cl + 1])), dscale2,
+                       f2_pack(__uint_as_float(nd[2 * hp]), __uint_as_float(nd[2 * hp + 1])));
+            float d0, d1;
+            f2_unpack(f2_mul(pp, dd), d0, d1);
+            wp[e] = pack_bf16x2(p0, p1);
+            wd[e] = pack_bf16x2(d0, d1);
+          }
         }
         const int chunk = 2 * h + cc;
         tmem_st16(t_lane + C::kTmemDP + 32 * chunk, wp);
@@ -654,10 +668,11 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         }
         const uint32_t s_col = t_lane + C::kTmemS + b * BMQ;
         const uint32_t ds_s = sbase + C::kOffDS + b * C::kDSBytes;
-        if (wg == 0)
-          slice(0, s_col, ds_s, nlse_s, ndel_s, keep[0], keep[1]);
+        const uint32_t klo = keep[2 * wg], khi = keep[2 * wg + 1];
+        if (__all_sync(0xffffffffu, (klo & khi) == 0xffffffffu))
+          slice(wg, s_col, ds_s, nlse_s, ndel_s, klo, khi, std::false_type{});
         else
-          slice(1, s_col, ds_s, nlse_s, ndel_s, keep[2], keep[3]);
+          slice(wg, s_col, ds_s, nlse_s, ndel_s, klo, khi, std::true_type{});
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();

@@ -220,7 +220,7 @@ int make_map_vt(CUtensorMap* map, const void* base, int B, int n, int n_pad, int
 // backward's bulk reduce-add of one warp's part of a query tile's dQ (rows
 // past the end of a half are skipped by the copy engine).
 int make_map_f32(CUtensorMap* map, const void* base, long long halves, int n, int H, int d,
-                 int rows, bool packed = false) {
+                 int rows, bool packed = false, bool swizzle = false) {
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(n),
                               packed ? 1u : static_cast<cuuint64_t>(halves), 1u};
@@ -231,8 +231,8 @@ int make_map_f32(CUtensorMap* map, const void* base, long long halves, int n, in
   const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DFA_OK : DFA_ECUDA;
 }
 
@@ -389,8 +389,13 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   if ((rc = make_map(&p.tm_do, dout, halves, n, H, d, ts.bwd_bm))) return rc;
   if ((rc = make_map(&p.tm_k, k, halves, n, Hk, d, ts.bwd_bn))) return rc;
   if ((rc = make_map(&p.tm_v, v, halves, n, Hk, d, ts.bwd_bn))) return rc;
+  // dq accumulator boxes of the bulk reduce-adds: 32 head dims x the rows of
+  // one warp (headdim 128: a warpgroup's queries of a tile; 64: a warp's 32
+  // query rows, 128-byte swizzled)
   if (d == 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, halves, n, H, d,
                                       ts.bwd_bm / kBwd2WarpgroupsD128)))
+    return rc;
+  if (d == 64 && (rc = make_map_f32(&p.tm_dq, dq_acc, halves, n, H, d, 32, false, true)))
     return rc;
   if (d == 128 && ((rc = make_map(&p.tm_dk, dk, halves, n, Hk, d, 32)) ||
                    (rc = make_map(&p.tm_dv, dv, halves, n, Hk, d, 32))))
@@ -600,7 +605,7 @@ int varlen_schedule(const int* cu, int batch, int heads, int tile, long long byt
 int varlen_maps(const std::vector<VarlenSlot>& slots, const void* q, const void* k,
                 const void* v, const void* dout, int H, int Hk, int d, int bm, int bn,
                 std::vector<VarlenMaps>* maps, const float* dq_acc = nullptr, int dq_rows = 0,
-                const void* dk = nullptr, const void* dv = nullptr) {
+                const void* dk = nullptr, const void* dv = nullptr, bool dq_swizzle = false) {
   maps->assign(slots.size(), VarlenMaps{});
   const size_t qrow = static_cast<size_t>(H) * d * 2, krow = static_cast<size_t>(Hk) * d * 2;
   for (size_t i = 0; i < slots.size(); ++i) {
@@ -618,7 +623,7 @@ int varlen_maps(const std::vector<VarlenSlot>& slots, const void* q, const void*
                        bm)))
       return rc;
     if (dq_acc && (rc = make_map_f32(&m.dq, dq_acc + static_cast<size_t>(sl.row0) * H * d, 2,
-                                     sl.n, H, d, dq_rows)))
+                                     sl.n, H, d, dq_rows, false, dq_swizzle)))
       return rc;
     if (dk && (rc = make_map(&m.dk, static_cast<const char*>(dk) + sl.row0 * krow, 2, sl.n, Hk,
                              d, 32)))
@@ -752,13 +757,14 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
     cudaFreeAsync(dq_acc, stream);
     return DFA_ECUDA;
   }
-  // q, dout, k, v, the dq accumulator and (headdim 128) dk, dv through
+  // q, dout, k, v, the dq accumulator (headdim 64, 128) and (128) dk, dv through
   // per-sample maps (rows past a half read zero; reduce-adds and stores past
   // a half are skipped)
   std::vector<VarlenMaps> maps;
   if ((rc = varlen_maps(slots, q, k, v, dout, H, Hk, d, ts.bwd_bm, ts.bwd_bn, &maps,
-                        d == 128 ? dq_acc : nullptr, ts.bwd_bm / kBwd2WarpgroupsD128,
-                        d == 128 ? dk : nullptr, d == 128 ? dv : nullptr)) ||
+                        d == 128 || d == 64 ? dq_acc : nullptr,
+                        d == 64 ? 32 : ts.bwd_bm / kBwd2WarpgroupsD128,
+                        d == 128 ? dk : nullptr, d == 128 ? dv : nullptr, d == 64)) ||
       (rc = upload_slots(slots, maps, stream, &dmaps, &dslots))) {
     cudaFreeAsync(delta, stream);
     cudaFreeAsync(dq_acc, stream);

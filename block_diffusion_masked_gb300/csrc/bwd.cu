@@ -19,8 +19,10 @@
 //        written back as bf16 into the columns of dP, dS^T also to shared
 //   dV  += P^T dO,  dK += dS^T Q    (A operand read from TMEM)
 //   dQ   = dS K                     -> TMEM S[b] (S is consumed by then),
-//        then added to a float32 accumulator in device memory, one query
-//        row per thread with 16-byte atomics.
+//        then added to a float32 accumulator in device memory: each warp
+//        stages its 32 query rows x 32 head dims in shared memory and adds
+//        them with one bulk tensor reduce (deterministic mode: one query row
+//        per thread with 16-byte atomics, in order).
 // Persistent: one CTA per SM takes items from a work counter until none are
 // left (the same order and counter as the other kernels); the barrier phases
 // run on across items, the next item's first query tiles load while the
@@ -505,10 +507,18 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
     const uint64_t dscale2 = f2_pack(p.scale, p.scale);
 
     // dQ of global tile gg (TMEM S[gg % 2], lane = query `row` of the tile,
-    // columns = head dims), added to dq_acc with 16-byte atomics; warpgroup
-    // wg adds head dims [32 wg, 32 wg + 32) of every query row.
+    // columns = head dims); warpgroup wg adds head dims [32 wg, 32 wg + 32)
+    // of every query row.  The warp stages its 32 rows x 32 dims (float32,
+    // 128-byte swizzled) in its own quarter of the tile's dS^T buffer --
+    // the part it writes itself, free once the tile's dQ product, its only
+    // reader, has completed -- and one lane adds the box into the
+    // accumulator with a bulk tensor reduce; before the warp writes that
+    // buffer again (two tiles later) it waits until the copy has read it.
+    // Deterministic mode: 16-byte atomics in the counters' order.
     auto drain_dq = [&](const BwdItem& it, int gg, int t) -> bool {
       constexpr int DW = D / 2;  // head dims per warpgroup
+      constexpr int kStageBytes = 32 * DW * 4;  // a warp's 32 rows x DW dims, float32
+      static_assert(8 * kStageBytes <= C::kDSBytes, "staging inside one dS^T buffer");
       const int b = gg & 1;
       if (!mbar_wait_warp(BAR(C::BAR_MMA2 + b), (gg >> 1) & 1, ab)) return false;
       tc_fence_after();
@@ -534,6 +544,29 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
               static_cast<size_t>(it.lhalf(l)) * n + qs;
         // the 8 compute warps of every earlier contribution have signalled
         if (!sem_wait_warp(sem, static_cast<unsigned>(8 * ord), ab)) return false;
+      }
+      if constexpr (!DET) {
+        const uint32_t stg = sbase + C::kOffDS + b * C::kDSBytes + warp * kStageBytes;
+#pragma unroll
+        for (int c = 0; c < DW / 4; ++c)
+          st_shared_v4(stg + lane * 128 + ((c ^ (lane & 7)) << 4), dq[4 * c], dq[4 * c + 1],
+                       dq[4 * c + 2], dq[4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && qs + (warp & 3) * 32 < n) {
+          // Varlen: through the sample's own map, so that rows of the box
+          // past the half are skipped rather than added to the next sample.
+          const CUtensorMap* mdq = VARLEN ? &p.vl_maps[it.slot].dq : &p.tm_dq;
+          const HalfRows dr = in_rows<VARLEN>(it.wi.b, it.lhalf(l));
+          if (p.pass == 2)  // noisy-diagonal pass: the rows' first contribution
+            tma_store_5d(mdq, stg, DW * wg, it.h0 + hh, dr.base + qs + (warp & 3) * 32, dr.c3,
+                         dr.c4);
+          else
+            tma_reduce_add_5d(mdq, stg, DW * wg, it.h0 + hh, dr.base + qs + (warp & 3) * 32,
+                              dr.c3, dr.c4);
+          bulk_commit_group();
+        }
+        return true;
       }
       if (q < n) {
         const size_t pos = static_cast<size_t>(it.lhalf(l)) * n + q;
@@ -631,6 +664,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       if (!(ok = mbar_wait_warp(BAR(C::BAR_ITEMFULL + (k & 3)), (k >> 2) & 1, ab))) break;
       const BwdItem it = *ring(k & 3);
       if (it.v < 0) break;
+      if constexpr (VARLEN && !DET) {
+        // this launch's dq map of the item's sample, as memory holds it
+        if (lane == 0) tensormap_acquire(&p.vl_maps[it.slot].dq);
+      }
       const int ks = it.wi.tile * BN;
       const int j = ks + row;  // key inside its half
       // Query rows that see key j, per segment of the item: computed once,
@@ -668,6 +705,11 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
         }
         const uint32_t s_col = t_lane + C::kTmemS + b * BMQ;
         const uint32_t ds_s = sbase + C::kOffDS + b * C::kDSBytes;
+        if constexpr (!DET) {
+          // this warp's quarter of buffer b staged the dQ of tile gg - 2
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+        }
         const uint32_t klo = keep[2 * wg], khi = keep[2 * wg + 1];
         if (__all_sync(0xffffffffu, (klo & khi) == 0xffffffffu))
           slice(wg, s_col, ds_s, nlse_s, ndel_s, klo, khi, std::false_type{});
@@ -718,6 +760,10 @@ __global__ void __launch_bounds__(384, 1) dfa_bwd_kernel(const __grid_constant__
       }
       g += it.ntiles;
       ++k;
+    }
+    // The last bulk reduce-adds must be complete before the CTA exits.
+    if constexpr (!DET) {
+      if (lane == 0) bulk_wait_all();
     }
   }
 #undef BAR

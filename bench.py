@@ -125,14 +125,13 @@ KERNEL_SOURCES = {
     "dfa_fwd2_kernel": "fwd2.cu",
     "dfa_fwd_kernel": "fwd.cu",
     "dfa_bwd2_kernel": "bwd2.cu",
-    "dfa_bwd_kernel": "bwd.cu",
 }
 
 
 def kernel_names(d):
     """(forward, backward main) kernel names as the library launches them."""
     fwd = "dfa_fwd_kernel<256>" if d == 256 else f"dfa_fwd2_kernel<{d}>"
-    bwd = "dfa_bwd_kernel<64>" if d == 64 else f"dfa_bwd2_kernel<{d}>"
+    bwd = f"dfa_bwd2_kernel<{d}>"
     return fwd, bwd
 
 

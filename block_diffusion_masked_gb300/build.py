@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdfa.so")
 
-SOURCES = ["fwd.cu", "fwd2.cu", "bwd.cu", "bwd2.cu", "aux.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["fwd.cu", "fwd2.cu", "bwd2.cu", "aux.cu", "api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -220,19 +220,20 @@ int make_map_vt(CUtensorMap* map, const void* base, int B, int n, int n_pad, int
 // backward's bulk reduce-add of one warp's part of a query tile's dQ (rows
 // past the end of a half are skipped by the copy engine).
 int make_map_f32(CUtensorMap* map, const void* base, long long halves, int n, int H, int d,
-                 int rows, bool packed = false, bool swizzle = false) {
+                 int rows, bool packed = false, int inner = 32) {
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(n),
                               packed ? 1u : static_cast<cuuint64_t>(halves), 1u};
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(H) * d * 4;
   const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * 4, row_bytes, row_bytes * n,
                                  row_bytes * n * (packed ? 1 : static_cast<cuuint64_t>(halves))};
-  const cuuint32_t box[5] = {32, 1, static_cast<cuuint32_t>(rows), 1, 1};
+  const cuuint32_t box[5] = {static_cast<cuuint32_t>(inner), 1, static_cast<cuuint32_t>(rows), 1,
+                             1};
   const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DFA_OK : DFA_ECUDA;
 }
 
@@ -389,13 +390,11 @@ int bwd_main_impl(int mode, const void* q, const void* k, const void* v, const v
   if ((rc = make_map(&p.tm_do, dout, halves, n, H, d, ts.bwd_bm))) return rc;
   if ((rc = make_map(&p.tm_k, k, halves, n, Hk, d, ts.bwd_bn))) return rc;
   if ((rc = make_map(&p.tm_v, v, halves, n, Hk, d, ts.bwd_bn))) return rc;
-  // dq accumulator boxes of the bulk reduce-adds: 32 head dims x the rows of
-  // one warp (headdim 128: a warpgroup's queries of a tile; 64: a warp's 32
-  // query rows, 128-byte swizzled)
-  if (d == 128 && (rc = make_map_f32(&p.tm_dq, dq_acc, halves, n, H, d,
-                                      ts.bwd_bm / kBwd2WarpgroupsD128)))
-    return rc;
-  if (d == 64 && (rc = make_map_f32(&p.tm_dq, dq_acc, halves, n, H, d, 32, false, true)))
+  // dq accumulator boxes of the bulk reduce-adds, one per warp: a
+  // warpgroup's queries of a tile x 32 head dims (headdim 128) or 16 (64)
+  if ((d == 128 || d == 64) &&
+      (rc = make_map_f32(&p.tm_dq, dq_acc, halves, n, H, d, ts.bwd_bm / kBwd2WarpgroupsD128,
+                         false, d == 64 ? 16 : 32)))
     return rc;
   if (d == 128 && ((rc = make_map(&p.tm_dk, dk, halves, n, Hk, d, 32)) ||
                    (rc = make_map(&p.tm_dv, dv, halves, n, Hk, d, 32))))
@@ -605,7 +604,7 @@ int varlen_schedule(const int* cu, int batch, int heads, int tile, long long byt
 int varlen_maps(const std::vector<VarlenSlot>& slots, const void* q, const void* k,
                 const void* v, const void* dout, int H, int Hk, int d, int bm, int bn,
                 std::vector<VarlenMaps>* maps, const float* dq_acc = nullptr, int dq_rows = 0,
-                const void* dk = nullptr, const void* dv = nullptr, bool dq_swizzle = false) {
+                const void* dk = nullptr, const void* dv = nullptr, int dq_inner = 32) {
   maps->assign(slots.size(), VarlenMaps{});
   const size_t qrow = static_cast<size_t>(H) * d * 2, krow = static_cast<size_t>(Hk) * d * 2;
   for (size_t i = 0; i < slots.size(); ++i) {
@@ -623,7 +622,7 @@ int varlen_maps(const std::vector<VarlenSlot>& slots, const void* q, const void*
                        bm)))
       return rc;
     if (dq_acc && (rc = make_map_f32(&m.dq, dq_acc + static_cast<size_t>(sl.row0) * H * d, 2,
-                                     sl.n, H, d, dq_rows, false, dq_swizzle)))
+                                     sl.n, H, d, dq_rows, false, dq_inner)))
       return rc;
     if (dk && (rc = make_map(&m.dk, static_cast<const char*>(dk) + sl.row0 * krow, 2, sl.n, Hk,
                              d, 32)))
@@ -763,8 +762,8 @@ int backward_varlen_impl(const void* q, const void* k, const void* v, const void
   std::vector<VarlenMaps> maps;
   if ((rc = varlen_maps(slots, q, k, v, dout, H, Hk, d, ts.bwd_bm, ts.bwd_bn, &maps,
                         d == 128 || d == 64 ? dq_acc : nullptr,
-                        d == 64 ? 32 : ts.bwd_bm / kBwd2WarpgroupsD128,
-                        d == 128 ? dk : nullptr, d == 128 ? dv : nullptr, d == 64)) ||
+                        ts.bwd_bm / kBwd2WarpgroupsD128, d == 128 ? dk : nullptr,
+                        d == 128 ? dv : nullptr, d == 64 ? 16 : 32)) ||
       (rc = upload_slots(slots, maps, stream, &dmaps, &dslots))) {
     cudaFreeAsync(delta, stream);
     cudaFreeAsync(dq_acc, stream);

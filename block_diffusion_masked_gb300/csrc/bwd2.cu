@@ -1,4 +1,5 @@
-// Backward kernel of block-diffusion attention, headdim 128 and 256, on sm_103a.
+// Backward kernel of block-diffusion attention, headdim 64, 128 and 256, on
+// sm_103a.
 //
 // Recompute-based backward of "FlashAttention: Exact Attention Without
 // Materialization", section 4.5.  Key-tile major: a work item is one 128-key
@@ -15,15 +16,16 @@
 //        bf16 P^T -> TMEM (two buffers), dS^T -> a shared-memory tile
 //        (two; headdim 256: one, and dS^T also -> TMEM beside P^T)
 //   dV  += P^T dO  (A operand read from TMEM),
-//   dK  += dS^T Q  (A operand read from the shared dS^T tile; headdim 256:
-//        from TMEM)
+//   dK  += dS^T Q  (A operand read from the shared dS^T tile; headdim 64
+//        and 256: from TMEM)
 //   dQ^T = K^T dS^T  -> TMEM DQ, then added to a float32 accumulator in
 //        device memory (each warp covers 32 consecutive head dims of a query)
 // TMEM (512 columns): S 64 | dP 64 | P 2 x 32 (headdim 256: P / dS 64) |
-// DQ 64 | dK 128 | dV 128.  With two P^T buffers and two dS^T tiles a
-// tile's P^T / dS^T are written while the tile before is still in its
-// products: the compute warpgroups wait only for the products of the tile
-// before that.
+// DQ 64 | dK 128 | dV 128; headdim 64: S 64 | dP 64 | P / dS 2 x 64 |
+// DQ (an M = 64 product: lanes 0-15 of each lane quarter) 64 | dK 64 |
+// dV 64.  With two P^T buffers and two dS^T tiles a tile's P^T / dS^T are
+// written while the tile before is still in its products: the compute
+// warpgroups wait only for the products of the tile before that.
 // With headdim 256 the dK and dV accumulators of all head dims would need
 // every TMEM column, so an item covers one 128-wide half of the head
 // dimension of its key tile: it recomputes S^T and dP^T in full (their
@@ -42,7 +44,7 @@
 // are computed while the warpgroups work.  At the end of an item the first
 // half of the warpgroups writes dV and the second half dK; the next item's
 // first dV / dK products wait until all have been read out of TMEM.
-// With headdim 128 each warp adds its part of dQ into the float32
+// With headdim 64 and 128 each warp adds its part of dQ into the float32
 // accumulator with a bulk tensor reduce from a shared staging tile; with 256
 // (no shared memory left) each thread adds its own with atomics.
 // Warps: 4 per compute warpgroup, then one TMA producer and three MMA
@@ -82,7 +84,7 @@ struct Bwd2Cfg {
   static constexpr int kRegCompute = NWG == 2 ? 184 : 104;
   static_assert(kRegCtl * 128 + kRegCompute * 128 * NWG <= kRegLaunch * kThreads,
                 "register split exceeds the launch pool");
-  static constexpr int DH = 128;       // head dims accumulated per item
+  static constexpr int DH = D < 128 ? D : 128;  // head dims accumulated per item
   static constexpr int NDH = D / DH;   // items per key tile
   static constexpr int BN = 128;  // keys per tile (MMA M)
   static constexpr int BMQ = 64;  // queries per tile
@@ -120,8 +122,11 @@ struct Bwd2Cfg {
   // dims], the source of that warp's bulk reduce-add into the accumulator
   // (headdim 128; with 256 the shared memory is full and dQ goes out with
   // per-thread atomics).
-  static constexpr bool kTmaDQ = D == 128 && KVBUF == 1;
-  static constexpr int kDQSBytes = HC * 32 * 4;
+  // Headdim 64: dQ^T (M = 64 head dims) lies in lanes [32 q, 32 q + 16) of
+  // each lane quarter q, so each warp stages its 16 head dims x HC queries.
+  static constexpr bool kD64 = D == 64;
+  static constexpr bool kTmaDQ = (D == 128 && KVBUF == 1) || kD64;
+  static constexpr int kDQSBytes = HC * (kD64 ? 16 : 32) * 4;
   static constexpr int kOffDQS = kOffDS + kDSBufs * kDSBytes;
   static constexpr int kOffLSE = kOffDQS + (kTmaDQ ? kComputeWarps * kDQSBytes : 0);  // kLseBufs x BMQ floats
   static constexpr int kOffDEL = kOffLSE + kLseBufs * BMQ * 4;  // kLseBufs x BMQ floats
@@ -154,10 +159,13 @@ struct Bwd2Cfg {
   // chunk c holding P^T of queries [32 c, 32 c + 32) in its first 16 columns
   // and dS^T in the last 16 (both A operands read from TMEM: with a single
   // dS^T tile, reading it from shared memory buys no overlap and costs the
-  // ring's shared-memory bandwidth).
+  // ring's shared-memory bandwidth).  Headdim 64: two such buffers, tile g
+  // in kTmemP + 64 (g % 2) (dK += dS^T Q with N = 64 head dims would need
+  // more shared-memory bandwidth than there is with both operands there);
+  // dQ^T (M = 64) then dK and dV of 64 columns each.
   static constexpr int kTmemP = 128;
-  static constexpr int kTmemDQ = 192;
-  static constexpr int kTmemDK = 256;
+  static constexpr int kTmemDQ = kD64 ? 256 : 192;
+  static constexpr int kTmemDK = kD64 ? 320 : 256;
   static constexpr int kTmemDV = 384;
   static constexpr int kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -673,6 +681,19 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
                 }
                 mma_commit(BAR(C::BAR_QEMPTY + slot));
               }
+            } else if constexpr (C::kD64) {
+              // P^T / dS^T of tile gg in TMEM buffer gg % 2: chunk kk / 2,
+              // P^T in its first 16 columns, dS^T in the last 16
+              const uint32_t pbase = tmem + C::kTmemP + 64 * (gg & 1);
+#pragma unroll
+              for (int kk = 0; kk < BMQ / 16; ++kk) {
+                const uint32_t col = pbase + 32 * (kk >> 1) + 8 * (kk & 1);
+                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                mma_ts(tmem + C::kTmemDV, col, adv(dO_mn, st_off + kk * 16 * 128), kIdKV, acc);
+                mma_ts(tmem + C::kTmemDK, col + 16, adv(dQ_mn, st_off + kk * 16 * 128), kIdKV,
+                       acc);
+              }
+              mma_commit(BAR(C::BAR_QEMPTY + (gg % STAGES)));
             } else {
               const uint32_t pcol = tmem + C::kTmemP + 32 * (gg & 1);
               const uint64_t dDS_k = sdesc_sw128(ds_base, 16, 1024);
@@ -724,9 +745,78 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
     const uint64_t scale2 = f2_pack(sl2, sl2);
     const uint64_t dscale2 = f2_pack(p.scale, p.scale);
     const size_t dq_stride = static_cast<size_t>(p.H) * D;
+    // Headdim 64: dQ^T (M = 64) has head dims 16 q .. 16 q + 15 in lanes
+    // 32 q .. 32 q + 15 of lane quarter q = warp % 4, read with the 16-lane
+    // shape: thread t holds head dim 16 q + t % 16 of the warpgroup's queries
+    // c0 + 16 (t / 16) + [0, 16).
+    auto drain_dq64 = [&](const Bwd2Item& it, int h, int qh, int qs) -> bool {
+      constexpr int QC = HC / 2;  // queries per thread
+      uint32_t dq[QC];
+      tmem_ld_half<QC, QC>(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kTmemDQ + c0,
+                           dq);
+      tmem_wait_ld();
+      tmem_pin<QC>(dq);
+      tc_fence_before();
+      mbar_arrive_warp(BAR(C::BAR_DQFREE));
+      const int n = VARLEN ? it.n : p.n;
+      const int up = lane >> 4;
+      if constexpr (!DET) {
+        // The warp's HC queries x 16 head dims (float32, 64-byte rows: the
+        // box of its bulk reduce) in its own staging tile; the upper half of
+        // the warp writes its queries one step later, so that the two halves
+        // of a store fall in different banks.
+        const uint32_t stg = sbase + C::kOffDQS + warp * C::kDQSBytes;
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < QC; ++c) {
+          const int cq = up ? ((c + 1) & (QC - 1)) : c;
+          const uint32_t v = up ? dq[(c + 1) & (QC - 1)] : dq[c];
+          st_shared_f32(stg + (QC * up + cq) * 64 + (lane & 15) * 4, __uint_as_float(v));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && qs + c0 < n) {
+          const CUtensorMap* mdq = VARLEN ? &p.vl_maps[it.slot].dq : &p.tm_dq;
+          const HalfRows dr = in_rows<VARLEN>(it.wi.b, qh);
+          if (p.pass == 2)  // noisy-diagonal pass: the rows' first contribution
+            tma_store_5d(mdq, stg, 16 * (warp & 3), h, dr.base + qs + c0, dr.c3, dr.c4);
+          else
+            tma_reduce_add_5d(mdq, stg, 16 * (warp & 3), h, dr.base + qs + c0, dr.c3, dr.c4);
+          bulk_commit_group();
+        }
+        return true;
+      } else {
+        const size_t first = VARLEN ? static_cast<size_t>(it.row0)
+                                    : static_cast<size_t>(it.wi.b) * 2 * static_cast<size_t>(p.n);
+        // after the contributions of the key tiles the work order takes earlier
+        const int ord = dq_ordinal(p.mode, n, VARLEN ? it.bs : p.bs, BMQ, BN, qh, qs / BMQ,
+                                   it.wi.half, it.wi.tile);
+        unsigned* sem = p.dq_sem + static_cast<size_t>(h) * p.sem_rows + first +
+                        static_cast<size_t>(qh) * n + qs;
+        if (!sem_wait_warp(sem, static_cast<unsigned>(C::kComputeWarps * ord), ab)) return false;
+        const int qo = c0 + QC * up;  // the thread's first query of the tile
+        float* ptr = p.dq_acc + ((first + static_cast<size_t>(qh) * n + qs + qo) * p.H + h) * D +
+                     16 * (warp & 3) + (lane & 15);
+        const int qmax = n - qs - qo;
+#pragma unroll
+        for (int c = 0; c < QC; ++c) {
+          if (c < qmax) {
+            if (p.pass == 2)
+              *ptr = __uint_as_float(dq[c]);
+            else
+              red_add_f32(ptr, __uint_as_float(dq[c]));
+          }
+          ptr += dq_stride;
+        }
+        sem_signal_warp(sem);
+        return true;
+      }
+    };
     // dQ^T of the tile whose products completed last: TMEM lane = head dim
     // `row`, columns = queries; added into the float32 accumulator.
     auto drain_dq = [&](const Bwd2Item& it, int h, int qh, int qs) -> bool {
+      if constexpr (C::kD64) return drain_dq64(it, h, qh, qs);
       uint32_t dq[HC];
       tmem_ld_cols<HC>(t_lane + C::kTmemDQ + c0, dq);
       tmem_wait_ld();
@@ -808,11 +898,13 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
       if (it.v < 0) break;
       if constexpr (VARLEN && C::kTmaDQ) {
         // this launch's dq, dk, dv maps of the item's sample, as memory
-        // holds them
+        // holds them (headdim 64: dq only)
         if (lane == 0) {
           if constexpr (!DET) tensormap_acquire(&p.vl_maps[it.slot].dq);
-          tensormap_acquire(&p.vl_maps[it.slot].dk);
-          tensormap_acquire(&p.vl_maps[it.slot].dv);
+          if constexpr (!C::kD64) {
+            tensormap_acquire(&p.vl_maps[it.slot].dk);
+            tensormap_acquire(&p.vl_maps[it.slot].dv);
+          }
         }
       }
       const int ks = it.wi.tile * BN;
@@ -919,6 +1011,12 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
           const uint32_t pds_col = C::kTmemP + 32 * (c0 / 32) + (c0 % 32) / 2;
           tmem_st_cols<HC / 2>(t_lane + pds_col, wp);
           tmem_st_cols<HC / 2>(t_lane + pds_col + 16, wd);
+        } else if constexpr (C::kD64) {
+          // buffer gg % 2, chunk c0 / 32 (HC = 32: the warpgroup's whole chunk)
+          static_assert(HC == 32, "one 32-query chunk per warpgroup");
+          const uint32_t pds_col = C::kTmemP + 64 * (gg & 1) + c0;
+          tmem_st_cols<16>(t_lane + pds_col, wp);
+          tmem_st_cols<16>(t_lane + pds_col + 16, wd);
         } else {
           // this warpgroup's HC queries: HC / 2 words of P^T from column c0 / 2
           tmem_st_cols<HC / 2>(t_lane + C::kTmemP + 32 * (gg & 1) + c0 / 2, wp);
@@ -1086,6 +1184,29 @@ cudaError_t launch_backward_d128(const BwdParams& p, cudaStream_t stream) {
   if (p.vl) return launch_bwd2_impl<128, 3, W, 1, true, true>(p, stream);
   return p.kv_group > 1 ? launch_bwd2_impl<128, 3, W, 1, true, false>(p, stream)
                         : launch_bwd2_impl<128, 3, W, 1, false, false>(p, stream);
+}
+
+// Headdim 64: 64-query tiles, the same pipeline as headdim 128 (P^T / dS^T
+// double-buffered in TMEM, S^T / dP^T released once read), four Q / dO
+// stages of 16 KB.
+cudaError_t launch_backward_d64(const BwdParams& p, cudaStream_t stream) {
+  if (p.dq_sem)
+    return p.vl ? launch_bwd2_impl<64, 4, 2, 1, true, true, true>(p, stream)
+                : launch_bwd2_impl<64, 4, 2, 1, true, false, true>(p, stream);
+  if (p.vl) return launch_bwd2_impl<64, 4, 2, 1, true, true>(p, stream);
+  return p.kv_group > 1 ? launch_bwd2_impl<64, 4, 2, 1, true, false>(p, stream)
+                        : launch_bwd2_impl<64, 4, 2, 1, false, false>(p, stream);
+}
+
+cudaError_t launch_backward_d256(const BwdParams& p, cudaStream_t stream);
+
+cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream) {
+  switch (headdim) {
+    case 64: return launch_backward_d64(p, stream);
+    case 128: return launch_backward_d128(p, stream);
+    case 256: return launch_backward_d256(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_backward_d256(const BwdParams& p, cudaStream_t stream) {

@@ -204,6 +204,7 @@ cudaError_t launch_forward_fp8(const FwdParams& p, int headdim, cudaStream_t str
 cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream);
 cudaError_t launch_backward_d128(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_backward_d256(const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_backward_d64(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16* out, const __nv_bfloat16* dout,
                                   float* delta, float* dq_acc, int B, int L, int H, int d,
                                   cudaStream_t stream);
@@ -224,7 +225,7 @@ struct TileShape {
 };
 inline bool tile_shape_for(int d, TileShape* t) {
   switch (d) {
-    case 64: *t = {128, 128, 128, 128}; return true;
+    case 64: *t = {128, 128, 128, 64}; return true;
     case 128: *t = {128, 128, 128, 64}; return true;
     case 256: *t = {128, 64, 128, 64}; return true;  // backward: 128 keys x 64 queries
     default: return false;

@@ -19,7 +19,8 @@
 //   dK  += dS^T Q  (A operand read from the shared dS^T tile; headdim 64
 //        and 256: from TMEM)
 //   dQ^T = K^T dS^T  -> TMEM DQ, then added to a float32 accumulator in
-//        device memory (each warp covers 32 consecutive head dims of a query)
+//        device memory (each warp covers 32 consecutive head dims of a
+//        query; headdim 64: 16)
 // TMEM (512 columns): S 64 | dP 64 | P 2 x 32 (headdim 256: P / dS 64) |
 // DQ 64 | dK 128 | dV 128; headdim 64: S 64 | dP 64 | P / dS 2 x 64 |
 // DQ (an M = 64 product: lanes 0-15 of each lane quarter) 64 | dK 64 |
@@ -119,9 +120,9 @@ struct Bwd2Cfg {
   static constexpr int kOffDS =
       kChunkRing ? kOffQ + (kOhSlots + kDhSlots) * kSlotBytes : kOffDO + STAGES * kQBytes;
   // dQ staging, one tile per compute warp: float32 [HC queries][32 head
-  // dims], the source of that warp's bulk reduce-add into the accumulator
-  // (headdim 128; with 256 the shared memory is full and dQ goes out with
-  // per-thread atomics).
+  // dims] (headdim 64: 16), the source of that warp's bulk reduce-add into
+  // the accumulator (with 256 the shared memory is full and dQ goes out
+  // with per-thread atomics).
   // Headdim 64: dQ^T (M = 64 head dims) lies in lanes [32 q, 32 q + 16) of
   // each lane quarter q, so each warp stages its 16 head dims x HC queries.
   static constexpr bool kD64 = D == 64;

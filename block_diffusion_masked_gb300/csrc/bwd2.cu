@@ -168,6 +168,11 @@ struct Bwd2Cfg {
   static constexpr int kTmemDQ = kD64 ? 256 : 192;
   static constexpr int kTmemDK = kD64 ? 320 : 256;
   static constexpr int kTmemDV = 384;
+  // Headdim 64: K and V of the item as the A operands of S^T and dP^T (32
+  // columns each): an N = 64 product with both operands in shared memory
+  // reads them faster than the port delivers.
+  static constexpr int kTmemKA = 448;
+  static constexpr int kTmemVA = 480;
   static constexpr int kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -245,6 +250,13 @@ __device__ __forceinline__ Bwd2Item bwd2_item(const BwdParams& p, int v) {
   it.rule1 = nseg > 1 ? seg[1].rule : 0;
   it.tb1 = nseg > 1 ? seg[1].t_begin : 0;
   return it;
+}
+
+// One 128-row x 256-bit block of a 128-byte-swizzled shared tile (the A
+// operand of one K = 16 step) into TMEM: lane r receives row r's eight
+// 32-bit words, the layout of an A operand read from TMEM.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 template <int D_, int STAGES_, int NWG_, int KVBUF_, bool GQA, bool VARLEN, bool DET>
@@ -607,6 +619,15 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
               mma_commit(BAR(C::BAR_SDPFULL));
             }
           } else {
+          if constexpr (C::kD64) {
+            // K (S^T warp) or V (dP^T warp) of the item into TMEM, after this
+            // warp's products of the previous item, which read them there
+            tc_fence_after();
+            const uint64_t a0 = dp ? dV_kmaj : dK_kmaj;
+            const uint32_t ta = tmem + (dp ? C::kTmemVA : C::kTmemKA);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) tmem_cp_128x256b(ta + 8 * kk, adv(a0, kk * 32));
+          }
           for (int i = 0; i < it.ntiles && ok; ++i) {
             const int gg = g + i;
             const int st = gg % STAGES;
@@ -623,7 +644,11 @@ __global__ void __launch_bounds__(Bwd2Cfg<D_, STAGES_, NWG_, KVBUF_>::kThreads, 
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
               const uint32_t qoff = (kk >> 2) * (BMQ * 128) + (kk & 3) * 32;
-              mma_ss(tmem + acc, adv(a0, koff), adv(b0, st_off + qoff), kIdS, kk > 0 ? 1u : 0u);
+              if constexpr (C::kD64)
+                mma_ts(tmem + acc, tmem + (dp ? C::kTmemVA : C::kTmemKA) + 8 * kk,
+                       adv(b0, st_off + qoff), kIdS, kk > 0 ? 1u : 0u);
+              else
+                mma_ss(tmem + acc, adv(a0, koff), adv(b0, st_off + qoff), kIdS, kk > 0 ? 1u : 0u);
             }
             mma_commit(BAR(C::BAR_SDPFULL));
           }

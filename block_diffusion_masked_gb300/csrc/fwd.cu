@@ -405,7 +405,7 @@ static cudaError_t launch_fwd_impl(const FwdParams& p, cudaStream_t stream) {
 cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream) {
   switch (headdim) {
     case 64:
-    case 128: return launch_forward_two_warpgroups(p, headdim, stream);
+    case 128: return launch_forward_persistent(p, headdim, stream);
     case 256:
       return p.vl ? launch_fwd_impl<256, 64, 2, true>(p, stream)
                   : launch_fwd_impl<256, 64, 2, false>(p, stream);

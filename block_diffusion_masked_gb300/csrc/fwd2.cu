@@ -34,7 +34,7 @@
 // and stores of the current one.
 // The softmax warps first; then one warp takes the items and loads Q, K and
 // V, one issues O += P V and one S = Q K^T, and one stores the out tiles (staged
-// by the softmax warpgroups in the item's query buffer) with TMA and zeroes
+// by the softmax warps in the item's query buffer) with TMA and zeroes
 // the backward's float32 dq accumulator when the caller asks for it.
 // The load/MMA warpgroup hands registers to the softmax warps (setmaxnreg):
 // launched with 168 per thread, it drops to 56 and the softmax warps rise to
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8>::kThreads, 1)
     // busy; from two warps on two schedulers they keep the tensor pipe fed.
     // The two streams meet only through barriers: S of tile g goes into
     // buffer g % kSBufs once P V of tile g - kSBufs (whose P it held) has
-    // completed (SFREE); P V of a tile waits for both warpgroups' P (PFULL),
+    // completed (SFREE); P V of a tile waits for all softmax warps' P (PFULL),
     // and the first P V of an item for the read-out of the O buffer it reuses
     // (OFREE).
     if (lane == 0) {
@@ -408,12 +408,12 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8>::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kPVSteps; ++kk) {
               // P of keys [kPVKeys kk, kPVKeys (kk + 1)): in the columns of the
-              // warpgroup that owns them, 8 columns per step (bf16 pairs or
+              // row half that holds them, 8 columns per step (bf16 pairs or
               // e4m3 quadruples); V: 16 key rows of 128 bytes, or (V^T) 32
               // bytes of 128-key rows
-              constexpr int kStepsPerWG = C::kCols / C::kPVKeys;
+              constexpr int kStepsPerHalf = C::kCols / C::kPVKeys;
               const uint32_t pcol =
-                  C::kTmemS + sb * BN + C::kCols * (kk / kStepsPerWG) + 8 * (kk % kStepsPerWG);
+                  C::kTmemS + sb * BN + C::kCols * (kk / kStepsPerHalf) + 8 * (kk % kStepsPerHalf);
               const uint64_t b =
                   adv(dV, vs * C::kKVBytes + (FP8 ? kk * 32 : kk * C::kPVKeys * 128));
               const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
@@ -434,13 +434,13 @@ __global__ void __launch_bounds__(Fwd2Cfg<D, STAGES, VSTAGES, FP8>::kThreads, 1)
     __syncwarp();
    } else {
     // ------------------------------------------------------------ out stores
-    // Warp 11 stores each item's out tile, which the softmax warpgroups stage
+    // Warp 11 stores each item's out tile, which the softmax warps stage
     // (bf16, 128-byte swizzled) in the item's query buffer, with TMA, and
     // then hands the buffer back to the producer.  Between items it zeroes
     // the backward's dq accumulator when asked, paced by the work counter so
     // that the stores spread over the launch.
     // Ring slots and staging barriers cannot run two phases ahead of this
-    // warp: the producer publishes item k + 4, and the softmax warpgroups
+    // warp: the producer publishes item k + 4, and the softmax warps
     // stage item k + 2, only after this warp has released item k's buffer.
     ZeroShare zs;
     if (p.zero_dst != nullptr) zs.init(p.zero_dst, p.zero_groups);
@@ -741,7 +741,7 @@ cudaError_t launch_forward_fp8(const FwdParams& p, int headdim, cudaStream_t str
 
 // K / V stages per head dimension: as many K tiles in flight as the shared
 // memory holds beside two query tiles and the V ring.
-cudaError_t launch_forward_two_warpgroups(const FwdParams& p, int headdim, cudaStream_t stream) {
+cudaError_t launch_forward_persistent(const FwdParams& p, int headdim, cudaStream_t stream) {
   switch (headdim) {
     case 64:
       return p.vl ? launch_fwd2_impl<64, 6, 4, true>(p, stream)

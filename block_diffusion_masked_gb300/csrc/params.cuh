@@ -199,7 +199,7 @@ int check_backward_args(int B, int n, int H, int d, int bs);
 
 // Launchers (one per translation unit).  Return a cudaError_t.
 cudaError_t launch_forward(const FwdParams& p, int headdim, cudaStream_t stream);
-cudaError_t launch_forward_two_warpgroups(const FwdParams& p, int headdim, cudaStream_t stream);
+cudaError_t launch_forward_persistent(const FwdParams& p, int headdim, cudaStream_t stream);
 cudaError_t launch_forward_fp8(const FwdParams& p, int headdim, cudaStream_t stream);
 cudaError_t launch_backward(const BwdParams& p, int headdim, cudaStream_t stream);
 cudaError_t launch_backward_d128(const BwdParams& p, cudaStream_t stream);
